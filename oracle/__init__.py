@@ -1,0 +1,49 @@
+"""CPU oracle for paged decode attention and its cache bookkeeping.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the product path imports, calls or links
+this package: only the tests, the smoke check and the benchmark's CPU-baseline
+and reference legs use it. It shares no code with the CUDA library (no common
+helpers, tables or constants); the two meet only at the seeded inputs drawn by
+the `synthetic` package.
+
+It is deliberately plain and slow: fp64 arithmetic, whole-sequence gathers in
+logical token order, and the textbook softmax with the maximum subtracted.
+
+Sources (web pages on PagedAttention):
+  * "Phase 7 · Document 04 — PagedAttention" (ai-engineer-zt0), §2 Core
+    Concept (fixed-size blocks, shared physical pool, per-sequence block table,
+    the C-style layout sketch, copy-on-write block sharing), §3 Mental Model
+    (sharing picture), §11 Engineering Decision Framework and §13 question 4
+    (capacity arithmetic).
+  * lux-666 notes "PagedAttention", sections 最小模型 (minimal model: logical
+    blocks -> block table -> physical blocks, worked mapping 0->7, 1->2, 2->9),
+    它为什么有效 (internal waste bounded by the last block; prefix sharing with
+    copy-on-write), and "block size 是容量与 kernel 的共同参数" (ceil(seq_len /
+    block_size) blocks per request).
+
+Where the pages are silent the reading taken is stated in the function's
+docstring. Every function here is pinned by tests that do not call the same
+formula twice (brute force, closed forms, invariances, printed figures).
+"""
+
+from .attention import (  # noqa: F401
+    gather_sequence,
+    decode_attention,
+    decode_attention_one,
+    split_partials,
+    merge_partials,
+    split_context_attention,
+)
+from .cache_ops import append_kv, copy_blocks  # noqa: F401
+from .allocator import BlockAllocator, OutOfBlocks  # noqa: F401
+from .accounting import (  # noqa: F401
+    blocks_needed,
+    paged_internal_waste,
+    naive_slab_waste,
+    concurrent_sequences,
+)
+from .step import (  # noqa: F401
+    place_batch,
+    decode_step,
+    DecodeStepResult,
+)

@@ -1,0 +1,167 @@
+"""Reference block manager: free list, reference counts, block tables.
+
+Test infrastructure only (see the package docstring).
+
+What the pages fix:
+  * Blocks come from a pool of same-size physical blocks; a sequence's table
+    maps logical block -> physical id ("Phase 7 · Document 04 —
+    PagedAttention", §2 Core Concept; lux-666 notes "PagedAttention", 最小模型).
+  * Allocation is on demand: a growing sequence takes one more block; a
+    finished one frees its blocks at once (same passages).
+  * A request of len tokens needs ceil(len / block_size) blocks (lux-666 notes,
+    "block size 是容量与 kernel 的共同参数").
+  * Prefix sharing points several tables at the same blocks, kept alive by
+    reference counts; a write into a shared block copies that block first
+    (Document 04, §2 "block sharing (copy-on-write)" and §3 Mental Model;
+    lux-666 notes, prefix sharing section).
+
+Readings taken where the pages are silent:
+  * The free list is FIFO: allocation pops the front, a block whose count
+    drops to zero is pushed to the back. A sequence's blocks are released in
+    logical order. The initial order is given (default ascending).
+  * A new block is taken exactly when the sequence's length is a multiple of
+    the block size before the append.
+  * Copy-on-write happens iff the block to be written has reference count > 1
+    at write time; the writer gets a fresh block, the pair (old, new) is
+    recorded and the old block's count drops by one. The last holder therefore
+    writes in place.
+  * Every operation is all-or-nothing: when the free list is too short the
+    state is left unchanged and OutOfBlocks is raised.
+"""
+
+from __future__ import annotations
+
+from collections import deque
+from typing import Dict, List, Optional, Tuple
+
+
+class OutOfBlocks(RuntimeError):
+    pass
+
+
+class BlockAllocator:
+    def __init__(self, num_blocks: int, block_size: int,
+                 initial_free_order=None):
+        if num_blocks <= 0 or block_size <= 0:
+            raise ValueError("num_blocks and block_size must be positive")
+        order = list(range(num_blocks)) if initial_free_order is None else \
+            [int(b) for b in initial_free_order]
+        if sorted(order) != list(range(num_blocks)):
+            raise ValueError("initial free order must be a permutation of the pool")
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+        self.free: deque = deque(order)
+        self.ref: List[int] = [0] * num_blocks
+        self.tables: Dict[int, List[int]] = {}
+        self.lens: Dict[int, int] = {}
+        self.cow_copies = 0
+        self.alloc_failures = 0
+
+    # -- helpers ------------------------------------------------------------
+    def _take(self) -> int:
+        b = self.free.popleft()
+        self.ref[b] = 1
+        return b
+
+    def _release(self, b: int) -> None:
+        self.ref[b] -= 1
+        if self.ref[b] == 0:
+            self.free.append(b)
+
+    def _blocks_for(self, length: int) -> int:
+        return -(-length // self.block_size)
+
+    # -- operations ---------------------------------------------------------
+    def add_seq(self, seq: int, length: int) -> None:
+        """Register a sequence already holding `length` tokens."""
+        if seq in self.tables or length < 0:
+            raise ValueError("sequence exists or negative length")
+        n = self._blocks_for(length)
+        if n > len(self.free):
+            self.alloc_failures += 1
+            raise OutOfBlocks(f"need {n} blocks, {len(self.free)} free")
+        self.tables[seq] = [self._take() for _ in range(n)]
+        self.lens[seq] = length
+
+    def fork(self, parent: int, child: int) -> None:
+        """The child shares every block of the parent (counts + 1)."""
+        if parent not in self.tables or child in self.tables:
+            raise ValueError("bad fork")
+        tab = list(self.tables[parent])
+        for b in tab:
+            self.ref[b] += 1
+        self.tables[child] = tab
+        self.lens[child] = self.lens[parent]
+
+    def append_slot(self, seq: int) -> Tuple[int, int, int]:
+        """Reserve the slot of the sequence's next token.
+
+        Returns (slot, cow_src, cow_dst); cow_src = cow_dst = -1 when no copy
+        is needed.
+        """
+        if seq not in self.tables:
+            raise ValueError("unknown sequence")
+        L = self.lens[seq]
+        tab = self.tables[seq]
+        BS = self.block_size
+        cow_src = cow_dst = -1
+        if L % BS == 0:
+            if not self.free:
+                self.alloc_failures += 1
+                raise OutOfBlocks("no free block for growth")
+            tab.append(self._take())
+        else:
+            last = tab[L // BS]
+            if self.ref[last] > 1:
+                if not self.free:
+                    self.alloc_failures += 1
+                    raise OutOfBlocks("no free block for copy-on-write")
+                new = self._take()
+                self.ref[last] -= 1
+                tab[L // BS] = new
+                cow_src, cow_dst = last, new
+                self.cow_copies += 1
+        slot = tab[L // BS] * BS + L % BS
+        self.lens[seq] = L + 1
+        return slot, cow_src, cow_dst
+
+    def free_seq(self, seq: int) -> None:
+        """Release every block of the sequence, in logical order."""
+        tab = self.tables.pop(seq)
+        self.lens.pop(seq)
+        for b in tab:
+            self._release(b)
+
+    # -- inspection ---------------------------------------------------------
+    def table(self, seq: int) -> List[int]:
+        return list(self.tables[seq])
+
+    def seq_len(self, seq: int) -> int:
+        return self.lens[seq]
+
+    def stats(self) -> dict:
+        used = sum(1 for r in self.ref if r > 0)
+        return {
+            "num_blocks": self.num_blocks,
+            "free": len(self.free),
+            "used": used,
+            "shared": sum(1 for r in self.ref if r > 1),
+            "cow_copies": self.cow_copies,
+            "alloc_failures": self.alloc_failures,
+            "total_refs": sum(self.ref),
+            "num_seqs": len(self.tables),
+        }
+
+    def export_state(self) -> Tuple[List[int], List[int]]:
+        """(free list front to back, reference count per block)."""
+        return list(self.free), list(self.ref)
+
+    def dense_table(self, seqs, max_blocks: int, fill: int = -1):
+        """int32-style nested list [len(seqs)][max_blocks], padded with `fill`."""
+        rows = []
+        for s in seqs:
+            t = self.tables[s]
+            if len(t) > max_blocks:
+                raise ValueError("table longer than max_blocks")
+            rows.append(t + [fill] * (max_blocks - len(t)))
+        return rows
