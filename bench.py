@@ -1,0 +1,446 @@
+#!/usr/bin/env python
+"""Paged decode attention benchmark — prints one JSON line.
+
+A step is one pass of the whole hot path over one decode batch: the host
+block manager's slot assignment (done once; the workload is the same every
+step, so each step rewrites the same slots), copy-on-write copies when the
+batch has any, the append of every sequence's new K/V token, and paged decode
+attention (with its split merge) over every cached token.
+
+Default workload: 64 sequences with lengths U[128,2048] (+1 appended token),
+32 query / 8 KV heads, head_dim 128, block 16, pool 1.25x the blocks needed
+with shuffled physical ids, fp16 K/V/q drawn N(0,1) from a fixed seed.
+
+value      KV GB/s: bytes of the K and V rows attended per step / device step
+           time (CUDA events on the launching stream; L2 flushed by a 512 MB
+           write between steps, outside the events)
+e2e        the same metric through the public API with pinned host buffers:
+           every step uploads q, new K/V, slot mapping, block table and
+           lengths and downloads the output inside the timed region
+roofline   the attention kernel alone: algorithmic bytes / mean launch time,
+           against the measured HBM copy bandwidth
+cpu_baseline  the fp64 CPU oracle, as it stands, on whole-batch passes
+
+--impl reference times the CPU oracle instead (the only reference this
+method has) on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "paged decode attention: KV GB/s (fraction of GB300 HBM peak) and tokens attended/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+def workload(name: str, seed_offset: int = 0):
+    import synthetic
+    if name == "gqa4_u128_2048":
+        return synthetic.config2_gqa_batch(seed=2 + 1000 * seed_offset)
+    if name == "mha32_lognormal800":
+        return synthetic.config3_mha_lognormal(seed=3 + 1000 * seed_offset)
+    if name.startswith("long32k_gqa8_bs"):
+        return synthetic.config5_long_context(block_size=int(name[len("long32k_gqa8_bs"):]),
+                                              seed=5 + 1000 * seed_offset)
+    raise SystemExit(f"unknown workload {name}")
+
+
+def describe(b) -> dict:
+    lens = b.attended_lens
+    return {
+        "workload": b.name,
+        "num_seqs": int(b.num_seqs),
+        "seq_len": f"{int(lens.min())}..{int(lens.max())} (mean {float(lens.mean()):.0f})",
+        "tokens_attended": int(lens.sum()),
+        "num_q_heads": b.num_q_heads,
+        "num_kv_heads": b.num_kv_heads,
+        "head_dim": b.head_dim,
+        "block_size": b.block_size,
+        "num_blocks": int(b.num_blocks),
+        "kv_storage": "fp16",
+        "l2": "flushed between steps (512 MB write outside the timed events)",
+    }
+
+
+def kv_bytes(b) -> int:
+    return int(b.attended_lens.astype(np.int64).sum()) * b.num_kv_heads * b.head_dim * 2 * 2
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("pa_decode.cu",):
+        with open(os.path.join(ROOT, "paged_kv_cache_40_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name: str):
+    """DRAM bytes per attention launch from a committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(workload_name)
+    if not ent or ent.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    return int(ent["dram_bytes_per_launch"])
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    """nvidia-smi samples of this GPU's clocks and throttle reasons."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str):
+        self.uuid = uuid.replace("GPU-", "").lower()
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9 and parts[0].replace("GPU-", "").lower() == self.uuid:
+                self.rows.append(parts)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4)
+                          if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------- distributed --
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------- CPU oracle --
+def time_oracle(b, budget_s: float, max_seqs=None):
+    """Time the CPU oracle's attention on whole-batch passes (or the first
+    `max_seqs` sequences) until `budget_s` seconds have passed."""
+    import oracle
+    ref = oracle.decode_step(b, compute_attention=False)
+    seqs = list(range(b.num_seqs if max_seqs is None else min(max_seqs, b.num_seqs)))
+    lens = ref.seq_lens.astype(np.int64)
+    bytes_per_pass = int(lens[seqs].sum()) * b.num_kv_heads * b.head_dim * 4
+    tokens_per_pass = int(lens[seqs].sum())
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode_attention(b.q, ref.k_pool, ref.v_pool, ref.block_table, ref.seq_lens,
+                                b.scale, seqs=seqs)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"seconds": el, "passes": passes, "bytes": bytes_per_pass * passes,
+            "tokens": tokens_per_pass * passes, "seqs": len(seqs)}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    b = workload(args.workload)
+    sample_seqs = args.ref_sample_seqs
+    for _ in range(args.warmup):
+        time_oracle(b, 0.0, max_seqs=sample_seqs)
+    t_total, byt, tok = 0.0, 0, 0
+    for _ in range(args.steps):
+        r = time_oracle(b, 0.0, max_seqs=sample_seqs)
+        t_total += r["seconds"]
+        byt += r["bytes"]
+        tok += r["tokens"]
+    gbs = byt / t_total / 1e9
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * t_total / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": describe(b),
+        "tokens_per_s": round(tok / t_total, 1),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"first {sample_seqs} of {b.num_seqs} sequences, all heads, "
+                                   f"attention only, per step"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- our arm --
+def run_ours(args, world, rank, local):
+    import torch
+    import paged_kv_cache_40_gb300 as pa
+    from paged_kv_cache_40_gb300 import build as pa_build
+    from paged_kv_cache_40_gb300.engine import DecodeBatchRunner
+
+    pa_build.build()
+    pa.lib()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device for the libpa arm")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    b = workload(args.workload, seed_offset=rank)
+    run = DecodeBatchRunner(b, device=dev, partition_tokens=args.partition)
+    plan = run.plan_step()
+    # host slot assignment (block manager) cost for this batch, measured on a
+    # second allocator holding the same placement
+    from paged_kv_cache_40_gb300 import BlockAllocator
+    a = BlockAllocator(b.num_blocks, b.block_size, b.free_order)
+    for op in b.churn:
+        if op.kind == "alloc":
+            a.add_seq(op.owner, op.nblocks * b.block_size)
+        else:
+            a.free_seq(op.owner)
+    for i in range(b.num_seqs):
+        a.add_seq(i, int(b.prefill_lens[i]))
+    t_host0 = time.perf_counter()
+    a.append_slots(list(range(b.num_seqs)))
+    a.build_tables(list(range(b.num_seqs)), run.max_blocks)
+    t_host = (time.perf_counter() - t_host0) * 1e6
+    a.close()
+    stream = torch.cuda.current_stream(dev)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    launches_per_step = (1 if len(plan.cow_pairs) else 0) + 2
+
+    def flush():
+        flush_buf.fill_(1)
+
+    for _ in range(args.warmup):
+        flush()
+        run.run_step()
+    torch.cuda.synchronize(dev)
+    assert pa.pa_device_error() == 0
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(str(torch.cuda.get_device_properties(dev).uuid))
+    sampler.start()
+    time.sleep(0.15)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    w0 = time.perf_counter()
+    for k in range(K):
+        flush()
+        ev[k][0].record(stream)
+        run.copy_and_append()
+        ev[k][1].record(stream)
+        run.attend()
+        ev[k][2].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    wall = time.perf_counter() - w0
+    clocks = sampler.stop()
+    step_ms = [ev[k][0].elapsed_time(ev[k][2]) for k in range(K)]
+    attn_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    assert pa.pa_device_error() == 0
+
+    # end to end through the public API with pinned host buffers
+    h = {
+        "q": torch.from_numpy(b.q).pin_memory(),
+        "k_new": torch.from_numpy(b.k_new).pin_memory(),
+        "v_new": torch.from_numpy(b.v_new).pin_memory(),
+        "slots": torch.from_numpy(plan.slots).pin_memory(),
+        "table": torch.from_numpy(plan.block_table).pin_memory(),
+        "lens": torch.from_numpy(plan.seq_lens).pin_memory(),
+    }
+    out_h = torch.empty(run.out.shape, dtype=run.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        run.q.copy_(h["q"], non_blocking=True)
+        run.k_new.copy_(h["k_new"], non_blocking=True)
+        run.v_new.copy_(h["v_new"], non_blocking=True)
+        run.d_slots.copy_(h["slots"], non_blocking=True)
+        run.d_table.copy_(h["table"], non_blocking=True)
+        run.d_lens.copy_(h["lens"], non_blocking=True)
+        run.run_step()
+        out_h.copy_(run.out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        flush()
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    Ke = max(1, min(K, args.e2e_steps))
+    eev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
+    barrier(world)
+    for k in range(Ke):
+        flush()
+        eev[k][0].record(stream)
+        e2e_step()
+        eev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = [eev[k][0].elapsed_time(eev[k][1]) for k in range(Ke)]
+    assert pa.pa_device_error() == 0
+
+    kvb = run.kv_bytes()
+    tokens = int(plan.seq_lens.astype(np.int64).sum())
+    t_steps = reduce_max(sum(step_ms) / 1e3, world)
+    t_e2e = reduce_max(sum(e2e_ms) / 1e3, world)
+    all_kv = reduce_sum(kvb * K, world)
+    all_kv_e2e = reduce_sum(kvb * Ke, world)
+    all_tok = reduce_sum(tokens * K, world)
+    attn_mean_s = statistics.mean(attn_ms) / 1e3
+    peak, peak_kind = hbm_peak()
+    achieved = run.io_bytes() / attn_mean_s / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = time_oracle(b, args.cpu_budget)
+        cpu = {"value": round(r["bytes"] / r["seconds"] / 1e9, 4), "unit": "GB/s",
+               "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{r['passes']} whole-batch pass(es) of the same {b.num_seqs}-sequence "
+                         f"batch, attention only, fp64 numpy, BLAS default threads",
+               "tokens_per_s": round(r["tokens"] / r["seconds"], 1)}
+    if rank != 0:
+        return
+    value = all_kv / t_steps / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(1e3 * t_steps / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic", "config": describe(b),
+        "tokens_per_s": round(all_tok / t_steps, 1),
+        "frac_of_hbm_peak": {"measured": round(value / peak, 4),
+                             "nominal_8tbs": round(value / 8000.0, 4)},
+        "attention_us": {"mean": round(1e6 * attn_mean_s, 3),
+                         "median": round(1e3 * statistics.median(attn_ms), 3),
+                         "min": round(1e3 * min(attn_ms), 3)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic(b.name), "peak_source": peak_kind,
+                     "kernel": "paged_decode_kernel",
+                     "bytes_per_launch": run.io_bytes()},
+        "e2e": {"value": round(all_kv_e2e / t_e2e / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": round(1e3 * t_e2e / Ke, 5), "steps": Ke},
+        "cpu_baseline": cpu,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+        "host_slot_assign_us": round(t_host, 1) if t_host is not None else None,
+        "wall_s_timed_region": round(wall, 4),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gqa4_u128_2048")
+    ap.add_argument("--partition", type=int, default=0, help="tokens per split (0 = default)")
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-sample-seqs", type=int, default=4)
+    args = ap.parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,286 @@
+/*
+ * pa.h — C ABI of libpa: paged decode attention and its KV-cache bookkeeping,
+ * hand-written CUDA for GB300 (sm_103a).
+ *
+ * The operations follow the PagedAttention pages:
+ *   - "Phase 7 · Document 04 — PagedAttention" (ai-engineer-zt0), §2 Core
+ *     Concept: the KV cache is cut into fixed-size blocks held in a shared pool
+ *     of physical blocks; each sequence's block table maps logical token
+ *     positions to scattered physical blocks; the attention kernel follows that
+ *     indirection to gather K/V during the dot product; blocks are allocated on
+ *     demand and freed at once; shared prefixes are copy-on-write (§2 "block
+ *     sharing", §3 Mental Model).
+ *   - lux-666 notes "PagedAttention", 最小模型 (minimal model): logical blocks
+ *     -> block table -> physical blocks; the kernel reads the table and visits
+ *     the physical blocks in logical token order; a growing request needs one
+ *     more block, a finished one frees its own blocks.
+ *
+ * Conventions shared by every call
+ *   - fp16 tensors are IEEE-754 binary16, passed as `pa_half*` (the raw 16-bit
+ *     patterns). Index tensors are int32.
+ *   - Pools: k_pool and v_pool are separate device buffers, each laid out
+ *     [num_blocks][block_size][num_kv_heads][head_dim], row-major, contiguous.
+ *     Pool "slot" s (0 <= s < num_blocks*block_size) is row s of the pool seen
+ *     as [num_blocks*block_size][num_kv_heads*head_dim]: physical block
+ *     s / block_size, offset s % block_size.
+ *   - Device pointers are owned by the caller (the library never allocates or
+ *     frees device memory) and must be 16-byte aligned. Device calls are
+ *     asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream): arguments are checked on the host before any launch, and a
+ *     PA_OK return means "launched", not "finished".
+ *   - Data-dependent checks (a block id or slot outside the pool, a length
+ *     longer than the table) happen on the device: the offending access is
+ *     skipped and a device error word is set. pa_device_error() reads and
+ *     clears it (it synchronises the stream).
+ *   - Every call returns a pa_status. On failure, pa_last_error() gives a
+ *     message for the calling thread. There is no fallback path: an unsupported
+ *     shape or device is an error, never a silent change of method.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t pa_half;   /* IEEE-754 binary16 bit pattern */
+typedef void* pa_stream_t;  /* cudaStream_t */
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,    /* a host-checked argument is out of range */
+  PA_ERR_OUT_OF_BLOCKS = 2,  /* the allocator's free list is too short */
+  PA_ERR_BAD_BLOCK_ID = 3,   /* device: a block id / slot / length out of range */
+  PA_ERR_UNSUPPORTED = 4,    /* shape or device this build does not serve */
+  PA_ERR_CUDA = 5,           /* a CUDA runtime call failed */
+  PA_ERR_TIMEOUT = 6         /* device: a bounded wait gave up */
+} pa_status;
+
+/* Message of the calling thread's last failed call ("" if none). */
+PA_API const char* pa_last_error(void);
+/* Static name of a status code. */
+PA_API const char* pa_status_string(pa_status s);
+/* Library version, major*10000 + minor*100 + patch. */
+PA_API int pa_version(void);
+
+/* ------------------------------------------------------------------------
+ * Device error word.
+ * Reads and clears the word the kernels set on data-dependent faults they
+ * skipped (bad block id, bad slot, length beyond the table, bounded wait that
+ * gave up). Synchronises `stream` first. *flags receives the raw bit set
+ * (PA_DEVERR_*), and the return value is PA_ERR_BAD_BLOCK_ID or
+ * PA_ERR_TIMEOUT when a bit was set, else PA_OK.
+ * ---------------------------------------------------------------------- */
+#define PA_DEVERR_BAD_BLOCK 1   /* block-table entry outside [0, num_blocks) */
+#define PA_DEVERR_BAD_SLOT 2    /* slot outside [0, num_blocks*block_size) */
+#define PA_DEVERR_BAD_LEN 4     /* seq_len < 0 or > max_blocks*block_size */
+#define PA_DEVERR_TIMEOUT 8     /* a pipeline wait hit its time limit */
+PA_API pa_status pa_device_error(pa_stream_t stream, int32_t* flags);
+
+/* ------------------------------------------------------------------------
+ * pa_append_kv — write each sequence's new K/V token into its cache slot.
+ *
+ * Source: the KV cache grows one token per decode step ("Phase 7 · Document
+ * 04 — PagedAttention", §2 primer; lux-666 notes, 问题从哪里来); the block
+ * manager decides where the token goes (same pages, on-demand allocation).
+ *
+ * k_new, v_new   device [num_tokens][num_kv_heads][head_dim] fp16 (read)
+ * k_pool, v_pool device pools (written at the mapped rows only)
+ * slot_mapping   device int32 [num_tokens]; token i goes to slot
+ *                slot_mapping[i]; a negative slot skips the token; a slot
+ *                >= num_blocks*block_size is skipped and sets
+ *                PA_DEVERR_BAD_SLOT.
+ * The copy is bit-exact. Two tokens mapped to the same slot race (one wins).
+ * Errors: PA_ERR_INVALID_ARG (bad sizes, NULL or misaligned pointers),
+ *         PA_ERR_UNSUPPORTED (head_dim not a multiple of 8), PA_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+PA_API pa_status pa_append_kv(const pa_half* k_new, const pa_half* v_new,
+                       pa_half* k_pool, pa_half* v_pool,
+                       const int32_t* slot_mapping, int num_tokens,
+                       int num_kv_heads, int head_dim, int block_size,
+                       int num_blocks, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * pa_copy_blocks — copy-on-write duplication of whole blocks.
+ *
+ * Source: "Phase 7 · Document 04 — PagedAttention", §2 "block sharing
+ * (copy-on-write)": sequences that share a prefix point at the same physical
+ * blocks and only the block that diverges is copied; §3 Mental Model; lux-666
+ * notes, prefix sharing splits at the copy-on-write boundary.
+ *
+ * pairs      device int32 [num_pairs][2] = (src, dst) physical block ids.
+ *            Block dst of both pools becomes a bit-exact copy of block src
+ *            (all block_size rows, every KV head). Destinations must be
+ *            distinct and must not appear as sources (the allocator's pairs
+ *            satisfy this); otherwise the result is unspecified (no fault).
+ *            An id outside [0, num_blocks) skips that pair and sets
+ *            PA_DEVERR_BAD_BLOCK.
+ * Errors: as pa_append_kv.
+ * ---------------------------------------------------------------------- */
+PA_API pa_status pa_copy_blocks(pa_half* k_pool, pa_half* v_pool,
+                         const int32_t* pairs, int num_pairs,
+                         int num_kv_heads, int head_dim, int block_size,
+                         int num_blocks, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * pa_decode_attention — single-query attention over the paged cache.
+ *
+ * Source: "Phase 7 · Document 04 — PagedAttention", §2 Core Concept (the
+ * layout sketch: per block K[BLOCK][HEADS][HEAD_DIM] and V likewise, one int32
+ * table row per sequence, and attention reading K/V one block at a time
+ * through that table); lux-666 notes, 最小模型 (the kernel reads the block
+ * table and visits physical blocks in logical token order).
+ *
+ * For each sequence i and query head h (KV head kv = h / (num_q_heads /
+ * num_kv_heads), consecutive groups):
+ *   K[t], V[t] = pool[block_table[i][t / block_size]][t % block_size][kv]
+ *   out[i][h] = sum_t softmax_t(scale * q[i][h] . K[t]) V[t],  t < seq_lens[i]
+ * computed in fp32 (max-subtracted online softmax), rounded once to fp16.
+ * A sequence of length 0 gets an all-zero output. Long sequences are split
+ * into partitions of `partition_tokens` tokens whose partial results are
+ * merged on the device (log-sum-exp); the caller sees one result.
+ *
+ * q            device [num_seqs][num_q_heads][head_dim] fp16
+ * k_pool, v_pool  device pools (read only)
+ * block_table  device int32 [num_seqs][max_blocks_per_seq]; only the first
+ *              ceil(seq_lens[i]/block_size) entries of row i are read.
+ * seq_lens     device int32 [num_seqs], tokens attended (the appended one
+ *              included); a value < 0 or > max_blocks_per_seq*block_size sets
+ *              PA_DEVERR_BAD_LEN and is clamped into range.
+ * scale        softmax scale (typically 1/sqrt(head_dim))
+ * out          device [num_seqs][num_q_heads][head_dim] fp16 (written)
+ * workspace    device scratch of >= pa_decode_workspace_bytes(...) bytes,
+ *              16-byte aligned, owned by the caller. It starts with
+ *              num_seqs*num_kv_heads int32 arrival counters that must be zero
+ *              before the first call (pa_decode_workspace_init, or any zero
+ *              fill of the whole buffer); every call that completes without a
+ *              device error leaves them zero again. The rest holds fp32
+ *              partial results of split sequences. Calls sharing one
+ *              workspace must not overlap on the device.
+ * partition_tokens  tokens per split; 0 = the library default (256). Must be
+ *              a multiple of block_size and at most 32*block_size.
+ * Supported shapes: head_dim in {64, 128}; block_size in {8, 16, 32};
+ * num_q_heads / num_kv_heads in {1, 2, 4, 8}; num_seqs <= 16384.
+ * Errors: PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED (shape outside the list, or
+ *         a device other than sm_103), PA_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+PA_API size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads,
+                                 int num_kv_heads, int head_dim,
+                                 int block_size, int max_blocks_per_seq,
+                                 int partition_tokens);
+
+PA_API pa_status pa_decode_workspace_init(void* workspace, size_t workspace_bytes,
+                                   int num_seqs, int num_kv_heads,
+                                   pa_stream_t stream);
+
+PA_API pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool,
+                              const pa_half* v_pool,
+                              const int32_t* block_table,
+                              const int32_t* seq_lens, int num_seqs,
+                              int num_q_heads, int num_kv_heads, int head_dim,
+                              int block_size, int max_blocks_per_seq,
+                              int num_blocks, float scale, pa_half* out,
+                              void* workspace, size_t workspace_bytes,
+                              int partition_tokens, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Host block allocator (block manager). Host memory only; no CUDA calls.
+ *
+ * Source: "Phase 7 · Document 04 — PagedAttention", §2 (a pool of physical
+ * blocks allocated on demand and freed instantly; per-sequence block table;
+ * copy-on-write sharing) and §3; lux-666 notes, 最小模型 (any free physical
+ * block may back a logical block), the block-size section (a request of L
+ * tokens holds ceil(L / block_size) blocks) and the prefix-sharing section
+ * (reference counts, copy-on-write at the fork boundary).
+ *
+ * Rules fixed here where the pages leave them open:
+ *   - the free list is FIFO: allocation takes the front; a block whose
+ *     reference count drops to zero goes to the back; a sequence's blocks are
+ *     released in logical order; the initial order is given or ascending;
+ *   - a token appended at length L opens a new block iff L % block_size == 0;
+ *   - writing into a block with reference count > 1 first moves the writer to
+ *     a fresh block (copy-on-write pair (old, new) returned, old count - 1);
+ *   - every call is all-or-nothing: on PA_ERR_OUT_OF_BLOCKS the state is
+ *     unchanged (the batched append stops at the failing sequence).
+ * Sequence ids are arbitrary int64 values. The handle is owned by the
+ * library; it is not thread-safe (one thread at a time per handle).
+ * ---------------------------------------------------------------------- */
+typedef struct pa_allocator pa_allocator;
+
+typedef struct pa_alloc_stats_t {
+  int64_t num_blocks;
+  int64_t free_blocks;
+  int64_t used_blocks;    /* reference count > 0 */
+  int64_t shared_blocks;  /* reference count > 1 */
+  int64_t cow_copies;     /* copy-on-write pairs issued so far */
+  int64_t alloc_failures; /* calls refused with PA_ERR_OUT_OF_BLOCKS */
+  int64_t total_refs;     /* sum of reference counts = table entries */
+  int64_t num_seqs;
+} pa_alloc_stats_t;
+
+/* initial_free_order: host int32 [num_blocks], a permutation of
+ * 0..num_blocks-1, or NULL for ascending. */
+PA_API pa_status pa_alloc_create(int num_blocks, int block_size,
+                          const int32_t* initial_free_order,
+                          pa_allocator** out);
+PA_API void pa_alloc_destroy(pa_allocator* a);
+
+/* Register sequence seq_id already holding `len` tokens: takes
+ * ceil(len / block_size) blocks from the front of the free list. */
+PA_API pa_status pa_alloc_add_seq(pa_allocator* a, int64_t seq_id, int64_t len);
+
+/* child shares every block of parent (each reference count + 1). */
+PA_API pa_status pa_alloc_fork(pa_allocator* a, int64_t parent, int64_t child);
+
+/* Reserve the slot of the next token of seq_id (length grows by one).
+ * *slot = physical_block * block_size + offset; *cow_src / *cow_dst = the
+ * copy-on-write pair, or -1 / -1 when no copy is needed. */
+PA_API pa_status pa_alloc_append_slot(pa_allocator* a, int64_t seq_id,
+                               int32_t* slot, int32_t* cow_src,
+                               int32_t* cow_dst);
+
+/* Batched form for one decode step: sequences processed in array order.
+ * slots: host int32 [n]; cow_pairs: host int32 [n][2], the first *num_cow
+ * rows filled; *num_done = sequences processed before any failure. */
+PA_API pa_status pa_alloc_append_slots(pa_allocator* a, const int64_t* seq_ids,
+                                int n, int32_t* slots, int32_t* cow_pairs,
+                                int* num_cow, int* num_done);
+
+/* Release every block of seq_id (logical order) and forget the sequence. */
+PA_API pa_status pa_alloc_free_seq(pa_allocator* a, int64_t seq_id);
+
+/* Copy seq_id's table (physical ids, logical order) into out[0..cap);
+ * *n = its full length (PA_ERR_INVALID_ARG if cap < *n). */
+PA_API pa_status pa_alloc_get_table(const pa_allocator* a, int64_t seq_id,
+                             int32_t* out, int cap, int* n);
+
+PA_API pa_status pa_alloc_seq_len(const pa_allocator* a, int64_t seq_id,
+                           int64_t* len);
+
+/* Dense tables for a batch: table host int32 [n][max_blocks] (rows padded
+ * with `fill`), seq_lens host int32 [n] = current lengths. */
+PA_API pa_status pa_alloc_build_tables(const pa_allocator* a, const int64_t* seq_ids,
+                                int n, int max_blocks, int32_t fill,
+                                int32_t* table, int32_t* seq_lens);
+
+PA_API pa_status pa_alloc_stats(const pa_allocator* a, pa_alloc_stats_t* out);
+
+/* free_order: host int32 [num_blocks], front to back, *num_free entries
+ * valid and the rest set to -1; refcounts: host int32 [num_blocks]. */
+PA_API pa_status pa_alloc_export_state(const pa_allocator* a, int32_t* free_order,
+                                int* num_free, int32_t* refcounts);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,287 @@
+"""paged_kv_cache_40_gb300 — paged decode attention for GB300 behind a C ABI.
+
+This module is the thin Python face of libpa.so (include/pa.h): each function
+has the C name, checks and marshals torch tensors (device pointers, sizes, the
+current CUDA stream) and calls the library. All device work runs in libpa's
+CUDA kernels; nothing here computes on the host, and there is no fallback.
+
+Device calls                      Host block manager
+  pa_append_kv                      BlockAllocator (pa_alloc_*)
+  pa_copy_blocks
+  pa_decode_attention
+  pa_decode_workspace_bytes / _init
+  pa_device_error
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import Iterable, Optional, Sequence, Tuple
+
+from ._lib import (  # noqa: F401
+    AllocStats,
+    OutOfBlocksError,
+    PaError,
+    PA_DEVERR_BAD_BLOCK,
+    PA_DEVERR_BAD_LEN,
+    PA_DEVERR_BAD_SLOT,
+    PA_DEVERR_TIMEOUT,
+    LIB_PATH,
+    check as _check,
+    load as _load,
+)
+
+__all__ = [
+    "pa_append_kv", "pa_copy_blocks", "pa_decode_attention",
+    "pa_decode_workspace_bytes", "pa_decode_workspace_init", "pa_device_error",
+    "pa_version", "BlockAllocator", "PaError", "OutOfBlocksError", "lib",
+    "DEFAULT_PARTITION_TOKENS",
+]
+
+DEFAULT_PARTITION_TOKENS = 256
+
+
+def lib() -> ctypes.CDLL:
+    return _load()
+
+
+def pa_version() -> int:
+    return int(_load().pa_version())
+
+
+# ----------------------------------------------------------------- helpers --
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    return ctypes.c_void_p(handle)
+
+
+def _dev(t, name, dtype, ndim=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (libpa has no host path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _pool_dims(k_pool, v_pool):
+    if k_pool.dim() != 4 or tuple(k_pool.shape) != tuple(v_pool.shape):
+        raise ValueError("k_pool and v_pool must both be [num_blocks][block_size][kv_heads][head_dim]")
+    nb, bs, hkv, d = (int(x) for x in k_pool.shape)
+    return nb, bs, hkv, d
+
+
+# ------------------------------------------------------------ device calls --
+def pa_append_kv(k_new, v_new, k_pool, v_pool, slot_mapping, stream=None) -> None:
+    """Write row i of k_new/v_new ([T][Hkv][D] fp16) into pool slot
+    slot_mapping[i] (int32; negative = skip)."""
+    torch = _torch()
+    nb, bs, hkv, d = _pool_dims(k_pool, v_pool)
+    T = int(slot_mapping.numel())
+    if tuple(k_new.shape) != (T, hkv, d) or tuple(v_new.shape) != (T, hkv, d):
+        raise ValueError("k_new/v_new must be [num_tokens][kv_heads][head_dim]")
+    args = (_dev(k_new, "k_new", torch.float16), _dev(v_new, "v_new", torch.float16),
+            _dev(k_pool, "k_pool", torch.float16), _dev(v_pool, "v_pool", torch.float16),
+            _dev(slot_mapping, "slot_mapping", torch.int32))
+    _check(_load().pa_append_kv(*args, T, hkv, d, bs, nb, _stream_ptr(stream)))
+
+
+def pa_copy_blocks(k_pool, v_pool, pairs, stream=None) -> None:
+    """Copy block src to block dst in both pools for each (src, dst) row of
+    pairs (int32 [n][2])."""
+    torch = _torch()
+    nb, bs, hkv, d = _pool_dims(k_pool, v_pool)
+    if pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be [n][2]")
+    n = int(pairs.shape[0])
+    args = (_dev(k_pool, "k_pool", torch.float16), _dev(v_pool, "v_pool", torch.float16),
+            _dev(pairs, "pairs", torch.int32))
+    _check(_load().pa_copy_blocks(*args, n, hkv, d, bs, nb, _stream_ptr(stream)))
+
+
+def pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                              block_size, max_blocks_per_seq,
+                              partition_tokens: int = 0) -> int:
+    n = int(_load().pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                              block_size, max_blocks_per_seq, partition_tokens))
+    if n == 0 and num_seqs > 0:
+        raise PaError(1, "pa_decode_workspace_bytes: unsupported or invalid shape")
+    return n
+
+
+def pa_decode_workspace_init(workspace, num_seqs, num_kv_heads, stream=None) -> None:
+    torch = _torch()
+    ptr = _dev(workspace, "workspace", torch.uint8)
+    _check(_load().pa_decode_workspace_init(ptr, workspace.numel(), num_seqs, num_kv_heads,
+                                            _stream_ptr(stream)))
+
+
+def alloc_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                    max_blocks_per_seq, partition_tokens: int = 0, device=None):
+    """A zero-filled uint8 CUDA buffer sized for pa_decode_attention."""
+    torch = _torch()
+    n = pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                  max_blocks_per_seq, partition_tokens)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def pa_decode_attention(q, k_pool, v_pool, block_table, seq_lens, scale, out=None,
+                        workspace=None, partition_tokens: int = 0, stream=None):
+    """Paged decode attention. q [S][Hq][D] fp16; pools [NB][BS][Hkv][D] fp16;
+    block_table int32 [S][MB]; seq_lens int32 [S]. Returns out [S][Hq][D] fp16."""
+    torch = _torch()
+    nb, bs, hkv, d = _pool_dims(k_pool, v_pool)
+    if q.dim() != 3 or int(q.shape[2]) != d:
+        raise ValueError("q must be [num_seqs][num_q_heads][head_dim]")
+    S, hq = int(q.shape[0]), int(q.shape[1])
+    if block_table.dim() != 2 or int(block_table.shape[0]) != S:
+        raise ValueError("block_table must be [num_seqs][max_blocks_per_seq]")
+    mb = int(block_table.shape[1])
+    if tuple(seq_lens.shape) != (S,):
+        raise ValueError("seq_lens must be [num_seqs]")
+    if out is None:
+        out = torch.empty_like(q)
+    elif tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must have q's shape")
+    if workspace is None:
+        workspace = alloc_workspace(S, hq, hkv, d, bs, mb, partition_tokens, q.device)
+    args = (_dev(q, "q", torch.float16), _dev(k_pool, "k_pool", torch.float16),
+            _dev(v_pool, "v_pool", torch.float16), _dev(block_table, "block_table", torch.int32),
+            _dev(seq_lens, "seq_lens", torch.int32))
+    _check(_load().pa_decode_attention(
+        *args, S, hq, hkv, d, bs, mb, nb, ctypes.c_float(float(scale)),
+        _dev(out, "out", torch.float16), _dev(workspace, "workspace", torch.uint8),
+        workspace.numel(), partition_tokens, _stream_ptr(stream)))
+    return out
+
+
+def pa_device_error(stream=None) -> int:
+    """Read and clear the device error word (synchronises the stream).
+    Returns the PA_DEVERR_* bit set; raises PaError if any bit was set."""
+    flags = ctypes.c_int32(0)
+    st = _load().pa_device_error(_stream_ptr(stream), ctypes.byref(flags))
+    if st != 0:
+        err = PaError(st, _load().pa_last_error().decode(errors="replace"))
+        err.flags = int(flags.value)
+        raise err
+    return int(flags.value)
+
+
+# ------------------------------------------------------------ host allocator --
+def _i32_array(values):
+    arr = (ctypes.c_int32 * len(values))(*[int(v) for v in values])
+    return arr
+
+
+class BlockAllocator:
+    """The host block manager of libpa (pa_alloc_*), one handle per pool."""
+
+    def __init__(self, num_blocks: int, block_size: int,
+                 initial_free_order: Optional[Sequence[int]] = None):
+        L = _load()
+        handle = ctypes.c_void_p()
+        order = None
+        if initial_free_order is not None:
+            if len(initial_free_order) != num_blocks:
+                raise ValueError("initial free order must list every block")
+            order = _i32_array(list(initial_free_order))
+        _check(L.pa_alloc_create(num_blocks, block_size, order, ctypes.byref(handle)))
+        self._h = handle
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) and self._h.value:
+            _load().pa_alloc_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add_seq(self, seq: int, length: int) -> None:
+        _check(_load().pa_alloc_add_seq(self._h, seq, length))
+
+    def fork(self, parent: int, child: int) -> None:
+        _check(_load().pa_alloc_fork(self._h, parent, child))
+
+    def append_slot(self, seq: int) -> Tuple[int, int, int]:
+        s, a, b = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        _check(_load().pa_alloc_append_slot(self._h, seq, ctypes.byref(s), ctypes.byref(a),
+                                            ctypes.byref(b)))
+        return s.value, a.value, b.value
+
+    def append_slots(self, seqs: Sequence[int]):
+        """One decode step: (slots int32 list, cow pairs list of (src, dst))."""
+        n = len(seqs)
+        ids = (ctypes.c_int64 * max(n, 1))(*[int(x) for x in seqs])
+        slots = (ctypes.c_int32 * max(n, 1))()
+        pairs = (ctypes.c_int32 * max(2 * n, 2))()
+        ncow, ndone = ctypes.c_int(), ctypes.c_int()
+        _check(_load().pa_alloc_append_slots(self._h, ids, n, slots, pairs, ctypes.byref(ncow),
+                                             ctypes.byref(ndone)))
+        return list(slots[:n]), [(pairs[2 * i], pairs[2 * i + 1]) for i in range(ncow.value)]
+
+    def free_seq(self, seq: int) -> None:
+        _check(_load().pa_alloc_free_seq(self._h, seq))
+
+    def table(self, seq: int):
+        n = ctypes.c_int()
+        st = _load().pa_alloc_get_table(self._h, seq, None, 0, ctypes.byref(n))
+        if st not in (0, 1):
+            _check(st)
+        buf = (ctypes.c_int32 * max(n.value, 1))()
+        _check(_load().pa_alloc_get_table(self._h, seq, buf, n.value, ctypes.byref(n)))
+        return list(buf[:n.value])
+
+    def seq_len(self, seq: int) -> int:
+        v = ctypes.c_int64()
+        _check(_load().pa_alloc_seq_len(self._h, seq, ctypes.byref(v)))
+        return v.value
+
+    def build_tables(self, seqs: Sequence[int], max_blocks: int, fill: int = -1):
+        """(table int32 [n][max_blocks] as a flat ctypes array, seq_lens [n])."""
+        import numpy as np
+        n = len(seqs)
+        ids = (ctypes.c_int64 * max(n, 1))(*[int(x) for x in seqs])
+        table = np.empty((n, max_blocks), dtype=np.int32)
+        lens = np.empty((n,), dtype=np.int32)
+        _check(_load().pa_alloc_build_tables(
+            self._h, ids, n, max_blocks, fill,
+            table.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))))
+        return table, lens
+
+    def stats(self) -> dict:
+        st = AllocStats()
+        _check(_load().pa_alloc_stats(self._h, ctypes.byref(st)))
+        return {
+            "num_blocks": st.num_blocks, "free": st.free_blocks, "used": st.used_blocks,
+            "shared": st.shared_blocks, "cow_copies": st.cow_copies,
+            "alloc_failures": st.alloc_failures, "total_refs": st.total_refs,
+            "num_seqs": st.num_seqs,
+        }
+
+    def export_state(self):
+        """(free list front to back, reference counts)."""
+        fo = (ctypes.c_int32 * self.num_blocks)()
+        rc = (ctypes.c_int32 * self.num_blocks)()
+        nf = ctypes.c_int()
+        _check(_load().pa_alloc_export_state(self._h, fo, ctypes.byref(nf), rc))
+        return list(fo[:nf.value]), list(rc)

@@ -1,0 +1,211 @@
+// KV-cache writes: per-token append through a slot mapping, and whole-block
+// copy-on-write duplication. Both are pure bit copies streamed with 16-byte
+// vector loads/stores; the pool is viewed as rows of num_kv_heads*head_dim
+// halves, so a slot is a row index and a block is block_size consecutive rows.
+//
+// Append: the cache grows by one token per decode step ("Phase 7 · Document
+// 04 — PagedAttention", §2 primer); the block manager picks the slot (§2 Core
+// Concept, on-demand allocation). Copy: copy-on-write of a shared block (§2
+// "block sharing", §3 Mental Model; lux-666 notes "PagedAttention", prefix
+// sharing section).
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "pa_internal.h"
+
+// Device error word: bits PA_DEVERR_* set by any libpa kernel that skipped
+// an out-of-range access. Read and cleared by pa_device_error().
+__device__ int32_t g_pa_device_error = 0;
+
+namespace {
+
+constexpr int kAppendThreads = 128;
+constexpr int kCopyThreads = 256;
+constexpr int kCopyVecsPerThread = 4;
+
+// One CTA per appended token: copy its K row and V row (row_vecs 16-byte
+// vectors each) into pool row `slot`.
+__global__ void __launch_bounds__(kAppendThreads)
+append_kv_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                 uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
+                 const int32_t* __restrict__ slots, int row_vecs, int64_t num_slots,
+                 int32_t* __restrict__ err) {
+  const int t = blockIdx.x;
+  const int32_t slot = __ldg(slots + t);
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (threadIdx.x == 0) atomicOr(err, PA_DEVERR_BAD_SLOT);
+    return;
+  }
+  const uint4* ks = k_new + static_cast<int64_t>(t) * row_vecs;
+  const uint4* vs = v_new + static_cast<int64_t>(t) * row_vecs;
+  uint4* kd = k_pool + static_cast<int64_t>(slot) * row_vecs;
+  uint4* vd = v_pool + static_cast<int64_t>(slot) * row_vecs;
+  for (int i = threadIdx.x; i < row_vecs; i += kAppendThreads) {
+    const uint4 a = __ldg(ks + i);
+    const uint4 b = __ldg(vs + i);
+    kd[i] = a;
+    vd[i] = b;
+  }
+}
+
+// Grid (pairs, slices): each CTA copies a slice of one block in both pools.
+__global__ void __launch_bounds__(kCopyThreads)
+copy_blocks_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
+                   const int32_t* __restrict__ pairs, int64_t block_vecs, int num_blocks,
+                   int32_t* __restrict__ err) {
+  const int p = blockIdx.x;
+  const int32_t src = __ldg(pairs + 2 * p);
+  const int32_t dst = __ldg(pairs + 2 * p + 1);
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(err, PA_DEVERR_BAD_BLOCK);
+    return;
+  }
+  const int64_t slice = static_cast<int64_t>(kCopyThreads) * kCopyVecsPerThread;
+  const int64_t lo = blockIdx.y * slice;
+  const int64_t hi = lo + slice < block_vecs ? lo + slice : block_vecs;
+  const uint4* ks = k_pool + src * block_vecs;
+  const uint4* vs = v_pool + src * block_vecs;
+  uint4* kd = k_pool + dst * block_vecs;
+  uint4* vd = v_pool + dst * block_vecs;
+  uint4 kb[kCopyVecsPerThread], vb[kCopyVecsPerThread];
+#pragma unroll
+  for (int j = 0; j < kCopyVecsPerThread; ++j) {
+    const int64_t i = lo + threadIdx.x + j * kCopyThreads;
+    if (i < hi) {
+      kb[j] = ks[i];
+      vb[j] = vs[i];
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kCopyVecsPerThread; ++j) {
+    const int64_t i = lo + threadIdx.x + j * kCopyThreads;
+    if (i < hi) {
+      kd[i] = kb[j];
+      vd[i] = vb[j];
+    }
+  }
+}
+
+pa_status check_pool_shape(const char* fn, int num_kv_heads, int head_dim, int block_size,
+                           int num_blocks) {
+  if (num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+    return pa::fail(PA_ERR_INVALID_ARG, "%s: kv_heads=%d head_dim=%d block_size=%d blocks=%d",
+                    fn, num_kv_heads, head_dim, block_size, num_blocks);
+  if (head_dim % 8)
+    return pa::fail(PA_ERR_UNSUPPORTED, "%s: head_dim %d is not a multiple of 8", fn, head_dim);
+  if (static_cast<int64_t>(num_blocks) * block_size > INT32_MAX)
+    return pa::fail(PA_ERR_INVALID_ARG, "%s: pool slots exceed int32", fn);
+  return PA_OK;
+}
+
+}  // namespace
+
+namespace pa {
+
+int32_t* device_error_word() {
+  static std::mutex mu;
+  static int32_t* addr[64] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    fail(PA_ERR_CUDA, "device_error_word: no current device");
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_pa_device_error);
+    if (e != cudaSuccess) {
+      cuda_fail(e, "cudaGetSymbolAddress(device error word)");
+      return nullptr;
+    }
+    addr[dev] = static_cast<int32_t*>(p);
+  }
+  return addr[dev];
+}
+
+}  // namespace pa
+
+extern "C" {
+
+pa_status pa_device_error(pa_stream_t stream, int32_t* flags) {
+  if (!flags) return pa::fail(PA_ERR_INVALID_ARG, "pa_device_error: flags is NULL");
+  *flags = 0;
+  int32_t* word = pa::device_error_word();
+  if (!word) return PA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, word, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(word, 0, sizeof(int32_t), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return pa::cuda_fail(e, "pa_device_error");
+  *flags = host;
+  if (host & PA_DEVERR_TIMEOUT)
+    return pa::fail(PA_ERR_TIMEOUT, "a device pipeline wait hit its time limit (flags 0x%x)", host);
+  if (host)
+    return pa::fail(PA_ERR_BAD_BLOCK_ID,
+                    "device skipped out-of-range accesses (flags 0x%x: 1=block id, 2=slot, "
+                    "4=length)", host);
+  return pa::ok();
+}
+
+pa_status pa_append_kv(const pa_half* k_new, const pa_half* v_new, pa_half* k_pool,
+                       pa_half* v_pool, const int32_t* slot_mapping, int num_tokens,
+                       int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                       pa_stream_t stream) {
+  if (pa_status s = check_pool_shape("pa_append_kv", num_kv_heads, head_dim, block_size,
+                                     num_blocks))
+    return s;
+  if (num_tokens < 0) return pa::fail(PA_ERR_INVALID_ARG, "pa_append_kv: num_tokens < 0");
+  if (num_tokens == 0) return pa::ok();
+  if (!k_new || !v_new || !k_pool || !v_pool || !slot_mapping)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_append_kv: NULL pointer");
+  if (!pa::aligned16(k_new) || !pa::aligned16(v_new) || !pa::aligned16(k_pool) ||
+      !pa::aligned16(v_pool) || (reinterpret_cast<uintptr_t>(slot_mapping) & 3))
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_append_kv: misaligned pointer");
+  pa::DeviceInfo dev;
+  if (pa_status s = pa::current_device(&dev)) return s;
+  int32_t* err = pa::device_error_word();
+  if (!err) return PA_ERR_CUDA;
+  const int row_vecs = num_kv_heads * head_dim / 8;
+  append_kv_kernel<<<num_tokens, kAppendThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint4*>(k_new), reinterpret_cast<const uint4*>(v_new),
+      reinterpret_cast<uint4*>(k_pool), reinterpret_cast<uint4*>(v_pool), slot_mapping,
+      row_vecs, static_cast<int64_t>(num_blocks) * block_size, err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return pa::cuda_fail(e, "pa_append_kv launch");
+  return pa::ok();
+}
+
+pa_status pa_copy_blocks(pa_half* k_pool, pa_half* v_pool, const int32_t* pairs,
+                         int num_pairs, int num_kv_heads, int head_dim, int block_size,
+                         int num_blocks, pa_stream_t stream) {
+  if (pa_status s = check_pool_shape("pa_copy_blocks", num_kv_heads, head_dim, block_size,
+                                     num_blocks))
+    return s;
+  if (num_pairs < 0) return pa::fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: num_pairs < 0");
+  if (num_pairs == 0) return pa::ok();
+  if (!k_pool || !v_pool || !pairs)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: NULL pointer");
+  if (!pa::aligned16(k_pool) || !pa::aligned16(v_pool) ||
+      (reinterpret_cast<uintptr_t>(pairs) & 3))
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: misaligned pointer");
+  pa::DeviceInfo dev;
+  if (pa_status s = pa::current_device(&dev)) return s;
+  int32_t* err = pa::device_error_word();
+  if (!err) return PA_ERR_CUDA;
+  const int64_t block_vecs = static_cast<int64_t>(block_size) * num_kv_heads * head_dim / 8;
+  const int64_t slice = static_cast<int64_t>(kCopyThreads) * kCopyVecsPerThread;
+  const int64_t slices = (block_vecs + slice - 1) / slice;
+  if (slices > 65535) return pa::fail(PA_ERR_UNSUPPORTED, "pa_copy_blocks: block too large");
+  dim3 grid(num_pairs, static_cast<unsigned>(slices));
+  copy_blocks_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<uint4*>(k_pool), reinterpret_cast<uint4*>(v_pool), pairs, block_vecs,
+      num_blocks, err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return pa::cuda_fail(e, "pa_copy_blocks launch");
+  return pa::ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,128 @@
+"""One decode step of a batch through libpa: the host block manager assigns
+slots (and copy-on-write pairs), then the device copies shared blocks, writes
+the new K/V rows and runs paged decode attention.
+
+Step order (the plain reading of "one decode step plus one append per
+sequence"): reserve slots -> copy-on-write copies -> append -> attend over
+every cached token including the appended one.
+
+The batch object is any container with the fields of a decode batch:
+num_blocks, block_size, num_q_heads, num_kv_heads, head_dim, prefill_lens,
+free_order, churn (ops with kind/owner/nblocks), q, k_pool, v_pool, k_new,
+v_new (numpy fp16) and scale.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import List, Optional, Tuple
+
+import numpy as np
+
+from . import (BlockAllocator, alloc_workspace, pa_append_kv, pa_copy_blocks,
+               pa_decode_attention)
+
+
+def _to_dev(arr, device, dtype=None):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(arr))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.to(device)
+
+
+@dataclass
+class StepPlan:
+    slots: np.ndarray          # int32 [S]
+    cow_pairs: np.ndarray      # int32 [n][2]
+    block_table: np.ndarray    # int32 [S][MB]
+    seq_lens: np.ndarray       # int32 [S]
+
+
+class DecodeBatchRunner:
+    """Holds a batch's pools on the device and runs its decode step."""
+
+    def __init__(self, batch, device="cuda", max_blocks: Optional[int] = None,
+                 partition_tokens: int = 0, table_fill: int = -1, k_pool=None, v_pool=None):
+        import torch
+        self.batch = batch
+        self.device = torch.device(device)
+        self.partition_tokens = partition_tokens
+        a = BlockAllocator(batch.num_blocks, batch.block_size, batch.free_order)
+        for op in getattr(batch, "churn", []):
+            if op.kind == "alloc":
+                a.add_seq(op.owner, op.nblocks * batch.block_size)
+            else:
+                a.free_seq(op.owner)
+        S = int(batch.prefill_lens.shape[0])
+        for i in range(S):
+            a.add_seq(i, int(batch.prefill_lens[i]))
+        self.alloc = a
+        self.num_seqs = S
+        bs = batch.block_size
+        need = max(1, max(-(-(int(L) + 1) // bs) for L in batch.prefill_lens)) if S else 1
+        self.max_blocks = int(max_blocks or need)
+        self.table_fill = table_fill
+        self.k_pool = k_pool if k_pool is not None else _to_dev(batch.k_pool, self.device)
+        self.v_pool = v_pool if v_pool is not None else _to_dev(batch.v_pool, self.device)
+        self.q = _to_dev(batch.q, self.device)
+        self.k_new = _to_dev(batch.k_new, self.device)
+        self.v_new = _to_dev(batch.v_new, self.device)
+        self.out = torch.empty_like(self.q)
+        self.workspace = alloc_workspace(S, batch.num_q_heads, batch.num_kv_heads,
+                                         batch.head_dim, bs, self.max_blocks,
+                                         partition_tokens, self.device)
+        self.plan: Optional[StepPlan] = None
+
+    # -- host: slot assignment ---------------------------------------------
+    def plan_step(self) -> StepPlan:
+        """Reserve one slot per sequence (host block manager) and upload the
+        slot mapping, copy-on-write pairs and block tables."""
+        import torch
+        slots, pairs = self.alloc.append_slots(list(range(self.num_seqs)))
+        table, lens = self.alloc.build_tables(list(range(self.num_seqs)), self.max_blocks,
+                                              self.table_fill)
+        plan = StepPlan(np.asarray(slots, np.int32),
+                        np.asarray(pairs, np.int32).reshape(-1, 2), table, lens)
+        self.plan = plan
+        self.d_slots = _to_dev(plan.slots, self.device)
+        self.d_pairs = _to_dev(plan.cow_pairs, self.device) if len(plan.cow_pairs) else None
+        self.d_table = _to_dev(plan.block_table, self.device)
+        self.d_lens = _to_dev(plan.seq_lens, self.device)
+        return plan
+
+    # -- device: the hot path ----------------------------------------------
+    def copy_and_append(self, stream=None) -> int:
+        launches = 0
+        if self.d_pairs is not None:
+            pa_copy_blocks(self.k_pool, self.v_pool, self.d_pairs, stream=stream)
+            launches += 1
+        pa_append_kv(self.k_new, self.v_new, self.k_pool, self.v_pool, self.d_slots,
+                     stream=stream)
+        return launches + 1
+
+    def attend(self, stream=None):
+        pa_decode_attention(self.q, self.k_pool, self.v_pool, self.d_table, self.d_lens,
+                            float(self.batch.scale), out=self.out, workspace=self.workspace,
+                            partition_tokens=self.partition_tokens, stream=stream)
+        return self.out
+
+    def run_step(self, stream=None):
+        """copy-on-write copies (if any), append, attend. Returns the kernel
+        launch count."""
+        n = self.copy_and_append(stream)
+        self.attend(stream)
+        return n + 1
+
+    def kv_bytes(self) -> int:
+        """Algorithmic K+V bytes one attention launch reads."""
+        b = self.batch
+        return int(self.plan.seq_lens.astype(np.int64).sum()) * b.num_kv_heads * b.head_dim * 2 * 2
+
+    def io_bytes(self) -> int:
+        """Algorithmic bytes of one attention launch: K/V rows attended, q,
+        out, the table entries used and the lengths."""
+        b = self.batch
+        lens = self.plan.seq_lens.astype(np.int64)
+        table_entries = int(sum(-(-int(L) // b.block_size) for L in lens))
+        return (self.kv_bytes() + 2 * self.q.numel() * 2 + table_entries * 4 + lens.size * 4)

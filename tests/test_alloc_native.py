@@ -1,0 +1,134 @@
+"""The native block manager (libpa pa_alloc_*) against the oracle's, bit for
+bit: free-list order, reference counts, tables, slots, copy-on-write pairs and
+counters after every operation."""
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+
+
+def _same(native, ref, seqs):
+    assert native.export_state() == ref.export_state()
+    for s in seqs:
+        assert native.table(s) == ref.table(s)
+        assert native.seq_len(s) == ref.seq_len(s)
+    ns, rs = native.stats(), ref.stats()
+    for k in ("free", "used", "shared", "cow_copies", "alloc_failures", "total_refs",
+              "num_seqs", "num_blocks"):
+        assert ns[k] == rs[k], k
+
+
+def test_random_ops_with_forks_and_copy_on_write(libpa):
+    rng = np.random.default_rng(31)
+    nb, bs = 300, 8
+    order = rng.permutation(nb).tolist()
+    nat = libpa.BlockAllocator(nb, bs, order)
+    ref = oracle.BlockAllocator(nb, bs, order)
+    live = []
+    next_id = 0
+    for step in range(3000):
+        r = rng.random()
+        if r < 0.25 or not live:
+            L = int(rng.integers(0, 50))
+            ok_n = ok_r = True
+            try:
+                nat.add_seq(next_id, L)
+            except libpa.OutOfBlocksError:
+                ok_n = False
+            try:
+                ref.add_seq(next_id, L)
+            except oracle.OutOfBlocks:
+                ok_r = False
+            assert ok_n == ok_r
+            if ok_n:
+                live.append(next_id)
+            next_id += 1
+        elif r < 0.35:
+            parent = live[int(rng.integers(len(live)))]
+            nat.fork(parent, next_id)
+            ref.fork(parent, next_id)
+            live.append(next_id)
+            next_id += 1
+        elif r < 0.8:
+            s = live[int(rng.integers(len(live)))]
+            try:
+                got = nat.append_slot(s)
+            except libpa.OutOfBlocksError:
+                got = None
+            try:
+                exp = ref.append_slot(s)
+            except oracle.OutOfBlocks:
+                exp = None
+            assert got == exp
+        else:
+            s = live.pop(int(rng.integers(len(live))))
+            nat.free_seq(s)
+            ref.free_seq(s)
+        if step % 50 == 0:
+            _same(nat, ref, live)
+    _same(nat, ref, live)
+    assert ref.stats()["cow_copies"] > 10 and ref.stats()["alloc_failures"] > 0
+
+
+def test_churned_placement_matches(libpa):
+    b = synthetic.config3_mha_lognormal(num_seqs=40, num_heads=1, head_dim=8, churn_ops=2000)
+    nat = libpa.BlockAllocator(b.num_blocks, b.block_size, b.free_order)
+    ref = oracle.BlockAllocator(b.num_blocks, b.block_size, b.free_order)
+    for op in b.churn:
+        if op.kind == "alloc":
+            nat.add_seq(op.owner, op.nblocks * b.block_size)
+            ref.add_seq(op.owner, op.nblocks * b.block_size)
+        else:
+            nat.free_seq(op.owner)
+            ref.free_seq(op.owner)
+    for i, L in enumerate(b.prefill_lens):
+        nat.add_seq(i, int(L))
+        ref.add_seq(i, int(L))
+    slots, pairs = nat.append_slots(list(range(40)))
+    exp = [ref.append_slot(i) for i in range(40)]
+    assert slots == [e[0] for e in exp] and pairs == [] and all(e[1] == -1 for e in exp)
+    _same(nat, ref, range(40))
+    table, lens = nat.build_tables(list(range(40)), 600, fill=-1)
+    assert table.tolist() == ref.dense_table(range(40), 600, fill=-1)
+    assert lens.tolist() == [ref.seq_len(i) for i in range(40)]
+
+
+def test_shared_prefix_step_pairs_match(libpa):
+    nat = libpa.BlockAllocator(400, 16)
+    ref = oracle.BlockAllocator(400, 16)
+    for a in (nat, ref):
+        a.add_seq(0, 2040)
+        for c in range(1, 128):
+            a.fork(0, c)
+    slots, pairs = nat.append_slots(list(range(128)))
+    exp = [ref.append_slot(i) for i in range(128)]
+    assert slots == [e[0] for e in exp]
+    assert pairs == [(e[1], e[2]) for e in exp if e[1] >= 0]
+    assert len(pairs) == 127
+    _same(nat, ref, range(128))
+
+
+def test_out_of_blocks_leaves_state(libpa):
+    nat = libpa.BlockAllocator(4, 4)
+    nat.add_seq(0, 12)
+    before = nat.export_state()
+    with pytest.raises(libpa.OutOfBlocksError):
+        nat.add_seq(1, 8)
+    assert nat.export_state() == before and nat.stats()["alloc_failures"] == 1
+    with pytest.raises(libpa.PaError):
+        nat.add_seq(0, 1)          # duplicate id
+    with pytest.raises(libpa.PaError):
+        libpa.BlockAllocator(4, 4, [0, 1, 1, 2])
+    slots, pairs = nat.append_slots([])
+    assert slots == [] and pairs == []
+
+
+def test_batched_append_stops_at_failure(libpa):
+    nat = libpa.BlockAllocator(3, 2)
+    nat.add_seq(0, 2)
+    nat.add_seq(1, 2)
+    with pytest.raises(libpa.OutOfBlocksError):
+        nat.append_slots([0, 1])     # seq 0 takes the last block, seq 1 fails
+    assert nat.seq_len(0) == 3 and nat.seq_len(1) == 2

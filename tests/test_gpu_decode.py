@@ -1,0 +1,213 @@
+"""Paged decode attention on the GPU (through the C ABI) against the fp64
+oracle, on the seeded workloads and on edge cases. Pool rows no sequence may
+read are NaN-poisoned, so any read outside a sequence's tokens fails."""
+
+import dataclasses
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from tests.gpu_helpers import assert_close_attention, poison_unread_rows
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def pa(libpa):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return libpa
+
+
+def _poisoned(batch):
+    """Batch with unread pool rows set to NaN (placement computed by the oracle)."""
+    ref = oracle.decode_step(batch, compute_attention=False)
+    kp, vp = poison_unread_rows(batch.k_pool, batch.v_pool, ref.block_table, ref.seq_lens,
+                                batch.block_size)
+    return dataclasses.replace(batch, k_pool=kp, v_pool=vp)
+
+
+def run_and_compare(pa, batch, partition_tokens=0, seqs=None, heads=None, poison=True):
+    from paged_kv_cache_40_gb300.engine import DecodeBatchRunner
+    if poison:
+        batch = _poisoned(batch)
+    ref = oracle.decode_step(batch, compute_attention=False)
+    run = DecodeBatchRunner(batch, partition_tokens=partition_tokens)
+    plan = run.plan_step()
+    # host slot assignment: bit-exact with the oracle's block manager
+    assert plan.slots.tolist() == ref.slot_mapping.tolist()
+    assert plan.cow_pairs.tolist() == ref.cow_pairs.tolist()
+    assert plan.block_table.tolist() == ref.block_table.tolist()
+    assert plan.seq_lens.tolist() == ref.seq_lens.tolist()
+    assert run.alloc.export_state() == ref.allocator.export_state()
+    run.run_step()
+    torch.cuda.synchronize()
+    assert pa.pa_device_error() == 0
+    # append (and copy) results: bit-exact pools
+    assert np.array_equal(run.k_pool.cpu().numpy().view(np.uint16), ref.k_pool.view(np.uint16))
+    assert np.array_equal(run.v_pool.cpu().numpy().view(np.uint16), ref.v_pool.view(np.uint16))
+    out = run.out.cpu().numpy()
+    exp = oracle.decode_attention(batch.q, ref.k_pool, ref.v_pool, ref.block_table,
+                                  ref.seq_lens, batch.scale, seqs=seqs, heads=heads)
+    S = batch.num_seqs
+    si = list(range(S)) if seqs is None else list(seqs)
+    hi = list(range(batch.num_q_heads)) if heads is None else list(heads)
+    assert_close_attention(out[np.ix_(si, hi)], exp[np.ix_(si, hi)], batch.name)
+    return run, ref
+
+
+def test_tiny_config(pa):
+    run_and_compare(pa, synthetic.config1_tiny())
+
+
+@pytest.mark.parametrize("partition", [0, 16, 32, 128, 512])
+def test_gqa_small_several_partitions(pa, partition):
+    b = synthetic.config2_gqa_batch(num_seqs=7, lo=1, hi=1100)
+    run_and_compare(pa, b, partition_tokens=partition)
+
+
+def test_gqa_batch_full_size(pa):
+    """64 sequences U[128,2048], 32q/8kv, D=128, BS=16: every output checked."""
+    run_and_compare(pa, synthetic.config2_gqa_batch())
+
+
+def test_mha_lognormal_small_churned(pa):
+    b = synthetic.config3_mha_lognormal(num_seqs=12, churn_ops=800)
+    run_and_compare(pa, b)
+
+
+def test_mha_lognormal_full_size_sampled(pa):
+    b = synthetic.config3_mha_lognormal()
+    rng = np.random.default_rng(0)
+    seqs = sorted(rng.choice(b.num_seqs, 12, replace=False).tolist())
+    seqs.append(int(np.argmax(b.prefill_lens)))          # the longest sequence too
+    run_and_compare(pa, b, seqs=sorted(set(seqs)), heads=[0, 7, 31])
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_long_context_small(pa, bs):
+    b = synthetic.config5_long_context(block_size=bs, num_seqs=3, seq_len=3000)
+    run_and_compare(pa, b)
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_long_context_full_size_sampled(pa, bs):
+    b = synthetic.config5_long_context(block_size=bs)
+    run_and_compare(pa, b, seqs=[0, 9, 15], heads=[0, 5, 63], poison=False)
+
+
+# ---------------------------------------------------------------- edge cases --
+def _direct(pa, q, kp, vp, table, lens, scale, partition=0):
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    out = pa.pa_decode_attention(d(q), d(kp), d(vp), d(table.astype(np.int32)),
+                                 d(np.asarray(lens, np.int32)), scale,
+                                 partition_tokens=partition)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def _random_case(seed, S, Hq, Hkv, D, BS, lens, nb_extra=3):
+    rng = np.random.default_rng(seed)
+    mb = max(1, max(-(-L // BS) for L in lens))
+    need = sum(-(-L // BS) for L in lens)
+    nb = need + nb_extra
+    perm = rng.permutation(nb)
+    table = -np.ones((S, mb), np.int32)
+    pos = 0
+    for i, L in enumerate(lens):
+        n = -(-L // BS)
+        table[i, :n] = perm[pos:pos + n]
+        pos += n
+    q = rng.standard_normal((S, Hq, D)).astype(np.float16)
+    kp = rng.standard_normal((nb, BS, Hkv, D)).astype(np.float16)
+    vp = rng.standard_normal((nb, BS, Hkv, D)).astype(np.float16)
+    kp, vp = poison_unread_rows(kp, vp, table, lens, BS)
+    return q, kp, vp, table
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("BS", [8, 16, 32])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_shape_matrix(pa, D, BS, G):
+    Hkv = 2
+    lens = [1, BS - 1, BS, BS + 1, 255, 256, 257, 700]
+    q, kp, vp, table = _random_case(D * 100 + BS * 10 + G, len(lens), G * Hkv, Hkv, D, BS, lens)
+    scale = np.float32(1 / math.sqrt(D))
+    got = _direct(pa, q, kp, vp, table, lens, scale)
+    exp = oracle.decode_attention(q, kp, vp, table, lens, scale)
+    assert_close_attention(got, exp, f"D{D} BS{BS} G{G}")
+    assert pa.pa_device_error() == 0
+
+
+def test_zero_length_gives_zeros(pa):
+    lens = [0, 5, 0, 40]
+    q, kp, vp, table = _random_case(5, 4, 8, 2, 128, 16, [1, 5, 1, 40])
+    got = _direct(pa, q, kp, vp, table, lens, np.float32(0.1))
+    assert not got[0].any() and not got[2].any()
+    exp = oracle.decode_attention(q, kp, vp, table, lens, np.float32(0.1))
+    assert_close_attention(got, exp, "zero length")
+
+
+@pytest.mark.parametrize("partition", [16, 48, 256, 512])
+def test_partition_sizes_agree(pa, partition):
+    lens = [1, 300, 1000, 4097]
+    q, kp, vp, table = _random_case(9, 4, 16, 4, 128, 16, lens)
+    got = _direct(pa, q, kp, vp, table, lens, np.float32(0.088), partition)
+    exp = oracle.decode_attention(q, kp, vp, table, lens, np.float32(0.088))
+    assert_close_attention(got, exp, f"partition {partition}")
+
+
+def test_large_scores_stay_finite(pa):
+    lens = [600]
+    q, kp, vp, table = _random_case(11, 1, 4, 1, 128, 16, lens)
+    q = (q.astype(np.float32) * 40).astype(np.float16)
+    got = _direct(pa, q, kp, vp, table, lens, np.float32(1.0))
+    exp = oracle.decode_attention(q, kp, vp, table, lens, np.float32(1.0))
+    assert np.isfinite(got).all()
+    assert_close_attention(got, exp, "large scores")
+
+
+def test_workspace_reuse_and_repeat(pa):
+    """Split sequences leave the arrival counters at zero: repeated calls and
+    calls with other lengths on one workspace give the right results."""
+    from paged_kv_cache_40_gb300 import alloc_workspace
+    lens_a = [3000, 20, 1500]
+    lens_b = [10, 2900, 700]
+    q, kp, vp, table = _random_case(13, 3, 8, 2, 128, 16, [3000, 2900, 1500])
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    ws = alloc_workspace(3, 8, 2, 128, 16, table.shape[1])
+    dq, dk, dv, dt = d(q), d(kp), d(vp), d(table)
+    for lens in (lens_a, lens_a, lens_b, lens_a):
+        out = pa.pa_decode_attention(dq, dk, dv, dt, d(np.asarray(lens, np.int32)), 0.0884,
+                                     workspace=ws)
+        torch.cuda.synchronize()
+        exp = oracle.decode_attention(q, kp, vp, table, lens, np.float32(0.0884))
+        assert_close_attention(out.cpu().numpy(), exp, f"reuse {lens}")
+    counters = ws[: 3 * 2 * 4].view(torch.int32).cpu()
+    assert not counters.any()
+
+
+def test_bad_block_id_is_reported_not_faulted(pa):
+    lens = [40, 40]
+    q, kp, vp, table = _random_case(17, 2, 4, 4, 64, 16, lens)
+    table = table.copy()
+    table[1, 1] = 10_000_000            # far outside the pool
+    table[0, 2] = -5
+    _direct(pa, q, kp, vp, table, lens, np.float32(0.125))
+    with pytest.raises(pa.PaError) as e:
+        pa.pa_device_error()
+    assert e.value.flags & pa.PA_DEVERR_BAD_BLOCK
+    assert pa.pa_device_error() == 0     # cleared
+
+
+def test_length_beyond_table_is_reported(pa):
+    q, kp, vp, table = _random_case(19, 1, 4, 4, 64, 16, [32])
+    _direct(pa, q, kp, vp, table, [33], np.float32(0.125))   # table holds 2 blocks
+    with pytest.raises(pa.PaError) as e:
+        pa.pa_device_error()
+    assert e.value.flags & pa.PA_DEVERR_BAD_LEN

@@ -1,0 +1,63 @@
+"""Host-side argument checks: refused before any device work (no GPU needed)."""
+
+import ctypes
+
+import pytest
+
+NULL = None
+
+
+def _decode(lib, **kw):
+    a = dict(q=NULL, k=NULL, v=NULL, table=NULL, lens=NULL, S=4, Hq=32, Hkv=8, D=128, BS=16,
+             MB=8, NB=64, scale=0.1, out=NULL, ws=NULL, wsb=0, pt=0, stream=NULL)
+    a.update(kw)
+    return lib.pa_decode_attention(a["q"], a["k"], a["v"], a["table"], a["lens"], a["S"], a["Hq"],
+                                   a["Hkv"], a["D"], a["BS"], a["MB"], a["NB"],
+                                   ctypes.c_float(a["scale"]), a["out"], a["ws"], a["wsb"],
+                                   a["pt"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Hq=30), 1),                 # not a multiple of kv heads
+    (dict(Hq=48, Hkv=3), 4),          # ratio 16 unsupported
+    (dict(D=96), 4),
+    (dict(BS=64), 4),
+    (dict(S=20000), 4),
+    (dict(MB=0), 1),
+    (dict(pt=24), 1),                 # not a multiple of the block size
+    (dict(pt=1024), 1),               # more than 32 blocks per partition
+    (dict(NB=0), 1),
+    (dict(scale=float("inf")), 1),
+    (dict(), 1),                      # NULL pointers
+])
+def test_decode_rejects(libpa, kw, status):
+    lib = libpa.lib()
+    assert _decode(lib, **kw) == status
+    assert lib.pa_last_error() != b""
+
+
+def test_decode_zero_sequences_is_a_no_op(libpa):
+    assert _decode(libpa.lib(), S=0) == 0
+
+
+def test_workspace_bytes(libpa):
+    lib = libpa.lib()
+    n = lib.pa_decode_workspace_bytes(64, 32, 8, 128, 16, 129, 0)
+    # counters + (m, l) + acc for 64 seqs x 8 kv heads x 9 partitions x 4 heads
+    units = 64 * 8 * 9
+    assert n >= 64 * 8 * 4 + units * 4 * 2 * 4 + units * 4 * 128 * 4
+    assert n % 256 == 0
+    assert lib.pa_decode_workspace_bytes(64, 32, 8, 96, 16, 129, 0) == 0
+    assert lib.pa_decode_workspace_bytes(64, 32, 8, 128, 16, 129, 512) > 0
+    assert lib.pa_decode_workspace_bytes(64, 32, 8, 128, 16, 129, 513) == 0
+
+
+def test_cache_ops_reject(libpa):
+    lib = libpa.lib()
+    assert lib.pa_append_kv(NULL, NULL, NULL, NULL, NULL, 4, 8, 100, 16, 64, NULL) == 4
+    assert lib.pa_append_kv(NULL, NULL, NULL, NULL, NULL, -1, 8, 128, 16, 64, NULL) == 1
+    assert lib.pa_append_kv(NULL, NULL, NULL, NULL, NULL, 0, 8, 128, 16, 64, NULL) == 0
+    assert lib.pa_append_kv(NULL, NULL, NULL, NULL, NULL, 4, 8, 128, 16, 64, NULL) == 1
+    assert lib.pa_copy_blocks(NULL, NULL, NULL, 3, 0, 128, 16, 64, NULL) == 1
+    assert lib.pa_copy_blocks(NULL, NULL, NULL, 0, 8, 128, 16, 64, NULL) == 0
+    assert lib.pa_copy_blocks(NULL, NULL, NULL, 2, 8, 128, 16, 64, NULL) == 1
