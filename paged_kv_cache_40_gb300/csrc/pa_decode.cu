@@ -8,34 +8,39 @@
 // block_table[i][t / BS], row t % BS, KV head h / G.
 //
 // How (GB300-first; the pages give no kernel, only the layout sketch):
-//   * Work item = (sequence, KV head, partition of `partition_tokens` tokens).
-//     All G query heads of a KV head are served by one item, so every K/V byte
+//   * Segments and balanced chunks. A segment is (sequence, KV head): the
+//     ceil(L/BS) blocks of one KV head of one sequence. All segments are laid
+//     end to end (sequence-major, KV head minor) into one stream of blocks,
+//     and the stream is cut into equal contiguous chunks, one per CTA of a
+//     persistent grid (SMs x resident CTAs). Every CTA therefore streams the
+//     same number of blocks. A segment that lies inside one chunk is finished
+//     there; a segment cut by chunk boundaries leaves a partial result per
+//     chunk, and the last chunk to finish it (an atomic arrival counter, never
+//     a spin) merges the partials with the log-sum-exp rule. A chunk has at
+//     most two cut segments (its first and its last).
+//   * All G query heads of a KV head are served together, so every K/V byte
 //     is read from HBM once per step (GQA head-group reuse).
-//   * Persistent grid (SMs x resident CTAs). Items are numbered KV-head-fastest
-//     so CTAs running side by side stream neighbouring rows of the same blocks.
-//     Each CTA derives the item list from a prefix sum of per-sequence
-//     partition counts held in shared memory (no host-side plan, no extra
-//     launch).
-//   * Warp specialisation: one producer warp walks the CTA's items, reads the
-//     block-table entries of an item with one coalesced load, and issues one
-//     bulk async copy (cp.async.bulk, completion counted on an mbarrier) per K
-//     row and per V row of each block into a ring of shared-memory stages.
-//     Four consumer warps take the stages round-robin.
-//   * Consumer math: a row of head_dim fp16 values is split over 8 or 16 lanes
-//     (16-byte vector reads from shared memory, conflict-free); each lane
-//     keeps q (pre-scaled by scale*log2 e) and its slice of the fp32
-//     accumulators in registers and uses the packed fp32 FMA (fma.rn.f32x2).
-//     Dot products are finished with xor-shuffles inside the lane group, and
-//     the softmax is the online (running max / running sum) form in base 2.
-//   * End of an item: warp partial states are merged with shuffles, then
-//     across warps through shared memory. An unsplit sequence writes fp16
-//     output directly. A split sequence writes its (max, sum, acc) partial to
-//     the workspace; the last CTA to finish a (sequence, KV head) — found with
-//     an atomic arrival counter, never a spin — merges all partials with the
-//     log-sum-exp rule and writes the output, then resets the counter.
+//   * Warp specialisation. A producer warp walks the CTA's chunk, loads block
+//     table entries 32 at a time with one coalesced load, and moves each
+//     (block, KV head) K tile and V tile into a ring of shared-memory stages
+//     with TMA: a 3-D tensor map over the pool seen as [NB*BS][Hkv][D], one
+//     tiled copy per 64-dimension half (box {64, 1, BS}), completion counted on
+//     an mbarrier. The tiles land with the 128-byte swizzle, so the
+//     tensor-core fragment loads (ldmatrix) are free of bank conflicts. (One
+//     copy per 256-byte row would leave the copy engine, not HBM, as the
+//     limit.) Four consumer warps take the stages round-robin.
+//   * Consumer math on tensor cores (mma.sync m16n8k16, fp16 in, fp32
+//     accumulate). Scores S = Q K^T with the G query heads as the M rows and
+//     8-token groups as N; the online softmax (base 2, running max and sum)
+//     works on the accumulator registers; then O^T += V^T P^T with head_dim as
+//     M and the heads as N, whose B operand is exactly the probabilities the
+//     score accumulators already hold (no transpose, no shared-memory trip).
+//     Rows of a partial last block are masked out of the softmax and zeroed in
+//     the V stage so they contribute exactly nothing.
 //   * Every wait is bounded (about one second of %globaltimer); on expiry the
 //     kernel records PA_DEVERR_TIMEOUT, stops issuing copies, drains the copies
 //     already in flight (again bounded) and finishes without faulting.
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -47,8 +52,8 @@ namespace {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kDefaultPartitionTokens = 256;
 constexpr int kMaxSeqs = 16384;
+constexpr int kMaxGrid = 2048;
 constexpr int kRingBytes = 64 * 1024;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -83,14 +88,18 @@ __device__ __forceinline__ unsigned long long global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Bulk async copy global -> this CTA's shared memory, completion on `bar`.
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                              uint32_t bar) {
+// TMA tiled copy of box {x, y, z} of a 3-D tensor map into this CTA's shared
+// memory, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
@@ -100,29 +109,36 @@ __device__ __forceinline__ float fast_exp2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// d = a * b + c on both halves (packed fp32 FMA, sm_100+).
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\t"
-      "mov.b64 rb, {%4, %5};\n\t"
-      "mov.b64 rc, {%6, %7};\n\t"
-      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
-      "mov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return d;
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\t"
-      "mov.b64 rb, {%4, %5};\n\t"
-      "mul.rn.f32x2 rd, ra, rb;\n\t"
-      "mov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+// D = A * B + D, m16n8k16, fp16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // Warp-collective bounded wait on an mbarrier phase. Every lane polls (so
@@ -156,32 +172,40 @@ __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity,
 // ------------------------------------------------------------- shapes ---
 template <int D, int BS, int G>
 struct Shape {
-  // lanes sharing one K/V row: keep G * (D / LPR) accumulators <= 64 floats
-  static constexpr int LPR = (G * (D / 8) <= 64) ? 8 : 16;
-  static constexpr int SG = 32 / LPR;      // row groups per warp
-  static constexpr int DPL = D / LPR;      // dims per lane
-  static constexpr int NCH = DPL / 8;      // 16-byte chunks per lane per row
-  static constexpr int H2 = DPL / 2;       // float2 per lane per head
-  static constexpr int TPS = BS / SG;      // rows per group per block
-  static constexpr int TB0 = (16 / G) > 0 ? (16 / G) : 1;
-  static constexpr int TB = TPS < TB0 ? TPS : TB0;  // rows per softmax update
-  static constexpr int NBATCH = TPS / TB;
-  static constexpr int ROW_BYTES = D * 2;
-  static constexpr int TILE_BYTES = BS * ROW_BYTES;  // K (or V) rows of one block, one head
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-  static constexpr int NST = (kRingBytes / STAGE_BYTES) > 4 ? (kRingBytes / STAGE_BYTES) : 4;
-  static_assert(D % (LPR * 8) == 0, "head_dim must split into 16-byte chunks per lane");
-  static_assert(BS % SG == 0 && TPS % TB == 0, "block size must split over row groups");
-  // shared-memory layout (bytes)
+  static_assert(G >= 1 && G <= 8, "at most 8 query heads per KV head (mma N = 8)");
+  static_assert(D % 16 == 0 && BS % 8 == 0, "shape");
+  static constexpr int NHALF = D / 64;                // 64-dim (128-byte) halves per row
+  static constexpr int HALF_BYTES = BS * 128;         // one half of a tile, swizzled
+  static constexpr int TILE_BYTES = NHALF * HALF_BYTES;  // K (or V) of one block, one head
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile then V tile
+  static_assert(D % 64 == 0 && HALF_BYTES % 1024 == 0, "swizzle atoms need 1 KB halves");
+  // Ring depth is a multiple of the consumer-warp count, so consecutive uses
+  // of a stage belong to the same consumer warp. A parity wait can only tell
+  // the current phase from the one before it; with this invariant a consumer
+  // never waits on a stage whose previous use is still in flight, which would
+  // otherwise read as "complete".
+  static constexpr int NST_RAW = kRingBytes / STAGE_BYTES;
+  static constexpr int NST = NST_RAW >= 2 * kConsumerWarps
+                                 ? NST_RAW / kConsumerWarps * kConsumerWarps
+                                 : kConsumerWarps;
+  static_assert(NST % kConsumerWarps == 0, "ring depth must be a multiple of consumer warps");
+  static constexpr int KSTEPS = D / 16;  // QK k-steps over head_dim
+  static constexpr int MT = D / 16;      // PV m-tiles over head_dim
+  static constexpr int NT = BS / 8;      // 8-token groups per block
+  static constexpr int PK = (NT + 1) / 2;  // PV k-steps (16 tokens each) per block
+  // shared-memory layout (bytes): barriers and flags at fixed offsets, then
+  // the ring at the next 1 KB-aligned absolute address (the swizzle pattern is
+  // a function of address bits 7..9), then the merge buffers and the prefix.
   static constexpr int OFF_FULL = 0;
   static constexpr int OFF_EMPTY = OFF_FULL + NST * 8;
-  static constexpr int OFF_FLAGS = OFF_EMPTY + NST * 8;           // abort, is_last, wsum[8]
-  static constexpr int OFF_RING = ((OFF_FLAGS + 64) + 127) / 128 * 128;
-  static constexpr int OFF_MACC = OFF_RING + NST * STAGE_BYTES;  // float [NC][G][D]
-  static constexpr int OFF_MML = OFF_MACC + kConsumerWarps * G * D * 4;  // float [NC][G][2]
-  static constexpr int OFF_PREFIX = OFF_MML + kConsumerWarps * G * 2 * 4;
+  static constexpr int OFF_FLAGS = OFF_EMPTY + NST * 8;  // abort, is_last, wsum[8]
+  static constexpr int RING_MIN = OFF_FLAGS + 64;
+  static constexpr int RING_BYTES = NST * STAGE_BYTES;
+  static constexpr int MACC_BYTES = kConsumerWarps * G * D * 4;  // float [NC][G][D]
+  static constexpr int MML_BYTES = kConsumerWarps * G * 2 * 4;   // float [NC][G][2]
   static size_t smem_bytes(int num_seqs) {
-    return static_cast<size_t>(OFF_PREFIX) + static_cast<size_t>(num_seqs + 1) * 4;
+    return static_cast<size_t>(RING_MIN + 1024 + RING_BYTES + MACC_BYTES + MML_BYTES) +
+           static_cast<size_t>(num_seqs + 1) * 4;
   }
 };
 
@@ -192,18 +216,16 @@ struct DecodeParams {
   const int32_t* block_table;
   const int32_t* seq_lens;
   __half* out;
-  int32_t* counters;  // [S][Hkv]
-  float* part_ml;     // [S][Hkv][max_splits][G][2]
-  float* part_acc;    // [S][Hkv][max_splits][G][D]
+  int32_t* counters;  // [S][Hkv] arrival counters of cut segments
+  float* records;     // [2 * max_chunks][G][D + 2] partial results of cut segments
   int32_t* err;
   int num_seqs;
   int num_q_heads;
   int num_kv_heads;
   int max_blocks;
   int num_blocks;
-  int part_blocks;  // blocks per partition (<= 32)
-  int max_splits;
-  float qscale;  // scale * log2(e)
+  int cap_blocks;  // max blocks per chunk (0 = balance over the grid)
+  float qscale;    // scale * log2(e)
 };
 
 __device__ __forceinline__ int clamp_len(int L, int cap, int32_t* err) {
@@ -214,38 +236,44 @@ __device__ __forceinline__ int clamp_len(int L, int cap, int32_t* err) {
   return L;
 }
 
-struct Item {
-  int seq, split, kvh;
+// Position in the block stream -> (sequence, KV head, block within segment).
+struct Cursor {
+  int seq, kvh, j, nb;  // nb = blocks in the segment (sequence)
+  long long seg_start;  // stream index of the segment's block 0
 };
 
-// Item w -> (sequence, partition, KV head), KV head fastest.
-__device__ __forceinline__ Item decode_item(long long w, int hkv, const int* prefix, int S) {
-  Item it;
-  it.kvh = static_cast<int>(w % hkv);
-  const int u = static_cast<int>(w / hkv);
-  int lo = 0, hi = S;  // largest i with prefix[i] <= u
+__device__ __forceinline__ Cursor locate(long long x, const int* pfx, int S, int hkv) {
+  int lo = 0, hi = S;  // largest i with pfx[i] * hkv <= x
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (prefix[mid] <= u) lo = mid;
+    if (static_cast<long long>(pfx[mid]) * hkv <= x) lo = mid;
     else hi = mid;
   }
-  it.seq = lo;
-  it.split = u - prefix[lo];
-  return it;
+  Cursor c;
+  c.seq = lo;
+  c.nb = pfx[lo + 1] - pfx[lo];
+  const long long r = x - static_cast<long long>(pfx[lo]) * hkv;
+  c.kvh = static_cast<int>(r / c.nb);
+  c.j = static_cast<int>(r % c.nb);
+  c.seg_start = static_cast<long long>(pfx[lo]) * hkv + static_cast<long long>(c.kvh) * c.nb;
+  return c;
 }
 
 template <int D, int BS, int G>
-__global__ void __launch_bounds__(kThreads, 2) paged_decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    paged_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap) {
   using SH = Shape<D, BS, G>;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_FULL);
   uint64_t* empty_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_EMPTY);
   int* flags = reinterpret_cast<int*>(smem + SH::OFF_FLAGS);
   volatile int* abort_flag = flags;
-  unsigned char* ring = smem + SH::OFF_RING;
-  float* m_acc = reinterpret_cast<float*>(smem + SH::OFF_MACC);
-  float* m_ml = reinterpret_cast<float*>(smem + SH::OFF_MML);
-  int* prefix = reinterpret_cast<int*>(smem + SH::OFF_PREFIX);
+  const uint32_t smem_base = smem_addr(smem);
+  unsigned char* ring = smem + (((smem_base + SH::RING_MIN + 1023u) & ~1023u) - smem_base);
+  float* m_acc = reinterpret_cast<float*>(ring + SH::RING_BYTES);
+  float* m_ml = m_acc + kConsumerWarps * G * D;
+  int* pfx = reinterpret_cast<int*>(m_ml + kConsumerWarps * G * 2);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -264,20 +292,18 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_kernel(const DecodeP
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
 
-  // ---- partitions per sequence, exclusive prefix sum in shared memory ----
+  // ---- blocks per sequence, exclusive prefix sum in shared memory ----
   for (int i = tid; i < S; i += kThreads) {
     const int L = clamp_len(__ldg(p.seq_lens + i), cap, p.err);
-    const int nblk = (L + BS - 1) / BS;
-    const int ns = (nblk + p.part_blocks - 1) / p.part_blocks;
-    prefix[i + 1] = ns > 0 ? ns : 1;
+    pfx[i + 1] = (L + BS - 1) / BS;
   }
-  if (tid == 0) prefix[0] = 0;
+  if (tid == 0) pfx[0] = 0;
   __syncthreads();
   {
     const int per = (S + kThreads - 1) / kThreads;
     const int lo = min(S, tid * per), hi = min(S, lo + per);
     int sum = 0;
-    for (int i = lo; i < hi; ++i) sum += prefix[i + 1];
+    for (int i = lo; i < hi; ++i) sum += pfx[i + 1];
     int incl = sum;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -290,53 +316,59 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_kernel(const DecodeP
     int run = incl - sum;
     for (int w = 0; w < warp; ++w) run += wsum[w];
     for (int i = lo; i < hi; ++i) {
-      run += prefix[i + 1];
-      prefix[i + 1] = run;
+      run += pfx[i + 1];
+      pfx[i + 1] = run;
     }
   }
   __syncthreads();
-  const long long total_items = static_cast<long long>(prefix[S]) * Hkv;
+
+  const long long total = static_cast<long long>(pfx[S]) * Hkv;  // blocks in the stream
+  long long chunk = (total + gridDim.x - 1) / gridDim.x;
+  if (p.cap_blocks > 0 && chunk > p.cap_blocks) chunk = p.cap_blocks;
+  if (chunk < 1) chunk = 1;
+  const long long nchunks = (total + chunk - 1) / chunk;
 
   if (warp == kConsumerWarps) {
     // =========================== producer warp ===========================
     uint32_t g = 0;  // ring sequence number
-    for (long long w = blockIdx.x; w < total_items; w += gridDim.x) {
-      const Item it = decode_item(w, Hkv, prefix, S);
-      const int L = min(max(__ldg(p.seq_lens + it.seq), 0), cap);
-      const int nblk = (L + BS - 1) / BS;
-      const int b0 = it.split * p.part_blocks;
-      const int nb = max(0, min(nblk, b0 + p.part_blocks) - b0);
-      const int phys_lane =
-          lane < nb ? __ldg(p.block_table + static_cast<long long>(it.seq) * p.max_blocks + b0 + lane)
-                    : 0;
-      for (int j = 0; j < nb; ++j, ++g) {
-        const int stage = g % SH::NST;
-        const uint32_t use = g / SH::NST;
-        const int phys = __shfl_sync(0xffffffffu, phys_lane, j);
-        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) continue;
-        if (use > 0 &&
-            !warp_wait_phase(smem_addr(&empty_bar[stage]), (use - 1) & 1, abort_flag, p.err))
-          continue;
-        const bool bad = phys < 0 || phys >= p.num_blocks;
-        const int rows = min(BS, L - (b0 + j) * BS);
-        const uint32_t fb = smem_addr(&full_bar[stage]);
-        if (lane == 0) {
-          if (bad) atomicOr(p.err, PA_DEVERR_BAD_BLOCK);
-          mbar_arrive_expect_tx(fb, bad ? 0u : 2u * rows * SH::ROW_BYTES);
-        }
-        __syncwarp();
-        if (!bad) {
-          const uint32_t kdst = smem_addr(ring + stage * SH::STAGE_BYTES);
-          const long long row0 = static_cast<long long>(phys) * BS;
-          for (int c = lane; c < 2 * rows; c += 32) {
-            const bool is_v = c >= rows;
-            const int r = is_v ? c - rows : c;
-            const __half* src =
-                (is_v ? p.v_pool : p.k_pool) + ((row0 + r) * Hkv + it.kvh) * static_cast<long long>(D);
-            bulk_copy_g2s(kdst + (is_v ? SH::TILE_BYTES : 0) + r * SH::ROW_BYTES, src,
-                          SH::ROW_BYTES, fb);
+    for (long long c = blockIdx.x; c < nchunks; c += gridDim.x) {
+      long long x = c * chunk;
+      const long long xe = min(total, x + chunk);
+      while (x < xe) {
+        const Cursor cur = locate(x, pfx, S, Hkv);
+        const int n = static_cast<int>(min(static_cast<long long>(cur.nb - cur.j), xe - x));
+        const int32_t* trow = p.block_table + static_cast<long long>(cur.seq) * p.max_blocks;
+        for (int j0 = 0; j0 < n; j0 += 32) {
+          const int phys_lane = (j0 + lane < n) ? __ldg(trow + cur.j + j0 + lane) : 0;
+          const int nn = min(32, n - j0);
+          for (int jj = 0; jj < nn; ++jj, ++g) {
+            const int stage = g % SH::NST;
+            const uint32_t use = g / SH::NST;
+            const int phys = __shfl_sync(0xffffffffu, phys_lane, jj);
+            if (__shfl_sync(0xffffffffu, *abort_flag, 0)) continue;
+            if (use > 0 &&
+                !warp_wait_phase(smem_addr(&empty_bar[stage]), (use - 1) & 1, abort_flag, p.err))
+              continue;
+            const bool bad = phys < 0 || phys >= p.num_blocks;
+            if (lane == 0) {
+              const uint32_t fb = smem_addr(&full_bar[stage]);
+              if (bad) atomicOr(p.err, PA_DEVERR_BAD_BLOCK);
+              // whole tiles: rows past the sequence end are masked by the consumers
+              mbar_arrive_expect_tx(fb, bad ? 0u : static_cast<uint32_t>(SH::STAGE_BYTES));
+              if (!bad) {
+                const uint32_t kdst = smem_addr(ring + stage * SH::STAGE_BYTES);
+#pragma unroll
+                for (int h = 0; h < SH::NHALF; ++h) {
+                  tma_load_3d(kdst + h * SH::HALF_BYTES, &kmap, 64 * h, cur.kvh, phys * BS, fb);
+                  tma_load_3d(kdst + SH::TILE_BYTES + h * SH::HALF_BYTES, &vmap, 64 * h, cur.kvh,
+                              phys * BS, fb);
+                }
+              }
+            }
+            __syncwarp();
           }
         }
+        x += n;
       }
     }
     // After an abort, wait (bounded) for copies still landing in the ring.
@@ -354,261 +386,339 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_kernel(const DecodeP
 
   // ============================ consumer warps ============================
   const int cw = warp;
-  const int grp = lane / SH::LPR;  // row group within the warp
-  const int gl = lane % SH::LPR;   // lane within the row group
-  const int ct = tid;              // consumer thread index 0..127
-  uint32_t g = 0;
+  const int gid = lane >> 2;  // mma group id: row of A / column of B
+  const int tig = lane & 3;   // thread in group
+  const int ct = tid;         // consumer thread 0..127
 
-  for (long long w = blockIdx.x; w < total_items; w += gridDim.x) {
-    const Item it = decode_item(w, Hkv, prefix, S);
-    const int L = min(max(__ldg(p.seq_lens + it.seq), 0), cap);
-    const int nblk = (L + BS - 1) / BS;
-    const int b0 = it.split * p.part_blocks;
-    const int nb = max(0, min(nblk, b0 + p.part_blocks) - b0);
-    const int nsplit = prefix[it.seq + 1] - prefix[it.seq];
-    const int head0 = it.kvh * G;
+  // zero outputs of empty sequences (this CTA's share)
+  for (int i = blockIdx.x; i < S; i += gridDim.x) {
+    if (pfx[i + 1] == pfx[i]) {
+      __half* o = p.out + static_cast<long long>(i) * p.num_q_heads * D;
+      for (int e = ct; e < p.num_q_heads * D; e += kConsumerWarps * 32) o[e] = __float2half_rn(0.f);
+    }
+  }
 
-    // q of the G heads, this lane's dims, pre-scaled into the base-2 domain
-    float2 q2[G][SH::H2];
+  // ldmatrix addressing inside a swizzled tile: lane supplies row (lane & 7)
+  // of matrix (lane >> 3); logical 16-byte chunk c of row t sits at chunk
+  // c ^ (t & 7) of its 128-byte line (rows of a matrix share t & 7 == lane & 7).
+  const int ld_row = lane & 7;
+  const int ld_mat = lane >> 3;
+
+  uint32_t g = 0;    // ring sequence number of the next block
+  uint32_t kblk = 0;  // block index within the CTA's stream (round-robin owner)
+  for (long long c = blockIdx.x; c < nchunks; c += gridDim.x) {
+    long long x = c * chunk;
+    const long long xe = min(total, x + chunk);
+    bool first_piece = true;
+    while (x < xe) {
+      const Cursor cur = locate(x, pfx, S, Hkv);
+      const int n = static_cast<int>(min(static_cast<long long>(cur.nb - cur.j), xe - x));
+      const int L = min(max(__ldg(p.seq_lens + cur.seq), 0), cap);
+      const int head0 = cur.kvh * G;
+
+      // Q fragments (A operand, heads as rows): a0/a2 of each k-step; rows >= G are zero
+      uint32_t qa[SH::KSTEPS][2];
+      {
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+            p.q + (static_cast<long long>(cur.seq) * p.num_q_heads + head0 + gid) * D);
 #pragma unroll
-    for (int gg = 0; gg < G; ++gg) {
-      const __half* qrow =
-          p.q + (static_cast<long long>(it.seq) * p.num_q_heads + head0 + gg) * static_cast<long long>(D);
-#pragma unroll
-      for (int c = 0; c < SH::NCH; ++c) {
-        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qrow) + c * SH::LPR + gl);
-        const __half2* h = reinterpret_cast<const __half2*>(&raw);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __half22float2(h[e]);
-          q2[gg][c * 4 + e] = make_float2(f.x * p.qscale, f.y * p.qscale);
+        for (int kk = 0; kk < SH::KSTEPS; ++kk) {
+          qa[kk][0] = gid < G ? __ldg(qrow + kk * 8 + tig) : 0u;
+          qa[kk][1] = gid < G ? __ldg(qrow + kk * 8 + 4 + tig) : 0u;
         }
       }
-    }
-    float m[G], l[G];
-    float2 acc[G][SH::H2];
+      float m_run = -INFINITY, l_run = 0.f;  // head gid: running max (log2 units), partial sum
+      float o[SH::MT][4];                     // O^T[d = mt*16 + gid (+8)][h = 2*tig (+1)]
 #pragma unroll
-    for (int gg = 0; gg < G; ++gg) {
-      m[gg] = -INFINITY;
-      l[gg] = 0.f;
-#pragma unroll
-      for (int e = 0; e < SH::H2; ++e) acc[gg][e] = make_float2(0.f, 0.f);
-    }
+      for (int mt = 0; mt < SH::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
-    for (int j = cw; j < nb; j += kConsumerWarps) {
-      const uint32_t gj = g + j;
-      const int stage = gj % SH::NST;
-      if (!warp_wait_phase(smem_addr(&full_bar[stage]), (gj / SH::NST) & 1, abort_flag, p.err))
-        continue;
-      const int rows = min(BS, L - (b0 + j) * BS);
-      const bool full = rows == BS;
-      const unsigned char* kt = ring + stage * SH::STAGE_BYTES;
-      const unsigned char* vt = kt + SH::TILE_BYTES;
+      for (int jj = 0; jj < n; ++jj) {
+        const uint32_t gj = g + jj;
+        if (((kblk + jj) % kConsumerWarps) != static_cast<uint32_t>(cw)) continue;
+        const int stage = gj % SH::NST;
+        if (!warp_wait_phase(smem_addr(&full_bar[stage]), (gj / SH::NST) & 1, abort_flag, p.err))
+          continue;
+        const int blk = cur.j + jj;
+        const int rows = min(BS, L - blk * BS);
+        unsigned char* kt = ring + stage * SH::STAGE_BYTES;
+        unsigned char* vt = kt + SH::TILE_BYTES;
+        if (rows < BS) {
+          // rows past the sequence end must add exactly zero to P V
+          const int words = (BS - rows) * 8;  // 16-byte words per half
 #pragma unroll
-      for (int bt = 0; bt < SH::NBATCH; ++bt) {
-        float s[SH::TB][G];
+          for (int h = 0; h < SH::NHALF; ++h) {
+            uint4* z = reinterpret_cast<uint4*>(vt + h * SH::HALF_BYTES + rows * 128);
+            for (int w = lane; w < words; w += 32) z[w] = make_uint4(0, 0, 0, 0);
+          }
+          __syncwarp();
+        }
+        const uint32_t kaddr = smem_addr(kt);
+        const uint32_t vaddr = smem_addr(vt);
+
+        // ---- S = Q K^T for each 8-token group ----
+        // x4 of k-steps (kk, kk+1): matrix m covers dims (2*kk + m) * 8 .. +8
+        float s[SH::NT][4];
 #pragma unroll
-        for (int k = 0; k < SH::TB; ++k) {
-          const int row = (bt * SH::TB + k) * SH::SG + grp;
-          float2 a[G];
+        for (int nt = 0; nt < SH::NT; ++nt) {
+          s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+          const uint32_t rowa = kaddr + (nt * 8 + ld_row) * 128;
 #pragma unroll
-          for (int gg = 0; gg < G; ++gg) a[gg] = make_float2(0.f, 0.f);
+          for (int kk = 0; kk < SH::KSTEPS; kk += 2) {
+            const int gc = 2 * kk + ld_mat;  // 16-byte chunk of the row, 0 .. D/8-1
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(rowa + (gc >> 3) * SH::HALF_BYTES + (((gc & 7) ^ ld_row) << 4), b0, b1, b2, b3);
+            mma_16816(s[nt], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+            mma_16816(s[nt], qa[kk + 1][0], 0u, qa[kk + 1][1], 0u, b2, b3);
+          }
+        }
+        // ---- online softmax over this block's tokens (row gid = head) ----
+        float mx = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < SH::NCH; ++c) {
-            const uint4 raw =
-                *reinterpret_cast<const uint4*>(kt + row * SH::ROW_BYTES + (c * SH::LPR + gl) * 16);
-            const __half2* h = reinterpret_cast<const __half2*>(&raw);
+        for (int nt = 0; nt < SH::NT; ++nt) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 kf = __half22float2(h[e]);
+          for (int e = 0; e < 2; ++e) {
+            const int t = nt * 8 + 2 * tig + e;
+            const float v = t < rows ? s[nt][e] * p.qscale : -INFINITY;
+            s[nt][e] = v;
+            mx = fmaxf(mx, v);
+          }
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run, mx);
+        const float mu = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = fast_exp2(m_run - mu);
+        m_run = m_new;
+        float ps = 0.f;
+        uint32_t pb[SH::NT];  // P as fp16 pairs: B operand of the PV mma
 #pragma unroll
-              for (int gg = 0; gg < G; ++gg) a[gg] = ffma2(q2[gg][c * 4 + e], kf, a[gg]);
+        for (int nt = 0; nt < SH::NT; ++nt) {
+          const float p0 = fast_exp2(s[nt][0] - mu);
+          const float p1 = fast_exp2(s[nt][1] - mu);
+          ps += p0 + p1;
+          pb[nt] = pack_half2(p0, p1);
+        }
+        l_run = l_run * alpha + ps;
+        // rescale O^T columns: heads 2*tig and 2*tig+1 live in mma groups 2*tig, 2*tig+1
+        const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * tig);
+        const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);
+#pragma unroll
+        for (int mt = 0; mt < SH::MT; ++mt) {
+          o[mt][0] *= a_lo;
+          o[mt][1] *= a_hi;
+          o[mt][2] *= a_lo;
+          o[mt][3] *= a_hi;
+        }
+        // ---- O^T += V^T P^T over 16-token k-steps ----
+        // x4.trans of m-tile mt: matrix m covers tokens +8*(m>>1), dims mt*16 + 8*(m&1)
+#pragma unroll
+        for (int pk = 0; pk < SH::PK; ++pk) {
+          const uint32_t pb0 = pb[2 * pk];
+          const uint32_t pb1 = (2 * pk + 1 < SH::NT) ? pb[2 * pk + 1] : 0u;
+          const uint32_t rowa = vaddr + (pk * 16 + ld_row + (ld_mat >> 1) * 8) * 128;
+#pragma unroll
+          for (int mt = 0; mt < SH::MT; ++mt) {
+            const int gc = 2 * mt + (ld_mat & 1);
+            const uint32_t addr = rowa + (gc >> 3) * SH::HALF_BYTES + (((gc & 7) ^ ld_row) << 4);
+            uint32_t a0, a1, a2, a3;
+            if (2 * pk + 1 < SH::NT) {
+              ldsm_x4_t(addr, a0, a1, a2, a3);
+            } else {
+              ldsm_x2_t(addr, a0, a1);
+              a2 = a3 = 0u;
             }
-          }
-#pragma unroll
-          for (int gg = 0; gg < G; ++gg) s[k][gg] = a[gg].x + a[gg].y;
-        }
-#pragma unroll
-        for (int off = 1; off < SH::LPR; off <<= 1) {
-#pragma unroll
-          for (int k = 0; k < SH::TB; ++k)
-#pragma unroll
-            for (int gg = 0; gg < G; ++gg) s[k][gg] += __shfl_xor_sync(0xffffffffu, s[k][gg], off);
-        }
-        // online softmax update (base 2)
-        float pr[SH::TB][G];
-#pragma unroll
-        for (int gg = 0; gg < G; ++gg) {
-          float mx = -INFINITY;
-#pragma unroll
-          for (int k = 0; k < SH::TB; ++k) {
-            const bool valid = full || ((bt * SH::TB + k) * SH::SG + grp) < rows;
-            if (valid) mx = fmaxf(mx, s[k][gg]);
-          }
-          const float mn = fmaxf(m[gg], mx);
-          const float mu = mn == -INFINITY ? 0.f : mn;
-          const float alpha = fast_exp2(m[gg] - mu);
-          float ps = 0.f;
-#pragma unroll
-          for (int k = 0; k < SH::TB; ++k) {
-            const bool valid = full || ((bt * SH::TB + k) * SH::SG + grp) < rows;
-            pr[k][gg] = valid ? fast_exp2(s[k][gg] - mu) : 0.f;
-            ps += pr[k][gg];
-          }
-          l[gg] = l[gg] * alpha + ps;
-          m[gg] = mn;
-          const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-          for (int e = 0; e < SH::H2; ++e) acc[gg][e] = fmul2(acc[gg][e], a2);
-        }
-        // weighted sum of V rows
-#pragma unroll
-        for (int k = 0; k < SH::TB; ++k) {
-          const int row = (bt * SH::TB + k) * SH::SG + grp;
-          if (!full && row >= rows) continue;
-#pragma unroll
-          for (int c = 0; c < SH::NCH; ++c) {
-            const uint4 raw =
-                *reinterpret_cast<const uint4*>(vt + row * SH::ROW_BYTES + (c * SH::LPR + gl) * 16);
-            const __half2* h = reinterpret_cast<const __half2*>(&raw);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 vf = __half22float2(h[e]);
-#pragma unroll
-              for (int gg = 0; gg < G; ++gg)
-                acc[gg][c * 4 + e] = ffma2(make_float2(pr[k][gg], pr[k][gg]), vf, acc[gg][c * 4 + e]);
-            }
+            mma_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
           }
         }
+        if (rows < BS) fence_proxy_async_smem();  // generic zero-fill before the next bulk copy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&empty_bar[stage]));
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&empty_bar[stage]));
-    }
-    g += nb;
 
-    // ---- merge the row groups of this warp (lanes with equal gl) ----
+      // ---- piece finished: merge the four warps ----
+      l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+      l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
 #pragma unroll
-    for (int off = SH::LPR; off < 32; off <<= 1) {
-#pragma unroll
-      for (int gg = 0; gg < G; ++gg) {
-        const float mo = __shfl_xor_sync(0xffffffffu, m[gg], off);
-        const float lo = __shfl_xor_sync(0xffffffffu, l[gg], off);
-        const float mn = fmaxf(m[gg], mo);
-        const float mu = mn == -INFINITY ? 0.f : mn;
-        const float wa = fast_exp2(m[gg] - mu), wb = fast_exp2(mo - mu);
-        l[gg] = l[gg] * wa + lo * wb;
-        m[gg] = mn;
-#pragma unroll
-        for (int e = 0; e < SH::H2; ++e) {
-          float2 o;
-          o.x = __shfl_xor_sync(0xffffffffu, acc[gg][e].x, off);
-          o.y = __shfl_xor_sync(0xffffffffu, acc[gg][e].y, off);
-          acc[gg][e] = ffma2(make_float2(wb, wb), o, fmul2(acc[gg][e], make_float2(wa, wa)));
+      for (int mt = 0; mt < SH::MT; ++mt) {
+        const int d = mt * 16 + gid;
+        const int h0 = 2 * tig, h1 = 2 * tig + 1;
+        if (h0 < G) {
+          m_acc[(cw * G + h0) * D + d] = o[mt][0];
+          m_acc[(cw * G + h0) * D + d + 8] = o[mt][2];
+        }
+        if (h1 < G) {
+          m_acc[(cw * G + h1) * D + d] = o[mt][1];
+          m_acc[(cw * G + h1) * D + d + 8] = o[mt][3];
         }
       }
-    }
-    // ---- across warps through shared memory ----
-    if (grp == 0) {
-#pragma unroll
-      for (int gg = 0; gg < G; ++gg) {
-        float* dst = m_acc + (cw * G + gg) * D;
-#pragma unroll
-        for (int c = 0; c < SH::NCH; ++c) {
-          float4* d4 = reinterpret_cast<float4*>(dst + (c * SH::LPR + gl) * 8);
-          d4[0] = make_float4(acc[gg][c * 4 + 0].x, acc[gg][c * 4 + 0].y, acc[gg][c * 4 + 1].x,
-                              acc[gg][c * 4 + 1].y);
-          d4[1] = make_float4(acc[gg][c * 4 + 2].x, acc[gg][c * 4 + 2].y, acc[gg][c * 4 + 3].x,
-                              acc[gg][c * 4 + 3].y);
-        }
+      if (tig == 0 && gid < G) {
+        m_ml[(cw * G + gid) * 2] = m_run;
+        m_ml[(cw * G + gid) * 2 + 1] = l_run;
       }
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int gg = 0; gg < G; ++gg) {
-        m_ml[(cw * G + gg) * 2] = m[gg];
-        m_ml[(cw * G + gg) * 2 + 1] = l[gg];
-      }
-    }
-    consumer_sync();
-    const long long rec =
-        (static_cast<long long>(it.seq) * Hkv + it.kvh) * p.max_splits + it.split;
-    for (int idx = ct; idx < G * D; idx += kConsumerWarps * 32) {
-      const int gg = idx / D, d = idx % D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int x = 0; x < kConsumerWarps; ++x) M = fmaxf(M, m_ml[(x * G + gg) * 2]);
-      const float mu = M == -INFINITY ? 0.f : M;
-      float Ls = 0.f, A = 0.f;
-#pragma unroll
-      for (int x = 0; x < kConsumerWarps; ++x) {
-        const float wgt = fast_exp2(m_ml[(x * G + gg) * 2] - mu);
-        Ls += m_ml[(x * G + gg) * 2 + 1] * wgt;
-        A += m_acc[(x * G + gg) * D + d] * wgt;
-      }
-      if (nsplit == 1) {
-        p.out[(static_cast<long long>(it.seq) * p.num_q_heads + head0 + gg) * D + d] =
-            __float2half_rn(Ls > 0.f ? A / Ls : 0.f);
-      } else {
-        p.part_acc[rec * (G * D) + idx] = A;
-        if (d == 0) {
-          p.part_ml[(rec * G + gg) * 2] = M;
-          p.part_ml[(rec * G + gg) * 2 + 1] = Ls;
-        }
-      }
-    }
-    if (nsplit > 1) {
-      __threadfence();
       consumer_sync();
-      int* cnt = p.counters + static_cast<long long>(it.seq) * Hkv + it.kvh;
-      if (ct == 0) flags[1] = (atomicAdd(cnt, 1) == nsplit - 1) ? 1 : 0;
-      consumer_sync();
-      if (flags[1]) {
-        __threadfence();
-        const long long rec0 = (static_cast<long long>(it.seq) * Hkv + it.kvh) * p.max_splits;
-        for (int idx = ct; idx < G * D; idx += kConsumerWarps * 32) {
-          const int gg = idx / D, d = idx % D;
-          float M = -INFINITY;
-          for (int x = 0; x < nsplit; ++x) M = fmaxf(M, __ldcg(p.part_ml + ((rec0 + x) * G + gg) * 2));
-          const float mu = M == -INFINITY ? 0.f : M;
-          float Ls = 0.f, A = 0.f;
-          for (int x = 0; x < nsplit; ++x) {
-            const float mx = __ldcg(p.part_ml + ((rec0 + x) * G + gg) * 2);
-            const float lx = __ldcg(p.part_ml + ((rec0 + x) * G + gg) * 2 + 1);
-            const float wgt = fast_exp2(mx - mu);
-            Ls += lx * wgt;
-            A += __ldcg(p.part_acc + (rec0 + x) * (G * D) + idx) * wgt;
-          }
-          p.out[(static_cast<long long>(it.seq) * p.num_q_heads + head0 + gg) * D + d] =
+      const bool cut = cur.j > 0 || cur.j + n < cur.nb;
+      const long long rec = 2 * c + (first_piece ? 0 : 1);
+      float* recp = p.records + rec * (G * (D + 2));
+      for (int idx = ct; idx < G * D; idx += kConsumerWarps * 32) {
+        const int gg = idx / D, d = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, m_ml[(w * G + gg) * 2]);
+        const float mu = M == -INFINITY ? 0.f : M;
+        float Ls = 0.f, A = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float wgt = fast_exp2(m_ml[(w * G + gg) * 2] - mu);
+          Ls += m_ml[(w * G + gg) * 2 + 1] * wgt;
+          A += m_acc[(w * G + gg) * D + d] * wgt;
+        }
+        if (!cut) {
+          p.out[(static_cast<long long>(cur.seq) * p.num_q_heads + head0 + gg) * D + d] =
               __float2half_rn(Ls > 0.f ? A / Ls : 0.f);
+        } else {
+          recp[idx] = A;
+          if (d == 0) {
+            recp[G * D + 2 * gg] = M;
+            recp[G * D + 2 * gg + 1] = Ls;
+          }
         }
-        if (ct == 0) atomicExch(cnt, 0);
       }
+      if (cut) {
+        // chunks covering this segment: c_first .. c_last; the last to arrive merges
+        const long long s0 = cur.seg_start, s1 = cur.seg_start + cur.nb;
+        const long long c_first = s0 / chunk, c_last = (s1 - 1) / chunk;
+        const int expected = static_cast<int>(c_last - c_first + 1);
+        __threadfence();
+        consumer_sync();
+        int* cnt = p.counters + static_cast<long long>(cur.seq) * Hkv + cur.kvh;
+        if (ct == 0) flags[1] = (atomicAdd(cnt, 1) == expected - 1) ? 1 : 0;
+        consumer_sync();
+        if (flags[1]) {
+          __threadfence();
+          for (int idx = ct; idx < G * D; idx += kConsumerWarps * 32) {
+            const int gg = idx / D, d = idx % D;
+            float M = -INFINITY;
+            for (long long cc = c_first; cc <= c_last; ++cc) {
+              const long long r = 2 * cc + ((cc == c_first && s0 > cc * chunk) ? 1 : 0);
+              M = fmaxf(M, __ldcg(p.records + r * (G * (D + 2)) + G * D + 2 * gg));
+            }
+            const float mu = M == -INFINITY ? 0.f : M;
+            float Ls = 0.f, A = 0.f;
+            for (long long cc = c_first; cc <= c_last; ++cc) {
+              const long long r = 2 * cc + ((cc == c_first && s0 > cc * chunk) ? 1 : 0);
+              const float* rp = p.records + r * (G * (D + 2));
+              const float wgt = fast_exp2(__ldcg(rp + G * D + 2 * gg) - mu);
+              Ls += __ldcg(rp + G * D + 2 * gg + 1) * wgt;
+              A += __ldcg(rp + idx) * wgt;
+            }
+            p.out[(static_cast<long long>(cur.seq) * p.num_q_heads + head0 + gg) * D + d] =
+                __float2half_rn(Ls > 0.f ? A / Ls : 0.f);
+          }
+          if (ct == 0) atomicExch(cnt, 0);
+        }
+      }
+      consumer_sync();  // merge buffers and flags[1] are reused by the next piece
+      g += n;
+      kblk += n;
+      x += n;
+      first_piece = false;
     }
-    consumer_sync();  // merge buffers and flags[1] are reused by the next item
   }
 }
 
 // --------------------------------------------------------------- host ---
-int default_partition(int /*block_size*/) { return kDefaultPartitionTokens; }
-
 struct Layout {
-  size_t counters = 0, part_ml = 0, part_acc = 0, total = 0;
-  int max_splits = 0;
+  size_t counters = 0, records = 0, total = 0;
+  long long max_records = 0;
 };
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
-Layout workspace_layout(int S, int Hq, int Hkv, int D, int BS, int MB, int part_tokens) {
+// Chunks a launch can produce: at most one per CTA of the grid (kMaxGrid),
+// or, with a per-chunk cap, enough to cover every block of every segment.
+long long max_chunks(int S, int Hkv, int MB, int cap_blocks) {
+  long long m = kMaxGrid;
+  if (cap_blocks > 0) {
+    const long long blocks = static_cast<long long>(S) * Hkv * MB;
+    const long long need = (blocks + cap_blocks - 1) / cap_blocks;
+    if (need > m) m = need;
+  }
+  return m;
+}
+
+Layout workspace_layout(int S, int Hq, int Hkv, int D, int MB, int cap_blocks) {
   Layout w;
-  const int pb = part_tokens / BS;
-  w.max_splits = (MB + pb - 1) / pb;
   const int G = Hq / Hkv;
-  const size_t units = static_cast<size_t>(S) * Hkv * w.max_splits;
+  w.max_records = 2 * max_chunks(S, Hkv, MB, cap_blocks);
   w.counters = 0;
-  w.part_ml = round256(static_cast<size_t>(S) * Hkv * 4);
-  w.part_acc = w.part_ml + round256(units * G * 2 * 4);
-  w.total = w.part_acc + round256(units * G * D * 4);
+  w.records = round256(static_cast<size_t>(S) * Hkv * 4);
+  w.total = w.records + round256(static_cast<size_t>(w.max_records) * G * (D + 2) * 4);
   return w;
+}
+
+// --- TMA descriptors of the pools -------------------------------------------
+// A 3-D tensor map over a pool seen as [NB*BS rows][Hkv][D] fp16 (innermost
+// first: D, Hkv, rows), box {64, 1, BS} with the 128-byte swizzle: one copy
+// moves one 64-dimension half of one KV head of one block. Encoding costs a
+// few microseconds of host time, so the last few maps are cached by (device,
+// pointer, shape).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct MapKey {
+  int device;
+  const void* ptr;
+  int D, BS, Hkv, NB;
+  bool operator==(const MapKey& o) const {
+    return device == o.device && ptr == o.ptr && D == o.D && BS == o.BS && Hkv == o.Hkv &&
+           NB == o.NB;
+  }
+};
+
+pa_status pool_tensor_map(const MapKey& key, CUtensorMap* out) {
+  static std::mutex mu;
+  static EncodeTiledFn encode = nullptr;
+  constexpr int kCache = 8;
+  static MapKey keys[kCache];
+  static CUtensorMap maps[kCache];
+  static int used = 0, next = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (keys[i] == key) {
+      *out = maps[i];
+      return PA_OK;
+    }
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e =
+        cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+      return pa::fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(key.D), static_cast<cuuint64_t>(key.Hkv),
+                              static_cast<cuuint64_t>(key.NB) * key.BS};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(key.D) * 2,
+                                 static_cast<cuuint64_t>(key.Hkv) * key.D * 2};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(key.BS)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUtensorMap m;
+  CUresult r = encode(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(key.ptr), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return pa::fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a pool of %d blocks",
+                    static_cast<int>(r), key.NB);
+  keys[next] = key;
+  maps[next] = m;
+  next = (next + 1) % kCache;
+  if (used < kCache) ++used;
+  *out = m;
+  return PA_OK;
 }
 
 template <int D, int BS, int G>
@@ -642,12 +752,14 @@ pa_status launch_decode(const DecodeParams& prm, const pa::DeviceInfo& dev, cuda
     occ = occ_val[dev.device];
   }
   if (occ < 1) return pa::fail(PA_ERR_UNSUPPORTED, "pa_decode_attention: kernel does not fit an SM");
-  const long long upper =
-      static_cast<long long>(prm.num_seqs) * prm.num_kv_heads * prm.max_splits;
+  CUtensorMap kmap, vmap;
+  MapKey kk{dev.device, prm.k_pool, D, BS, prm.num_kv_heads, prm.num_blocks};
+  MapKey vk{dev.device, prm.v_pool, D, BS, prm.num_kv_heads, prm.num_blocks};
+  if (pa_status s = pool_tensor_map(kk, &kmap)) return s;
+  if (pa_status s = pool_tensor_map(vk, &vmap)) return s;
   long long grid = static_cast<long long>(dev.sm_count) * occ;
-  if (grid > upper) grid = upper;
-  if (grid < 1) grid = 1;
-  kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(prm);
+  if (grid > kMaxGrid) grid = kMaxGrid;
+  kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(prm, kmap, vmap);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_decode_attention launch");
   return PA_OK;
@@ -688,9 +800,9 @@ pa_status check_decode_shape(int S, int Hq, int Hkv, int D, int BS, int MB, int 
   if (BS != 8 && BS != 16 && BS != 32)
     return pa::fail(PA_ERR_UNSUPPORTED, "block_size %d not in {8,16,32}", BS);
   if (S > kMaxSeqs) return pa::fail(PA_ERR_UNSUPPORTED, "num_seqs %d > %d", S, kMaxSeqs);
-  if (part_tokens <= 0 || part_tokens % BS || part_tokens > 32 * BS)
+  if (part_tokens < 0 || part_tokens % BS)
     return pa::fail(PA_ERR_INVALID_ARG,
-                    "partition_tokens %d must be a positive multiple of block_size <= 32 blocks",
+                    "partition_tokens %d must be 0 or a positive multiple of block_size",
                     part_tokens);
   if (static_cast<long long>(MB) * BS > INT32_MAX)
     return pa::fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq * block_size exceeds int32");
@@ -703,12 +815,11 @@ extern "C" {
 
 size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                  int block_size, int max_blocks_per_seq, int partition_tokens) {
-  const int pt = partition_tokens ? partition_tokens : default_partition(block_size);
   if (check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                         max_blocks_per_seq, pt) != PA_OK)
+                         max_blocks_per_seq, partition_tokens) != PA_OK)
     return 0;
-  return workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                          max_blocks_per_seq, pt)
+  return workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                          partition_tokens / block_size)
       .total;
 }
 
@@ -732,9 +843,8 @@ pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool, const pa_
                               int max_blocks_per_seq, int num_blocks, float scale, pa_half* out,
                               void* workspace, size_t workspace_bytes, int partition_tokens,
                               pa_stream_t stream) {
-  const int pt = partition_tokens ? partition_tokens : default_partition(block_size);
   if (pa_status s = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                                       max_blocks_per_seq, pt))
+                                       max_blocks_per_seq, partition_tokens))
     return s;
   if (num_blocks <= 0 || static_cast<long long>(num_blocks) * block_size > INT32_MAX)
     return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention: num_blocks %d", num_blocks);
@@ -747,8 +857,9 @@ pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool, const pa_
       !pa::aligned16(out) || !pa::aligned16(workspace) ||
       (reinterpret_cast<uintptr_t>(block_table) & 3) || (reinterpret_cast<uintptr_t>(seq_lens) & 3))
     return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention: misaligned pointer");
-  const Layout lay = workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                                      max_blocks_per_seq, pt);
+  const int cap_blocks = partition_tokens / block_size;
+  const Layout lay = workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                      max_blocks_per_seq, cap_blocks);
   if (workspace_bytes < lay.total)
     return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention: workspace %zu < %zu bytes",
                     workspace_bytes, lay.total);
@@ -763,8 +874,7 @@ pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool, const pa_
   prm.out = reinterpret_cast<__half*>(out);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   prm.counters = reinterpret_cast<int32_t*>(ws + lay.counters);
-  prm.part_ml = reinterpret_cast<float*>(ws + lay.part_ml);
-  prm.part_acc = reinterpret_cast<float*>(ws + lay.part_acc);
+  prm.records = reinterpret_cast<float*>(ws + lay.records);
   prm.err = pa::device_error_word();
   if (!prm.err) return PA_ERR_CUDA;
   prm.num_seqs = num_seqs;
@@ -772,8 +882,7 @@ pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool, const pa_
   prm.num_kv_heads = num_kv_heads;
   prm.max_blocks = max_blocks_per_seq;
   prm.num_blocks = num_blocks;
-  prm.part_blocks = pt / block_size;
-  prm.max_splits = lay.max_splits;
+  prm.cap_blocks = cap_blocks;
   prm.qscale = scale * kLog2e;
   const int G = num_q_heads / num_kv_heads;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -57,7 +57,8 @@ def run_shared_prefix(pa, w, heads_first=(0, 13, 31), heads_last=None):
         out = pa.pa_decode_attention(dev(q), dk, dv, dev(table), dev(lens), float(w.scale))
         retiring = [j for j, s in enumerate(active) if remaining[s] == 1]
         rows = list(range(len(active))) if step == 0 else retiring
-        heads = list(heads_first) if step == 0 else heads_last
+        heads = heads_first if step == 0 else heads_last
+        heads = None if heads is None else list(heads)
         if rows:
             got = out.cpu().numpy()
             e = oracle.decode_attention(q, kp, vp, table, lens, w.scale, seqs=rows, heads=heads)
