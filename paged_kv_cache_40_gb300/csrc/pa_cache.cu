@@ -31,6 +31,9 @@ append_kv_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_ne
                  uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
                  const int32_t* __restrict__ slots, int row_vecs, int64_t num_slots,
                  int32_t* __restrict__ err) {
+  // A decode launched right after this kernel may start its prologue now; it
+  // waits for this grid to finish before it reads the pool.
+  asm volatile("griddepcontrol.launch_dependents;");
   const int t = blockIdx.x;
   const int32_t slot = __ldg(slots + t);
   if (slot < 0) return;

@@ -37,6 +37,14 @@
 //     score accumulators already hold (no transpose, no shared-memory trip).
 //     Rows of a partial last block are masked out of the softmax and zeroed in
 //     the V stage so they contribute exactly nothing.
+//   * q of a piece is copied by the producer into a small ring of q slots;
+//     consumers read their A fragments from shared memory. At the end of a
+//     piece each consumer warp publishes its state into a merge slot (two,
+//     alternating) and the last warp to arrive merges, so no warp ever waits
+//     for the others and the ring keeps draining.
+//   * Programmatic dependent launch: the prologue (prefix sum of lengths) can
+//     overlap the previous kernel on the stream; K/V, q and table reads wait
+//     for it with griddepcontrol.wait.
 //   * Every wait is bounded (about one second of %globaltimer); on expiry the
 //     kernel records PA_DEVERR_TIMEOUT, stops issuing copies, drains the copies
 //     already in flight (again bounded) and finishes without faulting.
@@ -51,7 +59,9 @@
 namespace {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kProducerWarp = kConsumerWarps;      // warp index of the producer
+constexpr int kMergeWarp = kConsumerWarps + 1;     // warp index of the merger
+constexpr int kThreads = (kConsumerWarps + 2) * 32;
 constexpr int kMaxSeqs = 16384;
 constexpr int kMaxGrid = 2048;
 constexpr int kRingBytes = 64 * 1024;
@@ -88,6 +98,15 @@ __device__ __forceinline__ unsigned long long global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+// Bulk async copy global -> this CTA's shared memory, completion on `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
 // TMA tiled copy of box {x, y, z} of a 3-D tensor map into this CTA's shared
 // memory, completion counted on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
@@ -100,9 +119,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -170,14 +186,18 @@ __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity,
 }
 
 // ------------------------------------------------------------- shapes ---
+// A partial record holds acc [G][D] then (max, sum) per head, padded to a
+// multiple of 4 floats so every record starts on a 16-byte boundary.
+__host__ __device__ constexpr int rec_floats(int G, int D) { return (G * (D + 2) + 3) / 4 * 4; }
+
 template <int D, int BS, int G>
 struct Shape {
   static_assert(G >= 1 && G <= 8, "at most 8 query heads per KV head (mma N = 8)");
   static_assert(D % 16 == 0 && BS % 8 == 0, "shape");
-  static constexpr int NHALF = D / 64;                // 64-dim (128-byte) halves per row
-  static constexpr int HALF_BYTES = BS * 128;         // one half of a tile, swizzled
+  static constexpr int NHALF = D / 64;                   // 64-dim (128-byte) halves per row
+  static constexpr int HALF_BYTES = BS * 128;            // one half of a tile, swizzled
   static constexpr int TILE_BYTES = NHALF * HALF_BYTES;  // K (or V) of one block, one head
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile then V tile
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;     // K tile then V tile
   static_assert(D % 64 == 0 && HALF_BYTES % 1024 == 0, "swizzle atoms need 1 KB halves");
   // Ring depth is a multiple of the consumer-warp count, so consecutive uses
   // of a stage belong to the same consumer warp. A parity wait can only tell
@@ -189,25 +209,39 @@ struct Shape {
                                  ? NST_RAW / kConsumerWarps * kConsumerWarps
                                  : kConsumerWarps;
   static_assert(NST % kConsumerWarps == 0, "ring depth must be a multiple of consumer warps");
-  static constexpr int KSTEPS = D / 16;  // QK k-steps over head_dim
-  static constexpr int MT = D / 16;      // PV m-tiles over head_dim
-  static constexpr int NT = BS / 8;      // 8-token groups per block
+  static constexpr int KSTEPS = D / 16;    // QK k-steps over head_dim
+  static constexpr int MT = D / 16;        // PV m-tiles over head_dim
+  static constexpr int NT = BS / 8;        // 8-token groups per block
   static constexpr int PK = (NT + 1) / 2;  // PV k-steps (16 tokens each) per block
+  // q ring: one slot per piece (segment piece), 8 rows of D halves
+  static constexpr int QS = 4;
+  static constexpr int QSLOT_BYTES = 8 * D * 2;
+  // merge slots (double-buffered by piece parity): per warp O [G][D] + (m, l) [G]
+  static constexpr int MSLOT_FLOATS = kConsumerWarps * G * (D + 2);
   // shared-memory layout (bytes): barriers and flags at fixed offsets, then
   // the ring at the next 1 KB-aligned absolute address (the swizzle pattern is
-  // a function of address bits 7..9), then the merge buffers and the prefix.
+  // a function of address bits 7..9), then q slots, merge slots and the prefix.
   static constexpr int OFF_FULL = 0;
   static constexpr int OFF_EMPTY = OFF_FULL + NST * 8;
-  static constexpr int OFF_FLAGS = OFF_EMPTY + NST * 8;  // abort, is_last, wsum[8]
-  static constexpr int RING_MIN = OFF_FLAGS + 64;
+  static constexpr int OFF_QFULL = OFF_EMPTY + NST * 8;
+  static constexpr int OFF_QEMPTY = OFF_QFULL + QS * 8;
+  static constexpr int OFF_MFULL = OFF_QEMPTY + QS * 8;   // merge slots published
+  static constexpr int OFF_MEMPTY = OFF_MFULL + 2 * 8;    // merge slots free again
+  static constexpr int OFF_FLAGS = OFF_MEMPTY + 2 * 8;    // see kFlag* below
+  static constexpr int RING_MIN = OFF_FLAGS + 128;
   static constexpr int RING_BYTES = NST * STAGE_BYTES;
-  static constexpr int MACC_BYTES = kConsumerWarps * G * D * 4;  // float [NC][G][D]
-  static constexpr int MML_BYTES = kConsumerWarps * G * 2 * 4;   // float [NC][G][2]
+  static constexpr int SCRATCH_FLOATS = 32 * G * 2;  // merge warp: staged (max, sum) pairs
+  static constexpr int REC_FLOATS = rec_floats(G, D);  // partial record stride (16-byte multiple)
+  static constexpr int TAIL_BYTES = QS * QSLOT_BYTES + 2 * MSLOT_FLOATS * 4 + SCRATCH_FLOATS * 4;
   static size_t smem_bytes(int num_seqs) {
-    return static_cast<size_t>(RING_MIN + 1024 + RING_BYTES + MACC_BYTES + MML_BYTES) +
+    return static_cast<size_t>(RING_MIN + 1024 + RING_BYTES + TAIL_BYTES) +
            static_cast<size_t>(num_seqs + 1) * 4;
   }
 };
+
+// int flags in shared memory
+constexpr int kFlagAbort = 0;  // set when a bounded wait gave up
+constexpr int kFlagWsum = 8;   // [8] warp sums of the prefix scan
 
 struct DecodeParams {
   const __half* q;
@@ -217,7 +251,7 @@ struct DecodeParams {
   const int32_t* seq_lens;
   __half* out;
   int32_t* counters;  // [S][Hkv] arrival counters of cut segments
-  float* records;     // [2 * max_chunks][G][D + 2] partial results of cut segments
+  float* records;     // [2 * max_chunks][rec_floats(G, D)] partial results of cut segments
   int32_t* err;
   int num_seqs;
   int num_q_heads;
@@ -259,6 +293,132 @@ __device__ __forceinline__ Cursor locate(long long x, const int* pfx, int S, int
   return c;
 }
 
+// One warp combines `parts` per-warp states of a piece (merge slot `ms`) and
+// either writes the fp16 output (uncut segment) or the chunk's partial record.
+template <int D, int G>
+__device__ __forceinline__ void merge_warps(const float* ms, const int* who, int parts,
+                                            __half* out_row, float* rec, bool cut) {
+  const int lane = threadIdx.x & 31;
+  for (int gg = 0; gg < G; ++gg) {
+    float M = -INFINITY;
+    for (int x = 0; x < parts; ++x) M = fmaxf(M, ms[(who[x] * G + gg) * (D + 2) + D]);
+    const float mu = M == -INFINITY ? 0.f : M;
+    float wgt[kConsumerWarps];
+    float Ls = 0.f;
+#pragma unroll
+    for (int x = 0; x < kConsumerWarps; ++x) {
+      wgt[x] = 0.f;
+      if (x < parts) {
+        const float* w = ms + (who[x] * G + gg) * (D + 2);
+        wgt[x] = fast_exp2(w[D] - mu);
+        Ls += w[D + 1] * wgt[x];
+      }
+    }
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+    for (int d = lane; d < D; d += 32) {
+      float A = 0.f;
+#pragma unroll
+      for (int x = 0; x < kConsumerWarps; ++x)
+        if (x < parts) A += ms[(who[x] * G + gg) * (D + 2) + d] * wgt[x];
+      if (!cut) out_row[gg * D + d] = __float2half_rn(A * inv);
+      else rec[gg * D + d] = A;
+    }
+    if (cut && lane == 0) {
+      rec[G * D + 2 * gg] = M;
+      rec[G * D + 2 * gg + 1] = Ls;
+    }
+  }
+}
+
+// One warp merges the partial records of a cut segment and writes its fp16
+// output. Record i of the segment is `recs + rec_of(i) * rec_floats(G, D)` holding
+// acc [G][D], then (max, sum) per head. Records are folded in batches of 32
+// with the online log-sum-exp rule: the (max, sum) pairs of a batch are staged
+// in shared memory by 32 lanes at once, and every lane then streams its float4
+// slices of the accumulators with independent loads.
+template <int D, int G, typename RecOf>
+__device__ __forceinline__ void merge_records(const float* recs, int E, RecOf rec_of,
+                                              float* scratch, __half* out_row) {
+  constexpr int NV4 = G * D / 4;              // float4 slices of one accumulator
+  constexpr int PER = (NV4 + 31) / 32;        // slices per lane
+  constexpr int RS = rec_floats(G, D);        // floats per record (16-byte multiple)
+  const int lane = threadIdx.x & 31;
+  float M[G], Ls[G];
+  float4 A[PER];
+#pragma unroll
+  for (int gg = 0; gg < G; ++gg) {
+    M[gg] = -INFINITY;
+    Ls[gg] = 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < PER; ++k) A[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int base = 0; base < E; base += 32) {
+    const int nb = min(32, E - base);
+    if (lane < nb) {
+      const float* rp = recs + rec_of(base + lane) * RS + G * D;
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg) {
+        scratch[(lane * G + gg) * 2] = __ldcg(rp + 2 * gg);
+        scratch[(lane * G + gg) * 2 + 1] = __ldcg(rp + 2 * gg + 1);
+      }
+    }
+    __syncwarp();
+    float rescale[G];
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) {
+      float Mb = -INFINITY;
+      for (int r = 0; r < nb; ++r) Mb = fmaxf(Mb, scratch[(r * G + gg) * 2]);
+      const float Mn = fmaxf(M[gg], Mb);
+      const float mu = Mn == -INFINITY ? 0.f : Mn;
+      rescale[gg] = fast_exp2(M[gg] - mu);
+      float add = 0.f;
+      for (int r = 0; r < nb; ++r)
+        add += scratch[(r * G + gg) * 2 + 1] * fast_exp2(scratch[(r * G + gg) * 2] - mu);
+      Ls[gg] = Ls[gg] * rescale[gg] + add;
+      M[gg] = Mn;
+    }
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int i = lane + 32 * k;
+      const float f = i < NV4 ? rescale[(i * 4) / D] : 0.f;
+      A[k].x *= f;
+      A[k].y *= f;
+      A[k].z *= f;
+      A[k].w *= f;
+    }
+#pragma unroll 4
+    for (int r = 0; r < nb; ++r) {
+      const float4* rp = reinterpret_cast<const float4*>(recs + rec_of(base + r) * RS);
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        const int i = lane + 32 * k;
+        if (i < NV4) {
+          const int gg = (i * 4) / D;
+          const float mu = M[gg] == -INFINITY ? 0.f : M[gg];
+          const float w = fast_exp2(scratch[(r * G + gg) * 2] - mu);
+          const float4 v = __ldcg(rp + i);
+          A[k].x += v.x * w;
+          A[k].y += v.y * w;
+          A[k].z += v.z * w;
+          A[k].w += v.w * w;
+        }
+      }
+    }
+    __syncwarp();
+  }
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int i = lane + 32 * k;
+    if (i < NV4) {
+      const int gg = (i * 4) / D;
+      const float inv = Ls[gg] > 0.f ? 1.f / Ls[gg] : 0.f;
+      __half2* o = reinterpret_cast<__half2*>(out_row + i * 4);
+      o[0] = __floats2half2_rn(A[k].x * inv, A[k].y * inv);
+      o[1] = __floats2half2_rn(A[k].z * inv, A[k].w * inv);
+    }
+  }
+}
+
 template <int D, int BS, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
@@ -267,13 +427,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_FULL);
   uint64_t* empty_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_EMPTY);
+  uint64_t* qfull_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_QFULL);
+  uint64_t* qempty_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_QEMPTY);
+  uint64_t* mfull_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_MFULL);
+  uint64_t* mempty_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_MEMPTY);
   int* flags = reinterpret_cast<int*>(smem + SH::OFF_FLAGS);
-  volatile int* abort_flag = flags;
+  volatile int* abort_flag = flags + kFlagAbort;
   const uint32_t smem_base = smem_addr(smem);
   unsigned char* ring = smem + (((smem_base + SH::RING_MIN + 1023u) & ~1023u) - smem_base);
-  float* m_acc = reinterpret_cast<float*>(ring + SH::RING_BYTES);
-  float* m_ml = m_acc + kConsumerWarps * G * D;
-  int* pfx = reinterpret_cast<int*>(m_ml + kConsumerWarps * G * 2);
+  unsigned char* qring = ring + SH::RING_BYTES;
+  float* mslots = reinterpret_cast<float*>(qring + SH::QS * SH::QSLOT_BYTES);
+  float* scratch = mslots + 2 * SH::MSLOT_FLOATS;
+  int* pfx = reinterpret_cast<int*>(scratch + SH::SCRATCH_FLOATS);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -287,8 +452,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&full_bar[s]), 1);
       mbar_init(smem_addr(&empty_bar[s]), 1);
     }
-    flags[0] = 0;
-    flags[1] = 0;
+    for (int s = 0; s < SH::QS; ++s) {
+      mbar_init(smem_addr(&qfull_bar[s]), 1);
+      mbar_init(smem_addr(&qempty_bar[s]), kConsumerWarps);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_addr(&mfull_bar[s]), kConsumerWarps);
+      mbar_init(smem_addr(&mempty_bar[s]), 1);
+    }
+    flags[kFlagAbort] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
 
@@ -310,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int v = __shfl_up_sync(0xffffffffu, incl, off);
       if (lane >= off) incl += v;
     }
-    int* wsum = flags + 2;
+    int* wsum = flags + kFlagWsum;
     if (lane == 31) wsum[warp] = incl;
     __syncthreads();
     int run = incl - sum;
@@ -328,15 +500,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (chunk < 1) chunk = 1;
   const long long nchunks = (total + chunk - 1) / chunk;
 
-  if (warp == kConsumerWarps) {
+  // Everything above reads only seq_lens. The pool, q and the table may still
+  // be written by the kernel launched just before this one on the stream
+  // (programmatic dependent launch): wait for it before touching them.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  if (warp == kProducerWarp) {
     // =========================== producer warp ===========================
-    uint32_t g = 0;  // ring sequence number
+    uint32_t g = 0;   // ring sequence number
+    uint32_t pc = 0;  // piece number
     for (long long c = blockIdx.x; c < nchunks; c += gridDim.x) {
       long long x = c * chunk;
       const long long xe = min(total, x + chunk);
       while (x < xe) {
         const Cursor cur = locate(x, pfx, S, Hkv);
         const int n = static_cast<int>(min(static_cast<long long>(cur.nb - cur.j), xe - x));
+        // q rows of the piece's G heads -> q slot
+        {
+          const int qs = pc % SH::QS;
+          const uint32_t quse = pc / SH::QS;
+          if (!__shfl_sync(0xffffffffu, *abort_flag, 0) &&
+              (quse == 0 || warp_wait_phase(smem_addr(&qempty_bar[qs]), (quse - 1) & 1,
+                                            abort_flag, p.err))) {
+            if (lane == 0) {
+              const uint32_t qb = smem_addr(&qfull_bar[qs]);
+              mbar_arrive_expect_tx(qb, G * D * 2);
+              bulk_copy_g2s(smem_addr(qring + qs * SH::QSLOT_BYTES),
+                            p.q + (static_cast<long long>(cur.seq) * p.num_q_heads +
+                                   cur.kvh * G) * D,
+                            G * D * 2, qb);
+            }
+            __syncwarp();
+          }
+        }
         const int32_t* trow = p.block_table + static_cast<long long>(cur.seq) * p.max_blocks;
         for (int j0 = 0; j0 < n; j0 += 32) {
           const int phys_lane = (j0 + lane < n) ? __ldg(trow + cur.j + j0 + lane) : 0;
@@ -369,9 +565,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         x += n;
+        ++pc;
       }
     }
-    // After an abort, wait (bounded) for copies still landing in the ring.
+    // After an abort, wait (bounded) for copies still landing in shared memory.
     if (*abort_flag) {
       const uint32_t first = g > static_cast<uint32_t>(SH::NST) ? g - SH::NST : 0;
       for (uint32_t gi = first; gi < g; ++gi) {
@@ -379,6 +576,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         const unsigned long long t0 = global_ns();
         while (!mbar_try_wait(bar, (gi / SH::NST) & 1) && global_ns() - t0 < kWaitLimitNs) {
         }
+      }
+      const uint32_t qfirst = pc > static_cast<uint32_t>(SH::QS) ? pc - SH::QS : 0;
+      for (uint32_t pi = qfirst; pi < pc; ++pi) {
+        const uint32_t bar = smem_addr(&qfull_bar[pi % SH::QS]);
+        const unsigned long long t0 = global_ns();
+        while (!mbar_try_wait(bar, (pi / SH::QS) & 1) && global_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+    return;
+  }
+
+  if (warp == kMergeWarp) {
+    // ============================ merge warp =============================
+    // zero outputs of empty sequences (this CTA's share)
+    for (int i = blockIdx.x; i < S; i += gridDim.x) {
+      if (pfx[i + 1] == pfx[i]) {
+        __half* o = p.out + static_cast<long long>(i) * p.num_q_heads * D;
+        for (int e = lane; e < p.num_q_heads * D; e += 32) o[e] = __float2half_rn(0.f);
+      }
+    }
+    uint32_t g = 0;   // block index in the CTA's stream
+    uint32_t pc = 0;  // piece number
+    for (long long c = blockIdx.x; c < nchunks; c += gridDim.x) {
+      long long x = c * chunk;
+      const long long xe = min(total, x + chunk);
+      bool first_piece = true;
+      while (x < xe) {
+        const Cursor cur = locate(x, pfx, S, Hkv);
+        const int n = static_cast<int>(min(static_cast<long long>(cur.nb - cur.j), xe - x));
+        const int msi = pc & 1;
+        if (warp_wait_phase(smem_addr(&mfull_bar[msi]), (pc >> 1) & 1, abort_flag, p.err)) {
+          const int parts = min(n, kConsumerWarps);
+          int who[kConsumerWarps];
+#pragma unroll
+          for (int k = 0; k < kConsumerWarps; ++k)
+            who[k] = static_cast<int>((g + k) % kConsumerWarps);
+          const bool cut = cur.j > 0 || cur.j + n < cur.nb;
+          const long long rec_i = 2 * c + (first_piece ? 0 : 1);
+          __half* out_row = p.out +
+              (static_cast<long long>(cur.seq) * p.num_q_heads + cur.kvh * G) * D;
+          merge_warps<D, G>(mslots + msi * SH::MSLOT_FLOATS, who, parts, out_row,
+                            p.records + rec_i * SH::REC_FLOATS, cut);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&mempty_bar[msi]));  // slot free again
+          if (cut) {
+            // chunks covering this segment: c_first .. c_last; the last to arrive merges
+            const long long s0 = cur.seg_start, s1 = cur.seg_start + cur.nb;
+            const long long c_first = s0 / chunk, c_last = (s1 - 1) / chunk;
+            const int expected = static_cast<int>(c_last - c_first + 1);
+            __threadfence();
+            __syncwarp();
+            int* cnt = p.counters + static_cast<long long>(cur.seq) * Hkv + cur.kvh;
+            int fin = 0;
+            if (lane == 0) fin = atomicAdd(cnt, 1) == expected - 1;
+            fin = __shfl_sync(0xffffffffu, fin, 0);
+            if (fin) {
+              __threadfence();
+              auto rec_of = [&](int i) -> long long {
+                const long long cc = c_first + i;
+                return 2 * cc + ((cc == c_first && s0 > cc * chunk) ? 1 : 0);
+              };
+              merge_records<D, G>(p.records, expected, rec_of, scratch, out_row);
+              if (lane == 0) atomicExch(cnt, 0);
+            }
+          }
+        }
+        g += n;
+        x += n;
+        ++pc;
+        first_piece = false;
       }
     }
     return;
@@ -388,15 +656,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int cw = warp;
   const int gid = lane >> 2;  // mma group id: row of A / column of B
   const int tig = lane & 3;   // thread in group
-  const int ct = tid;         // consumer thread 0..127
-
-  // zero outputs of empty sequences (this CTA's share)
-  for (int i = blockIdx.x; i < S; i += gridDim.x) {
-    if (pfx[i + 1] == pfx[i]) {
-      __half* o = p.out + static_cast<long long>(i) * p.num_q_heads * D;
-      for (int e = ct; e < p.num_q_heads * D; e += kConsumerWarps * 32) o[e] = __float2half_rn(0.f);
-    }
-  }
 
   // ldmatrix addressing inside a swizzled tile: lane supplies row (lane & 7)
   // of matrix (lane >> 3); logical 16-byte chunk c of row t sits at chunk
@@ -404,224 +663,188 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ld_row = lane & 7;
   const int ld_mat = lane >> 3;
 
-  uint32_t g = 0;    // ring sequence number of the next block
-  uint32_t kblk = 0;  // block index within the CTA's stream (round-robin owner)
+  uint32_t g = 0;   // ring sequence number of the next block (= block index in the CTA stream)
+  uint32_t pc = 0;  // piece number
   for (long long c = blockIdx.x; c < nchunks; c += gridDim.x) {
     long long x = c * chunk;
     const long long xe = min(total, x + chunk);
-    bool first_piece = true;
     while (x < xe) {
       const Cursor cur = locate(x, pfx, S, Hkv);
       const int n = static_cast<int>(min(static_cast<long long>(cur.nb - cur.j), xe - x));
-      const int L = min(max(__ldg(p.seq_lens + cur.seq), 0), cap);
-      const int head0 = cur.kvh * G;
+      // blocks of this piece go round-robin: block j to warp (g + j) % NC
+      const int first_j =
+          (cw - static_cast<int>(g % kConsumerWarps) + kConsumerWarps) % kConsumerWarps;
+      const bool mine = first_j < n;
 
-      // Q fragments (A operand, heads as rows): a0/a2 of each k-step; rows >= G are zero
-      uint32_t qa[SH::KSTEPS][2];
+      // ---- q of the piece: every warp observes the slot's phase, then frees it ----
+      uint32_t qa[SH::KSTEPS][2];  // A fragments a0/a2 per k-step; rows (heads) >= G are zero
       {
-        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-            p.q + (static_cast<long long>(cur.seq) * p.num_q_heads + head0 + gid) * D);
+        const int qs = pc % SH::QS;
+        const bool ok = warp_wait_phase(smem_addr(&qfull_bar[qs]), (pc / SH::QS) & 1, abort_flag,
+                                        p.err);
+        if (ok && mine) {
+          const uint32_t qrow = smem_addr(qring + qs * SH::QSLOT_BYTES) + ld_row * (D * 2);
 #pragma unroll
-        for (int kk = 0; kk < SH::KSTEPS; ++kk) {
-          qa[kk][0] = gid < G ? __ldg(qrow + kk * 8 + tig) : 0u;
-          qa[kk][1] = gid < G ? __ldg(qrow + kk * 8 + 4 + tig) : 0u;
+          for (int kk = 0; kk < SH::KSTEPS; kk += 2) {
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4(qrow + (2 * kk + ld_mat) * 16, r0, r1, r2, r3);
+            qa[kk][0] = gid < G ? r0 : 0u;
+            qa[kk][1] = gid < G ? r1 : 0u;
+            qa[kk + 1][0] = gid < G ? r2 : 0u;
+            qa[kk + 1][1] = gid < G ? r3 : 0u;
+          }
         }
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(smem_addr(&qempty_bar[qs]));
       }
+
       float m_run = -INFINITY, l_run = 0.f;  // head gid: running max (log2 units), partial sum
       float o[SH::MT][4];                     // O^T[d = mt*16 + gid (+8)][h = 2*tig (+1)]
 #pragma unroll
       for (int mt = 0; mt < SH::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+      if (mine) {
+        const int L = min(max(__ldg(p.seq_lens + cur.seq), 0), cap);
+        for (int jj = first_j; jj < n; jj += kConsumerWarps) {
+          const uint32_t gj = g + jj;
+          const int stage = gj % SH::NST;
+          if (!warp_wait_phase(smem_addr(&full_bar[stage]), (gj / SH::NST) & 1, abort_flag,
+                               p.err))
+            continue;
+          const int blk = cur.j + jj;
+          const int rows = min(BS, L - blk * BS);
+          unsigned char* kt = ring + stage * SH::STAGE_BYTES;
+          unsigned char* vt = kt + SH::TILE_BYTES;
+          if (rows < BS) {
+            // rows past the sequence end must add exactly zero to P V
+            const int words = (BS - rows) * 8;  // 16-byte words per half
+#pragma unroll
+            for (int h = 0; h < SH::NHALF; ++h) {
+              uint4* z = reinterpret_cast<uint4*>(vt + h * SH::HALF_BYTES + rows * 128);
+              for (int w = lane; w < words; w += 32) z[w] = make_uint4(0, 0, 0, 0);
+            }
+            __syncwarp();
+          }
+          const uint32_t kaddr = smem_addr(kt);
+          const uint32_t vaddr = smem_addr(vt);
 
-      for (int jj = 0; jj < n; ++jj) {
-        const uint32_t gj = g + jj;
-        if (((kblk + jj) % kConsumerWarps) != static_cast<uint32_t>(cw)) continue;
-        const int stage = gj % SH::NST;
-        if (!warp_wait_phase(smem_addr(&full_bar[stage]), (gj / SH::NST) & 1, abort_flag, p.err))
-          continue;
-        const int blk = cur.j + jj;
-        const int rows = min(BS, L - blk * BS);
-        unsigned char* kt = ring + stage * SH::STAGE_BYTES;
-        unsigned char* vt = kt + SH::TILE_BYTES;
-        if (rows < BS) {
-          // rows past the sequence end must add exactly zero to P V
-          const int words = (BS - rows) * 8;  // 16-byte words per half
+          // ---- S = Q K^T for each 8-token group ----
+          // x4 of k-steps (kk, kk+1): matrix m covers dims (2*kk + m) * 8 .. +8
+          float s[SH::NT][4];
 #pragma unroll
-          for (int h = 0; h < SH::NHALF; ++h) {
-            uint4* z = reinterpret_cast<uint4*>(vt + h * SH::HALF_BYTES + rows * 128);
-            for (int w = lane; w < words; w += 32) z[w] = make_uint4(0, 0, 0, 0);
+          for (int nt = 0; nt < SH::NT; ++nt) {
+            s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+            const uint32_t rowa = kaddr + (nt * 8 + ld_row) * 128;
+#pragma unroll
+            for (int kk = 0; kk < SH::KSTEPS; kk += 2) {
+              const int gc = 2 * kk + ld_mat;  // 16-byte chunk of the row, 0 .. D/8-1
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4(rowa + (gc >> 3) * SH::HALF_BYTES + (((gc & 7) ^ ld_row) << 4), b0, b1, b2,
+                      b3);
+              mma_16816(s[nt], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+              mma_16816(s[nt], qa[kk + 1][0], 0u, qa[kk + 1][1], 0u, b2, b3);
+            }
           }
-          __syncwarp();
-        }
-        const uint32_t kaddr = smem_addr(kt);
-        const uint32_t vaddr = smem_addr(vt);
-
-        // ---- S = Q K^T for each 8-token group ----
-        // x4 of k-steps (kk, kk+1): matrix m covers dims (2*kk + m) * 8 .. +8
-        float s[SH::NT][4];
+          // ---- online softmax over this block's tokens (row gid = head) ----
+          float mx = -INFINITY;
 #pragma unroll
-        for (int nt = 0; nt < SH::NT; ++nt) {
-          s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-          const uint32_t rowa = kaddr + (nt * 8 + ld_row) * 128;
+          for (int nt = 0; nt < SH::NT; ++nt) {
 #pragma unroll
-          for (int kk = 0; kk < SH::KSTEPS; kk += 2) {
-            const int gc = 2 * kk + ld_mat;  // 16-byte chunk of the row, 0 .. D/8-1
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(rowa + (gc >> 3) * SH::HALF_BYTES + (((gc & 7) ^ ld_row) << 4), b0, b1, b2, b3);
-            mma_16816(s[nt], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
-            mma_16816(s[nt], qa[kk + 1][0], 0u, qa[kk + 1][1], 0u, b2, b3);
+            for (int e = 0; e < 2; ++e) {
+              const int t = nt * 8 + 2 * tig + e;
+              const float v = t < rows ? s[nt][e] * p.qscale : -INFINITY;
+              s[nt][e] = v;
+              mx = fmaxf(mx, v);
+            }
           }
-        }
-        // ---- online softmax over this block's tokens (row gid = head) ----
-        float mx = -INFINITY;
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          const float m_new = fmaxf(m_run, mx);
+          const float mu = m_new == -INFINITY ? 0.f : m_new;
+          const float alpha = fast_exp2(m_run - mu);
+          m_run = m_new;
+          float ps = 0.f;
+          uint32_t pb[SH::NT];  // P as fp16 pairs: B operand of the PV mma
 #pragma unroll
-        for (int nt = 0; nt < SH::NT; ++nt) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int t = nt * 8 + 2 * tig + e;
-            const float v = t < rows ? s[nt][e] * p.qscale : -INFINITY;
-            s[nt][e] = v;
-            mx = fmaxf(mx, v);
+          for (int nt = 0; nt < SH::NT; ++nt) {
+            const float p0 = fast_exp2(s[nt][0] - mu);
+            const float p1 = fast_exp2(s[nt][1] - mu);
+            ps += p0 + p1;
+            pb[nt] = pack_half2(p0, p1);
           }
-        }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run, mx);
-        const float mu = m_new == -INFINITY ? 0.f : m_new;
-        const float alpha = fast_exp2(m_run - mu);
-        m_run = m_new;
-        float ps = 0.f;
-        uint32_t pb[SH::NT];  // P as fp16 pairs: B operand of the PV mma
-#pragma unroll
-        for (int nt = 0; nt < SH::NT; ++nt) {
-          const float p0 = fast_exp2(s[nt][0] - mu);
-          const float p1 = fast_exp2(s[nt][1] - mu);
-          ps += p0 + p1;
-          pb[nt] = pack_half2(p0, p1);
-        }
-        l_run = l_run * alpha + ps;
-        // rescale O^T columns: heads 2*tig and 2*tig+1 live in mma groups 2*tig, 2*tig+1
-        const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * tig);
-        const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);
-#pragma unroll
-        for (int mt = 0; mt < SH::MT; ++mt) {
-          o[mt][0] *= a_lo;
-          o[mt][1] *= a_hi;
-          o[mt][2] *= a_lo;
-          o[mt][3] *= a_hi;
-        }
-        // ---- O^T += V^T P^T over 16-token k-steps ----
-        // x4.trans of m-tile mt: matrix m covers tokens +8*(m>>1), dims mt*16 + 8*(m&1)
-#pragma unroll
-        for (int pk = 0; pk < SH::PK; ++pk) {
-          const uint32_t pb0 = pb[2 * pk];
-          const uint32_t pb1 = (2 * pk + 1 < SH::NT) ? pb[2 * pk + 1] : 0u;
-          const uint32_t rowa = vaddr + (pk * 16 + ld_row + (ld_mat >> 1) * 8) * 128;
+          l_run = l_run * alpha + ps;
+          // rescale O^T columns: heads 2*tig and 2*tig+1 live in mma groups 2*tig, 2*tig+1
+          const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * tig);
+          const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);
 #pragma unroll
           for (int mt = 0; mt < SH::MT; ++mt) {
-            const int gc = 2 * mt + (ld_mat & 1);
-            const uint32_t addr = rowa + (gc >> 3) * SH::HALF_BYTES + (((gc & 7) ^ ld_row) << 4);
-            uint32_t a0, a1, a2, a3;
-            if (2 * pk + 1 < SH::NT) {
-              ldsm_x4_t(addr, a0, a1, a2, a3);
-            } else {
-              ldsm_x2_t(addr, a0, a1);
-              a2 = a3 = 0u;
-            }
-            mma_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+            o[mt][0] *= a_lo;
+            o[mt][1] *= a_hi;
+            o[mt][2] *= a_lo;
+            o[mt][3] *= a_hi;
           }
+          // ---- O^T += V^T P^T over 16-token k-steps ----
+          // x4.trans of m-tile mt: matrix m covers tokens +8*(m>>1), dims mt*16 + 8*(m&1)
+#pragma unroll
+          for (int pk = 0; pk < SH::PK; ++pk) {
+            const uint32_t pb0 = pb[2 * pk];
+            const uint32_t pb1 = (2 * pk + 1 < SH::NT) ? pb[2 * pk + 1] : 0u;
+            const uint32_t rowa = vaddr + (pk * 16 + ld_row + (ld_mat >> 1) * 8) * 128;
+#pragma unroll
+            for (int mt = 0; mt < SH::MT; ++mt) {
+              const int gc = 2 * mt + (ld_mat & 1);
+              const uint32_t addr = rowa + (gc >> 3) * SH::HALF_BYTES + (((gc & 7) ^ ld_row) << 4);
+              uint32_t a0, a1, a2, a3;
+              if (2 * pk + 1 < SH::NT) {
+                ldsm_x4_t(addr, a0, a1, a2, a3);
+              } else {
+                ldsm_x2_t(addr, a0, a1);
+                a2 = a3 = 0u;
+              }
+              mma_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+            }
+          }
+          if (rows < BS) fence_proxy_async_smem();  // generic zero-fill before the next TMA write
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&empty_bar[stage]));
         }
-        if (rows < BS) fence_proxy_async_smem();  // generic zero-fill before the next bulk copy
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&empty_bar[stage]));
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
       }
 
-      // ---- piece finished: merge the four warps ----
-      l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-      l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+      // ---- publish this warp's state for the merge warp; never wait for it ----
+      // Every consumer warp passes every slot phase in order (the merge
+      // barrier counts all four), so no wait can alias an older phase.
+      const int msi = pc & 1;
+      const bool slot_ok =
+          pc < 2 || warp_wait_phase(smem_addr(&mempty_bar[msi]), ((pc - 2) >> 1) & 1, abort_flag,
+                                    p.err);
+      if (slot_ok) {
+        if (mine) {
+          float* ms = mslots + msi * SH::MSLOT_FLOATS;
 #pragma unroll
-      for (int mt = 0; mt < SH::MT; ++mt) {
-        const int d = mt * 16 + gid;
-        const int h0 = 2 * tig, h1 = 2 * tig + 1;
-        if (h0 < G) {
-          m_acc[(cw * G + h0) * D + d] = o[mt][0];
-          m_acc[(cw * G + h0) * D + d + 8] = o[mt][2];
-        }
-        if (h1 < G) {
-          m_acc[(cw * G + h1) * D + d] = o[mt][1];
-          m_acc[(cw * G + h1) * D + d + 8] = o[mt][3];
-        }
-      }
-      if (tig == 0 && gid < G) {
-        m_ml[(cw * G + gid) * 2] = m_run;
-        m_ml[(cw * G + gid) * 2 + 1] = l_run;
-      }
-      consumer_sync();
-      const bool cut = cur.j > 0 || cur.j + n < cur.nb;
-      const long long rec = 2 * c + (first_piece ? 0 : 1);
-      float* recp = p.records + rec * (G * (D + 2));
-      for (int idx = ct; idx < G * D; idx += kConsumerWarps * 32) {
-        const int gg = idx / D, d = idx % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, m_ml[(w * G + gg) * 2]);
-        const float mu = M == -INFINITY ? 0.f : M;
-        float Ls = 0.f, A = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          const float wgt = fast_exp2(m_ml[(w * G + gg) * 2] - mu);
-          Ls += m_ml[(w * G + gg) * 2 + 1] * wgt;
-          A += m_acc[(w * G + gg) * D + d] * wgt;
-        }
-        if (!cut) {
-          p.out[(static_cast<long long>(cur.seq) * p.num_q_heads + head0 + gg) * D + d] =
-              __float2half_rn(Ls > 0.f ? A / Ls : 0.f);
-        } else {
-          recp[idx] = A;
-          if (d == 0) {
-            recp[G * D + 2 * gg] = M;
-            recp[G * D + 2 * gg + 1] = Ls;
+          for (int mt = 0; mt < SH::MT; ++mt) {
+            const int d = mt * 16 + gid;
+            const int h0 = 2 * tig, h1 = 2 * tig + 1;
+            if (h0 < G) {
+              ms[(cw * G + h0) * (D + 2) + d] = o[mt][0];
+              ms[(cw * G + h0) * (D + 2) + d + 8] = o[mt][2];
+            }
+            if (h1 < G) {
+              ms[(cw * G + h1) * (D + 2) + d] = o[mt][1];
+              ms[(cw * G + h1) * (D + 2) + d + 8] = o[mt][3];
+            }
+          }
+          if (tig == 0 && gid < G) {
+            ms[(cw * G + gid) * (D + 2) + D] = m_run;
+            ms[(cw * G + gid) * (D + 2) + D + 1] = l_run;
           }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&mfull_bar[msi]));
       }
-      if (cut) {
-        // chunks covering this segment: c_first .. c_last; the last to arrive merges
-        const long long s0 = cur.seg_start, s1 = cur.seg_start + cur.nb;
-        const long long c_first = s0 / chunk, c_last = (s1 - 1) / chunk;
-        const int expected = static_cast<int>(c_last - c_first + 1);
-        __threadfence();
-        consumer_sync();
-        int* cnt = p.counters + static_cast<long long>(cur.seq) * Hkv + cur.kvh;
-        if (ct == 0) flags[1] = (atomicAdd(cnt, 1) == expected - 1) ? 1 : 0;
-        consumer_sync();
-        if (flags[1]) {
-          __threadfence();
-          for (int idx = ct; idx < G * D; idx += kConsumerWarps * 32) {
-            const int gg = idx / D, d = idx % D;
-            float M = -INFINITY;
-            for (long long cc = c_first; cc <= c_last; ++cc) {
-              const long long r = 2 * cc + ((cc == c_first && s0 > cc * chunk) ? 1 : 0);
-              M = fmaxf(M, __ldcg(p.records + r * (G * (D + 2)) + G * D + 2 * gg));
-            }
-            const float mu = M == -INFINITY ? 0.f : M;
-            float Ls = 0.f, A = 0.f;
-            for (long long cc = c_first; cc <= c_last; ++cc) {
-              const long long r = 2 * cc + ((cc == c_first && s0 > cc * chunk) ? 1 : 0);
-              const float* rp = p.records + r * (G * (D + 2));
-              const float wgt = fast_exp2(__ldcg(rp + G * D + 2 * gg) - mu);
-              Ls += __ldcg(rp + G * D + 2 * gg + 1) * wgt;
-              A += __ldcg(rp + idx) * wgt;
-            }
-            p.out[(static_cast<long long>(cur.seq) * p.num_q_heads + head0 + gg) * D + d] =
-                __float2half_rn(Ls > 0.f ? A / Ls : 0.f);
-          }
-          if (ct == 0) atomicExch(cnt, 0);
-        }
-      }
-      consumer_sync();  // merge buffers and flags[1] are reused by the next piece
       g += n;
-      kblk += n;
       x += n;
-      first_piece = false;
+      ++pc;
     }
   }
 }
@@ -652,7 +875,7 @@ Layout workspace_layout(int S, int Hq, int Hkv, int D, int MB, int cap_blocks) {
   w.max_records = 2 * max_chunks(S, Hkv, MB, cap_blocks);
   w.counters = 0;
   w.records = round256(static_cast<size_t>(S) * Hkv * 4);
-  w.total = w.records + round256(static_cast<size_t>(w.max_records) * G * (D + 2) * 4);
+  w.total = w.records + round256(static_cast<size_t>(w.max_records) * rec_floats(G, D) * 4);
   return w;
 }
 
@@ -759,8 +982,21 @@ pa_status launch_decode(const DecodeParams& prm, const pa::DeviceInfo& dev, cuda
   if (pa_status s = pool_tensor_map(vk, &vmap)) return s;
   long long grid = static_cast<long long>(dev.sm_count) * occ;
   if (grid > kMaxGrid) grid = kMaxGrid;
-  kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(prm, kmap, vmap);
-  cudaError_t e = cudaGetLastError();
+  // Programmatic dependent launch: the prologue may overlap the tail of the
+  // previous kernel on the stream; the kernel waits for it (griddepcontrol)
+  // before reading the pool, q or the table.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm, kmap, vmap);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_decode_attention launch");
   return PA_OK;
 }
