@@ -193,6 +193,40 @@ PA_API pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool,
                               int partition_tokens, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * pa_decode_attention_fixed_scratch — pa_decode_attention without a
+ * caller-provided workspace; it allocates nothing.
+ *
+ * The pages have no counterpart for this call: it exists for callers that
+ * cannot give the library scratch memory, for instance a serving process that
+ * hands all of its device memory to its own KV pool and allocator up front,
+ * or one that must not call cudaMalloc on the decode path because that call
+ * synchronises the device. The scratch it needs (arrival counters and the
+ * partial results of split sequences) lives in a fixed 4 MiB device array
+ * inside libpa, which every GPU that loads the library keeps until the
+ * process exits.
+ *
+ * Arguments, layouts and results are those of pa_decode_attention (same
+ * kernel); only workspace and workspace_bytes are gone.
+ * - The first call on a device resolves the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture.
+ * - Every call uses the same array and clears its counters on `stream` before
+ *   the kernel runs; calls that overlap on the GPU (other streams, other host
+ *   threads) race on it and must not be issued.
+ * - Shapes whose scratch would exceed 4 MiB (about 2 x SMs x 2 partial results
+ *   of G x (head_dim + 2) floats, plus 4 bytes per (sequence, KV head)) are
+ *   refused with PA_ERR_UNSUPPORTED; use pa_decode_attention for them.
+ * - No cudaMalloc, cudaFree or allocating library routine is called.
+ * Errors: as pa_decode_attention, plus PA_ERR_UNSUPPORTED for the size limit.
+ * ---------------------------------------------------------------------- */
+PA_API pa_status pa_decode_attention_fixed_scratch(
+    const pa_half* q, const pa_half* k_pool, const pa_half* v_pool,
+    const int32_t* block_table, const int32_t* seq_lens, int num_seqs,
+    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+    int max_blocks_per_seq, int num_blocks, float scale, pa_half* out,
+    int partition_tokens, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Host block allocator (block manager). Host memory only; no CUDA calls.
  *
  * Source: "Phase 7 · Document 04 — PagedAttention", §2 (a pool of physical

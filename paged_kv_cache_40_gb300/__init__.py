@@ -34,6 +34,7 @@ from ._lib import (  # noqa: F401
 __all__ = [
     "pa_append_kv", "pa_copy_blocks", "pa_decode_attention",
     "pa_decode_workspace_bytes", "pa_decode_workspace_init", "pa_device_error",
+    "pa_decode_attention_fixed_scratch",
     "pa_version", "BlockAllocator", "PaError", "OutOfBlocksError", "lib",
     "DEFAULT_PARTITION_TOKENS",
 ]
@@ -166,6 +167,39 @@ def pa_decode_attention(q, k_pool, v_pool, block_table, seq_lens, scale, out=Non
         *args, S, hq, hkv, d, bs, mb, nb, ctypes.c_float(float(scale)),
         _dev(out, "out", torch.float16), _dev(workspace, "workspace", torch.uint8),
         workspace.numel(), partition_tokens, _stream_ptr(stream)))
+    return out
+
+
+def pa_decode_attention_fixed_scratch(q, k_pool, v_pool, block_table, seq_lens, scale,
+                                      out=None, partition_tokens: int = 0, stream=None):
+    """pa_decode_attention for callers that cannot provide a workspace.
+
+    For a process that cannot allocate device memory on the decode path (all
+    of it already belongs to its own KV pool and allocator, or cudaMalloc's
+    device synchronisation is not acceptable there): the scratch is a fixed
+    4 MiB array inside libpa. Same inputs and result as pa_decode_attention;
+    shapes needing more scratch raise PaError (PA_ERR_UNSUPPORTED). Calls that
+    overlap on the GPU share that array and must not be issued.
+    """
+    torch = _torch()
+    nb, bs, hkv, d = _pool_dims(k_pool, v_pool)
+    if q.dim() != 3 or int(q.shape[2]) != d:
+        raise ValueError("q must be [num_seqs][num_q_heads][head_dim]")
+    S, hq = int(q.shape[0]), int(q.shape[1])
+    if block_table.dim() != 2 or int(block_table.shape[0]) != S:
+        raise ValueError("block_table must be [num_seqs][max_blocks_per_seq]")
+    if tuple(seq_lens.shape) != (S,):
+        raise ValueError("seq_lens must be [num_seqs]")
+    if out is None:
+        out = torch.empty_like(q)
+    elif tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must have q's shape")
+    args = (_dev(q, "q", torch.float16), _dev(k_pool, "k_pool", torch.float16),
+            _dev(v_pool, "v_pool", torch.float16), _dev(block_table, "block_table", torch.int32),
+            _dev(seq_lens, "seq_lens", torch.int32))
+    _check(_load().pa_decode_attention_fixed_scratch(
+        *args, S, hq, hkv, d, bs, int(block_table.shape[1]), nb, ctypes.c_float(float(scale)),
+        _dev(out, "out", torch.float16), partition_tokens, _stream_ptr(stream)))
     return out
 
 

@@ -64,6 +64,8 @@ SIGNATURES = {
     "pa_decode_workspace_init": (_i32, [_vp, _sz, _i32, _i32, _vp]),
     "pa_decode_attention": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                    _i32, _i32, _f32, _vp, _vp, _sz, _i32, _vp]),
+    "pa_decode_attention_fixed_scratch": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                                                 _i32, _i32, _i32, _f32, _vp, _i32, _vp]),
     "pa_alloc_create": (_i32, [_i32, _i32, _pi32, ctypes.POINTER(_vp)]),
     "pa_alloc_destroy": (None, [_vp]),
     "pa_alloc_add_seq": (_i32, [_vp, _i64, _i64]),

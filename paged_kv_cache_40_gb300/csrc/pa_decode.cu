@@ -1045,6 +1045,69 @@ pa_status check_decode_shape(int S, int Hq, int Hkv, int D, int BS, int MB, int 
   return PA_OK;
 }
 
+
+// --- fixed scratch for the entry point that allocates nothing ----------------
+// Some callers cannot hand this library a workspace: every byte of device
+// memory they own is already given to their KV pool and their own allocator,
+// and calling cudaMalloc on the decode path (which also synchronises the
+// device) is not an option for them. For those callers the scratch lives in a
+// file-scope device array of fixed size instead. Every GPU that loads libpa
+// holds these 4 MiB until the process exits.
+constexpr size_t kFixedScratchBytes = size_t(4) << 20;
+static __device__ __align__(256) unsigned char g_pa_fixed_scratch[kFixedScratchBytes];
+
+// Device address of the fixed scratch on the current device, resolved once
+// per device (the host-side symbol is only a stand-in, never a device
+// address). Returns nullptr with a recorded message on failure.
+unsigned char* fixed_scratch_address(int device) {
+  static std::mutex mu;
+  static unsigned char* addr[64] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[device]) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_pa_fixed_scratch);
+    if (e != cudaSuccess) {
+      pa::cuda_fail(e, "cudaGetSymbolAddress(fixed decode scratch)");
+      return nullptr;
+    }
+    addr[device] = static_cast<unsigned char*>(ptr);
+  }
+  return addr[device];
+}
+
+// Grid the decode kernel of this shape gets on `dev` (same rule as the launch).
+template <int D, int BS, int G>
+pa_status decode_grid(const pa::DeviceInfo& dev, int S, long long* grid) {
+  using SH = Shape<D, BS, G>;
+  auto kernel = paged_decode_kernel<D, BS, G>;
+  const size_t smem = SH::smem_bytes(S);
+  if (smem > dev.smem_optin)
+    return pa::fail(PA_ERR_UNSUPPORTED, "pa_decode_attention: %zu bytes of shared memory needed",
+                    smem);
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(dev.smem_optin));
+  if (e != cudaSuccess) return pa::cuda_fail(e, "cudaFuncSetAttribute");
+  int occ = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, smem);
+  if (e != cudaSuccess) return pa::cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  long long g = static_cast<long long>(dev.sm_count) * occ;
+  *grid = g > kMaxGrid ? kMaxGrid : g;
+  return PA_OK;
+}
+
+pa_status decode_grid_any(int D, int BS, int G, const pa::DeviceInfo& dev, int S,
+                          long long* grid) {
+#define PA_GRID_CASE(d, bs, g) \
+  if (D == d && BS == bs && G == g) return decode_grid<d, bs, g>(dev, S, grid);
+#define PA_GRID_G(d, bs) PA_GRID_CASE(d, bs, 1) PA_GRID_CASE(d, bs, 2) PA_GRID_CASE(d, bs, 4) \
+  PA_GRID_CASE(d, bs, 8)
+  PA_GRID_G(64, 8) PA_GRID_G(64, 16) PA_GRID_G(64, 32)
+  PA_GRID_G(128, 8) PA_GRID_G(128, 16) PA_GRID_G(128, 32)
+#undef PA_GRID_G
+#undef PA_GRID_CASE
+  return pa::fail(PA_ERR_UNSUPPORTED, "pa_decode_attention: unsupported shape");
+}
+
 }  // namespace
 
 extern "C" {
@@ -1122,6 +1185,79 @@ pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool, const pa_
   prm.qscale = scale * kLog2e;
   const int G = num_q_heads / num_kv_heads;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  pa_status st = head_dim == 64 ? dispatch_bs<64>(block_size, G, prm, dev, s)
+                                : dispatch_bs<128>(block_size, G, prm, dev, s);
+  return st == PA_OK ? pa::ok() : st;
+}
+
+
+pa_status pa_decode_attention_fixed_scratch(const pa_half* q, const pa_half* k_pool,
+                                            const pa_half* v_pool, const int32_t* block_table,
+                                            const int32_t* seq_lens, int num_seqs,
+                                            int num_q_heads, int num_kv_heads, int head_dim,
+                                            int block_size, int max_blocks_per_seq,
+                                            int num_blocks, float scale, pa_half* out,
+                                            int partition_tokens, pa_stream_t stream) {
+  if (pa_status s = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                       max_blocks_per_seq, partition_tokens))
+    return s;
+  if (num_blocks <= 0 || static_cast<long long>(num_blocks) * block_size > INT32_MAX)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention_fixed_scratch: num_blocks %d",
+                    num_blocks);
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention_fixed_scratch: scale is not finite");
+  if (num_seqs == 0) return pa::ok();
+  if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !out)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention_fixed_scratch: NULL pointer");
+  if (!pa::aligned16(q) || !pa::aligned16(k_pool) || !pa::aligned16(v_pool) ||
+      !pa::aligned16(out) || (reinterpret_cast<uintptr_t>(block_table) & 3) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3))
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention_fixed_scratch: misaligned pointer");
+  pa::DeviceInfo dev;
+  if (pa_status s = pa::current_device(&dev)) return s;
+  const int G = num_q_heads / num_kv_heads;
+  long long grid = 0;
+  if (pa_status s = decode_grid_any(head_dim, block_size, G, dev, num_seqs, &grid)) return s;
+  // scratch this call needs: arrival counters, then two partial records per chunk
+  const int cap_blocks = partition_tokens / block_size;
+  long long chunks = grid;
+  if (cap_blocks > 0) {
+    const long long blocks = static_cast<long long>(num_seqs) * num_kv_heads * max_blocks_per_seq;
+    const long long capped = (blocks + cap_blocks - 1) / cap_blocks;
+    if (capped > chunks) chunks = capped;
+  }
+  const size_t counters = round256(static_cast<size_t>(num_seqs) * num_kv_heads * 4);
+  const size_t need =
+      counters + static_cast<size_t>(2 * chunks) * rec_floats(G, head_dim) * sizeof(float);
+  if (need > kFixedScratchBytes)
+    return pa::fail(PA_ERR_UNSUPPORTED,
+                    "pa_decode_attention_fixed_scratch: this shape needs %zu bytes of scratch; "
+                    "the fixed scratch holds %zu (use pa_decode_attention with a workspace)",
+                    need, kFixedScratchBytes);
+  unsigned char* ws = fixed_scratch_address(dev.device);
+  if (!ws) return PA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the scratch keeps the previous call's contents: the counters must start at zero
+  cudaError_t e = cudaMemsetAsync(ws, 0, static_cast<size_t>(num_seqs) * num_kv_heads * 4, s);
+  if (e != cudaSuccess) return pa::cuda_fail(e, "pa_decode_attention_fixed_scratch memset");
+  DecodeParams prm;
+  prm.q = reinterpret_cast<const __half*>(q);
+  prm.k_pool = reinterpret_cast<const __half*>(k_pool);
+  prm.v_pool = reinterpret_cast<const __half*>(v_pool);
+  prm.block_table = block_table;
+  prm.seq_lens = seq_lens;
+  prm.out = reinterpret_cast<__half*>(out);
+  prm.counters = reinterpret_cast<int32_t*>(ws);
+  prm.records = reinterpret_cast<float*>(ws + counters);
+  prm.err = pa::device_error_word();
+  if (!prm.err) return PA_ERR_CUDA;
+  prm.num_seqs = num_seqs;
+  prm.num_q_heads = num_q_heads;
+  prm.num_kv_heads = num_kv_heads;
+  prm.max_blocks = max_blocks_per_seq;
+  prm.num_blocks = num_blocks;
+  prm.cap_blocks = cap_blocks;
+  prm.qscale = scale * kLog2e;
   pa_status st = head_dim == 64 ? dispatch_bs<64>(block_size, G, prm, dev, s)
                                 : dispatch_bs<128>(block_size, G, prm, dev, s);
   return st == PA_OK ? pa::ok() : st;
