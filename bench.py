@@ -12,8 +12,9 @@ Default workload: 64 sequences with lengths U[128,2048] (+1 appended token),
 with shuffled physical ids, fp16 K/V/q drawn N(0,1) from a fixed seed.
 
 value      KV GB/s: bytes of the K and V rows attended per step / device step
-           time (CUDA events on the launching stream; L2 flushed by a 512 MB
-           write between steps, outside the events)
+           time (CUDA events on the launching stream; between steps, outside
+           the events, L2 is flushed by writing one 512 MB buffer and reading
+           another, so no input and no dirty line is left in it)
 e2e        the same metric through the public API with pinned host buffers:
            every step uploads q, new K/V, slot mapping, block table and
            lengths and downloads the output inside the timed region
@@ -73,7 +74,7 @@ def describe(b) -> dict:
         "block_size": b.block_size,
         "num_blocks": int(b.num_blocks),
         "kv_storage": "fp16",
-        "l2": "flushed between steps (512 MB write outside the timed events)",
+        "l2": "flushed between steps outside the timed events (512 MB write, then 512 MB read of another buffer)",
     }
 
 
@@ -294,11 +295,17 @@ def run_ours(args, world, rank, local):
     t_host = (time.perf_counter() - t_host0) * 1e6
     a.close()
     stream = torch.cuda.current_stream(dev)
-    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    # L2 flush between steps: write one buffer larger than L2, then read a
+    # second one, so the timed step starts with L2 holding neither its inputs
+    # nor dirty lines whose write-back it would pay for.
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
     launches_per_step = (1 if len(plan.cow_pairs) else 0) + 2
 
     def flush():
-        flush_buf.fill_(1)
+        flush_w.fill_(1)
+        torch.sum(flush_r, out=flush_sink)
 
     for _ in range(args.warmup):
         flush()

@@ -8,40 +8,41 @@
 // block_table[i][t / BS], row t % BS, KV head h / G.
 //
 // How (GB300-first; the pages give no kernel, only the layout sketch):
-//   * Segments and balanced chunks. A segment is (sequence, KV head): the
-//     ceil(L/BS) blocks of one KV head of one sequence. All segments are laid
-//     end to end (sequence-major, KV head minor) into one stream of blocks,
-//     and the stream is cut into equal contiguous chunks, one per CTA of a
-//     persistent grid (SMs x resident CTAs). Every CTA therefore streams the
-//     same number of blocks. A segment that lies inside one chunk is finished
-//     there; a segment cut by chunk boundaries leaves a partial result per
-//     chunk, and the last chunk to finish it (an atomic arrival counter, never
-//     a spin) merges the partials with the log-sum-exp rule. A chunk has at
-//     most two cut segments (its first and its last).
-//   * All G query heads of a KV head are served together, so every K/V byte
-//     is read from HBM once per step (GQA head-group reuse).
-//   * Warp specialisation. A producer warp walks the CTA's chunk, loads block
-//     table entries 32 at a time with one coalesced load, and moves each
-//     (block, KV head) K tile and V tile into a ring of shared-memory stages
-//     with TMA: a 3-D tensor map over the pool seen as [NB*BS][Hkv][D], one
-//     tiled copy per 64-dimension half (box {64, 1, BS}), completion counted on
-//     an mbarrier. The tiles land with the 128-byte swizzle, so the
-//     tensor-core fragment loads (ldmatrix) are free of bank conflicts. (One
-//     copy per 256-byte row would leave the copy engine, not HBM, as the
-//     limit.) Four consumer warps take the stages round-robin.
+//   * Head groups. A CTA streams HG KV heads of a block together (HG = the
+//     largest of 8, 4, 2, 1 dividing the KV head count). For the common 8-KV-
+//     head models that is the whole block: one contiguous 32 KB region of K
+//     and one of V per 16-token block, moved by four 16 KB TMA copies, which
+//     keeps DRAM pages and the copy engine efficient. One consumer warp owns
+//     one KV head of the group and all G query heads that read it (GQA
+//     head-group reuse: every K/V byte is read from HBM once per step).
+//   * Segments and balanced chunks. A segment is (sequence, head group): the
+//     ceil(L/BS) blocks of that group. Segments are laid end to end (sequence-
+//     major) into one stream of blocks, and the stream is cut into equal
+//     contiguous chunks, one per CTA of a persistent grid (SMs x resident
+//     CTAs): every CTA streams the same number of blocks. A segment inside one
+//     chunk is finished there and each warp writes its head's output straight
+//     from registers. A segment cut by chunk boundaries leaves one partial
+//     result per (chunk, head); the last warp to finish a head (an atomic
+//     arrival counter with acquire-release order, never a spin) merges that
+//     head's partials with the log-sum-exp rule. A chunk has at most two cut
+//     segments (its first and its last).
+//   * Warp specialisation. A producer warp walks the CTA's chunk, loads the
+//     block-table entries of the next 32 blocks while it issues the current
+//     ones, and moves K and V with TMA into a ring of shared-memory stages:
+//     a 4-D tensor map over the pool seen as (dim, token, KV head, block) —
+//     token stride larger than head stride — with box {64, tokens, HG, 1} and
+//     the 128-byte swizzle, so each head's rows land contiguously and the
+//     tensor-core fragment loads (ldmatrix) are free of bank conflicts. Every
+//     consumer warp reads every stage (its own head), so a stage is released
+//     after HG arrivals. q of each piece comes through a q slot the same way.
 //   * Consumer math on tensor cores (mma.sync m16n8k16, fp16 in, fp32
 //     accumulate). Scores S = Q K^T with the G query heads as the M rows and
 //     8-token groups as N; the online softmax (base 2, running max and sum)
 //     works on the accumulator registers; then O^T += V^T P^T with head_dim as
 //     M and the heads as N, whose B operand is exactly the probabilities the
 //     score accumulators already hold (no transpose, no shared-memory trip).
-//     Rows of a partial last block are masked out of the softmax and zeroed in
+//     Rows past the sequence end are masked out of the softmax and zeroed in
 //     the V stage so they contribute exactly nothing.
-//   * q of a piece is copied by the producer into a small ring of q slots;
-//     consumers read their A fragments from shared memory. At the end of a
-//     piece each consumer warp publishes its state into a merge slot (two,
-//     alternating) and the last warp to arrive merges, so no warp ever waits
-//     for the others and the ring keeps draining.
 //   * Programmatic dependent launch: the prologue (prefix sum of lengths) can
 //     overlap the previous kernel on the stream; K/V, q and table reads wait
 //     for it with griddepcontrol.wait.
@@ -58,13 +59,13 @@
 
 namespace {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kProducerWarp = kConsumerWarps;      // warp index of the producer
-constexpr int kMergeWarp = kConsumerWarps + 1;     // warp index of the merger
-constexpr int kThreads = (kConsumerWarps + 2) * 32;
+constexpr int kMaxHG = 8;                          // KV heads per group = consumer warps
+constexpr int kMaxThreads = (kMaxHG + 1) * 32;     // consumers + producer
 constexpr int kMaxSeqs = 16384;
-constexpr int kMaxGrid = 2048;
-constexpr int kRingBytes = 64 * 1024;
+constexpr int kMaxGrid = 1024;
+constexpr int kMaxStages = 16;
+constexpr int kRingBytesPerHead = 24 * 1024;       // ring size per KV head of the group
+constexpr int kMergeBatch = 16;                    // partial records folded per batch
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -107,15 +108,14 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
-// TMA tiled copy of box {x, y, z} of a 3-D tensor map into this CTA's shared
-// memory, completion counted on `bar`.
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            int z, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
-      : "memory");
+// Atomic add with acquire-release semantics at GPU scope: this thread's earlier
+// global writes are visible to whoever later observes the new count, and
+// writes released by earlier adders are visible to this thread afterwards.
+__device__ __forceinline__ int atomic_add_acq_rel(int* ptr, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v)
+               : "memory");
+  return old;
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -185,63 +185,49 @@ __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity,
   }
 }
 
+
 // ------------------------------------------------------------- shapes ---
 // A partial record holds acc [G][D] then (max, sum) per head, padded to a
 // multiple of 4 floats so every record starts on a 16-byte boundary.
 __host__ __device__ constexpr int rec_floats(int G, int D) { return (G * (D + 2) + 3) / 4 * 4; }
 
+// KV heads a CTA streams together: the largest of 8, 4, 2, 1 dividing Hkv.
+__host__ __device__ constexpr int head_group(int hkv) {
+  return hkv % 8 == 0 ? 8 : hkv % 4 == 0 ? 4 : hkv % 2 == 0 ? 2 : 1;
+}
+
 template <int D, int BS, int G>
 struct Shape {
   static_assert(G >= 1 && G <= 8, "at most 8 query heads per KV head (mma N = 8)");
-  static_assert(D % 16 == 0 && BS % 8 == 0, "shape");
-  static constexpr int NHALF = D / 64;                   // 64-dim (128-byte) halves per row
-  static constexpr int HALF_BYTES = BS * 128;            // one half of a tile, swizzled
-  static constexpr int TILE_BYTES = NHALF * HALF_BYTES;  // K (or V) of one block, one head
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;     // K tile then V tile
-  static_assert(D % 64 == 0 && HALF_BYTES % 1024 == 0, "swizzle atoms need 1 KB halves");
-  // Ring depth is a multiple of the consumer-warp count, so consecutive uses
-  // of a stage belong to the same consumer warp. A parity wait can only tell
-  // the current phase from the one before it; with this invariant a consumer
-  // never waits on a stage whose previous use is still in flight, which would
-  // otherwise read as "complete".
-  static constexpr int NST_RAW = kRingBytes / STAGE_BYTES;
-  static constexpr int NST = NST_RAW >= 2 * kConsumerWarps
-                                 ? NST_RAW / kConsumerWarps * kConsumerWarps
-                                 : kConsumerWarps;
-  static_assert(NST % kConsumerWarps == 0, "ring depth must be a multiple of consumer warps");
-  static constexpr int KSTEPS = D / 16;    // QK k-steps over head_dim
-  static constexpr int MT = D / 16;        // PV m-tiles over head_dim
-  static constexpr int NT = BS / 8;        // 8-token groups per block
-  static constexpr int PK = (NT + 1) / 2;  // PV k-steps (16 tokens each) per block
-  // q ring: one slot per piece (segment piece), 8 rows of D halves
-  static constexpr int QS = 4;
-  static constexpr int QSLOT_BYTES = 8 * D * 2;
-  // merge slots (double-buffered by piece parity): per warp O [G][D] + (m, l) [G]
-  static constexpr int MSLOT_FLOATS = kConsumerWarps * G * (D + 2);
-  // shared-memory layout (bytes): barriers and flags at fixed offsets, then
-  // the ring at the next 1 KB-aligned absolute address (the swizzle pattern is
-  // a function of address bits 7..9), then q slots, merge slots and the prefix.
+  static_assert(D % 64 == 0 && BS % 8 == 0, "shape");
+  static constexpr int NHALF = D / 64;               // 64-dim (128-byte) halves per row
+  static constexpr int TS = BS < 16 ? BS : 16;       // tokens per stage
+  static constexpr int KSTEPS = D / 16;              // QK k-steps over head_dim
+  static constexpr int MT = D / 16;                  // PV m-tiles over head_dim
+  static constexpr int NT = TS / 8;                  // 8-token groups per stage
+  static constexpr int PK = (NT + 1) / 2;            // PV k-steps (16 tokens) per stage
+  static constexpr int REC = rec_floats(G, D);
+  // shared-memory layout: fixed part (bytes)
   static constexpr int OFF_FULL = 0;
-  static constexpr int OFF_EMPTY = OFF_FULL + NST * 8;
-  static constexpr int OFF_QFULL = OFF_EMPTY + NST * 8;
-  static constexpr int OFF_QEMPTY = OFF_QFULL + QS * 8;
-  static constexpr int OFF_MFULL = OFF_QEMPTY + QS * 8;   // merge slots published
-  static constexpr int OFF_MEMPTY = OFF_MFULL + 2 * 8;    // merge slots free again
-  static constexpr int OFF_FLAGS = OFF_MEMPTY + 2 * 8;    // see kFlag* below
-  static constexpr int RING_MIN = OFF_FLAGS + 128;
-  static constexpr int RING_BYTES = NST * STAGE_BYTES;
-  static constexpr int SCRATCH_FLOATS = 32 * G * 2;  // merge warp: staged (max, sum) pairs
-  static constexpr int REC_FLOATS = rec_floats(G, D);  // partial record stride (16-byte multiple)
-  static constexpr int TAIL_BYTES = QS * QSLOT_BYTES + 2 * MSLOT_FLOATS * 4 + SCRATCH_FLOATS * 4;
-  static size_t smem_bytes(int num_seqs) {
-    return static_cast<size_t>(RING_MIN + 1024 + RING_BYTES + TAIL_BYTES) +
+  static constexpr int OFF_EMPTY = OFF_FULL + kMaxStages * 8;
+  static constexpr int OFF_QFULL = OFF_EMPTY + kMaxStages * 8;
+  static constexpr int OFF_QEMPTY = OFF_QFULL + 8;
+  static constexpr int OFF_FLAGS = OFF_QEMPTY + 8;  // 32 ints, see kFlag*
+  static constexpr int FIXED = OFF_FLAGS + 128;
+  static int stage_bytes(int hg) { return 2 * NHALF * hg * TS * 128; }
+  // then, from the next 1 KB-aligned address (the swizzle pattern is a
+  // function of address bits 7..9): ring, q slot, merge scratch, prefix
+  static size_t smem_bytes(int hg, int nst, int num_seqs) {
+    return static_cast<size_t>(FIXED) + 1024 + static_cast<size_t>(nst) * stage_bytes(hg) +
+           static_cast<size_t>(hg) * G * D * 2 + static_cast<size_t>(hg) * kMergeBatch * G * 2 * 4 +
            static_cast<size_t>(num_seqs + 1) * 4;
   }
 };
 
 // int flags in shared memory
-constexpr int kFlagAbort = 0;  // set when a bounded wait gave up
-constexpr int kFlagWsum = 8;   // [8] warp sums of the prefix scan
+constexpr int kFlagAbort = 0;   // set when a bounded wait gave up
+constexpr int kFlagWsum = 8;    // [9] warp sums of the prefix scan
+constexpr int kFlagQLen = 24;   // sequence length of the piece in the q slot
 
 struct DecodeParams {
   const __half* q;
@@ -251,7 +237,7 @@ struct DecodeParams {
   const int32_t* seq_lens;
   __half* out;
   int32_t* counters;  // [S][Hkv] arrival counters of cut segments
-  float* records;     // [2 * max_chunks][rec_floats(G, D)] partial results of cut segments
+  float* records;     // [2 * max_chunks][HG][rec_floats(G, D)] partials of cut segments
   int32_t* err;
   int num_seqs;
   int num_q_heads;
@@ -259,6 +245,8 @@ struct DecodeParams {
   int max_blocks;
   int num_blocks;
   int cap_blocks;  // max blocks per chunk (0 = balance over the grid)
+  int hg;          // KV heads per group (consumer warps)
+  int nst;         // ring stages
   float qscale;    // scale * log2(e)
 };
 
@@ -270,72 +258,46 @@ __device__ __forceinline__ int clamp_len(int L, int cap, int32_t* err) {
   return L;
 }
 
-// Position in the block stream -> (sequence, KV head, block within segment).
+// Position in the block stream -> (sequence, head group, block within segment).
 struct Cursor {
-  int seq, kvh, j, nb;  // nb = blocks in the segment (sequence)
+  int seq, hg, j, nb;   // nb = blocks in the segment (sequence)
   long long seg_start;  // stream index of the segment's block 0
 };
 
-__device__ __forceinline__ Cursor locate(long long x, const int* pfx, int S, int hkv) {
-  int lo = 0, hi = S;  // largest i with pfx[i] * hkv <= x
+__device__ __forceinline__ Cursor locate(long long x, const int* pfx, int S, int nhg) {
+  int lo = 0, hi = S;  // largest i with pfx[i] * nhg <= x
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (static_cast<long long>(pfx[mid]) * hkv <= x) lo = mid;
+    if (static_cast<long long>(pfx[mid]) * nhg <= x) lo = mid;
     else hi = mid;
   }
   Cursor c;
   c.seq = lo;
   c.nb = pfx[lo + 1] - pfx[lo];
-  const long long r = x - static_cast<long long>(pfx[lo]) * hkv;
-  c.kvh = static_cast<int>(r / c.nb);
+  const long long r = x - static_cast<long long>(pfx[lo]) * nhg;
+  c.hg = static_cast<int>(r / c.nb);
   c.j = static_cast<int>(r % c.nb);
-  c.seg_start = static_cast<long long>(pfx[lo]) * hkv + static_cast<long long>(c.kvh) * c.nb;
+  c.seg_start = static_cast<long long>(pfx[lo]) * nhg + static_cast<long long>(c.hg) * c.nb;
   return c;
 }
 
-// One warp combines `parts` per-warp states of a piece (merge slot `ms`) and
-// either writes the fp16 output (uncut segment) or the chunk's partial record.
-template <int D, int G>
-__device__ __forceinline__ void merge_warps(const float* ms, const int* who, int parts,
-                                            __half* out_row, float* rec, bool cut) {
-  const int lane = threadIdx.x & 31;
-  for (int gg = 0; gg < G; ++gg) {
-    float M = -INFINITY;
-    for (int x = 0; x < parts; ++x) M = fmaxf(M, ms[(who[x] * G + gg) * (D + 2) + D]);
-    const float mu = M == -INFINITY ? 0.f : M;
-    float wgt[kConsumerWarps];
-    float Ls = 0.f;
-#pragma unroll
-    for (int x = 0; x < kConsumerWarps; ++x) {
-      wgt[x] = 0.f;
-      if (x < parts) {
-        const float* w = ms + (who[x] * G + gg) * (D + 2);
-        wgt[x] = fast_exp2(w[D] - mu);
-        Ls += w[D + 1] * wgt[x];
-      }
-    }
-    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-    for (int d = lane; d < D; d += 32) {
-      float A = 0.f;
-#pragma unroll
-      for (int x = 0; x < kConsumerWarps; ++x)
-        if (x < parts) A += ms[(who[x] * G + gg) * (D + 2) + d] * wgt[x];
-      if (!cut) out_row[gg * D + d] = __float2half_rn(A * inv);
-      else rec[gg * D + d] = A;
-    }
-    if (cut && lane == 0) {
-      rec[G * D + 2 * gg] = M;
-      rec[G * D + 2 * gg + 1] = Ls;
-    }
-  }
+// TMA tiled copy of box {x, y, z, w} of a 4-D tensor map into this CTA's
+// shared memory, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, int w, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
 }
 
-// One warp merges the partial records of a cut segment and writes its fp16
-// output. Record i of the segment is `recs + rec_of(i) * rec_floats(G, D)` holding
-// acc [G][D], then (max, sum) per head. Records are folded in batches of 32
-// with the online log-sum-exp rule: the (max, sum) pairs of a batch are staged
-// in shared memory by 32 lanes at once, and every lane then streams its float4
-// slices of the accumulators with independent loads.
+// One warp merges the partial records of a cut segment's head and writes its
+// fp16 output. Record i is `recs + rec_of(i) * rec_floats(G, D)`: acc [G][D],
+// then (max, sum) per head. Records are folded in batches with the online
+// log-sum-exp rule: the (max, sum) pairs of a batch are staged in shared
+// memory by the lanes at once, then every lane streams its float4 slices of
+// the accumulators with independent loads.
 template <int D, int G, typename RecOf>
 __device__ __forceinline__ void merge_records(const float* recs, int E, RecOf rec_of,
                                               float* scratch, __half* out_row) {
@@ -352,8 +314,8 @@ __device__ __forceinline__ void merge_records(const float* recs, int E, RecOf re
   }
 #pragma unroll
   for (int k = 0; k < PER; ++k) A[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int base = 0; base < E; base += 32) {
-    const int nb = min(32, E - base);
+  for (int base = 0; base < E; base += kMergeBatch) {
+    const int nb = min(kMergeBatch, E - base);
     if (lane < nb) {
       const float* rp = recs + rec_of(base + lane) * RS + G * D;
 #pragma unroll
@@ -420,59 +382,57 @@ __device__ __forceinline__ void merge_records(const float* recs, int E, RecOf re
 }
 
 template <int D, int BS, int G>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kMaxThreads, 1)
     paged_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap) {
   using SH = Shape<D, BS, G>;
+  constexpr int TS = SH::TS;
   extern __shared__ __align__(128) unsigned char smem[];
+  const int HG = p.hg, NST = p.nst;
+  const int HALF = HG * TS * 128;        // one 64-dim half of one stage's K (or V)
+  const int TILE = SH::NHALF * HALF;     // K (or V) of one stage
+  const int STAGE = 2 * TILE;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_FULL);
   uint64_t* empty_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_EMPTY);
   uint64_t* qfull_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_QFULL);
   uint64_t* qempty_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_QEMPTY);
-  uint64_t* mfull_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_MFULL);
-  uint64_t* mempty_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_MEMPTY);
   int* flags = reinterpret_cast<int*>(smem + SH::OFF_FLAGS);
   volatile int* abort_flag = flags + kFlagAbort;
   const uint32_t smem_base = smem_addr(smem);
-  unsigned char* ring = smem + (((smem_base + SH::RING_MIN + 1023u) & ~1023u) - smem_base);
-  unsigned char* qring = ring + SH::RING_BYTES;
-  float* mslots = reinterpret_cast<float*>(qring + SH::QS * SH::QSLOT_BYTES);
-  float* scratch = mslots + 2 * SH::MSLOT_FLOATS;
-  int* pfx = reinterpret_cast<int*>(scratch + SH::SCRATCH_FLOATS);
+  unsigned char* ring = smem + (((smem_base + SH::FIXED + 1023u) & ~1023u) - smem_base);
+  unsigned char* qslot = ring + static_cast<size_t>(NST) * STAGE;
+  float* scratch_all = reinterpret_cast<float*>(qslot + HG * G * D * 2);
+  int* pfx = reinterpret_cast<int*>(scratch_all + HG * kMergeBatch * G * 2);
 
   const int tid = threadIdx.x;
+  const int nthreads = blockDim.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int S = p.num_seqs;
   const int Hkv = p.num_kv_heads;
+  const int NHG = Hkv / HG;
   const int cap = p.max_blocks * BS;
 
   if (tid == 0) {
-    for (int s = 0; s < SH::NST; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(smem_addr(&full_bar[s]), 1);
-      mbar_init(smem_addr(&empty_bar[s]), 1);
+      mbar_init(smem_addr(&empty_bar[s]), HG);
     }
-    for (int s = 0; s < SH::QS; ++s) {
-      mbar_init(smem_addr(&qfull_bar[s]), 1);
-      mbar_init(smem_addr(&qempty_bar[s]), kConsumerWarps);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_addr(&mfull_bar[s]), kConsumerWarps);
-      mbar_init(smem_addr(&mempty_bar[s]), 1);
-    }
+    mbar_init(smem_addr(qfull_bar), 1);
+    mbar_init(smem_addr(qempty_bar), HG);
     flags[kFlagAbort] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
 
   // ---- blocks per sequence, exclusive prefix sum in shared memory ----
-  for (int i = tid; i < S; i += kThreads) {
+  for (int i = tid; i < S; i += nthreads) {
     const int L = clamp_len(__ldg(p.seq_lens + i), cap, p.err);
     pfx[i + 1] = (L + BS - 1) / BS;
   }
   if (tid == 0) pfx[0] = 0;
   __syncthreads();
   {
-    const int per = (S + kThreads - 1) / kThreads;
+    const int per = (S + nthreads - 1) / nthreads;
     const int lo = min(S, tid * per), hi = min(S, lo + per);
     int sum = 0;
     for (int i = lo; i < hi; ++i) sum += pfx[i + 1];
@@ -494,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  const long long total = static_cast<long long>(pfx[S]) * Hkv;  // blocks in the stream
+  const long long total = static_cast<long long>(pfx[S]) * NHG;  // blocks in the stream
   long long chunk = (total + gridDim.x - 1) / gridDim.x;
   if (p.cap_blocks > 0 && chunk > p.cap_blocks) chunk = p.cap_blocks;
   if (chunk < 1) chunk = 1;
@@ -505,185 +465,170 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (programmatic dependent launch): wait for it before touching them.
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  if (warp == kProducerWarp) {
+  if (warp == HG) {
     // =========================== producer warp ===========================
-    uint32_t g = 0;   // ring sequence number
+    // The walk visits the CTA's chunks, their pieces, and each piece in groups
+    // of up to 32 blocks. The table entries (one per lane) and the sequence
+    // length of the next group are loaded while the current group is issued,
+    // so no piece boundary waits on a global load.
+    uint32_t g = 0;   // ring sequence number (stages)
     uint32_t pc = 0;  // piece number
-    for (long long c = blockIdx.x; c < nchunks; c += gridDim.x) {
-      long long x = c * chunk;
-      const long long xe = min(total, x + chunk);
-      while (x < xe) {
-        const Cursor cur = locate(x, pfx, S, Hkv);
-        const int n = static_cast<int>(min(static_cast<long long>(cur.nb - cur.j), xe - x));
-        // q rows of the piece's G heads -> q slot
-        {
-          const int qs = pc % SH::QS;
-          const uint32_t quse = pc / SH::QS;
-          if (!__shfl_sync(0xffffffffu, *abort_flag, 0) &&
-              (quse == 0 || warp_wait_phase(smem_addr(&qempty_bar[qs]), (quse - 1) & 1,
-                                            abort_flag, p.err))) {
-            if (lane == 0) {
-              const uint32_t qb = smem_addr(&qfull_bar[qs]);
-              mbar_arrive_expect_tx(qb, G * D * 2);
-              bulk_copy_g2s(smem_addr(qring + qs * SH::QSLOT_BYTES),
-                            p.q + (static_cast<long long>(cur.seq) * p.num_q_heads +
-                                   cur.kvh * G) * D,
-                            G * D * 2, qb);
-            }
-            __syncwarp();
+    long long c = blockIdx.x;
+    long long x = c * chunk, xe = min(total, x + chunk);
+    bool have = c < nchunks && x < xe;
+    Cursor cur{};
+    int n = 0, j0 = 0;
+    int phys_next = 0, len_next = 0;
+    if (have) {
+      cur = locate(x, pfx, S, NHG);
+      n = static_cast<int>(min(static_cast<long long>(cur.nb - cur.j), xe - x));
+      len_next = min(max(__ldg(p.seq_lens + cur.seq), 0), cap);
+      phys_next = lane < min(32, n)
+                      ? __ldg(p.block_table + static_cast<long long>(cur.seq) * p.max_blocks +
+                              cur.j + lane)
+                      : 0;
+    }
+    while (have) {
+      const Cursor gc = cur;
+      const int gn = n, gj0 = j0, glen = len_next, phys_lane = phys_next;
+      const int nn = min(32, gn - gj0);
+      // advance to the next group and start loading its table entries
+      j0 += 32;
+      if (j0 >= n) {
+        x += n;
+        if (x >= xe) {
+          c += gridDim.x;
+          have = c < nchunks;
+          if (have) {
+            x = c * chunk;
+            xe = min(total, x + chunk);
           }
         }
-        const int32_t* trow = p.block_table + static_cast<long long>(cur.seq) * p.max_blocks;
-        for (int j0 = 0; j0 < n; j0 += 32) {
-          const int phys_lane = (j0 + lane < n) ? __ldg(trow + cur.j + j0 + lane) : 0;
-          const int nn = min(32, n - j0);
-          for (int jj = 0; jj < nn; ++jj, ++g) {
-            const int stage = g % SH::NST;
-            const uint32_t use = g / SH::NST;
-            const int phys = __shfl_sync(0xffffffffu, phys_lane, jj);
-            if (__shfl_sync(0xffffffffu, *abort_flag, 0)) continue;
-            if (use > 0 &&
-                !warp_wait_phase(smem_addr(&empty_bar[stage]), (use - 1) & 1, abort_flag, p.err))
-              continue;
-            const bool bad = phys < 0 || phys >= p.num_blocks;
-            if (lane == 0) {
-              const uint32_t fb = smem_addr(&full_bar[stage]);
-              if (bad) atomicOr(p.err, PA_DEVERR_BAD_BLOCK);
-              // whole tiles: rows past the sequence end are masked by the consumers
-              mbar_arrive_expect_tx(fb, bad ? 0u : static_cast<uint32_t>(SH::STAGE_BYTES));
-              if (!bad) {
-                const uint32_t kdst = smem_addr(ring + stage * SH::STAGE_BYTES);
+        if (have) {
+          cur = locate(x, pfx, S, NHG);
+          n = static_cast<int>(min(static_cast<long long>(cur.nb - cur.j), xe - x));
+          j0 = 0;
+          len_next = min(max(__ldg(p.seq_lens + cur.seq), 0), cap);
+        }
+      }
+      if (have) {
+        const int cnt = min(32, n - j0);
+        phys_next = lane < cnt ? __ldg(p.block_table +
+                                       static_cast<long long>(cur.seq) * p.max_blocks + cur.j +
+                                       j0 + lane)
+                               : 0;
+      }
+      if (gj0 == 0) {
+        // new piece: q rows of the group's HG*G query heads and the length -> q slot
+        if (!__shfl_sync(0xffffffffu, *abort_flag, 0) &&
+            (pc == 0 ||
+             warp_wait_phase(smem_addr(qempty_bar), (pc - 1) & 1, abort_flag, p.err))) {
+          if (lane == 0) {
+            flags[kFlagQLen] = glen;  // published by the arrive below
+            const uint32_t qb = smem_addr(qfull_bar);
+            mbar_arrive_expect_tx(qb, HG * G * D * 2);
+            bulk_copy_g2s(smem_addr(qslot),
+                          p.q + (static_cast<long long>(gc.seq) * p.num_q_heads +
+                                 static_cast<long long>(gc.hg) * HG * G) * D,
+                          HG * G * D * 2, qb);
+          }
+          __syncwarp();
+        }
+      }
+      for (int jj = 0; jj < nn; ++jj) {
+        const int phys = __shfl_sync(0xffffffffu, phys_lane, jj);
+        const int blk = gc.j + gj0 + jj;
+        const int vb = min(BS, glen - blk * BS);   // valid rows of the block (>= 1)
+        const int nsb = (vb + TS - 1) / TS;         // stages that hold valid rows
+        const bool bad = phys < 0 || phys >= p.num_blocks;
+        for (int sb = 0; sb < nsb; ++sb, ++g) {
+          const int stage = g % NST;
+          const uint32_t use = g / NST;
+          if (__shfl_sync(0xffffffffu, *abort_flag, 0)) continue;
+          if (use > 0 &&
+              !warp_wait_phase(smem_addr(&empty_bar[stage]), (use - 1) & 1, abort_flag, p.err))
+            continue;
+          if (lane == 0) {
+            const uint32_t fb = smem_addr(&full_bar[stage]);
+            if (bad) atomicOr(p.err, PA_DEVERR_BAD_BLOCK);
+            // whole tiles: rows past the sequence end are masked by the consumers
+            mbar_arrive_expect_tx(fb, bad ? 0u : static_cast<uint32_t>(STAGE));
+            if (!bad) {
+              const uint32_t kdst = smem_addr(ring + static_cast<size_t>(stage) * STAGE);
 #pragma unroll
-                for (int h = 0; h < SH::NHALF; ++h) {
-                  tma_load_3d(kdst + h * SH::HALF_BYTES, &kmap, 64 * h, cur.kvh, phys * BS, fb);
-                  tma_load_3d(kdst + SH::TILE_BYTES + h * SH::HALF_BYTES, &vmap, 64 * h, cur.kvh,
-                              phys * BS, fb);
-                }
+              for (int h = 0; h < SH::NHALF; ++h) {
+                tma_load_4d(kdst + h * HALF, &kmap, 64 * h, sb * TS, gc.hg * HG, phys, fb);
+                tma_load_4d(kdst + TILE + h * HALF, &vmap, 64 * h, sb * TS, gc.hg * HG, phys,
+                            fb);
               }
             }
-            __syncwarp();
           }
+          __syncwarp();
         }
-        x += n;
-        ++pc;
       }
+      if (gj0 + 32 >= gn) ++pc;  // the piece's last group
     }
     // After an abort, wait (bounded) for copies still landing in shared memory.
     if (*abort_flag) {
-      const uint32_t first = g > static_cast<uint32_t>(SH::NST) ? g - SH::NST : 0;
+      const uint32_t first = g > static_cast<uint32_t>(NST) ? g - NST : 0;
       for (uint32_t gi = first; gi < g; ++gi) {
-        const uint32_t bar = smem_addr(&full_bar[gi % SH::NST]);
+        const uint32_t bar = smem_addr(&full_bar[gi % NST]);
         const unsigned long long t0 = global_ns();
-        while (!mbar_try_wait(bar, (gi / SH::NST) & 1) && global_ns() - t0 < kWaitLimitNs) {
+        while (!mbar_try_wait(bar, (gi / NST) & 1) && global_ns() - t0 < kWaitLimitNs) {
         }
       }
-      const uint32_t qfirst = pc > static_cast<uint32_t>(SH::QS) ? pc - SH::QS : 0;
-      for (uint32_t pi = qfirst; pi < pc; ++pi) {
-        const uint32_t bar = smem_addr(&qfull_bar[pi % SH::QS]);
+      if (pc > 0) {
         const unsigned long long t0 = global_ns();
-        while (!mbar_try_wait(bar, (pi / SH::QS) & 1) && global_ns() - t0 < kWaitLimitNs) {
+        while (!mbar_try_wait(smem_addr(qfull_bar), (pc - 1) & 1) &&
+               global_ns() - t0 < kWaitLimitNs) {
         }
-      }
-    }
-    return;
-  }
-
-  if (warp == kMergeWarp) {
-    // ============================ merge warp =============================
-    // zero outputs of empty sequences (this CTA's share)
-    for (int i = blockIdx.x; i < S; i += gridDim.x) {
-      if (pfx[i + 1] == pfx[i]) {
-        __half* o = p.out + static_cast<long long>(i) * p.num_q_heads * D;
-        for (int e = lane; e < p.num_q_heads * D; e += 32) o[e] = __float2half_rn(0.f);
-      }
-    }
-    uint32_t g = 0;   // block index in the CTA's stream
-    uint32_t pc = 0;  // piece number
-    for (long long c = blockIdx.x; c < nchunks; c += gridDim.x) {
-      long long x = c * chunk;
-      const long long xe = min(total, x + chunk);
-      bool first_piece = true;
-      while (x < xe) {
-        const Cursor cur = locate(x, pfx, S, Hkv);
-        const int n = static_cast<int>(min(static_cast<long long>(cur.nb - cur.j), xe - x));
-        const int msi = pc & 1;
-        if (warp_wait_phase(smem_addr(&mfull_bar[msi]), (pc >> 1) & 1, abort_flag, p.err)) {
-          const int parts = min(n, kConsumerWarps);
-          int who[kConsumerWarps];
-#pragma unroll
-          for (int k = 0; k < kConsumerWarps; ++k)
-            who[k] = static_cast<int>((g + k) % kConsumerWarps);
-          const bool cut = cur.j > 0 || cur.j + n < cur.nb;
-          const long long rec_i = 2 * c + (first_piece ? 0 : 1);
-          __half* out_row = p.out +
-              (static_cast<long long>(cur.seq) * p.num_q_heads + cur.kvh * G) * D;
-          merge_warps<D, G>(mslots + msi * SH::MSLOT_FLOATS, who, parts, out_row,
-                            p.records + rec_i * SH::REC_FLOATS, cut);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_addr(&mempty_bar[msi]));  // slot free again
-          if (cut) {
-            // chunks covering this segment: c_first .. c_last; the last to arrive merges
-            const long long s0 = cur.seg_start, s1 = cur.seg_start + cur.nb;
-            const long long c_first = s0 / chunk, c_last = (s1 - 1) / chunk;
-            const int expected = static_cast<int>(c_last - c_first + 1);
-            __threadfence();
-            __syncwarp();
-            int* cnt = p.counters + static_cast<long long>(cur.seq) * Hkv + cur.kvh;
-            int fin = 0;
-            if (lane == 0) fin = atomicAdd(cnt, 1) == expected - 1;
-            fin = __shfl_sync(0xffffffffu, fin, 0);
-            if (fin) {
-              __threadfence();
-              auto rec_of = [&](int i) -> long long {
-                const long long cc = c_first + i;
-                return 2 * cc + ((cc == c_first && s0 > cc * chunk) ? 1 : 0);
-              };
-              merge_records<D, G>(p.records, expected, rec_of, scratch, out_row);
-              if (lane == 0) atomicExch(cnt, 0);
-            }
-          }
-        }
-        g += n;
-        x += n;
-        ++pc;
-        first_piece = false;
       }
     }
     return;
   }
 
   // ============================ consumer warps ============================
-  const int cw = warp;
+  // Warp w owns KV head (group * HG + w) and its G query heads.
+  const int w = warp;
   const int gid = lane >> 2;  // mma group id: row of A / column of B
   const int tig = lane & 3;   // thread in group
+  float* scratch = scratch_all + w * kMergeBatch * G * 2;
+
+  // zero outputs of empty sequences (this CTA's share)
+  for (int i = blockIdx.x; i < S; i += gridDim.x) {
+    if (pfx[i + 1] == pfx[i]) {
+      __half* o = p.out + static_cast<long long>(i) * p.num_q_heads * D;
+      for (int e = tid; e < p.num_q_heads * D; e += HG * 32) o[e] = __float2half_rn(0.f);
+    }
+  }
 
   // ldmatrix addressing inside a swizzled tile: lane supplies row (lane & 7)
-  // of matrix (lane >> 3); logical 16-byte chunk c of row t sits at chunk
-  // c ^ (t & 7) of its 128-byte line (rows of a matrix share t & 7 == lane & 7).
+  // of matrix (lane >> 3); logical 16-byte chunk c of row r sits at chunk
+  // c ^ (r & 7) of its 128-byte line. A head's rows start at a multiple of 8
+  // rows, so r & 7 == lane & 7 for every row a lane addresses.
   const int ld_row = lane & 7;
   const int ld_mat = lane >> 3;
 
-  uint32_t g = 0;   // ring sequence number of the next block (= block index in the CTA stream)
+  uint32_t g = 0;   // ring sequence number of the next stage
   uint32_t pc = 0;  // piece number
   for (long long c = blockIdx.x; c < nchunks; c += gridDim.x) {
     long long x = c * chunk;
     const long long xe = min(total, x + chunk);
+    bool first_piece = true;
     while (x < xe) {
-      const Cursor cur = locate(x, pfx, S, Hkv);
+      const Cursor cur = locate(x, pfx, S, NHG);
       const int n = static_cast<int>(min(static_cast<long long>(cur.nb - cur.j), xe - x));
-      // blocks of this piece go round-robin: block j to warp (g + j) % NC
-      const int first_j =
-          (cw - static_cast<int>(g % kConsumerWarps) + kConsumerWarps) % kConsumerWarps;
-      const bool mine = first_j < n;
+      const int kvh = cur.hg * HG + w;
 
-      // ---- q of the piece: every warp observes the slot's phase, then frees it ----
+      // ---- q and length of the piece ----
       uint32_t qa[SH::KSTEPS][2];  // A fragments a0/a2 per k-step; rows (heads) >= G are zero
+      int L = 0;
       {
-        const int qs = pc % SH::QS;
-        const bool ok = warp_wait_phase(smem_addr(&qfull_bar[qs]), (pc / SH::QS) & 1, abort_flag,
-                                        p.err);
-        if (ok && mine) {
-          const uint32_t qrow = smem_addr(qring + qs * SH::QSLOT_BYTES) + ld_row * (D * 2);
+        const bool ok = warp_wait_phase(smem_addr(qfull_bar), pc & 1, abort_flag, p.err);
+        L = flags[kFlagQLen];
+        if (ok) {
+          const uint32_t qrow =
+              smem_addr(qslot) + (w * G + (ld_row < G ? ld_row : 0)) * (D * 2);
 #pragma unroll
           for (int kk = 0; kk < SH::KSTEPS; kk += 2) {
             uint32_t r0, r1, r2, r3;
@@ -695,37 +640,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         __syncwarp();
-        if (ok && lane == 0) mbar_arrive(smem_addr(&qempty_bar[qs]));
+        if (ok && lane == 0) mbar_arrive(smem_addr(qempty_bar));
       }
 
       float m_run = -INFINITY, l_run = 0.f;  // head gid: running max (log2 units), partial sum
       float o[SH::MT][4];                     // O^T[d = mt*16 + gid (+8)][h = 2*tig (+1)]
 #pragma unroll
       for (int mt = 0; mt < SH::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-      if (mine) {
-        const int L = min(max(__ldg(p.seq_lens + cur.seq), 0), cap);
-        for (int jj = first_j; jj < n; jj += kConsumerWarps) {
-          const uint32_t gj = g + jj;
-          const int stage = gj % SH::NST;
-          if (!warp_wait_phase(smem_addr(&full_bar[stage]), (gj / SH::NST) & 1, abort_flag,
-                               p.err))
+
+      for (int jj = 0; jj < n; ++jj) {
+        const int blk = cur.j + jj;
+        const int vb = min(BS, L - blk * BS);
+        const int nsb = (vb + TS - 1) / TS;
+        for (int sb = 0; sb < nsb; ++sb, ++g) {
+          const int stage = g % NST;
+          if (!warp_wait_phase(smem_addr(&full_bar[stage]), (g / NST) & 1, abort_flag, p.err))
             continue;
-          const int blk = cur.j + jj;
-          const int rows = min(BS, L - blk * BS);
-          unsigned char* kt = ring + stage * SH::STAGE_BYTES;
-          unsigned char* vt = kt + SH::TILE_BYTES;
-          if (rows < BS) {
+          const int rows = min(TS, vb - sb * TS);
+          unsigned char* kt = ring + static_cast<size_t>(stage) * STAGE;
+          unsigned char* vt = kt + TILE;
+          if (rows < TS) {
             // rows past the sequence end must add exactly zero to P V
-            const int words = (BS - rows) * 8;  // 16-byte words per half
+            const int words = (TS - rows) * 8;  // 16-byte words per half
 #pragma unroll
             for (int h = 0; h < SH::NHALF; ++h) {
-              uint4* z = reinterpret_cast<uint4*>(vt + h * SH::HALF_BYTES + rows * 128);
-              for (int w = lane; w < words; w += 32) z[w] = make_uint4(0, 0, 0, 0);
+              uint4* z = reinterpret_cast<uint4*>(vt + h * HALF + (w * TS + rows) * 128);
+              for (int i = lane; i < words; i += 32) z[i] = make_uint4(0, 0, 0, 0);
             }
             __syncwarp();
           }
-          const uint32_t kaddr = smem_addr(kt);
-          const uint32_t vaddr = smem_addr(vt);
+          const uint32_t kaddr = smem_addr(kt) + w * TS * 128;
+          const uint32_t vaddr = smem_addr(vt) + w * TS * 128;
 
           // ---- S = Q K^T for each 8-token group ----
           // x4 of k-steps (kk, kk+1): matrix m covers dims (2*kk + m) * 8 .. +8
@@ -738,13 +683,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < SH::KSTEPS; kk += 2) {
               const int gc = 2 * kk + ld_mat;  // 16-byte chunk of the row, 0 .. D/8-1
               uint32_t b0, b1, b2, b3;
-              ldsm_x4(rowa + (gc >> 3) * SH::HALF_BYTES + (((gc & 7) ^ ld_row) << 4), b0, b1, b2,
-                      b3);
+              ldsm_x4(rowa + (gc >> 3) * HALF + (((gc & 7) ^ ld_row) << 4), b0, b1, b2, b3);
               mma_16816(s[nt], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
               mma_16816(s[nt], qa[kk + 1][0], 0u, qa[kk + 1][1], 0u, b2, b3);
             }
           }
-          // ---- online softmax over this block's tokens (row gid = head) ----
+          // ---- online softmax over this stage's tokens (row gid = head) ----
           float mx = -INFINITY;
 #pragma unroll
           for (int nt = 0; nt < SH::NT; ++nt) {
@@ -792,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int mt = 0; mt < SH::MT; ++mt) {
               const int gc = 2 * mt + (ld_mat & 1);
-              const uint32_t addr = rowa + (gc >> 3) * SH::HALF_BYTES + (((gc & 7) ^ ld_row) << 4);
+              const uint32_t addr = rowa + (gc >> 3) * HALF + (((gc & 7) ^ ld_row) << 4);
               uint32_t a0, a1, a2, a3;
               if (2 * pk + 1 < SH::NT) {
                 ldsm_x4_t(addr, a0, a1, a2, a3);
@@ -803,88 +747,124 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
             }
           }
-          if (rows < BS) fence_proxy_async_smem();  // generic zero-fill before the next TMA write
+          if (rows < TS) fence_proxy_async_smem();  // generic zero-fill before the next TMA write
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_addr(&empty_bar[stage]));
         }
-        l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-        l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
       }
 
-      // ---- publish this warp's state for the merge warp; never wait for it ----
-      // Every consumer warp passes every slot phase in order (the merge
-      // barrier counts all four), so no wait can alias an older phase.
-      const int msi = pc & 1;
-      const bool slot_ok =
-          pc < 2 || warp_wait_phase(smem_addr(&mempty_bar[msi]), ((pc - 2) >> 1) & 1, abort_flag,
-                                    p.err);
-      if (slot_ok) {
-        if (mine) {
-          float* ms = mslots + msi * SH::MSLOT_FLOATS;
+      // ---- piece finished: this warp holds its head's whole state ----
+      l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+      l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+      const bool cut = cur.j > 0 || cur.j + n < cur.nb;
+      __half* out_row = p.out + (static_cast<long long>(cur.seq) * p.num_q_heads +
+                                 static_cast<long long>(kvh) * G) * D;
+      const int h0 = 2 * tig, h1 = 2 * tig + 1;
+      if (!cut) {
+        const float l0 = __shfl_sync(0xffffffffu, l_run, 8 * tig);
+        const float l1 = __shfl_sync(0xffffffffu, l_run, 8 * tig + 4);
+        const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
 #pragma unroll
-          for (int mt = 0; mt < SH::MT; ++mt) {
-            const int d = mt * 16 + gid;
-            const int h0 = 2 * tig, h1 = 2 * tig + 1;
-            if (h0 < G) {
-              ms[(cw * G + h0) * (D + 2) + d] = o[mt][0];
-              ms[(cw * G + h0) * (D + 2) + d + 8] = o[mt][2];
-            }
-            if (h1 < G) {
-              ms[(cw * G + h1) * (D + 2) + d] = o[mt][1];
-              ms[(cw * G + h1) * (D + 2) + d + 8] = o[mt][3];
-            }
+        for (int mt = 0; mt < SH::MT; ++mt) {
+          const int d = mt * 16 + gid;
+          if (h0 < G) {
+            out_row[h0 * D + d] = __float2half_rn(o[mt][0] * i0);
+            out_row[h0 * D + d + 8] = __float2half_rn(o[mt][2] * i0);
           }
-          if (tig == 0 && gid < G) {
-            ms[(cw * G + gid) * (D + 2) + D] = m_run;
-            ms[(cw * G + gid) * (D + 2) + D + 1] = l_run;
+          if (h1 < G) {
+            out_row[h1 * D + d] = __float2half_rn(o[mt][1] * i1);
+            out_row[h1 * D + d + 8] = __float2half_rn(o[mt][3] * i1);
           }
         }
+      } else {
+        float* rec = p.records +
+                     ((2 * c + (first_piece ? 0 : 1)) * HG + w) * static_cast<long long>(SH::REC);
+#pragma unroll
+        for (int mt = 0; mt < SH::MT; ++mt) {
+          const int d = mt * 16 + gid;
+          if (h0 < G) {
+            rec[h0 * D + d] = o[mt][0];
+            rec[h0 * D + d + 8] = o[mt][2];
+          }
+          if (h1 < G) {
+            rec[h1 * D + d] = o[mt][1];
+            rec[h1 * D + d + 8] = o[mt][3];
+          }
+        }
+        if (tig == 0 && gid < G) {
+          rec[G * D + 2 * gid] = m_run;
+          rec[G * D + 2 * gid + 1] = l_run;
+        }
+        // chunks covering this segment: c_first .. c_last; the last to arrive merges
+        const long long s0 = cur.seg_start, s1 = cur.seg_start + cur.nb;
+        const long long c_first = s0 / chunk, c_last = (s1 - 1) / chunk;
+        const int expected = static_cast<int>(c_last - c_first + 1);
+        // every lane's record writes precede lane 0's release-add (the warp
+        // barrier orders them within the CTA, the release extends it to the GPU)
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&mfull_bar[msi]));
+        int* cnt = p.counters + static_cast<long long>(cur.seq) * Hkv + kvh;
+        int fin = 0;
+        if (lane == 0) {
+          __threadfence_block();
+          fin = atomic_add_acq_rel(cnt, 1) == expected - 1;
+        }
+        fin = __shfl_sync(0xffffffffu, fin, 0);
+        __syncwarp();  // orders every lane's record loads after lane 0's acquire
+        if (fin) {
+          auto rec_of = [&](int i) -> long long {
+            const long long cc = c_first + i;
+            return (2 * cc + ((cc == c_first && s0 > cc * chunk) ? 1 : 0)) * HG + w;
+          };
+          merge_records<D, G>(p.records, expected, rec_of, scratch, out_row);
+          if (lane == 0) atomicExch(cnt, 0);
+        }
       }
-      g += n;
       x += n;
       ++pc;
+      first_piece = false;
     }
   }
 }
 
 // --------------------------------------------------------------- host ---
-struct Layout {
-  size_t counters = 0, records = 0, total = 0;
-  long long max_records = 0;
-};
-
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Chunks a launch can produce: at most one per CTA of the grid (kMaxGrid),
 // or, with a per-chunk cap, enough to cover every block of every segment.
-long long max_chunks(int S, int Hkv, int MB, int cap_blocks) {
+long long max_chunks(int S, int nhg, int MB, int cap_blocks) {
   long long m = kMaxGrid;
   if (cap_blocks > 0) {
-    const long long blocks = static_cast<long long>(S) * Hkv * MB;
+    const long long blocks = static_cast<long long>(S) * nhg * MB;
     const long long need = (blocks + cap_blocks - 1) / cap_blocks;
     if (need > m) m = need;
   }
   return m;
 }
 
+struct Layout {
+  size_t counters = 0, records = 0, total = 0;
+};
+
+// Workspace: int32 arrival counters [S][Hkv], then two partial records per
+// chunk and KV head of the group.
 Layout workspace_layout(int S, int Hq, int Hkv, int D, int MB, int cap_blocks) {
   Layout w;
   const int G = Hq / Hkv;
-  w.max_records = 2 * max_chunks(S, Hkv, MB, cap_blocks);
+  const int hg = head_group(Hkv);
+  const long long recs = 2 * max_chunks(S, Hkv / hg, MB, cap_blocks) * hg;
   w.counters = 0;
   w.records = round256(static_cast<size_t>(S) * Hkv * 4);
-  w.total = w.records + round256(static_cast<size_t>(w.max_records) * rec_floats(G, D) * 4);
+  w.total = w.records + round256(static_cast<size_t>(recs) * rec_floats(G, D) * 4);
   return w;
 }
 
 // --- TMA descriptors of the pools -------------------------------------------
-// A 3-D tensor map over a pool seen as [NB*BS rows][Hkv][D] fp16 (innermost
-// first: D, Hkv, rows), box {64, 1, BS} with the 128-byte swizzle: one copy
-// moves one 64-dimension half of one KV head of one block. Encoding costs a
-// few microseconds of host time, so the last few maps are cached by (device,
-// pointer, shape).
+// A 4-D tensor map over a pool seen as (dim, token, KV head, block) — the
+// token stride (Hkv*D*2 bytes) is larger than the head stride (D*2) — with box
+// {64, tokens per stage, HG, 1} and the 128-byte swizzle: one copy moves one
+// 64-dimension half of HG heads of a block, landing as [head][token][128 B].
+// Encoding costs a few microseconds of host time, so the last few maps are
+// cached by (device, pointer, shape).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -893,10 +873,10 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 struct MapKey {
   int device;
   const void* ptr;
-  int D, BS, Hkv, NB;
+  int D, BS, Hkv, NB, hg, ts;
   bool operator==(const MapKey& o) const {
     return device == o.device && ptr == o.ptr && D == o.D && BS == o.BS && Hkv == o.Hkv &&
-           NB == o.NB;
+           NB == o.NB && hg == o.hg && ts == o.ts;
   }
 };
 
@@ -922,14 +902,16 @@ pa_status pool_tensor_map(const MapKey& key, CUtensorMap* out) {
       return pa::fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     encode = reinterpret_cast<EncodeTiledFn>(fn);
   }
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(key.D), static_cast<cuuint64_t>(key.Hkv),
-                              static_cast<cuuint64_t>(key.NB) * key.BS};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(key.D) * 2,
-                                 static_cast<cuuint64_t>(key.Hkv) * key.D * 2};
-  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(key.BS)};
-  const cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(key.D), static_cast<cuuint64_t>(key.BS),
+                              static_cast<cuuint64_t>(key.Hkv), static_cast<cuuint64_t>(key.NB)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(key.Hkv) * key.D * 2,   // token
+                                 static_cast<cuuint64_t>(key.D) * 2,             // KV head
+                                 static_cast<cuuint64_t>(key.BS) * key.Hkv * key.D * 2};  // block
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(key.ts), static_cast<cuuint32_t>(key.hg),
+                             1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUtensorMap m;
-  CUresult r = encode(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(key.ptr), dims,
+  CUresult r = encode(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(key.ptr), dims,
                       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -944,58 +926,92 @@ pa_status pool_tensor_map(const MapKey& key, CUtensorMap* out) {
   return PA_OK;
 }
 
+// Launch shape of one decode: head group, ring depth, threads, shared memory
+// and the persistent grid (SMs x resident CTAs, at most kMaxGrid).
+struct LaunchCfg {
+  int hg = 0, nst = 0, threads = 0;
+  size_t smem = 0;
+  long long grid = 0;
+};
+
 template <int D, int BS, int G>
-pa_status launch_decode(const DecodeParams& prm, const pa::DeviceInfo& dev, cudaStream_t stream) {
+pa_status launch_config(const pa::DeviceInfo& dev, int S, int Hkv, LaunchCfg* cfg) {
   using SH = Shape<D, BS, G>;
   auto kernel = paged_decode_kernel<D, BS, G>;
-  const size_t smem = SH::smem_bytes(prm.num_seqs);
-  if (smem > dev.smem_optin)
+  cfg->hg = head_group(Hkv);
+  const int stage = SH::stage_bytes(cfg->hg);
+  int nst = cfg->hg * kRingBytesPerHead / stage;
+  nst = nst < 2 ? 2 : nst > kMaxStages ? kMaxStages : nst;
+  while (nst > 2 && SH::smem_bytes(cfg->hg, nst, S) > dev.smem_optin) --nst;
+  cfg->nst = nst;
+  cfg->smem = SH::smem_bytes(cfg->hg, nst, S);
+  if (cfg->smem > dev.smem_optin)
     return pa::fail(PA_ERR_UNSUPPORTED, "pa_decode_attention: %zu bytes of shared memory needed",
-                    smem);
+                    cfg->smem);
+  cfg->threads = (cfg->hg + 1) * 32;
   static std::mutex mu;
-  static size_t attr_set[64] = {};
-  static size_t occ_smem[64] = {};
-  static int occ_val[64] = {};
+  static bool attr_set[64] = {};
+  struct OccEntry {
+    int device, threads;
+    size_t smem;
+    int occ;
+  };
+  static OccEntry occ_cache[8];
+  static int occ_used = 0, occ_next = 0;
   int occ = 0;
   {
     std::lock_guard<std::mutex> lock(mu);
-    cudaError_t e;
-    if (attr_set[dev.device] < smem) {
-      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(dev.smem_optin));
+    if (!attr_set[dev.device]) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(dev.smem_optin));
       if (e != cudaSuccess) return pa::cuda_fail(e, "cudaFuncSetAttribute");
-      attr_set[dev.device] = dev.smem_optin;
+      attr_set[dev.device] = true;
     }
-    if (occ_smem[dev.device] != smem) {
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, smem);
+    for (int i = 0; i < occ_used; ++i) {
+      const OccEntry& o = occ_cache[i];
+      if (o.device == dev.device && o.threads == cfg->threads && o.smem == cfg->smem) occ = o.occ;
+    }
+    if (occ == 0) {
+      cudaError_t e =
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, cfg->threads, cfg->smem);
       if (e != cudaSuccess) return pa::cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-      occ_smem[dev.device] = smem;
-      occ_val[dev.device] = occ;
+      occ_cache[occ_next] = OccEntry{dev.device, cfg->threads, cfg->smem, occ};
+      occ_next = (occ_next + 1) % 8;
+      if (occ_used < 8) ++occ_used;
     }
-    occ = occ_val[dev.device];
   }
   if (occ < 1) return pa::fail(PA_ERR_UNSUPPORTED, "pa_decode_attention: kernel does not fit an SM");
+  long long grid = static_cast<long long>(dev.sm_count) * occ;
+  cfg->grid = grid > kMaxGrid ? kMaxGrid : grid;
+  return PA_OK;
+}
+
+template <int D, int BS, int G>
+pa_status launch_decode(DecodeParams prm, const pa::DeviceInfo& dev, cudaStream_t stream) {
+  using SH = Shape<D, BS, G>;
+  LaunchCfg cfg;
+  if (pa_status s = launch_config<D, BS, G>(dev, prm.num_seqs, prm.num_kv_heads, &cfg)) return s;
+  prm.hg = cfg.hg;
+  prm.nst = cfg.nst;
   CUtensorMap kmap, vmap;
-  MapKey kk{dev.device, prm.k_pool, D, BS, prm.num_kv_heads, prm.num_blocks};
-  MapKey vk{dev.device, prm.v_pool, D, BS, prm.num_kv_heads, prm.num_blocks};
+  MapKey kk{dev.device, prm.k_pool, D, BS, prm.num_kv_heads, prm.num_blocks, cfg.hg, SH::TS};
+  MapKey vk{dev.device, prm.v_pool, D, BS, prm.num_kv_heads, prm.num_blocks, cfg.hg, SH::TS};
   if (pa_status s = pool_tensor_map(kk, &kmap)) return s;
   if (pa_status s = pool_tensor_map(vk, &vmap)) return s;
-  long long grid = static_cast<long long>(dev.sm_count) * occ;
-  if (grid > kMaxGrid) grid = kMaxGrid;
   // Programmatic dependent launch: the prologue may overlap the tail of the
   // previous kernel on the stream; the kernel waits for it (griddepcontrol)
   // before reading the pool, q or the table.
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(static_cast<unsigned>(cfg.grid));
+  lc.blockDim = dim3(static_cast<unsigned>(cfg.threads));
+  lc.dynamicSmemBytes = cfg.smem;
+  lc.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm, kmap, vmap);
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&lc, paged_decode_kernel<D, BS, G>, prm, kmap, vmap);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_decode_attention launch");
   return PA_OK;
@@ -1022,6 +1038,21 @@ pa_status dispatch_bs(int BS, int G, const DecodeParams& prm, const pa::DeviceIn
     case 32: return dispatch_g<D, 32>(G, prm, dev, s);
   }
   return pa::fail(PA_ERR_UNSUPPORTED, "pa_decode_attention: block_size %d not in {8,16,32}", BS);
+}
+
+// Launch shape without launching (the allocation-free entry point sizes its
+// scratch from the grid).
+pa_status launch_config_any(int D, int BS, int G, const pa::DeviceInfo& dev, int S, int Hkv,
+                            LaunchCfg* cfg) {
+#define PA_CFG_CASE(d, bs, g) \
+  if (D == d && BS == bs && G == g) return launch_config<d, bs, g>(dev, S, Hkv, cfg);
+#define PA_CFG_G(d, bs) PA_CFG_CASE(d, bs, 1) PA_CFG_CASE(d, bs, 2) PA_CFG_CASE(d, bs, 4) \
+  PA_CFG_CASE(d, bs, 8)
+  PA_CFG_G(64, 8) PA_CFG_G(64, 16) PA_CFG_G(64, 32)
+  PA_CFG_G(128, 8) PA_CFG_G(128, 16) PA_CFG_G(128, 32)
+#undef PA_CFG_G
+#undef PA_CFG_CASE
+  return pa::fail(PA_ERR_UNSUPPORTED, "pa_decode_attention: unsupported shape");
 }
 
 pa_status check_decode_shape(int S, int Hq, int Hkv, int D, int BS, int MB, int part_tokens) {
@@ -1052,8 +1083,8 @@ pa_status check_decode_shape(int S, int Hq, int Hkv, int D, int BS, int MB, int 
 // and calling cudaMalloc on the decode path (which also synchronises the
 // device) is not an option for them. For those callers the scratch lives in a
 // file-scope device array of fixed size instead. Every GPU that loads libpa
-// holds these 4 MiB until the process exits.
-constexpr size_t kFixedScratchBytes = size_t(4) << 20;
+// holds these 16 MiB until the process exits.
+constexpr size_t kFixedScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) unsigned char g_pa_fixed_scratch[kFixedScratchBytes];
 
 // Device address of the fixed scratch on the current device, resolved once
@@ -1073,39 +1104,6 @@ unsigned char* fixed_scratch_address(int device) {
     addr[device] = static_cast<unsigned char*>(ptr);
   }
   return addr[device];
-}
-
-// Grid the decode kernel of this shape gets on `dev` (same rule as the launch).
-template <int D, int BS, int G>
-pa_status decode_grid(const pa::DeviceInfo& dev, int S, long long* grid) {
-  using SH = Shape<D, BS, G>;
-  auto kernel = paged_decode_kernel<D, BS, G>;
-  const size_t smem = SH::smem_bytes(S);
-  if (smem > dev.smem_optin)
-    return pa::fail(PA_ERR_UNSUPPORTED, "pa_decode_attention: %zu bytes of shared memory needed",
-                    smem);
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(dev.smem_optin));
-  if (e != cudaSuccess) return pa::cuda_fail(e, "cudaFuncSetAttribute");
-  int occ = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, smem);
-  if (e != cudaSuccess) return pa::cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-  long long g = static_cast<long long>(dev.sm_count) * occ;
-  *grid = g > kMaxGrid ? kMaxGrid : g;
-  return PA_OK;
-}
-
-pa_status decode_grid_any(int D, int BS, int G, const pa::DeviceInfo& dev, int S,
-                          long long* grid) {
-#define PA_GRID_CASE(d, bs, g) \
-  if (D == d && BS == bs && G == g) return decode_grid<d, bs, g>(dev, S, grid);
-#define PA_GRID_G(d, bs) PA_GRID_CASE(d, bs, 1) PA_GRID_CASE(d, bs, 2) PA_GRID_CASE(d, bs, 4) \
-  PA_GRID_CASE(d, bs, 8)
-  PA_GRID_G(64, 8) PA_GRID_G(64, 16) PA_GRID_G(64, 32)
-  PA_GRID_G(128, 8) PA_GRID_G(128, 16) PA_GRID_G(128, 32)
-#undef PA_GRID_G
-#undef PA_GRID_CASE
-  return pa::fail(PA_ERR_UNSUPPORTED, "pa_decode_attention: unsupported shape");
 }
 
 }  // namespace
@@ -1136,26 +1134,72 @@ pa_status pa_decode_workspace_init(void* workspace, size_t workspace_bytes, int 
   return pa::ok();
 }
 
+// Host checks shared by both decode entry points.
+static pa_status check_decode_call(const char* fn, const pa_half* q, const pa_half* k_pool,
+                                   const pa_half* v_pool, const int32_t* block_table,
+                                   const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int block_size,
+                                   int max_blocks_per_seq, int num_blocks, float scale,
+                                   const pa_half* out, int partition_tokens) {
+  if (pa_status s = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                       max_blocks_per_seq, partition_tokens))
+    return s;
+  if (num_blocks <= 0 || static_cast<long long>(num_blocks) * block_size > INT32_MAX)
+    return pa::fail(PA_ERR_INVALID_ARG, "%s: num_blocks %d", fn, num_blocks);
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+    return pa::fail(PA_ERR_INVALID_ARG, "%s: scale is not finite", fn);
+  if (num_seqs == 0) return PA_OK;
+  if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !out)
+    return pa::fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+  if (!pa::aligned16(q) || !pa::aligned16(k_pool) || !pa::aligned16(v_pool) ||
+      !pa::aligned16(out) || (reinterpret_cast<uintptr_t>(block_table) & 3) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3))
+    return pa::fail(PA_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+  return PA_OK;
+}
+
+static DecodeParams make_params(const pa_half* q, const pa_half* k_pool, const pa_half* v_pool,
+                                const int32_t* block_table, const int32_t* seq_lens,
+                                int num_seqs, int num_q_heads, int num_kv_heads,
+                                int max_blocks_per_seq, int num_blocks, float scale, pa_half* out,
+                                unsigned char* ws, size_t records_offset, int cap_blocks) {
+  DecodeParams prm;
+  prm.q = reinterpret_cast<const __half*>(q);
+  prm.k_pool = reinterpret_cast<const __half*>(k_pool);
+  prm.v_pool = reinterpret_cast<const __half*>(v_pool);
+  prm.block_table = block_table;
+  prm.seq_lens = seq_lens;
+  prm.out = reinterpret_cast<__half*>(out);
+  prm.counters = reinterpret_cast<int32_t*>(ws);
+  prm.records = reinterpret_cast<float*>(ws + records_offset);
+  prm.err = nullptr;
+  prm.num_seqs = num_seqs;
+  prm.num_q_heads = num_q_heads;
+  prm.num_kv_heads = num_kv_heads;
+  prm.max_blocks = max_blocks_per_seq;
+  prm.num_blocks = num_blocks;
+  prm.cap_blocks = cap_blocks;
+  prm.hg = 0;   // set by the launch
+  prm.nst = 0;  // set by the launch
+  prm.qscale = scale * kLog2e;
+  return prm;
+}
+
 pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool, const pa_half* v_pool,
                               const int32_t* block_table, const int32_t* seq_lens, int num_seqs,
                               int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                               int max_blocks_per_seq, int num_blocks, float scale, pa_half* out,
                               void* workspace, size_t workspace_bytes, int partition_tokens,
                               pa_stream_t stream) {
-  if (pa_status s = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                                       max_blocks_per_seq, partition_tokens))
+  if (pa_status s = check_decode_call("pa_decode_attention", q, k_pool, v_pool, block_table,
+                                      seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                      block_size, max_blocks_per_seq, num_blocks, scale, out,
+                                      partition_tokens))
     return s;
-  if (num_blocks <= 0 || static_cast<long long>(num_blocks) * block_size > INT32_MAX)
-    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention: num_blocks %d", num_blocks);
-  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
-    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention: scale is not finite");
   if (num_seqs == 0) return pa::ok();
-  if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !out || !workspace)
-    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention: NULL pointer");
-  if (!pa::aligned16(q) || !pa::aligned16(k_pool) || !pa::aligned16(v_pool) ||
-      !pa::aligned16(out) || !pa::aligned16(workspace) ||
-      (reinterpret_cast<uintptr_t>(block_table) & 3) || (reinterpret_cast<uintptr_t>(seq_lens) & 3))
-    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention: misaligned pointer");
+  if (!workspace) return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention: NULL workspace");
+  if (!pa::aligned16(workspace))
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention: misaligned workspace");
   const int cap_blocks = partition_tokens / block_size;
   const Layout lay = workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                       max_blocks_per_seq, cap_blocks);
@@ -1164,32 +1208,17 @@ pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool, const pa_
                     workspace_bytes, lay.total);
   pa::DeviceInfo dev;
   if (pa_status s = pa::current_device(&dev)) return s;
-  DecodeParams prm;
-  prm.q = reinterpret_cast<const __half*>(q);
-  prm.k_pool = reinterpret_cast<const __half*>(k_pool);
-  prm.v_pool = reinterpret_cast<const __half*>(v_pool);
-  prm.block_table = block_table;
-  prm.seq_lens = seq_lens;
-  prm.out = reinterpret_cast<__half*>(out);
-  unsigned char* ws = static_cast<unsigned char*>(workspace);
-  prm.counters = reinterpret_cast<int32_t*>(ws + lay.counters);
-  prm.records = reinterpret_cast<float*>(ws + lay.records);
+  DecodeParams prm = make_params(q, k_pool, v_pool, block_table, seq_lens, num_seqs, num_q_heads,
+                                 num_kv_heads, max_blocks_per_seq, num_blocks, scale, out,
+                                 static_cast<unsigned char*>(workspace), lay.records, cap_blocks);
   prm.err = pa::device_error_word();
   if (!prm.err) return PA_ERR_CUDA;
-  prm.num_seqs = num_seqs;
-  prm.num_q_heads = num_q_heads;
-  prm.num_kv_heads = num_kv_heads;
-  prm.max_blocks = max_blocks_per_seq;
-  prm.num_blocks = num_blocks;
-  prm.cap_blocks = cap_blocks;
-  prm.qscale = scale * kLog2e;
   const int G = num_q_heads / num_kv_heads;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   pa_status st = head_dim == 64 ? dispatch_bs<64>(block_size, G, prm, dev, s)
                                 : dispatch_bs<128>(block_size, G, prm, dev, s);
   return st == PA_OK ? pa::ok() : st;
 }
-
 
 pa_status pa_decode_attention_fixed_scratch(const pa_half* q, const pa_half* k_pool,
                                             const pa_half* v_pool, const int32_t* block_table,
@@ -1198,37 +1227,31 @@ pa_status pa_decode_attention_fixed_scratch(const pa_half* q, const pa_half* k_p
                                             int block_size, int max_blocks_per_seq,
                                             int num_blocks, float scale, pa_half* out,
                                             int partition_tokens, pa_stream_t stream) {
-  if (pa_status s = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                                       max_blocks_per_seq, partition_tokens))
+  if (pa_status s = check_decode_call("pa_decode_attention_fixed_scratch", q, k_pool, v_pool,
+                                      block_table, seq_lens, num_seqs, num_q_heads, num_kv_heads,
+                                      head_dim, block_size, max_blocks_per_seq, num_blocks, scale,
+                                      out, partition_tokens))
     return s;
-  if (num_blocks <= 0 || static_cast<long long>(num_blocks) * block_size > INT32_MAX)
-    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention_fixed_scratch: num_blocks %d",
-                    num_blocks);
-  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
-    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention_fixed_scratch: scale is not finite");
   if (num_seqs == 0) return pa::ok();
-  if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !out)
-    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention_fixed_scratch: NULL pointer");
-  if (!pa::aligned16(q) || !pa::aligned16(k_pool) || !pa::aligned16(v_pool) ||
-      !pa::aligned16(out) || (reinterpret_cast<uintptr_t>(block_table) & 3) ||
-      (reinterpret_cast<uintptr_t>(seq_lens) & 3))
-    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention_fixed_scratch: misaligned pointer");
   pa::DeviceInfo dev;
   if (pa_status s = pa::current_device(&dev)) return s;
   const int G = num_q_heads / num_kv_heads;
-  long long grid = 0;
-  if (pa_status s = decode_grid_any(head_dim, block_size, G, dev, num_seqs, &grid)) return s;
-  // scratch this call needs: arrival counters, then two partial records per chunk
+  LaunchCfg cfg;
+  if (pa_status s = launch_config_any(head_dim, block_size, G, dev, num_seqs, num_kv_heads, &cfg))
+    return s;
+  // scratch this call needs: arrival counters, then two partial records per
+  // chunk and KV head of the group
   const int cap_blocks = partition_tokens / block_size;
-  long long chunks = grid;
+  long long chunks = cfg.grid;
   if (cap_blocks > 0) {
-    const long long blocks = static_cast<long long>(num_seqs) * num_kv_heads * max_blocks_per_seq;
+    const long long blocks =
+        static_cast<long long>(num_seqs) * (num_kv_heads / cfg.hg) * max_blocks_per_seq;
     const long long capped = (blocks + cap_blocks - 1) / cap_blocks;
     if (capped > chunks) chunks = capped;
   }
   const size_t counters = round256(static_cast<size_t>(num_seqs) * num_kv_heads * 4);
-  const size_t need =
-      counters + static_cast<size_t>(2 * chunks) * rec_floats(G, head_dim) * sizeof(float);
+  const size_t need = counters + static_cast<size_t>(2 * chunks) * cfg.hg *
+                                     rec_floats(G, head_dim) * sizeof(float);
   if (need > kFixedScratchBytes)
     return pa::fail(PA_ERR_UNSUPPORTED,
                     "pa_decode_attention_fixed_scratch: this shape needs %zu bytes of scratch; "
@@ -1240,24 +1263,11 @@ pa_status pa_decode_attention_fixed_scratch(const pa_half* q, const pa_half* k_p
   // the scratch keeps the previous call's contents: the counters must start at zero
   cudaError_t e = cudaMemsetAsync(ws, 0, static_cast<size_t>(num_seqs) * num_kv_heads * 4, s);
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_decode_attention_fixed_scratch memset");
-  DecodeParams prm;
-  prm.q = reinterpret_cast<const __half*>(q);
-  prm.k_pool = reinterpret_cast<const __half*>(k_pool);
-  prm.v_pool = reinterpret_cast<const __half*>(v_pool);
-  prm.block_table = block_table;
-  prm.seq_lens = seq_lens;
-  prm.out = reinterpret_cast<__half*>(out);
-  prm.counters = reinterpret_cast<int32_t*>(ws);
-  prm.records = reinterpret_cast<float*>(ws + counters);
+  DecodeParams prm = make_params(q, k_pool, v_pool, block_table, seq_lens, num_seqs, num_q_heads,
+                                 num_kv_heads, max_blocks_per_seq, num_blocks, scale, out, ws,
+                                 counters, cap_blocks);
   prm.err = pa::device_error_word();
   if (!prm.err) return PA_ERR_CUDA;
-  prm.num_seqs = num_seqs;
-  prm.num_q_heads = num_q_heads;
-  prm.num_kv_heads = num_kv_heads;
-  prm.max_blocks = max_blocks_per_seq;
-  prm.num_blocks = num_blocks;
-  prm.cap_blocks = cap_blocks;
-  prm.qscale = scale * kLog2e;
   pa_status st = head_dim == 64 ? dispatch_bs<64>(block_size, G, prm, dev, s)
                                 : dispatch_bs<128>(block_size, G, prm, dev, s);
   return st == PA_OK ? pa::ok() : st;
