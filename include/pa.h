@@ -201,7 +201,7 @@ PA_API pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool,
  * hands all of its device memory to its own KV pool and allocator up front,
  * or one that must not call cudaMalloc on the decode path because that call
  * synchronises the device. The scratch it needs (arrival counters and the
- * partial results of split sequences) lives in a fixed 4 MiB device array
+ * partial results of split sequences) lives in a fixed 16 MiB device array
  * inside libpa, which every GPU that loads the library keeps until the
  * process exits.
  *
@@ -213,9 +213,10 @@ PA_API pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool,
  * - Every call uses the same array and clears its counters on `stream` before
  *   the kernel runs; calls that overlap on the GPU (other streams, other host
  *   threads) race on it and must not be issued.
- * - Shapes whose scratch would exceed 4 MiB (about 2 x SMs x 2 partial results
- *   of G x (head_dim + 2) floats, plus 4 bytes per (sequence, KV head)) are
- *   refused with PA_ERR_UNSUPPORTED; use pa_decode_attention for them.
+ * - Shapes whose scratch would exceed 16 MiB (4 bytes per (sequence, KV
+ *   head), plus two partial results of G x (head_dim + 2) floats per CTA of
+ *   the grid and per KV head a CTA streams, up to 8) are refused with
+ *   PA_ERR_UNSUPPORTED; use pa_decode_attention for them.
  * - No cudaMalloc, cudaFree or allocating library routine is called.
  * Errors: as pa_decode_attention, plus PA_ERR_UNSUPPORTED for the size limit.
  * ---------------------------------------------------------------------- */

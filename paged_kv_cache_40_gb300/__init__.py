@@ -177,7 +177,7 @@ def pa_decode_attention_fixed_scratch(q, k_pool, v_pool, block_table, seq_lens, 
     For a process that cannot allocate device memory on the decode path (all
     of it already belongs to its own KV pool and allocator, or cudaMalloc's
     device synchronisation is not acceptable there): the scratch is a fixed
-    4 MiB array inside libpa. Same inputs and result as pa_decode_attention;
+    16 MiB array inside libpa. Same inputs and result as pa_decode_attention;
     shapes needing more scratch raise PaError (PA_ERR_UNSUPPORTED). Calls that
     overlap on the GPU share that array and must not be issued.
     """
