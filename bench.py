@@ -301,11 +301,11 @@ def run_ours(args, world, rank, local):
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     flush_sink = torch.empty((), dtype=torch.int64, device=dev)
-    launches_per_step = (1 if len(plan.cow_pairs) else 0) + 2
+    launches_per_step = (1 if len(plan.cow_pairs) else 0) + 1 + DecodeBatchRunner.ATTEND_LAUNCHES
 
     def flush():
         flush_w.fill_(1)
-        torch.sum(flush_r, out=flush_sink)
+        torch.sum(flush_r, dim=0, out=flush_sink)
 
     for _ in range(args.warmup):
         flush()

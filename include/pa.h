@@ -145,9 +145,11 @@ PA_API pa_status pa_copy_blocks(pa_half* k_pool, pa_half* v_pool,
  *   K[t], V[t] = pool[block_table[i][t / block_size]][t % block_size][kv]
  *   out[i][h] = sum_t softmax_t(scale * q[i][h] . K[t]) V[t],  t < seq_lens[i]
  * computed in fp32 (max-subtracted online softmax), rounded once to fp16.
- * A sequence of length 0 gets an all-zero output. Long sequences are split
- * into partitions of `partition_tokens` tokens whose partial results are
- * merged on the device (log-sum-exp); the caller sees one result.
+ * A sequence of length 0 gets an all-zero output. The block stream of the
+ * batch is cut into equal chunks, one per CTA, so a sequence may be split
+ * across CTAs; the partial results of a split sequence are merged on the
+ * device (log-sum-exp) by the last CTA to finish one of its chunks; the
+ * caller sees one result.
  *
  * q            device [num_seqs][num_q_heads][head_dim] fp16
  * k_pool, v_pool  device pools (read only)
@@ -159,20 +161,29 @@ PA_API pa_status pa_copy_blocks(pa_half* k_pool, pa_half* v_pool,
  * scale        softmax scale (typically 1/sqrt(head_dim))
  * out          device [num_seqs][num_q_heads][head_dim] fp16 (written)
  * workspace    device scratch of >= pa_decode_workspace_bytes(...) bytes,
- *              16-byte aligned, owned by the caller. It starts with
- *              num_seqs*num_kv_heads int32 arrival counters that must be zero
- *              before the first call (pa_decode_workspace_init, or any zero
- *              fill of the whole buffer); every call that completes without a
- *              device error leaves them zero again. The rest holds fp32
- *              partial results of split sequences. Calls sharing one
- *              workspace must not overlap on the device.
- * partition_tokens  tokens per split; 0 = the library default (256). Must be
- *              a multiple of block_size and at most 32*block_size.
+ *              16-byte aligned, owned by the caller. It holds an arrival
+ *              counter per (sequence, KV head) and the fp32 partial results
+ *              of split sequences. It needs no initialisation: each counter
+ *              word carries a tag unique to the call that wrote it, and words
+ *              with another tag count as empty. Calls sharing one workspace
+ *              must not overlap on the device.
+ * partition_tokens  0 = chunks as equal as the grid allows (the default);
+ *              otherwise a positive multiple of block_size capping the
+ *              tokens of one chunk (more, shorter chunks: a CTA then streams
+ *              several).
+ * The call enqueues one kernel on `stream` (launched as a programmatic
+ * dependent: its prologue, which reads only seq_lens, may overlap the end of
+ * the previous kernel on the stream).
  * Supported shapes: head_dim in {64, 128}; block_size in {8, 16, 32};
  * num_q_heads / num_kv_heads in {1, 2, 4, 8}; num_seqs <= 16384.
  * Errors: PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED (shape outside the list, or
  *         a device other than sm_103), PA_ERR_CUDA.
  * ---------------------------------------------------------------------- */
+/* Bytes of workspace pa_decode_attention needs for this shape (0 if the
+ * shape is invalid or unsupported). pa_decode_workspace_init zero-fills the
+ * counters at the start of a workspace (num_seqs*num_kv_heads*8 bytes); the
+ * attention call does not require it and it is kept for callers that clear
+ * workspaces explicitly. */
 PA_API size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads,
                                  int num_kv_heads, int head_dim,
                                  int block_size, int max_blocks_per_seq,
@@ -210,10 +221,10 @@ PA_API pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool,
  * - The first call on a device resolves the array's device address (once per
  *   device, with that device current); make that first call before any stream
  *   capture.
- * - Every call uses the same array and clears its counters on `stream` before
- *   the kernel runs; calls that overlap on the GPU (other streams, other host
- *   threads) race on it and must not be issued.
- * - Shapes whose scratch would exceed 16 MiB (4 bytes per (sequence, KV
+ * - Every call uses the same array (its counters need no clearing, as in
+ *   pa_decode_attention); calls that overlap on the GPU (other streams,
+ *   other host threads) race on it and must not be issued.
+ * - Shapes whose scratch would exceed 16 MiB (8 bytes per (sequence, KV
  *   head), plus two partial results of G x (head_dim + 2) floats per CTA of
  *   the grid and per KV head a CTA streams, up to 8) are refused with
  *   PA_ERR_UNSUPPORTED; use pa_decode_attention for them.

@@ -171,6 +171,20 @@ pa_status pa_append_kv(const pa_half* k_new, const pa_half* v_new, pa_half* k_po
   if (pa_status s = pa::current_device(&dev)) return s;
   int32_t* err = pa::device_error_word();
   if (!err) return PA_ERR_CUDA;
+  {
+    // Same shared-memory carveout as the attention kernel that usually
+    // follows, so its CTAs can start on SMs this kernel still occupies.
+    static std::mutex mu;
+    static bool set[64] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (!set[dev.device]) {
+      cudaError_t e = cudaFuncSetAttribute(append_kv_kernel,
+                                           cudaFuncAttributePreferredSharedMemoryCarveout,
+                                           cudaSharedmemCarveoutMaxShared);
+      if (e != cudaSuccess) return pa::cuda_fail(e, "cudaFuncSetAttribute(append)");
+      set[dev.device] = true;
+    }
+  }
   const int row_vecs = num_kv_heads * head_dim / 8;
   append_kv_kernel<<<num_tokens, kAppendThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       reinterpret_cast<const uint4*>(k_new), reinterpret_cast<const uint4*>(v_new),

@@ -22,10 +22,15 @@
 //     CTAs): every CTA streams the same number of blocks. A segment inside one
 //     chunk is finished there and each warp writes its head's output straight
 //     from registers. A segment cut by chunk boundaries leaves one partial
-//     result per (chunk, head); the last warp to finish a head (an atomic
-//     arrival counter with acquire-release order, never a spin) merges that
-//     head's partials with the log-sum-exp rule. A chunk has at most two cut
-//     segments (its first and its last).
+//     result per (chunk, head); the last warp to finish a head merges that
+//     head's partials with the log-sum-exp rule. It learns that it is last
+//     from an arrival counter per (sequence, KV head), taken with a
+//     compare-and-swap, never a spin: the counter word carries a tag unique
+//     to the call next to the count, so a word left by an earlier call (or
+//     never written) counts as zero arrivals and the workspace needs no
+//     clearing. A chunk has at most two cut pieces, its first and its last;
+//     each CTA streams them before the uncut segments in between, so most
+//     merges happen while the other CTAs are still streaming.
 //   * Warp specialisation. A producer warp walks the CTA's chunk, loads the
 //     block-table entries of the next 32 blocks while it issues the current
 //     ones, and moves K and V with TMA into a ring of shared-memory stages:
@@ -35,6 +40,12 @@
 //     tensor-core fragment loads (ldmatrix) are free of bank conflicts. Every
 //     consumer warp reads every stage (its own head), so a stage is released
 //     after HG arrivals. q of each piece comes through a q slot the same way.
+//     A merge warp takes the cut pieces off the consumers' critical path: a
+//     consumer warp writes its partial record, arrives on a shared-memory
+//     barrier and goes on streaming; the merge warp, walking the same piece
+//     sequence, counts the arrivals of all HG heads at once (one lane each)
+//     and merges the heads whose partials are complete. Only the CTA's final
+//     piece is merged by the consumer warps themselves, in parallel.
 //   * Consumer math on tensor cores (mma.sync m16n8k16, fp16 in, fp32
 //     accumulate). Scores S = Q K^T with the G query heads as the M rows and
 //     8-token groups as N; the online softmax (base 2, running max and sum)
@@ -53,6 +64,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "pa_internal.h"
@@ -60,12 +72,14 @@
 namespace {
 
 constexpr int kMaxHG = 8;                          // KV heads per group = consumer warps
-constexpr int kMaxThreads = (kMaxHG + 1) * 32;     // consumers + producer
+constexpr int kMergeWarps = 3;                     // warps merging cut pieces off the stream
+constexpr int kMaxThreads = (kMaxHG + 1 + kMergeWarps) * 32;  // consumers, producer, mergers
+constexpr int kMsgSlots = 4;                       // cut pieces in flight to the merge warps
 constexpr int kMaxSeqs = 16384;
 constexpr int kMaxGrid = 1024;
 constexpr int kMaxStages = 16;
 constexpr int kRingBytesPerHead = 24 * 1024;       // ring size per KV head of the group
-constexpr int kMergeBatch = 16;                    // partial records folded per batch
+constexpr int kArrivalBits = 20;                   // low bits of a counter word: arrivals
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -108,14 +122,10 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
-// Atomic add with acquire-release semantics at GPU scope: this thread's earlier
-// global writes are visible to whoever later observes the new count, and
-// writes released by earlier adders are visible to this thread afterwards.
-__device__ __forceinline__ int atomic_add_acq_rel(int* ptr, int v) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v)
-               : "memory");
-  return old;
+// Release/acquire fence at GPU scope (orders this thread's earlier and later
+// memory operations around a relaxed atomic).
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -162,7 +172,9 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 // taken by lane 0 and broadcast, so the result is warp-uniform. Returns false
 // if the phase does not complete within the time limit (the CTA is then
 // flagged as aborted and PA_DEVERR_TIMEOUT recorded once) or if the CTA was
-// already aborted.
+// already aborted. A warp that is not latency critical passes kSleepNs > 0 to
+// sleep between polls and leave the issue slots to the warps that are.
+template <unsigned kSleepNs = 0>
 __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity,
                                                 volatile int* abort_flag, int32_t* err) {
   const int lane = threadIdx.x & 31;
@@ -170,6 +182,7 @@ __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity,
   for (int iter = 0;; ++iter) {
     const bool done = mbar_try_wait(bar, parity);
     if (__all_sync(0xffffffffu, done)) return true;
+    if (kSleepNs > 0) __nanosleep(kSleepNs);
     int give_up = 0;
     if (lane == 0) {
       if (iter == 0) {
@@ -212,21 +225,22 @@ struct Shape {
   static constexpr int OFF_EMPTY = OFF_FULL + kMaxStages * 8;
   static constexpr int OFF_QFULL = OFF_EMPTY + kMaxStages * 8;
   static constexpr int OFF_QEMPTY = OFF_QFULL + 8;
-  static constexpr int OFF_FLAGS = OFF_QEMPTY + 8;  // 32 ints, see kFlag*
+  static constexpr int OFF_MFULL = OFF_QEMPTY + 8;              // [kMsgSlots]
+  static constexpr int OFF_MEMPTY = OFF_MFULL + kMsgSlots * 8;  // [kMsgSlots]
+  static constexpr int OFF_FLAGS = OFF_MEMPTY + kMsgSlots * 8;  // 32 ints, see kFlag*
   static constexpr int FIXED = OFF_FLAGS + 128;
   static int stage_bytes(int hg) { return 2 * NHALF * hg * TS * 128; }
   // then, from the next 1 KB-aligned address (the swizzle pattern is a
-  // function of address bits 7..9): ring, q slot, merge scratch, prefix
+  // function of address bits 7..9): ring, q slot, prefix
   static size_t smem_bytes(int hg, int nst, int num_seqs) {
     return static_cast<size_t>(FIXED) + 1024 + static_cast<size_t>(nst) * stage_bytes(hg) +
-           static_cast<size_t>(hg) * G * D * 2 + static_cast<size_t>(hg) * kMergeBatch * G * 2 * 4 +
-           static_cast<size_t>(num_seqs + 1) * 4;
+           static_cast<size_t>(hg) * G * D * 2 + static_cast<size_t>(num_seqs + 1) * 4;
   }
 };
 
 // int flags in shared memory
 constexpr int kFlagAbort = 0;   // set when a bounded wait gave up
-constexpr int kFlagWsum = 8;    // [9] warp sums of the prefix scan
+constexpr int kFlagWsum = 8;    // [12] warp sums of the prefix scan
 constexpr int kFlagQLen = 24;   // sequence length of the piece in the q slot
 
 struct DecodeParams {
@@ -236,8 +250,9 @@ struct DecodeParams {
   const int32_t* block_table;
   const int32_t* seq_lens;
   __half* out;
-  int32_t* counters;  // [S][Hkv] arrival counters of cut segments
-  float* records;     // [2 * max_chunks][HG][rec_floats(G, D)] partials of cut segments
+  float* records;  // [2 * max_chunks][HG][rec_floats(G, D)] partials of cut segments
+  unsigned long long* counters;  // [num_seqs][num_kv_heads] (tag << kArrivalBits) | arrivals
+  unsigned long long tag;        // this call's tag, nonzero, < 2^(64 - kArrivalBits)
   int32_t* err;
   int num_seqs;
   int num_q_heads;
@@ -256,6 +271,62 @@ __device__ __forceinline__ int clamp_len(int L, int cap, int32_t* err) {
     L = L < 0 ? 0 : cap;
   }
   return L;
+}
+
+// Blocks per sequence -> exclusive prefix sum pfx[0..S] in shared memory,
+// computed by all threads of the block (wsum: one int per warp). Lengths
+// outside [0, cap] are clamped and reported.
+__device__ __forceinline__ void block_prefix(int* pfx, int* wsum, const int32_t* seq_lens, int S,
+                                             int bs, int cap, int32_t* err) {
+  const int tid = threadIdx.x, nthreads = blockDim.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < S; i += nthreads) {
+    const int L = clamp_len(__ldg(seq_lens + i), cap, err);
+    pfx[i + 1] = (L + bs - 1) / bs;
+  }
+  if (tid == 0) pfx[0] = 0;
+  __syncthreads();
+  const int per = (S + nthreads - 1) / nthreads;
+  const int lo = min(S, tid * per), hi = min(S, lo + per);
+  int sum = 0;
+  for (int i = lo; i < hi; ++i) sum += pfx[i + 1];
+  int incl = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  int run = incl - sum;
+  for (int w = 0; w < warp; ++w) run += wsum[w];
+  for (int i = lo; i < hi; ++i) {
+    run += pfx[i + 1];
+    pfx[i + 1] = run;
+  }
+  __syncthreads();
+}
+
+// The block stream cut into chunks: one per CTA (or of at most cap_blocks
+// blocks each, a CTA then taking every gridDim.x-th chunk).
+struct Geometry {
+  long long total, chunk, nchunks;
+};
+__device__ __forceinline__ Geometry chunk_geometry(long long total, int grid, int cap_blocks) {
+  Geometry g;
+  g.total = total;
+  g.chunk = (total + grid - 1) / grid;
+  if (cap_blocks > 0 && g.chunk > cap_blocks) g.chunk = cap_blocks;
+  if (g.chunk < 1) g.chunk = 1;
+  g.nchunks = (total + g.chunk - 1) / g.chunk;
+  return g;
+}
+
+// Record of chunk cc for a segment starting at stream index s0 whose first
+// chunk is c_first: slot 0 if the segment covers the chunk's start (the
+// chunk's first piece), slot 1 if it begins inside the chunk.
+__device__ __forceinline__ long long record_index(long long cc, long long c_first, long long s0,
+                                                  long long chunk, int hg, int w) {
+  return (2 * cc + ((cc == c_first && s0 > cc * chunk) ? 1 : 0)) * hg + w;
 }
 
 // Position in the block stream -> (sequence, head group, block within segment).
@@ -292,88 +363,164 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// One warp merges the partial records of a cut segment's head and writes its
-// fp16 output. Record i is `recs + rec_of(i) * rec_floats(G, D)`: acc [G][D],
-// then (max, sum) per head. Records are folded in batches with the online
-// log-sum-exp rule: the (max, sum) pairs of a batch are staged in shared
-// memory by the lanes at once, then every lane streams its float4 slices of
-// the accumulators with independent loads.
-template <int D, int G, typename RecOf>
-__device__ __forceinline__ void merge_records(const float* recs, int E, RecOf rec_of,
-                                              float* scratch, __half* out_row) {
-  constexpr int NV4 = G * D / 4;              // float4 slices of one accumulator
-  constexpr int PER = (NV4 + 31) / 32;        // slices per lane
-  constexpr int RS = rec_floats(G, D);        // floats per record (16-byte multiple)
-  const int lane = threadIdx.x & 31;
-  float M[G], Ls[G];
-  float4 A[PER];
-#pragma unroll
-  for (int gg = 0; gg < G; ++gg) {
-    M[gg] = -INFINITY;
-    Ls[gg] = 0.f;
+// Pieces of chunk c in the order a CTA streams them: the piece at the chunk's
+// start, then the piece at its end if that one's segment runs past the chunk,
+// then the uncut segments in between. Both cut pieces (whose partials other
+// chunks wait for) are thus finished early. Producer and consumers walk the
+// same sequence.
+struct Walk {
+  long long c;       // chunk
+  long long x0, xe;  // chunk [x0, xe) of the block stream
+  long long x1;      // end of the first piece
+  long long xl;      // start of the trailing cut piece (xe if there is none)
+  long long xm;      // next uncut segment
+  int phase;         // 0: first piece next, 1: trailing cut piece next, 2: middle
+};
+
+__device__ __forceinline__ void walk_begin(Walk& wk, long long c, const Geometry& geo,
+                                           const int* pfx, int S, int nhg) {
+  wk.c = c;
+  wk.phase = 0;
+  if (c >= geo.nchunks) return;
+  wk.x0 = c * geo.chunk;
+  wk.xe = min(geo.total, wk.x0 + geo.chunk);
+  const Cursor a = locate(wk.x0, pfx, S, nhg);
+  wk.x1 = min(a.seg_start + a.nb, wk.xe);
+  wk.xl = wk.xe;
+  if (wk.x1 < wk.xe) {
+    const Cursor b = locate(wk.xe - 1, pfx, S, nhg);
+    if (b.seg_start + b.nb > wk.xe) wk.xl = b.seg_start;
   }
-#pragma unroll
-  for (int k = 0; k < PER; ++k) A[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int base = 0; base < E; base += kMergeBatch) {
-    const int nb = min(kMergeBatch, E - base);
-    if (lane < nb) {
-      const float* rp = recs + rec_of(base + lane) * RS + G * D;
-#pragma unroll
-      for (int gg = 0; gg < G; ++gg) {
-        scratch[(lane * G + gg) * 2] = __ldcg(rp + 2 * gg);
-        scratch[(lane * G + gg) * 2 + 1] = __ldcg(rp + 2 * gg + 1);
+  wk.xm = wk.x1;
+}
+
+// Next piece of the walk (cursor at its first block, n blocks), moving on to
+// the CTA's next chunk (c + stride) when this one is done. False at the end.
+__device__ __forceinline__ bool walk_next(Walk& wk, const Geometry& geo, long long stride,
+                                          const int* pfx, int S, int nhg, Cursor& cur, int& n) {
+  while (wk.c < geo.nchunks) {
+    if (wk.phase == 0) {
+      wk.phase = 1;
+      cur = locate(wk.x0, pfx, S, nhg);
+      n = static_cast<int>(wk.x1 - wk.x0);
+      return true;
+    }
+    if (wk.phase == 1) {
+      wk.phase = 2;
+      if (wk.xl < wk.xe) {
+        cur = locate(wk.xl, pfx, S, nhg);
+        n = static_cast<int>(wk.xe - wk.xl);
+        return true;
       }
     }
-    __syncwarp();
-    float rescale[G];
-#pragma unroll
-    for (int gg = 0; gg < G; ++gg) {
-      float Mb = -INFINITY;
-      for (int r = 0; r < nb; ++r) Mb = fmaxf(Mb, scratch[(r * G + gg) * 2]);
-      const float Mn = fmaxf(M[gg], Mb);
-      const float mu = Mn == -INFINITY ? 0.f : Mn;
-      rescale[gg] = fast_exp2(M[gg] - mu);
-      float add = 0.f;
-      for (int r = 0; r < nb; ++r)
-        add += scratch[(r * G + gg) * 2 + 1] * fast_exp2(scratch[(r * G + gg) * 2] - mu);
-      Ls[gg] = Ls[gg] * rescale[gg] + add;
-      M[gg] = Mn;
+    if (wk.xm < wk.xl) {
+      cur = locate(wk.xm, pfx, S, nhg);
+      n = static_cast<int>(min(static_cast<long long>(cur.nb - cur.j), wk.xl - wk.xm));
+      wk.xm += n;
+      return true;
     }
+    walk_begin(wk, wk.c + stride, geo, pfx, S, nhg);
+  }
+  return false;
+}
+
+// Counts one arrival of a cut segment's head on its tagged counter word and
+// returns true for the arrival that completes the count (E arrivals), which
+// also puts the word back to zero so that a later call, even one with the
+// same tag (a replayed launch), starts from no arrivals. A word whose tag is
+// not this call's is stale and counts as zero. Each compare-and-swap starts
+// from a guess of the word: `guess_last` guesses that this is the last
+// arrival (E - 1 arrivals so far), otherwise that it is the first (a zero
+// word). A failed attempt returns the current word, and every failure means
+// another arrival succeeded, so at most E + 1 attempts are made (false, with
+// PA_DEVERR_TIMEOUT, if that were ever exceeded).
+__device__ __forceinline__ bool arrive_last(unsigned long long* word, unsigned long long tag,
+                                            unsigned E, bool guess_last, int32_t* err) {
+  constexpr unsigned long long kCountMask = (1ull << kArrivalBits) - 1;
+  unsigned long long cur = guess_last ? (tag << kArrivalBits) | (E - 1) : 0ull;
+  for (unsigned i = 0; i <= E + 1; ++i) {
+    const unsigned long long seen = (cur >> kArrivalBits) == tag ? (cur & kCountMask) : 0ull;
+    const bool last = seen + 1 == E;
+    const unsigned long long want = last ? 0ull : (tag << kArrivalBits) | (seen + 1);
+    const unsigned long long got = atomicCAS(word, cur, want);
+    if (got == cur) return last;
+    cur = got;
+  }
+  atomicOr(err, PA_DEVERR_TIMEOUT);
+  return false;
+}
+
+// One warp merges the E partial records of one KV head of a cut segment with
+// the log-sum-exp rule and writes that head's G fp16 output rows. Record i is
+// `recs + rec_of(i) * rec_floats(G, D)`: acc [G][D], then (max, sum) per
+// head. Lane l owns the float4 slices l, l + 32, ... of the accumulator; a
+// slice lies inside one query head, whose (max, sum) the lane reads with it.
+// All loads of a batch of records are issued before any is used, so a merge
+// costs about one L2 round trip per batch.
+template <int D, int G, typename RecOf>
+__device__ __forceinline__ void merge_partials(const float* recs, int E, RecOf rec_of,
+                                               __half* out_row) {
+  constexpr int NV4 = G * D / 4;         // float4 slices of one accumulator
+  constexpr int PER = (NV4 + 31) / 32;   // slices per lane
+  // records per batch: as many as registers allow without spilling
+  constexpr int KB = PER == 1 ? 6 : PER == 2 ? 4 : PER == 4 ? 3 : 1;
+  constexpr int RS = rec_floats(G, D);   // floats per record (16-byte multiple)
+  const int lane = threadIdx.x & 31;
+  float M[PER], Ls[PER];
+  float4 A[PER];
 #pragma unroll
-    for (int k = 0; k < PER; ++k) {
-      const int i = lane + 32 * k;
-      const float f = i < NV4 ? rescale[(i * 4) / D] : 0.f;
-      A[k].x *= f;
-      A[k].y *= f;
-      A[k].z *= f;
-      A[k].w *= f;
-    }
-#pragma unroll 4
-    for (int r = 0; r < nb; ++r) {
-      const float4* rp = reinterpret_cast<const float4*>(recs + rec_of(base + r) * RS);
+  for (int k = 0; k < PER; ++k) {
+    M[k] = -INFINITY;
+    Ls[k] = 0.f;
+    A[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int base = 0; base < E; base += KB) {
+    float4 v[KB][PER];
+    float2 ml[KB][PER];
+#pragma unroll
+    for (int r = 0; r < KB; ++r) {
+      const bool have = base + r < E;
+      const float* rp = recs + (have ? rec_of(base + r) : 0) * RS;
 #pragma unroll
       for (int k = 0; k < PER; ++k) {
         const int i = lane + 32 * k;
-        if (i < NV4) {
-          const int gg = (i * 4) / D;
-          const float mu = M[gg] == -INFINITY ? 0.f : M[gg];
-          const float w = fast_exp2(scratch[(r * G + gg) * 2] - mu);
-          const float4 v = __ldcg(rp + i);
-          A[k].x += v.x * w;
-          A[k].y += v.y * w;
-          A[k].z += v.z * w;
-          A[k].w += v.w * w;
+        if (have && i < NV4) {
+          v[r][k] = __ldcg(reinterpret_cast<const float4*>(rp) + i);
+          ml[r][k] = __ldcg(reinterpret_cast<const float2*>(rp + G * D) + (i * 4) / D);
+        } else {
+          v[r][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          ml[r][k] = make_float2(-INFINITY, 0.f);
         }
       }
     }
-    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      float mb = M[k];
+#pragma unroll
+      for (int r = 0; r < KB; ++r) mb = fmaxf(mb, ml[r][k].x);
+      const float mu = mb == -INFINITY ? 0.f : mb;
+      const float f = fast_exp2(M[k] - mu);
+      float4 a = make_float4(A[k].x * f, A[k].y * f, A[k].z * f, A[k].w * f);
+      float l = Ls[k] * f;
+#pragma unroll
+      for (int r = 0; r < KB; ++r) {
+        const float wr = fast_exp2(ml[r][k].x - mu);
+        a.x += v[r][k].x * wr;
+        a.y += v[r][k].y * wr;
+        a.z += v[r][k].z * wr;
+        a.w += v[r][k].w * wr;
+        l += ml[r][k].y * wr;
+      }
+      A[k] = a;
+      Ls[k] = l;
+      M[k] = mb;
+    }
   }
 #pragma unroll
   for (int k = 0; k < PER; ++k) {
     const int i = lane + 32 * k;
     if (i < NV4) {
-      const int gg = (i * 4) / D;
-      const float inv = Ls[gg] > 0.f ? 1.f / Ls[gg] : 0.f;
+      const float inv = Ls[k] > 0.f ? 1.f / Ls[k] : 0.f;
       __half2* o = reinterpret_cast<__half2*>(out_row + i * 4);
       o[0] = __floats2half2_rn(A[k].x * inv, A[k].y * inv);
       o[1] = __floats2half2_rn(A[k].z * inv, A[k].w * inv);
@@ -396,16 +543,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   uint64_t* empty_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_EMPTY);
   uint64_t* qfull_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_QFULL);
   uint64_t* qempty_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_QEMPTY);
+  uint64_t* mfull_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_MFULL);
+  uint64_t* mempty_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_MEMPTY);
   int* flags = reinterpret_cast<int*>(smem + SH::OFF_FLAGS);
   volatile int* abort_flag = flags + kFlagAbort;
   const uint32_t smem_base = smem_addr(smem);
   unsigned char* ring = smem + (((smem_base + SH::FIXED + 1023u) & ~1023u) - smem_base);
   unsigned char* qslot = ring + static_cast<size_t>(NST) * STAGE;
-  float* scratch_all = reinterpret_cast<float*>(qslot + HG * G * D * 2);
-  int* pfx = reinterpret_cast<int*>(scratch_all + HG * kMergeBatch * G * 2);
+  int* pfx = reinterpret_cast<int*>(qslot + HG * G * D * 2);
 
   const int tid = threadIdx.x;
-  const int nthreads = blockDim.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int S = p.num_seqs;
@@ -420,68 +567,61 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     }
     mbar_init(smem_addr(qfull_bar), 1);
     mbar_init(smem_addr(qempty_bar), HG);
+    for (int m = 0; m < kMsgSlots; ++m) {
+      mbar_init(smem_addr(&mfull_bar[m]), HG);  // one arrival per consumer warp
+      mbar_init(smem_addr(&mempty_bar[m]), kMergeWarps);
+    }
     flags[kFlagAbort] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
 
   // ---- blocks per sequence, exclusive prefix sum in shared memory ----
-  for (int i = tid; i < S; i += nthreads) {
-    const int L = clamp_len(__ldg(p.seq_lens + i), cap, p.err);
-    pfx[i + 1] = (L + BS - 1) / BS;
-  }
-  if (tid == 0) pfx[0] = 0;
-  __syncthreads();
-  {
-    const int per = (S + nthreads - 1) / nthreads;
-    const int lo = min(S, tid * per), hi = min(S, lo + per);
-    int sum = 0;
-    for (int i = lo; i < hi; ++i) sum += pfx[i + 1];
-    int incl = sum;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += v;
-    }
-    int* wsum = flags + kFlagWsum;
-    if (lane == 31) wsum[warp] = incl;
-    __syncthreads();
-    int run = incl - sum;
-    for (int w = 0; w < warp; ++w) run += wsum[w];
-    for (int i = lo; i < hi; ++i) {
-      run += pfx[i + 1];
-      pfx[i + 1] = run;
-    }
-  }
-  __syncthreads();
+  block_prefix(pfx, flags + kFlagWsum, p.seq_lens, S, BS, cap, p.err);
+  const Geometry geo = chunk_geometry(static_cast<long long>(pfx[S]) * NHG, gridDim.x, p.cap_blocks);
+  const long long chunk = geo.chunk;
 
-  const long long total = static_cast<long long>(pfx[S]) * NHG;  // blocks in the stream
-  long long chunk = (total + gridDim.x - 1) / gridDim.x;
-  if (p.cap_blocks > 0 && chunk > p.cap_blocks) chunk = p.cap_blocks;
-  if (chunk < 1) chunk = 1;
-  const long long nchunks = (total + chunk - 1) / chunk;
+  // The producer's first piece, and an L2 prefetch of its table entries and
+  // q rows: a prefetch may run before the wait below, because L2 stays
+  // coherent with whatever the previous kernel writes.
+  Walk pwk;
+  Cursor pcur0{};
+  int pn0 = 0;
+  bool phave = false;
+  if (warp == HG) {
+    walk_begin(pwk, blockIdx.x, geo, pfx, S, NHG);
+    phave = walk_next(pwk, geo, gridDim.x, pfx, S, NHG, pcur0, pn0);
+    if (phave) {
+      const int32_t* trow = p.block_table + static_cast<long long>(pcur0.seq) * p.max_blocks + pcur0.j;
+      if (lane < min(32, pn0)) asm volatile("prefetch.global.L2 [%0];" ::"l"(trow + lane));
+      const char* qrow = reinterpret_cast<const char*>(
+          p.q + (static_cast<long long>(pcur0.seq) * p.num_q_heads +
+                 static_cast<long long>(pcur0.hg) * HG * G) * D);
+      for (int off = lane * 128; off < HG * G * D * 2; off += 32 * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow + off));
+    }
+  }
 
   // Everything above reads only seq_lens. The pool, q and the table may still
   // be written by the kernel launched just before this one on the stream
   // (programmatic dependent launch): wait for it before touching them.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // a dependent kernel launched after this one may start its own prologue
+  asm volatile("griddepcontrol.launch_dependents;");
 
   if (warp == HG) {
     // =========================== producer warp ===========================
-    // The walk visits the CTA's chunks, their pieces, and each piece in groups
-    // of up to 32 blocks. The table entries (one per lane) and the sequence
-    // length of the next group are loaded while the current group is issued,
-    // so no piece boundary waits on a global load.
+    // The walk visits the CTA's pieces, each in groups of up to 32 blocks.
+    // The table entries (one per lane) and the sequence length of the next
+    // group are loaded while the current group is issued, so no piece
+    // boundary waits on a global load.
     uint32_t g = 0;   // ring sequence number (stages)
     uint32_t pc = 0;  // piece number
-    long long c = blockIdx.x;
-    long long x = c * chunk, xe = min(total, x + chunk);
-    bool have = c < nchunks && x < xe;
-    Cursor cur{};
-    int n = 0, j0 = 0;
+    Walk wk = pwk;
+    Cursor cur = pcur0;
+    int n = pn0, j0 = 0;
     int phys_next = 0, len_next = 0;
+    bool have = phave;
     if (have) {
-      cur = locate(x, pfx, S, NHG);
-      n = static_cast<int>(min(static_cast<long long>(cur.nb - cur.j), xe - x));
       len_next = min(max(__ldg(p.seq_lens + cur.seq), 0), cap);
       phys_next = lane < min(32, n)
                       ? __ldg(p.block_table + static_cast<long long>(cur.seq) * p.max_blocks +
@@ -495,18 +635,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       // advance to the next group and start loading its table entries
       j0 += 32;
       if (j0 >= n) {
-        x += n;
-        if (x >= xe) {
-          c += gridDim.x;
-          have = c < nchunks;
-          if (have) {
-            x = c * chunk;
-            xe = min(total, x + chunk);
-          }
-        }
+        have = walk_next(wk, geo, gridDim.x, pfx, S, NHG, cur, n);
         if (have) {
-          cur = locate(x, pfx, S, NHG);
-          n = static_cast<int>(min(static_cast<long long>(cur.nb - cur.j), xe - x));
           j0 = 0;
           len_next = min(max(__ldg(p.seq_lens + cur.seq), 0), cap);
         }
@@ -587,12 +717,64 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     return;
   }
 
+  if (warp > HG) {
+    // ============================= merge warps ============================
+    // Each walks the CTA's pieces like the consumers. For every cut piece that
+    // is not the CTA's last, it waits until all consumer warps have written
+    // their records (message m in slot m % kMsgSlots), counts one arrival for
+    // each of its heads (head h belongs to merge warp h % kMergeWarps, lane h
+    // counts it) and merges each of its heads whose arrivals are complete.
+    const int mw = warp - HG - 1;
+    Walk wk;
+    walk_begin(wk, blockIdx.x, geo, pfx, S, NHG);
+    Cursor cur{};
+    int n = 0;
+    bool have = walk_next(wk, geo, gridDim.x, pfx, S, NHG, cur, n);
+    uint32_t mc = 0;
+    while (have) {
+      const Cursor pcur = cur;
+      const int pn = n;
+      have = walk_next(wk, geo, gridDim.x, pfx, S, NHG, cur, n);
+      const bool cut = pcur.j > 0 || pcur.j + pn < pcur.nb;
+      if (!cut || !have) continue;  // uncut, or the CTA's last piece (merged by the consumers)
+      const int ms = static_cast<int>(mc % kMsgSlots);
+      if (!warp_wait_phase<256>(smem_addr(&mfull_bar[ms]), (mc / kMsgSlots) & 1, abort_flag,
+                                p.err))
+        break;
+      // the consumers' records (ordered before their arrivals on the barrier)
+      // become visible to the whole GPU before any arrival is counted
+      fence_acq_rel_gpu();
+      if (lane == 0) mbar_arrive(smem_addr(&mempty_bar[ms]));
+      ++mc;
+      const long long s0 = pcur.seg_start;
+      const long long c_first = s0 / chunk, c_last = (s0 + pcur.nb - 1) / chunk;
+      const int E = static_cast<int>(c_last - c_first + 1);
+      unsigned long long* words =
+          p.counters + static_cast<long long>(pcur.seq) * Hkv + static_cast<long long>(pcur.hg) * HG;
+      const bool mine = lane < HG && lane % kMergeWarps == mw;
+      const bool done =
+          mine && arrive_last(words + lane, p.tag, static_cast<unsigned>(E), false, p.err);
+      unsigned last = __ballot_sync(0xffffffffu, done);
+      if (last) fence_acq_rel_gpu();  // acquire: the other chunks' records are visible
+      while (last) {
+        const int h = __ffs(last) - 1;
+        last &= last - 1;
+        auto rec_of = [&](int i) -> long long {
+          return record_index(c_first + i, c_first, s0, chunk, HG, h);
+        };
+        __half* out_row = p.out + (static_cast<long long>(pcur.seq) * p.num_q_heads +
+                                   static_cast<long long>(pcur.hg * HG + h) * G) * D;
+        merge_partials<D, G>(p.records, E, rec_of, out_row);
+      }
+    }
+    return;
+  }
+
   // ============================ consumer warps ============================
   // Warp w owns KV head (group * HG + w) and its G query heads.
   const int w = warp;
   const int gid = lane >> 2;  // mma group id: row of A / column of B
   const int tig = lane & 3;   // thread in group
-  float* scratch = scratch_all + w * kMergeBatch * G * 2;
 
   // zero outputs of empty sequences (this CTA's share)
   for (int i = blockIdx.x; i < S; i += gridDim.x) {
@@ -611,14 +793,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
   uint32_t g = 0;   // ring sequence number of the next stage
   uint32_t pc = 0;  // piece number
-  for (long long c = blockIdx.x; c < nchunks; c += gridDim.x) {
-    long long x = c * chunk;
-    const long long xe = min(total, x + chunk);
-    bool first_piece = true;
-    while (x < xe) {
-      const Cursor cur = locate(x, pfx, S, NHG);
-      const int n = static_cast<int>(min(static_cast<long long>(cur.nb - cur.j), xe - x));
+  uint32_t mc = 0;  // cut pieces handed to the merge warp
+  Walk wk;
+  walk_begin(wk, blockIdx.x, geo, pfx, S, NHG);
+  Cursor cur{};
+  int n = 0;
+  bool have = walk_next(wk, geo, gridDim.x, pfx, S, NHG, cur, n);
+  while (have) {
+    {
       const int kvh = cur.hg * HG + w;
+      const long long c = wk.c, x0 = wk.x0;  // the piece's chunk
 
       // ---- q and length of the piece ----
       uint32_t qa[SH::KSTEPS][2];  // A fragments a0/a2 per k-step; rows (heads) >= G are zero
@@ -754,6 +938,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       }
 
       // ---- piece finished: this warp holds its head's whole state ----
+      // (the walk moves on to the next piece once the results are stored)
+      Cursor ncur{};
+      int nn = 0;
+      bool more;
       l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
       l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
       const bool cut = cur.j > 0 || cur.j + n < cur.nb;
@@ -776,9 +964,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             out_row[h1 * D + d + 8] = __float2half_rn(o[mt][3] * i1);
           }
         }
+        more = walk_next(wk, geo, gridDim.x, pfx, S, NHG, ncur, nn);
       } else {
-        float* rec = p.records +
-                     ((2 * c + (first_piece ? 0 : 1)) * HG + w) * static_cast<long long>(SH::REC);
+        // cut segment: record this chunk's partial (slot 0 if the piece starts
+        // the chunk, else 1); the last of the segment's chunks to arrive merges
+        const long long s0 = cur.seg_start;
+        const int slot = s0 + cur.j == x0 ? 0 : 1;
+        float* rec = p.records + ((2 * c + slot) * HG + w) * static_cast<long long>(SH::REC);
 #pragma unroll
         for (int mt = 0; mt < SH::MT; ++mt) {
           const int d = mt * 16 + gid;
@@ -795,36 +987,56 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           rec[G * D + 2 * gid] = m_run;
           rec[G * D + 2 * gid + 1] = l_run;
         }
-        // chunks covering this segment: c_first .. c_last; the last to arrive merges
-        const long long s0 = cur.seg_start, s1 = cur.seg_start + cur.nb;
-        const long long c_first = s0 / chunk, c_last = (s1 - 1) / chunk;
-        const int expected = static_cast<int>(c_last - c_first + 1);
-        // every lane's record writes precede lane 0's release-add (the warp
-        // barrier orders them within the CTA, the release extends it to the GPU)
-        __syncwarp();
-        int* cnt = p.counters + static_cast<long long>(cur.seq) * Hkv + kvh;
-        int fin = 0;
-        if (lane == 0) {
-          __threadfence_block();
-          fin = atomic_add_acq_rel(cnt, 1) == expected - 1;
-        }
-        fin = __shfl_sync(0xffffffffu, fin, 0);
-        __syncwarp();  // orders every lane's record loads after lane 0's acquire
-        if (fin) {
-          auto rec_of = [&](int i) -> long long {
-            const long long cc = c_first + i;
-            return (2 * cc + ((cc == c_first && s0 > cc * chunk) ? 1 : 0)) * HG + w;
-          };
-          merge_records<D, G>(p.records, expected, rec_of, scratch, out_row);
-          if (lane == 0) atomicExch(cnt, 0);
+        more = walk_next(wk, geo, gridDim.x, pfx, S, NHG, ncur, nn);
+        if (more) {
+          // hand the arrival (and any merge) to the merge warps: the warp
+          // barrier orders every lane's record stores before lane 0's arrival,
+          // whose release makes them visible to the merge warps' acquire
+          if (mc >= kMsgSlots)
+            warp_wait_phase(smem_addr(&mempty_bar[mc % kMsgSlots]), ((mc / kMsgSlots) - 1) & 1,
+                            abort_flag, p.err);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&mfull_bar[mc % kMsgSlots]));
+          ++mc;
+        } else {
+          // The CTA's last piece: count the arrival here and merge if it
+          // completes the segment, which it usually does (the other chunks'
+          // pieces are mostly done). First try to claim the last arrival
+          // outright: a last arrival's record is read by no other warp, so it
+          // needs no release and the claim does not wait for its stores.
+          // Otherwise release the record and count the arrival as usual.
+          __syncwarp();  // the record's lanes, before any lane reads it back
+          const long long c_first = s0 / chunk, c_last = (s0 + cur.nb - 1) / chunk;
+          const int E = static_cast<int>(c_last - c_first + 1);
+          unsigned long long* word = p.counters + static_cast<long long>(cur.seq) * Hkv + kvh;
+          const unsigned long long claim = (p.tag << kArrivalBits) | static_cast<unsigned>(E - 1);
+          int done = 0;
+          if (lane == 0) done = atomicCAS(word, claim, 0ull) == claim;
+          done = __shfl_sync(0xffffffffu, done, 0);
+          if (!done) {
+            fence_acq_rel_gpu();  // release: the record is visible before the arrival
+            __syncwarp();
+            if (lane == 0) done = arrive_last(word, p.tag, static_cast<unsigned>(E), false, p.err);
+            done = __shfl_sync(0xffffffffu, done, 0);
+          }
+          if (done) {
+            // acquire: the other chunks' records are visible to this warp
+            fence_acq_rel_gpu();
+            auto rec_of = [&](int i) -> long long {
+              return record_index(c_first + i, c_first, s0, chunk, HG, w);
+            };
+            merge_partials<D, G>(p.records, E, rec_of, out_row);
+          }
         }
       }
-      x += n;
       ++pc;
-      first_piece = false;
+      cur = ncur;
+      n = nn;
+      have = more;
     }
   }
 }
+
 
 // --------------------------------------------------------------- host ---
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
@@ -845,17 +1057,28 @@ struct Layout {
   size_t counters = 0, records = 0, total = 0;
 };
 
-// Workspace: int32 arrival counters [S][Hkv], then two partial records per
-// chunk and KV head of the group.
+// Workspace: arrival counters (8 bytes per sequence and KV head), then two
+// partial records per chunk and KV head of the group (written by CTAs whose
+// chunk cuts a segment, read by the warp that merges it). No part of it needs
+// initialising: counter words carry the tag of the call that wrote them.
 Layout workspace_layout(int S, int Hq, int Hkv, int D, int MB, int cap_blocks) {
   Layout w;
   const int G = Hq / Hkv;
   const int hg = head_group(Hkv);
   const long long recs = 2 * max_chunks(S, Hkv / hg, MB, cap_blocks) * hg;
   w.counters = 0;
-  w.records = round256(static_cast<size_t>(S) * Hkv * 4);
+  w.records = round256(static_cast<size_t>(S) * Hkv * 8);
   w.total = w.records + round256(static_cast<size_t>(recs) * rec_floats(G, D) * 4);
   return w;
+}
+
+// Tag of the next decode call: unique within the process (2^44 values), never
+// zero, so a zero counter word always reads as "no arrivals".
+unsigned long long next_call_tag() {
+  static std::atomic<unsigned long long> counter{0};
+  constexpr unsigned long long kTagMask = (1ull << (64 - kArrivalBits)) - 1;
+  unsigned long long t = (counter.fetch_add(1, std::memory_order_relaxed) + 1) & kTagMask;
+  return t == 0 ? 1 : t;
 }
 
 // --- TMA descriptors of the pools -------------------------------------------
@@ -948,7 +1171,7 @@ pa_status launch_config(const pa::DeviceInfo& dev, int S, int Hkv, LaunchCfg* cf
   if (cfg->smem > dev.smem_optin)
     return pa::fail(PA_ERR_UNSUPPORTED, "pa_decode_attention: %zu bytes of shared memory needed",
                     cfg->smem);
-  cfg->threads = (cfg->hg + 1) * 32;
+  cfg->threads = (cfg->hg + 1 + kMergeWarps) * 32;
   static std::mutex mu;
   static bool attr_set[64] = {};
   struct OccEntry {
@@ -964,6 +1187,9 @@ pa_status launch_config(const pa::DeviceInfo& dev, int S, int Hkv, LaunchCfg* cf
     if (!attr_set[dev.device]) {
       cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(dev.smem_optin));
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
       if (e != cudaSuccess) return pa::cuda_fail(e, "cudaFuncSetAttribute");
       attr_set[dev.device] = true;
     }
@@ -1014,6 +1240,7 @@ pa_status launch_decode(DecodeParams prm, const pa::DeviceInfo& dev, cudaStream_
   cudaError_t e = cudaLaunchKernelEx(&lc, paged_decode_kernel<D, BS, G>, prm, kmap, vmap);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_decode_attention launch");
+
   return PA_OK;
 }
 
@@ -1073,6 +1300,13 @@ pa_status check_decode_shape(int S, int Hq, int Hkv, int D, int BS, int MB, int 
                     part_tokens);
   if (static_cast<long long>(MB) * BS > INT32_MAX)
     return pa::fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq * block_size exceeds int32");
+  // the chunks one sequence can span must fit the arrival count of a counter word
+  const long long cap = part_tokens / BS;
+  const long long span = cap > 0 ? (MB + cap - 1) / cap + 1 : kMaxGrid;
+  if (span >= (1ll << kArrivalBits))
+    return pa::fail(PA_ERR_UNSUPPORTED,
+                    "partition_tokens %d splits a sequence of %d blocks into too many chunks",
+                    part_tokens, MB);
   return PA_OK;
 }
 
@@ -1125,7 +1359,7 @@ pa_status pa_decode_workspace_init(void* workspace, size_t workspace_bytes, int 
   if (num_seqs < 0 || num_kv_heads <= 0)
     return pa::fail(PA_ERR_INVALID_ARG, "workspace_init: seqs=%d kv_heads=%d", num_seqs,
                     num_kv_heads);
-  const size_t need = static_cast<size_t>(num_seqs) * num_kv_heads * 4;
+  const size_t need = static_cast<size_t>(num_seqs) * num_kv_heads * 8;
   if (need == 0) return pa::ok();
   if (!workspace || workspace_bytes < need)
     return pa::fail(PA_ERR_INVALID_ARG, "workspace_init: %zu bytes < %zu", workspace_bytes, need);
@@ -1162,7 +1396,7 @@ static DecodeParams make_params(const pa_half* q, const pa_half* k_pool, const p
                                 const int32_t* block_table, const int32_t* seq_lens,
                                 int num_seqs, int num_q_heads, int num_kv_heads,
                                 int max_blocks_per_seq, int num_blocks, float scale, pa_half* out,
-                                unsigned char* ws, size_t records_offset, int cap_blocks) {
+                                unsigned char* ws, const Layout& lay, int cap_blocks) {
   DecodeParams prm;
   prm.q = reinterpret_cast<const __half*>(q);
   prm.k_pool = reinterpret_cast<const __half*>(k_pool);
@@ -1170,8 +1404,9 @@ static DecodeParams make_params(const pa_half* q, const pa_half* k_pool, const p
   prm.block_table = block_table;
   prm.seq_lens = seq_lens;
   prm.out = reinterpret_cast<__half*>(out);
-  prm.counters = reinterpret_cast<int32_t*>(ws);
-  prm.records = reinterpret_cast<float*>(ws + records_offset);
+  prm.records = reinterpret_cast<float*>(ws + lay.records);
+  prm.counters = reinterpret_cast<unsigned long long*>(ws + lay.counters);
+  prm.tag = next_call_tag();
   prm.err = nullptr;
   prm.num_seqs = num_seqs;
   prm.num_q_heads = num_q_heads;
@@ -1210,7 +1445,7 @@ pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool, const pa_
   if (pa_status s = pa::current_device(&dev)) return s;
   DecodeParams prm = make_params(q, k_pool, v_pool, block_table, seq_lens, num_seqs, num_q_heads,
                                  num_kv_heads, max_blocks_per_seq, num_blocks, scale, out,
-                                 static_cast<unsigned char*>(workspace), lay.records, cap_blocks);
+                                 static_cast<unsigned char*>(workspace), lay, cap_blocks);
   prm.err = pa::device_error_word();
   if (!prm.err) return PA_ERR_CUDA;
   const int G = num_q_heads / num_kv_heads;
@@ -1240,7 +1475,8 @@ pa_status pa_decode_attention_fixed_scratch(const pa_half* q, const pa_half* k_p
   if (pa_status s = launch_config_any(head_dim, block_size, G, dev, num_seqs, num_kv_heads, &cfg))
     return s;
   // scratch this call needs: arrival counters, then two partial records per
-  // chunk and KV head of the group
+  // chunk (one per CTA of this grid, or more with a partition cap) and KV
+  // head of the group
   const int cap_blocks = partition_tokens / block_size;
   long long chunks = cfg.grid;
   if (cap_blocks > 0) {
@@ -1249,9 +1485,12 @@ pa_status pa_decode_attention_fixed_scratch(const pa_half* q, const pa_half* k_p
     const long long capped = (blocks + cap_blocks - 1) / cap_blocks;
     if (capped > chunks) chunks = capped;
   }
-  const size_t counters = round256(static_cast<size_t>(num_seqs) * num_kv_heads * 4);
-  const size_t need = counters + static_cast<size_t>(2 * chunks) * cfg.hg *
-                                     rec_floats(G, head_dim) * sizeof(float);
+  Layout lay;
+  lay.counters = 0;
+  lay.records = round256(static_cast<size_t>(num_seqs) * num_kv_heads * 8);
+  lay.total = lay.records + static_cast<size_t>(2 * chunks) * cfg.hg *
+                                rec_floats(G, head_dim) * sizeof(float);
+  const size_t need = lay.total;
   if (need > kFixedScratchBytes)
     return pa::fail(PA_ERR_UNSUPPORTED,
                     "pa_decode_attention_fixed_scratch: this shape needs %zu bytes of scratch; "
@@ -1260,12 +1499,9 @@ pa_status pa_decode_attention_fixed_scratch(const pa_half* q, const pa_half* k_p
   unsigned char* ws = fixed_scratch_address(dev.device);
   if (!ws) return PA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the scratch keeps the previous call's contents: the counters must start at zero
-  cudaError_t e = cudaMemsetAsync(ws, 0, static_cast<size_t>(num_seqs) * num_kv_heads * 4, s);
-  if (e != cudaSuccess) return pa::cuda_fail(e, "pa_decode_attention_fixed_scratch memset");
   DecodeParams prm = make_params(q, k_pool, v_pool, block_table, seq_lens, num_seqs, num_q_heads,
-                                 num_kv_heads, max_blocks_per_seq, num_blocks, scale, out, ws,
-                                 counters, cap_blocks);
+                                 num_kv_heads, max_blocks_per_seq, num_blocks, scale, out, ws, lay,
+                                 cap_blocks);
   prm.err = pa::device_error_word();
   if (!prm.err) return PA_ERR_CUDA;
   pa_status st = head_dim == 64 ? dispatch_bs<64>(block_size, G, prm, dev, s)

@@ -107,12 +107,16 @@ class DecodeBatchRunner:
                             partition_tokens=self.partition_tokens, stream=stream)
         return self.out
 
+    # kernels one attend() enqueues (the attention kernel merges split
+    # sequences itself)
+    ATTEND_LAUNCHES = 1
+
     def run_step(self, stream=None):
         """copy-on-write copies (if any), append, attend. Returns the kernel
         launch count."""
         n = self.copy_and_append(stream)
         self.attend(stream)
-        return n + 1
+        return n + self.ATTEND_LAUNCHES
 
     def kv_bytes(self) -> int:
         """Algorithmic K+V bytes one attention launch reads."""

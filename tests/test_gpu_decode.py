@@ -173,8 +173,9 @@ def test_large_scores_stay_finite(pa):
 
 
 def test_workspace_reuse_and_repeat(pa):
-    """Split sequences leave the arrival counters at zero: repeated calls and
-    calls with other lengths on one workspace give the right results."""
+    """One workspace serves repeated calls and calls with other lengths: the
+    partial results of split sequences never leak from one call into the
+    next."""
     from paged_kv_cache_40_gb300 import alloc_workspace
     lens_a = [3000, 20, 1500]
     lens_b = [10, 2900, 700]
@@ -188,8 +189,16 @@ def test_workspace_reuse_and_repeat(pa):
         torch.cuda.synchronize()
         exp = oracle.decode_attention(q, kp, vp, table, lens, np.float32(0.0884))
         assert_close_attention(out.cpu().numpy(), exp, f"reuse {lens}")
-    counters = ws[: 3 * 2 * 4].view(torch.int32).cpu()
-    assert not counters.any()
+    # a completed call leaves every arrival counter word (8 bytes per sequence
+    # and KV head, at the start of the workspace) back at zero
+    assert not ws[: 3 * 2 * 8].view(torch.int64).cpu().any()
+    ws.fill_(255)                   # garbage in the workspace must not matter
+    lens = lens_b
+    out = pa.pa_decode_attention(dq, dk, dv, dt, d(np.asarray(lens, np.int32)), 0.0884,
+                                 workspace=ws)
+    torch.cuda.synchronize()
+    exp = oracle.decode_attention(q, kp, vp, table, lens, np.float32(0.0884))
+    assert_close_attention(out.cpu().numpy(), exp, "garbage workspace")
 
 
 def test_bad_block_id_is_reported_not_faulted(pa):

@@ -42,15 +42,18 @@ def test_decode_zero_sequences_is_a_no_op(libpa):
 
 def test_workspace_bytes(libpa):
     lib = libpa.lib()
+    # an 8-byte arrival counter per (sequence, KV head), then two partial
+    # records per chunk (at most 1024 chunks) and per KV head a CTA streams (8
+    # here), each G x (head_dim + 2) floats
     n = lib.pa_decode_workspace_bytes(64, 32, 8, 128, 16, 129, 0)
-    # arrival counters + two partial records per chunk (<= 2048 chunks),
-    # each G x (head_dim + 2) floats
-    assert n >= 64 * 8 * 4 + 2 * 2048 * 4 * 130 * 4
+    assert n >= 64 * 8 * 8 + 2 * 1024 * 8 * (4 * 130) * 4
     assert n % 256 == 0
     assert lib.pa_decode_workspace_bytes(64, 32, 8, 96, 16, 129, 0) == 0
-    # a per-chunk cap can need more records than the grid has CTAs
+    # a per-chunk cap of one block can need one chunk per block of the stream
     capped = lib.pa_decode_workspace_bytes(64, 32, 8, 128, 16, 129, 16)
-    assert capped >= 64 * 8 * 4 + 2 * (64 * 8 * 129) * 4 * 130 * 4
+    assert capped >= 64 * 8 * 8 + 2 * (64 * 129) * 8 * (4 * 130) * 4
+    # records are padded to 16-byte multiples: G=1, head_dim 64 -> 68 floats
+    assert lib.pa_decode_workspace_bytes(4, 1, 1, 64, 16, 4, 0) >= 4 * 8 + 2 * 1024 * 68 * 4
     assert lib.pa_decode_workspace_bytes(64, 32, 8, 128, 16, 129, 513) == 0
 
 
