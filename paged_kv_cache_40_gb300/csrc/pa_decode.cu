@@ -223,25 +223,26 @@ struct Shape {
   // shared-memory layout: fixed part (bytes)
   static constexpr int OFF_FULL = 0;
   static constexpr int OFF_EMPTY = OFF_FULL + kMaxStages * 8;
-  static constexpr int OFF_QFULL = OFF_EMPTY + kMaxStages * 8;
-  static constexpr int OFF_QEMPTY = OFF_QFULL + 8;
-  static constexpr int OFF_MFULL = OFF_QEMPTY + 8;              // [kMsgSlots]
-  static constexpr int OFF_MEMPTY = OFF_MFULL + kMsgSlots * 8;  // [kMsgSlots]
-  static constexpr int OFF_FLAGS = OFF_MEMPTY + kMsgSlots * 8;  // 32 ints, see kFlag*
+  static constexpr int OFF_QFULL = OFF_EMPTY + kMaxStages * 8;   // [2]
+  static constexpr int OFF_QEMPTY = OFF_QFULL + 2 * 8;            // [2]
+  static constexpr int OFF_MFULL = OFF_QEMPTY + 2 * 8;            // [kMsgSlots]
+  static constexpr int OFF_MEMPTY = OFF_MFULL + kMsgSlots * 8;    // [kMsgSlots]
+  static constexpr int OFF_PMETA = OFF_MEMPTY + kMsgSlots * 8;    // PieceMeta [2]
+  static constexpr int OFF_MMETA = OFF_PMETA + 2 * 64;            // MsgMeta [kMsgSlots]
+  static constexpr int OFF_FLAGS = OFF_MMETA + kMsgSlots * 32;    // 32 ints, see kFlag*
   static constexpr int FIXED = OFF_FLAGS + 128;
   static int stage_bytes(int hg) { return 2 * NHALF * hg * TS * 128; }
   // then, from the next 1 KB-aligned address (the swizzle pattern is a
-  // function of address bits 7..9): ring, q slot, prefix
+  // function of address bits 7..9): ring, two q slots, prefix
   static size_t smem_bytes(int hg, int nst, int num_seqs) {
     return static_cast<size_t>(FIXED) + 1024 + static_cast<size_t>(nst) * stage_bytes(hg) +
-           static_cast<size_t>(hg) * G * D * 2 + static_cast<size_t>(num_seqs + 1) * 4;
+           2 * static_cast<size_t>(hg) * G * D * 2 + static_cast<size_t>(num_seqs + 1) * 4;
   }
 };
 
 // int flags in shared memory
 constexpr int kFlagAbort = 0;   // set when a bounded wait gave up
 constexpr int kFlagWsum = 8;    // [12] warp sums of the prefix scan
-constexpr int kFlagQLen = 24;   // sequence length of the piece in the q slot
 
 struct DecodeParams {
   const __half* q;
@@ -307,11 +308,12 @@ __device__ __forceinline__ void block_prefix(int* pfx, int* wsum, const int32_t*
 }
 
 // The block stream cut into chunks: one per CTA (or of at most cap_blocks
-// blocks each, a CTA then taking every gridDim.x-th chunk).
+// blocks each, a CTA then taking every gridDim.x-th chunk). Stream positions
+// fit in 32 bits (the host checks num_seqs x head groups x max blocks).
 struct Geometry {
-  long long total, chunk, nchunks;
+  int total, chunk, nchunks;
 };
-__device__ __forceinline__ Geometry chunk_geometry(long long total, int grid, int cap_blocks) {
+__device__ __forceinline__ Geometry chunk_geometry(int total, int grid, int cap_blocks) {
   Geometry g;
   g.total = total;
   g.chunk = (total + grid - 1) / grid;
@@ -324,31 +326,31 @@ __device__ __forceinline__ Geometry chunk_geometry(long long total, int grid, in
 // Record of chunk cc for a segment starting at stream index s0 whose first
 // chunk is c_first: slot 0 if the segment covers the chunk's start (the
 // chunk's first piece), slot 1 if it begins inside the chunk.
-__device__ __forceinline__ long long record_index(long long cc, long long c_first, long long s0,
-                                                  long long chunk, int hg, int w) {
-  return (2 * cc + ((cc == c_first && s0 > cc * chunk) ? 1 : 0)) * hg + w;
+__device__ __forceinline__ long long record_index(int cc, int c_first, int s0, int chunk, int hg,
+                                                  int w) {
+  return static_cast<long long>(2 * cc + ((cc == c_first && s0 > cc * chunk) ? 1 : 0)) * hg + w;
 }
 
 // Position in the block stream -> (sequence, head group, block within segment).
 struct Cursor {
-  int seq, hg, j, nb;   // nb = blocks in the segment (sequence)
-  long long seg_start;  // stream index of the segment's block 0
+  int seq, hg, j, nb;  // nb = blocks in the segment (sequence)
+  int seg_start;       // stream index of the segment's block 0
 };
 
-__device__ __forceinline__ Cursor locate(long long x, const int* pfx, int S, int nhg) {
+__device__ __forceinline__ Cursor locate(int x, const int* pfx, int S, int nhg) {
   int lo = 0, hi = S;  // largest i with pfx[i] * nhg <= x
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (static_cast<long long>(pfx[mid]) * nhg <= x) lo = mid;
+    if (pfx[mid] * nhg <= x) lo = mid;
     else hi = mid;
   }
   Cursor c;
   c.seq = lo;
   c.nb = pfx[lo + 1] - pfx[lo];
-  const long long r = x - static_cast<long long>(pfx[lo]) * nhg;
-  c.hg = static_cast<int>(r / c.nb);
-  c.j = static_cast<int>(r % c.nb);
-  c.seg_start = static_cast<long long>(pfx[lo]) * nhg + static_cast<long long>(c.hg) * c.nb;
+  const int r = x - pfx[lo] * nhg;
+  c.hg = r / c.nb;
+  c.j = r - c.hg * c.nb;
+  c.seg_start = pfx[lo] * nhg + c.hg * c.nb;
   return c;
 }
 
@@ -366,19 +368,19 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
 // Pieces of chunk c in the order a CTA streams them: the piece at the chunk's
 // start, then the piece at its end if that one's segment runs past the chunk,
 // then the uncut segments in between. Both cut pieces (whose partials other
-// chunks wait for) are thus finished early. Producer and consumers walk the
-// same sequence.
+// chunks wait for) are thus finished early. Only the producer walks; the
+// other warps learn each piece from it.
 struct Walk {
-  long long c;       // chunk
-  long long x0, xe;  // chunk [x0, xe) of the block stream
-  long long x1;      // end of the first piece
-  long long xl;      // start of the trailing cut piece (xe if there is none)
-  long long xm;      // next uncut segment
-  int phase;         // 0: first piece next, 1: trailing cut piece next, 2: middle
+  int c;       // chunk
+  int x0, xe;  // chunk [x0, xe) of the block stream
+  int x1;      // end of the first piece
+  int xl;      // start of the trailing cut piece (xe if there is none)
+  int xm;      // next uncut segment
+  int phase;   // 0: first piece next, 1: trailing cut piece next, 2: middle
 };
 
-__device__ __forceinline__ void walk_begin(Walk& wk, long long c, const Geometry& geo,
-                                           const int* pfx, int S, int nhg) {
+__device__ __forceinline__ void walk_begin(Walk& wk, int c, const Geometry& geo, const int* pfx,
+                                           int S, int nhg) {
   wk.c = c;
   wk.phase = 0;
   if (c >= geo.nchunks) return;
@@ -394,35 +396,52 @@ __device__ __forceinline__ void walk_begin(Walk& wk, long long c, const Geometry
   wk.xm = wk.x1;
 }
 
-// Next piece of the walk (cursor at its first block, n blocks), moving on to
-// the CTA's next chunk (c + stride) when this one is done. False at the end.
-__device__ __forceinline__ bool walk_next(Walk& wk, const Geometry& geo, long long stride,
-                                          const int* pfx, int S, int nhg, Cursor& cur, int& n) {
+// A piece: cursor at its first block, n blocks, and its chunk.
+struct Piece {
+  Cursor cur;
+  int n, c;
+};
+
+// Next piece of the walk, moving on to the CTA's next chunk (c + stride) when
+// this one is done. False at the end.
+__device__ __forceinline__ bool walk_next(Walk& wk, const Geometry& geo, int stride,
+                                          const int* pfx, int S, int nhg, Piece& pc) {
   while (wk.c < geo.nchunks) {
+    pc.c = wk.c;
     if (wk.phase == 0) {
       wk.phase = 1;
-      cur = locate(wk.x0, pfx, S, nhg);
-      n = static_cast<int>(wk.x1 - wk.x0);
+      pc.cur = locate(wk.x0, pfx, S, nhg);
+      pc.n = wk.x1 - wk.x0;
       return true;
     }
     if (wk.phase == 1) {
       wk.phase = 2;
       if (wk.xl < wk.xe) {
-        cur = locate(wk.xl, pfx, S, nhg);
-        n = static_cast<int>(wk.xe - wk.xl);
+        pc.cur = locate(wk.xl, pfx, S, nhg);
+        pc.n = wk.xe - wk.xl;
         return true;
       }
     }
     if (wk.xm < wk.xl) {
-      cur = locate(wk.xm, pfx, S, nhg);
-      n = static_cast<int>(min(static_cast<long long>(cur.nb - cur.j), wk.xl - wk.xm));
-      wk.xm += n;
+      pc.cur = locate(wk.xm, pfx, S, nhg);
+      pc.n = min(pc.cur.nb - pc.cur.j, wk.xl - wk.xm);
+      wk.xm += pc.n;
       return true;
     }
     walk_begin(wk, wk.c + stride, geo, pfx, S, nhg);
   }
   return false;
 }
+
+// What the producer tells the other warps about a piece (in shared memory,
+// published by the arrival on the piece's q slot barrier).
+struct PieceMeta {
+  int seq, hg, j, n, nb, len, s0, c, last, pad[7];
+};
+// A cut piece handed from the consumer warps to the merge warps.
+struct MsgMeta {
+  int seq, hg, nb, s0, stop, pad[3];
+};
 
 // Counts one arrival of a cut segment's head on its tagged counter word and
 // returns true for the arrival that completes the count (E arrivals), which
@@ -534,23 +553,27 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                         const __grid_constant__ CUtensorMap vmap) {
   using SH = Shape<D, BS, G>;
   constexpr int TS = SH::TS;
+  constexpr int QBYTES_PER_HEAD = G * D * 2;
   extern __shared__ __align__(128) unsigned char smem[];
   const int HG = p.hg, NST = p.nst;
   const int HALF = HG * TS * 128;        // one 64-dim half of one stage's K (or V)
   const int TILE = SH::NHALF * HALF;     // K (or V) of one stage
   const int STAGE = 2 * TILE;
+  const int QSLOT = HG * QBYTES_PER_HEAD;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_FULL);
   uint64_t* empty_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_EMPTY);
   uint64_t* qfull_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_QFULL);
   uint64_t* qempty_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_QEMPTY);
   uint64_t* mfull_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_MFULL);
   uint64_t* mempty_bar = reinterpret_cast<uint64_t*>(smem + SH::OFF_MEMPTY);
+  PieceMeta* pmeta = reinterpret_cast<PieceMeta*>(smem + SH::OFF_PMETA);
+  MsgMeta* mmeta = reinterpret_cast<MsgMeta*>(smem + SH::OFF_MMETA);
   int* flags = reinterpret_cast<int*>(smem + SH::OFF_FLAGS);
   volatile int* abort_flag = flags + kFlagAbort;
   const uint32_t smem_base = smem_addr(smem);
   unsigned char* ring = smem + (((smem_base + SH::FIXED + 1023u) & ~1023u) - smem_base);
-  unsigned char* qslot = ring + static_cast<size_t>(NST) * STAGE;
-  int* pfx = reinterpret_cast<int*>(qslot + HG * G * D * 2);
+  unsigned char* qslot = ring + static_cast<size_t>(NST) * STAGE;  // [2][HG][G][D] fp16
+  int* pfx = reinterpret_cast<int*>(qslot + 2 * QSLOT);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -565,8 +588,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       mbar_init(smem_addr(&full_bar[s]), 1);
       mbar_init(smem_addr(&empty_bar[s]), HG);
     }
-    mbar_init(smem_addr(qfull_bar), 1);
-    mbar_init(smem_addr(qempty_bar), HG);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(smem_addr(&qfull_bar[q]), 1);
+      mbar_init(smem_addr(&qempty_bar[q]), HG);
+    }
     for (int m = 0; m < kMsgSlots; ++m) {
       mbar_init(smem_addr(&mfull_bar[m]), HG);  // one arrival per consumer warp
       mbar_init(smem_addr(&mempty_bar[m]), kMergeWarps);
@@ -577,26 +602,27 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
   // ---- blocks per sequence, exclusive prefix sum in shared memory ----
   block_prefix(pfx, flags + kFlagWsum, p.seq_lens, S, BS, cap, p.err);
-  const Geometry geo = chunk_geometry(static_cast<long long>(pfx[S]) * NHG, gridDim.x, p.cap_blocks);
-  const long long chunk = geo.chunk;
+  const Geometry geo = chunk_geometry(pfx[S] * NHG, gridDim.x, p.cap_blocks);
+  const int chunk = geo.chunk;
+  const bool has_work = static_cast<int>(blockIdx.x) < geo.nchunks;
 
   // The producer's first piece, and an L2 prefetch of its table entries and
   // q rows: a prefetch may run before the wait below, because L2 stays
   // coherent with whatever the previous kernel writes.
-  Walk pwk;
-  Cursor pcur0{};
-  int pn0 = 0;
-  bool phave = false;
+  Walk wk;
+  Piece P{};
+  bool have = false;
   if (warp == HG) {
-    walk_begin(pwk, blockIdx.x, geo, pfx, S, NHG);
-    phave = walk_next(pwk, geo, gridDim.x, pfx, S, NHG, pcur0, pn0);
-    if (phave) {
-      const int32_t* trow = p.block_table + static_cast<long long>(pcur0.seq) * p.max_blocks + pcur0.j;
-      if (lane < min(32, pn0)) asm volatile("prefetch.global.L2 [%0];" ::"l"(trow + lane));
+    walk_begin(wk, blockIdx.x, geo, pfx, S, NHG);
+    have = walk_next(wk, geo, gridDim.x, pfx, S, NHG, P);
+    if (have) {
+      const int32_t* trow =
+          p.block_table + static_cast<long long>(P.cur.seq) * p.max_blocks + P.cur.j;
+      if (lane < min(32, P.n)) asm volatile("prefetch.global.L2 [%0];" ::"l"(trow + lane));
       const char* qrow = reinterpret_cast<const char*>(
-          p.q + (static_cast<long long>(pcur0.seq) * p.num_q_heads +
-                 static_cast<long long>(pcur0.hg) * HG * G) * D);
-      for (int off = lane * 128; off < HG * G * D * 2; off += 32 * 128)
+          p.q + (static_cast<long long>(P.cur.seq) * p.num_q_heads +
+                 static_cast<long long>(P.cur.hg) * HG * G) * D);
+      for (int off = lane * 128; off < QSLOT; off += 32 * 128)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow + off));
     }
   }
@@ -610,66 +636,74 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
   if (warp == HG) {
     // =========================== producer warp ===========================
-    // The walk visits the CTA's pieces, each in groups of up to 32 blocks.
-    // The table entries (one per lane) and the sequence length of the next
-    // group are loaded while the current group is issued, so no piece
-    // boundary waits on a global load.
+    // Streams the CTA's pieces, each in groups of up to 32 blocks. For each
+    // piece it first publishes, in q slot (piece & 1), the piece's metadata
+    // and its HG*G q rows. The table entries of the next group (in this piece
+    // or the next) are loaded while the current group is issued, so no group
+    // or piece boundary waits on a global load.
     uint32_t g = 0;   // ring sequence number (stages)
     uint32_t pc = 0;  // piece number
-    Walk wk = pwk;
-    Cursor cur = pcur0;
-    int n = pn0, j0 = 0;
-    int phys_next = 0, len_next = 0;
-    bool have = phave;
+    Piece PN{};
+    bool nhave = have && walk_next(wk, geo, gridDim.x, pfx, S, NHG, PN);
+    int j0 = 0;
+    int phys_cur = 0, len_cur = 0;
     if (have) {
-      len_next = min(max(__ldg(p.seq_lens + cur.seq), 0), cap);
-      phys_next = lane < min(32, n)
-                      ? __ldg(p.block_table + static_cast<long long>(cur.seq) * p.max_blocks +
-                              cur.j + lane)
-                      : 0;
+      len_cur = min(max(__ldg(p.seq_lens + P.cur.seq), 0), cap);
+      phys_cur = lane < min(32, P.n)
+                     ? __ldg(p.block_table + static_cast<long long>(P.cur.seq) * p.max_blocks +
+                             P.cur.j + lane)
+                     : 0;
     }
     while (have) {
-      const Cursor gc = cur;
-      const int gn = n, gj0 = j0, glen = len_next, phys_lane = phys_next;
-      const int nn = min(32, gn - gj0);
-      // advance to the next group and start loading its table entries
-      j0 += 32;
-      if (j0 >= n) {
-        have = walk_next(wk, geo, gridDim.x, pfx, S, NHG, cur, n);
-        if (have) {
-          j0 = 0;
-          len_next = min(max(__ldg(p.seq_lens + cur.seq), 0), cap);
-        }
-      }
-      if (have) {
-        const int cnt = min(32, n - j0);
-        phys_next = lane < cnt ? __ldg(p.block_table +
-                                       static_cast<long long>(cur.seq) * p.max_blocks + cur.j +
-                                       j0 + lane)
-                               : 0;
-      }
-      if (gj0 == 0) {
-        // new piece: q rows of the group's HG*G query heads and the length -> q slot
+      if (j0 == 0) {
+        // new piece: metadata and q rows -> q slot (pc & 1)
+        const int qs = static_cast<int>(pc & 1);
         if (!__shfl_sync(0xffffffffu, *abort_flag, 0) &&
-            (pc == 0 ||
-             warp_wait_phase(smem_addr(qempty_bar), (pc - 1) & 1, abort_flag, p.err))) {
+            (pc < 2 ||
+             warp_wait_phase(smem_addr(&qempty_bar[qs]), ((pc >> 1) - 1) & 1, abort_flag, p.err))) {
           if (lane == 0) {
-            flags[kFlagQLen] = glen;  // published by the arrive below
-            const uint32_t qb = smem_addr(qfull_bar);
-            mbar_arrive_expect_tx(qb, HG * G * D * 2);
-            bulk_copy_g2s(smem_addr(qslot),
-                          p.q + (static_cast<long long>(gc.seq) * p.num_q_heads +
-                                 static_cast<long long>(gc.hg) * HG * G) * D,
-                          HG * G * D * 2, qb);
+            PieceMeta* m = pmeta + qs;
+            m->seq = P.cur.seq;
+            m->hg = P.cur.hg;
+            m->j = P.cur.j;
+            m->n = P.n;
+            m->nb = P.cur.nb;
+            m->len = len_cur;
+            m->s0 = P.cur.seg_start;
+            m->c = P.c;
+            m->last = nhave ? 0 : 1;
+            const uint32_t qb = smem_addr(&qfull_bar[qs]);
+            // the arrival releases the metadata stores above
+            mbar_arrive_expect_tx(qb, QSLOT);
+            bulk_copy_g2s(smem_addr(qslot + qs * QSLOT),
+                          p.q + (static_cast<long long>(P.cur.seq) * p.num_q_heads +
+                                 static_cast<long long>(P.cur.hg) * HG * G) * D,
+                          QSLOT, qb);
           }
           __syncwarp();
         }
       }
+      const int nn = min(32, P.n - j0);
+      // table entries (and length) of the next group
+      const bool next_in_piece = j0 + 32 < P.n;
+      int phys_nxt = 0, len_nxt = len_cur;
+      if (next_in_piece) {
+        phys_nxt = lane < min(32, P.n - j0 - 32)
+                       ? __ldg(p.block_table + static_cast<long long>(P.cur.seq) * p.max_blocks +
+                               P.cur.j + j0 + 32 + lane)
+                       : 0;
+      } else if (nhave) {
+        len_nxt = min(max(__ldg(p.seq_lens + PN.cur.seq), 0), cap);
+        phys_nxt = lane < min(32, PN.n)
+                       ? __ldg(p.block_table + static_cast<long long>(PN.cur.seq) * p.max_blocks +
+                               PN.cur.j + lane)
+                       : 0;
+      }
       for (int jj = 0; jj < nn; ++jj) {
-        const int phys = __shfl_sync(0xffffffffu, phys_lane, jj);
-        const int blk = gc.j + gj0 + jj;
-        const int vb = min(BS, glen - blk * BS);   // valid rows of the block (>= 1)
-        const int nsb = (vb + TS - 1) / TS;         // stages that hold valid rows
+        const int phys = __shfl_sync(0xffffffffu, phys_cur, jj);
+        const int blk = P.cur.j + j0 + jj;
+        const int vb = min(BS, len_cur - blk * BS);  // valid rows of the block (>= 1)
+        const int nsb = (vb + TS - 1) / TS;           // stages that hold valid rows
         const bool bad = phys < 0 || phys >= p.num_blocks;
         for (int sb = 0; sb < nsb; ++sb, ++g) {
           const int stage = g % NST;
@@ -687,8 +721,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
               const uint32_t kdst = smem_addr(ring + static_cast<size_t>(stage) * STAGE);
 #pragma unroll
               for (int h = 0; h < SH::NHALF; ++h) {
-                tma_load_4d(kdst + h * HALF, &kmap, 64 * h, sb * TS, gc.hg * HG, phys, fb);
-                tma_load_4d(kdst + TILE + h * HALF, &vmap, 64 * h, sb * TS, gc.hg * HG, phys,
+                tma_load_4d(kdst + h * HALF, &kmap, 64 * h, sb * TS, P.cur.hg * HG, phys, fb);
+                tma_load_4d(kdst + TILE + h * HALF, &vmap, 64 * h, sb * TS, P.cur.hg * HG, phys,
                             fb);
               }
             }
@@ -696,7 +730,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           __syncwarp();
         }
       }
-      if (gj0 + 32 >= gn) ++pc;  // the piece's last group
+      if (next_in_piece) {
+        j0 += 32;
+      } else {
+        ++pc;
+        P = PN;
+        have = nhave;
+        j0 = 0;
+        if (have) nhave = walk_next(wk, geo, gridDim.x, pfx, S, NHG, PN);
+      }
+      phys_cur = phys_nxt;
+      len_cur = len_nxt;
     }
     // After an abort, wait (bounded) for copies still landing in shared memory.
     if (*abort_flag) {
@@ -707,9 +751,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         while (!mbar_try_wait(bar, (gi / NST) & 1) && global_ns() - t0 < kWaitLimitNs) {
         }
       }
-      if (pc > 0) {
+      for (uint32_t pi = pc > 2 ? pc - 2 : 0; pi < pc; ++pi) {
         const unsigned long long t0 = global_ns();
-        while (!mbar_try_wait(smem_addr(qfull_bar), (pc - 1) & 1) &&
+        while (!mbar_try_wait(smem_addr(&qfull_bar[pi & 1]), (pi >> 1) & 1) &&
                global_ns() - t0 < kWaitLimitNs) {
         }
       }
@@ -719,38 +763,29 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
   if (warp > HG) {
     // ============================= merge warps ============================
-    // Each walks the CTA's pieces like the consumers. For every cut piece that
-    // is not the CTA's last, it waits until all consumer warps have written
-    // their records (message m in slot m % kMsgSlots), counts one arrival for
-    // each of its heads (head h belongs to merge warp h % kMergeWarps, lane h
-    // counts it) and merges each of its heads whose arrivals are complete.
+    // For every cut piece that is not the CTA's last, the consumer warps send
+    // a message (slot m % kMsgSlots) once all their records are written. Each
+    // merge warp counts one arrival for each of its heads (head h belongs to
+    // merge warp h % kMergeWarps, lane h counts it) and merges each of its
+    // heads whose arrivals are complete. A stop message ends the loop.
     const int mw = warp - HG - 1;
-    Walk wk;
-    walk_begin(wk, blockIdx.x, geo, pfx, S, NHG);
-    Cursor cur{};
-    int n = 0;
-    bool have = walk_next(wk, geo, gridDim.x, pfx, S, NHG, cur, n);
-    uint32_t mc = 0;
-    while (have) {
-      const Cursor pcur = cur;
-      const int pn = n;
-      have = walk_next(wk, geo, gridDim.x, pfx, S, NHG, cur, n);
-      const bool cut = pcur.j > 0 || pcur.j + pn < pcur.nb;
-      if (!cut || !have) continue;  // uncut, or the CTA's last piece (merged by the consumers)
+    for (uint32_t mc = 0; has_work; ++mc) {
       const int ms = static_cast<int>(mc % kMsgSlots);
       if (!warp_wait_phase<256>(smem_addr(&mfull_bar[ms]), (mc / kMsgSlots) & 1, abort_flag,
                                 p.err))
         break;
+      const MsgMeta msg = mmeta[ms];
       // the consumers' records (ordered before their arrivals on the barrier)
       // become visible to the whole GPU before any arrival is counted
       fence_acq_rel_gpu();
+      __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&mempty_bar[ms]));
-      ++mc;
-      const long long s0 = pcur.seg_start;
-      const long long c_first = s0 / chunk, c_last = (s0 + pcur.nb - 1) / chunk;
-      const int E = static_cast<int>(c_last - c_first + 1);
+      if (msg.stop) break;
+      const int s0 = msg.s0;
+      const int c_first = s0 / chunk, c_last = (s0 + msg.nb - 1) / chunk;
+      const int E = c_last - c_first + 1;
       unsigned long long* words =
-          p.counters + static_cast<long long>(pcur.seq) * Hkv + static_cast<long long>(pcur.hg) * HG;
+          p.counters + static_cast<long long>(msg.seq) * Hkv + static_cast<long long>(msg.hg) * HG;
       const bool mine = lane < HG && lane % kMergeWarps == mw;
       const bool done =
           mine && arrive_last(words + lane, p.tag, static_cast<unsigned>(E), false, p.err);
@@ -762,8 +797,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         auto rec_of = [&](int i) -> long long {
           return record_index(c_first + i, c_first, s0, chunk, HG, h);
         };
-        __half* out_row = p.out + (static_cast<long long>(pcur.seq) * p.num_q_heads +
-                                   static_cast<long long>(pcur.hg * HG + h) * G) * D;
+        __half* out_row = p.out + (static_cast<long long>(msg.seq) * p.num_q_heads +
+                                   static_cast<long long>(msg.hg * HG + h) * G) * D;
         merge_partials<D, G>(p.records, E, rec_of, out_row);
       }
     }
@@ -783,6 +818,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       for (int e = tid; e < p.num_q_heads * D; e += HG * 32) o[e] = __float2half_rn(0.f);
     }
   }
+  if (!has_work) return;
 
   // ldmatrix addressing inside a swizzled tile: lane supplies row (lane & 7)
   // of matrix (lane >> 3); logical 16-byte chunk c of row r sits at chunk
@@ -792,40 +828,31 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   const int ld_mat = lane >> 3;
 
   uint32_t g = 0;   // ring sequence number of the next stage
-  uint32_t pc = 0;  // piece number
-  uint32_t mc = 0;  // cut pieces handed to the merge warp
-  Walk wk;
-  walk_begin(wk, blockIdx.x, geo, pfx, S, NHG);
-  Cursor cur{};
-  int n = 0;
-  bool have = walk_next(wk, geo, gridDim.x, pfx, S, NHG, cur, n);
-  while (have) {
+  uint32_t mc = 0;  // messages sent to the merge warps
+  for (uint32_t pc = 0;; ++pc) {
+    // ---- the piece: metadata and q from q slot (pc & 1) ----
+    const int qs = static_cast<int>(pc & 1);
+    const bool qok = warp_wait_phase(smem_addr(&qfull_bar[qs]), (pc >> 1) & 1, abort_flag, p.err);
+    if (!qok) break;
+    const PieceMeta pm = pmeta[qs];
+    const int pj = pm.j, n = pm.n, L = pm.len;
+    const int kvh = pm.hg * HG + w;
+    uint32_t qa[SH::KSTEPS][2];  // A fragments a0/a2 per k-step; rows (heads) >= G are zero
     {
-      const int kvh = cur.hg * HG + w;
-      const long long c = wk.c, x0 = wk.x0;  // the piece's chunk
-
-      // ---- q and length of the piece ----
-      uint32_t qa[SH::KSTEPS][2];  // A fragments a0/a2 per k-step; rows (heads) >= G are zero
-      int L = 0;
-      {
-        const bool ok = warp_wait_phase(smem_addr(qfull_bar), pc & 1, abort_flag, p.err);
-        L = flags[kFlagQLen];
-        if (ok) {
-          const uint32_t qrow =
-              smem_addr(qslot) + (w * G + (ld_row < G ? ld_row : 0)) * (D * 2);
+      const uint32_t qrow = smem_addr(qslot + qs * QSLOT) +
+                            (w * G + (ld_row < G ? ld_row : 0)) * (D * 2);
 #pragma unroll
-          for (int kk = 0; kk < SH::KSTEPS; kk += 2) {
-            uint32_t r0, r1, r2, r3;
-            ldsm_x4(qrow + (2 * kk + ld_mat) * 16, r0, r1, r2, r3);
-            qa[kk][0] = gid < G ? r0 : 0u;
-            qa[kk][1] = gid < G ? r1 : 0u;
-            qa[kk + 1][0] = gid < G ? r2 : 0u;
-            qa[kk + 1][1] = gid < G ? r3 : 0u;
-          }
-        }
-        __syncwarp();
-        if (ok && lane == 0) mbar_arrive(smem_addr(qempty_bar));
+      for (int kk = 0; kk < SH::KSTEPS; kk += 2) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(qrow + (2 * kk + ld_mat) * 16, r0, r1, r2, r3);
+        qa[kk][0] = gid < G ? r0 : 0u;
+        qa[kk][1] = gid < G ? r1 : 0u;
+        qa[kk + 1][0] = gid < G ? r2 : 0u;
+        qa[kk + 1][1] = gid < G ? r3 : 0u;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&qempty_bar[qs]));
+    }
 
       float m_run = -INFINITY, l_run = 0.f;  // head gid: running max (log2 units), partial sum
       float o[SH::MT][4];                     // O^T[d = mt*16 + gid (+8)][h = 2*tig (+1)]
@@ -833,7 +860,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       for (int mt = 0; mt < SH::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
       for (int jj = 0; jj < n; ++jj) {
-        const int blk = cur.j + jj;
+        const int blk = pj + jj;
         const int vb = min(BS, L - blk * BS);
         const int nsb = (vb + TS - 1) / TS;
         for (int sb = 0; sb < nsb; ++sb, ++g) {
@@ -938,14 +965,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       }
 
       // ---- piece finished: this warp holds its head's whole state ----
-      // (the walk moves on to the next piece once the results are stored)
-      Cursor ncur{};
-      int nn = 0;
-      bool more;
       l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
       l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-      const bool cut = cur.j > 0 || cur.j + n < cur.nb;
-      __half* out_row = p.out + (static_cast<long long>(cur.seq) * p.num_q_heads +
+      const bool cut = pj > 0 || pj + n < pm.nb;
+      __half* out_row = p.out + (static_cast<long long>(pm.seq) * p.num_q_heads +
                                  static_cast<long long>(kvh) * G) * D;
       const int h0 = 2 * tig, h1 = 2 * tig + 1;
       if (!cut) {
@@ -964,13 +987,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             out_row[h1 * D + d + 8] = __float2half_rn(o[mt][3] * i1);
           }
         }
-        more = walk_next(wk, geo, gridDim.x, pfx, S, NHG, ncur, nn);
       } else {
         // cut segment: record this chunk's partial (slot 0 if the piece starts
         // the chunk, else 1); the last of the segment's chunks to arrive merges
-        const long long s0 = cur.seg_start;
-        const int slot = s0 + cur.j == x0 ? 0 : 1;
-        float* rec = p.records + ((2 * c + slot) * HG + w) * static_cast<long long>(SH::REC);
+        const int s0 = pm.s0;
+        const int slot = s0 + pj == pm.c * chunk ? 0 : 1;
+        float* rec = p.records + ((2ll * pm.c + slot) * HG + w) * static_cast<long long>(SH::REC);
 #pragma unroll
         for (int mt = 0; mt < SH::MT; ++mt) {
           const int d = mt * 16 + gid;
@@ -987,14 +1009,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           rec[G * D + 2 * gid] = m_run;
           rec[G * D + 2 * gid + 1] = l_run;
         }
-        more = walk_next(wk, geo, gridDim.x, pfx, S, NHG, ncur, nn);
-        if (more) {
+        if (!pm.last) {
           // hand the arrival (and any merge) to the merge warps: the warp
           // barrier orders every lane's record stores before lane 0's arrival,
           // whose release makes them visible to the merge warps' acquire
           if (mc >= kMsgSlots)
             warp_wait_phase(smem_addr(&mempty_bar[mc % kMsgSlots]), ((mc / kMsgSlots) - 1) & 1,
                             abort_flag, p.err);
+          if (w == 0 && lane == 0) {
+            MsgMeta* m = mmeta + mc % kMsgSlots;
+            m->seq = pm.seq;
+            m->hg = pm.hg;
+            m->nb = pm.nb;
+            m->s0 = s0;
+            m->stop = 0;
+          }
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_addr(&mfull_bar[mc % kMsgSlots]));
           ++mc;
@@ -1006,9 +1035,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           // needs no release and the claim does not wait for its stores.
           // Otherwise release the record and count the arrival as usual.
           __syncwarp();  // the record's lanes, before any lane reads it back
-          const long long c_first = s0 / chunk, c_last = (s0 + cur.nb - 1) / chunk;
-          const int E = static_cast<int>(c_last - c_first + 1);
-          unsigned long long* word = p.counters + static_cast<long long>(cur.seq) * Hkv + kvh;
+          const int c_first = s0 / chunk, c_last = (s0 + pm.nb - 1) / chunk;
+          const int E = c_last - c_first + 1;
+          unsigned long long* word = p.counters + static_cast<long long>(pm.seq) * Hkv + kvh;
           const unsigned long long claim = (p.tag << kArrivalBits) | static_cast<unsigned>(E - 1);
           int done = 0;
           if (lane == 0) done = atomicCAS(word, claim, 0ull) == claim;
@@ -1029,11 +1058,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           }
         }
       }
-      ++pc;
-      cur = ncur;
-      n = nn;
-      have = more;
-    }
+    if (pm.last) break;
+  }
+  // tell the merge warps there is nothing more
+  if (!*abort_flag) {
+    if (mc >= kMsgSlots)
+      warp_wait_phase(smem_addr(&mempty_bar[mc % kMsgSlots]), ((mc / kMsgSlots) - 1) & 1,
+                      abort_flag, p.err);
+    if (w == 0 && lane == 0) mmeta[mc % kMsgSlots].stop = 1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&mfull_bar[mc % kMsgSlots]));
   }
 }
 
@@ -1300,6 +1334,10 @@ pa_status check_decode_shape(int S, int Hq, int Hkv, int D, int BS, int MB, int 
                     part_tokens);
   if (static_cast<long long>(MB) * BS > INT32_MAX)
     return pa::fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq * block_size exceeds int32");
+  // block-stream positions are 32-bit in the kernel
+  if (static_cast<long long>(S) * (Hkv / head_group(Hkv)) * MB >= (1ll << 31))
+    return pa::fail(PA_ERR_UNSUPPORTED,
+                    "num_seqs x KV head groups x max_blocks_per_seq must stay below 2^31");
   // the chunks one sequence can span must fit the arrival count of a counter word
   const long long cap = part_tokens / BS;
   const long long span = cap > 0 ? (MB + cap - 1) / cap + 1 : kMaxGrid;
