@@ -299,8 +299,10 @@ def run_ours(args, world, rank, local):
     # second one, so the timed step starts with L2 holding neither its inputs
     # nor dirty lines whose write-back it would pay for.
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+    # float32 so the reduction reads the buffer once (an int32 sum would first
+    # convert the whole buffer to int64)
+    flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
     launches_per_step = (1 if len(plan.cow_pairs) else 0) + 1 + DecodeBatchRunner.ATTEND_LAUNCHES
 
     def flush():

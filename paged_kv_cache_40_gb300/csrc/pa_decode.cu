@@ -31,20 +31,23 @@
 //     clearing. A chunk has at most two cut pieces, its first and its last;
 //     each CTA streams them before the uncut segments in between, so most
 //     merges happen while the other CTAs are still streaming.
-//   * Warp specialisation. A producer warp walks the CTA's chunk, loads the
-//     block-table entries of the next 32 blocks while it issues the current
-//     ones, and moves K and V with TMA into a ring of shared-memory stages:
-//     a 4-D tensor map over the pool seen as (dim, token, KV head, block) —
-//     token stride larger than head stride — with box {64, tokens, HG, 1} and
-//     the 128-byte swizzle, so each head's rows land contiguously and the
-//     tensor-core fragment loads (ldmatrix) are free of bank conflicts. Every
-//     consumer warp reads every stage (its own head), so a stage is released
-//     after HG arrivals. q of each piece comes through a q slot the same way.
-//     A merge warp takes the cut pieces off the consumers' critical path: a
-//     consumer warp writes its partial record, arrives on a shared-memory
-//     barrier and goes on streaming; the merge warp, walking the same piece
-//     sequence, counts the arrivals of all HG heads at once (one lane each)
-//     and merges the heads whose partials are complete. Only the CTA's final
+//   * Warp specialisation. A producer warp is the only one that walks the
+//     CTA's chunk. It loads the block-table entries of the next 32 blocks
+//     while it issues the current ones, and moves K and V with TMA into a
+//     ring of shared-memory stages: a 4-D tensor map over the pool seen as
+//     (dim, token, KV head, block) — token stride larger than head stride —
+//     with box {64, tokens, HG, 1} and the 128-byte swizzle, so each head's
+//     rows land contiguously and the tensor-core fragment loads (ldmatrix)
+//     are free of bank conflicts. Every consumer warp reads every stage (its
+//     own head), so a stage is released after HG arrivals. For each piece the
+//     producer also publishes, in one of two q slots, the piece's metadata
+//     and its q rows, so the next piece's q is in flight while the current
+//     one streams and the consumers never search the block stream.
+//     Merge warps take the cut pieces off the consumers' critical path: the
+//     consumer warps write their partial records, send a message (segment and
+//     place) through a small shared-memory ring and go on streaming; the
+//     merge warps count the arrivals of all HG heads at once (one lane each)
+//     and merge the heads whose partials are complete. Only the CTA's final
 //     piece is merged by the consumer warps themselves, in parallel.
 //   * Consumer math on tensor cores (mma.sync m16n8k16, fp16 in, fp32
 //     accumulate). Scores S = Q K^T with the G query heads as the M rows and
