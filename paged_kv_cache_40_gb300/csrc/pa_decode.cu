@@ -475,17 +475,21 @@ __device__ __forceinline__ bool arrive_last(unsigned long long* word, unsigned l
 // One warp merges the E partial records of one KV head of a cut segment with
 // the log-sum-exp rule and writes that head's G fp16 output rows. Record i is
 // `recs + rec_of(i) * rec_floats(G, D)`: acc [G][D], then (max, sum) per
-// head. Lane l owns the float4 slices l, l + 32, ... of the accumulator; a
-// slice lies inside one query head, whose (max, sum) the lane reads with it.
-// All loads of a batch of records are issued before any is used, so a merge
-// costs about one L2 round trip per batch.
+// head. Records are folded in batches of KB: lane r*G + h loads the (max,
+// sum) of record r, head h, and every lane loads its float4 slices (l,
+// l + 32, ...) of each record's accumulator; a slice lies inside one query
+// head, whose (max, sum) the lane then takes by shuffle. All loads of a batch
+// are issued before any is used, so a batch costs one L2 round trip.
 template <int D, int G, typename RecOf>
 __device__ __forceinline__ void merge_partials(const float* recs, int E, RecOf rec_of,
                                                __half* out_row) {
   constexpr int NV4 = G * D / 4;         // float4 slices of one accumulator
   constexpr int PER = (NV4 + 31) / 32;   // slices per lane
-  // records per batch: as many as registers allow without spilling
-  constexpr int KB = PER == 1 ? 6 : PER == 2 ? 4 : PER == 4 ? 3 : 1;
+  // records per batch: (max, sum) pairs fit one per lane, and the slices in
+  // flight stay within registers
+  constexpr int KB_ML = 32 / G;
+  constexpr int KB_REG = PER >= 8 ? 2 : 20 / PER;
+  constexpr int KB = KB_ML < KB_REG ? KB_ML : KB_REG;
   constexpr int RS = rec_floats(G, D);   // floats per record (16-byte multiple)
   const int lane = threadIdx.x & 31;
   float M[PER], Ls[PER];
@@ -497,8 +501,13 @@ __device__ __forceinline__ void merge_partials(const float* recs, int E, RecOf r
     A[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   for (int base = 0; base < E; base += KB) {
+    float2 mlv = make_float2(-INFINITY, 0.f);
+    {
+      const int r = lane / G, h = lane % G;
+      if (r < KB && base + r < E)
+        mlv = __ldcg(reinterpret_cast<const float2*>(recs + rec_of(base + r) * RS + G * D) + h);
+    }
     float4 v[KB][PER];
-    float2 ml[KB][PER];
 #pragma unroll
     for (int r = 0; r < KB; ++r) {
       const bool have = base + r < E;
@@ -506,32 +515,35 @@ __device__ __forceinline__ void merge_partials(const float* recs, int E, RecOf r
 #pragma unroll
       for (int k = 0; k < PER; ++k) {
         const int i = lane + 32 * k;
-        if (have && i < NV4) {
-          v[r][k] = __ldcg(reinterpret_cast<const float4*>(rp) + i);
-          ml[r][k] = __ldcg(reinterpret_cast<const float2*>(rp + G * D) + (i * 4) / D);
-        } else {
-          v[r][k] = make_float4(0.f, 0.f, 0.f, 0.f);
-          ml[r][k] = make_float2(-INFINITY, 0.f);
-        }
+        v[r][k] = have && i < NV4 ? __ldcg(reinterpret_cast<const float4*>(rp) + i)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
+      const int i = lane + 32 * k;
+      const int hk = i < NV4 ? (i * 4) / D : 0;
+      float mr[KB], lr[KB];
+#pragma unroll
+      for (int r = 0; r < KB; ++r) {
+        mr[r] = __shfl_sync(0xffffffffu, mlv.x, r * G + hk);
+        lr[r] = __shfl_sync(0xffffffffu, mlv.y, r * G + hk);
+      }
       float mb = M[k];
 #pragma unroll
-      for (int r = 0; r < KB; ++r) mb = fmaxf(mb, ml[r][k].x);
+      for (int r = 0; r < KB; ++r) mb = fmaxf(mb, mr[r]);
       const float mu = mb == -INFINITY ? 0.f : mb;
       const float f = fast_exp2(M[k] - mu);
       float4 a = make_float4(A[k].x * f, A[k].y * f, A[k].z * f, A[k].w * f);
       float l = Ls[k] * f;
 #pragma unroll
       for (int r = 0; r < KB; ++r) {
-        const float wr = fast_exp2(ml[r][k].x - mu);
+        const float wr = fast_exp2(mr[r] - mu);
         a.x += v[r][k].x * wr;
         a.y += v[r][k].y * wr;
         a.z += v[r][k].z * wr;
         a.w += v[r][k].w * wr;
-        l += ml[r][k].y * wr;
+        l += lr[r] * wr;
       }
       A[k] = a;
       Ls[k] = l;
