@@ -15,6 +15,9 @@ Sources (web pages on PagedAttention):
     the C-style layout sketch, copy-on-write block sharing), §3 Mental Model
     (sharing picture), §11 Engineering Decision Framework and §13 question 4
     (capacity arithmetic).
+  * The fp8 (E4M3) KV cache of `fp8.py` follows Document 04 §11/§12 (KV
+    quantization as a way to fit more sequences); its format readings are in
+    that module's docstring.
   * lux-666 notes "PagedAttention", sections 最小模型 (minimal model: logical
     blocks -> block table -> physical blocks, worked mapping 0->7, 1->2, 2->9),
     它为什么有效 (internal waste bounded by the last block; prefix sharing with
@@ -35,6 +38,14 @@ from .attention import (  # noqa: F401
     split_context_attention,
 )
 from .cache_ops import append_kv, copy_blocks  # noqa: F401
+from .fp8 import (  # noqa: F401
+    e4m3_decode,
+    e4m3_encode,
+    quantize_rows,
+    append_kv_fp8,
+    dequantize_pool,
+    decode_attention_fp8,
+)
 from .allocator import BlockAllocator, OutOfBlocks  # noqa: F401
 from .accounting import (  # noqa: F401
     blocks_needed,

@@ -15,6 +15,10 @@ here too and passed in as plain data.
 Draw order per config (one `numpy.random.default_rng(seed)` PCG64 stream):
 lengths, free order, [churn ops], q, k_pool, v_pool, k_new, v_new. Integer
 uniforms are inclusive on both ends.
+
+An fp8 (E4M3) cache for a batch (`fp8_cache`) comes from a stream of its own:
+its bytes are composed from random sign, exponent and mantissa fields, so no
+quantization is computed here either.
 """
 
 from .configs import (  # noqa: F401
@@ -28,4 +32,7 @@ from .configs import (  # noqa: F401
     config4_shared_prefix,
     config5_long_context,
     CONFIG_NAMES,
+    Fp8Cache,
+    fp8_codes,
+    fp8_cache,
 )

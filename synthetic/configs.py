@@ -299,3 +299,47 @@ def config5_long_context(block_size: int = 16, seed: int = 5,
     nb = _pool_for(lens + 1, block_size)
     return make_batch(f"long32k_gqa8_bs{block_size}", rng, lens, num_q_heads,
                       num_kv_heads, head_dim, block_size, nb, seed=seed)
+
+
+# --- fp8 (E4M3) cache -------------------------------------------------------
+@dataclass
+class Fp8Cache:
+    """An E4M3 KV cache for a batch: byte pools [NB][BS][Hkv][D] and one fp32
+    scale per KV head for K and for V."""
+    k_pool: np.ndarray
+    v_pool: np.ndarray
+    k_scale: np.ndarray
+    v_scale: np.ndarray
+
+
+def fp8_codes(rng: np.random.Generator, shape) -> np.ndarray:
+    """Random E4M3 bytes composed from their fields: a fair sign bit, an
+    exponent field drawn from 8..14 (magnitudes 2 .. 480, where a per-head
+    scaled N(0,1) tensor mostly lands) with more weight on the upper fields, and
+    a uniform mantissa. Field 15 with mantissa 7 (NaN) is never drawn."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint8)
+    exps = np.arange(8, 15)
+    w = np.array([1, 1, 2, 3, 4, 4, 3], dtype=np.float64)
+    w /= w.sum()
+    for lo in range(0, n, _CHUNK):
+        hi = min(n, lo + _CHUNK)
+        m = hi - lo
+        sign = rng.integers(0, 2, m, dtype=np.uint8)
+        e = rng.choice(exps, m, p=w).astype(np.uint8)
+        man = rng.integers(0, 8, m, dtype=np.uint8)
+        out[lo:hi] = (sign << 7) | (e << 3) | man
+    return out.reshape(shape)
+
+
+def fp8_cache(batch: "DecodeBatch", seed: int = 100) -> Fp8Cache:
+    """An E4M3 cache with the shape of `batch`'s pools, from its own stream
+    (draw order: k_pool, v_pool, k_scale, v_scale); scales U[0.002, 0.02]."""
+    rng = np.random.default_rng(seed)
+    shape = batch.k_pool.shape
+    hkv = shape[2]
+    k = fp8_codes(rng, shape)
+    v = fp8_codes(rng, shape)
+    ks = rng.uniform(0.002, 0.02, hkv).astype(np.float32)
+    vs = rng.uniform(0.002, 0.02, hkv).astype(np.float32)
+    return Fp8Cache(k, v, ks, vs)

@@ -43,3 +43,17 @@ def test_shared_prefix_step_inputs_keyed_by_step():
     q3, _, _ = w.step_inputs(1, 4)
     assert q1.tobytes() == q2.tobytes() and q1.tobytes() != q3.tobytes()
     assert k1.shape == (4, 8, 16)
+
+
+def test_fp8_cache_is_seeded_and_finite():
+    import synthetic
+    b = synthetic.config1_tiny()
+    a1 = synthetic.fp8_cache(b, seed=5)
+    a2 = synthetic.fp8_cache(b, seed=5)
+    assert (a1.k_pool == a2.k_pool).all() and (a1.v_scale == a2.v_scale).all()
+    assert a1.k_pool.shape == b.k_pool.shape and a1.k_pool.dtype == np.uint8
+    for pool in (a1.k_pool, a1.v_pool):
+        assert not ((pool & 0x7F) == 0x7F).any()          # no NaN codes
+        e = (pool >> 3) & 0xF
+        assert e.min() >= 8 and e.max() <= 14
+    assert (a1.k_scale > 0).all() and (a1.v_scale > 0).all()
