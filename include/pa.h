@@ -239,6 +239,58 @@ PA_API pa_status pa_decode_attention_fixed_scratch(
     int partition_tokens, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * fp8 KV cache — the append, the block copy and decode attention over pools
+ * of OCP E4M3 bytes with one fp32 scale per KV head for K and for V.
+ *
+ * Source: "Phase 7 · Document 04 — PagedAttention", §11 Engineering Decision
+ * Framework (shrink per-sequence KV with `--kv-cache-dtype fp8`, KV
+ * quantization) and §12 Hands-On Lab, step 3 (more sequences fit). The pages
+ * fix no format; this library reads it as: a cached value is
+ * e4m3(code) * scale[kv_head]; quantization is code = e4m3(fp32(x) /
+ * scale[kv_head]) with the division in IEEE fp32 and round-to-nearest-even,
+ * magnitudes above 448 saturating to 448.
+ *
+ * Pools: uint8 [num_blocks][block_size][num_kv_heads][head_dim], the same
+ * order as the fp16 pools, one byte per value. k_scale, v_scale: device fp32
+ * [num_kv_heads], 4-byte aligned, read only. Ownership, streams, device error
+ * word and status codes as for the fp16 calls.
+ * ---------------------------------------------------------------------- */
+
+/* pa_append_kv with quantization: row i of k_new/v_new (fp16, as in
+ * pa_append_kv) is quantized per KV head and written at slot_mapping[i]. */
+PA_API pa_status pa_append_kv_fp8(const pa_half* k_new, const pa_half* v_new,
+                                  uint8_t* k_pool, uint8_t* v_pool,
+                                  const int32_t* slot_mapping,
+                                  const float* k_scale, const float* v_scale,
+                                  int num_tokens, int num_kv_heads, int head_dim,
+                                  int block_size, int num_blocks, pa_stream_t stream);
+
+/* pa_copy_blocks over one-byte elements (head_dim a multiple of 16). */
+PA_API pa_status pa_copy_blocks_fp8(uint8_t* k_pool, uint8_t* v_pool,
+                                    const int32_t* pairs, int num_pairs,
+                                    int num_kv_heads, int head_dim, int block_size,
+                                    int num_blocks, pa_stream_t stream);
+
+/* pa_decode_attention over E4M3 pools: out[i][h] = sum_t softmax_t(scale *
+ * q[i][h] . Kd[t]) Vd[t] with Kd, Vd the dequantized rows (code value times
+ * the KV head's scale), computed in fp32 and rounded once to fp16. q, out,
+ * block_table, seq_lens, workspace (sized by pa_decode_workspace_bytes with
+ * the same shape) and partition_tokens as for pa_decode_attention.
+ * Supported shapes: head_dim 128; block_size 16 or 32; num_q_heads /
+ * num_kv_heads in {1, 2, 4, 8}; num_seqs <= 16384.
+ * Errors: as pa_decode_attention. */
+PA_API pa_status pa_decode_attention_fp8(const pa_half* q, const uint8_t* k_pool,
+                                         const uint8_t* v_pool,
+                                         const float* k_scale, const float* v_scale,
+                                         const int32_t* block_table,
+                                         const int32_t* seq_lens, int num_seqs,
+                                         int num_q_heads, int num_kv_heads, int head_dim,
+                                         int block_size, int max_blocks_per_seq,
+                                         int num_blocks, float scale, pa_half* out,
+                                         void* workspace, size_t workspace_bytes,
+                                         int partition_tokens, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Host block allocator (block manager). Host memory only; no CUDA calls.
  *
  * Source: "Phase 7 · Document 04 — PagedAttention", §2 (a pool of physical

@@ -34,6 +34,7 @@ from ._lib import (  # noqa: F401
 __all__ = [
     "pa_append_kv", "pa_copy_blocks", "pa_decode_attention",
     "pa_decode_workspace_bytes", "pa_decode_workspace_init", "pa_device_error",
+    "pa_append_kv_fp8", "pa_copy_blocks_fp8", "pa_decode_attention_fp8",
     "pa_decode_attention_fixed_scratch",
     "pa_version", "BlockAllocator", "PaError", "OutOfBlocksError", "lib",
     "DEFAULT_PARTITION_TOKENS",
@@ -164,6 +165,75 @@ def pa_decode_attention(q, k_pool, v_pool, block_table, seq_lens, scale, out=Non
             _dev(v_pool, "v_pool", torch.float16), _dev(block_table, "block_table", torch.int32),
             _dev(seq_lens, "seq_lens", torch.int32))
     _check(_load().pa_decode_attention(
+        *args, S, hq, hkv, d, bs, mb, nb, ctypes.c_float(float(scale)),
+        _dev(out, "out", torch.float16), _dev(workspace, "workspace", torch.uint8),
+        workspace.numel(), partition_tokens, _stream_ptr(stream)))
+    return out
+
+
+# ------------------------------------------------------- fp8 (E4M3) cache --
+def _scales(k_scale, v_scale, hkv):
+    torch = _torch()
+    if tuple(k_scale.shape) != (hkv,) or tuple(v_scale.shape) != (hkv,):
+        raise ValueError("k_scale and v_scale must be [num_kv_heads] fp32")
+    return _dev(k_scale, "k_scale", torch.float32), _dev(v_scale, "v_scale", torch.float32)
+
+
+def pa_append_kv_fp8(k_new, v_new, k_pool, v_pool, slot_mapping, k_scale, v_scale,
+                     stream=None) -> None:
+    """pa_append_kv into E4M3 pools (uint8 [NB][BS][Hkv][D]): row i of
+    k_new/v_new (fp16 [T][Hkv][D]) is quantized with the per-KV-head scales
+    and written at slot slot_mapping[i]."""
+    torch = _torch()
+    nb, bs, hkv, d = _pool_dims(k_pool, v_pool)
+    T = int(slot_mapping.numel())
+    if tuple(k_new.shape) != (T, hkv, d) or tuple(v_new.shape) != (T, hkv, d):
+        raise ValueError("k_new/v_new must be [num_tokens][kv_heads][head_dim]")
+    ks, vs = _scales(k_scale, v_scale, hkv)
+    args = (_dev(k_new, "k_new", torch.float16), _dev(v_new, "v_new", torch.float16),
+            _dev(k_pool, "k_pool", torch.uint8), _dev(v_pool, "v_pool", torch.uint8),
+            _dev(slot_mapping, "slot_mapping", torch.int32), ks, vs)
+    _check(_load().pa_append_kv_fp8(*args, T, hkv, d, bs, nb, _stream_ptr(stream)))
+
+
+def pa_copy_blocks_fp8(k_pool, v_pool, pairs, stream=None) -> None:
+    """pa_copy_blocks over E4M3 pools (uint8 [NB][BS][Hkv][D])."""
+    torch = _torch()
+    nb, bs, hkv, d = _pool_dims(k_pool, v_pool)
+    if pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be [n][2]")
+    n = int(pairs.shape[0])
+    args = (_dev(k_pool, "k_pool", torch.uint8), _dev(v_pool, "v_pool", torch.uint8),
+            _dev(pairs, "pairs", torch.int32))
+    _check(_load().pa_copy_blocks_fp8(*args, n, hkv, d, bs, nb, _stream_ptr(stream)))
+
+
+def pa_decode_attention_fp8(q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, scale,
+                            out=None, workspace=None, partition_tokens: int = 0, stream=None):
+    """pa_decode_attention over E4M3 pools (uint8 [NB][BS][Hkv][D]) with fp32
+    per-KV-head scales k_scale, v_scale [Hkv]. Returns out [S][Hq][D] fp16."""
+    torch = _torch()
+    nb, bs, hkv, d = _pool_dims(k_pool, v_pool)
+    if q.dim() != 3 or int(q.shape[2]) != d:
+        raise ValueError("q must be [num_seqs][num_q_heads][head_dim]")
+    S, hq = int(q.shape[0]), int(q.shape[1])
+    if block_table.dim() != 2 or int(block_table.shape[0]) != S:
+        raise ValueError("block_table must be [num_seqs][max_blocks_per_seq]")
+    mb = int(block_table.shape[1])
+    if tuple(seq_lens.shape) != (S,):
+        raise ValueError("seq_lens must be [num_seqs]")
+    if out is None:
+        out = torch.empty_like(q)
+    elif tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must have q's shape")
+    if workspace is None:
+        workspace = alloc_workspace(S, hq, hkv, d, bs, mb, partition_tokens, q.device)
+    ks, vs = _scales(k_scale, v_scale, hkv)
+    args = (_dev(q, "q", torch.float16), _dev(k_pool, "k_pool", torch.uint8),
+            _dev(v_pool, "v_pool", torch.uint8), ks, vs,
+            _dev(block_table, "block_table", torch.int32),
+            _dev(seq_lens, "seq_lens", torch.int32))
+    _check(_load().pa_decode_attention_fp8(
         *args, S, hq, hkv, d, bs, mb, nb, ctypes.c_float(float(scale)),
         _dev(out, "out", torch.float16), _dev(workspace, "workspace", torch.uint8),
         workspace.numel(), partition_tokens, _stream_ptr(stream)))

@@ -66,6 +66,11 @@ SIGNATURES = {
                                    _i32, _i32, _f32, _vp, _vp, _sz, _i32, _vp]),
     "pa_decode_attention_fixed_scratch": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                                  _i32, _i32, _i32, _f32, _vp, _i32, _vp]),
+    "pa_append_kv_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                _vp]),
+    "pa_copy_blocks_fp8": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp]),
+    "pa_decode_attention_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                                       _i32, _i32, _i32, _f32, _vp, _vp, _sz, _i32, _vp]),
     "pa_alloc_create": (_i32, [_i32, _i32, _pi32, ctypes.POINTER(_vp)]),
     "pa_alloc_destroy": (None, [_vp]),
     "pa_alloc_add_seq": (_i32, [_vp, _i64, _i64]),

@@ -8,6 +8,13 @@
 // Concept, on-demand allocation). Copy: copy-on-write of a shared block (§2
 // "block sharing", §3 Mental Model; lux-666 notes "PagedAttention", prefix
 // sharing section).
+//
+// fp8 cache (Document 04, §11: `--kv-cache-dtype fp8`, KV quantization to fit
+// more sequences): the append quantizes each fp16 value to an OCP E4M3 byte,
+// code = e4m3(fp32(x) / scale[head]) with the division in IEEE fp32 and the
+// conversion rounding to nearest even and saturating at +-448; the block copy
+// is the same bit copy over one-byte elements.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -50,6 +57,57 @@ append_kv_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_ne
     const uint4 b = __ldg(vs + i);
     kd[i] = a;
     vd[i] = b;
+  }
+}
+
+// Two fp32 values -> two E4M3 bytes (lo in the low byte), round to nearest
+// even, saturating.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// One CTA per appended token: quantize its K row and V row (Hkv*D fp16 each)
+// to E4M3 and store them in pool row `slot`. Each thread takes 8 values (one
+// 16-byte load, one 8-byte store) of one head.
+__global__ void __launch_bounds__(kAppendThreads)
+append_kv_fp8_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                     uint2* __restrict__ k_pool, uint2* __restrict__ v_pool,
+                     const int32_t* __restrict__ slots, const float* __restrict__ k_scale,
+                     const float* __restrict__ v_scale, int row_vecs, int head_vecs,
+                     int64_t num_slots, int32_t* __restrict__ err) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int t = blockIdx.x;
+  const int32_t slot = __ldg(slots + t);
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (threadIdx.x == 0) atomicOr(err, PA_DEVERR_BAD_SLOT);
+    return;
+  }
+  const uint4* ks = k_new + static_cast<int64_t>(t) * row_vecs;
+  const uint4* vs = v_new + static_cast<int64_t>(t) * row_vecs;
+  uint2* kd = k_pool + static_cast<int64_t>(slot) * row_vecs;
+  uint2* vd = v_pool + static_cast<int64_t>(slot) * row_vecs;
+  for (int i = threadIdx.x; i < row_vecs; i += kAppendThreads) {
+    const int h = i / head_vecs;
+    const float sk = __ldg(k_scale + h), sv = __ldg(v_scale + h);
+    const uint4 a = __ldg(ks + i);
+    const uint4 b = __ldg(vs + i);
+    const __half2* ah = reinterpret_cast<const __half2*>(&a);
+    const __half2* bh = reinterpret_cast<const __half2*>(&b);
+    uint32_t ko[2] = {0, 0}, vo[2] = {0, 0};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 x = __half22float2(ah[j]);
+      const float2 y = __half22float2(bh[j]);
+      const uint32_t kq = f32x2_to_e4m3x2(__fdiv_rn(x.x, sk), __fdiv_rn(x.y, sk));
+      const uint32_t vq = f32x2_to_e4m3x2(__fdiv_rn(y.x, sv), __fdiv_rn(y.y, sv));
+      ko[j >> 1] |= kq << (16 * (j & 1));
+      vo[j >> 1] |= vq << (16 * (j & 1));
+    }
+    kd[i] = make_uint2(ko[0], ko[1]);
+    vd[i] = make_uint2(vo[0], vo[1]);
   }
 }
 
@@ -222,6 +280,80 @@ pa_status pa_copy_blocks(pa_half* k_pool, pa_half* v_pool, const int32_t* pairs,
       num_blocks, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_copy_blocks launch");
+  return pa::ok();
+}
+
+pa_status pa_append_kv_fp8(const pa_half* k_new, const pa_half* v_new, uint8_t* k_pool,
+                           uint8_t* v_pool, const int32_t* slot_mapping, const float* k_scale,
+                           const float* v_scale, int num_tokens, int num_kv_heads, int head_dim,
+                           int block_size, int num_blocks, pa_stream_t stream) {
+  if (pa_status s = check_pool_shape("pa_append_kv_fp8", num_kv_heads, head_dim, block_size,
+                                     num_blocks))
+    return s;
+  if (num_tokens < 0) return pa::fail(PA_ERR_INVALID_ARG, "pa_append_kv_fp8: num_tokens < 0");
+  if (num_tokens == 0) return pa::ok();
+  if (!k_new || !v_new || !k_pool || !v_pool || !slot_mapping || !k_scale || !v_scale)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_append_kv_fp8: NULL pointer");
+  if (!pa::aligned16(k_new) || !pa::aligned16(v_new) || !pa::aligned16(k_pool) ||
+      !pa::aligned16(v_pool) || (reinterpret_cast<uintptr_t>(slot_mapping) & 3) ||
+      (reinterpret_cast<uintptr_t>(k_scale) & 3) || (reinterpret_cast<uintptr_t>(v_scale) & 3))
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_append_kv_fp8: misaligned pointer");
+  pa::DeviceInfo dev;
+  if (pa_status s = pa::current_device(&dev)) return s;
+  int32_t* err = pa::device_error_word();
+  if (!err) return PA_ERR_CUDA;
+  {
+    static std::mutex mu;
+    static bool set[64] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (!set[dev.device]) {
+      cudaError_t e = cudaFuncSetAttribute(append_kv_fp8_kernel,
+                                           cudaFuncAttributePreferredSharedMemoryCarveout,
+                                           cudaSharedmemCarveoutMaxShared);
+      if (e != cudaSuccess) return pa::cuda_fail(e, "cudaFuncSetAttribute(append fp8)");
+      set[dev.device] = true;
+    }
+  }
+  const int row_vecs = num_kv_heads * head_dim / 8;
+  append_kv_fp8_kernel<<<num_tokens, kAppendThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint4*>(k_new), reinterpret_cast<const uint4*>(v_new),
+      reinterpret_cast<uint2*>(k_pool), reinterpret_cast<uint2*>(v_pool), slot_mapping, k_scale,
+      v_scale, row_vecs, head_dim / 8, static_cast<int64_t>(num_blocks) * block_size, err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return pa::cuda_fail(e, "pa_append_kv_fp8 launch");
+  return pa::ok();
+}
+
+pa_status pa_copy_blocks_fp8(uint8_t* k_pool, uint8_t* v_pool, const int32_t* pairs,
+                             int num_pairs, int num_kv_heads, int head_dim, int block_size,
+                             int num_blocks, pa_stream_t stream) {
+  if (pa_status s = check_pool_shape("pa_copy_blocks_fp8", num_kv_heads, head_dim, block_size,
+                                     num_blocks))
+    return s;
+  if (head_dim % 16)
+    return pa::fail(PA_ERR_UNSUPPORTED, "pa_copy_blocks_fp8: head_dim %d not a multiple of 16",
+                    head_dim);
+  if (num_pairs < 0) return pa::fail(PA_ERR_INVALID_ARG, "pa_copy_blocks_fp8: num_pairs < 0");
+  if (num_pairs == 0) return pa::ok();
+  if (!k_pool || !v_pool || !pairs)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_copy_blocks_fp8: NULL pointer");
+  if (!pa::aligned16(k_pool) || !pa::aligned16(v_pool) ||
+      (reinterpret_cast<uintptr_t>(pairs) & 3))
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_copy_blocks_fp8: misaligned pointer");
+  pa::DeviceInfo dev;
+  if (pa_status s = pa::current_device(&dev)) return s;
+  int32_t* err = pa::device_error_word();
+  if (!err) return PA_ERR_CUDA;
+  const int64_t block_vecs = static_cast<int64_t>(block_size) * num_kv_heads * head_dim / 16;
+  const int64_t slice = static_cast<int64_t>(kCopyThreads) * kCopyVecsPerThread;
+  const int64_t slices = (block_vecs + slice - 1) / slice;
+  if (slices > 65535) return pa::fail(PA_ERR_UNSUPPORTED, "pa_copy_blocks_fp8: block too large");
+  dim3 grid(num_pairs, static_cast<unsigned>(slices));
+  copy_blocks_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<uint4*>(k_pool), reinterpret_cast<uint4*>(v_pool), pairs, block_vecs,
+      num_blocks, err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return pa::cuda_fail(e, "pa_copy_blocks_fp8 launch");
   return pa::ok();
 }
 

@@ -143,6 +143,27 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// Two E4M3 bytes (low 16 bits of v) -> two fp16 (f16x2, byte 0 in the low
+// half); exact, every E4M3 value is an fp16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
+  uint32_t r;
+  const uint16_t b = static_cast<uint16_t>(v);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(b));
+  return r;
+}
+// Byte permute: result byte i = byte (sel >> 4i) & 7 of {b, a} (a = bytes 0..3).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+// Transpose of an 8x8 matrix of 16-bit values held one row-pair per lane in
+// the mma fragment layout (lane t: row t/4, columns 2(t%4), 2(t%4)+1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(a));
+  return r;
+}
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -212,11 +233,13 @@ __host__ __device__ constexpr int head_group(int hkv) {
   return hkv % 8 == 0 ? 8 : hkv % 4 == 0 ? 4 : hkv % 2 == 0 ? 2 : 1;
 }
 
-template <int D, int BS, int G>
+template <int D, int BS, int G, bool KV8 = false>
 struct Shape {
   static_assert(G >= 1 && G <= 8, "at most 8 query heads per KV head (mma N = 8)");
   static_assert(D % 64 == 0 && BS % 8 == 0, "shape");
-  static constexpr int NHALF = D / 64;               // 64-dim (128-byte) halves per row
+  static_assert(!KV8 || (D == 128 && BS >= 16), "fp8 pools: head_dim 128, 16-token stages");
+  static constexpr int ESZ = KV8 ? 1 : 2;            // bytes per cached value
+  static constexpr int NHALF = D * ESZ / 128;        // 128-byte lines per row
   static constexpr int TS = BS < 16 ? BS : 16;       // tokens per stage
   static constexpr int KSTEPS = D / 16;              // QK k-steps over head_dim
   static constexpr int MT = D / 16;                  // PV m-tiles over head_dim
@@ -254,6 +277,8 @@ struct DecodeParams {
   const int32_t* block_table;
   const int32_t* seq_lens;
   __half* out;
+  const float* k_scale;  // fp8 pools: [num_kv_heads] dequantization scales (else unused)
+  const float* v_scale;
   float* records;  // [2 * max_chunks][HG][rec_floats(G, D)] partials of cut segments
   unsigned long long* counters;  // [num_seqs][num_kv_heads] (tag << kArrivalBits) | arrivals
   unsigned long long tag;        // this call's tag, nonzero, < 2^(64 - kArrivalBits)
@@ -562,11 +587,11 @@ __device__ __forceinline__ void merge_partials(const float* recs, int E, RecOf r
   }
 }
 
-template <int D, int BS, int G>
+template <int D, int BS, int G, bool KV8>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     paged_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap) {
-  using SH = Shape<D, BS, G>;
+  using SH = Shape<D, BS, G, KV8>;
   constexpr int TS = SH::TS;
   constexpr int QBYTES_PER_HEAD = G * D * 2;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -736,9 +761,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
               const uint32_t kdst = smem_addr(ring + static_cast<size_t>(stage) * STAGE);
 #pragma unroll
               for (int h = 0; h < SH::NHALF; ++h) {
-                tma_load_4d(kdst + h * HALF, &kmap, 64 * h, sb * TS, P.cur.hg * HG, phys, fb);
-                tma_load_4d(kdst + TILE + h * HALF, &vmap, 64 * h, sb * TS, P.cur.hg * HG, phys,
-                            fb);
+                const int x = (128 / SH::ESZ) * h;  // first value of the 128-byte line
+                tma_load_4d(kdst + h * HALF, &kmap, x, sb * TS, P.cur.hg * HG, phys, fb);
+                tma_load_4d(kdst + TILE + h * HALF, &vmap, x, sb * TS, P.cur.hg * HG, phys, fb);
               }
             }
           }
@@ -852,27 +877,44 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     const PieceMeta pm = pmeta[qs];
     const int pj = pm.j, n = pm.n, L = pm.len;
     const int kvh = pm.hg * HG + w;
-    uint32_t qa[SH::KSTEPS][2];  // A fragments a0/a2 per k-step; rows (heads) >= G are zero
-    {
-      const uint32_t qrow = smem_addr(qslot + qs * QSLOT) +
-                            (w * G + (ld_row < G ? ld_row : 0)) * (D * 2);
+    const bool cut = pj > 0 || pj + n < pm.nb;
+    __half* out_row = p.out + (static_cast<long long>(pm.seq) * p.num_q_heads +
+                               static_cast<long long>(kvh) * G) * D;
+    // a cut piece's partial record: slot 0 if the piece starts its chunk, else 1
+    const int s0 = pm.s0;
+    float* rec = p.records + ((2ll * pm.c + (s0 + pj == pm.c * chunk ? 0 : 1)) * HG + w) *
+                                 static_cast<long long>(SH::REC);
+    if constexpr (KV8) {
+      // ---- fp8 pools: E4M3 tiles, converted to fp16 fragments in registers ----
+      // Scores as S^T = K Q^T: the 16 tokens of a stage are the M rows, the
+      // heads the N columns, so a stage takes D/16 mma. The K fragments come
+      // from ldmatrix on byte pairs: lane (gid, tig) gets 4 consecutive values
+      // (dims 4*tig .. +3 of a 16-dim chunk) of token gid (and gid + 8); the
+      // dot product's order over dims is free, so mma k-index 2*tig + e takes
+      // dim 4*tig + e and k-index 2*tig + 8 + e takes dim 4*tig + 2 + e, and q
+      // is loaded in the same order. k_scale folds into the score scale and
+      // v_scale into the result.
+      uint32_t qb[D / 16][2];
+      {
+        const unsigned char* qrow =
+            qslot + qs * QSLOT + (w * G + (gid < G ? gid : 0)) * (D * 2);
 #pragma unroll
-      for (int kk = 0; kk < SH::KSTEPS; kk += 2) {
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4(qrow + (2 * kk + ld_mat) * 16, r0, r1, r2, r3);
-        qa[kk][0] = gid < G ? r0 : 0u;
-        qa[kk][1] = gid < G ? r1 : 0u;
-        qa[kk + 1][0] = gid < G ? r2 : 0u;
-        qa[kk + 1][1] = gid < G ? r3 : 0u;
+        for (int c = 0; c < D / 16; ++c) {
+          const uint2 v = *reinterpret_cast<const uint2*>(qrow + (16 * c + 4 * tig) * 2);
+          qb[c][0] = gid < G ? v.x : 0u;
+          qb[c][1] = gid < G ? v.y : 0u;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&qempty_bar[qs]));
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&qempty_bar[qs]));
-    }
-
-      float m_run = -INFINITY, l_run = 0.f;  // head gid: running max (log2 units), partial sum
-      float o[SH::MT][4];                     // O^T[d = mt*16 + gid (+8)][h = 2*tig (+1)]
+      const float qsc = p.qscale * __ldg(p.k_scale + kvh);
+      const float vsc = __ldg(p.v_scale + kvh);
+      float m0 = -INFINITY, m1 = -INFINITY;  // heads 2*tig, 2*tig+1: running max (log2 units)
+      float l0 = 0.f, l1 = 0.f;              // and partial sums over this lane's tokens
+      float o[D / 16][4];                    // O^T[dim 16*mt + 2*gid (+1)][head 2*tig (+1)]
 #pragma unroll
-      for (int mt = 0; mt < SH::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+      for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+      const int tok = ((ld_mat & 1) << 3) + ld_row;  // row this lane addresses for ldmatrix
 
       for (int jj = 0; jj < n; ++jj) {
         const int blk = pj + jj;
@@ -887,91 +929,76 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           unsigned char* vt = kt + TILE;
           if (rows < TS) {
             // rows past the sequence end must add exactly zero to P V
-            const int words = (TS - rows) * 8;  // 16-byte words per half
-#pragma unroll
-            for (int h = 0; h < SH::NHALF; ++h) {
-              uint4* z = reinterpret_cast<uint4*>(vt + h * HALF + (w * TS + rows) * 128);
-              for (int i = lane; i < words; i += 32) z[i] = make_uint4(0, 0, 0, 0);
-            }
+            uint4* z = reinterpret_cast<uint4*>(vt + (w * TS + rows) * 128);
+            for (int i = lane; i < (TS - rows) * 8; i += 32) z[i] = make_uint4(0, 0, 0, 0);
             __syncwarp();
           }
           const uint32_t kaddr = smem_addr(kt) + w * TS * 128;
           const uint32_t vaddr = smem_addr(vt) + w * TS * 128;
 
-          // ---- S = Q K^T for each 8-token group ----
-          // x4 of k-steps (kk, kk+1): matrix m covers dims (2*kk + m) * 8 .. +8
-          float s[SH::NT][4];
+          // ---- S^T = K Q^T ----
+          float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int nt = 0; nt < SH::NT; ++nt) {
-            s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-            const uint32_t rowa = kaddr + (nt * 8 + ld_row) * 128;
-#pragma unroll
-            for (int kk = 0; kk < SH::KSTEPS; kk += 2) {
-              const int gc = 2 * kk + ld_mat;  // 16-byte chunk of the row, 0 .. D/8-1
-              uint32_t b0, b1, b2, b3;
-              ldsm_x4(rowa + (gc >> 3) * HALF + (((gc & 7) ^ ld_row) << 4), b0, b1, b2, b3);
-              mma_16816(s[nt], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
-              mma_16816(s[nt], qa[kk + 1][0], 0u, qa[kk + 1][1], 0u, b2, b3);
-            }
+          for (int cc = 0; cc < D / 32; ++cc) {
+            // matrices: tokens 0-7 / 8-15 of 16-dim chunks 2*cc and 2*cc + 1
+            const int ch = 2 * cc + (ld_mat >> 1);
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4(kaddr + tok * 128 + ((ch ^ ld_row) << 4), r0, r1, r2, r3);
+            mma_16816(sc, e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r0 >> 16),
+                      e4m3x2_to_f16x2(r1 >> 16), qb[2 * cc][0], qb[2 * cc][1]);
+            mma_16816(sc, e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
+                      e4m3x2_to_f16x2(r3 >> 16), qb[2 * cc + 1][0], qb[2 * cc + 1][1]);
           }
-          // ---- online softmax over this stage's tokens (row gid = head) ----
-          float mx = -INFINITY;
+          // ---- online softmax per head over the stage's tokens ----
+          // sc: [token gid][head 2tig], [gid][2tig+1], [gid+8][2tig], [gid+8][2tig+1]
+          const bool t0 = gid < rows, t1 = gid + 8 < rows;
+          const float x0 = t0 ? sc[0] * qsc : -INFINITY;
+          const float x1 = t0 ? sc[1] * qsc : -INFINITY;
+          const float x2 = t1 ? sc[2] * qsc : -INFINITY;
+          const float x3 = t1 ? sc[3] * qsc : -INFINITY;
+          float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
-          for (int nt = 0; nt < SH::NT; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int t = nt * 8 + 2 * tig + e;
-              const float v = t < rows ? s[nt][e] * p.qscale : -INFINITY;
-              s[nt][e] = v;
-              mx = fmaxf(mx, v);
-            }
+          for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
           }
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          const float m_new = fmaxf(m_run, mx);
-          const float mu = m_new == -INFINITY ? 0.f : m_new;
-          const float alpha = fast_exp2(m_run - mu);
-          m_run = m_new;
-          float ps = 0.f;
-          uint32_t pb[SH::NT];  // P as fp16 pairs: B operand of the PV mma
+          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+          const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+          const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+          const float al0 = fast_exp2(m0 - mu0), al1 = fast_exp2(m1 - mu1);
+          m0 = mn0;
+          m1 = mn1;
+          const float p0 = fast_exp2(x0 - mu0), p1 = fast_exp2(x1 - mu1);
+          const float p2 = fast_exp2(x2 - mu0), p3 = fast_exp2(x3 - mu1);
+          l0 = l0 * al0 + p0 + p2;
+          l1 = l1 * al1 + p1 + p3;
 #pragma unroll
-          for (int nt = 0; nt < SH::NT; ++nt) {
-            const float p0 = fast_exp2(s[nt][0] - mu);
-            const float p1 = fast_exp2(s[nt][1] - mu);
-            ps += p0 + p1;
-            pb[nt] = pack_half2(p0, p1);
+          for (int mt = 0; mt < D / 16; ++mt) {
+            o[mt][0] *= al0;
+            o[mt][1] *= al1;
+            o[mt][2] *= al0;
+            o[mt][3] *= al1;
           }
-          l_run = l_run * alpha + ps;
-          // rescale O^T columns: heads 2*tig and 2*tig+1 live in mma groups 2*tig, 2*tig+1
-          const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * tig);
-          const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);
+          // P^T as the B operand (k = token, n = head): transpose the two
+          // 8x8 blocks (tokens 0-7 and 8-15) of P held [token][head]
+          const uint32_t pb0 = movmatrix_trans(pack_half2(p0, p1));
+          const uint32_t pb1 = movmatrix_trans(pack_half2(p2, p3));
+          // ---- O^T += V^T P^T ----
+          // ldmatrix.trans on byte pairs gives lane (gid, tig) the bytes
+          // V[2tig][d], V[2tig][d+1], V[2tig+1][d], V[2tig+1][d+1] with
+          // d = 2*gid of the chunk; A row gid takes dim d and row gid + 8 dim
+          // d + 1 (the rows of O^T are then those dims).
 #pragma unroll
-          for (int mt = 0; mt < SH::MT; ++mt) {
-            o[mt][0] *= a_lo;
-            o[mt][1] *= a_hi;
-            o[mt][2] *= a_lo;
-            o[mt][3] *= a_hi;
-          }
-          // ---- O^T += V^T P^T over 16-token k-steps ----
-          // x4.trans of m-tile mt: matrix m covers tokens +8*(m>>1), dims mt*16 + 8*(m&1)
-#pragma unroll
-          for (int pk = 0; pk < SH::PK; ++pk) {
-            const uint32_t pb0 = pb[2 * pk];
-            const uint32_t pb1 = (2 * pk + 1 < SH::NT) ? pb[2 * pk + 1] : 0u;
-            const uint32_t rowa = vaddr + (pk * 16 + ld_row + (ld_mat >> 1) * 8) * 128;
-#pragma unroll
-            for (int mt = 0; mt < SH::MT; ++mt) {
-              const int gc = 2 * mt + (ld_mat & 1);
-              const uint32_t addr = rowa + (gc >> 3) * HALF + (((gc & 7) ^ ld_row) << 4);
-              uint32_t a0, a1, a2, a3;
-              if (2 * pk + 1 < SH::NT) {
-                ldsm_x4_t(addr, a0, a1, a2, a3);
-              } else {
-                ldsm_x2_t(addr, a0, a1);
-                a2 = a3 = 0u;
-              }
-              mma_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
-            }
+          for (int cc = 0; cc < D / 32; ++cc) {
+            const int ch = 2 * cc + (ld_mat >> 1);
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4_t(vaddr + tok * 128 + ((ch ^ ld_row) << 4), r0, r1, r2, r3);
+            const uint32_t u0 = prmt(r0, 0u, 0x3120u), u1 = prmt(r1, 0u, 0x3120u);
+            const uint32_t u2 = prmt(r2, 0u, 0x3120u), u3 = prmt(r3, 0u, 0x3120u);
+            mma_16816(o[2 * cc], e4m3x2_to_f16x2(u0), e4m3x2_to_f16x2(u0 >> 16),
+                      e4m3x2_to_f16x2(u1), e4m3x2_to_f16x2(u1 >> 16), pb0, pb1);
+            mma_16816(o[2 * cc + 1], e4m3x2_to_f16x2(u2), e4m3x2_to_f16x2(u2 >> 16),
+                      e4m3x2_to_f16x2(u3), e4m3x2_to_f16x2(u3 >> 16), pb0, pb1);
           }
           if (rows < TS) fence_proxy_async_smem();  // generic zero-fill before the next TMA write
           __syncwarp();
@@ -979,100 +1006,264 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         }
       }
 
-      // ---- piece finished: this warp holds its head's whole state ----
-      l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-      l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-      const bool cut = pj > 0 || pj + n < pm.nb;
-      __half* out_row = p.out + (static_cast<long long>(pm.seq) * p.num_q_heads +
-                                 static_cast<long long>(kvh) * G) * D;
+      // ---- piece finished: sums over all tokens of the piece ----
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+      }
       const int h0 = 2 * tig, h1 = 2 * tig + 1;
       if (!cut) {
-        const float l0 = __shfl_sync(0xffffffffu, l_run, 8 * tig);
-        const float l1 = __shfl_sync(0xffffffffu, l_run, 8 * tig + 4);
-        const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+        const float i0 = l0 > 0.f ? vsc / l0 : 0.f, i1 = l1 > 0.f ? vsc / l1 : 0.f;
 #pragma unroll
-        for (int mt = 0; mt < SH::MT; ++mt) {
-          const int d = mt * 16 + gid;
-          if (h0 < G) {
-            out_row[h0 * D + d] = __float2half_rn(o[mt][0] * i0);
-            out_row[h0 * D + d + 8] = __float2half_rn(o[mt][2] * i0);
-          }
-          if (h1 < G) {
-            out_row[h1 * D + d] = __float2half_rn(o[mt][1] * i1);
-            out_row[h1 * D + d + 8] = __float2half_rn(o[mt][3] * i1);
-          }
+        for (int mt = 0; mt < D / 16; ++mt) {
+          const int d = mt * 16 + 2 * gid;
+          if (h0 < G)
+            *reinterpret_cast<__half2*>(out_row + h0 * D + d) =
+                __floats2half2_rn(o[mt][0] * i0, o[mt][2] * i0);
+          if (h1 < G)
+            *reinterpret_cast<__half2*>(out_row + h1 * D + d) =
+                __floats2half2_rn(o[mt][1] * i1, o[mt][3] * i1);
         }
       } else {
-        // cut segment: record this chunk's partial (slot 0 if the piece starts
-        // the chunk, else 1); the last of the segment's chunks to arrive merges
-        const int s0 = pm.s0;
-        const int slot = s0 + pj == pm.c * chunk ? 0 : 1;
-        float* rec = p.records + ((2ll * pm.c + slot) * HG + w) * static_cast<long long>(SH::REC);
+        // the record holds the dequantized accumulator (v_scale applied)
 #pragma unroll
-        for (int mt = 0; mt < SH::MT; ++mt) {
-          const int d = mt * 16 + gid;
+        for (int mt = 0; mt < D / 16; ++mt) {
+          const int d = mt * 16 + 2 * gid;
+          if (h0 < G)
+            *reinterpret_cast<float2*>(rec + h0 * D + d) = make_float2(o[mt][0] * vsc, o[mt][2] * vsc);
+          if (h1 < G)
+            *reinterpret_cast<float2*>(rec + h1 * D + d) = make_float2(o[mt][1] * vsc, o[mt][3] * vsc);
+        }
+        if (gid == 0) {
           if (h0 < G) {
-            rec[h0 * D + d] = o[mt][0];
-            rec[h0 * D + d + 8] = o[mt][2];
+            rec[G * D + 2 * h0] = m0;
+            rec[G * D + 2 * h0 + 1] = l0;
           }
           if (h1 < G) {
-            rec[h1 * D + d] = o[mt][1];
-            rec[h1 * D + d + 8] = o[mt][3];
-          }
-        }
-        if (tig == 0 && gid < G) {
-          rec[G * D + 2 * gid] = m_run;
-          rec[G * D + 2 * gid + 1] = l_run;
-        }
-        if (!pm.last) {
-          // hand the arrival (and any merge) to the merge warps: the warp
-          // barrier orders every lane's record stores before lane 0's arrival,
-          // whose release makes them visible to the merge warps' acquire
-          if (mc >= kMsgSlots)
-            warp_wait_phase(smem_addr(&mempty_bar[mc % kMsgSlots]), ((mc / kMsgSlots) - 1) & 1,
-                            abort_flag, p.err);
-          if (w == 0 && lane == 0) {
-            MsgMeta* m = mmeta + mc % kMsgSlots;
-            m->seq = pm.seq;
-            m->hg = pm.hg;
-            m->nb = pm.nb;
-            m->s0 = s0;
-            m->stop = 0;
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_addr(&mfull_bar[mc % kMsgSlots]));
-          ++mc;
-        } else {
-          // The CTA's last piece: count the arrival here and merge if it
-          // completes the segment, which it usually does (the other chunks'
-          // pieces are mostly done). First try to claim the last arrival
-          // outright: a last arrival's record is read by no other warp, so it
-          // needs no release and the claim does not wait for its stores.
-          // Otherwise release the record and count the arrival as usual.
-          __syncwarp();  // the record's lanes, before any lane reads it back
-          const int c_first = s0 / chunk, c_last = (s0 + pm.nb - 1) / chunk;
-          const int E = c_last - c_first + 1;
-          unsigned long long* word = p.counters + static_cast<long long>(pm.seq) * Hkv + kvh;
-          const unsigned long long claim = (p.tag << kArrivalBits) | static_cast<unsigned>(E - 1);
-          int done = 0;
-          if (lane == 0) done = atomicCAS(word, claim, 0ull) == claim;
-          done = __shfl_sync(0xffffffffu, done, 0);
-          if (!done) {
-            fence_acq_rel_gpu();  // release: the record is visible before the arrival
-            __syncwarp();
-            if (lane == 0) done = arrive_last(word, p.tag, static_cast<unsigned>(E), false, p.err);
-            done = __shfl_sync(0xffffffffu, done, 0);
-          }
-          if (done) {
-            // acquire: the other chunks' records are visible to this warp
-            fence_acq_rel_gpu();
-            auto rec_of = [&](int i) -> long long {
-              return record_index(c_first + i, c_first, s0, chunk, HG, w);
-            };
-            merge_partials<D, G>(p.records, E, rec_of, out_row);
+            rec[G * D + 2 * h1] = m1;
+            rec[G * D + 2 * h1 + 1] = l1;
           }
         }
       }
+    } else {
+      uint32_t qa[SH::KSTEPS][2];  // A fragments a0/a2 per k-step; rows (heads) >= G are zero
+      {
+        const uint32_t qrow = smem_addr(qslot + qs * QSLOT) +
+                              (w * G + (ld_row < G ? ld_row : 0)) * (D * 2);
+  #pragma unroll
+        for (int kk = 0; kk < SH::KSTEPS; kk += 2) {
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4(qrow + (2 * kk + ld_mat) * 16, r0, r1, r2, r3);
+          qa[kk][0] = gid < G ? r0 : 0u;
+          qa[kk][1] = gid < G ? r1 : 0u;
+          qa[kk + 1][0] = gid < G ? r2 : 0u;
+          qa[kk + 1][1] = gid < G ? r3 : 0u;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&qempty_bar[qs]));
+      }
+
+        float m_run = -INFINITY, l_run = 0.f;  // head gid: running max (log2 units), partial sum
+        float o[SH::MT][4];                     // O^T[d = mt*16 + gid (+8)][h = 2*tig (+1)]
+  #pragma unroll
+        for (int mt = 0; mt < SH::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+        for (int jj = 0; jj < n; ++jj) {
+          const int blk = pj + jj;
+          const int vb = min(BS, L - blk * BS);
+          const int nsb = (vb + TS - 1) / TS;
+          for (int sb = 0; sb < nsb; ++sb, ++g) {
+            const int stage = g % NST;
+            if (!warp_wait_phase(smem_addr(&full_bar[stage]), (g / NST) & 1, abort_flag, p.err))
+              continue;
+            const int rows = min(TS, vb - sb * TS);
+            unsigned char* kt = ring + static_cast<size_t>(stage) * STAGE;
+            unsigned char* vt = kt + TILE;
+            if (rows < TS) {
+              // rows past the sequence end must add exactly zero to P V
+              const int words = (TS - rows) * 8;  // 16-byte words per half
+  #pragma unroll
+              for (int h = 0; h < SH::NHALF; ++h) {
+                uint4* z = reinterpret_cast<uint4*>(vt + h * HALF + (w * TS + rows) * 128);
+                for (int i = lane; i < words; i += 32) z[i] = make_uint4(0, 0, 0, 0);
+              }
+              __syncwarp();
+            }
+            const uint32_t kaddr = smem_addr(kt) + w * TS * 128;
+            const uint32_t vaddr = smem_addr(vt) + w * TS * 128;
+
+            // ---- S = Q K^T for each 8-token group ----
+            // x4 of k-steps (kk, kk+1): matrix m covers dims (2*kk + m) * 8 .. +8
+            float s[SH::NT][4];
+  #pragma unroll
+            for (int nt = 0; nt < SH::NT; ++nt) {
+              s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+              const uint32_t rowa = kaddr + (nt * 8 + ld_row) * 128;
+  #pragma unroll
+              for (int kk = 0; kk < SH::KSTEPS; kk += 2) {
+                const int gc = 2 * kk + ld_mat;  // 16-byte chunk of the row, 0 .. D/8-1
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(rowa + (gc >> 3) * HALF + (((gc & 7) ^ ld_row) << 4), b0, b1, b2, b3);
+                mma_16816(s[nt], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+                mma_16816(s[nt], qa[kk + 1][0], 0u, qa[kk + 1][1], 0u, b2, b3);
+              }
+            }
+            // ---- online softmax over this stage's tokens (row gid = head) ----
+            float mx = -INFINITY;
+  #pragma unroll
+            for (int nt = 0; nt < SH::NT; ++nt) {
+  #pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int t = nt * 8 + 2 * tig + e;
+                const float v = t < rows ? s[nt][e] * p.qscale : -INFINITY;
+                s[nt][e] = v;
+                mx = fmaxf(mx, v);
+              }
+            }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float m_new = fmaxf(m_run, mx);
+            const float mu = m_new == -INFINITY ? 0.f : m_new;
+            const float alpha = fast_exp2(m_run - mu);
+            m_run = m_new;
+            float ps = 0.f;
+            uint32_t pb[SH::NT];  // P as fp16 pairs: B operand of the PV mma
+  #pragma unroll
+            for (int nt = 0; nt < SH::NT; ++nt) {
+              const float p0 = fast_exp2(s[nt][0] - mu);
+              const float p1 = fast_exp2(s[nt][1] - mu);
+              ps += p0 + p1;
+              pb[nt] = pack_half2(p0, p1);
+            }
+            l_run = l_run * alpha + ps;
+            // rescale O^T columns: heads 2*tig and 2*tig+1 live in mma groups 2*tig, 2*tig+1
+            const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * tig);
+            const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);
+  #pragma unroll
+            for (int mt = 0; mt < SH::MT; ++mt) {
+              o[mt][0] *= a_lo;
+              o[mt][1] *= a_hi;
+              o[mt][2] *= a_lo;
+              o[mt][3] *= a_hi;
+            }
+            // ---- O^T += V^T P^T over 16-token k-steps ----
+            // x4.trans of m-tile mt: matrix m covers tokens +8*(m>>1), dims mt*16 + 8*(m&1)
+  #pragma unroll
+            for (int pk = 0; pk < SH::PK; ++pk) {
+              const uint32_t pb0 = pb[2 * pk];
+              const uint32_t pb1 = (2 * pk + 1 < SH::NT) ? pb[2 * pk + 1] : 0u;
+              const uint32_t rowa = vaddr + (pk * 16 + ld_row + (ld_mat >> 1) * 8) * 128;
+  #pragma unroll
+              for (int mt = 0; mt < SH::MT; ++mt) {
+                const int gc = 2 * mt + (ld_mat & 1);
+                const uint32_t addr = rowa + (gc >> 3) * HALF + (((gc & 7) ^ ld_row) << 4);
+                uint32_t a0, a1, a2, a3;
+                if (2 * pk + 1 < SH::NT) {
+                  ldsm_x4_t(addr, a0, a1, a2, a3);
+                } else {
+                  ldsm_x2_t(addr, a0, a1);
+                  a2 = a3 = 0u;
+                }
+                mma_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+              }
+            }
+            if (rows < TS) fence_proxy_async_smem();  // generic zero-fill before the next TMA write
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&empty_bar[stage]));
+          }
+        }
+
+        // ---- piece finished: this warp holds its head's whole state ----
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+        const int h0 = 2 * tig, h1 = 2 * tig + 1;
+        if (!cut) {
+          const float l0 = __shfl_sync(0xffffffffu, l_run, 8 * tig);
+          const float l1 = __shfl_sync(0xffffffffu, l_run, 8 * tig + 4);
+          const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+  #pragma unroll
+          for (int mt = 0; mt < SH::MT; ++mt) {
+            const int d = mt * 16 + gid;
+            if (h0 < G) {
+              out_row[h0 * D + d] = __float2half_rn(o[mt][0] * i0);
+              out_row[h0 * D + d + 8] = __float2half_rn(o[mt][2] * i0);
+            }
+            if (h1 < G) {
+              out_row[h1 * D + d] = __float2half_rn(o[mt][1] * i1);
+              out_row[h1 * D + d + 8] = __float2half_rn(o[mt][3] * i1);
+            }
+          }
+        } else {
+          // cut segment: this chunk's partial record
+  #pragma unroll
+          for (int mt = 0; mt < SH::MT; ++mt) {
+            const int d = mt * 16 + gid;
+            if (h0 < G) {
+              rec[h0 * D + d] = o[mt][0];
+              rec[h0 * D + d + 8] = o[mt][2];
+            }
+            if (h1 < G) {
+              rec[h1 * D + d] = o[mt][1];
+              rec[h1 * D + d + 8] = o[mt][3];
+            }
+          }
+          if (tig == 0 && gid < G) {
+            rec[G * D + 2 * gid] = m_run;
+            rec[G * D + 2 * gid + 1] = l_run;
+          }
+        }
+    }
+    if (cut) {
+          if (!pm.last) {
+            // hand the arrival (and any merge) to the merge warps: the warp
+            // barrier orders every lane's record stores before lane 0's arrival,
+            // whose release makes them visible to the merge warps' acquire
+            if (mc >= kMsgSlots)
+              warp_wait_phase(smem_addr(&mempty_bar[mc % kMsgSlots]), ((mc / kMsgSlots) - 1) & 1,
+                              abort_flag, p.err);
+            if (w == 0 && lane == 0) {
+              MsgMeta* m = mmeta + mc % kMsgSlots;
+              m->seq = pm.seq;
+              m->hg = pm.hg;
+              m->nb = pm.nb;
+              m->s0 = s0;
+              m->stop = 0;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&mfull_bar[mc % kMsgSlots]));
+            ++mc;
+          } else {
+            // The CTA's last piece: count the arrival here and merge if it
+            // completes the segment, which it usually does (the other chunks'
+            // pieces are mostly done). First try to claim the last arrival
+            // outright: a last arrival's record is read by no other warp, so it
+            // needs no release and the claim does not wait for its stores.
+            // Otherwise release the record and count the arrival as usual.
+            __syncwarp();  // the record's lanes, before any lane reads it back
+            const int c_first = s0 / chunk, c_last = (s0 + pm.nb - 1) / chunk;
+            const int E = c_last - c_first + 1;
+            unsigned long long* word = p.counters + static_cast<long long>(pm.seq) * Hkv + kvh;
+            const unsigned long long claim = (p.tag << kArrivalBits) | static_cast<unsigned>(E - 1);
+            int done = 0;
+            if (lane == 0) done = atomicCAS(word, claim, 0ull) == claim;
+            done = __shfl_sync(0xffffffffu, done, 0);
+            if (!done) {
+              fence_acq_rel_gpu();  // release: the record is visible before the arrival
+              __syncwarp();
+              if (lane == 0) done = arrive_last(word, p.tag, static_cast<unsigned>(E), false, p.err);
+              done = __shfl_sync(0xffffffffu, done, 0);
+            }
+            if (done) {
+              // acquire: the other chunks' records are visible to this warp
+              fence_acq_rel_gpu();
+              auto rec_of = [&](int i) -> long long {
+                return record_index(c_first + i, c_first, s0, chunk, HG, w);
+              };
+              merge_partials<D, G>(p.records, E, rec_of, out_row);
+            }
+          }
+    }
     if (pm.last) break;
   }
   // tell the merge warps there is nothing more
@@ -1146,9 +1337,10 @@ struct MapKey {
   int device;
   const void* ptr;
   int D, BS, Hkv, NB, hg, ts;
+  int esz;  // bytes per value: 2 (fp16) or 1 (E4M3)
   bool operator==(const MapKey& o) const {
     return device == o.device && ptr == o.ptr && D == o.D && BS == o.BS && Hkv == o.Hkv &&
-           NB == o.NB && hg == o.hg && ts == o.ts;
+           NB == o.NB && hg == o.hg && ts == o.ts && esz == o.esz;
   }
 };
 
@@ -1176,14 +1368,17 @@ pa_status pool_tensor_map(const MapKey& key, CUtensorMap* out) {
   }
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(key.D), static_cast<cuuint64_t>(key.BS),
                               static_cast<cuuint64_t>(key.Hkv), static_cast<cuuint64_t>(key.NB)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(key.Hkv) * key.D * 2,   // token
-                                 static_cast<cuuint64_t>(key.D) * 2,             // KV head
-                                 static_cast<cuuint64_t>(key.BS) * key.Hkv * key.D * 2};  // block
-  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(key.ts), static_cast<cuuint32_t>(key.hg),
-                             1};
+  const cuuint64_t e = static_cast<cuuint64_t>(key.esz);
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(key.Hkv) * key.D * e,   // token
+                                 static_cast<cuuint64_t>(key.D) * e,             // KV head
+                                 static_cast<cuuint64_t>(key.BS) * key.Hkv * key.D * e};  // block
+  // the box's inner extent is one 128-byte line: 64 fp16 or 128 E4M3 values
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / key.esz),
+                             static_cast<cuuint32_t>(key.ts), static_cast<cuuint32_t>(key.hg), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUtensorMap m;
-  CUresult r = encode(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(key.ptr), dims,
+  CUresult r = encode(&m, key.esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                      4, const_cast<void*>(key.ptr), dims,
                       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1206,10 +1401,10 @@ struct LaunchCfg {
   long long grid = 0;
 };
 
-template <int D, int BS, int G>
+template <int D, int BS, int G, bool KV8 = false>
 pa_status launch_config(const pa::DeviceInfo& dev, int S, int Hkv, LaunchCfg* cfg) {
-  using SH = Shape<D, BS, G>;
-  auto kernel = paged_decode_kernel<D, BS, G>;
+  using SH = Shape<D, BS, G, KV8>;
+  auto kernel = paged_decode_kernel<D, BS, G, KV8>;
   cfg->hg = head_group(Hkv);
   const int stage = SH::stage_bytes(cfg->hg);
   int nst = cfg->hg * kRingBytesPerHead / stage;
@@ -1261,16 +1456,19 @@ pa_status launch_config(const pa::DeviceInfo& dev, int S, int Hkv, LaunchCfg* cf
   return PA_OK;
 }
 
-template <int D, int BS, int G>
+template <int D, int BS, int G, bool KV8>
 pa_status launch_decode(DecodeParams prm, const pa::DeviceInfo& dev, cudaStream_t stream) {
-  using SH = Shape<D, BS, G>;
+  using SH = Shape<D, BS, G, KV8>;
   LaunchCfg cfg;
-  if (pa_status s = launch_config<D, BS, G>(dev, prm.num_seqs, prm.num_kv_heads, &cfg)) return s;
+  if (pa_status s = launch_config<D, BS, G, KV8>(dev, prm.num_seqs, prm.num_kv_heads, &cfg))
+    return s;
   prm.hg = cfg.hg;
   prm.nst = cfg.nst;
   CUtensorMap kmap, vmap;
-  MapKey kk{dev.device, prm.k_pool, D, BS, prm.num_kv_heads, prm.num_blocks, cfg.hg, SH::TS};
-  MapKey vk{dev.device, prm.v_pool, D, BS, prm.num_kv_heads, prm.num_blocks, cfg.hg, SH::TS};
+  MapKey kk{dev.device, prm.k_pool, D, BS, prm.num_kv_heads, prm.num_blocks, cfg.hg, SH::TS,
+            SH::ESZ};
+  MapKey vk{dev.device, prm.v_pool, D, BS, prm.num_kv_heads, prm.num_blocks, cfg.hg, SH::TS,
+            SH::ESZ};
   if (pa_status s = pool_tensor_map(kk, &kmap)) return s;
   if (pa_status s = pool_tensor_map(vk, &vmap)) return s;
   // Programmatic dependent launch: the prologue may overlap the tail of the
@@ -1286,20 +1484,20 @@ pa_status launch_decode(DecodeParams prm, const pa::DeviceInfo& dev, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&lc, paged_decode_kernel<D, BS, G>, prm, kmap, vmap);
+  cudaError_t e = cudaLaunchKernelEx(&lc, paged_decode_kernel<D, BS, G, KV8>, prm, kmap, vmap);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_decode_attention launch");
 
   return PA_OK;
 }
 
-template <int D, int BS>
+template <int D, int BS, bool KV8 = false>
 pa_status dispatch_g(int G, const DecodeParams& prm, const pa::DeviceInfo& dev, cudaStream_t s) {
   switch (G) {
-    case 1: return launch_decode<D, BS, 1>(prm, dev, s);
-    case 2: return launch_decode<D, BS, 2>(prm, dev, s);
-    case 4: return launch_decode<D, BS, 4>(prm, dev, s);
-    case 8: return launch_decode<D, BS, 8>(prm, dev, s);
+    case 1: return launch_decode<D, BS, 1, KV8>(prm, dev, s);
+    case 2: return launch_decode<D, BS, 2, KV8>(prm, dev, s);
+    case 4: return launch_decode<D, BS, 4, KV8>(prm, dev, s);
+    case 8: return launch_decode<D, BS, 8, KV8>(prm, dev, s);
   }
   return pa::fail(PA_ERR_UNSUPPORTED, "pa_decode_attention: query/KV head ratio %d not in {1,2,4,8}",
                   G);
@@ -1456,6 +1654,8 @@ static DecodeParams make_params(const pa_half* q, const pa_half* k_pool, const p
   prm.v_pool = reinterpret_cast<const __half*>(v_pool);
   prm.block_table = block_table;
   prm.seq_lens = seq_lens;
+  prm.k_scale = nullptr;
+  prm.v_scale = nullptr;
   prm.out = reinterpret_cast<__half*>(out);
   prm.records = reinterpret_cast<float*>(ws + lay.records);
   prm.counters = reinterpret_cast<unsigned long long*>(ws + lay.counters);
@@ -1505,6 +1705,54 @@ pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool, const pa_
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   pa_status st = head_dim == 64 ? dispatch_bs<64>(block_size, G, prm, dev, s)
                                 : dispatch_bs<128>(block_size, G, prm, dev, s);
+  return st == PA_OK ? pa::ok() : st;
+}
+
+pa_status pa_decode_attention_fp8(const pa_half* q, const uint8_t* k_pool, const uint8_t* v_pool,
+                                  const float* k_scale, const float* v_scale,
+                                  const int32_t* block_table, const int32_t* seq_lens,
+                                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int block_size, int max_blocks_per_seq, int num_blocks,
+                                  float scale, pa_half* out, void* workspace,
+                                  size_t workspace_bytes, int partition_tokens,
+                                  pa_stream_t stream) {
+  const pa_half* kp = reinterpret_cast<const pa_half*>(k_pool);
+  const pa_half* vp = reinterpret_cast<const pa_half*>(v_pool);
+  if (pa_status s = check_decode_call("pa_decode_attention_fp8", q, kp, vp, block_table, seq_lens,
+                                      num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                      max_blocks_per_seq, num_blocks, scale, out,
+                                      partition_tokens))
+    return s;
+  if (head_dim != 128 || (block_size != 16 && block_size != 32))
+    return pa::fail(PA_ERR_UNSUPPORTED,
+                    "pa_decode_attention_fp8: head_dim %d / block_size %d (fp8 pools support "
+                    "head_dim 128 and block_size 16 or 32)", head_dim, block_size);
+  if (num_seqs == 0) return pa::ok();
+  if (!k_scale || !v_scale || (reinterpret_cast<uintptr_t>(k_scale) & 3) ||
+      (reinterpret_cast<uintptr_t>(v_scale) & 3))
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention_fp8: NULL or misaligned scales");
+  if (!workspace) return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention_fp8: NULL workspace");
+  if (!pa::aligned16(workspace))
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention_fp8: misaligned workspace");
+  const int cap_blocks = partition_tokens / block_size;
+  const Layout lay = workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                      max_blocks_per_seq, cap_blocks);
+  if (workspace_bytes < lay.total)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention_fp8: workspace %zu < %zu bytes",
+                    workspace_bytes, lay.total);
+  pa::DeviceInfo dev;
+  if (pa_status s = pa::current_device(&dev)) return s;
+  DecodeParams prm = make_params(q, kp, vp, block_table, seq_lens, num_seqs, num_q_heads,
+                                 num_kv_heads, max_blocks_per_seq, num_blocks, scale, out,
+                                 static_cast<unsigned char*>(workspace), lay, cap_blocks);
+  prm.k_scale = k_scale;
+  prm.v_scale = v_scale;
+  prm.err = pa::device_error_word();
+  if (!prm.err) return PA_ERR_CUDA;
+  const int G = num_q_heads / num_kv_heads;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  pa_status st = block_size == 16 ? dispatch_g<128, 16, true>(G, prm, dev, s)
+                                  : dispatch_g<128, 32, true>(G, prm, dev, s);
   return st == PA_OK ? pa::ok() : st;
 }
 

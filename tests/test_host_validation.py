@@ -66,3 +66,41 @@ def test_cache_ops_reject(libpa):
     assert lib.pa_copy_blocks(NULL, NULL, NULL, 3, 0, 128, 16, 64, NULL) == 1
     assert lib.pa_copy_blocks(NULL, NULL, NULL, 0, 8, 128, 16, 64, NULL) == 0
     assert lib.pa_copy_blocks(NULL, NULL, NULL, 2, 8, 128, 16, 64, NULL) == 1
+
+
+def _decode_fp8(lib, **kw):
+    a = dict(q=NULL, k=NULL, v=NULL, ks=NULL, vs=NULL, table=NULL, lens=NULL, S=4, Hq=32, Hkv=8,
+             D=128, BS=16, MB=8, NB=64, scale=0.1, out=NULL, ws=NULL, wsb=0, pt=0, stream=NULL)
+    a.update(kw)
+    return lib.pa_decode_attention_fp8(a["q"], a["k"], a["v"], a["ks"], a["vs"], a["table"],
+                                       a["lens"], a["S"], a["Hq"], a["Hkv"], a["D"], a["BS"],
+                                       a["MB"], a["NB"], ctypes.c_float(a["scale"]), a["out"],
+                                       a["ws"], a["wsb"], a["pt"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Hq=30), 1),
+    (dict(D=96), 4),
+    (dict(BS=64), 4),
+    (dict(), 1),                      # NULL pointers
+])
+def test_decode_fp8_rejects(libpa, kw, status):
+    lib = libpa.lib()
+    assert _decode_fp8(lib, **kw) == status
+    assert lib.pa_last_error() != b""
+
+
+def test_decode_fp8_zero_sequences_is_a_no_op(libpa):
+    assert _decode_fp8(libpa.lib(), S=0) == 0
+
+
+def test_cache_ops_fp8_reject(libpa):
+    lib = libpa.lib()
+    # NULL scales / pools with work to do
+    assert lib.pa_append_kv_fp8(NULL, NULL, NULL, NULL, NULL, NULL, NULL, 4, 8, 128, 16, 64,
+                                NULL) == 1
+    assert lib.pa_append_kv_fp8(NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, 8, 128, 16, 64,
+                                NULL) == 0
+    assert lib.pa_copy_blocks_fp8(NULL, NULL, NULL, 0, 8, 128, 16, 64, NULL) == 0
+    assert lib.pa_copy_blocks_fp8(NULL, NULL, NULL, 2, 8, 120, 16, 64, NULL) == 4  # 120 % 16
+    assert lib.pa_copy_blocks_fp8(NULL, NULL, NULL, 2, 8, 128, 16, 64, NULL) == 1
