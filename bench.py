@@ -61,7 +61,7 @@ def workload(name: str, seed_offset: int = 0):
     raise SystemExit(f"unknown workload {name}")
 
 
-def describe(b) -> dict:
+def describe(b, kv_dtype: str = "fp16") -> dict:
     lens = b.attended_lens
     return {
         "workload": b.name,
@@ -73,7 +73,7 @@ def describe(b) -> dict:
         "head_dim": b.head_dim,
         "block_size": b.block_size,
         "num_blocks": int(b.num_blocks),
-        "kv_storage": "fp16",
+        "kv_storage": "fp16" if kv_dtype == "fp16" else "fp8 e4m3 bytes, fp32 scale per KV head",
         "l2": "flushed between steps outside the timed events (512 MB write, then 512 MB read of another buffer)",
     }
 
@@ -208,19 +208,25 @@ def barrier(world: int):
 
 
 # --------------------------------------------------------------- CPU oracle --
-def time_oracle(b, budget_s: float, max_seqs=None):
+def time_oracle(b, budget_s: float, max_seqs=None, fp8=None):
     """Time the CPU oracle's attention on whole-batch passes (or the first
-    `max_seqs` sequences) until `budget_s` seconds have passed."""
+    `max_seqs` sequences) until `budget_s` seconds have passed. With `fp8` (an
+    E4M3 cache for the batch) the oracle's attention over that cache is timed."""
     import oracle
     ref = oracle.decode_step(b, compute_attention=False)
     seqs = list(range(b.num_seqs if max_seqs is None else min(max_seqs, b.num_seqs)))
     lens = ref.seq_lens.astype(np.int64)
-    bytes_per_pass = int(lens[seqs].sum()) * b.num_kv_heads * b.head_dim * 4
+    esize = 1 if fp8 is not None else 2
+    bytes_per_pass = int(lens[seqs].sum()) * b.num_kv_heads * b.head_dim * esize * 2
     tokens_per_pass = int(lens[seqs].sum())
     passes, t0 = 0, time.perf_counter()
     while True:
-        oracle.decode_attention(b.q, ref.k_pool, ref.v_pool, ref.block_table, ref.seq_lens,
-                                b.scale, seqs=seqs)
+        if fp8 is not None:
+            oracle.decode_attention_fp8(b.q, fp8.k_pool, fp8.v_pool, fp8.k_scale, fp8.v_scale,
+                                        ref.block_table, ref.seq_lens, b.scale, seqs=seqs)
+        else:
+            oracle.decode_attention(b.q, ref.k_pool, ref.v_pool, ref.block_table,
+                                    ref.seq_lens, b.scale, seqs=seqs)
         passes += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
@@ -233,12 +239,16 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     b = workload(args.workload)
+    fp8 = None
+    if args.kv_dtype == "fp8":
+        import synthetic
+        fp8 = synthetic.fp8_cache(b)
     sample_seqs = args.ref_sample_seqs
     for _ in range(args.warmup):
-        time_oracle(b, 0.0, max_seqs=sample_seqs)
+        time_oracle(b, 0.0, max_seqs=sample_seqs, fp8=fp8)
     t_total, byt, tok = 0.0, 0, 0
     for _ in range(args.steps):
-        r = time_oracle(b, 0.0, max_seqs=sample_seqs)
+        r = time_oracle(b, 0.0, max_seqs=sample_seqs, fp8=fp8)
         t_total += r["seconds"]
         byt += r["bytes"]
         tok += r["tokens"]
@@ -249,7 +259,7 @@ def run_reference(args, world, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * t_total / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": describe(b),
+        "config": describe(b, args.kv_dtype),
         "tokens_per_s": round(tok / t_total, 1),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
                          "kind": "oracle",
@@ -276,7 +286,15 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     b = workload(args.workload, seed_offset=rank)
-    run = DecodeBatchRunner(b, device=dev, partition_tokens=args.partition)
+    fp8 = None
+    if args.kv_dtype == "fp8":
+        import synthetic
+        fp8 = synthetic.fp8_cache(b, seed=100 + 1000 * rank)
+        run = DecodeBatchRunner(b, device=dev, partition_tokens=args.partition, kv_dtype="fp8",
+                                k_pool=fp8.k_pool, v_pool=fp8.v_pool, k_scale=fp8.k_scale,
+                                v_scale=fp8.v_scale)
+    else:
+        run = DecodeBatchRunner(b, device=dev, partition_tokens=args.partition)
     plan = run.plan_step()
     # host slot assignment (block manager) cost for this batch, measured on a
     # second allocator holding the same placement
@@ -391,7 +409,7 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        r = time_oracle(b, args.cpu_budget)
+        r = time_oracle(b, args.cpu_budget, fp8=fp8)
         cpu = {"value": round(r["bytes"] / r["seconds"] / 1e9, 4), "unit": "GB/s",
                "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"{r['passes']} whole-batch pass(es) of the same {b.num_seqs}-sequence "
@@ -404,7 +422,7 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(1e3 * t_steps / K, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic", "config": describe(b),
+        "dtype": "f32", "data": "synthetic", "config": describe(b, args.kv_dtype),
         "tokens_per_s": round(all_tok / t_steps, 1),
         "frac_of_hbm_peak": {"measured": round(value / peak, 4),
                              "nominal_8tbs": round(value / 8000.0, 4)},
@@ -413,7 +431,8 @@ def run_ours(args, world, rank, local):
                          "min": round(1e3 * min(attn_ms), 3)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(b.name), "peak_source": peak_kind,
+                     "traffic": recorded_traffic(b.name + ("_fp8" if fp8 is not None else "")),
+                     "peak_source": peak_kind,
                      "kernel": "paged_decode_kernel",
                      "bytes_per_launch": run.io_bytes()},
         "e2e": {"value": round(all_kv_e2e / t_e2e / 1e9, 2), "unit": "GB/s",
@@ -436,6 +455,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa4_u128_2048")
     ap.add_argument("--partition", type=int, default=0, help="tokens per split (0 = default)")
+    ap.add_argument("--kv-dtype", choices=["fp16", "fp8"], default="fp16",
+                    help="KV cache storage: fp16, or E4M3 bytes with per-head scales")
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

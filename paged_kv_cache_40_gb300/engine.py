@@ -10,6 +10,10 @@ The batch object is any container with the fields of a decode batch:
 num_blocks, block_size, num_q_heads, num_kv_heads, head_dim, prefill_lens,
 free_order, churn (ops with kind/owner/nblocks), q, k_pool, v_pool, k_new,
 v_new (numpy fp16) and scale.
+
+With kv_dtype "fp8" the cache is E4M3 bytes with one fp32 scale per KV head
+for K and V (given as k_pool, v_pool, k_scale, v_scale); the new tokens are
+quantized by the append.
 """
 
 from __future__ import annotations
@@ -19,8 +23,8 @@ from typing import List, Optional, Tuple
 
 import numpy as np
 
-from . import (BlockAllocator, alloc_workspace, pa_append_kv, pa_copy_blocks,
-               pa_decode_attention)
+from . import (BlockAllocator, alloc_workspace, pa_append_kv, pa_append_kv_fp8, pa_copy_blocks,
+               pa_copy_blocks_fp8, pa_decode_attention, pa_decode_attention_fp8)
 
 
 def _to_dev(arr, device, dtype=None):
@@ -43,8 +47,15 @@ class DecodeBatchRunner:
     """Holds a batch's pools on the device and runs its decode step."""
 
     def __init__(self, batch, device="cuda", max_blocks: Optional[int] = None,
-                 partition_tokens: int = 0, table_fill: int = -1, k_pool=None, v_pool=None):
+                 partition_tokens: int = 0, table_fill: int = -1, k_pool=None, v_pool=None,
+                 kv_dtype: str = "fp16", k_scale=None, v_scale=None):
         import torch
+        if kv_dtype not in ("fp16", "fp8"):
+            raise ValueError("kv_dtype must be 'fp16' or 'fp8'")
+        if kv_dtype == "fp8" and (k_pool is None or v_pool is None or k_scale is None
+                                  or v_scale is None):
+            raise ValueError("an fp8 cache needs k_pool, v_pool, k_scale and v_scale")
+        self.kv_dtype = kv_dtype
         self.batch = batch
         self.device = torch.device(device)
         self.partition_tokens = partition_tokens
@@ -63,8 +74,15 @@ class DecodeBatchRunner:
         need = max(1, max(-(-(int(L) + 1) // bs) for L in batch.prefill_lens)) if S else 1
         self.max_blocks = int(max_blocks or need)
         self.table_fill = table_fill
-        self.k_pool = k_pool if k_pool is not None else _to_dev(batch.k_pool, self.device)
-        self.v_pool = v_pool if v_pool is not None else _to_dev(batch.v_pool, self.device)
+        def dev_pool(p, default):
+            if p is None:
+                return _to_dev(default, self.device)
+            return p if isinstance(p, torch.Tensor) else _to_dev(p, self.device)
+
+        self.k_pool = dev_pool(k_pool, batch.k_pool)
+        self.v_pool = dev_pool(v_pool, batch.v_pool)
+        self.k_scale = _to_dev(k_scale, self.device, torch.float32) if k_scale is not None else None
+        self.v_scale = _to_dev(v_scale, self.device, torch.float32) if v_scale is not None else None
         self.q = _to_dev(batch.q, self.device)
         self.k_new = _to_dev(batch.k_new, self.device)
         self.v_new = _to_dev(batch.v_new, self.device)
@@ -94,17 +112,29 @@ class DecodeBatchRunner:
     # -- device: the hot path ----------------------------------------------
     def copy_and_append(self, stream=None) -> int:
         launches = 0
+        fp8 = self.kv_dtype == "fp8"
         if self.d_pairs is not None:
-            pa_copy_blocks(self.k_pool, self.v_pool, self.d_pairs, stream=stream)
+            (pa_copy_blocks_fp8 if fp8 else pa_copy_blocks)(self.k_pool, self.v_pool, self.d_pairs,
+                                                            stream=stream)
             launches += 1
-        pa_append_kv(self.k_new, self.v_new, self.k_pool, self.v_pool, self.d_slots,
-                     stream=stream)
+        if fp8:
+            pa_append_kv_fp8(self.k_new, self.v_new, self.k_pool, self.v_pool, self.d_slots,
+                             self.k_scale, self.v_scale, stream=stream)
+        else:
+            pa_append_kv(self.k_new, self.v_new, self.k_pool, self.v_pool, self.d_slots,
+                         stream=stream)
         return launches + 1
 
     def attend(self, stream=None):
-        pa_decode_attention(self.q, self.k_pool, self.v_pool, self.d_table, self.d_lens,
-                            float(self.batch.scale), out=self.out, workspace=self.workspace,
-                            partition_tokens=self.partition_tokens, stream=stream)
+        if self.kv_dtype == "fp8":
+            pa_decode_attention_fp8(self.q, self.k_pool, self.v_pool, self.k_scale, self.v_scale,
+                                    self.d_table, self.d_lens, float(self.batch.scale),
+                                    out=self.out, workspace=self.workspace,
+                                    partition_tokens=self.partition_tokens, stream=stream)
+        else:
+            pa_decode_attention(self.q, self.k_pool, self.v_pool, self.d_table, self.d_lens,
+                                float(self.batch.scale), out=self.out, workspace=self.workspace,
+                                partition_tokens=self.partition_tokens, stream=stream)
         return self.out
 
     # kernels one attend() enqueues (the attention kernel merges split
@@ -121,7 +151,8 @@ class DecodeBatchRunner:
     def kv_bytes(self) -> int:
         """Algorithmic K+V bytes one attention launch reads."""
         b = self.batch
-        return int(self.plan.seq_lens.astype(np.int64).sum()) * b.num_kv_heads * b.head_dim * 2 * 2
+        esize = 1 if self.kv_dtype == "fp8" else 2
+        return int(self.plan.seq_lens.astype(np.int64).sum()) * b.num_kv_heads * b.head_dim * esize * 2
 
     def io_bytes(self) -> int:
         """Algorithmic bytes of one attention launch: K/V rows attended, q,
