@@ -55,14 +55,16 @@ def workload(name: str, seed_offset: int = 0):
         return synthetic.config2_gqa_batch(seed=2 + 1000 * seed_offset)
     if name == "mha32_lognormal800":
         return synthetic.config3_mha_lognormal(seed=3 + 1000 * seed_offset)
+    if name == "shared_prefix_cow":
+        return synthetic.config4_shared_prefix(seed=4 + 1000 * seed_offset)
     if name.startswith("long32k_gqa8_bs"):
         return synthetic.config5_long_context(block_size=int(name[len("long32k_gqa8_bs"):]),
                                               seed=5 + 1000 * seed_offset)
     raise SystemExit(f"unknown workload {name}")
 
 
-def describe(b, kv_dtype: str = "fp16") -> dict:
-    lens = b.attended_lens
+def describe(b, kv_dtype: str = "fp16", lens=None) -> dict:
+    lens = b.attended_lens if lens is None else np.asarray(lens)
     return {
         "workload": b.name,
         "num_seqs": int(b.num_seqs),
@@ -208,25 +210,45 @@ def barrier(world: int):
 
 
 # --------------------------------------------------------------- CPU oracle --
+def oracle_step_inputs(b):
+    """(q, k_pool, v_pool, block_table, seq_lens) of the workload's decode
+    step, from the oracle's own block manager."""
+    import oracle
+    if hasattr(b, "prefix_len"):
+        # shared prefix: sequence 0 holds it, the others are forks; one step
+        a = oracle.BlockAllocator(b.num_blocks, b.block_size, b.free_order)
+        a.add_seq(0, int(b.prefix_len))
+        for c in range(1, b.num_seqs):
+            a.fork(0, c)
+        active = list(range(b.num_seqs))
+        for s_ in active:
+            a.append_slot(s_)
+        mb = -(-(int(b.prefix_len) + 1) // b.block_size)
+        table = np.asarray(a.dense_table(active, mb), np.int32)
+        lens = np.full(b.num_seqs, int(b.prefix_len) + 1, np.int32)
+        return b.step_inputs(0, b.num_seqs)[0], b.k_pool, b.v_pool, table, lens
+    ref = oracle.decode_step(b, compute_attention=False)
+    return b.q, ref.k_pool, ref.v_pool, ref.block_table, ref.seq_lens
+
+
 def time_oracle(b, budget_s: float, max_seqs=None, fp8=None):
     """Time the CPU oracle's attention on whole-batch passes (or the first
     `max_seqs` sequences) until `budget_s` seconds have passed. With `fp8` (an
     E4M3 cache for the batch) the oracle's attention over that cache is timed."""
     import oracle
-    ref = oracle.decode_step(b, compute_attention=False)
+    q, kp, vp, table, seq_lens = oracle_step_inputs(b)
     seqs = list(range(b.num_seqs if max_seqs is None else min(max_seqs, b.num_seqs)))
-    lens = ref.seq_lens.astype(np.int64)
+    lens = np.asarray(seq_lens).astype(np.int64)
     esize = 1 if fp8 is not None else 2
     bytes_per_pass = int(lens[seqs].sum()) * b.num_kv_heads * b.head_dim * esize * 2
     tokens_per_pass = int(lens[seqs].sum())
     passes, t0 = 0, time.perf_counter()
     while True:
         if fp8 is not None:
-            oracle.decode_attention_fp8(b.q, fp8.k_pool, fp8.v_pool, fp8.k_scale, fp8.v_scale,
-                                        ref.block_table, ref.seq_lens, b.scale, seqs=seqs)
+            oracle.decode_attention_fp8(q, fp8.k_pool, fp8.v_pool, fp8.k_scale, fp8.v_scale,
+                                        table, seq_lens, b.scale, seqs=seqs)
         else:
-            oracle.decode_attention(b.q, ref.k_pool, ref.v_pool, ref.block_table,
-                                    ref.seq_lens, b.scale, seqs=seqs)
+            oracle.decode_attention(q, kp, vp, table, seq_lens, b.scale, seqs=seqs)
         passes += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
@@ -259,7 +281,7 @@ def run_reference(args, world, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * t_total / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": describe(b, args.kv_dtype),
+        "config": describe(b, args.kv_dtype, oracle_step_inputs(b)[4]),
         "tokens_per_s": round(tok / t_total, 1),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
                          "kind": "oracle",
@@ -287,7 +309,13 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     b = workload(args.workload, seed_offset=rank)
     fp8 = None
-    if args.kv_dtype == "fp8":
+    shared = args.workload == "shared_prefix_cow"
+    if shared:
+        from paged_kv_cache_40_gb300.engine import SharedPrefixRunner
+        if args.kv_dtype != "fp16":
+            raise SystemExit("the shared-prefix step is measured on an fp16 cache")
+        run = SharedPrefixRunner(b, device=dev, partition_tokens=args.partition)
+    elif args.kv_dtype == "fp8":
         import synthetic
         fp8 = synthetic.fp8_cache(b, seed=100 + 1000 * rank)
         run = DecodeBatchRunner(b, device=dev, partition_tokens=args.partition, kv_dtype="fp8",
@@ -300,13 +328,18 @@ def run_ours(args, world, rank, local):
     # second allocator holding the same placement
     from paged_kv_cache_40_gb300 import BlockAllocator
     a = BlockAllocator(b.num_blocks, b.block_size, b.free_order)
-    for op in b.churn:
-        if op.kind == "alloc":
-            a.add_seq(op.owner, op.nblocks * b.block_size)
-        else:
-            a.free_seq(op.owner)
-    for i in range(b.num_seqs):
-        a.add_seq(i, int(b.prefill_lens[i]))
+    if shared:
+        a.add_seq(0, int(b.prefix_len))
+        for c in range(1, b.num_seqs):
+            a.fork(0, c)
+    else:
+        for op in b.churn:
+            if op.kind == "alloc":
+                a.add_seq(op.owner, op.nblocks * b.block_size)
+            else:
+                a.free_seq(op.owner)
+        for i in range(b.num_seqs):
+            a.add_seq(i, int(b.prefill_lens[i]))
     t_host0 = time.perf_counter()
     a.append_slots(list(range(b.num_seqs)))
     a.build_tables(list(range(b.num_seqs)), run.max_blocks)
@@ -358,9 +391,9 @@ def run_ours(args, world, rank, local):
 
     # end to end through the public API with pinned host buffers
     h = {
-        "q": torch.from_numpy(b.q).pin_memory(),
-        "k_new": torch.from_numpy(b.k_new).pin_memory(),
-        "v_new": torch.from_numpy(b.v_new).pin_memory(),
+        "q": run.q.cpu().pin_memory(),
+        "k_new": run.k_new.cpu().pin_memory(),
+        "v_new": run.v_new.cpu().pin_memory(),
         "slots": torch.from_numpy(plan.slots).pin_memory(),
         "table": torch.from_numpy(plan.block_table).pin_memory(),
         "lens": torch.from_numpy(plan.seq_lens).pin_memory(),
@@ -418,11 +451,20 @@ def run_ours(args, world, rank, local):
     if rank != 0:
         return
     value = all_kv / t_steps / 1e9
+    config = describe(b, args.kv_dtype, plan.seq_lens)
+    if shared:
+        config.update({
+            "prefix_len": int(b.prefix_len),
+            "cow_copies_per_step": int(len(plan.cow_pairs)),
+            "unique_kv_bytes": run.unique_kv_bytes(),
+            "note": "every sequence attends the same 2040-token prefix; bytes are logical "
+                    "(per sequence), the prefix's blocks are served from L2 after the first read",
+        })
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(1e3 * t_steps / K, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic", "config": describe(b, args.kv_dtype),
+        "dtype": "f32", "data": "synthetic", "config": config,
         "tokens_per_s": round(all_tok / t_steps, 1),
         "frac_of_hbm_peak": {"measured": round(value / peak, 4),
                              "nominal_8tbs": round(value / 8000.0, 4)},

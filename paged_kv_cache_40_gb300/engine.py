@@ -161,3 +161,55 @@ class DecodeBatchRunner:
         lens = self.plan.seq_lens.astype(np.int64)
         table_entries = int(sum(-(-int(L) // b.block_size) for L in lens))
         return (self.kv_bytes() + 2 * self.q.numel() * 2 + table_entries * 4 + lens.size * 4)
+
+
+class SharedPrefixRunner(DecodeBatchRunner):
+    """The first decode step of sequences that share one prompt prefix.
+
+    Sequence 0 holds the prefix; sequences 1..S-1 are forks of it, so every
+    prefix block is referenced by all S block tables ("Phase 7 · Document 04
+    — PagedAttention", §2 block sharing and §3 Mental Model). The step appends
+    one token per sequence: the prefix's partial last block is copied for
+    every holder but the last, which writes in place (copy-on-write), then all
+    sequences attend over prefix + new token. Repeating the step repeats the
+    same copies and writes, so it can be timed in a loop.
+
+    The workload object provides num_blocks, block_size, num_q_heads,
+    num_kv_heads, head_dim, prefix_len, num_seqs, free_order, k_pool, v_pool,
+    scale and step_inputs(step, num_active) -> (q, k_new, v_new).
+    """
+
+    def __init__(self, workload, device="cuda", partition_tokens: int = 0):
+        import torch
+        w = workload
+        self.kv_dtype = "fp16"
+        self.batch = w
+        self.device = torch.device(device)
+        self.partition_tokens = partition_tokens
+        self.num_seqs = int(w.num_seqs)
+        a = BlockAllocator(w.num_blocks, w.block_size, w.free_order)
+        a.add_seq(0, int(w.prefix_len))
+        for c in range(1, self.num_seqs):
+            a.fork(0, c)
+        self.alloc = a
+        self.max_blocks = -(-(int(w.prefix_len) + 1) // w.block_size)
+        self.table_fill = -1
+        self.k_pool = _to_dev(w.k_pool, self.device)
+        self.v_pool = _to_dev(w.v_pool, self.device)
+        self.k_scale = self.v_scale = None
+        q, kn, vn = w.step_inputs(0, self.num_seqs)
+        self.q = _to_dev(q, self.device)
+        self.k_new = _to_dev(kn, self.device)
+        self.v_new = _to_dev(vn, self.device)
+        self.out = torch.empty_like(self.q)
+        self.workspace = alloc_workspace(self.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                         w.head_dim, w.block_size, self.max_blocks,
+                                         partition_tokens, self.device)
+        self.plan = None
+
+    def unique_kv_bytes(self) -> int:
+        """K+V bytes of the distinct rows the step attends (the shared prefix
+        once, plus each sequence's private copy of the last block)."""
+        w = self.batch
+        rows = int(w.prefix_len) + self.num_seqs * (int(w.prefix_len) % w.block_size + 1)
+        return rows * w.num_kv_heads * w.head_dim * 2 * 2
