@@ -314,7 +314,8 @@ def run_ours(args, world, rank, local):
         from paged_kv_cache_40_gb300.engine import SharedPrefixRunner
         if args.kv_dtype != "fp16":
             raise SystemExit("the shared-prefix step is measured on an fp16 cache")
-        run = SharedPrefixRunner(b, device=dev, partition_tokens=args.partition)
+        run = SharedPrefixRunner(b, device=dev, partition_tokens=args.partition,
+                                 prefix_aware=not args.plain_decode)
     elif args.kv_dtype == "fp8":
         import synthetic
         fp8 = synthetic.fp8_cache(b, seed=100 + 1000 * rank)
@@ -354,7 +355,8 @@ def run_ours(args, world, rank, local):
     # convert the whole buffer to int64)
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_sink = torch.empty((), dtype=torch.float32, device=dev)
-    launches_per_step = (1 if len(plan.cow_pairs) else 0) + 1 + DecodeBatchRunner.ATTEND_LAUNCHES
+    launches_per_step = ((1 if len(plan.cow_pairs) else 0) + 1 +
+                         getattr(run, "attend_launches", DecodeBatchRunner.ATTEND_LAUNCHES))
 
     def flush():
         flush_w.fill_(1)
@@ -456,6 +458,8 @@ def run_ours(args, world, rank, local):
         config.update({
             "prefix_len": int(b.prefix_len),
             "cow_copies_per_step": int(len(plan.cow_pairs)),
+            "attention": "prefix-aware (prefix blocks read once per KV head for all sequences)"
+                         if run.prefix_aware else "generic paged decode",
             "unique_kv_bytes": run.unique_kv_bytes(),
             "note": "every sequence attends the same 2040-token prefix; bytes are logical "
                     "(per sequence), the prefix's blocks are served from L2 after the first read",
@@ -497,6 +501,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa4_u128_2048")
     ap.add_argument("--partition", type=int, default=0, help="tokens per split (0 = default)")
+    ap.add_argument("--plain-decode", action="store_true",
+                    help="shared-prefix workload: attend with the generic call, not the "
+                         "prefix-aware one")
     ap.add_argument("--kv-dtype", choices=["fp16", "fp8"], default="fp16",
                     help="KV cache storage: fp16, or E4M3 bytes with per-head scales")
     ap.add_argument("--e2e-steps", type=int, default=500)

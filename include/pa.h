@@ -239,6 +239,50 @@ PA_API pa_status pa_decode_attention_fixed_scratch(
     int partition_tokens, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * pa_decode_attention_shared_prefix — pa_decode_attention for a batch whose
+ * sequences all begin with the same physical blocks (a shared prompt).
+ *
+ * Source: "Phase 7 · Document 04 — PagedAttention", §2 Core Concept (block
+ * sharing: sequences reference the same physical blocks, copy-on-write on
+ * divergence) and §3 Mental Model (A->[b3,b7,b1], B->[b3,b9]); lux-666 notes
+ * "PagedAttention", prefix sharing. The pages share the blocks' memory; this
+ * call also shares their reading: each prefix block of a KV head is streamed
+ * once and contracted on tensor cores against the query rows of every
+ * sequence, and each sequence's remaining blocks are streamed as in
+ * pa_decode_attention, the two parts merged per (sequence, head).
+ *
+ * The result is that of pa_decode_attention with the same arguments
+ * (prefix_blocks is a statement about block_table, not extra input):
+ * precondition: block_table[i][j] == prefix_blocks[j] for j <
+ * num_prefix_blocks and seq_lens[i] >= num_prefix_blocks * block_size for
+ * every sequence i. A sequence shorter than the prefix sets
+ * PA_DEVERR_BAD_LEN; a table that disagrees with prefix_blocks gives the
+ * attention over prefix_blocks instead.
+ *
+ * prefix_blocks   device int32 [num_prefix_blocks], full blocks shared by
+ *                 every sequence (num_prefix_blocks = 0 is plain
+ *                 pa_decode_attention).
+ * workspace       >= pa_decode_shared_prefix_workspace_bytes(...) bytes,
+ *                 16-byte aligned, no initialisation needed.
+ * Enqueues two kernels on `stream` (the second launched as a programmatic
+ * dependent of the first). Supported: head_dim 128, block_size 16 or 32,
+ * num_q_heads / num_kv_heads in {1, 2, 4, 8}.
+ * Errors: as pa_decode_attention.
+ * ---------------------------------------------------------------------- */
+PA_API size_t pa_decode_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads,
+                                                      int num_kv_heads, int head_dim,
+                                                      int block_size, int max_blocks_per_seq,
+                                                      int num_prefix_blocks);
+
+PA_API pa_status pa_decode_attention_shared_prefix(
+    const pa_half* q, const pa_half* k_pool, const pa_half* v_pool,
+    const int32_t* prefix_blocks, int num_prefix_blocks,
+    const int32_t* block_table, const int32_t* seq_lens, int num_seqs,
+    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+    int max_blocks_per_seq, int num_blocks, float scale, pa_half* out,
+    void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * fp8 KV cache — the append, the block copy and decode attention over pools
  * of OCP E4M3 bytes with one fp32 scale per KV head for K and for V.
  *

@@ -35,6 +35,7 @@ __all__ = [
     "pa_append_kv", "pa_copy_blocks", "pa_decode_attention",
     "pa_decode_workspace_bytes", "pa_decode_workspace_init", "pa_device_error",
     "pa_append_kv_fp8", "pa_copy_blocks_fp8", "pa_decode_attention_fp8",
+    "pa_decode_attention_shared_prefix", "pa_decode_shared_prefix_workspace_bytes",
     "pa_decode_attention_fixed_scratch",
     "pa_version", "BlockAllocator", "PaError", "OutOfBlocksError", "lib",
     "DEFAULT_PARTITION_TOKENS",
@@ -168,6 +169,54 @@ def pa_decode_attention(q, k_pool, v_pool, block_table, seq_lens, scale, out=Non
         *args, S, hq, hkv, d, bs, mb, nb, ctypes.c_float(float(scale)),
         _dev(out, "out", torch.float16), _dev(workspace, "workspace", torch.uint8),
         workspace.numel(), partition_tokens, _stream_ptr(stream)))
+    return out
+
+
+# ------------------------------------------------------------ shared prefix --
+def pa_decode_shared_prefix_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                            block_size, max_blocks_per_seq,
+                                            num_prefix_blocks) -> int:
+    n = int(_load().pa_decode_shared_prefix_workspace_bytes(
+        num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+        num_prefix_blocks))
+    if n == 0 and num_seqs > 0:
+        raise PaError(1, "pa_decode_shared_prefix_workspace_bytes: unsupported or invalid shape")
+    return n
+
+
+def pa_decode_attention_shared_prefix(q, k_pool, v_pool, prefix_blocks, block_table, seq_lens,
+                                      scale, out=None, workspace=None, stream=None):
+    """pa_decode_attention for sequences that all begin with the physical
+    blocks `prefix_blocks` (int32 [P]): block_table[i][:P] must equal them and
+    seq_lens[i] >= P * block_size. The prefix blocks are read once for the
+    whole batch. Returns out [S][Hq][D] fp16."""
+    torch = _torch()
+    nb, bs, hkv, d = _pool_dims(k_pool, v_pool)
+    if q.dim() != 3 or int(q.shape[2]) != d:
+        raise ValueError("q must be [num_seqs][num_q_heads][head_dim]")
+    S, hq = int(q.shape[0]), int(q.shape[1])
+    if block_table.dim() != 2 or int(block_table.shape[0]) != S:
+        raise ValueError("block_table must be [num_seqs][max_blocks_per_seq]")
+    mb = int(block_table.shape[1])
+    if tuple(seq_lens.shape) != (S,) or prefix_blocks.dim() != 1:
+        raise ValueError("seq_lens must be [num_seqs] and prefix_blocks one-dimensional")
+    P = int(prefix_blocks.numel())
+    if out is None:
+        out = torch.empty_like(q)
+    elif tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must have q's shape")
+    if workspace is None:
+        n = pa_decode_shared_prefix_workspace_bytes(S, hq, hkv, d, bs, mb, P)
+        workspace = torch.zeros(max(n, 16), dtype=torch.uint8, device=q.device)
+    args = (_dev(q, "q", torch.float16), _dev(k_pool, "k_pool", torch.float16),
+            _dev(v_pool, "v_pool", torch.float16),
+            _dev(prefix_blocks, "prefix_blocks", torch.int32) if P else ctypes.c_void_p(0), P,
+            _dev(block_table, "block_table", torch.int32),
+            _dev(seq_lens, "seq_lens", torch.int32))
+    _check(_load().pa_decode_attention_shared_prefix(
+        *args, S, hq, hkv, d, bs, mb, nb, ctypes.c_float(float(scale)),
+        _dev(out, "out", torch.float16), _dev(workspace, "workspace", torch.uint8),
+        workspace.numel(), _stream_ptr(stream)))
     return out
 
 

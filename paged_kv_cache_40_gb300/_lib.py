@@ -71,6 +71,10 @@ SIGNATURES = {
     "pa_copy_blocks_fp8": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp]),
     "pa_decode_attention_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                        _i32, _i32, _i32, _f32, _vp, _vp, _sz, _i32, _vp]),
+    "pa_decode_shared_prefix_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32]),
+    "pa_decode_attention_shared_prefix": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32,
+                                                 _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp,
+                                                 _sz, _vp]),
     "pa_alloc_create": (_i32, [_i32, _i32, _pi32, ctypes.POINTER(_vp)]),
     "pa_alloc_destroy": (None, [_vp]),
     "pa_alloc_add_seq": (_i32, [_vp, _i64, _i64]),

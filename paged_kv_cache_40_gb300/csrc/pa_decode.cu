@@ -289,6 +289,14 @@ struct DecodeParams {
   int max_blocks;
   int num_blocks;
   int cap_blocks;  // max blocks per chunk (0 = balance over the grid)
+  // shared-prefix mode: the table pointer starts past the prefix's
+  // pfx_blocks columns, lengths count past its pfx_blocks * BS tokens, and
+  // every result also folds the pfx_chunks prefix records of its (sequence,
+  // KV head), record index pfx_rec_base + (chunk * S + seq) * Hkv + kvh
+  int pfx_blocks;
+  int pfx_chunks;
+  long long pfx_rec_base;
+  long long pfx_own_base;  // [S][Hkv] records of segments streamed whole
   int hg;          // KV heads per group (consumer warps)
   int nst;         // ring stages
   float qscale;    // scale * log2(e)
@@ -306,10 +314,12 @@ __device__ __forceinline__ int clamp_len(int L, int cap, int32_t* err) {
 // computed by all threads of the block (wsum: one int per warp). Lengths
 // outside [0, cap] are clamped and reported.
 __device__ __forceinline__ void block_prefix(int* pfx, int* wsum, const int32_t* seq_lens, int S,
-                                             int bs, int cap, int32_t* err) {
+                                             int bs, int cap, int32_t* err, int len_off = 0) {
   const int tid = threadIdx.x, nthreads = blockDim.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < S; i += nthreads) {
-    const int L = clamp_len(__ldg(seq_lens + i), cap, err);
+    const int Lfull = __ldg(seq_lens + i);
+    if (Lfull < len_off) atomicOr(err, PA_DEVERR_BAD_LEN);  // shorter than a shared prefix
+    const int L = clamp_len(max(Lfull - len_off, 0), cap, err);
     pfx[i + 1] = (L + bs - 1) / bs;
   }
   if (tid == 0) pfx[0] = 0;
@@ -587,7 +597,7 @@ __device__ __forceinline__ void merge_partials(const float* recs, int E, RecOf r
   }
 }
 
-template <int D, int BS, int G, bool KV8>
+template <int D, int BS, int G, bool KV8, bool PFX = false>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     paged_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap) {
@@ -621,7 +631,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   const int S = p.num_seqs;
   const int Hkv = p.num_kv_heads;
   const int NHG = Hkv / HG;
-  const int cap = p.max_blocks * BS;
+  const int cap = (p.max_blocks - (PFX ? p.pfx_blocks : 0)) * BS;
+  const int loff = PFX ? p.pfx_blocks * BS : 0;  // tokens before the streamed part
 
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
@@ -641,7 +652,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   }
 
   // ---- blocks per sequence, exclusive prefix sum in shared memory ----
-  block_prefix(pfx, flags + kFlagWsum, p.seq_lens, S, BS, cap, p.err);
+  block_prefix(pfx, flags + kFlagWsum, p.seq_lens, S, BS, cap, p.err, loff);
   const Geometry geo = chunk_geometry(pfx[S] * NHG, gridDim.x, p.cap_blocks);
   const int chunk = geo.chunk;
   const bool has_work = static_cast<int>(blockIdx.x) < geo.nchunks;
@@ -688,7 +699,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     int j0 = 0;
     int phys_cur = 0, len_cur = 0;
     if (have) {
-      len_cur = min(max(__ldg(p.seq_lens + P.cur.seq), 0), cap);
+      len_cur = min(max(__ldg(p.seq_lens + P.cur.seq) - loff, 0), cap);
       phys_cur = lane < min(32, P.n)
                      ? __ldg(p.block_table + static_cast<long long>(P.cur.seq) * p.max_blocks +
                              P.cur.j + lane)
@@ -733,7 +744,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                                P.cur.j + j0 + 32 + lane)
                        : 0;
       } else if (nhave) {
-        len_nxt = min(max(__ldg(p.seq_lens + PN.cur.seq), 0), cap);
+        len_nxt = min(max(__ldg(p.seq_lens + PN.cur.seq) - loff, 0), cap);
         phys_nxt = lane < min(32, PN.n)
                        ? __ldg(p.block_table + static_cast<long long>(PN.cur.seq) * p.max_blocks +
                                PN.cur.j + lane)
@@ -834,12 +845,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       while (last) {
         const int h = __ffs(last) - 1;
         last &= last - 1;
+        const int kvh_m = msg.hg * HG + h;
         auto rec_of = [&](int i) -> long long {
+          if (PFX && i >= E)
+            return p.pfx_rec_base +
+                   (static_cast<long long>(i - E) * S + msg.seq) * Hkv + kvh_m;
           return record_index(c_first + i, c_first, s0, chunk, HG, h);
         };
         __half* out_row = p.out + (static_cast<long long>(msg.seq) * p.num_q_heads +
-                                   static_cast<long long>(msg.hg * HG + h) * G) * D;
-        merge_partials<D, G>(p.records, E, rec_of, out_row);
+                                   static_cast<long long>(kvh_m) * G) * D;
+        merge_partials<D, G>(p.records, E + (PFX ? p.pfx_chunks : 0), rec_of, out_row);
       }
     }
     return;
@@ -851,11 +866,23 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   const int gid = lane >> 2;  // mma group id: row of A / column of B
   const int tig = lane & 3;   // thread in group
 
-  // zero outputs of empty sequences (this CTA's share)
+  // outputs of sequences with nothing to stream (this CTA's share): zero, or
+  // in shared-prefix mode the merge of the prefix records alone
   for (int i = blockIdx.x; i < S; i += gridDim.x) {
     if (pfx[i + 1] == pfx[i]) {
-      __half* o = p.out + static_cast<long long>(i) * p.num_q_heads * D;
-      for (int e = tid; e < p.num_q_heads * D; e += HG * 32) o[e] = __float2half_rn(0.f);
+      if constexpr (PFX) {
+        for (int kv = w; kv < Hkv; kv += HG) {
+          auto rec_of = [&](int k) -> long long {
+            return p.pfx_rec_base + (static_cast<long long>(k) * S + i) * Hkv + kv;
+          };
+          merge_partials<D, G>(p.records, p.pfx_chunks, rec_of,
+                               p.out + (static_cast<long long>(i) * p.num_q_heads +
+                                        static_cast<long long>(kv) * G) * D);
+        }
+      } else {
+        __half* o = p.out + static_cast<long long>(i) * p.num_q_heads * D;
+        for (int e = tid; e < p.num_q_heads * D; e += HG * 32) o[e] = __float2half_rn(0.f);
+      }
     }
   }
   if (!has_work) return;
@@ -877,13 +904,19 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     const PieceMeta pm = pmeta[qs];
     const int pj = pm.j, n = pm.n, L = pm.len;
     const int kvh = pm.hg * HG + w;
-    const bool cut = pj > 0 || pj + n < pm.nb;
+    // in shared-prefix mode every piece is merged with the prefix records
+    const bool cut = PFX || pj > 0 || pj + n < pm.nb;
     __half* out_row = p.out + (static_cast<long long>(pm.seq) * p.num_q_heads +
                                static_cast<long long>(kvh) * G) * D;
     // a cut piece's partial record: slot 0 if the piece starts its chunk, else 1
+    // (in shared-prefix mode a whole segment uses its (sequence, KV head) slot)
     const int s0 = pm.s0;
-    float* rec = p.records + ((2ll * pm.c + (s0 + pj == pm.c * chunk ? 0 : 1)) * HG + w) *
-                                 static_cast<long long>(SH::REC);
+    const bool whole = !(pj > 0 || pj + n < pm.nb);
+    float* rec = p.records +
+                 (PFX && whole
+                      ? p.pfx_own_base + static_cast<long long>(pm.seq) * Hkv + kvh
+                      : (2ll * pm.c + (s0 + pj == pm.c * chunk ? 0 : 1)) * HG + w) *
+                     static_cast<long long>(SH::REC);
     if constexpr (KV8) {
       // ---- fp8 pools: E4M3 tiles, converted to fp16 fragments in registers ----
       // Scores as S^T = K Q^T: the 16 tokens of a stage are the M rows, the
@@ -1214,7 +1247,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           }
         }
     }
-    if (cut) {
+    if (PFX && whole) {
+      // the whole segment is here: merge it with the prefix records now
+      __syncwarp();  // the record's lanes, before any lane reads it back
+      auto rec_of = [&](int i) -> long long {
+        if (i == 0) return p.pfx_own_base + static_cast<long long>(pm.seq) * Hkv + kvh;
+        return p.pfx_rec_base + (static_cast<long long>(i - 1) * S + pm.seq) * Hkv + kvh;
+      };
+      merge_partials<D, G>(p.records, 1 + p.pfx_chunks, rec_of, out_row);
+    } else if (cut) {
           if (!pm.last) {
             // hand the arrival (and any merge) to the merge warps: the warp
             // barrier orders every lane's record stores before lane 0's arrival,
@@ -1258,9 +1299,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
               // acquire: the other chunks' records are visible to this warp
               fence_acq_rel_gpu();
               auto rec_of = [&](int i) -> long long {
+                if (PFX && i >= E)
+                  return p.pfx_rec_base +
+                         (static_cast<long long>(i - E) * S + pm.seq) * Hkv + kvh;
                 return record_index(c_first + i, c_first, s0, chunk, HG, w);
               };
-              merge_partials<D, G>(p.records, E, rec_of, out_row);
+              merge_partials<D, G>(p.records, E + (PFX ? p.pfx_chunks : 0), rec_of, out_row);
             }
           }
     }
@@ -1277,6 +1321,243 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   }
 }
 
+
+// ------------------------------------------------------ shared prefix ---
+// Sequences that begin with the same physical blocks (a shared prompt prefix:
+// "Phase 7 · Document 04 — PagedAttention", §2 block sharing and §3 Mental
+// Model; lux-666 notes "PagedAttention", prefix sharing) attend those blocks
+// with the same K and V rows. The prefix kernel streams each prefix tile of a
+// KV head once and contracts it against the query rows of every sequence
+// that shares it: rows (sequence, query head of the group), 16 per consumer
+// warp, 64 per CTA, every mma row real. S = Q K^T, online softmax per row,
+// O = P V with P reused from the score registers as the A operand; the
+// prefix's tokens are split into chunks across CTAs, and each (chunk,
+// sequence, KV head) leaves one partial record (the layout the merges use).
+// The attention kernel then streams each sequence's remaining blocks and
+// merges the prefix chunks' records into that sequence's result.
+constexpr int kPfxWarps = 4;                    // consumer warps of a prefix CTA
+constexpr int kPfxRows = 16 * kPfxWarps;        // query rows per prefix CTA
+constexpr int kPfxStages = 4;
+constexpr int kMaxPfxChunks = 32;
+
+struct PrefixParams {
+  const __half* q;
+  const int32_t* prefix_blocks;  // [num_prefix_blocks] physical ids shared by every sequence
+  float* records;                // prefix records [nchunks][S][Hkv][rec_floats(G, D)]
+  int32_t* err;
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int num_blocks;
+  int prefix_blocks_n;
+  int chunk_blocks;              // prefix blocks per chunk
+  float qscale;                  // scale * log2(e)
+};
+
+template <int D, int BS, int G>
+__global__ void __launch_bounds__((kPfxWarps + 1) * 32)
+    paged_prefix_kernel(const PrefixParams p, const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap) {
+  constexpr int TS = 16;                       // tokens per stage
+  constexpr int NHALF = D / 64;
+  constexpr int HALF = TS * 128;               // one 64-dim half of one head's 16 rows
+  constexpr int TILE = NHALF * HALF;
+  constexpr int STAGE = 2 * TILE;
+  constexpr int RS = rec_floats(G, D);
+  extern __shared__ __align__(128) unsigned char psm[];
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(psm);
+  uint64_t* empty_bar = full_bar + kPfxStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(psm + 2 * kPfxStages * 8);
+  const uint32_t base = smem_addr(psm);
+  unsigned char* ring = psm + (((base + 256 + 1023u) & ~1023u) - base);
+  unsigned char* qtile = ring + kPfxStages * STAGE;  // [kPfxRows][D] fp16, 16-byte chunks swizzled
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kvh = blockIdx.y, c = blockIdx.z;
+  const int S = p.num_seqs;
+  const int j_lo = c * p.chunk_blocks;
+  const int j_hi = min(p.prefix_blocks_n, j_lo + p.chunk_blocks);
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kPfxStages; ++st) {
+      mbar_init(smem_addr(&full_bar[st]), 1);
+      mbar_init(smem_addr(&empty_bar[st]), kPfxWarps);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  if (warp == kPfxWarps) {
+    // ---- producer: this chunk's prefix blocks, 16 tokens per stage ----
+    uint32_t g = 0;
+    for (int j0 = j_lo; j0 < j_hi; j0 += 32) {
+      const int nn = min(32, j_hi - j0);
+      const int phys_lane = lane < nn ? __ldg(p.prefix_blocks + j0 + lane) : 0;
+      for (int jj = 0; jj < nn; ++jj) {
+        const int phys = __shfl_sync(0xffffffffu, phys_lane, jj);
+        const bool bad = phys < 0 || phys >= p.num_blocks;
+        for (int sb = 0; sb < BS / TS; ++sb, ++g) {
+          const int st = g % kPfxStages;
+          const uint32_t use = g / kPfxStages;
+          if (__shfl_sync(0xffffffffu, *abort_flag, 0)) continue;
+          if (use > 0 &&
+              !warp_wait_phase(smem_addr(&empty_bar[st]), (use - 1) & 1, abort_flag, p.err))
+            continue;
+          if (lane == 0) {
+            const uint32_t fb = smem_addr(&full_bar[st]);
+            if (bad) atomicOr(p.err, PA_DEVERR_BAD_BLOCK);
+            mbar_arrive_expect_tx(fb, bad ? 0u : static_cast<uint32_t>(STAGE));
+            if (!bad) {
+              const uint32_t dst = smem_addr(ring + static_cast<size_t>(st) * STAGE);
+#pragma unroll
+              for (int h = 0; h < NHALF; ++h) {
+                tma_load_4d(dst + h * HALF, &kmap, 64 * h, sb * TS, kvh, phys, fb);
+                tma_load_4d(dst + TILE + h * HALF, &vmap, 64 * h, sb * TS, kvh, phys, fb);
+              }
+            }
+          }
+          __syncwarp();
+        }
+      }
+    }
+    if (*abort_flag) {
+      const uint32_t first = g > static_cast<uint32_t>(kPfxStages) ? g - kPfxStages : 0;
+      for (uint32_t gi = first; gi < g; ++gi) {
+        const unsigned long long t0 = global_ns();
+        while (!mbar_try_wait(smem_addr(&full_bar[gi % kPfxStages]), (gi / kPfxStages) & 1) &&
+               global_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+    return;
+  }
+
+  // ---- consumer warp: 16 query rows (sequence, query head of the group) ----
+  const int gid = lane >> 2, tig = lane & 3;
+  const int ld_row = lane & 7, ld_mat = lane >> 3;
+  const int row0 = blockIdx.x * kPfxRows + warp * 16;
+  unsigned char* qw = qtile + warp * 16 * (D * 2);
+  // q rows -> shared memory (zero rows past the batch), then A fragments
+  for (int e = lane; e < 16 * (D / 8); e += 32) {
+    const int r = e / (D / 8), ch = e % (D / 8);
+    const int row = row0 + r, seq = row / G, gg = row % G;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (seq < S)
+      v = __ldg(reinterpret_cast<const uint4*>(
+          p.q + (static_cast<long long>(seq) * p.num_q_heads + kvh * G + gg) * D) + ch);
+    *reinterpret_cast<uint4*>(qw + r * (D * 2) + ((ch ^ (r & 7)) << 4)) = v;
+  }
+  __syncwarp();
+  uint32_t qa[D / 16][4];
+  {
+    const int r = ((ld_mat & 1) << 3) + ld_row;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int ch = 2 * kk + (ld_mat >> 1);
+      ldsm_x4(smem_addr(qw) + r * (D * 2) + ((ch ^ ld_row) << 4), qa[kk][0], qa[kk][1],
+              qa[kk][2], qa[kk][3]);
+    }
+  }
+  float m0 = -INFINITY, m1 = -INFINITY;  // rows gid, gid + 8: running max (log2 units)
+  float l0 = 0.f, l1 = 0.f;              // and partial sums over this lane's tokens
+  float o[D / 8][4];                     // O[row gid (+8)][dim 8*nd + 2*tig (+1)]
+#pragma unroll
+  for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+
+  const uint32_t nstages = static_cast<uint32_t>(j_hi > j_lo ? (j_hi - j_lo) * (BS / TS) : 0);
+  for (uint32_t g = 0; g < nstages; ++g) {
+    const int st = g % kPfxStages;
+    if (!warp_wait_phase(smem_addr(&full_bar[st]), (g / kPfxStages) & 1, abort_flag, p.err))
+      continue;
+    const uint32_t kaddr = smem_addr(ring + static_cast<size_t>(st) * STAGE);
+    const uint32_t vaddr = kaddr + TILE;
+    // ---- S = Q K^T (16 rows x 16 tokens) ----
+    float sc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+      const uint32_t rowa = kaddr + (nt * 8 + ld_row) * 128;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; kk += 2) {
+        const int gc = 2 * kk + ld_mat;  // 8-dim chunk of the row
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(rowa + (gc >> 3) * HALF + (((gc & 7) ^ ld_row) << 4), b0, b1, b2, b3);
+        mma_16816(sc[nt], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+        mma_16816(sc[nt], qa[kk + 1][0], qa[kk + 1][1], qa[kk + 1][2], qa[kk + 1][3], b2, b3);
+      }
+    }
+    // ---- online softmax per row ----
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[nt][e] *= p.qscale;
+      mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
+      mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    uint32_t pa[4];  // P as the A operand: rows gid / gid + 8, tokens 2tig.. / 8 + 2tig..
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const float p0 = fast_exp2(sc[nt][0] - mn0), p1 = fast_exp2(sc[nt][1] - mn0);
+      const float p2 = fast_exp2(sc[nt][2] - mn1), p3 = fast_exp2(sc[nt][3] - mn1);
+      s0 += p0 + p1;
+      s1 += p2 + p3;
+      pa[2 * nt] = pack_half2(p0, p1);
+      pa[2 * nt + 1] = pack_half2(p2, p3);
+    }
+    l0 = l0 * al0 + s0;
+    l1 = l1 * al1 + s1;
+#pragma unroll
+    for (int nd = 0; nd < D / 8; ++nd) {
+      o[nd][0] *= al0;
+      o[nd][1] *= al0;
+      o[nd][2] *= al1;
+      o[nd][3] *= al1;
+    }
+    // ---- O += P V: B = V [token][dim] by ldmatrix.trans, two 8-dim tiles per x4 ----
+    const uint32_t rowv = vaddr + (((ld_mat & 1) << 3) + ld_row) * 128;
+#pragma unroll
+    for (int q2 = 0; q2 < D / 16; ++q2) {
+      const int gc = 2 * q2 + (ld_mat >> 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(rowv + (gc >> 3) * HALF + (((gc & 7) ^ ld_row) << 4), b0, b1, b2, b3);
+      mma_16816(o[2 * q2], pa[0], pa[1], pa[2], pa[3], b0, b1);
+      mma_16816(o[2 * q2 + 1], pa[0], pa[1], pa[2], pa[3], b2, b3);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&empty_bar[st]));
+  }
+
+  // ---- the chunk's partial record of each row ----
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int row = row0 + gid + 8 * half, seq = row / G, gg = row % G;
+    if (seq >= S) continue;
+    float* rec = p.records + ((static_cast<long long>(c) * S + seq) * p.num_kv_heads + kvh) * RS;
+#pragma unroll
+    for (int nd = 0; nd < D / 8; ++nd)
+      *reinterpret_cast<float2*>(rec + gg * D + 8 * nd + 2 * tig) =
+          make_float2(o[nd][2 * half], o[nd][2 * half + 1]);
+    if (tig == 0) {
+      rec[G * D + 2 * gg] = half ? m1 : m0;
+      rec[G * D + 2 * gg + 1] = half ? l1 : l0;
+    }
+  }
+}
 
 // --------------------------------------------------------------- host ---
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
@@ -1401,10 +1682,10 @@ struct LaunchCfg {
   long long grid = 0;
 };
 
-template <int D, int BS, int G, bool KV8 = false>
+template <int D, int BS, int G, bool KV8 = false, bool PFX = false>
 pa_status launch_config(const pa::DeviceInfo& dev, int S, int Hkv, LaunchCfg* cfg) {
   using SH = Shape<D, BS, G, KV8>;
-  auto kernel = paged_decode_kernel<D, BS, G, KV8>;
+  auto kernel = paged_decode_kernel<D, BS, G, KV8, PFX>;
   cfg->hg = head_group(Hkv);
   const int stage = SH::stage_bytes(cfg->hg);
   int nst = cfg->hg * kRingBytesPerHead / stage;
@@ -1456,11 +1737,11 @@ pa_status launch_config(const pa::DeviceInfo& dev, int S, int Hkv, LaunchCfg* cf
   return PA_OK;
 }
 
-template <int D, int BS, int G, bool KV8>
+template <int D, int BS, int G, bool KV8, bool PFX = false>
 pa_status launch_decode(DecodeParams prm, const pa::DeviceInfo& dev, cudaStream_t stream) {
   using SH = Shape<D, BS, G, KV8>;
   LaunchCfg cfg;
-  if (pa_status s = launch_config<D, BS, G, KV8>(dev, prm.num_seqs, prm.num_kv_heads, &cfg))
+  if (pa_status s = launch_config<D, BS, G, KV8, PFX>(dev, prm.num_seqs, prm.num_kv_heads, &cfg))
     return s;
   prm.hg = cfg.hg;
   prm.nst = cfg.nst;
@@ -1484,7 +1765,7 @@ pa_status launch_decode(DecodeParams prm, const pa::DeviceInfo& dev, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&lc, paged_decode_kernel<D, BS, G, KV8>, prm, kmap, vmap);
+  cudaError_t e = cudaLaunchKernelEx(&lc, paged_decode_kernel<D, BS, G, KV8, PFX>, prm, kmap, vmap);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_decode_attention launch");
 
@@ -1527,6 +1808,100 @@ pa_status launch_config_any(int D, int BS, int G, const pa::DeviceInfo& dev, int
 #undef PA_CFG_G
 #undef PA_CFG_CASE
   return pa::fail(PA_ERR_UNSUPPORTED, "pa_decode_attention: unsupported shape");
+}
+
+// --- shared prefix ---------------------------------------------------------
+// Prefix chunks: enough (row tiles x KV heads x chunks) CTAs to cover the SMs
+// about twice, at most kMaxPfxChunks and at most one per prefix block.
+struct PfxGeom {
+  int row_tiles, chunks, chunk_blocks;
+};
+PfxGeom prefix_geometry(int S, int G, int Hkv, int P, int sm_count) {
+  PfxGeom g;
+  g.row_tiles = (S * G + kPfxRows - 1) / kPfxRows;
+  const long long base = static_cast<long long>(g.row_tiles) * Hkv;
+  long long c = (2ll * sm_count + base - 1) / base;
+  if (c > kMaxPfxChunks) c = kMaxPfxChunks;
+  if (c > P) c = P;
+  if (c < 1) c = 1;
+  g.chunk_blocks = static_cast<int>((P + c - 1) / c);
+  g.chunks = (P + g.chunk_blocks - 1) / g.chunk_blocks;
+  return g;
+}
+
+template <int D, int BS, int G>
+pa_status launch_prefix(const PrefixParams& pp, const PfxGeom& geo, const void* k_pool,
+                        const void* v_pool, int Hkv, int NB, const pa::DeviceInfo& dev,
+                        cudaStream_t stream) {
+  constexpr int STAGE = 2 * (D / 64) * 16 * 128;
+  const size_t smem = 256 + 1024 + static_cast<size_t>(kPfxStages) * STAGE +
+                      static_cast<size_t>(kPfxRows) * D * 2;
+  auto kernel = paged_prefix_kernel<D, BS, G>;
+  {
+    static std::mutex mu;
+    static bool set[64] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (!set[dev.device]) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+      if (e != cudaSuccess) return pa::cuda_fail(e, "cudaFuncSetAttribute(prefix)");
+      set[dev.device] = true;
+    }
+  }
+  CUtensorMap kmap, vmap;
+  MapKey kk{dev.device, k_pool, D, BS, Hkv, NB, 1, 16, 2};
+  MapKey vk{dev.device, v_pool, D, BS, Hkv, NB, 1, 16, 2};
+  if (pa_status s = pool_tensor_map(kk, &kmap)) return s;
+  if (pa_status s = pool_tensor_map(vk, &vmap)) return s;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(static_cast<unsigned>(geo.row_tiles), static_cast<unsigned>(Hkv),
+                    static_cast<unsigned>(geo.chunks));
+  lc.blockDim = dim3((kPfxWarps + 1) * 32);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&lc, kernel, pp, kmap, vmap);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return pa::cuda_fail(e, "shared-prefix kernel launch");
+  return PA_OK;
+}
+
+template <int BS, int G>
+pa_status shared_prefix_pass(const PrefixParams& pp, const PfxGeom& geo, DecodeParams prm,
+                             const void* k_pool, const void* v_pool, const pa::DeviceInfo& dev,
+                             cudaStream_t s) {
+  if (pa_status st = launch_prefix<128, BS, G>(pp, geo, k_pool, v_pool, prm.num_kv_heads,
+                                                prm.num_blocks, dev, s))
+    return st;
+  return launch_decode<128, BS, G, false, true>(prm, dev, s);
+}
+
+// Workspace of the shared-prefix call: the regular layout, then one record per
+// (sequence, KV head) for segments streamed whole, then the prefix chunks'
+// records.
+// Regions are counted in whole records from the start of the record area, so
+// every record index addresses a record-aligned slot.
+struct PfxLayout {
+  Layout base;
+  long long own_rec = 0, pfx_rec = 0;  // first record of each region
+  size_t total = 0;
+};
+PfxLayout shared_prefix_layout(int S, int Hq, int Hkv, int D, int MB, int P) {
+  PfxLayout w;
+  w.base = workspace_layout(S, Hq, Hkv, D, MB, 0);
+  const int hg = head_group(Hkv);
+  const size_t rec = static_cast<size_t>(rec_floats(Hq / Hkv, D)) * 4;
+  const long long cmax = P < kMaxPfxChunks ? (P > 0 ? P : 1) : kMaxPfxChunks;
+  w.own_rec = 2 * max_chunks(S, Hkv / hg, MB, 0) * hg;  // after the chunk records
+  w.pfx_rec = w.own_rec + static_cast<long long>(S) * Hkv;
+  const long long nrec = w.pfx_rec + cmax * S * Hkv;
+  w.total = w.base.records + round256(static_cast<size_t>(nrec) * rec);
+  if (w.total < w.base.total) w.total = w.base.total;
+  return w;
 }
 
 pa_status check_decode_shape(int S, int Hq, int Hkv, int D, int BS, int MB, int part_tokens) {
@@ -1656,6 +2031,10 @@ static DecodeParams make_params(const pa_half* q, const pa_half* k_pool, const p
   prm.seq_lens = seq_lens;
   prm.k_scale = nullptr;
   prm.v_scale = nullptr;
+  prm.pfx_blocks = 0;
+  prm.pfx_chunks = 0;
+  prm.pfx_rec_base = 0;
+  prm.pfx_own_base = 0;
   prm.out = reinterpret_cast<__half*>(out);
   prm.records = reinterpret_cast<float*>(ws + lay.records);
   prm.counters = reinterpret_cast<unsigned long long*>(ws + lay.counters);
@@ -1753,6 +2132,95 @@ pa_status pa_decode_attention_fp8(const pa_half* q, const uint8_t* k_pool, const
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   pa_status st = block_size == 16 ? dispatch_g<128, 16, true>(G, prm, dev, s)
                                   : dispatch_g<128, 32, true>(G, prm, dev, s);
+  return st == PA_OK ? pa::ok() : st;
+}
+
+size_t pa_decode_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                                int head_dim, int block_size,
+                                                int max_blocks_per_seq, int num_prefix_blocks) {
+  if (check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                         max_blocks_per_seq, 0) != PA_OK)
+    return 0;
+  if (num_prefix_blocks < 0 || num_prefix_blocks > max_blocks_per_seq) return 0;
+  return shared_prefix_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                              num_prefix_blocks)
+      .total;
+}
+
+pa_status pa_decode_attention_shared_prefix(
+    const pa_half* q, const pa_half* k_pool, const pa_half* v_pool, const int32_t* prefix_blocks,
+    int num_prefix_blocks, const int32_t* block_table, const int32_t* seq_lens, int num_seqs,
+    int num_q_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+    int num_blocks, float scale, pa_half* out, void* workspace, size_t workspace_bytes,
+    pa_stream_t stream) {
+  if (pa_status s = check_decode_call("pa_decode_attention_shared_prefix", q, k_pool, v_pool,
+                                      block_table, seq_lens, num_seqs, num_q_heads, num_kv_heads,
+                                      head_dim, block_size, max_blocks_per_seq, num_blocks, scale,
+                                      out, 0))
+    return s;
+  if (head_dim != 128 || (block_size != 16 && block_size != 32))
+    return pa::fail(PA_ERR_UNSUPPORTED,
+                    "pa_decode_attention_shared_prefix: head_dim %d / block_size %d (supported: "
+                    "head_dim 128, block_size 16 or 32)", head_dim, block_size);
+  if (num_prefix_blocks < 0 || num_prefix_blocks > max_blocks_per_seq)
+    return pa::fail(PA_ERR_INVALID_ARG,
+                    "pa_decode_attention_shared_prefix: num_prefix_blocks %d not in [0, %d]",
+                    num_prefix_blocks, max_blocks_per_seq);
+  if (num_seqs == 0) return pa::ok();
+  if (num_prefix_blocks > 0 &&
+      (!prefix_blocks || (reinterpret_cast<uintptr_t>(prefix_blocks) & 3)))
+    return pa::fail(PA_ERR_INVALID_ARG,
+                    "pa_decode_attention_shared_prefix: NULL or misaligned prefix_blocks");
+  if (!workspace || !pa::aligned16(workspace))
+    return pa::fail(PA_ERR_INVALID_ARG,
+                    "pa_decode_attention_shared_prefix: NULL or misaligned workspace");
+  const PfxLayout lay = shared_prefix_layout(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                             max_blocks_per_seq, num_prefix_blocks);
+  if (workspace_bytes < lay.total)
+    return pa::fail(PA_ERR_INVALID_ARG,
+                    "pa_decode_attention_shared_prefix: workspace %zu < %zu bytes",
+                    workspace_bytes, lay.total);
+  if (num_prefix_blocks == 0)
+    return pa_decode_attention(q, k_pool, v_pool, block_table, seq_lens, num_seqs, num_q_heads,
+                               num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                               num_blocks, scale, out, workspace, workspace_bytes, 0, stream);
+  pa::DeviceInfo dev;
+  if (pa_status s = pa::current_device(&dev)) return s;
+  const int G = num_q_heads / num_kv_heads;
+  const int P = num_prefix_blocks;
+  const PfxGeom geo = prefix_geometry(num_seqs, G, num_kv_heads, P, dev.sm_count);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  const size_t rec_bytes = static_cast<size_t>(rec_floats(G, head_dim)) * 4;
+  // the suffix pass: the table past the prefix's columns, lengths past its tokens
+  DecodeParams prm = make_params(q, k_pool, v_pool, block_table + P, seq_lens, num_seqs,
+                                 num_q_heads, num_kv_heads, max_blocks_per_seq, num_blocks, scale,
+                                 out, ws, lay.base, 0);
+  prm.err = pa::device_error_word();
+  if (!prm.err) return PA_ERR_CUDA;
+  prm.pfx_blocks = P;
+  prm.pfx_chunks = geo.chunks;
+  prm.pfx_own_base = lay.own_rec;
+  prm.pfx_rec_base = lay.pfx_rec;
+  PrefixParams pp;
+  pp.q = reinterpret_cast<const __half*>(q);
+  pp.prefix_blocks = prefix_blocks;
+  pp.records = reinterpret_cast<float*>(ws + lay.base.records + lay.pfx_rec * rec_bytes);
+  pp.err = prm.err;
+  pp.num_seqs = num_seqs;
+  pp.num_q_heads = num_q_heads;
+  pp.num_kv_heads = num_kv_heads;
+  pp.num_blocks = num_blocks;
+  pp.prefix_blocks_n = P;
+  pp.chunk_blocks = geo.chunk_blocks;
+  pp.qscale = scale * kLog2e;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  pa_status st;
+#define PA_PFX_CASE(bs, g) \
+  if (block_size == bs && G == g) st = shared_prefix_pass<bs, g>(pp, geo, prm, k_pool, v_pool, dev, s); else
+  PA_PFX_CASE(16, 1) PA_PFX_CASE(16, 2) PA_PFX_CASE(16, 4) PA_PFX_CASE(16, 8)
+  PA_PFX_CASE(32, 1) PA_PFX_CASE(32, 2) PA_PFX_CASE(32, 4) PA_PFX_CASE(32, 8)
+  st = pa::fail(PA_ERR_UNSUPPORTED, "pa_decode_attention_shared_prefix: unsupported shape");
+#undef PA_PFX_CASE
   return st == PA_OK ? pa::ok() : st;
 }
 

@@ -24,7 +24,8 @@ from typing import List, Optional, Tuple
 import numpy as np
 
 from . import (BlockAllocator, alloc_workspace, pa_append_kv, pa_append_kv_fp8, pa_copy_blocks,
-               pa_copy_blocks_fp8, pa_decode_attention, pa_decode_attention_fp8)
+               pa_copy_blocks_fp8, pa_decode_attention, pa_decode_attention_fp8,
+               pa_decode_attention_shared_prefix, pa_decode_shared_prefix_workspace_bytes)
 
 
 def _to_dev(arr, device, dtype=None):
@@ -179,9 +180,11 @@ class SharedPrefixRunner(DecodeBatchRunner):
     scale and step_inputs(step, num_active) -> (q, k_new, v_new).
     """
 
-    def __init__(self, workload, device="cuda", partition_tokens: int = 0):
+    def __init__(self, workload, device="cuda", partition_tokens: int = 0,
+                 prefix_aware: bool = True):
         import torch
         w = workload
+        self.prefix_aware = prefix_aware
         self.kv_dtype = "fp16"
         self.batch = w
         self.device = torch.device(device)
@@ -205,7 +208,33 @@ class SharedPrefixRunner(DecodeBatchRunner):
         self.workspace = alloc_workspace(self.num_seqs, w.num_q_heads, w.num_kv_heads,
                                          w.head_dim, w.block_size, self.max_blocks,
                                          partition_tokens, self.device)
+        # the full blocks of the prefix, shared by every table
+        self.num_prefix_blocks = int(w.prefix_len) // w.block_size
+        if prefix_aware:
+            n = pa_decode_shared_prefix_workspace_bytes(self.num_seqs, w.num_q_heads,
+                                                        w.num_kv_heads, w.head_dim, w.block_size,
+                                                        self.max_blocks, self.num_prefix_blocks)
+            self.workspace = torch.zeros(max(n, 16), dtype=torch.uint8, device=self.device)
         self.plan = None
+
+    def plan_step(self):
+        plan = super().plan_step()
+        self.d_prefix = _to_dev(plan.block_table[0, :self.num_prefix_blocks].astype(np.int32),
+                                self.device)
+        return plan
+
+    def attend(self, stream=None):
+        if not self.prefix_aware:
+            return super().attend(stream)
+        pa_decode_attention_shared_prefix(self.q, self.k_pool, self.v_pool, self.d_prefix,
+                                          self.d_table, self.d_lens, float(self.batch.scale),
+                                          out=self.out, workspace=self.workspace, stream=stream)
+        return self.out
+
+    # kernels one attend() enqueues with the prefix-aware call
+    @property
+    def attend_launches(self) -> int:
+        return 2 if self.prefix_aware else 1
 
     def unique_kv_bytes(self) -> int:
         """K+V bytes of the distinct rows the step attends (the shared prefix

@@ -1,0 +1,123 @@
+"""pa_decode_attention_shared_prefix on the GPU (through the C ABI) against the
+fp64 oracle's plain attention: sequences that share their first P physical
+blocks, with private suffixes of every length class. Rows no sequence may read
+are NaN-poisoned."""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from tests.gpu_helpers import assert_close_attention, poison_unread_rows
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def pa(libpa):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return libpa
+
+
+def d(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _case(seed, S, Hq, Hkv, BS, P, suffix_lens, D=128, extra=4):
+    """P shared blocks, then per-sequence private blocks for its suffix."""
+    rng = np.random.default_rng(seed)
+    lens = [P * BS + s for s in suffix_lens]
+    priv = [-(-s // BS) for s in suffix_lens]
+    nb = P + sum(priv) + extra
+    perm = rng.permutation(nb).astype(np.int32)
+    prefix = perm[:P]
+    mb = P + max(priv) + 1
+    table = -np.ones((S, mb), np.int32)
+    pos = P
+    for i in range(S):
+        table[i, :P] = prefix
+        table[i, P:P + priv[i]] = perm[pos:pos + priv[i]]
+        pos += priv[i]
+    q = rng.standard_normal((S, Hq, D)).astype(np.float16)
+    kp = rng.standard_normal((nb, BS, Hkv, D)).astype(np.float16)
+    vp = rng.standard_normal((nb, BS, Hkv, D)).astype(np.float16)
+    kp, vp = poison_unread_rows(kp, vp, table, lens, BS)
+    return q, kp, vp, prefix, table, np.asarray(lens, np.int32)
+
+
+def _run(pa, q, kp, vp, prefix, table, lens, scale):
+    out = pa.pa_decode_attention_shared_prefix(d(q), d(kp), d(vp), d(prefix), d(table), d(lens),
+                                               scale)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+@pytest.mark.parametrize("BS", [16, 32])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_shared_prefix_matrix(pa, BS, G):
+    Hkv = 2
+    suffix = [0, 1, BS - 1, BS, 3 * BS + 5, 200, 7]
+    q, kp, vp, prefix, table, lens = _case(BS * 10 + G, len(suffix), G * Hkv, Hkv, BS, 5, suffix)
+    scale = np.float32(1 / math.sqrt(128))
+    got = _run(pa, q, kp, vp, prefix, table, lens, scale)
+    exp = oracle.decode_attention(q, kp, vp, table, lens, scale)
+    assert_close_attention(got, exp, f"shared prefix BS{BS} G{G}")
+    assert pa.pa_device_error() == 0
+
+
+def test_shared_prefix_many_rows_and_chunks(pa):
+    """300 sequences (19 row tiles of 64 (sequence, head) rows per KV head)
+    over a 96-block prefix split into chunks."""
+    rng = np.random.default_rng(3)
+    suffix = rng.integers(0, 80, 300).tolist()
+    q, kp, vp, prefix, table, lens = _case(4, 300, 32, 8, 16, 96, suffix)
+    got = _run(pa, q, kp, vp, prefix, table, lens, np.float32(0.088))
+    seqs = [0, 1, 63, 64, 150, 299]
+    exp = oracle.decode_attention(q, kp, vp, table, lens, np.float32(0.088), seqs=seqs)
+    assert_close_attention(got[seqs], exp[seqs], "many rows")
+    assert np.isfinite(got).all()
+
+
+def test_shared_prefix_first_step_of_prefix_workload(pa):
+    """The shared-prefix workload's first decode step (128 sequences forked
+    from one 2040-token prefix, 32q/8kv): tables from the native block
+    manager after the copy-on-write step; the 127 full prefix blocks are the
+    shared prefix."""
+    w = synthetic.config4_shared_prefix()
+    a = pa.BlockAllocator(w.num_blocks, w.block_size, w.free_order)
+    a.add_seq(0, w.prefix_len)
+    for c in range(1, w.num_seqs):
+        a.fork(0, c)
+    active = list(range(w.num_seqs))
+    a.append_slots(active)
+    mb = -(-(w.prefix_len + 1) // w.block_size)
+    table, lens = a.build_tables(active, mb)
+    P = w.prefix_len // w.block_size
+    prefix = table[0, :P].copy()
+    assert (table[:, :P] == prefix).all()
+    q = w.step_inputs(0, w.num_seqs)[0]
+    got = _run(pa, q, w.k_pool, w.v_pool, prefix, table, lens, w.scale)
+    seqs = [0, 5, 64, 127]
+    exp = oracle.decode_attention(q, w.k_pool, w.v_pool, table, lens, w.scale, seqs=seqs)
+    assert_close_attention(got[seqs], exp[seqs], "prefix workload first step")
+
+
+def test_zero_prefix_blocks_is_plain_decode(pa):
+    q, kp, vp, prefix, table, lens = _case(8, 3, 8, 2, 16, 0, [5, 40, 300])
+    got = _run(pa, q, kp, vp, np.zeros(0, np.int32), table, lens, np.float32(0.1))
+    exp = oracle.decode_attention(q, kp, vp, table, lens, np.float32(0.1))
+    assert_close_attention(got, exp, "P = 0")
+
+
+def test_sequence_shorter_than_prefix_is_reported(pa):
+    q, kp, vp, prefix, table, lens = _case(9, 2, 8, 2, 16, 4, [3, 3])
+    lens = lens.copy()
+    lens[1] = 20                                   # 4 prefix blocks hold 64 tokens
+    _run(pa, q, kp, vp, prefix, table, lens, np.float32(0.1))
+    with pytest.raises(pa.PaError) as e:
+        pa.pa_device_error()
+    assert e.value.flags & pa.PA_DEVERR_BAD_LEN
