@@ -37,7 +37,7 @@ from .attention import (  # noqa: F401
     merge_partials,
     split_context_attention,
 )
-from .cache_ops import append_kv, copy_blocks  # noqa: F401
+from .cache_ops import append_kv, copy_blocks, swap_blocks  # noqa: F401
 from .fp8 import (  # noqa: F401
     e4m3_decode,
     e4m3_encode,

@@ -27,6 +27,19 @@ Readings taken where the pages are silent:
     writes in place.
   * Every operation is all-or-nothing: when the free list is too short the
     state is left unchanged and OutOfBlocks is raised.
+
+Swapping (Document 04, §9/§10: under memory pressure a scheduler may preempt
+a sequence by swapping its blocks out; the pages give no mechanism). Readings:
+  * The manager also owns a pool of host blocks with its own FIFO free list.
+  * swap_out(seq) takes one host block per logical block (in logical order),
+    returns the (device, host) pairs to copy, then drops the sequence's device
+    references in logical order: a block other tables still reference stays
+    on the device for them. The sequence keeps its length; it cannot append,
+    fork or appear in a table until it is swapped back in.
+  * swap_in(seq) takes fresh device blocks (private: sharing is not restored),
+    returns the (host, device) pairs to copy, then returns the host blocks to
+    the host free list in logical order.
+  * Freeing a swapped-out sequence returns its host blocks.
 """
 
 from __future__ import annotations
@@ -56,6 +69,11 @@ class BlockAllocator:
         self.lens: Dict[int, int] = {}
         self.cow_copies = 0
         self.alloc_failures = 0
+        self.host_free: deque = deque()
+        self.num_host_blocks = 0
+        self.host_tables: Dict[int, List[int]] = {}
+        self.swap_outs = 0
+        self.swap_ins = 0
 
     # -- helpers ------------------------------------------------------------
     def _take(self) -> int:
@@ -74,7 +92,7 @@ class BlockAllocator:
     # -- operations ---------------------------------------------------------
     def add_seq(self, seq: int, length: int) -> None:
         """Register a sequence already holding `length` tokens."""
-        if seq in self.tables or length < 0:
+        if seq in self.lens or length < 0:
             raise ValueError("sequence exists or negative length")
         n = self._blocks_for(length)
         if n > len(self.free):
@@ -85,7 +103,7 @@ class BlockAllocator:
 
     def fork(self, parent: int, child: int) -> None:
         """The child shares every block of the parent (counts + 1)."""
-        if parent not in self.tables or child in self.tables:
+        if parent not in self.tables or child in self.lens:
             raise ValueError("bad fork")
         tab = list(self.tables[parent])
         for b in tab:
@@ -100,7 +118,7 @@ class BlockAllocator:
         is needed.
         """
         if seq not in self.tables:
-            raise ValueError("unknown sequence")
+            raise ValueError("unknown or swapped-out sequence")
         L = self.lens[seq]
         tab = self.tables[seq]
         BS = self.block_size
@@ -126,11 +144,68 @@ class BlockAllocator:
         return slot, cow_src, cow_dst
 
     def free_seq(self, seq: int) -> None:
-        """Release every block of the sequence, in logical order."""
+        """Release every block of the sequence, in logical order (host
+        blocks if it is swapped out)."""
+        if seq in self.host_tables:
+            for h in self.host_tables.pop(seq):
+                self.host_free.append(h)
+            self.lens.pop(seq)
+            return
         tab = self.tables.pop(seq)
         self.lens.pop(seq)
         for b in tab:
             self._release(b)
+
+    # -- swapping -------------------------------------------------------------
+    def add_host_pool(self, num_host_blocks: int, initial_free_order=None) -> None:
+        if self.num_host_blocks or num_host_blocks <= 0:
+            raise ValueError("host pool exists or bad size")
+        order = list(range(num_host_blocks)) if initial_free_order is None else \
+            [int(b) for b in initial_free_order]
+        if sorted(order) != list(range(num_host_blocks)):
+            raise ValueError("host free order must be a permutation of the host pool")
+        self.num_host_blocks = num_host_blocks
+        self.host_free = deque(order)
+
+    def swap_out(self, seq: int) -> List[Tuple[int, int]]:
+        """(device, host) block pairs to copy, in logical order; the sequence
+        then holds host blocks only."""
+        if seq not in self.tables:
+            raise ValueError("unknown or swapped-out sequence")
+        tab = self.tables[seq]
+        if len(tab) > len(self.host_free):
+            self.alloc_failures += 1
+            raise OutOfBlocks(f"need {len(tab)} host blocks, {len(self.host_free)} free")
+        hosts = [self.host_free.popleft() for _ in tab]
+        pairs = list(zip(tab, hosts))
+        for b in tab:
+            self._release(b)
+        del self.tables[seq]
+        self.host_tables[seq] = hosts
+        self.swap_outs += 1
+        return pairs
+
+    def swap_in(self, seq: int) -> List[Tuple[int, int]]:
+        """(host, device) block pairs to copy, in logical order; the sequence
+        then holds fresh device blocks."""
+        if seq not in self.host_tables:
+            raise ValueError("sequence is not swapped out")
+        hosts = self.host_tables[seq]
+        if len(hosts) > len(self.free):
+            self.alloc_failures += 1
+            raise OutOfBlocks(f"need {len(hosts)} blocks, {len(self.free)} free")
+        devs = [self._take() for _ in hosts]
+        for h in hosts:
+            self.host_free.append(h)
+        del self.host_tables[seq]
+        self.tables[seq] = devs
+        self.swap_ins += 1
+        return list(zip(hosts, devs))
+
+    def export_host_state(self) -> Tuple[List[int], int, int, int]:
+        """(host free list front to back, swapped-out sequences, swap-outs,
+        swap-ins)."""
+        return list(self.host_free), len(self.host_tables), self.swap_outs, self.swap_ins
 
     # -- inspection ---------------------------------------------------------
     def table(self, seq: int) -> List[int]:
@@ -149,7 +224,7 @@ class BlockAllocator:
             "cow_copies": self.cow_copies,
             "alloc_failures": self.alloc_failures,
             "total_refs": sum(self.ref),
-            "num_seqs": len(self.tables),
+            "num_seqs": len(self.lens),
         }
 
     def export_state(self) -> Tuple[List[int], List[int]]:

@@ -41,3 +41,17 @@ def copy_blocks(k_pool: np.ndarray, v_pool: np.ndarray, pairs) -> tuple:
         k[dst] = k_pool[src]
         v[dst] = v_pool[src]
     return k, v
+
+
+def swap_blocks(src_k: np.ndarray, src_v: np.ndarray, dst_k: np.ndarray, dst_v: np.ndarray,
+                pairs) -> tuple:
+    """Return copies of the destination pools with block dst := source block
+    src for each (src, dst) pair: a block moving between the device pool and
+    the host pool when a sequence is swapped out or back in (Document 04, §9:
+    under memory pressure a sequence's blocks may be swapped)."""
+    k = dst_k.copy()
+    v = dst_v.copy()
+    for src, dst in np.asarray(pairs).reshape(-1, 2).tolist():
+        k[dst] = src_k[src]
+        v[dst] = src_v[src]
+    return k, v
