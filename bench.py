@@ -294,6 +294,79 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------- swapping --
+def run_swap(args):
+    """Swap half of the batch's sequences out to a pinned host pool and back
+    in, each step: the block manager's pairs, then pa_swap_blocks each way."""
+    import torch
+    import paged_kv_cache_40_gb300 as pa
+    from paged_kv_cache_40_gb300 import build as pa_build
+    from paged_kv_cache_40_gb300.engine import DecodeBatchRunner
+
+    pa_build.build()
+    dev = torch.device("cuda", 0)
+    b = workload(args.workload)
+    run = DecodeBatchRunner(b, device=dev)
+    run.plan_step()
+    a = run.alloc
+    a.add_host_pool(b.num_blocks)
+    hk = torch.empty(tuple(run.k_pool.shape), dtype=run.k_pool.dtype).pin_memory()
+    hv = torch.empty(tuple(run.v_pool.shape), dtype=run.v_pool.dtype).pin_memory()
+    seqs = list(range(0, b.num_seqs, 2))
+    stream = torch.cuda.current_stream(dev)
+    block_bytes = run.k_pool[0].numel() * run.k_pool.element_size()
+
+    def step(ev=None):
+        t0 = time.perf_counter()
+        out = [p for s_ in seqs for p in a.swap_out(s_)]
+        t1 = time.perf_counter()
+        po = torch.tensor(out, dtype=torch.int32).pin_memory()
+        if ev:
+            ev[0].record(stream)
+        pa.pa_swap_blocks(run.k_pool, run.v_pool, hk, hv, po)
+        if ev:
+            ev[1].record(stream)
+        t2 = time.perf_counter()
+        back = [p for s_ in seqs for p in a.swap_in(s_)]
+        t3 = time.perf_counter()
+        pi = torch.tensor(back, dtype=torch.int32).pin_memory()
+        pa.pa_swap_blocks(hk, hv, run.k_pool, run.v_pool, pi)
+        if ev:
+            ev[2].record(stream)
+        return len(out), (t1 - t0) + (t3 - t2)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    host_s, nblk = 0.0, 0
+    for k in range(K):
+        nblk, hs = step(evs[k])
+        host_s += hs
+    torch.cuda.synchronize()
+    assert pa.pa_device_error() == 0
+    out_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    in_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    moved = nblk * block_bytes * 2
+    gbs_out = moved / (statistics.mean(out_ms) / 1e3) / 1e9
+    gbs_in = moved / (statistics.mean(in_ms) / 1e3) / 1e9
+    print(json.dumps({
+        "metric": "swap: K/V block bytes per second between the device pool and pinned host "
+                  "memory (pa_swap_blocks)",
+        "value": round(2 * moved / ((statistics.mean(out_ms) + statistics.mean(in_ms)) / 1e3) / 1e9,
+                       2),
+        "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,
+        "higher_is_better": True, "data": "synthetic",
+        "config": {"workload": b.name, "sequences_swapped": len(seqs), "blocks_per_step": nblk,
+                   "bytes_each_way": moved},
+        "out_gbs": round(gbs_out, 2), "in_gbs": round(gbs_in, 2),
+        "out_us": round(1e3 * statistics.mean(out_ms), 2),
+        "in_us": round(1e3 * statistics.mean(in_ms), 2),
+        "host_block_manager_us_per_step": round(1e6 * host_s / K, 1),
+    }), flush=True)
+
+
 # ----------------------------------------------------------------- our arm --
 def run_ours(args, world, rank, local):
     import torch
@@ -501,6 +574,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa4_u128_2048")
     ap.add_argument("--partition", type=int, default=0, help="tokens per split (0 = default)")
+    ap.add_argument("--op", choices=["decode", "swap"], default="decode",
+                    help="decode: the decode step (default); swap: swapping throughput")
     ap.add_argument("--plain-decode", action="store_true",
                     help="shared-prefix workload: attend with the generic call, not the "
                          "prefix-aware one")
@@ -512,7 +587,10 @@ def main():
     ap.add_argument("--ref-sample-seqs", type=int, default=4)
     args = ap.parse_args()
     world, rank, local = dist_setup(args)
-    if args.impl == "reference":
+    if args.op == "swap" and args.impl != "reference":
+        if rank == 0:
+            run_swap(args)
+    elif args.impl == "reference":
         run_reference(args, world, rank)
     else:
         run_ours(args, world, rank, local)

@@ -421,6 +421,56 @@ PA_API pa_status pa_alloc_stats(const pa_allocator* a, pa_alloc_stats_t* out);
 PA_API pa_status pa_alloc_export_state(const pa_allocator* a, int32_t* free_order,
                                 int* num_free, int32_t* refcounts);
 
+/* ------------------------------------------------------------------------
+ * Swapping a sequence's blocks to a host pool and back (preemption).
+ *
+ * Source: "Phase 7 · Document 04 — PagedAttention", §9 (under memory
+ * pressure the scheduler may evict/recompute or swap a sequence's blocks)
+ * and §10 (preemption by evict/recompute/swap is a latency event). The pages
+ * give no mechanism; this library's reading: the block manager owns an
+ * optional host pool with its own FIFO free list (ids 0 .. num_host_blocks-1
+ * of a caller-owned host pool with the device pool's block shape);
+ * pa_alloc_swap_out takes one host block per logical block of the sequence
+ * (all or nothing), writes the (device, host) pairs to copy in logical order
+ * and drops the sequence's device references (blocks other tables share stay
+ * for them); the sequence keeps its length but cannot append, fork or be
+ * tabled until pa_alloc_swap_in takes fresh private device blocks (all or
+ * nothing), writes the (host, device) pairs and returns the host blocks.
+ * pa_alloc_free_seq of a swapped-out sequence returns its host blocks.
+ * Issue the block copy (pa_swap_blocks) for swap-out pairs before any later
+ * write can reuse the released device blocks (stream order suffices).
+ * ---------------------------------------------------------------------- */
+
+/* Host pool of num_host_blocks blocks; order = initial host free list
+ * (a permutation, NULL = ascending). Once per handle. */
+PA_API pa_status pa_alloc_add_host_pool(pa_allocator* a, int num_host_blocks,
+                                        const int32_t* order);
+
+/* pairs: host int32 [cap][2]; *n = blocks moved (pairs written). */
+PA_API pa_status pa_alloc_swap_out(pa_allocator* a, int64_t seq_id, int32_t* pairs,
+                                   int cap, int* n);
+PA_API pa_status pa_alloc_swap_in(pa_allocator* a, int64_t seq_id, int32_t* pairs,
+                                  int cap, int* n);
+
+/* free_order: host int32 [num_host_blocks] (front to back, *num_free valid,
+ * the rest -1); counts: host int64 [4] = host blocks, swapped-out sequences,
+ * swap-outs, swap-ins. */
+PA_API pa_status pa_alloc_export_host_state(const pa_allocator* a, int32_t* free_order,
+                                            int* num_free, int64_t* counts);
+
+/* Copy whole blocks between two pool pairs: block pairs[i][1] of dst_k/dst_v
+ * := block pairs[i][0] of src_k/src_v, each block block_bytes bytes (a
+ * multiple of 16; BS * Hkv * D * element size). Each pool, and pairs (int32
+ * [num_pairs][2]), may be device memory or pinned (page-locked) host memory,
+ * which the kernel reads and writes through its device mapping. An id outside
+ * [0, src_blocks) or [0, dst_blocks) skips that pair and sets
+ * PA_DEVERR_BAD_BLOCK. Errors: PA_ERR_INVALID_ARG (pageable host memory,
+ * NULL or misaligned pointers), PA_ERR_CUDA. */
+PA_API pa_status pa_swap_blocks(const void* src_k, const void* src_v, int src_blocks,
+                                void* dst_k, void* dst_v, int dst_blocks,
+                                const int32_t* pairs, int num_pairs, int block_bytes,
+                                pa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -36,6 +36,7 @@ __all__ = [
     "pa_decode_workspace_bytes", "pa_decode_workspace_init", "pa_device_error",
     "pa_append_kv_fp8", "pa_copy_blocks_fp8", "pa_decode_attention_fp8",
     "pa_decode_attention_shared_prefix", "pa_decode_shared_prefix_workspace_bytes",
+    "pa_swap_blocks",
     "pa_decode_attention_fixed_scratch",
     "pa_version", "BlockAllocator", "PaError", "OutOfBlocksError", "lib",
     "DEFAULT_PARTITION_TOKENS",
@@ -170,6 +171,30 @@ def pa_decode_attention(q, k_pool, v_pool, block_table, seq_lens, scale, out=Non
         _dev(out, "out", torch.float16), _dev(workspace, "workspace", torch.uint8),
         workspace.numel(), partition_tokens, _stream_ptr(stream)))
     return out
+
+
+# ------------------------------------------------------------------ swapping --
+def pa_swap_blocks(src_k, src_v, dst_k, dst_v, pairs, stream=None) -> None:
+    """Block pairs[i][1] of dst := block pairs[i][0] of src, for K and V. Pools
+    are [blocks][BS][Hkv][D] of one element type, each a CUDA tensor or a
+    pinned CPU tensor; pairs is int32 [n][2], CUDA or pinned CPU."""
+    torch = _torch()
+    for t, name in ((src_k, "src_k"), (src_v, "src_v"), (dst_k, "dst_k"), (dst_v, "dst_v"),
+                    (pairs, "pairs")):
+        if not isinstance(t, torch.Tensor) or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous tensor")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    if src_k.shape[1:] != dst_k.shape[1:] or src_k.dtype != dst_k.dtype or \
+            src_k.shape != src_v.shape or dst_k.shape != dst_v.shape:
+        raise ValueError("source and destination pools must share their block shape and type")
+    if pairs.dtype != torch.int32 or pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be int32 [n][2]")
+    block_bytes = int(src_k[0].numel() * src_k.element_size())
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())
+    _check(_load().pa_swap_blocks(ptr(src_k), ptr(src_v), int(src_k.shape[0]), ptr(dst_k),
+                                  ptr(dst_v), int(dst_k.shape[0]), ptr(pairs),
+                                  int(pairs.shape[0]), block_bytes, _stream_ptr(stream)))
 
 
 # ------------------------------------------------------------ shared prefix --
@@ -430,6 +455,40 @@ class BlockAllocator:
             "alloc_failures": st.alloc_failures, "total_refs": st.total_refs,
             "num_seqs": st.num_seqs,
         }
+
+    # -- swapping -------------------------------------------------------------
+    def add_host_pool(self, num_host_blocks: int, initial_free_order=None) -> None:
+        order = None
+        if initial_free_order is not None:
+            order = _i32_array(initial_free_order)
+        _check(_load().pa_alloc_add_host_pool(self._h, int(num_host_blocks), order))
+        self.num_host_blocks = int(num_host_blocks)
+
+    def _swap(self, fn, seq):
+        # a sequence never holds more blocks than either pool
+        cap = max(self.num_blocks, getattr(self, "num_host_blocks", 0), 1)
+        n = ctypes.c_int()
+        buf = (ctypes.c_int32 * (2 * cap))()
+        _check(fn(self._h, seq, buf, cap, ctypes.byref(n)))
+        return [(buf[2 * i], buf[2 * i + 1]) for i in range(n.value)]
+
+    def swap_out(self, seq: int):
+        """Move the sequence to host blocks: (device, host) pairs to copy."""
+        return self._swap(_load().pa_alloc_swap_out, seq)
+
+    def swap_in(self, seq: int):
+        """Bring the sequence back to fresh device blocks: (host, device) pairs."""
+        return self._swap(_load().pa_alloc_swap_in, seq)
+
+    def export_host_state(self):
+        """(host free list front to back, swapped-out sequences, swap-outs,
+        swap-ins)."""
+        nh = getattr(self, "num_host_blocks", 0)
+        fo = (ctypes.c_int32 * max(nh, 1))()
+        nf = ctypes.c_int()
+        cnt = (ctypes.c_int64 * 4)()
+        _check(_load().pa_alloc_export_host_state(self._h, fo, ctypes.byref(nf), cnt))
+        return list(fo[:nf.value]), int(cnt[1]), int(cnt[2]), int(cnt[3])
 
     def export_state(self):
         """(free list front to back, reference counts)."""

@@ -87,6 +87,11 @@ SIGNATURES = {
     "pa_alloc_build_tables": (_i32, [_vp, _pi64, _i32, _i32, ctypes.c_int32, _pi32, _pi32]),
     "pa_alloc_stats": (_i32, [_vp, ctypes.POINTER(AllocStats)]),
     "pa_alloc_export_state": (_i32, [_vp, _pi32, _pint, _pi32]),
+    "pa_alloc_add_host_pool": (_i32, [_vp, _i32, _pi32]),
+    "pa_alloc_swap_out": (_i32, [_vp, _i64, _pi32, _i32, _pint]),
+    "pa_alloc_swap_in": (_i32, [_vp, _i64, _pi32, _i32, _pint]),
+    "pa_alloc_export_host_state": (_i32, [_vp, _pi32, _pint, _pi64]),
+    "pa_swap_blocks": (_i32, [_vp, _vp, _i32, _vp, _vp, _i32, _vp, _i32, _i32, _vp]),
 }
 
 _lib = None

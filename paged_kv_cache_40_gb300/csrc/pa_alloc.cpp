@@ -13,6 +13,15 @@
 // the ring at most once, so a ring of num_blocks entries never overflows.
 // All state changes are all-or-nothing; a refused request leaves the state
 // as it was.
+//
+// Swapping (Document 04, §9/§10: under memory pressure a scheduler may
+// preempt a sequence by swapping its blocks): an optional host pool with its
+// own FIFO ring. Swap-out takes one host block per logical block, reports
+// the (device, host) pairs to copy and drops the sequence's device
+// references (blocks other tables share stay for them); swap-in takes fresh
+// private device blocks, reports the (host, device) pairs and returns the
+// host blocks. A swapped-out sequence keeps its length but cannot append,
+// fork or be tabled until it is swapped back in.
 #include <algorithm>
 #include <unordered_map>
 #include <vector>
@@ -28,9 +37,26 @@ struct pa_allocator {
   int64_t count = 0;  // elements in the ring
   std::vector<int32_t> ref;
   struct Seq {
-    std::vector<int32_t> table;
+    std::vector<int32_t> table;  // device blocks (empty while swapped out)
+    std::vector<int32_t> host;   // host blocks while swapped out
     int64_t len = 0;
+    bool swapped = false;
   };
+  // host pool: FIFO ring as above
+  int num_host = 0;
+  std::vector<int32_t> hring;
+  int64_t hhead = 0, hcount = 0;
+  int64_t swapped_seqs = 0, swap_outs = 0, swap_ins = 0;
+  int32_t host_take() {
+    int32_t h = hring[hhead];
+    hhead = (hhead + 1) % num_host;
+    --hcount;
+    return h;
+  }
+  void host_push(int32_t h) {
+    hring[(hhead + hcount) % num_host] = h;
+    ++hcount;
+  }
   std::unordered_map<int64_t, Seq> seqs;
   int64_t cow_copies = 0;
   int64_t alloc_failures = 0;
@@ -81,6 +107,9 @@ pa_status append_one(pa_allocator* a, int64_t seq_id, int32_t* slot, int32_t* cs
     return pa::fail(PA_ERR_INVALID_ARG, "append_slot: unknown sequence %lld",
                     (long long)seq_id);
   auto& s = it->second;
+  if (s.swapped)
+    return pa::fail(PA_ERR_INVALID_ARG, "append_slot: sequence %lld is swapped out",
+                    (long long)seq_id);
   const int64_t L = s.len;
   const int BS = a->block_size;
   int32_t src = -1, dst = -1;
@@ -172,8 +201,9 @@ pa_status pa_alloc_add_seq(pa_allocator* a, int64_t seq_id, int64_t len) {
 pa_status pa_alloc_fork(pa_allocator* a, int64_t parent, int64_t child) {
   if (pa_status s = check_handle(a)) return s;
   auto it = a->seqs.find(parent);
-  if (it == a->seqs.end() || a->seqs.count(child))
-    return pa::fail(PA_ERR_INVALID_ARG, "fork: parent %lld missing or child %lld exists",
+  if (it == a->seqs.end() || it->second.swapped || a->seqs.count(child))
+    return pa::fail(PA_ERR_INVALID_ARG,
+                    "fork: parent %lld missing or swapped out, or child %lld exists",
                     (long long)parent, (long long)child);
   pa_allocator::Seq s = it->second;
   for (int32_t b : s.table) a->inc(b);
@@ -217,8 +247,114 @@ pa_status pa_alloc_free_seq(pa_allocator* a, int64_t seq_id) {
   auto it = a->seqs.find(seq_id);
   if (it == a->seqs.end())
     return pa::fail(PA_ERR_INVALID_ARG, "free_seq: unknown sequence %lld", (long long)seq_id);
+  if (it->second.swapped) {
+    for (int32_t h : it->second.host) a->host_push(h);
+    --a->swapped_seqs;
+  }
   for (int32_t b : it->second.table) a->dec(b);
   a->seqs.erase(it);
+  return pa::ok();
+}
+
+pa_status pa_alloc_add_host_pool(pa_allocator* a, int num_host_blocks, const int32_t* order) {
+  if (pa_status s = check_handle(a)) return s;
+  if (a->num_host > 0 || num_host_blocks <= 0)
+    return pa::fail(PA_ERR_INVALID_ARG, "add_host_pool: pool exists or size %d", num_host_blocks);
+  std::vector<int32_t> ring(num_host_blocks);
+  std::vector<char> seen(num_host_blocks, 0);
+  for (int i = 0; i < num_host_blocks; ++i) {
+    const int32_t h = order ? order[i] : i;
+    if (h < 0 || h >= num_host_blocks || seen[h])
+      return pa::fail(PA_ERR_INVALID_ARG,
+                      "add_host_pool: order is not a permutation (entry %d = %d)", i, h);
+    seen[h] = 1;
+    ring[i] = h;
+  }
+  a->num_host = num_host_blocks;
+  a->hring = std::move(ring);
+  a->hhead = 0;
+  a->hcount = num_host_blocks;
+  return pa::ok();
+}
+
+pa_status pa_alloc_swap_out(pa_allocator* a, int64_t seq_id, int32_t* pairs, int cap, int* n) {
+  if (pa_status s = check_handle(a)) return s;
+  if (!n) return pa::fail(PA_ERR_INVALID_ARG, "swap_out: n is NULL");
+  *n = 0;
+  auto it = a->seqs.find(seq_id);
+  if (it == a->seqs.end() || it->second.swapped)
+    return pa::fail(PA_ERR_INVALID_ARG, "swap_out: sequence %lld unknown or swapped out",
+                    (long long)seq_id);
+  auto& sq = it->second;
+  const int nb = static_cast<int>(sq.table.size());
+  if (cap < nb || (nb > 0 && !pairs))
+    return pa::fail(PA_ERR_INVALID_ARG, "swap_out: capacity %d < %d pairs", cap, nb);
+  if (nb > a->hcount) {
+    ++a->alloc_failures;
+    return pa::fail(PA_ERR_OUT_OF_BLOCKS, "swap_out: need %d host blocks, %lld free", nb,
+                    (long long)a->hcount);
+  }
+  sq.host.clear();
+  for (int j = 0; j < nb; ++j) {
+    const int32_t h = a->host_take();
+    sq.host.push_back(h);
+    pairs[2 * j] = sq.table[j];
+    pairs[2 * j + 1] = h;
+  }
+  for (int32_t b : sq.table) a->dec(b);
+  sq.table.clear();
+  sq.swapped = true;
+  ++a->swapped_seqs;
+  ++a->swap_outs;
+  *n = nb;
+  return pa::ok();
+}
+
+pa_status pa_alloc_swap_in(pa_allocator* a, int64_t seq_id, int32_t* pairs, int cap, int* n) {
+  if (pa_status s = check_handle(a)) return s;
+  if (!n) return pa::fail(PA_ERR_INVALID_ARG, "swap_in: n is NULL");
+  *n = 0;
+  auto it = a->seqs.find(seq_id);
+  if (it == a->seqs.end() || !it->second.swapped)
+    return pa::fail(PA_ERR_INVALID_ARG, "swap_in: sequence %lld is not swapped out",
+                    (long long)seq_id);
+  auto& sq = it->second;
+  const int nb = static_cast<int>(sq.host.size());
+  if (cap < nb || (nb > 0 && !pairs))
+    return pa::fail(PA_ERR_INVALID_ARG, "swap_in: capacity %d < %d pairs", cap, nb);
+  if (nb > a->count) {
+    ++a->alloc_failures;
+    return pa::fail(PA_ERR_OUT_OF_BLOCKS, "swap_in: need %d blocks, %lld free", nb,
+                    (long long)a->count);
+  }
+  sq.table.clear();
+  for (int j = 0; j < nb; ++j) {
+    const int32_t b = a->take();
+    sq.table.push_back(b);
+    pairs[2 * j] = sq.host[j];
+    pairs[2 * j + 1] = b;
+  }
+  for (int32_t h : sq.host) a->host_push(h);
+  sq.host.clear();
+  sq.swapped = false;
+  --a->swapped_seqs;
+  ++a->swap_ins;
+  *n = nb;
+  return pa::ok();
+}
+
+pa_status pa_alloc_export_host_state(const pa_allocator* a, int32_t* free_order, int* num_free,
+                                     int64_t* counts) {
+  if (pa_status s = check_handle(a)) return s;
+  if (!num_free || !counts || (a->num_host > 0 && !free_order))
+    return pa::fail(PA_ERR_INVALID_ARG, "export_host_state: NULL output");
+  for (int64_t i = 0; i < a->num_host; ++i)
+    free_order[i] = i < a->hcount ? a->hring[(a->hhead + i) % a->num_host] : -1;
+  *num_free = static_cast<int>(a->hcount);
+  counts[0] = a->num_host;
+  counts[1] = a->swapped_seqs;
+  counts[2] = a->swap_outs;
+  counts[3] = a->swap_ins;
   return pa::ok();
 }
 
@@ -227,8 +363,9 @@ pa_status pa_alloc_get_table(const pa_allocator* a, int64_t seq_id, int32_t* out
   if (pa_status s = check_handle(a)) return s;
   if (!n) return pa::fail(PA_ERR_INVALID_ARG, "get_table: n is NULL");
   auto it = a->seqs.find(seq_id);
-  if (it == a->seqs.end())
-    return pa::fail(PA_ERR_INVALID_ARG, "get_table: unknown sequence %lld", (long long)seq_id);
+  if (it == a->seqs.end() || it->second.swapped)
+    return pa::fail(PA_ERR_INVALID_ARG, "get_table: sequence %lld unknown or swapped out",
+                    (long long)seq_id);
   const auto& t = it->second.table;
   *n = static_cast<int>(t.size());
   if (cap < *n || (*n > 0 && !out))
@@ -254,8 +391,8 @@ pa_status pa_alloc_build_tables(const pa_allocator* a, const int64_t* seq_ids, i
     return pa::fail(PA_ERR_INVALID_ARG, "build_tables: bad arguments");
   for (int i = 0; i < n; ++i) {
     auto it = a->seqs.find(seq_ids[i]);
-    if (it == a->seqs.end())
-      return pa::fail(PA_ERR_INVALID_ARG, "build_tables: unknown sequence %lld",
+    if (it == a->seqs.end() || it->second.swapped)
+      return pa::fail(PA_ERR_INVALID_ARG, "build_tables: sequence %lld unknown or swapped out",
                       (long long)seq_ids[i]);
     const auto& t = it->second.table;
     if (static_cast<int64_t>(t.size()) > max_blocks)

@@ -111,25 +111,28 @@ append_kv_fp8_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ 
   }
 }
 
-// Grid (pairs, slices): each CTA copies a slice of one block in both pools.
+// Grid (pairs, slices): each CTA copies a slice of one block of the source
+// pools into a block of the destination pools (the same pools for
+// copy-on-write; the device pools and a host pool for swapping).
 __global__ void __launch_bounds__(kCopyThreads)
-copy_blocks_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
-                   const int32_t* __restrict__ pairs, int64_t block_vecs, int num_blocks,
-                   int32_t* __restrict__ err) {
+copy_blocks_kernel(const uint4* __restrict__ src_k, const uint4* __restrict__ src_v,
+                   uint4* __restrict__ dst_k, uint4* __restrict__ dst_v,
+                   const int32_t* __restrict__ pairs, int64_t block_vecs, int src_blocks,
+                   int dst_blocks, int32_t* __restrict__ err) {
   const int p = blockIdx.x;
   const int32_t src = __ldg(pairs + 2 * p);
   const int32_t dst = __ldg(pairs + 2 * p + 1);
-  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+  if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
     if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(err, PA_DEVERR_BAD_BLOCK);
     return;
   }
   const int64_t slice = static_cast<int64_t>(kCopyThreads) * kCopyVecsPerThread;
   const int64_t lo = blockIdx.y * slice;
   const int64_t hi = lo + slice < block_vecs ? lo + slice : block_vecs;
-  const uint4* ks = k_pool + src * block_vecs;
-  const uint4* vs = v_pool + src * block_vecs;
-  uint4* kd = k_pool + dst * block_vecs;
-  uint4* vd = v_pool + dst * block_vecs;
+  const uint4* ks = src_k + src * block_vecs;
+  const uint4* vs = src_v + src * block_vecs;
+  uint4* kd = dst_k + dst * block_vecs;
+  uint4* vd = dst_v + dst * block_vecs;
   uint4 kb[kCopyVecsPerThread], vb[kCopyVecsPerThread];
 #pragma unroll
   for (int j = 0; j < kCopyVecsPerThread; ++j) {
@@ -276,8 +279,9 @@ pa_status pa_copy_blocks(pa_half* k_pool, pa_half* v_pool, const int32_t* pairs,
   if (slices > 65535) return pa::fail(PA_ERR_UNSUPPORTED, "pa_copy_blocks: block too large");
   dim3 grid(num_pairs, static_cast<unsigned>(slices));
   copy_blocks_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint4*>(k_pool), reinterpret_cast<const uint4*>(v_pool),
       reinterpret_cast<uint4*>(k_pool), reinterpret_cast<uint4*>(v_pool), pairs, block_vecs,
-      num_blocks, err);
+      num_blocks, num_blocks, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_copy_blocks launch");
   return pa::ok();
@@ -350,10 +354,69 @@ pa_status pa_copy_blocks_fp8(uint8_t* k_pool, uint8_t* v_pool, const int32_t* pa
   if (slices > 65535) return pa::fail(PA_ERR_UNSUPPORTED, "pa_copy_blocks_fp8: block too large");
   dim3 grid(num_pairs, static_cast<unsigned>(slices));
   copy_blocks_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint4*>(k_pool), reinterpret_cast<const uint4*>(v_pool),
       reinterpret_cast<uint4*>(k_pool), reinterpret_cast<uint4*>(v_pool), pairs, block_vecs,
-      num_blocks, err);
+      num_blocks, num_blocks, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_copy_blocks_fp8 launch");
+  return pa::ok();
+}
+
+// A pointer the device can dereference: device memory as it is, pinned host
+// memory through its device mapping; anything else is refused.
+static pa_status device_view(const char* fn, const void* p, void** out) {
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) return pa::cuda_fail(e, fn);
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) {
+    *out = const_cast<void*>(p);
+    return PA_OK;
+  }
+  if (at.type == cudaMemoryTypeHost) {
+    void* d = nullptr;
+    e = cudaHostGetDevicePointer(&d, const_cast<void*>(p), 0);
+    if (e != cudaSuccess) return pa::cuda_fail(e, fn);
+    *out = d;
+    return PA_OK;
+  }
+  return pa::fail(PA_ERR_INVALID_ARG, "%s: host memory must be pinned (page-locked)", fn);
+}
+
+pa_status pa_swap_blocks(const void* src_k, const void* src_v, int src_blocks, void* dst_k,
+                         void* dst_v, int dst_blocks, const int32_t* pairs, int num_pairs,
+                         int block_bytes, pa_stream_t stream) {
+  if (num_pairs < 0 || src_blocks <= 0 || dst_blocks <= 0 || block_bytes <= 0 ||
+      block_bytes % 16)
+    return pa::fail(PA_ERR_INVALID_ARG,
+                    "pa_swap_blocks: pairs=%d src_blocks=%d dst_blocks=%d block_bytes=%d",
+                    num_pairs, src_blocks, dst_blocks, block_bytes);
+  if (num_pairs == 0) return pa::ok();
+  if (!src_k || !src_v || !dst_k || !dst_v || !pairs)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: NULL pointer");
+  if (!pa::aligned16(src_k) || !pa::aligned16(src_v) || !pa::aligned16(dst_k) ||
+      !pa::aligned16(dst_v) || (reinterpret_cast<uintptr_t>(pairs) & 3))
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: misaligned pointer");
+  pa::DeviceInfo dev;
+  if (pa_status s = pa::current_device(&dev)) return s;
+  void *sk, *sv, *dk, *dv, *pp;
+  if (pa_status s = device_view("pa_swap_blocks(src_k)", src_k, &sk)) return s;
+  if (pa_status s = device_view("pa_swap_blocks(src_v)", src_v, &sv)) return s;
+  if (pa_status s = device_view("pa_swap_blocks(dst_k)", dst_k, &dk)) return s;
+  if (pa_status s = device_view("pa_swap_blocks(dst_v)", dst_v, &dv)) return s;
+  if (pa_status s = device_view("pa_swap_blocks(pairs)", pairs, &pp)) return s;
+  int32_t* err = pa::device_error_word();
+  if (!err) return PA_ERR_CUDA;
+  const int64_t block_vecs = block_bytes / 16;
+  const int64_t slice = static_cast<int64_t>(kCopyThreads) * kCopyVecsPerThread;
+  const int64_t slices = (block_vecs + slice - 1) / slice;
+  if (slices > 65535) return pa::fail(PA_ERR_UNSUPPORTED, "pa_swap_blocks: block too large");
+  dim3 grid(num_pairs, static_cast<unsigned>(slices));
+  copy_blocks_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(sk), static_cast<const uint4*>(sv), static_cast<uint4*>(dk),
+      static_cast<uint4*>(dv), static_cast<const int32_t*>(pp), block_vecs, src_blocks,
+      dst_blocks, err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return pa::cuda_fail(e, "pa_swap_blocks launch");
   return pa::ok();
 }
 

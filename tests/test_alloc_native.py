@@ -132,3 +132,85 @@ def test_batched_append_stops_at_failure(libpa):
     with pytest.raises(libpa.OutOfBlocksError):
         nat.append_slots([0, 1])     # seq 0 takes the last block, seq 1 fails
     assert nat.seq_len(0) == 3 and nat.seq_len(1) == 2
+
+
+def test_random_ops_with_swapping(libpa):
+    """Native block manager against the oracle's under random adds, forks,
+    appends, frees, swap-outs and swap-ins: identical results, refusals and
+    state (device and host free lists, reference counts) after every op."""
+    rng = np.random.default_rng(77)
+    nb, bs, nh = 200, 8, 120
+    order = rng.permutation(nb).tolist()
+    horder = rng.permutation(nh).tolist()
+    nat = libpa.BlockAllocator(nb, bs, order)
+    ref = oracle.BlockAllocator(nb, bs, order)
+    nat.add_host_pool(nh, horder)
+    ref.add_host_pool(nh, horder)
+    resident, swapped = [], []
+    next_id = 0
+
+    def both(fn_n, fn_r):
+        try:
+            a = fn_n()
+        except libpa.OutOfBlocksError:
+            a = "oob"
+        try:
+            b = fn_r()
+        except oracle.OutOfBlocks:
+            b = "oob"
+        assert a == b
+        return a
+
+    for step in range(3000):
+        r = rng.random()
+        if r < 0.2 or not (resident or swapped):
+            L = int(rng.integers(0, 60))
+            if both(lambda: nat.add_seq(next_id, L), lambda: ref.add_seq(next_id, L)) != "oob":
+                resident.append(next_id)
+            next_id += 1
+        elif r < 0.28 and resident:
+            p = resident[int(rng.integers(len(resident)))]
+            both(lambda: nat.fork(p, next_id), lambda: ref.fork(p, next_id))
+            resident.append(next_id)
+            next_id += 1
+        elif r < 0.6 and resident:
+            s = resident[int(rng.integers(len(resident)))]
+            both(lambda: nat.append_slot(s), lambda: ref.append_slot(s))
+        elif r < 0.72 and resident:
+            s = resident[int(rng.integers(len(resident)))]
+            got = both(lambda: nat.swap_out(s), lambda: ref.swap_out(s))
+            if got != "oob":
+                resident.remove(s)
+                swapped.append(s)
+        elif r < 0.84 and swapped:
+            s = swapped[int(rng.integers(len(swapped)))]
+            got = both(lambda: nat.swap_in(s), lambda: ref.swap_in(s))
+            if got != "oob":
+                swapped.remove(s)
+                resident.append(s)
+        else:
+            pool = resident + swapped
+            if not pool:
+                continue
+            s = pool[int(rng.integers(len(pool)))]
+            nat.free_seq(s)
+            ref.free_seq(s)
+            (resident if s in resident else swapped).remove(s)
+        assert nat.export_state() == ref.export_state()
+        assert nat.export_host_state() == ref.export_host_state()
+    assert nat.stats() == ref.stats()
+    assert nat.export_host_state()[2] > 20 and nat.export_host_state()[3] > 10
+
+
+def test_swapped_sequence_is_refused(libpa):
+    a = libpa.BlockAllocator(16, 4)
+    a.add_host_pool(8)
+    a.add_seq(1, 6)
+    a.swap_out(1)
+    for call in (lambda: a.append_slot(1), lambda: a.fork(1, 2), lambda: a.table(1),
+                 lambda: a.build_tables([1], 4), lambda: a.swap_out(1)):
+        with pytest.raises(libpa.PaError):
+            call()
+    assert a.seq_len(1) == 6
+    a.swap_in(1)
+    assert len(a.table(1)) == 2
