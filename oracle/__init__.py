@@ -15,6 +15,8 @@ Sources (web pages on PagedAttention):
     the C-style layout sketch, copy-on-write block sharing), §3 Mental Model
     (sharing picture), §11 Engineering Decision Framework and §13 question 4
     (capacity arithmetic).
+  * The one-pool layout of `interleaved.py` (one record per physical block,
+    K then V) is the layout sketch of Document 04 §2 taken literally.
   * The fp8 (E4M3) KV cache of `fp8.py` follows Document 04 §11/§12 (KV
     quantization as a way to fit more sequences); its format readings are in
     that module's docstring.
@@ -45,6 +47,15 @@ from .fp8 import (  # noqa: F401
     append_kv_fp8,
     dequantize_pool,
     decode_attention_fp8,
+)
+from .interleaved import (  # noqa: F401
+    kv_block_dtype,
+    make_kv_pool,
+    split_kv_pool,
+    append_kv_interleaved,
+    copy_blocks_interleaved,
+    decode_attention_interleaved,
+    decode_attention_interleaved_fp8,
 )
 from .allocator import BlockAllocator, OutOfBlocks  # noqa: F401
 from .accounting import (  # noqa: F401
