@@ -388,15 +388,16 @@ def run_ours(args, world, rank, local):
         if args.kv_dtype != "fp16":
             raise SystemExit("the shared-prefix step is measured on an fp16 cache")
         run = SharedPrefixRunner(b, device=dev, partition_tokens=args.partition,
-                                 prefix_aware=not args.plain_decode)
+                                 prefix_aware=not args.plain_decode, layout=args.layout)
     elif args.kv_dtype == "fp8":
         import synthetic
         fp8 = synthetic.fp8_cache(b, seed=100 + 1000 * rank)
         run = DecodeBatchRunner(b, device=dev, partition_tokens=args.partition, kv_dtype="fp8",
                                 k_pool=fp8.k_pool, v_pool=fp8.v_pool, k_scale=fp8.k_scale,
-                                v_scale=fp8.v_scale)
+                                v_scale=fp8.v_scale, layout=args.layout)
     else:
-        run = DecodeBatchRunner(b, device=dev, partition_tokens=args.partition)
+        run = DecodeBatchRunner(b, device=dev, partition_tokens=args.partition,
+                                layout=args.layout)
     plan = run.plan_step()
     # host slot assignment (block manager) cost for this batch, measured on a
     # second allocator holding the same placement
@@ -527,6 +528,9 @@ def run_ours(args, world, rank, local):
         return
     value = all_kv / t_steps / 1e9
     config = describe(b, args.kv_dtype, plan.seq_lens)
+    if args.layout == "records":
+        config["pool_layout"] = ("one pool of per-block records (K rows then V rows), "
+                                 "block stride two blocks")
     if shared:
         config.update({
             "prefix_len": int(b.prefix_len),
@@ -550,7 +554,8 @@ def run_ours(args, world, rank, local):
                          "min": round(1e3 * min(attn_ms), 3)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(b.name + ("_fp8" if fp8 is not None else "")),
+                     "traffic": recorded_traffic(b.name + ("_fp8" if fp8 is not None else "")
+                                                + ("_records" if args.layout == "records" else "")),
                      "peak_source": peak_kind,
                      "kernel": "paged_decode_kernel",
                      "bytes_per_launch": run.io_bytes()},
@@ -581,6 +586,8 @@ def main():
                          "prefix-aware one")
     ap.add_argument("--kv-dtype", choices=["fp16", "fp8"], default="fp16",
                     help="KV cache storage: fp16, or E4M3 bytes with per-head scales")
+    ap.add_argument("--layout", choices=["separate", "records"], default="separate",
+                    help="KV pools: two separate pools, or one pool of per-block K/V records")
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

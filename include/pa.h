@@ -18,11 +18,20 @@
  * Conventions shared by every call
  *   - fp16 tensors are IEEE-754 binary16, passed as `pa_half*` (the raw 16-bit
  *     patterns). Index tensors are int32.
- *   - Pools: k_pool and v_pool are separate device buffers, each laid out
- *     [num_blocks][block_size][num_kv_heads][head_dim], row-major, contiguous.
- *     Pool "slot" s (0 <= s < num_blocks*block_size) is row s of the pool seen
- *     as [num_blocks*block_size][num_kv_heads*head_dim]: physical block
- *     s / block_size, offset s % block_size.
+ *   - Pools: k_pool and v_pool each hold num_blocks physical blocks of
+ *     [block_size][num_kv_heads][head_dim] values, row-major and contiguous
+ *     within a block. Block b of a pool starts pool_block_stride values after
+ *     block b-1 (0 = block_size*num_kv_heads*head_dim: a dense
+ *     [num_blocks][block_size][num_kv_heads][head_dim] array). Pool "slot" s
+ *     (0 <= s < num_blocks*block_size) is row s % block_size of block
+ *     s / block_size.
+ *   - The one-pool layout of the layout sketch ("Phase 7 · Document 04 —
+ *     PagedAttention", §2 Core Concept: an array of per-block records, each a
+ *     K array followed by a V array) is served by the same calls: with E =
+ *     block_size*num_kv_heads*head_dim and kv the record array, pass
+ *     k_pool = kv, v_pool = kv + E and pool_block_stride = 2*E. A stride must
+ *     be at least E values and a multiple of 16 bytes. Calls that write the
+ *     pools refuse a K and a V pool whose blocks overlap.
  *   - Device pointers are owned by the caller (the library never allocates or
  *     frees device memory) and must be 16-byte aligned. Device calls are
  *     asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
@@ -100,14 +109,16 @@ PA_API pa_status pa_device_error(pa_stream_t stream, int32_t* flags);
  *                >= num_blocks*block_size is skipped and sets
  *                PA_DEVERR_BAD_SLOT.
  * The copy is bit-exact. Two tokens mapped to the same slot race (one wins).
- * Errors: PA_ERR_INVALID_ARG (bad sizes, NULL or misaligned pointers),
- *         PA_ERR_UNSUPPORTED (head_dim not a multiple of 8), PA_ERR_CUDA.
+ * Errors: PA_ERR_INVALID_ARG (bad sizes or stride, NULL or misaligned
+ *         pointers, overlapping K and V blocks), PA_ERR_UNSUPPORTED (head_dim
+ *         not a multiple of 8), PA_ERR_CUDA.
  * ---------------------------------------------------------------------- */
 PA_API pa_status pa_append_kv(const pa_half* k_new, const pa_half* v_new,
                        pa_half* k_pool, pa_half* v_pool,
                        const int32_t* slot_mapping, int num_tokens,
                        int num_kv_heads, int head_dim, int block_size,
-                       int num_blocks, pa_stream_t stream);
+                       int num_blocks, int64_t pool_block_stride,
+                       pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * pa_copy_blocks — copy-on-write duplication of whole blocks.
@@ -129,7 +140,8 @@ PA_API pa_status pa_append_kv(const pa_half* k_new, const pa_half* v_new,
 PA_API pa_status pa_copy_blocks(pa_half* k_pool, pa_half* v_pool,
                          const int32_t* pairs, int num_pairs,
                          int num_kv_heads, int head_dim, int block_size,
-                         int num_blocks, pa_stream_t stream);
+                         int num_blocks, int64_t pool_block_stride,
+                         pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * pa_decode_attention — single-query attention over the paged cache.
@@ -152,7 +164,7 @@ PA_API pa_status pa_copy_blocks(pa_half* k_pool, pa_half* v_pool,
  * caller sees one result.
  *
  * q            device [num_seqs][num_q_heads][head_dim] fp16
- * k_pool, v_pool  device pools (read only)
+ * k_pool, v_pool  device pools (read only), pool_block_stride as above
  * block_table  device int32 [num_seqs][max_blocks_per_seq]; only the first
  *              ceil(seq_lens[i]/block_size) entries of row i are read.
  * seq_lens     device int32 [num_seqs], tokens attended (the appended one
@@ -199,7 +211,8 @@ PA_API pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool,
                               const int32_t* seq_lens, int num_seqs,
                               int num_q_heads, int num_kv_heads, int head_dim,
                               int block_size, int max_blocks_per_seq,
-                              int num_blocks, float scale, pa_half* out,
+                              int num_blocks, int64_t pool_block_stride,
+                              float scale, pa_half* out,
                               void* workspace, size_t workspace_bytes,
                               int partition_tokens, pa_stream_t stream);
 
@@ -235,8 +248,8 @@ PA_API pa_status pa_decode_attention_fixed_scratch(
     const pa_half* q, const pa_half* k_pool, const pa_half* v_pool,
     const int32_t* block_table, const int32_t* seq_lens, int num_seqs,
     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-    int max_blocks_per_seq, int num_blocks, float scale, pa_half* out,
-    int partition_tokens, pa_stream_t stream);
+    int max_blocks_per_seq, int num_blocks, int64_t pool_block_stride,
+    float scale, pa_half* out, int partition_tokens, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * pa_decode_attention_shared_prefix — pa_decode_attention for a batch whose
@@ -279,8 +292,9 @@ PA_API pa_status pa_decode_attention_shared_prefix(
     const int32_t* prefix_blocks, int num_prefix_blocks,
     const int32_t* block_table, const int32_t* seq_lens, int num_seqs,
     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-    int max_blocks_per_seq, int num_blocks, float scale, pa_half* out,
-    void* workspace, size_t workspace_bytes, pa_stream_t stream);
+    int max_blocks_per_seq, int num_blocks, int64_t pool_block_stride,
+    float scale, pa_half* out, void* workspace, size_t workspace_bytes,
+    pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * fp8 KV cache — the append, the block copy and decode attention over pools
@@ -294,8 +308,9 @@ PA_API pa_status pa_decode_attention_shared_prefix(
  * scale[kv_head]) with the division in IEEE fp32 and round-to-nearest-even,
  * magnitudes above 448 saturating to 448.
  *
- * Pools: uint8 [num_blocks][block_size][num_kv_heads][head_dim], the same
- * order as the fp16 pools, one byte per value. k_scale, v_scale: device fp32
+ * Pools: blocks of uint8 [block_size][num_kv_heads][head_dim], the same
+ * order as the fp16 pools, one byte per value, pool_block_stride values
+ * (bytes) apart (0 = dense). k_scale, v_scale: device fp32
  * [num_kv_heads], 4-byte aligned, read only. Ownership, streams, device error
  * word and status codes as for the fp16 calls.
  * ---------------------------------------------------------------------- */
@@ -307,13 +322,15 @@ PA_API pa_status pa_append_kv_fp8(const pa_half* k_new, const pa_half* v_new,
                                   const int32_t* slot_mapping,
                                   const float* k_scale, const float* v_scale,
                                   int num_tokens, int num_kv_heads, int head_dim,
-                                  int block_size, int num_blocks, pa_stream_t stream);
+                                  int block_size, int num_blocks,
+                                  int64_t pool_block_stride, pa_stream_t stream);
 
 /* pa_copy_blocks over one-byte elements (head_dim a multiple of 16). */
 PA_API pa_status pa_copy_blocks_fp8(uint8_t* k_pool, uint8_t* v_pool,
                                     const int32_t* pairs, int num_pairs,
                                     int num_kv_heads, int head_dim, int block_size,
-                                    int num_blocks, pa_stream_t stream);
+                                    int num_blocks, int64_t pool_block_stride,
+                                    pa_stream_t stream);
 
 /* pa_decode_attention over E4M3 pools: out[i][h] = sum_t softmax_t(scale *
  * q[i][h] . Kd[t]) Vd[t] with Kd, Vd the dequantized rows (code value times
@@ -330,7 +347,8 @@ PA_API pa_status pa_decode_attention_fp8(const pa_half* q, const uint8_t* k_pool
                                          const int32_t* seq_lens, int num_seqs,
                                          int num_q_heads, int num_kv_heads, int head_dim,
                                          int block_size, int max_blocks_per_seq,
-                                         int num_blocks, float scale, pa_half* out,
+                                         int num_blocks, int64_t pool_block_stride,
+                                         float scale, pa_half* out,
                                          void* workspace, size_t workspace_bytes,
                                          int partition_tokens, pa_stream_t stream);
 
@@ -460,14 +478,20 @@ PA_API pa_status pa_alloc_export_host_state(const pa_allocator* a, int32_t* free
 
 /* Copy whole blocks between two pool pairs: block pairs[i][1] of dst_k/dst_v
  * := block pairs[i][0] of src_k/src_v, each block block_bytes bytes (a
- * multiple of 16; BS * Hkv * D * element size). Each pool, and pairs (int32
+ * multiple of 16; BS * Hkv * D * element size). Block b of a source pool
+ * starts at b * src_block_stride bytes, of a destination pool at b *
+ * dst_block_stride bytes (0 = block_bytes; otherwise at least block_bytes and
+ * a multiple of 16). A one-pool record array moves as K and V members
+ * (v = k + block_bytes, stride 2*block_bytes) or, with src_v == dst_v == NULL,
+ * as whole records of block_bytes each. Each pool, and pairs (int32
  * [num_pairs][2]), may be device memory or pinned (page-locked) host memory,
  * which the kernel reads and writes through its device mapping. An id outside
  * [0, src_blocks) or [0, dst_blocks) skips that pair and sets
  * PA_DEVERR_BAD_BLOCK. Errors: PA_ERR_INVALID_ARG (pageable host memory,
  * NULL or misaligned pointers), PA_ERR_CUDA. */
 PA_API pa_status pa_swap_blocks(const void* src_k, const void* src_v, int src_blocks,
-                                void* dst_k, void* dst_v, int dst_blocks,
+                                int64_t src_block_stride, void* dst_k, void* dst_v,
+                                int dst_blocks, int64_t dst_block_stride,
                                 const int32_t* pairs, int num_pairs, int block_bytes,
                                 pa_stream_t stream);
 

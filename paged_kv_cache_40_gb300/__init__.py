@@ -37,7 +37,7 @@ __all__ = [
     "pa_append_kv_fp8", "pa_copy_blocks_fp8", "pa_decode_attention_fp8",
     "pa_decode_attention_shared_prefix", "pa_decode_shared_prefix_workspace_bytes",
     "pa_swap_blocks",
-    "pa_decode_attention_fixed_scratch",
+    "pa_decode_attention_fixed_scratch", "kv_block_pool", "kv_views",
     "pa_version", "BlockAllocator", "PaError", "OutOfBlocksError", "lib",
     "DEFAULT_PARTITION_TOKENS",
 ]
@@ -82,11 +82,58 @@ def _dev(t, name, dtype, ndim=None):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _block_stride(t, name) -> int:
+    """Values from one block of a pool to the next; each block itself must be
+    a contiguous [block_size][kv_heads][head_dim] array."""
+    nb, bs, hkv, d = (int(x) for x in t.shape)
+    if (bs > 1 and t.stride(1) != hkv * d) or (hkv > 1 and t.stride(2) != d) or \
+            (d > 1 and t.stride(3) != 1):
+        raise ValueError(f"{name}: each block must be a contiguous [block_size][kv_heads][head_dim]")
+    return int(t.stride(0)) if nb > 1 else bs * hkv * d
+
+
 def _pool_dims(k_pool, v_pool):
+    """(num_blocks, block_size, kv_heads, head_dim, block stride in values) of
+    a K/V pool pair: two dense pools, or the two member views of one record
+    pool (kv_block_pool)."""
     if k_pool.dim() != 4 or tuple(k_pool.shape) != tuple(v_pool.shape):
         raise ValueError("k_pool and v_pool must both be [num_blocks][block_size][kv_heads][head_dim]")
     nb, bs, hkv, d = (int(x) for x in k_pool.shape)
-    return nb, bs, hkv, d
+    stride = _block_stride(k_pool, "k_pool")
+    if _block_stride(v_pool, "v_pool") != stride:
+        raise ValueError("k_pool and v_pool must have the same block stride")
+    return nb, bs, hkv, d, stride
+
+
+def _pool(t, name, dtype):
+    """Device pointer of a pool (blocks may be strided; see _block_stride)."""
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (libpa has no host path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def kv_block_pool(num_blocks, block_size, num_kv_heads, head_dim, dtype=None, device=None):
+    """One pool of per-block records, each a block's K rows followed by its V
+    rows (the layout sketch of "Phase 7 · Document 04 — PagedAttention", §2):
+    a zero-filled tensor [num_blocks][2][block_size][num_kv_heads][head_dim]
+    (fp16 by default; torch.uint8 for an E4M3 cache). kv_views() gives the K
+    and V pools every call takes."""
+    torch = _torch()
+    return torch.zeros((num_blocks, 2, block_size, num_kv_heads, head_dim),
+                       dtype=dtype or torch.float16, device=device or "cuda")
+
+
+def kv_views(kv_pool):
+    """(k_pool, v_pool) views [NB][BS][Hkv][D] of a record pool (kv_block_pool);
+    consecutive blocks of each are two blocks apart."""
+    if kv_pool.dim() != 5 or int(kv_pool.shape[1]) != 2:
+        raise ValueError("kv_pool must be [num_blocks][2][block_size][kv_heads][head_dim]")
+    return kv_pool[:, 0], kv_pool[:, 1]
 
 
 # ------------------------------------------------------------ device calls --
@@ -94,27 +141,27 @@ def pa_append_kv(k_new, v_new, k_pool, v_pool, slot_mapping, stream=None) -> Non
     """Write row i of k_new/v_new ([T][Hkv][D] fp16) into pool slot
     slot_mapping[i] (int32; negative = skip)."""
     torch = _torch()
-    nb, bs, hkv, d = _pool_dims(k_pool, v_pool)
+    nb, bs, hkv, d, stride = _pool_dims(k_pool, v_pool)
     T = int(slot_mapping.numel())
     if tuple(k_new.shape) != (T, hkv, d) or tuple(v_new.shape) != (T, hkv, d):
         raise ValueError("k_new/v_new must be [num_tokens][kv_heads][head_dim]")
     args = (_dev(k_new, "k_new", torch.float16), _dev(v_new, "v_new", torch.float16),
-            _dev(k_pool, "k_pool", torch.float16), _dev(v_pool, "v_pool", torch.float16),
+            _pool(k_pool, "k_pool", torch.float16), _pool(v_pool, "v_pool", torch.float16),
             _dev(slot_mapping, "slot_mapping", torch.int32))
-    _check(_load().pa_append_kv(*args, T, hkv, d, bs, nb, _stream_ptr(stream)))
+    _check(_load().pa_append_kv(*args, T, hkv, d, bs, nb, stride, _stream_ptr(stream)))
 
 
 def pa_copy_blocks(k_pool, v_pool, pairs, stream=None) -> None:
     """Copy block src to block dst in both pools for each (src, dst) row of
     pairs (int32 [n][2])."""
     torch = _torch()
-    nb, bs, hkv, d = _pool_dims(k_pool, v_pool)
+    nb, bs, hkv, d, stride = _pool_dims(k_pool, v_pool)
     if pairs.dim() != 2 or pairs.shape[1] != 2:
         raise ValueError("pairs must be [n][2]")
     n = int(pairs.shape[0])
-    args = (_dev(k_pool, "k_pool", torch.float16), _dev(v_pool, "v_pool", torch.float16),
+    args = (_pool(k_pool, "k_pool", torch.float16), _pool(v_pool, "v_pool", torch.float16),
             _dev(pairs, "pairs", torch.int32))
-    _check(_load().pa_copy_blocks(*args, n, hkv, d, bs, nb, _stream_ptr(stream)))
+    _check(_load().pa_copy_blocks(*args, n, hkv, d, bs, nb, stride, _stream_ptr(stream)))
 
 
 def pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
@@ -148,7 +195,7 @@ def pa_decode_attention(q, k_pool, v_pool, block_table, seq_lens, scale, out=Non
     """Paged decode attention. q [S][Hq][D] fp16; pools [NB][BS][Hkv][D] fp16;
     block_table int32 [S][MB]; seq_lens int32 [S]. Returns out [S][Hq][D] fp16."""
     torch = _torch()
-    nb, bs, hkv, d = _pool_dims(k_pool, v_pool)
+    nb, bs, hkv, d, stride = _pool_dims(k_pool, v_pool)
     if q.dim() != 3 or int(q.shape[2]) != d:
         raise ValueError("q must be [num_seqs][num_q_heads][head_dim]")
     S, hq = int(q.shape[0]), int(q.shape[1])
@@ -163,11 +210,11 @@ def pa_decode_attention(q, k_pool, v_pool, block_table, seq_lens, scale, out=Non
         raise ValueError("out must have q's shape")
     if workspace is None:
         workspace = alloc_workspace(S, hq, hkv, d, bs, mb, partition_tokens, q.device)
-    args = (_dev(q, "q", torch.float16), _dev(k_pool, "k_pool", torch.float16),
-            _dev(v_pool, "v_pool", torch.float16), _dev(block_table, "block_table", torch.int32),
+    args = (_dev(q, "q", torch.float16), _pool(k_pool, "k_pool", torch.float16),
+            _pool(v_pool, "v_pool", torch.float16), _dev(block_table, "block_table", torch.int32),
             _dev(seq_lens, "seq_lens", torch.int32))
     _check(_load().pa_decode_attention(
-        *args, S, hq, hkv, d, bs, mb, nb, ctypes.c_float(float(scale)),
+        *args, S, hq, hkv, d, bs, mb, nb, stride, ctypes.c_float(float(scale)),
         _dev(out, "out", torch.float16), _dev(workspace, "workspace", torch.uint8),
         workspace.numel(), partition_tokens, _stream_ptr(stream)))
     return out
@@ -176,25 +223,52 @@ def pa_decode_attention(q, k_pool, v_pool, block_table, seq_lens, scale, out=Non
 # ------------------------------------------------------------------ swapping --
 def pa_swap_blocks(src_k, src_v, dst_k, dst_v, pairs, stream=None) -> None:
     """Block pairs[i][1] of dst := block pairs[i][0] of src, for K and V. Pools
-    are [blocks][BS][Hkv][D] of one element type, each a CUDA tensor or a
-    pinned CPU tensor; pairs is int32 [n][2], CUDA or pinned CPU."""
+    are [blocks][BS][Hkv][D] of one element type (dense, or the member views
+    of a record pool), each a CUDA tensor or pinned CPU memory; pairs is int32
+    [n][2], CUDA or pinned CPU. With src_v and dst_v None, src_k and dst_k are
+    record pools (kv_block_pool layout) and whole records move."""
     torch = _torch()
-    for t, name in ((src_k, "src_k"), (src_v, "src_v"), (dst_k, "dst_k"), (dst_v, "dst_v"),
-                    (pairs, "pairs")):
-        if not isinstance(t, torch.Tensor) or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous tensor")
+    records = src_v is None and dst_v is None
+    if (src_v is None) != (dst_v is None):
+        raise ValueError("src_v and dst_v must both be tensors or both None")
+    named = [(src_k, "src_k"), (dst_k, "dst_k"), (pairs, "pairs")]
+    if not records:
+        named += [(src_v, "src_v"), (dst_v, "dst_v")]
+    for t, name in named:
+        if not isinstance(t, torch.Tensor):
+            raise ValueError(f"{name} must be a tensor")
         if not t.is_cuda and not t.is_pinned():
             raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
-    if src_k.shape[1:] != dst_k.shape[1:] or src_k.dtype != dst_k.dtype or \
-            src_k.shape != src_v.shape or dst_k.shape != dst_v.shape:
+    if src_k.shape[1:] != dst_k.shape[1:] or src_k.dtype != dst_k.dtype:
         raise ValueError("source and destination pools must share their block shape and type")
-    if pairs.dtype != torch.int32 or pairs.dim() != 2 or pairs.shape[1] != 2:
-        raise ValueError("pairs must be int32 [n][2]")
-    block_bytes = int(src_k[0].numel() * src_k.element_size())
+    if pairs.dtype != torch.int32 or pairs.dim() != 2 or pairs.shape[1] != 2 or \
+            not pairs.is_contiguous():
+        raise ValueError("pairs must be contiguous int32 [n][2]")
+    esz = src_k.element_size()
+    if records:
+        if src_k.dim() != 5 or int(src_k.shape[1]) != 2:
+            raise ValueError("record pools must be [blocks][2][block_size][kv_heads][head_dim]")
+        for t, name in ((src_k, "src_k"), (dst_k, "dst_k")):
+            if not t[0].is_contiguous():
+                raise ValueError(f"{name}: each record must be contiguous")
+        s_stride = int(src_k.stride(0)) if src_k.shape[0] > 1 else int(src_k[0].numel())
+        d_stride = int(dst_k.stride(0)) if dst_k.shape[0] > 1 else int(dst_k[0].numel())
+        sv = dv = ctypes.c_void_p(0)
+    else:
+        if src_k.dim() != 4 or src_k.shape != src_v.shape or dst_k.shape != dst_v.shape or \
+                src_v.dtype != src_k.dtype or dst_v.dtype != dst_k.dtype:
+            raise ValueError("source and destination pools must share their block shape and type")
+        s_stride = _block_stride(src_k, "src_k")
+        d_stride = _block_stride(dst_k, "dst_k")
+        if _block_stride(src_v, "src_v") != s_stride or _block_stride(dst_v, "dst_v") != d_stride:
+            raise ValueError("the K and V pools of one side must have the same block stride")
+        sv, dv = ctypes.c_void_p(src_v.data_ptr()), ctypes.c_void_p(dst_v.data_ptr())
+    block_bytes = int(src_k[0].numel() * esz)
     ptr = lambda t: ctypes.c_void_p(t.data_ptr())
-    _check(_load().pa_swap_blocks(ptr(src_k), ptr(src_v), int(src_k.shape[0]), ptr(dst_k),
-                                  ptr(dst_v), int(dst_k.shape[0]), ptr(pairs),
-                                  int(pairs.shape[0]), block_bytes, _stream_ptr(stream)))
+    _check(_load().pa_swap_blocks(ptr(src_k), sv, int(src_k.shape[0]), s_stride * esz,
+                                  ptr(dst_k), dv, int(dst_k.shape[0]), d_stride * esz,
+                                  ptr(pairs), int(pairs.shape[0]), block_bytes,
+                                  _stream_ptr(stream)))
 
 
 # ------------------------------------------------------------ shared prefix --
@@ -216,7 +290,7 @@ def pa_decode_attention_shared_prefix(q, k_pool, v_pool, prefix_blocks, block_ta
     seq_lens[i] >= P * block_size. The prefix blocks are read once for the
     whole batch. Returns out [S][Hq][D] fp16."""
     torch = _torch()
-    nb, bs, hkv, d = _pool_dims(k_pool, v_pool)
+    nb, bs, hkv, d, stride = _pool_dims(k_pool, v_pool)
     if q.dim() != 3 or int(q.shape[2]) != d:
         raise ValueError("q must be [num_seqs][num_q_heads][head_dim]")
     S, hq = int(q.shape[0]), int(q.shape[1])
@@ -233,13 +307,13 @@ def pa_decode_attention_shared_prefix(q, k_pool, v_pool, prefix_blocks, block_ta
     if workspace is None:
         n = pa_decode_shared_prefix_workspace_bytes(S, hq, hkv, d, bs, mb, P)
         workspace = torch.zeros(max(n, 16), dtype=torch.uint8, device=q.device)
-    args = (_dev(q, "q", torch.float16), _dev(k_pool, "k_pool", torch.float16),
-            _dev(v_pool, "v_pool", torch.float16),
+    args = (_dev(q, "q", torch.float16), _pool(k_pool, "k_pool", torch.float16),
+            _pool(v_pool, "v_pool", torch.float16),
             _dev(prefix_blocks, "prefix_blocks", torch.int32) if P else ctypes.c_void_p(0), P,
             _dev(block_table, "block_table", torch.int32),
             _dev(seq_lens, "seq_lens", torch.int32))
     _check(_load().pa_decode_attention_shared_prefix(
-        *args, S, hq, hkv, d, bs, mb, nb, ctypes.c_float(float(scale)),
+        *args, S, hq, hkv, d, bs, mb, nb, stride, ctypes.c_float(float(scale)),
         _dev(out, "out", torch.float16), _dev(workspace, "workspace", torch.uint8),
         workspace.numel(), _stream_ptr(stream)))
     return out
@@ -259,27 +333,27 @@ def pa_append_kv_fp8(k_new, v_new, k_pool, v_pool, slot_mapping, k_scale, v_scal
     k_new/v_new (fp16 [T][Hkv][D]) is quantized with the per-KV-head scales
     and written at slot slot_mapping[i]."""
     torch = _torch()
-    nb, bs, hkv, d = _pool_dims(k_pool, v_pool)
+    nb, bs, hkv, d, stride = _pool_dims(k_pool, v_pool)
     T = int(slot_mapping.numel())
     if tuple(k_new.shape) != (T, hkv, d) or tuple(v_new.shape) != (T, hkv, d):
         raise ValueError("k_new/v_new must be [num_tokens][kv_heads][head_dim]")
     ks, vs = _scales(k_scale, v_scale, hkv)
     args = (_dev(k_new, "k_new", torch.float16), _dev(v_new, "v_new", torch.float16),
-            _dev(k_pool, "k_pool", torch.uint8), _dev(v_pool, "v_pool", torch.uint8),
+            _pool(k_pool, "k_pool", torch.uint8), _pool(v_pool, "v_pool", torch.uint8),
             _dev(slot_mapping, "slot_mapping", torch.int32), ks, vs)
-    _check(_load().pa_append_kv_fp8(*args, T, hkv, d, bs, nb, _stream_ptr(stream)))
+    _check(_load().pa_append_kv_fp8(*args, T, hkv, d, bs, nb, stride, _stream_ptr(stream)))
 
 
 def pa_copy_blocks_fp8(k_pool, v_pool, pairs, stream=None) -> None:
     """pa_copy_blocks over E4M3 pools (uint8 [NB][BS][Hkv][D])."""
     torch = _torch()
-    nb, bs, hkv, d = _pool_dims(k_pool, v_pool)
+    nb, bs, hkv, d, stride = _pool_dims(k_pool, v_pool)
     if pairs.dim() != 2 or pairs.shape[1] != 2:
         raise ValueError("pairs must be [n][2]")
     n = int(pairs.shape[0])
-    args = (_dev(k_pool, "k_pool", torch.uint8), _dev(v_pool, "v_pool", torch.uint8),
+    args = (_pool(k_pool, "k_pool", torch.uint8), _pool(v_pool, "v_pool", torch.uint8),
             _dev(pairs, "pairs", torch.int32))
-    _check(_load().pa_copy_blocks_fp8(*args, n, hkv, d, bs, nb, _stream_ptr(stream)))
+    _check(_load().pa_copy_blocks_fp8(*args, n, hkv, d, bs, nb, stride, _stream_ptr(stream)))
 
 
 def pa_decode_attention_fp8(q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, scale,
@@ -287,7 +361,7 @@ def pa_decode_attention_fp8(q, k_pool, v_pool, k_scale, v_scale, block_table, se
     """pa_decode_attention over E4M3 pools (uint8 [NB][BS][Hkv][D]) with fp32
     per-KV-head scales k_scale, v_scale [Hkv]. Returns out [S][Hq][D] fp16."""
     torch = _torch()
-    nb, bs, hkv, d = _pool_dims(k_pool, v_pool)
+    nb, bs, hkv, d, stride = _pool_dims(k_pool, v_pool)
     if q.dim() != 3 or int(q.shape[2]) != d:
         raise ValueError("q must be [num_seqs][num_q_heads][head_dim]")
     S, hq = int(q.shape[0]), int(q.shape[1])
@@ -303,12 +377,12 @@ def pa_decode_attention_fp8(q, k_pool, v_pool, k_scale, v_scale, block_table, se
     if workspace is None:
         workspace = alloc_workspace(S, hq, hkv, d, bs, mb, partition_tokens, q.device)
     ks, vs = _scales(k_scale, v_scale, hkv)
-    args = (_dev(q, "q", torch.float16), _dev(k_pool, "k_pool", torch.uint8),
-            _dev(v_pool, "v_pool", torch.uint8), ks, vs,
+    args = (_dev(q, "q", torch.float16), _pool(k_pool, "k_pool", torch.uint8),
+            _pool(v_pool, "v_pool", torch.uint8), ks, vs,
             _dev(block_table, "block_table", torch.int32),
             _dev(seq_lens, "seq_lens", torch.int32))
     _check(_load().pa_decode_attention_fp8(
-        *args, S, hq, hkv, d, bs, mb, nb, ctypes.c_float(float(scale)),
+        *args, S, hq, hkv, d, bs, mb, nb, stride, ctypes.c_float(float(scale)),
         _dev(out, "out", torch.float16), _dev(workspace, "workspace", torch.uint8),
         workspace.numel(), partition_tokens, _stream_ptr(stream)))
     return out
@@ -326,7 +400,7 @@ def pa_decode_attention_fixed_scratch(q, k_pool, v_pool, block_table, seq_lens, 
     overlap on the GPU share that array and must not be issued.
     """
     torch = _torch()
-    nb, bs, hkv, d = _pool_dims(k_pool, v_pool)
+    nb, bs, hkv, d, stride = _pool_dims(k_pool, v_pool)
     if q.dim() != 3 or int(q.shape[2]) != d:
         raise ValueError("q must be [num_seqs][num_q_heads][head_dim]")
     S, hq = int(q.shape[0]), int(q.shape[1])
@@ -338,11 +412,12 @@ def pa_decode_attention_fixed_scratch(q, k_pool, v_pool, block_table, seq_lens, 
         out = torch.empty_like(q)
     elif tuple(out.shape) != tuple(q.shape):
         raise ValueError("out must have q's shape")
-    args = (_dev(q, "q", torch.float16), _dev(k_pool, "k_pool", torch.float16),
-            _dev(v_pool, "v_pool", torch.float16), _dev(block_table, "block_table", torch.int32),
+    args = (_dev(q, "q", torch.float16), _pool(k_pool, "k_pool", torch.float16),
+            _pool(v_pool, "v_pool", torch.float16), _dev(block_table, "block_table", torch.int32),
             _dev(seq_lens, "seq_lens", torch.int32))
     _check(_load().pa_decode_attention_fixed_scratch(
-        *args, S, hq, hkv, d, bs, int(block_table.shape[1]), nb, ctypes.c_float(float(scale)),
+        *args, S, hq, hkv, d, bs, int(block_table.shape[1]), nb, stride,
+        ctypes.c_float(float(scale)),
         _dev(out, "out", torch.float16), partition_tokens, _stream_ptr(stream)))
     return out
 

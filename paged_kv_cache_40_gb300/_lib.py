@@ -58,23 +58,23 @@ SIGNATURES = {
     "pa_status_string": (ctypes.c_char_p, [_i32]),
     "pa_version": (_i32, []),
     "pa_device_error": (_i32, [_vp, _pi32]),
-    "pa_append_kv": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp]),
-    "pa_copy_blocks": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp]),
+    "pa_append_kv": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _vp]),
+    "pa_copy_blocks": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _vp]),
     "pa_decode_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32]),
     "pa_decode_workspace_init": (_i32, [_vp, _sz, _i32, _i32, _vp]),
     "pa_decode_attention": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
-                                   _i32, _i32, _f32, _vp, _vp, _sz, _i32, _vp]),
+                                   _i32, _i32, _i64, _f32, _vp, _vp, _sz, _i32, _vp]),
     "pa_decode_attention_fixed_scratch": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
-                                                 _i32, _i32, _i32, _f32, _vp, _i32, _vp]),
+                                                 _i32, _i32, _i32, _i64, _f32, _vp, _i32, _vp]),
     "pa_append_kv_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
-                                _vp]),
-    "pa_copy_blocks_fp8": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp]),
+                                _i64, _vp]),
+    "pa_copy_blocks_fp8": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _vp]),
     "pa_decode_attention_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
-                                       _i32, _i32, _i32, _f32, _vp, _vp, _sz, _i32, _vp]),
+                                       _i32, _i32, _i32, _i64, _f32, _vp, _vp, _sz, _i32, _vp]),
     "pa_decode_shared_prefix_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32]),
     "pa_decode_attention_shared_prefix": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32,
-                                                 _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp,
-                                                 _sz, _vp]),
+                                                 _i32, _i32, _i32, _i32, _i32, _i64, _f32, _vp,
+                                                 _vp, _sz, _vp]),
     "pa_alloc_create": (_i32, [_i32, _i32, _pi32, ctypes.POINTER(_vp)]),
     "pa_alloc_destroy": (None, [_vp]),
     "pa_alloc_add_seq": (_i32, [_vp, _i64, _i64]),
@@ -91,7 +91,7 @@ SIGNATURES = {
     "pa_alloc_swap_out": (_i32, [_vp, _i64, _pi32, _i32, _pint]),
     "pa_alloc_swap_in": (_i32, [_vp, _i64, _pi32, _i32, _pint]),
     "pa_alloc_export_host_state": (_i32, [_vp, _pi32, _pint, _pi64]),
-    "pa_swap_blocks": (_i32, [_vp, _vp, _i32, _vp, _vp, _i32, _vp, _i32, _i32, _vp]),
+    "pa_swap_blocks": (_i32, [_vp, _vp, _i32, _i64, _vp, _vp, _i32, _i64, _vp, _i32, _i32, _vp]),
 }
 
 _lib = None

@@ -1,7 +1,10 @@
 // KV-cache writes: per-token append through a slot mapping, and whole-block
 // copy-on-write duplication. Both are pure bit copies streamed with 16-byte
-// vector loads/stores; the pool is viewed as rows of num_kv_heads*head_dim
-// halves, so a slot is a row index and a block is block_size consecutive rows.
+// vector loads/stores; a block is block_size consecutive rows of
+// num_kv_heads*head_dim values, and consecutive blocks of a pool sit a block
+// stride apart (the dense stride for two separate pools, twice a block for
+// the one-pool record layout of the layout sketch, where each record holds a
+// block's K rows and then its V rows: Document 04, §2 Core Concept).
 //
 // Append: the cache grows by one token per decode step ("Phase 7 · Document
 // 04 — PagedAttention", §2 primer); the block manager picks the slot (§2 Core
@@ -36,8 +39,8 @@ constexpr int kCopyVecsPerThread = 4;
 __global__ void __launch_bounds__(kAppendThreads)
 append_kv_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
                  uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
-                 const int32_t* __restrict__ slots, int row_vecs, int64_t num_slots,
-                 int32_t* __restrict__ err) {
+                 const int32_t* __restrict__ slots, int row_vecs, int block_size,
+                 int64_t block_vecs, int64_t num_slots, int32_t* __restrict__ err) {
   // A decode launched right after this kernel may start its prologue now; it
   // waits for this grid to finish before it reads the pool.
   asm volatile("griddepcontrol.launch_dependents;");
@@ -50,8 +53,10 @@ append_kv_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_ne
   }
   const uint4* ks = k_new + static_cast<int64_t>(t) * row_vecs;
   const uint4* vs = v_new + static_cast<int64_t>(t) * row_vecs;
-  uint4* kd = k_pool + static_cast<int64_t>(slot) * row_vecs;
-  uint4* vd = v_pool + static_cast<int64_t>(slot) * row_vecs;
+  const int64_t row = (slot / block_size) * block_vecs +
+                      static_cast<int64_t>(slot % block_size) * row_vecs;
+  uint4* kd = k_pool + row;
+  uint4* vd = v_pool + row;
   for (int i = threadIdx.x; i < row_vecs; i += kAppendThreads) {
     const uint4 a = __ldg(ks + i);
     const uint4 b = __ldg(vs + i);
@@ -76,7 +81,8 @@ append_kv_fp8_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ 
                      uint2* __restrict__ k_pool, uint2* __restrict__ v_pool,
                      const int32_t* __restrict__ slots, const float* __restrict__ k_scale,
                      const float* __restrict__ v_scale, int row_vecs, int head_vecs,
-                     int64_t num_slots, int32_t* __restrict__ err) {
+                     int block_size, int64_t block_vecs, int64_t num_slots,
+                     int32_t* __restrict__ err) {
   asm volatile("griddepcontrol.launch_dependents;");
   const int t = blockIdx.x;
   const int32_t slot = __ldg(slots + t);
@@ -87,8 +93,10 @@ append_kv_fp8_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ 
   }
   const uint4* ks = k_new + static_cast<int64_t>(t) * row_vecs;
   const uint4* vs = v_new + static_cast<int64_t>(t) * row_vecs;
-  uint2* kd = k_pool + static_cast<int64_t>(slot) * row_vecs;
-  uint2* vd = v_pool + static_cast<int64_t>(slot) * row_vecs;
+  const int64_t row = (slot / block_size) * block_vecs +
+                      static_cast<int64_t>(slot % block_size) * row_vecs;
+  uint2* kd = k_pool + row;
+  uint2* vd = v_pool + row;
   for (int i = threadIdx.x; i < row_vecs; i += kAppendThreads) {
     const int h = i / head_vecs;
     const float sk = __ldg(k_scale + h), sv = __ldg(v_scale + h);
@@ -113,12 +121,15 @@ append_kv_fp8_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ 
 
 // Grid (pairs, slices): each CTA copies a slice of one block of the source
 // pools into a block of the destination pools (the same pools for
-// copy-on-write; the device pools and a host pool for swapping).
+// copy-on-write; the device pools and a host pool for swapping). Blocks are
+// block_vecs long and sit src_stride / dst_stride vectors apart; with no V
+// pools (src_v == dst_v == nullptr) only the K side is copied.
 __global__ void __launch_bounds__(kCopyThreads)
 copy_blocks_kernel(const uint4* __restrict__ src_k, const uint4* __restrict__ src_v,
                    uint4* __restrict__ dst_k, uint4* __restrict__ dst_v,
-                   const int32_t* __restrict__ pairs, int64_t block_vecs, int src_blocks,
-                   int dst_blocks, int32_t* __restrict__ err) {
+                   const int32_t* __restrict__ pairs, int64_t block_vecs, int64_t src_stride,
+                   int64_t dst_stride, int src_blocks, int dst_blocks,
+                   int32_t* __restrict__ err) {
   const int p = blockIdx.x;
   const int32_t src = __ldg(pairs + 2 * p);
   const int32_t dst = __ldg(pairs + 2 * p + 1);
@@ -129,17 +140,18 @@ copy_blocks_kernel(const uint4* __restrict__ src_k, const uint4* __restrict__ sr
   const int64_t slice = static_cast<int64_t>(kCopyThreads) * kCopyVecsPerThread;
   const int64_t lo = blockIdx.y * slice;
   const int64_t hi = lo + slice < block_vecs ? lo + slice : block_vecs;
-  const uint4* ks = src_k + src * block_vecs;
-  const uint4* vs = src_v + src * block_vecs;
-  uint4* kd = dst_k + dst * block_vecs;
-  uint4* vd = dst_v + dst * block_vecs;
+  const bool two = src_v != nullptr;
+  const uint4* ks = src_k + src * src_stride;
+  const uint4* vs = two ? src_v + src * src_stride : nullptr;
+  uint4* kd = dst_k + dst * dst_stride;
+  uint4* vd = two ? dst_v + dst * dst_stride : nullptr;
   uint4 kb[kCopyVecsPerThread], vb[kCopyVecsPerThread];
 #pragma unroll
   for (int j = 0; j < kCopyVecsPerThread; ++j) {
     const int64_t i = lo + threadIdx.x + j * kCopyThreads;
     if (i < hi) {
       kb[j] = ks[i];
-      vb[j] = vs[i];
+      if (two) vb[j] = vs[i];
     }
   }
 #pragma unroll
@@ -147,7 +159,7 @@ copy_blocks_kernel(const uint4* __restrict__ src_k, const uint4* __restrict__ sr
     const int64_t i = lo + threadIdx.x + j * kCopyThreads;
     if (i < hi) {
       kd[i] = kb[j];
-      vd[i] = vb[j];
+      if (two) vd[i] = vb[j];
     }
   }
 }
@@ -164,9 +176,49 @@ pa_status check_pool_shape(const char* fn, int num_kv_heads, int head_dim, int b
   return PA_OK;
 }
 
+// Block stride (values) of the K and V pools a writing call gets, checked:
+// a valid stride and K blocks that do not overlap V blocks.
+pa_status writer_stride(const char* fn, const void* k_pool, const void* v_pool, int num_kv_heads,
+                        int head_dim, int block_size, int num_blocks, int64_t stride, int esz,
+                        int64_t* out) {
+  const int64_t dense = static_cast<int64_t>(block_size) * num_kv_heads * head_dim;
+  if (pa_status s = pa::resolve_block_stride(fn, stride, dense, esz, out)) return s;
+  return pa::check_pools_disjoint(fn, k_pool, v_pool, num_blocks, *out * esz, dense * esz);
+}
+
 }  // namespace
 
 namespace pa {
+
+pa_status resolve_block_stride(const char* fn, int64_t stride, int64_t dense, int esz,
+                               int64_t* out) {
+  if (stride == 0) {
+    *out = dense;
+    return PA_OK;
+  }
+  if (stride < dense || (stride * esz) % 16 != 0 || stride > (int64_t{1} << 40) / esz)
+    return fail(PA_ERR_INVALID_ARG,
+                "%s: pool_block_stride %lld values (a block holds %lld; the stride must be at "
+                "least that and a multiple of 16 bytes)",
+                fn, static_cast<long long>(stride), static_cast<long long>(dense));
+  *out = stride;
+  return PA_OK;
+}
+
+pa_status check_pools_disjoint(const char* fn, const void* k, const void* v, int num_blocks,
+                               int64_t stride_bytes, int64_t block_bytes) {
+  const int64_t span = (static_cast<int64_t>(num_blocks) - 1) * stride_bytes + block_bytes;
+  const int64_t kb = static_cast<int64_t>(reinterpret_cast<uintptr_t>(k));
+  const int64_t vb = static_cast<int64_t>(reinterpret_cast<uintptr_t>(v));
+  const int64_t delta = vb - kb;
+  if (delta >= span || -delta >= span) return PA_OK;  // the pools' extents do not meet
+  // Interleaved extents: every V block must fall in a gap between K blocks.
+  const int64_t r = ((delta % stride_bytes) + stride_bytes) % stride_bytes;
+  if (r >= block_bytes && r <= stride_bytes - block_bytes) return PA_OK;
+  return fail(PA_ERR_INVALID_ARG, "%s: K and V pool blocks overlap (v - k = %lld bytes, block "
+              "%lld bytes, stride %lld bytes)", fn, static_cast<long long>(delta),
+              static_cast<long long>(block_bytes), static_cast<long long>(stride_bytes));
+}
 
 int32_t* device_error_word() {
   static std::mutex mu;
@@ -217,7 +269,7 @@ pa_status pa_device_error(pa_stream_t stream, int32_t* flags) {
 pa_status pa_append_kv(const pa_half* k_new, const pa_half* v_new, pa_half* k_pool,
                        pa_half* v_pool, const int32_t* slot_mapping, int num_tokens,
                        int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                       pa_stream_t stream) {
+                       int64_t pool_block_stride, pa_stream_t stream) {
   if (pa_status s = check_pool_shape("pa_append_kv", num_kv_heads, head_dim, block_size,
                                      num_blocks))
     return s;
@@ -228,6 +280,10 @@ pa_status pa_append_kv(const pa_half* k_new, const pa_half* v_new, pa_half* k_po
   if (!pa::aligned16(k_new) || !pa::aligned16(v_new) || !pa::aligned16(k_pool) ||
       !pa::aligned16(v_pool) || (reinterpret_cast<uintptr_t>(slot_mapping) & 3))
     return pa::fail(PA_ERR_INVALID_ARG, "pa_append_kv: misaligned pointer");
+  int64_t stride = 0;
+  if (pa_status s = writer_stride("pa_append_kv", k_pool, v_pool, num_kv_heads, head_dim,
+                                  block_size, num_blocks, pool_block_stride, 2, &stride))
+    return s;
   pa::DeviceInfo dev;
   if (pa_status s = pa::current_device(&dev)) return s;
   int32_t* err = pa::device_error_word();
@@ -250,7 +306,7 @@ pa_status pa_append_kv(const pa_half* k_new, const pa_half* v_new, pa_half* k_po
   append_kv_kernel<<<num_tokens, kAppendThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       reinterpret_cast<const uint4*>(k_new), reinterpret_cast<const uint4*>(v_new),
       reinterpret_cast<uint4*>(k_pool), reinterpret_cast<uint4*>(v_pool), slot_mapping,
-      row_vecs, static_cast<int64_t>(num_blocks) * block_size, err);
+      row_vecs, block_size, stride / 8, static_cast<int64_t>(num_blocks) * block_size, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_append_kv launch");
   return pa::ok();
@@ -258,7 +314,7 @@ pa_status pa_append_kv(const pa_half* k_new, const pa_half* v_new, pa_half* k_po
 
 pa_status pa_copy_blocks(pa_half* k_pool, pa_half* v_pool, const int32_t* pairs,
                          int num_pairs, int num_kv_heads, int head_dim, int block_size,
-                         int num_blocks, pa_stream_t stream) {
+                         int num_blocks, int64_t pool_block_stride, pa_stream_t stream) {
   if (pa_status s = check_pool_shape("pa_copy_blocks", num_kv_heads, head_dim, block_size,
                                      num_blocks))
     return s;
@@ -269,6 +325,10 @@ pa_status pa_copy_blocks(pa_half* k_pool, pa_half* v_pool, const int32_t* pairs,
   if (!pa::aligned16(k_pool) || !pa::aligned16(v_pool) ||
       (reinterpret_cast<uintptr_t>(pairs) & 3))
     return pa::fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: misaligned pointer");
+  int64_t stride = 0;
+  if (pa_status s = writer_stride("pa_copy_blocks", k_pool, v_pool, num_kv_heads, head_dim,
+                                  block_size, num_blocks, pool_block_stride, 2, &stride))
+    return s;
   pa::DeviceInfo dev;
   if (pa_status s = pa::current_device(&dev)) return s;
   int32_t* err = pa::device_error_word();
@@ -281,7 +341,7 @@ pa_status pa_copy_blocks(pa_half* k_pool, pa_half* v_pool, const int32_t* pairs,
   copy_blocks_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       reinterpret_cast<const uint4*>(k_pool), reinterpret_cast<const uint4*>(v_pool),
       reinterpret_cast<uint4*>(k_pool), reinterpret_cast<uint4*>(v_pool), pairs, block_vecs,
-      num_blocks, num_blocks, err);
+      stride / 8, stride / 8, num_blocks, num_blocks, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_copy_blocks launch");
   return pa::ok();
@@ -290,7 +350,8 @@ pa_status pa_copy_blocks(pa_half* k_pool, pa_half* v_pool, const int32_t* pairs,
 pa_status pa_append_kv_fp8(const pa_half* k_new, const pa_half* v_new, uint8_t* k_pool,
                            uint8_t* v_pool, const int32_t* slot_mapping, const float* k_scale,
                            const float* v_scale, int num_tokens, int num_kv_heads, int head_dim,
-                           int block_size, int num_blocks, pa_stream_t stream) {
+                           int block_size, int num_blocks, int64_t pool_block_stride,
+                           pa_stream_t stream) {
   if (pa_status s = check_pool_shape("pa_append_kv_fp8", num_kv_heads, head_dim, block_size,
                                      num_blocks))
     return s;
@@ -302,6 +363,10 @@ pa_status pa_append_kv_fp8(const pa_half* k_new, const pa_half* v_new, uint8_t* 
       !pa::aligned16(v_pool) || (reinterpret_cast<uintptr_t>(slot_mapping) & 3) ||
       (reinterpret_cast<uintptr_t>(k_scale) & 3) || (reinterpret_cast<uintptr_t>(v_scale) & 3))
     return pa::fail(PA_ERR_INVALID_ARG, "pa_append_kv_fp8: misaligned pointer");
+  int64_t stride = 0;
+  if (pa_status s = writer_stride("pa_append_kv_fp8", k_pool, v_pool, num_kv_heads, head_dim,
+                                  block_size, num_blocks, pool_block_stride, 1, &stride))
+    return s;
   pa::DeviceInfo dev;
   if (pa_status s = pa::current_device(&dev)) return s;
   int32_t* err = pa::device_error_word();
@@ -322,7 +387,8 @@ pa_status pa_append_kv_fp8(const pa_half* k_new, const pa_half* v_new, uint8_t* 
   append_kv_fp8_kernel<<<num_tokens, kAppendThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       reinterpret_cast<const uint4*>(k_new), reinterpret_cast<const uint4*>(v_new),
       reinterpret_cast<uint2*>(k_pool), reinterpret_cast<uint2*>(v_pool), slot_mapping, k_scale,
-      v_scale, row_vecs, head_dim / 8, static_cast<int64_t>(num_blocks) * block_size, err);
+      v_scale, row_vecs, head_dim / 8, block_size, stride / 8,
+      static_cast<int64_t>(num_blocks) * block_size, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_append_kv_fp8 launch");
   return pa::ok();
@@ -330,7 +396,7 @@ pa_status pa_append_kv_fp8(const pa_half* k_new, const pa_half* v_new, uint8_t* 
 
 pa_status pa_copy_blocks_fp8(uint8_t* k_pool, uint8_t* v_pool, const int32_t* pairs,
                              int num_pairs, int num_kv_heads, int head_dim, int block_size,
-                             int num_blocks, pa_stream_t stream) {
+                             int num_blocks, int64_t pool_block_stride, pa_stream_t stream) {
   if (pa_status s = check_pool_shape("pa_copy_blocks_fp8", num_kv_heads, head_dim, block_size,
                                      num_blocks))
     return s;
@@ -344,6 +410,10 @@ pa_status pa_copy_blocks_fp8(uint8_t* k_pool, uint8_t* v_pool, const int32_t* pa
   if (!pa::aligned16(k_pool) || !pa::aligned16(v_pool) ||
       (reinterpret_cast<uintptr_t>(pairs) & 3))
     return pa::fail(PA_ERR_INVALID_ARG, "pa_copy_blocks_fp8: misaligned pointer");
+  int64_t stride = 0;
+  if (pa_status s = writer_stride("pa_copy_blocks_fp8", k_pool, v_pool, num_kv_heads, head_dim,
+                                  block_size, num_blocks, pool_block_stride, 1, &stride))
+    return s;
   pa::DeviceInfo dev;
   if (pa_status s = pa::current_device(&dev)) return s;
   int32_t* err = pa::device_error_word();
@@ -356,7 +426,7 @@ pa_status pa_copy_blocks_fp8(uint8_t* k_pool, uint8_t* v_pool, const int32_t* pa
   copy_blocks_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       reinterpret_cast<const uint4*>(k_pool), reinterpret_cast<const uint4*>(v_pool),
       reinterpret_cast<uint4*>(k_pool), reinterpret_cast<uint4*>(v_pool), pairs, block_vecs,
-      num_blocks, num_blocks, err);
+      stride / 16, stride / 16, num_blocks, num_blocks, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_copy_blocks_fp8 launch");
   return pa::ok();
@@ -382,27 +452,44 @@ static pa_status device_view(const char* fn, const void* p, void** out) {
   return pa::fail(PA_ERR_INVALID_ARG, "%s: host memory must be pinned (page-locked)", fn);
 }
 
-pa_status pa_swap_blocks(const void* src_k, const void* src_v, int src_blocks, void* dst_k,
-                         void* dst_v, int dst_blocks, const int32_t* pairs, int num_pairs,
+pa_status pa_swap_blocks(const void* src_k, const void* src_v, int src_blocks,
+                         int64_t src_block_stride, void* dst_k, void* dst_v, int dst_blocks,
+                         int64_t dst_block_stride, const int32_t* pairs, int num_pairs,
                          int block_bytes, pa_stream_t stream) {
   if (num_pairs < 0 || src_blocks <= 0 || dst_blocks <= 0 || block_bytes <= 0 ||
       block_bytes % 16)
     return pa::fail(PA_ERR_INVALID_ARG,
                     "pa_swap_blocks: pairs=%d src_blocks=%d dst_blocks=%d block_bytes=%d",
                     num_pairs, src_blocks, dst_blocks, block_bytes);
+  int64_t src_stride = 0, dst_stride = 0;
+  if (pa_status s = pa::resolve_block_stride("pa_swap_blocks(src)", src_block_stride,
+                                             block_bytes, 1, &src_stride))
+    return s;
+  if (pa_status s = pa::resolve_block_stride("pa_swap_blocks(dst)", dst_block_stride,
+                                             block_bytes, 1, &dst_stride))
+    return s;
   if (num_pairs == 0) return pa::ok();
-  if (!src_k || !src_v || !dst_k || !dst_v || !pairs)
-    return pa::fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: NULL pointer");
+  const bool two = src_v != nullptr;
+  if (!src_k || !dst_k || !pairs || two != (dst_v != nullptr))
+    return pa::fail(PA_ERR_INVALID_ARG,
+                    "pa_swap_blocks: NULL pointer (src_v and dst_v are both set or both NULL)");
   if (!pa::aligned16(src_k) || !pa::aligned16(src_v) || !pa::aligned16(dst_k) ||
       !pa::aligned16(dst_v) || (reinterpret_cast<uintptr_t>(pairs) & 3))
     return pa::fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: misaligned pointer");
+  if (two) {
+    if (pa_status s = pa::check_pools_disjoint("pa_swap_blocks(dst)", dst_k, dst_v, dst_blocks,
+                                               dst_stride, block_bytes))
+      return s;
+  }
   pa::DeviceInfo dev;
   if (pa_status s = pa::current_device(&dev)) return s;
-  void *sk, *sv, *dk, *dv, *pp;
+  void *sk = nullptr, *sv = nullptr, *dk = nullptr, *dv = nullptr, *pp = nullptr;
   if (pa_status s = device_view("pa_swap_blocks(src_k)", src_k, &sk)) return s;
-  if (pa_status s = device_view("pa_swap_blocks(src_v)", src_v, &sv)) return s;
   if (pa_status s = device_view("pa_swap_blocks(dst_k)", dst_k, &dk)) return s;
-  if (pa_status s = device_view("pa_swap_blocks(dst_v)", dst_v, &dv)) return s;
+  if (two) {
+    if (pa_status s = device_view("pa_swap_blocks(src_v)", src_v, &sv)) return s;
+    if (pa_status s = device_view("pa_swap_blocks(dst_v)", dst_v, &dv)) return s;
+  }
   if (pa_status s = device_view("pa_swap_blocks(pairs)", pairs, &pp)) return s;
   int32_t* err = pa::device_error_word();
   if (!err) return PA_ERR_CUDA;
@@ -413,8 +500,8 @@ pa_status pa_swap_blocks(const void* src_k, const void* src_v, int src_blocks, v
   dim3 grid(num_pairs, static_cast<unsigned>(slices));
   copy_blocks_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(sk), static_cast<const uint4*>(sv), static_cast<uint4*>(dk),
-      static_cast<uint4*>(dv), static_cast<const int32_t*>(pp), block_vecs, src_blocks,
-      dst_blocks, err);
+      static_cast<uint4*>(dv), static_cast<const int32_t*>(pp), block_vecs, src_stride / 16,
+      dst_stride / 16, src_blocks, dst_blocks, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_swap_blocks launch");
   return pa::ok();

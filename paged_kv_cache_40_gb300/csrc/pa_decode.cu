@@ -300,6 +300,7 @@ struct DecodeParams {
   int hg;          // KV heads per group (consumer warps)
   int nst;         // ring stages
   float qscale;    // scale * log2(e)
+  long long block_stride_bytes;  // host only: the pools' block stride, for their tensor maps
 };
 
 __device__ __forceinline__ int clamp_len(int L, int cap, int32_t* err) {
@@ -1604,7 +1605,9 @@ unsigned long long next_call_tag() {
 
 // --- TMA descriptors of the pools -------------------------------------------
 // A 4-D tensor map over a pool seen as (dim, token, KV head, block) — the
-// token stride (Hkv*D*2 bytes) is larger than the head stride (D*2) — with box
+// token stride (Hkv*D*2 bytes) is larger than the head stride (D*2), and the
+// block stride is the pool's (a dense block, or two for the one-pool record
+// layout whose records hold a block's K and then its V) — with box
 // {64, tokens per stage, HG, 1} and the 128-byte swizzle: one copy moves one
 // 64-dimension half of HG heads of a block, landing as [head][token][128 B].
 // Encoding costs a few microseconds of host time, so the last few maps are
@@ -1618,10 +1621,11 @@ struct MapKey {
   int device;
   const void* ptr;
   int D, BS, Hkv, NB, hg, ts;
-  int esz;  // bytes per value: 2 (fp16) or 1 (E4M3)
+  int esz;             // bytes per value: 2 (fp16) or 1 (E4M3)
+  long long stride;    // bytes from one block to the next
   bool operator==(const MapKey& o) const {
     return device == o.device && ptr == o.ptr && D == o.D && BS == o.BS && Hkv == o.Hkv &&
-           NB == o.NB && hg == o.hg && ts == o.ts && esz == o.esz;
+           NB == o.NB && hg == o.hg && ts == o.ts && esz == o.esz && stride == o.stride;
   }
 };
 
@@ -1652,7 +1656,7 @@ pa_status pool_tensor_map(const MapKey& key, CUtensorMap* out) {
   const cuuint64_t e = static_cast<cuuint64_t>(key.esz);
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(key.Hkv) * key.D * e,   // token
                                  static_cast<cuuint64_t>(key.D) * e,             // KV head
-                                 static_cast<cuuint64_t>(key.BS) * key.Hkv * key.D * e};  // block
+                                 static_cast<cuuint64_t>(key.stride)};                  // block
   // the box's inner extent is one 128-byte line: 64 fp16 or 128 E4M3 values
   const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / key.esz),
                              static_cast<cuuint32_t>(key.ts), static_cast<cuuint32_t>(key.hg), 1};
@@ -1747,9 +1751,9 @@ pa_status launch_decode(DecodeParams prm, const pa::DeviceInfo& dev, cudaStream_
   prm.nst = cfg.nst;
   CUtensorMap kmap, vmap;
   MapKey kk{dev.device, prm.k_pool, D, BS, prm.num_kv_heads, prm.num_blocks, cfg.hg, SH::TS,
-            SH::ESZ};
+            SH::ESZ, prm.block_stride_bytes};
   MapKey vk{dev.device, prm.v_pool, D, BS, prm.num_kv_heads, prm.num_blocks, cfg.hg, SH::TS,
-            SH::ESZ};
+            SH::ESZ, prm.block_stride_bytes};
   if (pa_status s = pool_tensor_map(kk, &kmap)) return s;
   if (pa_status s = pool_tensor_map(vk, &vmap)) return s;
   // Programmatic dependent launch: the prologue may overlap the tail of the
@@ -1831,8 +1835,8 @@ PfxGeom prefix_geometry(int S, int G, int Hkv, int P, int sm_count) {
 
 template <int D, int BS, int G>
 pa_status launch_prefix(const PrefixParams& pp, const PfxGeom& geo, const void* k_pool,
-                        const void* v_pool, int Hkv, int NB, const pa::DeviceInfo& dev,
-                        cudaStream_t stream) {
+                        const void* v_pool, int Hkv, int NB, long long stride_bytes,
+                        const pa::DeviceInfo& dev, cudaStream_t stream) {
   constexpr int STAGE = 2 * (D / 64) * 16 * 128;
   const size_t smem = 256 + 1024 + static_cast<size_t>(kPfxStages) * STAGE +
                       static_cast<size_t>(kPfxRows) * D * 2;
@@ -1849,8 +1853,8 @@ pa_status launch_prefix(const PrefixParams& pp, const PfxGeom& geo, const void* 
     }
   }
   CUtensorMap kmap, vmap;
-  MapKey kk{dev.device, k_pool, D, BS, Hkv, NB, 1, 16, 2};
-  MapKey vk{dev.device, v_pool, D, BS, Hkv, NB, 1, 16, 2};
+  MapKey kk{dev.device, k_pool, D, BS, Hkv, NB, 1, 16, 2, stride_bytes};
+  MapKey vk{dev.device, v_pool, D, BS, Hkv, NB, 1, 16, 2, stride_bytes};
   if (pa_status s = pool_tensor_map(kk, &kmap)) return s;
   if (pa_status s = pool_tensor_map(vk, &vmap)) return s;
   cudaLaunchConfig_t lc = {};
@@ -1875,7 +1879,7 @@ pa_status shared_prefix_pass(const PrefixParams& pp, const PfxGeom& geo, DecodeP
                              const void* k_pool, const void* v_pool, const pa::DeviceInfo& dev,
                              cudaStream_t s) {
   if (pa_status st = launch_prefix<128, BS, G>(pp, geo, k_pool, v_pool, prm.num_kv_heads,
-                                                prm.num_blocks, dev, s))
+                                                prm.num_blocks, prm.block_stride_bytes, dev, s))
     return st;
   return launch_decode<128, BS, G, false, true>(prm, dev, s);
 }
@@ -1999,13 +2003,21 @@ static pa_status check_decode_call(const char* fn, const pa_half* q, const pa_ha
                                    const pa_half* v_pool, const int32_t* block_table,
                                    const int32_t* seq_lens, int num_seqs, int num_q_heads,
                                    int num_kv_heads, int head_dim, int block_size,
-                                   int max_blocks_per_seq, int num_blocks, float scale,
-                                   const pa_half* out, int partition_tokens) {
+                                   int max_blocks_per_seq, int num_blocks,
+                                   int64_t pool_block_stride, int esz, float scale,
+                                   const pa_half* out, int partition_tokens,
+                                   long long* stride_bytes) {
   if (pa_status s = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                                        max_blocks_per_seq, partition_tokens))
     return s;
   if (num_blocks <= 0 || static_cast<long long>(num_blocks) * block_size > INT32_MAX)
     return pa::fail(PA_ERR_INVALID_ARG, "%s: num_blocks %d", fn, num_blocks);
+  int64_t stride = 0;
+  if (pa_status s = pa::resolve_block_stride(
+          fn, pool_block_stride, static_cast<int64_t>(block_size) * num_kv_heads * head_dim, esz,
+          &stride))
+    return s;
+  *stride_bytes = stride * esz;
   if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
     return pa::fail(PA_ERR_INVALID_ARG, "%s: scale is not finite", fn);
   if (num_seqs == 0) return PA_OK;
@@ -2021,8 +2033,9 @@ static pa_status check_decode_call(const char* fn, const pa_half* q, const pa_ha
 static DecodeParams make_params(const pa_half* q, const pa_half* k_pool, const pa_half* v_pool,
                                 const int32_t* block_table, const int32_t* seq_lens,
                                 int num_seqs, int num_q_heads, int num_kv_heads,
-                                int max_blocks_per_seq, int num_blocks, float scale, pa_half* out,
-                                unsigned char* ws, const Layout& lay, int cap_blocks) {
+                                int max_blocks_per_seq, int num_blocks, long long stride_bytes,
+                                float scale, pa_half* out, unsigned char* ws, const Layout& lay,
+                                int cap_blocks) {
   DecodeParams prm;
   prm.q = reinterpret_cast<const __half*>(q);
   prm.k_pool = reinterpret_cast<const __half*>(k_pool);
@@ -2049,19 +2062,22 @@ static DecodeParams make_params(const pa_half* q, const pa_half* k_pool, const p
   prm.hg = 0;   // set by the launch
   prm.nst = 0;  // set by the launch
   prm.qscale = scale * kLog2e;
+  prm.block_stride_bytes = stride_bytes;
   return prm;
 }
 
 pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool, const pa_half* v_pool,
                               const int32_t* block_table, const int32_t* seq_lens, int num_seqs,
                               int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                              int max_blocks_per_seq, int num_blocks, float scale, pa_half* out,
-                              void* workspace, size_t workspace_bytes, int partition_tokens,
-                              pa_stream_t stream) {
+                              int max_blocks_per_seq, int num_blocks, int64_t pool_block_stride,
+                              float scale, pa_half* out, void* workspace, size_t workspace_bytes,
+                              int partition_tokens, pa_stream_t stream) {
+  long long stride_bytes = 0;
   if (pa_status s = check_decode_call("pa_decode_attention", q, k_pool, v_pool, block_table,
                                       seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                      block_size, max_blocks_per_seq, num_blocks, scale, out,
-                                      partition_tokens))
+                                      block_size, max_blocks_per_seq, num_blocks,
+                                      pool_block_stride, 2, scale, out, partition_tokens,
+                                      &stride_bytes))
     return s;
   if (num_seqs == 0) return pa::ok();
   if (!workspace) return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention: NULL workspace");
@@ -2076,8 +2092,9 @@ pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool, const pa_
   pa::DeviceInfo dev;
   if (pa_status s = pa::current_device(&dev)) return s;
   DecodeParams prm = make_params(q, k_pool, v_pool, block_table, seq_lens, num_seqs, num_q_heads,
-                                 num_kv_heads, max_blocks_per_seq, num_blocks, scale, out,
-                                 static_cast<unsigned char*>(workspace), lay, cap_blocks);
+                                 num_kv_heads, max_blocks_per_seq, num_blocks, stride_bytes,
+                                 scale, out, static_cast<unsigned char*>(workspace), lay,
+                                 cap_blocks);
   prm.err = pa::device_error_word();
   if (!prm.err) return PA_ERR_CUDA;
   const int G = num_q_heads / num_kv_heads;
@@ -2092,15 +2109,16 @@ pa_status pa_decode_attention_fp8(const pa_half* q, const uint8_t* k_pool, const
                                   const int32_t* block_table, const int32_t* seq_lens,
                                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                   int block_size, int max_blocks_per_seq, int num_blocks,
-                                  float scale, pa_half* out, void* workspace,
-                                  size_t workspace_bytes, int partition_tokens,
+                                  int64_t pool_block_stride, float scale, pa_half* out,
+                                  void* workspace, size_t workspace_bytes, int partition_tokens,
                                   pa_stream_t stream) {
   const pa_half* kp = reinterpret_cast<const pa_half*>(k_pool);
   const pa_half* vp = reinterpret_cast<const pa_half*>(v_pool);
+  long long stride_bytes = 0;
   if (pa_status s = check_decode_call("pa_decode_attention_fp8", q, kp, vp, block_table, seq_lens,
                                       num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                                      max_blocks_per_seq, num_blocks, scale, out,
-                                      partition_tokens))
+                                      max_blocks_per_seq, num_blocks, pool_block_stride, 1, scale,
+                                      out, partition_tokens, &stride_bytes))
     return s;
   if (head_dim != 128 || (block_size != 16 && block_size != 32))
     return pa::fail(PA_ERR_UNSUPPORTED,
@@ -2122,8 +2140,9 @@ pa_status pa_decode_attention_fp8(const pa_half* q, const uint8_t* k_pool, const
   pa::DeviceInfo dev;
   if (pa_status s = pa::current_device(&dev)) return s;
   DecodeParams prm = make_params(q, kp, vp, block_table, seq_lens, num_seqs, num_q_heads,
-                                 num_kv_heads, max_blocks_per_seq, num_blocks, scale, out,
-                                 static_cast<unsigned char*>(workspace), lay, cap_blocks);
+                                 num_kv_heads, max_blocks_per_seq, num_blocks, stride_bytes,
+                                 scale, out, static_cast<unsigned char*>(workspace), lay,
+                                 cap_blocks);
   prm.k_scale = k_scale;
   prm.v_scale = v_scale;
   prm.err = pa::device_error_word();
@@ -2151,12 +2170,13 @@ pa_status pa_decode_attention_shared_prefix(
     const pa_half* q, const pa_half* k_pool, const pa_half* v_pool, const int32_t* prefix_blocks,
     int num_prefix_blocks, const int32_t* block_table, const int32_t* seq_lens, int num_seqs,
     int num_q_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
-    int num_blocks, float scale, pa_half* out, void* workspace, size_t workspace_bytes,
-    pa_stream_t stream) {
+    int num_blocks, int64_t pool_block_stride, float scale, pa_half* out, void* workspace,
+    size_t workspace_bytes, pa_stream_t stream) {
+  long long stride_bytes = 0;
   if (pa_status s = check_decode_call("pa_decode_attention_shared_prefix", q, k_pool, v_pool,
                                       block_table, seq_lens, num_seqs, num_q_heads, num_kv_heads,
-                                      head_dim, block_size, max_blocks_per_seq, num_blocks, scale,
-                                      out, 0))
+                                      head_dim, block_size, max_blocks_per_seq, num_blocks,
+                                      pool_block_stride, 2, scale, out, 0, &stride_bytes))
     return s;
   if (head_dim != 128 || (block_size != 16 && block_size != 32))
     return pa::fail(PA_ERR_UNSUPPORTED,
@@ -2183,7 +2203,8 @@ pa_status pa_decode_attention_shared_prefix(
   if (num_prefix_blocks == 0)
     return pa_decode_attention(q, k_pool, v_pool, block_table, seq_lens, num_seqs, num_q_heads,
                                num_kv_heads, head_dim, block_size, max_blocks_per_seq,
-                               num_blocks, scale, out, workspace, workspace_bytes, 0, stream);
+                               num_blocks, pool_block_stride, scale, out, workspace,
+                               workspace_bytes, 0, stream);
   pa::DeviceInfo dev;
   if (pa_status s = pa::current_device(&dev)) return s;
   const int G = num_q_heads / num_kv_heads;
@@ -2193,8 +2214,8 @@ pa_status pa_decode_attention_shared_prefix(
   const size_t rec_bytes = static_cast<size_t>(rec_floats(G, head_dim)) * 4;
   // the suffix pass: the table past the prefix's columns, lengths past its tokens
   DecodeParams prm = make_params(q, k_pool, v_pool, block_table + P, seq_lens, num_seqs,
-                                 num_q_heads, num_kv_heads, max_blocks_per_seq, num_blocks, scale,
-                                 out, ws, lay.base, 0);
+                                 num_q_heads, num_kv_heads, max_blocks_per_seq, num_blocks,
+                                 stride_bytes, scale, out, ws, lay.base, 0);
   prm.err = pa::device_error_word();
   if (!prm.err) return PA_ERR_CUDA;
   prm.pfx_blocks = P;
@@ -2229,12 +2250,15 @@ pa_status pa_decode_attention_fixed_scratch(const pa_half* q, const pa_half* k_p
                                             const int32_t* seq_lens, int num_seqs,
                                             int num_q_heads, int num_kv_heads, int head_dim,
                                             int block_size, int max_blocks_per_seq,
-                                            int num_blocks, float scale, pa_half* out,
-                                            int partition_tokens, pa_stream_t stream) {
+                                            int num_blocks, int64_t pool_block_stride,
+                                            float scale, pa_half* out, int partition_tokens,
+                                            pa_stream_t stream) {
+  long long stride_bytes = 0;
   if (pa_status s = check_decode_call("pa_decode_attention_fixed_scratch", q, k_pool, v_pool,
                                       block_table, seq_lens, num_seqs, num_q_heads, num_kv_heads,
-                                      head_dim, block_size, max_blocks_per_seq, num_blocks, scale,
-                                      out, partition_tokens))
+                                      head_dim, block_size, max_blocks_per_seq, num_blocks,
+                                      pool_block_stride, 2, scale, out, partition_tokens,
+                                      &stride_bytes))
     return s;
   if (num_seqs == 0) return pa::ok();
   pa::DeviceInfo dev;
@@ -2269,8 +2293,8 @@ pa_status pa_decode_attention_fixed_scratch(const pa_half* q, const pa_half* k_p
   if (!ws) return PA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   DecodeParams prm = make_params(q, k_pool, v_pool, block_table, seq_lens, num_seqs, num_q_heads,
-                                 num_kv_heads, max_blocks_per_seq, num_blocks, scale, out, ws, lay,
-                                 cap_blocks);
+                                 num_kv_heads, max_blocks_per_seq, num_blocks, stride_bytes,
+                                 scale, out, ws, lay, cap_blocks);
   prm.err = pa::device_error_word();
   if (!prm.err) return PA_ERR_CUDA;
   pa_status st = head_dim == 64 ? dispatch_bs<64>(block_size, G, prm, dev, s)

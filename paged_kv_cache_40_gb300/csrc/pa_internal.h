@@ -27,6 +27,21 @@ inline bool aligned16(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
 
+// Block stride of a pool in values: 0 selects the dense stride `dense`
+// (block_size*num_kv_heads*head_dim); otherwise the stride must be at least
+// `dense` and a multiple of 16 bytes (`esz` bytes per value). Writes the
+// stride in values to *out, or records a message naming `fn` and returns
+// PA_ERR_INVALID_ARG.
+pa_status resolve_block_stride(const char* fn, int64_t stride, int64_t dense, int esz,
+                               int64_t* out);
+
+// For calls that write both pools: blocks of `block_bytes` at k + b*stride
+// and v + b*stride (b < num_blocks, stride in bytes) must not overlap between
+// the two pools. Records a message naming `fn` and returns PA_ERR_INVALID_ARG
+// when they do.
+pa_status check_pools_disjoint(const char* fn, const void* k, const void* v, int num_blocks,
+                               int64_t stride_bytes, int64_t block_bytes);
+
 // Properties of the current device used for launch shaping.
 struct DeviceInfo {
   int device = -1;

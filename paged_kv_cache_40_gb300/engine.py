@@ -14,6 +14,11 @@ v_new (numpy fp16) and scale.
 With kv_dtype "fp8" the cache is E4M3 bytes with one fp32 scale per KV head
 for K and V (given as k_pool, v_pool, k_scale, v_scale); the new tokens are
 quantized by the append.
+
+With layout "records" the cache is one pool of per-block records, each a
+block's K rows then its V rows (the layout sketch of "Phase 7 · Document 04 —
+PagedAttention", §2), held in `kv_pool`; `k_pool` / `v_pool` are its member
+views and every call takes them as it takes two separate pools.
 """
 
 from __future__ import annotations
@@ -23,9 +28,10 @@ from typing import List, Optional, Tuple
 
 import numpy as np
 
-from . import (BlockAllocator, alloc_workspace, pa_append_kv, pa_append_kv_fp8, pa_copy_blocks,
-               pa_copy_blocks_fp8, pa_decode_attention, pa_decode_attention_fp8,
-               pa_decode_attention_shared_prefix, pa_decode_shared_prefix_workspace_bytes)
+from . import (BlockAllocator, alloc_workspace, kv_block_pool, kv_views, pa_append_kv,
+               pa_append_kv_fp8, pa_copy_blocks, pa_copy_blocks_fp8, pa_decode_attention,
+               pa_decode_attention_fp8, pa_decode_attention_shared_prefix,
+               pa_decode_shared_prefix_workspace_bytes)
 
 
 def _to_dev(arr, device, dtype=None):
@@ -34,6 +40,25 @@ def _to_dev(arr, device, dtype=None):
     if dtype is not None:
         t = t.to(dtype)
     return t.to(device)
+
+
+def _device_pools(k, v, layout, device):
+    """(kv_pool or None, k_pool, v_pool) on the device from host or device
+    pools [NB][BS][Hkv][D]: two dense pools, or one record pool and its
+    member views."""
+    import torch
+    dev = lambda p: p if isinstance(p, torch.Tensor) else _to_dev(p, device)
+    if layout == "separate":
+        return None, dev(k), dev(v)
+    if layout != "records":
+        raise ValueError("layout must be 'separate' or 'records'")
+    kt, vt = dev(k), dev(v)
+    nb, bs, h, d = (int(x) for x in kt.shape)
+    kv = kv_block_pool(nb, bs, h, d, kt.dtype, device)
+    kp, vp = kv_views(kv)
+    kp.copy_(kt)
+    vp.copy_(vt)
+    return kv, kp, vp
 
 
 @dataclass
@@ -49,7 +74,7 @@ class DecodeBatchRunner:
 
     def __init__(self, batch, device="cuda", max_blocks: Optional[int] = None,
                  partition_tokens: int = 0, table_fill: int = -1, k_pool=None, v_pool=None,
-                 kv_dtype: str = "fp16", k_scale=None, v_scale=None):
+                 kv_dtype: str = "fp16", k_scale=None, v_scale=None, layout: str = "separate"):
         import torch
         if kv_dtype not in ("fp16", "fp8"):
             raise ValueError("kv_dtype must be 'fp16' or 'fp8'")
@@ -75,13 +100,10 @@ class DecodeBatchRunner:
         need = max(1, max(-(-(int(L) + 1) // bs) for L in batch.prefill_lens)) if S else 1
         self.max_blocks = int(max_blocks or need)
         self.table_fill = table_fill
-        def dev_pool(p, default):
-            if p is None:
-                return _to_dev(default, self.device)
-            return p if isinstance(p, torch.Tensor) else _to_dev(p, self.device)
-
-        self.k_pool = dev_pool(k_pool, batch.k_pool)
-        self.v_pool = dev_pool(v_pool, batch.v_pool)
+        self.layout = layout
+        self.kv_pool, self.k_pool, self.v_pool = _device_pools(
+            batch.k_pool if k_pool is None else k_pool,
+            batch.v_pool if v_pool is None else v_pool, layout, self.device)
         self.k_scale = _to_dev(k_scale, self.device, torch.float32) if k_scale is not None else None
         self.v_scale = _to_dev(v_scale, self.device, torch.float32) if v_scale is not None else None
         self.q = _to_dev(batch.q, self.device)
@@ -181,7 +203,7 @@ class SharedPrefixRunner(DecodeBatchRunner):
     """
 
     def __init__(self, workload, device="cuda", partition_tokens: int = 0,
-                 prefix_aware: bool = True):
+                 prefix_aware: bool = True, layout: str = "separate"):
         import torch
         w = workload
         self.prefix_aware = prefix_aware
@@ -197,8 +219,9 @@ class SharedPrefixRunner(DecodeBatchRunner):
         self.alloc = a
         self.max_blocks = -(-(int(w.prefix_len) + 1) // w.block_size)
         self.table_fill = -1
-        self.k_pool = _to_dev(w.k_pool, self.device)
-        self.v_pool = _to_dev(w.v_pool, self.device)
+        self.layout = layout
+        self.kv_pool, self.k_pool, self.v_pool = _device_pools(w.k_pool, w.v_pool, layout,
+                                                               self.device)
         self.k_scale = self.v_scale = None
         q, kn, vn = w.step_inputs(0, self.num_seqs)
         self.q = _to_dev(q, self.device)

@@ -9,10 +9,10 @@ NULL = None
 
 def _decode(lib, **kw):
     a = dict(q=NULL, k=NULL, v=NULL, table=NULL, lens=NULL, S=4, Hq=32, Hkv=8, D=128, BS=16,
-             MB=8, NB=64, scale=0.1, out=NULL, ws=NULL, wsb=0, pt=0, stream=NULL)
+             MB=8, NB=64, stride=0, scale=0.1, out=NULL, ws=NULL, wsb=0, pt=0, stream=NULL)
     a.update(kw)
     return lib.pa_decode_attention(a["q"], a["k"], a["v"], a["table"], a["lens"], a["S"], a["Hq"],
-                                   a["Hkv"], a["D"], a["BS"], a["MB"], a["NB"],
+                                   a["Hkv"], a["D"], a["BS"], a["MB"], a["NB"], a["stride"],
                                    ctypes.c_float(a["scale"]), a["out"], a["ws"], a["wsb"],
                                    a["pt"], a["stream"])
 
@@ -59,23 +59,76 @@ def test_workspace_bytes(libpa):
 
 def test_cache_ops_reject(libpa):
     lib = libpa.lib()
-    assert lib.pa_append_kv(NULL, NULL, NULL, NULL, NULL, 4, 8, 100, 16, 64, NULL) == 4
-    assert lib.pa_append_kv(NULL, NULL, NULL, NULL, NULL, -1, 8, 128, 16, 64, NULL) == 1
-    assert lib.pa_append_kv(NULL, NULL, NULL, NULL, NULL, 0, 8, 128, 16, 64, NULL) == 0
-    assert lib.pa_append_kv(NULL, NULL, NULL, NULL, NULL, 4, 8, 128, 16, 64, NULL) == 1
-    assert lib.pa_copy_blocks(NULL, NULL, NULL, 3, 0, 128, 16, 64, NULL) == 1
-    assert lib.pa_copy_blocks(NULL, NULL, NULL, 0, 8, 128, 16, 64, NULL) == 0
-    assert lib.pa_copy_blocks(NULL, NULL, NULL, 2, 8, 128, 16, 64, NULL) == 1
+    assert lib.pa_append_kv(NULL, NULL, NULL, NULL, NULL, 4, 8, 100, 16, 64, 0, NULL) == 4
+    assert lib.pa_append_kv(NULL, NULL, NULL, NULL, NULL, -1, 8, 128, 16, 64, 0, NULL) == 1
+    assert lib.pa_append_kv(NULL, NULL, NULL, NULL, NULL, 0, 8, 128, 16, 64, 0, NULL) == 0
+    assert lib.pa_append_kv(NULL, NULL, NULL, NULL, NULL, 4, 8, 128, 16, 64, 0, NULL) == 1
+    assert lib.pa_copy_blocks(NULL, NULL, NULL, 3, 0, 128, 16, 64, 0, NULL) == 1
+    assert lib.pa_copy_blocks(NULL, NULL, NULL, 0, 8, 128, 16, 64, 0, NULL) == 0
+    assert lib.pa_copy_blocks(NULL, NULL, NULL, 2, 8, 128, 16, 64, 0, NULL) == 1
+
+
+# Stand-in addresses: every call below is refused by a host check that runs
+# before any device work, so they are never dereferenced.
+_K = 0x10000000
+_E = 16 * 8 * 128          # values in one block of the shape used below
+
+
+@pytest.mark.parametrize("v_off,stride,msg", [
+    (64 * _E * 2, _E - 8, b"pool_block_stride"),     # shorter than a block
+    (64 * _E * 2, _E + 4, b"pool_block_stride"),     # not a multiple of 16 bytes
+    (64 * _E * 2 - 16, 0, b"overlap"),               # dense pools that overlap by 16 bytes
+    (16, 2 * _E, b"overlap"),                        # records with V one vector into K
+    (4 * _E - 16, 2 * _E, b"overlap"),               # V's end runs into the next record
+])
+def test_pool_layout_rejects(libpa, v_off, stride, msg):
+    """Strided and record pools: strides shorter than a block or not a
+    multiple of 16 bytes, and K blocks that overlap V blocks (v_off in bytes),
+    are refused."""
+    lib = libpa.lib()
+    k = ctypes.c_void_p(_K)
+    v = ctypes.c_void_p(_K + v_off)
+    src = ctypes.c_void_p(0x20000000)
+    slots = ctypes.c_void_p(0x30000000)
+    assert lib.pa_append_kv(src, src, k, v, slots, 4, 8, 128, 16, 64, stride, NULL) == 1
+    assert msg in lib.pa_last_error()
+    assert lib.pa_copy_blocks(k, v, slots, 2, 8, 128, 16, 64, stride, NULL) == 1
+    assert msg in lib.pa_last_error()
+
+
+def test_record_pool_stride_is_accepted_up_to_the_device(libpa):
+    """The record layout (v = k + one block, stride two blocks) passes every
+    host check; without a GPU the call then stops at the device query."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("would launch on stand-in addresses")
+    lib = libpa.lib()
+    k = ctypes.c_void_p(_K)
+    v = ctypes.c_void_p(_K + _E * 2)
+    slots = ctypes.c_void_p(0x30000000)
+    st = lib.pa_copy_blocks(k, v, slots, 2, 8, 128, 16, 64, 2 * _E, NULL)
+    assert st == 5 and b"overlap" not in lib.pa_last_error()
+
+
+def test_decode_rejects_bad_strides(libpa):
+    lib = libpa.lib()
+    assert _decode(lib, stride=_E - 8) == 1
+    assert b"pool_block_stride" in lib.pa_last_error()
+    assert _decode(lib, stride=_E + 4) == 1
+    assert b"pool_block_stride" in lib.pa_last_error()
+    assert _decode_fp8(lib, stride=_E + 8) == 1          # fp8: 8 bytes is not 16
+    assert b"pool_block_stride" in lib.pa_last_error()
 
 
 def _decode_fp8(lib, **kw):
     a = dict(q=NULL, k=NULL, v=NULL, ks=NULL, vs=NULL, table=NULL, lens=NULL, S=4, Hq=32, Hkv=8,
-             D=128, BS=16, MB=8, NB=64, scale=0.1, out=NULL, ws=NULL, wsb=0, pt=0, stream=NULL)
+             D=128, BS=16, MB=8, NB=64, stride=0, scale=0.1, out=NULL, ws=NULL, wsb=0, pt=0,
+             stream=NULL)
     a.update(kw)
     return lib.pa_decode_attention_fp8(a["q"], a["k"], a["v"], a["ks"], a["vs"], a["table"],
                                        a["lens"], a["S"], a["Hq"], a["Hkv"], a["D"], a["BS"],
-                                       a["MB"], a["NB"], ctypes.c_float(a["scale"]), a["out"],
-                                       a["ws"], a["wsb"], a["pt"], a["stream"])
+                                       a["MB"], a["NB"], a["stride"], ctypes.c_float(a["scale"]),
+                                       a["out"], a["ws"], a["wsb"], a["pt"], a["stream"])
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -98,9 +151,9 @@ def test_cache_ops_fp8_reject(libpa):
     lib = libpa.lib()
     # NULL scales / pools with work to do
     assert lib.pa_append_kv_fp8(NULL, NULL, NULL, NULL, NULL, NULL, NULL, 4, 8, 128, 16, 64,
-                                NULL) == 1
+                                0, NULL) == 1
     assert lib.pa_append_kv_fp8(NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, 8, 128, 16, 64,
-                                NULL) == 0
-    assert lib.pa_copy_blocks_fp8(NULL, NULL, NULL, 0, 8, 128, 16, 64, NULL) == 0
-    assert lib.pa_copy_blocks_fp8(NULL, NULL, NULL, 2, 8, 120, 16, 64, NULL) == 4  # 120 % 16
-    assert lib.pa_copy_blocks_fp8(NULL, NULL, NULL, 2, 8, 128, 16, 64, NULL) == 1
+                                0, NULL) == 0
+    assert lib.pa_copy_blocks_fp8(NULL, NULL, NULL, 0, 8, 128, 16, 64, 0, NULL) == 0
+    assert lib.pa_copy_blocks_fp8(NULL, NULL, NULL, 2, 8, 120, 16, 64, 0, NULL) == 4  # 120 % 16
+    assert lib.pa_copy_blocks_fp8(NULL, NULL, NULL, 2, 8, 128, 16, 64, 0, NULL) == 1
