@@ -508,6 +508,13 @@ __device__ __forceinline__ bool arrive_last(unsigned long long* word, unsigned l
   return false;
 }
 
+// Shared-prefix mode: wait for the prefix kernel (the grid launched just
+// before on the stream) before reading its records.
+template <bool PFX>
+__device__ __forceinline__ void pfx_wait() {
+  if constexpr (PFX) asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // One warp merges the E partial records of one KV head of a cut segment with
 // the log-sum-exp rule and writes that head's G fp16 output rows. Record i is
 // `recs + rec_of(i) * rec_floats(G, D)`: acc [G][D], then (max, sum) per
@@ -681,8 +688,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
   // Everything above reads only seq_lens. The pool, q and the table may still
   // be written by the kernel launched just before this one on the stream
-  // (programmatic dependent launch): wait for it before touching them.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // (programmatic dependent launch): wait for it before touching them. In
+  // shared-prefix mode that kernel is the prefix kernel, which writes only
+  // the prefix records and lets this kernel start once everything before it
+  // has completed; the wait then sits before the first read of a prefix
+  // record (pfx_wait), and the streaming overlaps the prefix kernel.
+  if constexpr (!PFX) asm volatile("griddepcontrol.wait;" ::: "memory");
   // a dependent kernel launched after this one may start its own prologue
   asm volatile("griddepcontrol.launch_dependents;");
 
@@ -855,6 +866,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         };
         __half* out_row = p.out + (static_cast<long long>(msg.seq) * p.num_q_heads +
                                    static_cast<long long>(kvh_m) * G) * D;
+        pfx_wait<PFX>();
         merge_partials<D, G>(p.records, E + (PFX ? p.pfx_chunks : 0), rec_of, out_row);
       }
     }
@@ -872,6 +884,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   for (int i = blockIdx.x; i < S; i += gridDim.x) {
     if (pfx[i + 1] == pfx[i]) {
       if constexpr (PFX) {
+        pfx_wait<PFX>();
         for (int kv = w; kv < Hkv; kv += HG) {
           auto rec_of = [&](int k) -> long long {
             return p.pfx_rec_base + (static_cast<long long>(k) * S + i) * Hkv + kv;
@@ -1255,6 +1268,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         if (i == 0) return p.pfx_own_base + static_cast<long long>(pm.seq) * Hkv + kvh;
         return p.pfx_rec_base + (static_cast<long long>(i - 1) * S + pm.seq) * Hkv + kvh;
       };
+      pfx_wait<PFX>();
       merge_partials<D, G>(p.records, 1 + p.pfx_chunks, rec_of, out_row);
     } else if (cut) {
           if (!pm.last) {
@@ -1305,6 +1319,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                          (static_cast<long long>(i - E) * S + pm.seq) * Hkv + kvh;
                 return record_index(c_first + i, c_first, s0, chunk, HG, w);
               };
+              pfx_wait<PFX>();
               merge_partials<D, G>(p.records, E + (PFX ? p.pfx_chunks : 0), rec_of, out_row);
             }
           }
@@ -1327,19 +1342,33 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 // Sequences that begin with the same physical blocks (a shared prompt prefix:
 // "Phase 7 · Document 04 — PagedAttention", §2 block sharing and §3 Mental
 // Model; lux-666 notes "PagedAttention", prefix sharing) attend those blocks
-// with the same K and V rows. The prefix kernel streams each prefix tile of a
-// KV head once and contracts it against the query rows of every sequence
-// that shares it: rows (sequence, query head of the group), 16 per consumer
-// warp, 64 per CTA, every mma row real. S = Q K^T, online softmax per row,
-// O = P V with P reused from the score registers as the A operand; the
-// prefix's tokens are split into chunks across CTAs, and each (chunk,
-// sequence, KV head) leaves one partial record (the layout the merges use).
-// The attention kernel then streams each sequence's remaining blocks and
-// merges the prefix chunks' records into that sequence's result.
-constexpr int kPfxWarps = 4;                    // consumer warps of a prefix CTA
-constexpr int kPfxRows = 16 * kPfxWarps;        // query rows per prefix CTA
-constexpr int kPfxStages = 4;
+// with the same K and V rows, so for one KV head the prefix is a dense
+// contraction: S = Q K^T with Q the query rows of every sharing sequence
+// (rows (sequence, query head of the group), 128 per CTA) and K the prefix's
+// tokens, then O = P V. The prefix kernel runs it on the 5th-generation
+// tensor cores: Q, K, V and P sit in shared memory as 128-byte-swizzled
+// operand tiles, S and O accumulate in tensor memory (TMEM), one thread
+// issues the MMAs, one warp streams K/V tiles with TMA, and four warps (one
+// TMEM lane quarter each, one query row per thread) run the softmax. The
+// prefix's tokens are split into chunks across CTAs and each chunk into
+// sub-chunks of up to 128 tokens; a row's online softmax runs over its
+// chunk's sub-chunks, and each (chunk, sequence, KV head) leaves one partial
+// record (the layout the merges use). The attention kernel then streams each
+// sequence's remaining blocks and merges the prefix chunks' records into that
+// sequence's result.
+constexpr int kPfxRows = 128;                   // query rows per CTA = TMEM lanes
+constexpr int kPfxTok = 128;                    // tokens per sub-chunk (MMA N of S)
+constexpr int kPfxSoftmaxWarps = 4;             // warps 0-3: one TMEM lane quarter each
+constexpr int kPfxWarpK = 4;                    // TMA of K tiles
+constexpr int kPfxWarpS = 5;                    // S = Q K^T issuer; owns the TMEM allocation
+constexpr int kPfxWarpPV = 6;                   // O = P V issuer
+constexpr int kPfxWarpV = 7;                    // TMA of V tiles
+constexpr int kPfxThreads = 8 * 32;
+constexpr int kPfxStages = 2;                   // K and V tiles in flight
 constexpr int kMaxPfxChunks = 32;
+constexpr int kPfxTmemCols = 512;               // S[2] and O[2], 128 fp32 columns each
+constexpr int kPfxTile = kPfxTok * 256;         // one operand tile: 128 rows x 128 fp16
+constexpr int kPfxSmem = 1024 + 256 + (3 + 2 * kPfxStages) * kPfxTile;  // Q, P[2], K, V
 
 struct PrefixParams {
   const __half* q;
@@ -1355,208 +1384,411 @@ struct PrefixParams {
   float qscale;                  // scale * log2(e)
 };
 
-template <int D, int BS, int G>
-__global__ void __launch_bounds__((kPfxWarps + 1) * 32)
+// ---- tcgen05 ----------------------------------------------------------------
+// Shared-memory operand descriptor: a tile of rows of 128 bytes with the
+// 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r % 8)), 8-row
+// groups `sbo` bytes apart; `lbo` is the distance between the two 64-value
+// halves of an MN-major operand (unused for K-major tiles).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor of an M=128 x N MMA, fp16 A and B, fp32 accumulate;
+// A K-major, B K-major or (b_mn) MN-major.
+__device__ __forceinline__ uint32_t f16_idesc(int n, bool b_mn) {
+  return (1u << 4) | (b_mn ? 1u << 16 : 0u) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(128 >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+// Arrive on `bar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// 16 / 32 consecutive fp32 columns of this thread's TMEM lane; returns after
+// the load has completed.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];\n\ttcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int BS, int G>
+__global__ void __launch_bounds__(kPfxThreads, 1)
     paged_prefix_kernel(const PrefixParams p, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap) {
-  constexpr int TS = 16;                       // tokens per stage
-  constexpr int NHALF = D / 64;
-  constexpr int HALF = TS * 128;               // one 64-dim half of one head's 16 rows
-  constexpr int TILE = NHALF * HALF;
-  constexpr int STAGE = 2 * TILE;
+  constexpr int D = 128;
+  constexpr int HALF = kPfxTile / 2;           // one 64-value half: 128 rows x 128 B
   constexpr int RS = rec_floats(G, D);
-  extern __shared__ __align__(128) unsigned char psm[];
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(psm);
-  uint64_t* empty_bar = full_bar + kPfxStages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(psm + 2 * kPfxStages * 8);
-  const uint32_t base = smem_addr(psm);
-  unsigned char* ring = psm + (((base + 256 + 1023u) & ~1023u) - base);
-  unsigned char* qtile = ring + kPfxStages * STAGE;  // [kPfxRows][D] fp16, 16-byte chunks swizzled
+  static_assert(kPfxTok % BS == 0 && BS % 16 == 0, "sub-chunks are whole blocks of 16-token boxes");
+  extern __shared__ __align__(1024) unsigned char psm[];
+  // barriers and flags, then 1024-aligned tiles: Q, P[2], K[stages], V[stages]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(psm);
+  uint64_t* k_full = bars;                     // [stages] TMA -> S issuer
+  uint64_t* v_full = bars + 2;                 // [stages] TMA -> PV issuer
+  uint64_t* k_empty = bars + 4;                // [stages] S MMAs done with a K tile
+  uint64_t* v_empty = bars + 6;                // [stages] PV MMAs done with a V tile
+  uint64_t* s_full = bars + 8;                 // [2] S buffer written
+  uint64_t* s_free = bars + 10;                // [2] S buffer read by the softmax warps
+  uint64_t* p_full = bars + 12;                // [2] P buffer written
+  uint64_t* o_full = bars + 14;                // [2] O buffer written (and its P buffer read)
+  uint64_t* o_free = bars + 16;                // [2] O buffer read by the softmax warps
+  uint64_t* mma_done = bars + 18;              // [2] every MMA of an issuer completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t sbase = smem_addr(psm);
+  unsigned char* tiles = psm + (((sbase + 256 + 1023u) & ~1023u) - sbase);
+  unsigned char* q_s = tiles;
+  unsigned char* p_s = tiles + kPfxTile;                       // [2]
+  unsigned char* k_s = tiles + 3 * kPfxTile;                   // [stages]
+  unsigned char* v_s = tiles + (3 + kPfxStages) * kPfxTile;    // [stages]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kvh = blockIdx.y, c = blockIdx.z;
   const int S = p.num_seqs;
-  const int j_lo = c * p.chunk_blocks;
-  const int j_hi = min(p.prefix_blocks_n, j_lo + p.chunk_blocks);
+  const int tok_lo = c * p.chunk_blocks * BS;
+  const int tok_hi = min(p.prefix_blocks_n, (c + 1) * p.chunk_blocks) * BS;
+  const int nsub = (tok_hi - tok_lo + kPfxTok - 1) / kPfxTok;
+  auto sub_len = [&](int t) { return min(kPfxTok, tok_hi - (tok_lo + t * kPfxTok)); };
+
   if (threadIdx.x == 0) {
-    for (int st = 0; st < kPfxStages; ++st) {
-      mbar_init(smem_addr(&full_bar[st]), 1);
-      mbar_init(smem_addr(&empty_bar[st]), kPfxWarps);
-    }
+    // s_free, p_full and o_free count the four softmax warps; the others one
+    // arrival (a TMA transaction count or an MMA commit)
+    for (int i = 0; i < 20; ++i)
+      mbar_init(smem_addr(&bars[i]),
+                (i >= 10 && i < 14) || (i >= 16 && i < 18) ? kPfxSoftmaxWarps : 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
   asm volatile("griddepcontrol.wait;" ::: "memory");
-
-  if (warp == kPfxWarps) {
-    // ---- producer: this chunk's prefix blocks, 16 tokens per stage ----
-    uint32_t g = 0;
-    for (int j0 = j_lo; j0 < j_hi; j0 += 32) {
-      const int nn = min(32, j_hi - j0);
-      const int phys_lane = lane < nn ? __ldg(p.prefix_blocks + j0 + lane) : 0;
-      for (int jj = 0; jj < nn; ++jj) {
-        const int phys = __shfl_sync(0xffffffffu, phys_lane, jj);
-        const bool bad = phys < 0 || phys >= p.num_blocks;
-        for (int sb = 0; sb < BS / TS; ++sb, ++g) {
-          const int st = g % kPfxStages;
-          const uint32_t use = g / kPfxStages;
-          if (__shfl_sync(0xffffffffu, *abort_flag, 0)) continue;
-          if (use > 0 &&
-              !warp_wait_phase(smem_addr(&empty_bar[st]), (use - 1) & 1, abort_flag, p.err))
-            continue;
-          if (lane == 0) {
-            const uint32_t fb = smem_addr(&full_bar[st]);
-            if (bad) atomicOr(p.err, PA_DEVERR_BAD_BLOCK);
-            mbar_arrive_expect_tx(fb, bad ? 0u : static_cast<uint32_t>(STAGE));
-            if (!bad) {
-              const uint32_t dst = smem_addr(ring + static_cast<size_t>(st) * STAGE);
+  // Everything launched before this kernel has completed: the attention
+  // kernel that follows may start streaming (it waits for this kernel only
+  // before it reads the prefix records).
+  asm volatile("griddepcontrol.launch_dependents;");
+  const bool tma_warp = warp == kPfxWarpK || warp == kPfxWarpV;
+  uint32_t tmem = 0;
+  if (!tma_warp) {
+    // the TMA warps start streaming at once; the other six warps stage Q and
+    // allocate TMEM, then meet on a named barrier
+    if (warp == kPfxWarpS) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_addr(tmem_slot)),
+                   "n"(kPfxTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // Q rows -> shared memory as the K-major A operand (zero rows past the
+    // batch); every load of a thread is in flight before its first store
+    constexpr int kQThreads = kPfxThreads - 64;
+    const int qt = warp < kPfxWarpK ? threadIdx.x : threadIdx.x - 32;  // 0..191
+    constexpr int kPer = (kPfxRows * (D / 8) + kQThreads - 1) / kQThreads;
+    uint4 v[kPer];
 #pragma unroll
-              for (int h = 0; h < NHALF; ++h) {
-                tma_load_4d(dst + h * HALF, &kmap, 64 * h, sb * TS, kvh, phys, fb);
-                tma_load_4d(dst + TILE + h * HALF, &vmap, 64 * h, sb * TS, kvh, phys, fb);
-              }
-            }
-          }
-          __syncwarp();
+    for (int i = 0; i < kPer; ++i) {
+      const int e = qt + i * kQThreads;
+      const int r = e / (D / 8), ch = e % (D / 8);
+      const int row = blockIdx.x * kPfxRows + r, seq = row / G, gg = row % G;
+      v[i] = make_uint4(0, 0, 0, 0);
+      if (e < kPfxRows * (D / 8) && seq < S)
+        v[i] = __ldg(reinterpret_cast<const uint4*>(
+            p.q + (static_cast<long long>(seq) * p.num_q_heads + kvh * G + gg) * D) + ch);
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = qt + i * kQThreads;
+      const int r = e / (D / 8), ch = e % (D / 8);
+      if (e < kPfxRows * (D / 8))
+        *reinterpret_cast<uint4*>(q_s + (ch >> 3) * HALF + r * 128 +
+                                  (((ch & 7) ^ (r & 7)) << 4)) = v[i];
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    asm volatile("bar.sync 1, %0;" ::"n"(kPfxThreads - 64) : "memory");
+    tc_fence_after();
+    tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  }
+
+  int issued = 0;  // sub-chunks whose copies a TMA warp issued
+  if (tma_warp) {
+    // ---- TMA: the K (or V) tile of each sub-chunk, 16-token boxes per half ----
+    const bool is_k = warp == kPfxWarpK;
+    const CUtensorMap* map = is_k ? &kmap : &vmap;
+    uint64_t* full = is_k ? k_full : v_full;
+    uint64_t* empty = is_k ? k_empty : v_empty;
+    unsigned char* ring = is_k ? k_s : v_s;
+    // block ids of a sub-chunk: one per lane, all loaded at once; the next
+    // sub-chunk's are in flight while this one's copies are issued
+    auto load_ids = [&](int t) {
+      const int nb = sub_len(t) / BS;
+      int id = 0;
+      if (lane < nb) {
+        id = __ldg(p.prefix_blocks + (tok_lo + t * kPfxTok) / BS + lane);
+        if (id < 0 || id >= p.num_blocks) {
+          if (is_k) atomicOr(p.err, PA_DEVERR_BAD_BLOCK);
+          id = 0;  // an in-range block keeps the byte count; the result is flagged
         }
       }
+      return id;
+    };
+    int next_ids = nsub > 0 ? load_ids(0) : 0;
+    for (int t = 0; t < nsub; ++t, ++issued) {
+      const int st = t % kPfxStages, n = sub_len(t);
+      const int ids = next_ids;
+      if (t >= kPfxStages &&
+          !warp_wait_phase(smem_addr(&empty[st]), ((t / kPfxStages) - 1) & 1, abort_flag, p.err))
+        break;
+      const uint32_t dst = smem_addr(ring + st * kPfxTile), bar = smem_addr(&full[st]);
+      if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n) * 256u);
+      for (int j = 0; j < n / BS; ++j) {
+        const int phys = __shfl_sync(0xffffffffu, ids, j);
+        if (lane == 0) {
+#pragma unroll
+          for (int sb = 0; sb < BS / 16; ++sb) {
+            const uint32_t off = static_cast<uint32_t>(j * BS + sb * 16) * 128u;
+            tma_load_4d(dst + off, map, 0, sb * 16, kvh, phys, bar);
+            tma_load_4d(dst + HALF + off, map, 64, sb * 16, kvh, phys, bar);
+          }
+        }
+      }
+      if (t + 1 < nsub) next_ids = load_ids(t + 1);
+      __syncwarp();
     }
     if (*abort_flag) {
-      const uint32_t first = g > static_cast<uint32_t>(kPfxStages) ? g - kPfxStages : 0;
-      for (uint32_t gi = first; gi < g; ++gi) {
-        const unsigned long long t0 = global_ns();
-        while (!mbar_try_wait(smem_addr(&full_bar[gi % kPfxStages]), (gi / kPfxStages) & 1) &&
-               global_ns() - t0 < kWaitLimitNs) {
+      // the last copies issued into each stage land before the CTA exits
+      for (int t = issued > kPfxStages ? issued - kPfxStages : 0; t < issued; ++t) {
+        const unsigned long long w0 = global_ns();
+        while (!mbar_try_wait(smem_addr(&full[t % kPfxStages]), (t / kPfxStages) & 1) &&
+               global_ns() - w0 < kWaitLimitNs) {
         }
       }
     }
-    return;
-  }
-
-  // ---- consumer warp: 16 query rows (sequence, query head of the group) ----
-  const int gid = lane >> 2, tig = lane & 3;
-  const int ld_row = lane & 7, ld_mat = lane >> 3;
-  const int row0 = blockIdx.x * kPfxRows + warp * 16;
-  unsigned char* qw = qtile + warp * 16 * (D * 2);
-  // q rows -> shared memory (zero rows past the batch), then A fragments
-  for (int e = lane; e < 16 * (D / 8); e += 32) {
-    const int r = e / (D / 8), ch = e % (D / 8);
-    const int row = row0 + r, seq = row / G, gg = row % G;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (seq < S)
-      v = __ldg(reinterpret_cast<const uint4*>(
-          p.q + (static_cast<long long>(seq) * p.num_q_heads + kvh * G + gg) * D) + ch);
-    *reinterpret_cast<uint4*>(qw + r * (D * 2) + ((ch ^ (r & 7)) << 4)) = v;
-  }
-  __syncwarp();
-  uint32_t qa[D / 16][4];
-  {
-    const int r = ((ld_mat & 1) << 3) + ld_row;
+  } else if (warp == kPfxWarpS) {
+    // ---- S issuer: S_t = Q K_t^T into TMEM buffer t % 2 ----
+    const uint32_t qa = smem_addr(q_s);
+    for (int t = 0; t < nsub; ++t) {
+      const int st = t % kPfxStages, b = t & 1;
+      if (!warp_wait_phase(smem_addr(&k_full[st]), (t / kPfxStages) & 1, abort_flag, p.err)) break;
+      if (t >= 2 && !warp_wait_phase(smem_addr(&s_free[b]), ((t - 2) >> 1) & 1, abort_flag, p.err))
+        break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t kb = smem_addr(k_s + st * kPfxTile);
+        const uint32_t id = f16_idesc(sub_len(t), false);
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const int ch = 2 * kk + (ld_mat >> 1);
-      ldsm_x4(smem_addr(qw) + r * (D * 2) + ((ch ^ ld_row) << 4), qa[kk][0], qa[kk][1],
-              qa[kk][2], qa[kk][3]);
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * HALF + (k & 3) * 32;
+          tc_mma(tmem + b * kPfxTok, sw128_desc(qa + off, 16, 1024),
+                 sw128_desc(kb + off, 16, 1024), id, k > 0);
+        }
+        tc_commit(smem_addr(&s_full[b]));
+        tc_commit(smem_addr(&k_empty[st]));
+      }
+      __syncwarp();
     }
-  }
-  float m0 = -INFINITY, m1 = -INFINITY;  // rows gid, gid + 8: running max (log2 units)
-  float l0 = 0.f, l1 = 0.f;              // and partial sums over this lane's tokens
-  float o[D / 8][4];                     // O[row gid (+8)][dim 8*nd + 2*tig (+1)]
+    if (lane == 0) tc_commit(smem_addr(&mma_done[0]));
+    __syncwarp();
+    const unsigned long long w0 = global_ns();
+    while (!mbar_try_wait(smem_addr(&mma_done[0]), 0) && global_ns() - w0 < kWaitLimitNs) {
+    }
+  } else if (warp == kPfxWarpPV) {
+    // ---- PV issuer: O_t = P_t V_t into TMEM buffer 2 + t % 2 ----
+    for (int t = 0; t < nsub; ++t) {
+      const int st = t % kPfxStages, b = t & 1;
+      if (!warp_wait_phase(smem_addr(&p_full[b]), (t >> 1) & 1, abort_flag, p.err)) break;
+      if (!warp_wait_phase(smem_addr(&v_full[st]), (t / kPfxStages) & 1, abort_flag, p.err)) break;
+      if (t >= 2 && !warp_wait_phase(smem_addr(&o_free[b]), ((t - 2) >> 1) & 1, abort_flag, p.err))
+        break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t pa = smem_addr(p_s + b * kPfxTile);
+        const uint32_t vb = smem_addr(v_s + st * kPfxTile);
+        const uint32_t id = f16_idesc(D, true);
+        const int n = sub_len(t);
+        for (int k = 0; k < n / 16; ++k)
+          tc_mma(tmem + (2 + b) * kPfxTok, sw128_desc(pa + (k >> 2) * HALF + (k & 3) * 32, 16, 1024),
+                 sw128_desc(vb + k * 2048, HALF, 1024), id, k > 0);
+        tc_commit(smem_addr(&o_full[b]));
+        tc_commit(smem_addr(&v_empty[st]));
+      }
+      __syncwarp();
+    }
+    if (lane == 0) tc_commit(smem_addr(&mma_done[1]));
+    __syncwarp();
+    const unsigned long long w0 = global_ns();
+    while (!mbar_try_wait(smem_addr(&mma_done[1]), 0) && global_ns() - w0 < kWaitLimitNs) {
+    }
+  } else {
+    // ---- softmax warps: query row r = 32 * warp + lane (TMEM lane r) ----
+    const int r = warp * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    float o[D];
 #pragma unroll
-  for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-
-  const uint32_t nstages = static_cast<uint32_t>(j_hi > j_lo ? (j_hi - j_lo) * (BS / TS) : 0);
-  for (uint32_t g = 0; g < nstages; ++g) {
-    const int st = g % kPfxStages;
-    if (!warp_wait_phase(smem_addr(&full_bar[st]), (g / kPfxStages) & 1, abort_flag, p.err))
-      continue;
-    const uint32_t kaddr = smem_addr(ring + static_cast<size_t>(st) * STAGE);
-    const uint32_t vaddr = kaddr + TILE;
-    // ---- S = Q K^T (16 rows x 16 tokens) ----
-    float sc[2][4];
+    for (int i = 0; i < D; ++i) o[i] = 0.f;
+    float m = -INFINITY, l = 0.f, alpha_prev = 0.f;
+    bool ok = true;
+    // fold O_t (relative to the max after sub-chunk t) into o
+    auto fold = [&](int t, float alpha) -> bool {
+      const int b = t & 1;
+      if (!warp_wait_phase(smem_addr(&o_full[b]), (t >> 1) & 1, abort_flag, p.err)) return false;
+      tc_fence_after();
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-      const uint32_t rowa = kaddr + (nt * 8 + ld_row) * 128;
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float v[32];
+        tmem_ld32(lane_base + (2 + b) * kPfxTok + c0, v);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; kk += 2) {
-        const int gc = 2 * kk + ld_mat;  // 8-dim chunk of the row
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(rowa + (gc >> 3) * HALF + (((gc & 7) ^ ld_row) << 4), b0, b1, b2, b3);
-        mma_16816(sc[nt], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-        mma_16816(sc[nt], qa[kk + 1][0], qa[kk + 1][1], qa[kk + 1][2], qa[kk + 1][3], b2, b3);
+        for (int i = 0; i < 32; ++i) o[c0 + i] = fmaf(o[c0 + i], alpha, v[i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&o_free[b]));
+      return true;
+    };
+    for (int t = 0; t < nsub && ok; ++t) {
+      const int n = sub_len(t), b = t & 1;
+      if (!warp_wait_phase(smem_addr(&s_full[b]), (t >> 1) & 1, abort_flag, p.err)) break;
+      tc_fence_after();
+      const uint32_t sa = lane_base + b * kPfxTok;
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      int c0 = 0;
+      for (; c0 + 32 <= n; c0 += 32) {
+        float v[32];
+        tmem_ld32(sa + c0, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], v[i] * p.qscale);
+      }
+      if (c0 < n) {
+        float v[16];
+        tmem_ld16(sa + c0, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], v[i] * p.qscale);
+      }
+      const float mn = fmaxf(m, fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])));
+      const float alpha = fast_exp2(m - mn);
+      m = mn;
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      unsigned char* prow = p_s + b * kPfxTile + r * 128;
+      // P = exp2(S * qscale - m) as fp16, 16 tokens (two 16-byte chunks) at a time
+      auto emit16 = [&](const float* v, int col) {
+        uint32_t h[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float e0 = fast_exp2(fmaf(v[2 * i], p.qscale, -mn));
+          const float e1 = fast_exp2(fmaf(v[2 * i + 1], p.qscale, -mn));
+          sum4[(2 * i) & 3] += e0;
+          sum4[(2 * i + 1) & 3] += e1;
+          h[i] = pack_half2(e0, e1);
+        }
+        const int ch = (col & 63) >> 3;
+        unsigned char* dst = prow + (col >> 6) * HALF;
+        *reinterpret_cast<uint4*>(dst + ((ch ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(dst + (((ch + 1) ^ (r & 7)) << 4)) =
+            make_uint4(h[4], h[5], h[6], h[7]);
+      };
+      for (c0 = 0; c0 + 32 <= n; c0 += 32) {
+        float v[32];
+        tmem_ld32(sa + c0, v);
+        emit16(v, c0);
+        emit16(v + 16, c0 + 16);
+      }
+      if (c0 < n) {
+        float v[16];
+        tmem_ld16(sa + c0, v);
+        emit16(v, c0);
+      }
+      l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_addr(&s_free[b]));
+        mbar_arrive(smem_addr(&p_full[b]));
+      }
+      // O of the previous sub-chunk, folded while the tensor cores run this one's
+      if (t > 0) ok = fold(t - 1, alpha_prev);
+      alpha_prev = alpha;
+    }
+    if (ok && nsub > 0) ok = fold(nsub - 1, alpha_prev);
+    // ---- the chunk's partial records of this warp's 32 rows ----
+    // Every MMA has completed (the last O was folded), so the K tiles are
+    // free: each warp stages its rows there (16 KB, rows padded to 132 floats
+    // against bank conflicts) and writes each sequence's G rows as one
+    // contiguous run, 512 bytes per store instruction.
+    constexpr int kPad = D + 4;
+    float* stage = reinterpret_cast<float*>(k_s) + warp * 32 * kPad;
+#pragma unroll
+    for (int i = 0; i < D; i += 4)
+      *reinterpret_cast<float4*>(stage + lane * kPad + i) =
+          make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+    __syncwarp();
+    const int row = blockIdx.x * kPfxRows + r, seq = row / G, gg = row % G;
+    const bool write = ok && !*abort_flag;
+    if (seq < S && write) {
+      float* rec = p.records + ((static_cast<long long>(c) * S + seq) * p.num_kv_heads + kvh) * RS;
+      rec[G * D + 2 * gg] = m;
+      rec[G * D + 2 * gg + 1] = l;
+    }
+    if (write) {
+      // the warp's rows 32w .. 32w+31 belong to sequences row / G; a record's
+      // G rows are contiguous ([G][D] floats)
+      const int row0 = blockIdx.x * kPfxRows + warp * 32;
+      for (int e = lane; e < 32 * (D / 4); e += 32) {
+        const int rr = e / (D / 4), i4 = e % (D / 4);
+        const int rw = row0 + rr, sq = rw / G, g2 = rw % G;
+        if (sq < S) {
+          float* rec =
+              p.records + ((static_cast<long long>(c) * S + sq) * p.num_kv_heads + kvh) * RS;
+          *reinterpret_cast<float4*>(rec + g2 * D + 4 * i4) =
+              *reinterpret_cast<const float4*>(stage + rr * kPad + 4 * i4);
+        }
       }
     }
-    // ---- online softmax per row ----
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sc[nt][e] *= p.qscale;
-      mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
-      mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
-    m0 = mn0;
-    m1 = mn1;
-    uint32_t pa[4];  // P as the A operand: rows gid / gid + 8, tokens 2tig.. / 8 + 2tig..
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const float p0 = fast_exp2(sc[nt][0] - mn0), p1 = fast_exp2(sc[nt][1] - mn0);
-      const float p2 = fast_exp2(sc[nt][2] - mn1), p3 = fast_exp2(sc[nt][3] - mn1);
-      s0 += p0 + p1;
-      s1 += p2 + p3;
-      pa[2 * nt] = pack_half2(p0, p1);
-      pa[2 * nt + 1] = pack_half2(p2, p3);
-    }
-    l0 = l0 * al0 + s0;
-    l1 = l1 * al1 + s1;
-#pragma unroll
-    for (int nd = 0; nd < D / 8; ++nd) {
-      o[nd][0] *= al0;
-      o[nd][1] *= al0;
-      o[nd][2] *= al1;
-      o[nd][3] *= al1;
-    }
-    // ---- O += P V: B = V [token][dim] by ldmatrix.trans, two 8-dim tiles per x4 ----
-    const uint32_t rowv = vaddr + (((ld_mat & 1) << 3) + ld_row) * 128;
-#pragma unroll
-    for (int q2 = 0; q2 < D / 16; ++q2) {
-      const int gc = 2 * q2 + (ld_mat >> 1);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(rowv + (gc >> 3) * HALF + (((gc & 7) ^ ld_row) << 4), b0, b1, b2, b3);
-      mma_16816(o[2 * q2], pa[0], pa[1], pa[2], pa[3], b0, b1);
-      mma_16816(o[2 * q2 + 1], pa[0], pa[1], pa[2], pa[3], b2, b3);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&empty_bar[st]));
   }
-
-  // ---- the chunk's partial record of each row ----
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int row = row0 + gid + 8 * half, seq = row / G, gg = row % G;
-    if (seq >= S) continue;
-    float* rec = p.records + ((static_cast<long long>(c) * S + seq) * p.num_kv_heads + kvh) * RS;
-#pragma unroll
-    for (int nd = 0; nd < D / 8; ++nd)
-      *reinterpret_cast<float2*>(rec + gg * D + 8 * nd + 2 * tig) =
-          make_float2(o[nd][2 * half], o[nd][2 * half + 1]);
-    if (tig == 0) {
-      rec[G * D + 2 * gg] = half ? m1 : m0;
-      rec[G * D + 2 * gg + 1] = half ? l1 : l0;
-    }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kPfxWarpS) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "n"(kPfxTmemCols)
+                 : "memory");
   }
 }
 
@@ -1815,8 +2047,9 @@ pa_status launch_config_any(int D, int BS, int G, const pa::DeviceInfo& dev, int
 }
 
 // --- shared prefix ---------------------------------------------------------
-// Prefix chunks: enough (row tiles x KV heads x chunks) CTAs to cover the SMs
-// about twice, at most kMaxPfxChunks and at most one per prefix block.
+// Prefix chunks: as many (row tiles x KV heads x chunks) CTAs as fit one wave
+// of one CTA per SM (at least one chunk), at most kMaxPfxChunks and at most
+// one per prefix block.
 struct PfxGeom {
   int row_tiles, chunks, chunk_blocks;
 };
@@ -1824,7 +2057,7 @@ PfxGeom prefix_geometry(int S, int G, int Hkv, int P, int sm_count) {
   PfxGeom g;
   g.row_tiles = (S * G + kPfxRows - 1) / kPfxRows;
   const long long base = static_cast<long long>(g.row_tiles) * Hkv;
-  long long c = (2ll * sm_count + base - 1) / base;
+  long long c = sm_count / base;
   if (c > kMaxPfxChunks) c = kMaxPfxChunks;
   if (c > P) c = P;
   if (c < 1) c = 1;
@@ -1833,21 +2066,19 @@ PfxGeom prefix_geometry(int S, int G, int Hkv, int P, int sm_count) {
   return g;
 }
 
-template <int D, int BS, int G>
+template <int BS, int G>
 pa_status launch_prefix(const PrefixParams& pp, const PfxGeom& geo, const void* k_pool,
                         const void* v_pool, int Hkv, int NB, long long stride_bytes,
                         const pa::DeviceInfo& dev, cudaStream_t stream) {
-  constexpr int STAGE = 2 * (D / 64) * 16 * 128;
-  const size_t smem = 256 + 1024 + static_cast<size_t>(kPfxStages) * STAGE +
-                      static_cast<size_t>(kPfxRows) * D * 2;
-  auto kernel = paged_prefix_kernel<D, BS, G>;
+  constexpr int D = 128;
+  auto kernel = paged_prefix_kernel<BS, G>;
   {
     static std::mutex mu;
     static bool set[64] = {};
     std::lock_guard<std::mutex> lock(mu);
     if (!set[dev.device]) {
       cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
+                                           kPfxSmem);
       if (e != cudaSuccess) return pa::cuda_fail(e, "cudaFuncSetAttribute(prefix)");
       set[dev.device] = true;
     }
@@ -1860,8 +2091,8 @@ pa_status launch_prefix(const PrefixParams& pp, const PfxGeom& geo, const void* 
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(static_cast<unsigned>(geo.row_tiles), static_cast<unsigned>(Hkv),
                     static_cast<unsigned>(geo.chunks));
-  lc.blockDim = dim3((kPfxWarps + 1) * 32);
-  lc.dynamicSmemBytes = smem;
+  lc.blockDim = dim3(kPfxThreads);
+  lc.dynamicSmemBytes = kPfxSmem;
   lc.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1878,7 +2109,7 @@ template <int BS, int G>
 pa_status shared_prefix_pass(const PrefixParams& pp, const PfxGeom& geo, DecodeParams prm,
                              const void* k_pool, const void* v_pool, const pa::DeviceInfo& dev,
                              cudaStream_t s) {
-  if (pa_status st = launch_prefix<128, BS, G>(pp, geo, k_pool, v_pool, prm.num_kv_heads,
+  if (pa_status st = launch_prefix<BS, G>(pp, geo, k_pool, v_pool, prm.num_kv_heads,
                                                 prm.num_blocks, prm.block_stride_bytes, dev, s))
     return st;
   return launch_decode<128, BS, G, false, true>(prm, dev, s);
