@@ -443,50 +443,54 @@ def run_ours(args, world, rank, local):
     assert pa.pa_device_error() == 0
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     sampler = ClockSampler(str(torch.cuda.get_device_properties(dev).uuid))
     sampler.start()
     time.sleep(0.15)
     barrier(world)
     torch.cuda.synchronize(dev)
     w0 = time.perf_counter()
+    # the step as a caller issues it: nothing between the append and the
+    # attention kernel, which is launched as a programmatic dependent and so
+    # may start its prologue while the append runs
     for k in range(K):
         flush()
         ev[k][0].record(stream)
         run.copy_and_append()
-        ev[k][1].record(stream)
         run.attend()
-        ev[k][2].record(stream)
+        ev[k][1].record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     wall = time.perf_counter() - w0
     clocks = sampler.stop()
-    step_ms = [ev[k][0].elapsed_time(ev[k][2]) for k in range(K)]
-    attn_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    step_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    assert pa.pa_device_error() == 0
+    # the attention call alone (the roofline's kernel), same number of steps
+    eva = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for k in range(K):
+        flush()
+        eva[k][0].record(stream)
+        run.attend()
+        eva[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    attn_ms = [eva[k][0].elapsed_time(eva[k][1]) for k in range(K)]
     assert pa.pa_device_error() == 0
 
-    # end to end through the public API with pinned host buffers
-    h = {
-        "q": run.q.cpu().pin_memory(),
-        "k_new": run.k_new.cpu().pin_memory(),
-        "v_new": run.v_new.cpu().pin_memory(),
-        "slots": torch.from_numpy(plan.slots).pin_memory(),
-        "table": torch.from_numpy(plan.block_table).pin_memory(),
-        "lens": torch.from_numpy(plan.seq_lens).pin_memory(),
-    }
+    # end to end through the public API with pinned host buffers: every step
+    # uploads its inputs (q, new K/V rows, slots, copy pairs, table, lengths)
+    # from one pinned host buffer with one copy, and the attention kernel
+    # writes the result into pinned host memory through its device mapping
+    # (NVLink-C2C), so the result crosses to the host without a copy call
+    run.pack_inputs()
     out_h = torch.empty(run.out.shape, dtype=run.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    dev_out = run.out
+    run.out = out_h
+    h2d = int(run.host_arena.numel())
     d2h = out_h.numel() * out_h.element_size()
 
     def e2e_step():
-        run.q.copy_(h["q"], non_blocking=True)
-        run.k_new.copy_(h["k_new"], non_blocking=True)
-        run.v_new.copy_(h["v_new"], non_blocking=True)
-        run.d_slots.copy_(h["slots"], non_blocking=True)
-        run.d_table.copy_(h["table"], non_blocking=True)
-        run.d_lens.copy_(h["lens"], non_blocking=True)
+        run.upload_inputs()
         run.run_step()
-        out_h.copy_(run.out, non_blocking=True)
 
     for _ in range(args.warmup):
         flush()
@@ -504,6 +508,7 @@ def run_ours(args, world, rank, local):
     barrier(world)
     e2e_ms = [eev[k][0].elapsed_time(eev[k][1]) for k in range(Ke)]
     assert pa.pa_device_error() == 0
+    run.out = dev_out
 
     kvb = run.kv_bytes()
     tokens = int(plan.seq_lens.astype(np.int64).sum())
@@ -561,7 +566,9 @@ def run_ours(args, world, rank, local):
                      "bytes_per_launch": run.io_bytes()},
         "e2e": {"value": round(all_kv_e2e / t_e2e / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "ms_per_step": round(1e3 * t_e2e / Ke, 5), "steps": Ke},
+                "ms_per_step": round(1e3 * t_e2e / Ke, 5), "steps": Ke,
+                "path": "inputs packed in one pinned host buffer, one host-to-device copy; the "
+                        "attention kernel writes the output into pinned host memory"},
         "cpu_baseline": cpu,
         "gpu_launches": launches_per_step * K,
         "clocks": clocks,

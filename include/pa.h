@@ -171,7 +171,12 @@ PA_API pa_status pa_copy_blocks(pa_half* k_pool, pa_half* v_pool,
  *              included); a value < 0 or > max_blocks_per_seq*block_size sets
  *              PA_DEVERR_BAD_LEN and is clamped into range.
  * scale        softmax scale (typically 1/sqrt(head_dim))
- * out          device [num_seqs][num_q_heads][head_dim] fp16 (written)
+ * out          [num_seqs][num_q_heads][head_dim] fp16 (written): device
+ *              memory, or pinned (page-locked) host memory, which the kernel
+ *              writes through its device mapping (no separate copy back;
+ *              visible to the host once the stream has been synchronised).
+ *              Pageable host memory is refused (PA_ERR_INVALID_ARG). The
+ *              same holds for `out` of every attention call below.
  * workspace    device scratch of >= pa_decode_workspace_bytes(...) bytes,
  *              16-byte aligned, owned by the caller. It holds an arrival
  *              counter per (sequence, KV head) and the fp32 partial results

@@ -82,6 +82,19 @@ def _dev(t, name, dtype, ndim=None):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _out(t, like):
+    """Output pointer: a CUDA tensor, or pinned host memory that the kernel
+    writes through its device mapping (no copy back)."""
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float16 or not t.is_contiguous():
+        raise TypeError("out must be a contiguous float16 tensor")
+    if tuple(t.shape) != tuple(like.shape):
+        raise ValueError("out must have q's shape")
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError("out must be a CUDA tensor or pinned host memory")
+    return ctypes.c_void_p(t.data_ptr())
+
+
 def _block_stride(t, name) -> int:
     """Values from one block of a pool to the next; each block itself must be
     a contiguous [block_size][kv_heads][head_dim] array."""
@@ -206,8 +219,6 @@ def pa_decode_attention(q, k_pool, v_pool, block_table, seq_lens, scale, out=Non
         raise ValueError("seq_lens must be [num_seqs]")
     if out is None:
         out = torch.empty_like(q)
-    elif tuple(out.shape) != tuple(q.shape):
-        raise ValueError("out must have q's shape")
     if workspace is None:
         workspace = alloc_workspace(S, hq, hkv, d, bs, mb, partition_tokens, q.device)
     args = (_dev(q, "q", torch.float16), _pool(k_pool, "k_pool", torch.float16),
@@ -215,7 +226,7 @@ def pa_decode_attention(q, k_pool, v_pool, block_table, seq_lens, scale, out=Non
             _dev(seq_lens, "seq_lens", torch.int32))
     _check(_load().pa_decode_attention(
         *args, S, hq, hkv, d, bs, mb, nb, stride, ctypes.c_float(float(scale)),
-        _dev(out, "out", torch.float16), _dev(workspace, "workspace", torch.uint8),
+        _out(out, q), _dev(workspace, "workspace", torch.uint8),
         workspace.numel(), partition_tokens, _stream_ptr(stream)))
     return out
 
@@ -302,8 +313,6 @@ def pa_decode_attention_shared_prefix(q, k_pool, v_pool, prefix_blocks, block_ta
     P = int(prefix_blocks.numel())
     if out is None:
         out = torch.empty_like(q)
-    elif tuple(out.shape) != tuple(q.shape):
-        raise ValueError("out must have q's shape")
     if workspace is None:
         n = pa_decode_shared_prefix_workspace_bytes(S, hq, hkv, d, bs, mb, P)
         workspace = torch.zeros(max(n, 16), dtype=torch.uint8, device=q.device)
@@ -314,7 +323,7 @@ def pa_decode_attention_shared_prefix(q, k_pool, v_pool, prefix_blocks, block_ta
             _dev(seq_lens, "seq_lens", torch.int32))
     _check(_load().pa_decode_attention_shared_prefix(
         *args, S, hq, hkv, d, bs, mb, nb, stride, ctypes.c_float(float(scale)),
-        _dev(out, "out", torch.float16), _dev(workspace, "workspace", torch.uint8),
+        _out(out, q), _dev(workspace, "workspace", torch.uint8),
         workspace.numel(), _stream_ptr(stream)))
     return out
 
@@ -372,8 +381,6 @@ def pa_decode_attention_fp8(q, k_pool, v_pool, k_scale, v_scale, block_table, se
         raise ValueError("seq_lens must be [num_seqs]")
     if out is None:
         out = torch.empty_like(q)
-    elif tuple(out.shape) != tuple(q.shape):
-        raise ValueError("out must have q's shape")
     if workspace is None:
         workspace = alloc_workspace(S, hq, hkv, d, bs, mb, partition_tokens, q.device)
     ks, vs = _scales(k_scale, v_scale, hkv)
@@ -383,7 +390,7 @@ def pa_decode_attention_fp8(q, k_pool, v_pool, k_scale, v_scale, block_table, se
             _dev(seq_lens, "seq_lens", torch.int32))
     _check(_load().pa_decode_attention_fp8(
         *args, S, hq, hkv, d, bs, mb, nb, stride, ctypes.c_float(float(scale)),
-        _dev(out, "out", torch.float16), _dev(workspace, "workspace", torch.uint8),
+        _out(out, q), _dev(workspace, "workspace", torch.uint8),
         workspace.numel(), partition_tokens, _stream_ptr(stream)))
     return out
 
@@ -410,15 +417,13 @@ def pa_decode_attention_fixed_scratch(q, k_pool, v_pool, block_table, seq_lens, 
         raise ValueError("seq_lens must be [num_seqs]")
     if out is None:
         out = torch.empty_like(q)
-    elif tuple(out.shape) != tuple(q.shape):
-        raise ValueError("out must have q's shape")
     args = (_dev(q, "q", torch.float16), _pool(k_pool, "k_pool", torch.float16),
             _pool(v_pool, "v_pool", torch.float16), _dev(block_table, "block_table", torch.int32),
             _dev(seq_lens, "seq_lens", torch.int32))
     _check(_load().pa_decode_attention_fixed_scratch(
         *args, S, hq, hkv, d, bs, int(block_table.shape[1]), nb, stride,
         ctypes.c_float(float(scale)),
-        _dev(out, "out", torch.float16), partition_tokens, _stream_ptr(stream)))
+        _out(out, q), partition_tokens, _stream_ptr(stream)))
     return out
 
 

@@ -432,9 +432,11 @@ pa_status pa_copy_blocks_fp8(uint8_t* k_pool, uint8_t* v_pool, const int32_t* pa
   return pa::ok();
 }
 
-// A pointer the device can dereference: device memory as it is, pinned host
-// memory through its device mapping; anything else is refused.
-static pa_status device_view(const char* fn, const void* p, void** out) {
+}  // extern "C"
+
+namespace pa {
+
+pa_status device_view(const char* fn, const void* p, void** out) {
   cudaPointerAttributes at;
   cudaError_t e = cudaPointerGetAttributes(&at, p);
   if (e != cudaSuccess) return pa::cuda_fail(e, fn);
@@ -451,6 +453,10 @@ static pa_status device_view(const char* fn, const void* p, void** out) {
   }
   return pa::fail(PA_ERR_INVALID_ARG, "%s: host memory must be pinned (page-locked)", fn);
 }
+
+}  // namespace pa
+
+extern "C" {
 
 pa_status pa_swap_blocks(const void* src_k, const void* src_v, int src_blocks,
                          int64_t src_block_stride, void* dst_k, void* dst_v, int dst_blocks,
@@ -484,13 +490,13 @@ pa_status pa_swap_blocks(const void* src_k, const void* src_v, int src_blocks,
   pa::DeviceInfo dev;
   if (pa_status s = pa::current_device(&dev)) return s;
   void *sk = nullptr, *sv = nullptr, *dk = nullptr, *dv = nullptr, *pp = nullptr;
-  if (pa_status s = device_view("pa_swap_blocks(src_k)", src_k, &sk)) return s;
-  if (pa_status s = device_view("pa_swap_blocks(dst_k)", dst_k, &dk)) return s;
+  if (pa_status s = pa::device_view("pa_swap_blocks(src_k)", src_k, &sk)) return s;
+  if (pa_status s = pa::device_view("pa_swap_blocks(dst_k)", dst_k, &dk)) return s;
   if (two) {
-    if (pa_status s = device_view("pa_swap_blocks(src_v)", src_v, &sv)) return s;
-    if (pa_status s = device_view("pa_swap_blocks(dst_v)", dst_v, &dv)) return s;
+    if (pa_status s = pa::device_view("pa_swap_blocks(src_v)", src_v, &sv)) return s;
+    if (pa_status s = pa::device_view("pa_swap_blocks(dst_v)", dst_v, &dv)) return s;
   }
-  if (pa_status s = device_view("pa_swap_blocks(pairs)", pairs, &pp)) return s;
+  if (pa_status s = pa::device_view("pa_swap_blocks(pairs)", pairs, &pp)) return s;
   int32_t* err = pa::device_error_word();
   if (!err) return PA_ERR_CUDA;
   const int64_t block_vecs = block_bytes / 16;

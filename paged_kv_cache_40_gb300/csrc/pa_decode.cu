@@ -2261,6 +2261,15 @@ static pa_status check_decode_call(const char* fn, const pa_half* q, const pa_ha
   return PA_OK;
 }
 
+// The output may be device memory or pinned host memory, which the kernels
+// then write through its device mapping (zero-copy over the CPU-GPU link).
+static pa_status device_out(const char* fn, pa_half* out, pa_half** dev_out) {
+  void* d = nullptr;
+  if (pa_status s = pa::device_view(fn, out, &d)) return s;
+  *dev_out = static_cast<pa_half*>(d);
+  return PA_OK;
+}
+
 static DecodeParams make_params(const pa_half* q, const pa_half* k_pool, const pa_half* v_pool,
                                 const int32_t* block_table, const int32_t* seq_lens,
                                 int num_seqs, int num_q_heads, int num_kv_heads,
@@ -2311,6 +2320,7 @@ pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool, const pa_
                                       &stride_bytes))
     return s;
   if (num_seqs == 0) return pa::ok();
+  if (pa_status s = device_out("pa_decode_attention(out)", out, &out)) return s;
   if (!workspace) return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention: NULL workspace");
   if (!pa::aligned16(workspace))
     return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention: misaligned workspace");
@@ -2356,6 +2366,7 @@ pa_status pa_decode_attention_fp8(const pa_half* q, const uint8_t* k_pool, const
                     "pa_decode_attention_fp8: head_dim %d / block_size %d (fp8 pools support "
                     "head_dim 128 and block_size 16 or 32)", head_dim, block_size);
   if (num_seqs == 0) return pa::ok();
+  if (pa_status s = device_out("pa_decode_attention_fp8(out)", out, &out)) return s;
   if (!k_scale || !v_scale || (reinterpret_cast<uintptr_t>(k_scale) & 3) ||
       (reinterpret_cast<uintptr_t>(v_scale) & 3))
     return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention_fp8: NULL or misaligned scales");
@@ -2418,6 +2429,7 @@ pa_status pa_decode_attention_shared_prefix(
                     "pa_decode_attention_shared_prefix: num_prefix_blocks %d not in [0, %d]",
                     num_prefix_blocks, max_blocks_per_seq);
   if (num_seqs == 0) return pa::ok();
+  if (pa_status s = device_out("pa_decode_attention_shared_prefix(out)", out, &out)) return s;
   if (num_prefix_blocks > 0 &&
       (!prefix_blocks || (reinterpret_cast<uintptr_t>(prefix_blocks) & 3)))
     return pa::fail(PA_ERR_INVALID_ARG,
@@ -2492,6 +2504,7 @@ pa_status pa_decode_attention_fixed_scratch(const pa_half* q, const pa_half* k_p
                                       &stride_bytes))
     return s;
   if (num_seqs == 0) return pa::ok();
+  if (pa_status s = device_out("pa_decode_attention_fixed_scratch(out)", out, &out)) return s;
   pa::DeviceInfo dev;
   if (pa_status s = pa::current_device(&dev)) return s;
   const int G = num_q_heads / num_kv_heads;

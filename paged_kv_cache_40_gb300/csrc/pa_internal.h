@@ -42,6 +42,11 @@ pa_status resolve_block_stride(const char* fn, int64_t stride, int64_t dense, in
 pa_status check_pools_disjoint(const char* fn, const void* k, const void* v, int num_blocks,
                                int64_t stride_bytes, int64_t block_bytes);
 
+// A pointer the device can dereference: device (or managed) memory as it is,
+// pinned host memory through its device mapping; pageable host memory is
+// refused (PA_ERR_INVALID_ARG, message naming `fn`).
+pa_status device_view(const char* fn, const void* p, void** out);
+
 // Properties of the current device used for launch shaping.
 struct DeviceInfo {
   int device = -1;

@@ -164,6 +164,46 @@ class DecodeBatchRunner:
     # sequences itself)
     ATTEND_LAUNCHES = 1
 
+    # -- host <-> device: one copy of the step's inputs ----------------------
+    def pack_inputs(self) -> None:
+        """Re-home the step's inputs (q, the new K/V rows, slots, copy pairs,
+        tables, lengths; call after plan_step) in one device buffer with a
+        pinned host mirror of the same layout (`host_inputs`), so that
+        upload_inputs() moves a step's inputs with a single host-to-device
+        copy."""
+        import torch
+        names = ["q", "k_new", "v_new", "d_slots", "d_table", "d_lens"]
+        if self.d_pairs is not None:
+            names.append("d_pairs")
+        offs, pos = [], 0
+        for n in names:
+            t = getattr(self, n)
+            offs.append(pos)
+            pos += (t.numel() * t.element_size() + 255) // 256 * 256
+        dev_arena = torch.empty(pos, dtype=torch.uint8, device=self.device)
+        host_arena = torch.empty(pos, dtype=torch.uint8).pin_memory()
+        self.host_inputs = {}
+        for n, off in zip(names, offs):
+            t = getattr(self, n)
+            nb = t.numel() * t.element_size()
+            dv = dev_arena[off:off + nb].view(t.dtype).view(t.shape)
+            dv.copy_(t)
+            hv = host_arena[off:off + nb].view(t.dtype).view(t.shape)
+            hv.copy_(t.cpu())
+            setattr(self, n, dv)
+            self.host_inputs[n] = hv
+        self.input_arena, self.host_arena = dev_arena, host_arena
+
+    def upload_inputs(self, stream=None) -> int:
+        """One host-to-device copy of the packed inputs; returns its bytes."""
+        import torch
+        if stream is None:
+            self.input_arena.copy_(self.host_arena, non_blocking=True)
+        else:
+            with torch.cuda.stream(stream):
+                self.input_arena.copy_(self.host_arena, non_blocking=True)
+        return int(self.host_arena.numel())
+
     def run_step(self, stream=None):
         """copy-on-write copies (if any), append, attend. Returns the kernel
         launch count."""

@@ -1,0 +1,148 @@
+"""Host-memory paths of a decode step on the GPU: the attention calls write
+their output straight into pinned host memory (through its device mapping),
+bit-equal to a device output, pageable host memory is refused before any
+launch, and a step whose inputs are packed into one buffer and uploaded with
+one copy gives the same pools and output as the unpacked step."""
+
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from tests.gpu_helpers import assert_close_attention, poison_unread_rows
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def pa(libpa):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return libpa
+
+
+def d(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _case(seed=3, BS=16):
+    rng = np.random.default_rng(seed)
+    lens = [1, 40, 300, 1000, 17]
+    S, Hkv, G, D = len(lens), 2, 4, 128
+    mb = max(-(-L // BS) for L in lens)
+    nb = sum(-(-L // BS) for L in lens) + 3
+    perm = rng.permutation(nb)
+    table = -np.ones((S, mb), np.int32)
+    pos = 0
+    for i, L in enumerate(lens):
+        n = -(-L // BS)
+        table[i, :n] = perm[pos:pos + n]
+        pos += n
+    q = rng.standard_normal((S, G * Hkv, D)).astype(np.float16)
+    kp = rng.standard_normal((nb, BS, Hkv, D)).astype(np.float16)
+    vp = rng.standard_normal((nb, BS, Hkv, D)).astype(np.float16)
+    kp, vp = poison_unread_rows(kp, vp, table, lens, BS)
+    return q, kp, vp, table, np.asarray(lens, np.int32)
+
+
+def test_output_into_pinned_host_memory(pa):
+    q, kp, vp, table, lens = _case()
+    args = (d(q), d(kp), d(vp), d(table), d(lens), 0.088)
+    dev = pa.pa_decode_attention(*args)
+    host = torch.empty(q.shape, dtype=torch.float16).pin_memory()
+    pa.pa_decode_attention(*args, out=host)
+    fixed_host = torch.empty(q.shape, dtype=torch.float16).pin_memory()
+    pa.pa_decode_attention_fixed_scratch(*args, out=fixed_host)
+    torch.cuda.synchronize()
+    assert torch.equal(host, dev.cpu())
+    assert torch.equal(fixed_host, dev.cpu())
+    exp = oracle.decode_attention(q, kp, vp, table, lens, np.float32(0.088))
+    assert_close_attention(host.numpy(), exp, "output in pinned host memory")
+
+
+def test_fp8_and_shared_prefix_outputs_into_pinned_host_memory(pa):
+    rng = np.random.default_rng(9)
+    q, kp, vp, table, lens = _case(seed=9)
+    k8 = synthetic.fp8_codes(rng, kp.shape)
+    v8 = synthetic.fp8_codes(rng, vp.shape)
+    ks = np.full(2, 0.01, np.float32)
+    vs = np.full(2, 0.02, np.float32)
+    a8 = (d(q), d(k8), d(v8), d(ks), d(vs), d(table), d(lens), 0.088)
+    dev8 = pa.pa_decode_attention_fp8(*a8)
+    host8 = torch.empty(q.shape, dtype=torch.float16).pin_memory()
+    pa.pa_decode_attention_fp8(*a8, out=host8)
+    # shared prefix: every table starts with the same two blocks
+    t2 = table.copy()
+    t2[:, :2] = table[3, :2]
+    lens2 = np.maximum(lens, 33).astype(np.int32)
+    for i in range(len(lens2)):
+        need = -(-int(lens2[i]) // 16)
+        for j in range(need):
+            if t2[i, j] < 0:
+                t2[i, j] = table[3, j]
+    prefix = d(t2[0, :2].copy())
+    ap = (d(q), d(kp), d(vp), prefix, d(t2), d(lens2), 0.088)
+    devp = pa.pa_decode_attention_shared_prefix(*ap)
+    hostp = torch.empty(q.shape, dtype=torch.float16).pin_memory()
+    pa.pa_decode_attention_shared_prefix(*ap, out=hostp)
+    torch.cuda.synchronize()
+    assert torch.equal(host8, dev8.cpu())
+    assert torch.equal(hostp, devp.cpu())
+
+
+def test_pageable_output_is_refused_before_launch(pa):
+    q, kp, vp, table, lens = _case()
+    host = torch.empty(q.shape, dtype=torch.float16)           # not pinned
+    with pytest.raises(ValueError):
+        pa.pa_decode_attention(d(q), d(kp), d(vp), d(table), d(lens), 0.1, out=host)
+    # the library refuses it too (the binding is not the only guard)
+    lib = pa.lib()
+    S, Hq, D = q.shape
+    nb, BS, Hkv, _ = kp.shape
+    dq, dk, dv, dt, dl = d(q), d(kp), d(vp), d(table), d(lens)
+    ws = pa.alloc_workspace(S, Hq, Hkv, D, BS, table.shape[1])
+    pageable = np.zeros(q.size, np.float16)
+    st = lib.pa_decode_attention(
+        ctypes.c_void_p(dq.data_ptr()), ctypes.c_void_p(dk.data_ptr()),
+        ctypes.c_void_p(dv.data_ptr()), ctypes.c_void_p(dt.data_ptr()),
+        ctypes.c_void_p(dl.data_ptr()), S, Hq, Hkv, D, BS, table.shape[1], nb, 0,
+        ctypes.c_float(0.1), ctypes.c_void_p(pageable.ctypes.data), ctypes.c_void_p(ws.data_ptr()),
+        ws.numel(), 0, None)
+    assert st == 1 and b"pinned" in lib.pa_last_error()
+
+
+def test_packed_inputs_step_matches_unpacked(pa):
+    """One decode step of the copy-on-write batch (127 copies) with its inputs
+    packed and uploaded in one copy, the output written to pinned host memory."""
+    from paged_kv_cache_40_gb300.engine import DecodeBatchRunner, SharedPrefixRunner
+    w = synthetic.config4_shared_prefix()
+    a = SharedPrefixRunner(w)
+    a.plan_step()
+    a.run_step()
+    b = SharedPrefixRunner(w)
+    b.plan_step()
+    b.pack_inputs()
+    host = torch.empty(b.out.shape, dtype=torch.float16).pin_memory()
+    b.out = host
+    assert b.upload_inputs() == b.host_arena.numel()
+    b.run_step()
+    torch.cuda.synchronize()
+    assert torch.equal(a.k_pool, b.k_pool) and torch.equal(a.v_pool, b.v_pool)
+    assert torch.equal(a.out.cpu(), host)
+    assert pa.pa_device_error() == 0
+    # the plain runner on the GQA batch, several uploads of the same step
+    g = synthetic.config2_gqa_batch(num_seqs=9, lo=1, hi=700)
+    r1 = DecodeBatchRunner(g)
+    r1.plan_step()
+    r1.run_step()
+    r2 = DecodeBatchRunner(g)
+    r2.plan_step()
+    r2.pack_inputs()
+    for _ in range(3):
+        r2.upload_inputs()
+        r2.run_step()
+    torch.cuda.synchronize()
+    assert torch.equal(r1.out, r2.out)
