@@ -183,24 +183,36 @@ def dist_setup(args):
     return world, rank, local
 
 
-def reduce_max(x: float, world: int) -> float:
+def _reduce(x: float, world: int, op: str) -> float:
+    """All-reduce one float over the ranks (on the GPU under NCCL, on the host
+    under gloo)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
     return float(t.item())
+
+
+def reduce_max(x: float, world: int) -> float:
+    return _reduce(x, world, "max")
 
 
 def reduce_sum(x: float, world: int) -> float:
-    if world == 1:
-        return x
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+    return _reduce(x, world, "sum")
+
+
+def aggregate(kv_bytes: int, tokens: int, steps: int, seconds: float, world: int):
+    """Whole-job throughput of a weakly scaled run: every rank processed its
+    own batch `steps` times in `seconds`; the job's time is the slowest
+    rank's, its work the sum over ranks. Returns (KV GB/s, tokens/s, job
+    seconds)."""
+    t = reduce_max(seconds, world)
+    kv = reduce_sum(float(kv_bytes) * steps, world)
+    tok = reduce_sum(float(tokens) * steps, world)
+    return kv / t / 1e9, tok / t, t
 
 
 def barrier(world: int):
@@ -512,11 +524,8 @@ def run_ours(args, world, rank, local):
 
     kvb = run.kv_bytes()
     tokens = int(plan.seq_lens.astype(np.int64).sum())
-    t_steps = reduce_max(sum(step_ms) / 1e3, world)
-    t_e2e = reduce_max(sum(e2e_ms) / 1e3, world)
-    all_kv = reduce_sum(kvb * K, world)
-    all_kv_e2e = reduce_sum(kvb * Ke, world)
-    all_tok = reduce_sum(tokens * K, world)
+    value, tok_per_s, t_steps = aggregate(kvb, tokens, K, sum(step_ms) / 1e3, world)
+    value_e2e, _, t_e2e = aggregate(kvb, tokens, Ke, sum(e2e_ms) / 1e3, world)
     attn_mean_s = statistics.mean(attn_ms) / 1e3
     peak, peak_kind = hbm_peak()
     achieved = run.io_bytes() / attn_mean_s / 1e9
@@ -531,7 +540,6 @@ def run_ours(args, world, rank, local):
                "tokens_per_s": round(r["tokens"] / r["seconds"], 1)}
     if rank != 0:
         return
-    value = all_kv / t_steps / 1e9
     config = describe(b, args.kv_dtype, plan.seq_lens)
     if args.layout == "records":
         config["pool_layout"] = ("one pool of per-block records (K rows then V rows), "
@@ -551,7 +559,7 @@ def run_ours(args, world, rank, local):
         "steps": K, "warmup": args.warmup, "ms_per_step": round(1e3 * t_steps / K, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic", "config": config,
-        "tokens_per_s": round(all_tok / t_steps, 1),
+        "tokens_per_s": round(tok_per_s, 1),
         "frac_of_hbm_peak": {"measured": round(value / peak, 4),
                              "nominal_8tbs": round(value / 8000.0, 4)},
         "attention_us": {"mean": round(1e6 * attn_mean_s, 3),
@@ -564,7 +572,7 @@ def run_ours(args, world, rank, local):
                      "peak_source": peak_kind,
                      "kernel": "paged_decode_kernel",
                      "bytes_per_launch": run.io_bytes()},
-        "e2e": {"value": round(all_kv_e2e / t_e2e / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(value_e2e, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(1e3 * t_e2e / Ke, 5), "steps": Ke,
                 "path": "inputs packed in one pinned host buffer, one host-to-device copy; the "
