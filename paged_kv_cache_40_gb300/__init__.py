@@ -5,12 +5,17 @@ has the C name, checks and marshals torch tensors (device pointers, sizes, the
 current CUDA stream) and calls the library. All device work runs in libpa's
 CUDA kernels; nothing here computes on the host, and there is no fallback.
 
-Device calls                      Host block manager
-  pa_append_kv                      BlockAllocator (pa_alloc_*)
-  pa_copy_blocks
-  pa_decode_attention
+Device calls                            Host block manager
+  pa_append_kv, pa_append_kv_fp8          BlockAllocator (pa_alloc_*), with
+  pa_copy_blocks, pa_copy_blocks_fp8      a host pool for swapping
+  pa_swap_blocks
+  pa_decode_attention (+ _fp8, _shared_prefix, _fixed_scratch)
   pa_decode_workspace_bytes / _init
   pa_device_error
+
+Pools are [num_blocks][block_size][kv_heads][head_dim] tensors, dense or the
+K and V member views of one record pool (kv_block_pool / kv_views); the block
+stride is read from the tensors. Attention outputs may be pinned host memory.
 """
 
 from __future__ import annotations
@@ -39,10 +44,7 @@ __all__ = [
     "pa_swap_blocks",
     "pa_decode_attention_fixed_scratch", "kv_block_pool", "kv_views",
     "pa_version", "BlockAllocator", "PaError", "OutOfBlocksError", "lib",
-    "DEFAULT_PARTITION_TOKENS",
 ]
-
-DEFAULT_PARTITION_TOKENS = 256
 
 
 def lib() -> ctypes.CDLL:
