@@ -1346,9 +1346,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 // contraction: S = Q K^T with Q the query rows of every sharing sequence
 // (rows (sequence, query head of the group), 128 per CTA) and K the prefix's
 // tokens, then O = P V. The prefix kernel runs it on the 5th-generation
-// tensor cores: Q, K, V and P sit in shared memory as 128-byte-swizzled
-// operand tiles, S and O accumulate in tensor memory (TMEM), one thread
-// issues the MMAs, one warp streams K/V tiles with TMA, and four warps (one
+// tensor cores: Q, K and V sit in shared memory as 128-byte-swizzled operand
+// tiles, S and O accumulate in tensor memory (TMEM) and P is written over
+// its S in TMEM, whence the PV MMA reads it; one thread issues each kind of
+// MMA, a warp each streams the K and V tiles with TMA, and four warps (one
 // TMEM lane quarter each, one query row per thread) run the softmax. The
 // prefix's tokens are split into chunks across CTAs and each chunk into
 // sub-chunks of up to 128 tokens; a row's online softmax runs over its
@@ -1364,11 +1365,14 @@ constexpr int kPfxWarpS = 5;                    // S = Q K^T issuer; owns the TM
 constexpr int kPfxWarpPV = 6;                   // O = P V issuer
 constexpr int kPfxWarpV = 7;                    // TMA of V tiles
 constexpr int kPfxThreads = 8 * 32;
-constexpr int kPfxStages = 2;                   // K and V tiles in flight
+constexpr int kPfxKStages = 3;                  // K tiles in flight (S runs ahead)
+constexpr int kPfxVStages = 3;                  // V tiles in flight
 constexpr int kMaxPfxChunks = 32;
-constexpr int kPfxTmemCols = 512;               // S[2] and O[2], 128 fp32 columns each
+constexpr int kPfxTmemCols = 512;               // S[2] (P over S) and O[2], 128 columns each
 constexpr int kPfxTile = kPfxTok * 256;         // one operand tile: 128 rows x 128 fp16
-constexpr int kPfxSmem = 1024 + 256 + (3 + 2 * kPfxStages) * kPfxTile;  // Q, P[2], K, V
+// barriers, then the 1024-aligned tiles Q, K[stages], V[stages]
+constexpr int kPfxHead = 256;
+constexpr int kPfxSmem = 1024 + kPfxHead + (1 + kPfxKStages + kPfxVStages) * kPfxTile;
 
 struct PrefixParams {
   const __half* q;
@@ -1407,6 +1411,15 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
+// The same MMA with A read from tensor memory: row i of A in lane i, two
+// fp16 values per 32-bit column (the lower K index in the low half).
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
+}
 // Arrive on `bar` once every MMA this thread issued so far has completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -1434,6 +1447,23 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 16 / 8 consecutive 32-bit columns of this thread's TMEM lane; returns after
+// the store has completed.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};\n\ttcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   asm volatile(
@@ -1460,26 +1490,28 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
   constexpr int RS = rec_floats(G, D);
   static_assert(kPfxTok % BS == 0 && BS % 16 == 0, "sub-chunks are whole blocks of 16-token boxes");
   extern __shared__ __align__(1024) unsigned char psm[];
-  // barriers and flags, then 1024-aligned tiles: Q, P[2], K[stages], V[stages]
+  // barriers and flags, then 1024-aligned tiles: Q, K[NK], V[NV]
+  constexpr int NK = kPfxKStages, NV = kPfxVStages;
   uint64_t* bars = reinterpret_cast<uint64_t*>(psm);
-  uint64_t* k_full = bars;                     // [stages] TMA -> S issuer
-  uint64_t* v_full = bars + 2;                 // [stages] TMA -> PV issuer
-  uint64_t* k_empty = bars + 4;                // [stages] S MMAs done with a K tile
-  uint64_t* v_empty = bars + 6;                // [stages] PV MMAs done with a V tile
-  uint64_t* s_full = bars + 8;                 // [2] S buffer written
-  uint64_t* s_free = bars + 10;                // [2] S buffer read by the softmax warps
-  uint64_t* p_full = bars + 12;                // [2] P buffer written
-  uint64_t* o_full = bars + 14;                // [2] O buffer written (and its P buffer read)
-  uint64_t* o_free = bars + 16;                // [2] O buffer read by the softmax warps
-  uint64_t* mma_done = bars + 18;              // [2] every MMA of an issuer completed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+  uint64_t* k_full = bars;                     // [NK] TMA -> S issuer
+  uint64_t* k_empty = bars + NK;               // [NK] S MMAs done with a K tile
+  uint64_t* v_full = bars + 2 * NK;            // [NV] TMA -> PV issuer
+  uint64_t* v_empty = bars + 2 * NK + NV;      // [NV] PV MMAs done with a V tile
+  uint64_t* s_full = bars + 2 * NK + 2 * NV;   // [2] S buffer written
+  uint64_t* s_free = s_full + 2;               // [2] PV MMAs done with the P written over S
+  uint64_t* p_full = s_full + 4;               // [2] P written (4 softmax warps)
+  uint64_t* o_full = s_full + 6;               // [2] O buffer written
+  uint64_t* o_free = s_full + 8;               // [2] O buffer read (4 softmax warps)
+  uint64_t* mma_done = s_full + 10;            // [2] every MMA of an issuer completed
+  constexpr int kBars = 2 * NK + 2 * NV + 12;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  static_assert(kBars * 8 + 8 <= 256, "barriers fit below the tiles");
   const uint32_t sbase = smem_addr(psm);
-  unsigned char* tiles = psm + (((sbase + 256 + 1023u) & ~1023u) - sbase);
+  unsigned char* tiles = psm + (((sbase + kPfxHead + 1023u) & ~1023u) - sbase);
   unsigned char* q_s = tiles;
-  unsigned char* p_s = tiles + kPfxTile;                       // [2]
-  unsigned char* k_s = tiles + 3 * kPfxTile;                   // [stages]
-  unsigned char* v_s = tiles + (3 + kPfxStages) * kPfxTile;    // [stages]
+  unsigned char* k_s = tiles + kPfxTile;                       // [NK]
+  unsigned char* v_s = tiles + (1 + NK) * kPfxTile;            // [NV]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kvh = blockIdx.y, c = blockIdx.z;
@@ -1490,11 +1522,13 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
   auto sub_len = [&](int t) { return min(kPfxTok, tok_hi - (tok_lo + t * kPfxTok)); };
 
   if (threadIdx.x == 0) {
-    // s_free, p_full and o_free count the four softmax warps; the others one
-    // arrival (a TMA transaction count or an MMA commit)
-    for (int i = 0; i < 20; ++i)
-      mbar_init(smem_addr(&bars[i]),
-                (i >= 10 && i < 14) || (i >= 16 && i < 18) ? kPfxSoftmaxWarps : 1);
+    // p_full and o_free count the four softmax warps; the others one arrival
+    // (a TMA transaction count or an MMA commit)
+    for (int i = 0; i < kBars; ++i) {
+      const uint64_t* b = &bars[i];
+      const bool softmax = (b >= p_full && b < p_full + 2) || (b >= o_free && b < o_free + 2);
+      mbar_init(smem_addr(&bars[i]), softmax ? kPfxSoftmaxWarps : 1);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -1554,6 +1588,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
     const CUtensorMap* map = is_k ? &kmap : &vmap;
     uint64_t* full = is_k ? k_full : v_full;
     uint64_t* empty = is_k ? k_empty : v_empty;
+    const int nst = is_k ? NK : NV;
     unsigned char* ring = is_k ? k_s : v_s;
     // block ids of a sub-chunk: one per lane, all loaded at once; the next
     // sub-chunk's are in flight while this one's copies are issued
@@ -1571,10 +1606,10 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
     };
     int next_ids = nsub > 0 ? load_ids(0) : 0;
     for (int t = 0; t < nsub; ++t, ++issued) {
-      const int st = t % kPfxStages, n = sub_len(t);
+      const int st = t % nst, n = sub_len(t);
       const int ids = next_ids;
-      if (t >= kPfxStages &&
-          !warp_wait_phase(smem_addr(&empty[st]), ((t / kPfxStages) - 1) & 1, abort_flag, p.err))
+      if (t >= nst &&
+          !warp_wait_phase(smem_addr(&empty[st]), ((t / nst) - 1) & 1, abort_flag, p.err))
         break;
       const uint32_t dst = smem_addr(ring + st * kPfxTile), bar = smem_addr(&full[st]);
       if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n) * 256u);
@@ -1594,9 +1629,9 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
     }
     if (*abort_flag) {
       // the last copies issued into each stage land before the CTA exits
-      for (int t = issued > kPfxStages ? issued - kPfxStages : 0; t < issued; ++t) {
+      for (int t = issued > nst ? issued - nst : 0; t < issued; ++t) {
         const unsigned long long w0 = global_ns();
-        while (!mbar_try_wait(smem_addr(&full[t % kPfxStages]), (t / kPfxStages) & 1) &&
+        while (!mbar_try_wait(smem_addr(&full[t % nst]), (t / nst) & 1) &&
                global_ns() - w0 < kWaitLimitNs) {
         }
       }
@@ -1605,8 +1640,8 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
     // ---- S issuer: S_t = Q K_t^T into TMEM buffer t % 2 ----
     const uint32_t qa = smem_addr(q_s);
     for (int t = 0; t < nsub; ++t) {
-      const int st = t % kPfxStages, b = t & 1;
-      if (!warp_wait_phase(smem_addr(&k_full[st]), (t / kPfxStages) & 1, abort_flag, p.err)) break;
+      const int st = t % NK, b = t & 1;
+      if (!warp_wait_phase(smem_addr(&k_full[st]), (t / NK) & 1, abort_flag, p.err)) break;
       if (t >= 2 && !warp_wait_phase(smem_addr(&s_free[b]), ((t - 2) >> 1) & 1, abort_flag, p.err))
         break;
       tc_fence_after();
@@ -1632,22 +1667,23 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
   } else if (warp == kPfxWarpPV) {
     // ---- PV issuer: O_t = P_t V_t into TMEM buffer 2 + t % 2 ----
     for (int t = 0; t < nsub; ++t) {
-      const int st = t % kPfxStages, b = t & 1;
+      const int st = t % NV, b = t & 1;
       if (!warp_wait_phase(smem_addr(&p_full[b]), (t >> 1) & 1, abort_flag, p.err)) break;
-      if (!warp_wait_phase(smem_addr(&v_full[st]), (t / kPfxStages) & 1, abort_flag, p.err)) break;
+      if (!warp_wait_phase(smem_addr(&v_full[st]), (t / NV) & 1, abort_flag, p.err)) break;
       if (t >= 2 && !warp_wait_phase(smem_addr(&o_free[b]), ((t - 2) >> 1) & 1, abort_flag, p.err))
         break;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t pa = smem_addr(p_s + b * kPfxTile);
         const uint32_t vb = smem_addr(v_s + st * kPfxTile);
         const uint32_t id = f16_idesc(D, true);
         const int n = sub_len(t);
+        // A = P over S buffer b: 16 tokens per MMA, 8 TMEM columns
         for (int k = 0; k < n / 16; ++k)
-          tc_mma(tmem + (2 + b) * kPfxTok, sw128_desc(pa + (k >> 2) * HALF + (k & 3) * 32, 16, 1024),
-                 sw128_desc(vb + k * 2048, HALF, 1024), id, k > 0);
+          tc_mma_ts(tmem + (2 + b) * kPfxTok, tmem + b * kPfxTok + 8 * k,
+                    sw128_desc(vb + k * 2048, HALF, 1024), id, k > 0);
         tc_commit(smem_addr(&o_full[b]));
         tc_commit(smem_addr(&v_empty[st]));
+        tc_commit(smem_addr(&s_free[b]));
       }
       __syncwarp();
     }
@@ -1705,43 +1741,38 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
       const float alpha = fast_exp2(m - mn);
       m = mn;
       float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-      unsigned char* prow = p_s + b * kPfxTile + r * 128;
-      // P = exp2(S * qscale - m) as fp16, 16 tokens (two 16-byte chunks) at a time
-      auto emit16 = [&](const float* v, int col) {
-        uint32_t h[8];
+      // P = exp2(S * qscale - m) as fp16 pairs, written over the S columns
+      // already read: tokens c0 .. c0+2k-1 go to columns c0/2 .. c0/2+k-1
+      auto emit = [&](const float* v, uint32_t* h, int cnt) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float e0 = fast_exp2(fmaf(v[2 * i], p.qscale, -mn));
-          const float e1 = fast_exp2(fmaf(v[2 * i + 1], p.qscale, -mn));
-          sum4[(2 * i) & 3] += e0;
-          sum4[(2 * i + 1) & 3] += e1;
-          h[i] = pack_half2(e0, e1);
+        for (int i = 0; i < 16; ++i) {
+          if (i < cnt) {
+            const float e0 = fast_exp2(fmaf(v[2 * i], p.qscale, -mn));
+            const float e1 = fast_exp2(fmaf(v[2 * i + 1], p.qscale, -mn));
+            sum4[(2 * i) & 3] += e0;
+            sum4[(2 * i + 1) & 3] += e1;
+            h[i] = pack_half2(e0, e1);
+          }
         }
-        const int ch = (col & 63) >> 3;
-        unsigned char* dst = prow + (col >> 6) * HALF;
-        *reinterpret_cast<uint4*>(dst + ((ch ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(dst + (((ch + 1) ^ (r & 7)) << 4)) =
-            make_uint4(h[4], h[5], h[6], h[7]);
       };
       for (c0 = 0; c0 + 32 <= n; c0 += 32) {
         float v[32];
         tmem_ld32(sa + c0, v);
-        emit16(v, c0);
-        emit16(v + 16, c0 + 16);
+        uint32_t h[16];
+        emit(v, h, 16);
+        tmem_st16(sa + c0 / 2, h);
       }
       if (c0 < n) {
         float v[16];
         tmem_ld16(sa + c0, v);
-        emit16(v, c0);
+        uint32_t h[16];
+        emit(v, h, 8);
+        tmem_st8(sa + c0 / 2, h);
       }
       l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_addr(&s_free[b]));
-        mbar_arrive(smem_addr(&p_full[b]));
-      }
+      if (lane == 0) mbar_arrive(smem_addr(&p_full[b]));
       // O of the previous sub-chunk, folded while the tensor cores run this one's
       if (t > 0) ok = fold(t - 1, alpha_prev);
       alpha_prev = alpha;
@@ -1749,8 +1780,8 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
     if (ok && nsub > 0) ok = fold(nsub - 1, alpha_prev);
     // ---- the chunk's partial records of this warp's 32 rows ----
     // Every MMA has completed (the last O was folded), so the K tiles are
-    // free: each warp stages its rows there (16 KB, rows padded to 132 floats
-    // against bank conflicts) and writes each sequence's G rows as one
+    // free: each warp stages its rows there (16.5 KB, rows padded to 132
+    // floats against bank conflicts) and writes each sequence's G rows as one
     // contiguous run, 512 bytes per store instruction.
     constexpr int kPad = D + 4;
     float* stage = reinterpret_cast<float*>(k_s) + warp * 32 * kPad;
