@@ -29,6 +29,11 @@ def _decode(lib, **kw):
     (dict(NB=0), 1),
     (dict(scale=float("inf")), 1),
     (dict(), 1),                      # NULL pointers
+    # the largest batch's block stream must keep 32-bit positions:
+    # 16384 sequences x 1 head group x 131072 blocks = 2^31
+    (dict(S=16384, Hq=8, Hkv=8, MB=131072), 4),
+    # one-block chunks of a 2^20-block sequence overflow a counter word's arrivals
+    (dict(S=1, Hq=8, Hkv=8, MB=1 << 20, pt=16), 4),
 ])
 def test_decode_rejects(libpa, kw, status):
     lib = libpa.lib()
