@@ -32,8 +32,15 @@
  *     k_pool = kv, v_pool = kv + E and pool_block_stride = 2*E. A stride must
  *     be at least E values and a multiple of 16 bytes. Calls that write the
  *     pools refuse a K and a V pool whose blocks overlap.
- *   - Device pointers are owned by the caller (the library never allocates or
- *     frees device memory) and must be 16-byte aligned. Device calls are
+ *   - Memory is owned by the caller (the library never allocates or frees
+ *     device memory); array pointers must be 16-byte aligned (index arrays
+ *     4-byte). Pools and workspaces must be device memory. The arrays a call
+ *     reads or writes in place (q, new K/V rows, slot mappings, copy pairs,
+ *     block tables, lengths, scales, prefix block lists, outputs) may instead
+ *     be pinned (page-locked) host memory, which the kernels then access
+ *     through its device mapping over the CPU-GPU link, with no copy call;
+ *     pageable host memory is refused with PA_ERR_INVALID_ARG before any
+ *     launch. Device calls are
  *     asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
  *     stream): arguments are checked on the host before any launch, and a
  *     PA_OK return means "launched", not "finished".

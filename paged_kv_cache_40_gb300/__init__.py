@@ -69,12 +69,16 @@ def _stream_ptr(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(handle)
 
 
-def _dev(t, name, dtype, ndim=None):
+def _dev(t, name, dtype, ndim=None, host_ok=False):
+    """Pointer of a contiguous tensor the kernels use: a CUDA tensor, or (for
+    the arrays a call reads or writes in place, host_ok) pinned host memory,
+    which the kernels reach through its device mapping."""
     torch = _torch()
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor (libpa has no host path)")
+    if not t.is_cuda and not (host_ok and t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor" +
+                         (" or pinned host memory" if host_ok else ""))
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -82,6 +86,10 @@ def _dev(t, name, dtype, ndim=None):
     if ndim is not None and t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
     return ctypes.c_void_p(t.data_ptr())
+
+
+def _in(t, name, dtype):
+    return _dev(t, name, dtype, host_ok=True)
 
 
 def _out(t, like):
@@ -160,9 +168,9 @@ def pa_append_kv(k_new, v_new, k_pool, v_pool, slot_mapping, stream=None) -> Non
     T = int(slot_mapping.numel())
     if tuple(k_new.shape) != (T, hkv, d) or tuple(v_new.shape) != (T, hkv, d):
         raise ValueError("k_new/v_new must be [num_tokens][kv_heads][head_dim]")
-    args = (_dev(k_new, "k_new", torch.float16), _dev(v_new, "v_new", torch.float16),
+    args = (_in(k_new, "k_new", torch.float16), _in(v_new, "v_new", torch.float16),
             _pool(k_pool, "k_pool", torch.float16), _pool(v_pool, "v_pool", torch.float16),
-            _dev(slot_mapping, "slot_mapping", torch.int32))
+            _in(slot_mapping, "slot_mapping", torch.int32))
     _check(_load().pa_append_kv(*args, T, hkv, d, bs, nb, stride, _stream_ptr(stream)))
 
 
@@ -175,7 +183,7 @@ def pa_copy_blocks(k_pool, v_pool, pairs, stream=None) -> None:
         raise ValueError("pairs must be [n][2]")
     n = int(pairs.shape[0])
     args = (_pool(k_pool, "k_pool", torch.float16), _pool(v_pool, "v_pool", torch.float16),
-            _dev(pairs, "pairs", torch.int32))
+            _in(pairs, "pairs", torch.int32))
     _check(_load().pa_copy_blocks(*args, n, hkv, d, bs, nb, stride, _stream_ptr(stream)))
 
 
@@ -220,12 +228,12 @@ def pa_decode_attention(q, k_pool, v_pool, block_table, seq_lens, scale, out=Non
     if tuple(seq_lens.shape) != (S,):
         raise ValueError("seq_lens must be [num_seqs]")
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=torch.float16, device=k_pool.device)
     if workspace is None:
-        workspace = alloc_workspace(S, hq, hkv, d, bs, mb, partition_tokens, q.device)
-    args = (_dev(q, "q", torch.float16), _pool(k_pool, "k_pool", torch.float16),
-            _pool(v_pool, "v_pool", torch.float16), _dev(block_table, "block_table", torch.int32),
-            _dev(seq_lens, "seq_lens", torch.int32))
+        workspace = alloc_workspace(S, hq, hkv, d, bs, mb, partition_tokens, k_pool.device)
+    args = (_in(q, "q", torch.float16), _pool(k_pool, "k_pool", torch.float16),
+            _pool(v_pool, "v_pool", torch.float16), _in(block_table, "block_table", torch.int32),
+            _in(seq_lens, "seq_lens", torch.int32))
     _check(_load().pa_decode_attention(
         *args, S, hq, hkv, d, bs, mb, nb, stride, ctypes.c_float(float(scale)),
         _out(out, q), _dev(workspace, "workspace", torch.uint8),
@@ -314,15 +322,15 @@ def pa_decode_attention_shared_prefix(q, k_pool, v_pool, prefix_blocks, block_ta
         raise ValueError("seq_lens must be [num_seqs] and prefix_blocks one-dimensional")
     P = int(prefix_blocks.numel())
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=torch.float16, device=k_pool.device)
     if workspace is None:
         n = pa_decode_shared_prefix_workspace_bytes(S, hq, hkv, d, bs, mb, P)
-        workspace = torch.zeros(max(n, 16), dtype=torch.uint8, device=q.device)
-    args = (_dev(q, "q", torch.float16), _pool(k_pool, "k_pool", torch.float16),
+        workspace = torch.zeros(max(n, 16), dtype=torch.uint8, device=k_pool.device)
+    args = (_in(q, "q", torch.float16), _pool(k_pool, "k_pool", torch.float16),
             _pool(v_pool, "v_pool", torch.float16),
-            _dev(prefix_blocks, "prefix_blocks", torch.int32) if P else ctypes.c_void_p(0), P,
-            _dev(block_table, "block_table", torch.int32),
-            _dev(seq_lens, "seq_lens", torch.int32))
+            _in(prefix_blocks, "prefix_blocks", torch.int32) if P else ctypes.c_void_p(0), P,
+            _in(block_table, "block_table", torch.int32),
+            _in(seq_lens, "seq_lens", torch.int32))
     _check(_load().pa_decode_attention_shared_prefix(
         *args, S, hq, hkv, d, bs, mb, nb, stride, ctypes.c_float(float(scale)),
         _out(out, q), _dev(workspace, "workspace", torch.uint8),
@@ -335,7 +343,7 @@ def _scales(k_scale, v_scale, hkv):
     torch = _torch()
     if tuple(k_scale.shape) != (hkv,) or tuple(v_scale.shape) != (hkv,):
         raise ValueError("k_scale and v_scale must be [num_kv_heads] fp32")
-    return _dev(k_scale, "k_scale", torch.float32), _dev(v_scale, "v_scale", torch.float32)
+    return _in(k_scale, "k_scale", torch.float32), _in(v_scale, "v_scale", torch.float32)
 
 
 def pa_append_kv_fp8(k_new, v_new, k_pool, v_pool, slot_mapping, k_scale, v_scale,
@@ -349,9 +357,9 @@ def pa_append_kv_fp8(k_new, v_new, k_pool, v_pool, slot_mapping, k_scale, v_scal
     if tuple(k_new.shape) != (T, hkv, d) or tuple(v_new.shape) != (T, hkv, d):
         raise ValueError("k_new/v_new must be [num_tokens][kv_heads][head_dim]")
     ks, vs = _scales(k_scale, v_scale, hkv)
-    args = (_dev(k_new, "k_new", torch.float16), _dev(v_new, "v_new", torch.float16),
+    args = (_in(k_new, "k_new", torch.float16), _in(v_new, "v_new", torch.float16),
             _pool(k_pool, "k_pool", torch.uint8), _pool(v_pool, "v_pool", torch.uint8),
-            _dev(slot_mapping, "slot_mapping", torch.int32), ks, vs)
+            _in(slot_mapping, "slot_mapping", torch.int32), ks, vs)
     _check(_load().pa_append_kv_fp8(*args, T, hkv, d, bs, nb, stride, _stream_ptr(stream)))
 
 
@@ -363,7 +371,7 @@ def pa_copy_blocks_fp8(k_pool, v_pool, pairs, stream=None) -> None:
         raise ValueError("pairs must be [n][2]")
     n = int(pairs.shape[0])
     args = (_pool(k_pool, "k_pool", torch.uint8), _pool(v_pool, "v_pool", torch.uint8),
-            _dev(pairs, "pairs", torch.int32))
+            _in(pairs, "pairs", torch.int32))
     _check(_load().pa_copy_blocks_fp8(*args, n, hkv, d, bs, nb, stride, _stream_ptr(stream)))
 
 
@@ -382,14 +390,14 @@ def pa_decode_attention_fp8(q, k_pool, v_pool, k_scale, v_scale, block_table, se
     if tuple(seq_lens.shape) != (S,):
         raise ValueError("seq_lens must be [num_seqs]")
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=torch.float16, device=k_pool.device)
     if workspace is None:
-        workspace = alloc_workspace(S, hq, hkv, d, bs, mb, partition_tokens, q.device)
+        workspace = alloc_workspace(S, hq, hkv, d, bs, mb, partition_tokens, k_pool.device)
     ks, vs = _scales(k_scale, v_scale, hkv)
-    args = (_dev(q, "q", torch.float16), _pool(k_pool, "k_pool", torch.uint8),
+    args = (_in(q, "q", torch.float16), _pool(k_pool, "k_pool", torch.uint8),
             _pool(v_pool, "v_pool", torch.uint8), ks, vs,
-            _dev(block_table, "block_table", torch.int32),
-            _dev(seq_lens, "seq_lens", torch.int32))
+            _in(block_table, "block_table", torch.int32),
+            _in(seq_lens, "seq_lens", torch.int32))
     _check(_load().pa_decode_attention_fp8(
         *args, S, hq, hkv, d, bs, mb, nb, stride, ctypes.c_float(float(scale)),
         _out(out, q), _dev(workspace, "workspace", torch.uint8),
@@ -418,10 +426,10 @@ def pa_decode_attention_fixed_scratch(q, k_pool, v_pool, block_table, seq_lens, 
     if tuple(seq_lens.shape) != (S,):
         raise ValueError("seq_lens must be [num_seqs]")
     if out is None:
-        out = torch.empty_like(q)
-    args = (_dev(q, "q", torch.float16), _pool(k_pool, "k_pool", torch.float16),
-            _pool(v_pool, "v_pool", torch.float16), _dev(block_table, "block_table", torch.int32),
-            _dev(seq_lens, "seq_lens", torch.int32))
+        out = torch.empty(q.shape, dtype=torch.float16, device=k_pool.device)
+    args = (_in(q, "q", torch.float16), _pool(k_pool, "k_pool", torch.float16),
+            _pool(v_pool, "v_pool", torch.float16), _in(block_table, "block_table", torch.int32),
+            _in(seq_lens, "seq_lens", torch.int32))
     _check(_load().pa_decode_attention_fixed_scratch(
         *args, S, hq, hkv, d, bs, int(block_table.shape[1]), nb, stride,
         ctypes.c_float(float(scale)),

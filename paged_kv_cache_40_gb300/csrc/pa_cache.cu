@@ -284,6 +284,10 @@ pa_status pa_append_kv(const pa_half* k_new, const pa_half* v_new, pa_half* k_po
   if (pa_status s = writer_stride("pa_append_kv", k_pool, v_pool, num_kv_heads, head_dim,
                                   block_size, num_blocks, pool_block_stride, 2, &stride))
     return s;
+  if (pa_status s = pa::device_only("pa_append_kv(k_pool)", k_pool)) return s;
+  if (pa_status s = pa::device_in("pa_append_kv(k_new)", k_new)) return s;
+  if (pa_status s = pa::device_in("pa_append_kv(v_new)", v_new)) return s;
+  if (pa_status s = pa::device_in("pa_append_kv(slot_mapping)", slot_mapping)) return s;
   pa::DeviceInfo dev;
   if (pa_status s = pa::current_device(&dev)) return s;
   int32_t* err = pa::device_error_word();
@@ -329,6 +333,8 @@ pa_status pa_copy_blocks(pa_half* k_pool, pa_half* v_pool, const int32_t* pairs,
   if (pa_status s = writer_stride("pa_copy_blocks", k_pool, v_pool, num_kv_heads, head_dim,
                                   block_size, num_blocks, pool_block_stride, 2, &stride))
     return s;
+  if (pa_status s = pa::device_only("pa_copy_blocks(k_pool)", k_pool)) return s;
+  if (pa_status s = pa::device_in("pa_copy_blocks(pairs)", pairs)) return s;
   pa::DeviceInfo dev;
   if (pa_status s = pa::current_device(&dev)) return s;
   int32_t* err = pa::device_error_word();
@@ -367,6 +373,12 @@ pa_status pa_append_kv_fp8(const pa_half* k_new, const pa_half* v_new, uint8_t* 
   if (pa_status s = writer_stride("pa_append_kv_fp8", k_pool, v_pool, num_kv_heads, head_dim,
                                   block_size, num_blocks, pool_block_stride, 1, &stride))
     return s;
+  if (pa_status s = pa::device_only("pa_append_kv_fp8(k_pool)", k_pool)) return s;
+  if (pa_status s = pa::device_in("pa_append_kv_fp8(k_new)", k_new)) return s;
+  if (pa_status s = pa::device_in("pa_append_kv_fp8(v_new)", v_new)) return s;
+  if (pa_status s = pa::device_in("pa_append_kv_fp8(slot_mapping)", slot_mapping)) return s;
+  if (pa_status s = pa::device_in("pa_append_kv_fp8(k_scale)", k_scale)) return s;
+  if (pa_status s = pa::device_in("pa_append_kv_fp8(v_scale)", v_scale)) return s;
   pa::DeviceInfo dev;
   if (pa_status s = pa::current_device(&dev)) return s;
   int32_t* err = pa::device_error_word();
@@ -414,6 +426,8 @@ pa_status pa_copy_blocks_fp8(uint8_t* k_pool, uint8_t* v_pool, const int32_t* pa
   if (pa_status s = writer_stride("pa_copy_blocks_fp8", k_pool, v_pool, num_kv_heads, head_dim,
                                   block_size, num_blocks, pool_block_stride, 1, &stride))
     return s;
+  if (pa_status s = pa::device_only("pa_copy_blocks_fp8(k_pool)", k_pool)) return s;
+  if (pa_status s = pa::device_in("pa_copy_blocks_fp8(pairs)", pairs)) return s;
   pa::DeviceInfo dev;
   if (pa_status s = pa::current_device(&dev)) return s;
   int32_t* err = pa::device_error_word();
@@ -452,6 +466,14 @@ pa_status device_view(const char* fn, const void* p, void** out) {
     return PA_OK;
   }
   return pa::fail(PA_ERR_INVALID_ARG, "%s: host memory must be pinned (page-locked)", fn);
+}
+
+pa_status device_only(const char* fn, const void* p) {
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) return pa::cuda_fail(e, fn);
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return PA_OK;
+  return pa::fail(PA_ERR_INVALID_ARG, "%s: must be device memory", fn);
 }
 
 }  // namespace pa

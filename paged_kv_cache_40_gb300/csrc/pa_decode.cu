@@ -2292,13 +2292,19 @@ static pa_status check_decode_call(const char* fn, const pa_half* q, const pa_ha
   return PA_OK;
 }
 
-// The output may be device memory or pinned host memory, which the kernels
-// then write through its device mapping (zero-copy over the CPU-GPU link).
-static pa_status device_out(const char* fn, pa_half* out, pa_half** dev_out) {
-  void* d = nullptr;
-  if (pa_status s = pa::device_view(fn, out, &d)) return s;
-  *dev_out = static_cast<pa_half*>(d);
-  return PA_OK;
+// q, the table, the lengths and the output may be device memory or pinned
+// host memory, which the kernels then read and write through its device
+// mapping (zero-copy over the CPU-GPU link); the pools must be device memory
+// (the kernels reach them through TMA).
+static pa_status resolve_io(const char* fn, const pa_half*& q, const void* k_pool,
+                            const void* v_pool, const int32_t*& block_table,
+                            const int32_t*& seq_lens, pa_half*& out) {
+  if (pa_status s = pa::device_only(fn, k_pool)) return s;
+  if (pa_status s = pa::device_only(fn, v_pool)) return s;
+  if (pa_status s = pa::device_in(fn, q)) return s;
+  if (pa_status s = pa::device_in(fn, block_table)) return s;
+  if (pa_status s = pa::device_in(fn, seq_lens)) return s;
+  return pa::device_in(fn, out);
 }
 
 static DecodeParams make_params(const pa_half* q, const pa_half* k_pool, const pa_half* v_pool,
@@ -2351,7 +2357,12 @@ pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool, const pa_
                                       &stride_bytes))
     return s;
   if (num_seqs == 0) return pa::ok();
-  if (pa_status s = device_out("pa_decode_attention(out)", out, &out)) return s;
+  if (pa_status s = resolve_io("pa_decode_attention", q, k_pool, v_pool, block_table, seq_lens,
+                               out))
+    return s;
+  if (workspace) {
+    if (pa_status s = pa::device_only("pa_decode_attention(workspace)", workspace)) return s;
+  }
   if (!workspace) return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention: NULL workspace");
   if (!pa::aligned16(workspace))
     return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention: misaligned workspace");
@@ -2397,7 +2408,14 @@ pa_status pa_decode_attention_fp8(const pa_half* q, const uint8_t* k_pool, const
                     "pa_decode_attention_fp8: head_dim %d / block_size %d (fp8 pools support "
                     "head_dim 128 and block_size 16 or 32)", head_dim, block_size);
   if (num_seqs == 0) return pa::ok();
-  if (pa_status s = device_out("pa_decode_attention_fp8(out)", out, &out)) return s;
+  if (pa_status s = resolve_io("pa_decode_attention_fp8", q, k_pool, v_pool, block_table,
+                               seq_lens, out))
+    return s;
+  if (pa_status s = pa::device_in("pa_decode_attention_fp8(k_scale)", k_scale)) return s;
+  if (workspace) {
+    if (pa_status s = pa::device_only("pa_decode_attention_fp8(workspace)", workspace)) return s;
+  }
+  if (pa_status s = pa::device_in("pa_decode_attention_fp8(v_scale)", v_scale)) return s;
   if (!k_scale || !v_scale || (reinterpret_cast<uintptr_t>(k_scale) & 3) ||
       (reinterpret_cast<uintptr_t>(v_scale) & 3))
     return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_attention_fp8: NULL or misaligned scales");
@@ -2460,7 +2478,16 @@ pa_status pa_decode_attention_shared_prefix(
                     "pa_decode_attention_shared_prefix: num_prefix_blocks %d not in [0, %d]",
                     num_prefix_blocks, max_blocks_per_seq);
   if (num_seqs == 0) return pa::ok();
-  if (pa_status s = device_out("pa_decode_attention_shared_prefix(out)", out, &out)) return s;
+  if (pa_status s = resolve_io("pa_decode_attention_shared_prefix", q, k_pool, v_pool,
+                               block_table, seq_lens, out))
+    return s;
+  if (pa_status s = pa::device_in("pa_decode_attention_shared_prefix(prefix_blocks)",
+                                  prefix_blocks))
+    return s;
+  if (workspace) {
+    if (pa_status s = pa::device_only("pa_decode_attention_shared_prefix(workspace)", workspace))
+      return s;
+  }
   if (num_prefix_blocks > 0 &&
       (!prefix_blocks || (reinterpret_cast<uintptr_t>(prefix_blocks) & 3)))
     return pa::fail(PA_ERR_INVALID_ARG,
@@ -2535,7 +2562,9 @@ pa_status pa_decode_attention_fixed_scratch(const pa_half* q, const pa_half* k_p
                                       &stride_bytes))
     return s;
   if (num_seqs == 0) return pa::ok();
-  if (pa_status s = device_out("pa_decode_attention_fixed_scratch(out)", out, &out)) return s;
+  if (pa_status s = resolve_io("pa_decode_attention_fixed_scratch", q, k_pool, v_pool,
+                               block_table, seq_lens, out))
+    return s;
   pa::DeviceInfo dev;
   if (pa_status s = pa::current_device(&dev)) return s;
   const int G = num_q_heads / num_kv_heads;

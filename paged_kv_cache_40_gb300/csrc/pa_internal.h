@@ -47,6 +47,21 @@ pa_status check_pools_disjoint(const char* fn, const void* k, const void* v, int
 // refused (PA_ERR_INVALID_ARG, message naming `fn`).
 pa_status device_view(const char* fn, const void* p, void** out);
 
+// device_view for a pointer the call reads or writes in place (NULL stays
+// NULL); the const-ness of the caller's pointer is kept.
+template <typename T>
+pa_status device_in(const char* fn, T*& p) {
+  if (!p) return PA_OK;
+  void* d = nullptr;
+  if (pa_status s = device_view(fn, p, &d)) return s;
+  p = static_cast<T*>(d);
+  return PA_OK;
+}
+
+// Memory the kernels reach through TMA or hold across calls (pools,
+// workspaces) must be device memory: PA_ERR_INVALID_ARG otherwise.
+pa_status device_only(const char* fn, const void* p);
+
 // Properties of the current device used for launch shaping.
 struct DeviceInfo {
   int device = -1;

@@ -168,7 +168,8 @@ class DecodeBatchRunner:
     def pack_inputs(self) -> None:
         """Re-home the step's inputs (q, the new K/V rows, slots, copy pairs,
         tables, lengths; call after plan_step) in one device buffer with a
-        pinned host mirror of the same layout (`host_inputs`), so that
+        pinned host mirror of the same layout (`packed_host`, views by
+        name), so that
         upload_inputs() moves a step's inputs with a single host-to-device
         copy."""
         import torch
@@ -182,7 +183,7 @@ class DecodeBatchRunner:
             pos += (t.numel() * t.element_size() + 255) // 256 * 256
         dev_arena = torch.empty(pos, dtype=torch.uint8, device=self.device)
         host_arena = torch.empty(pos, dtype=torch.uint8).pin_memory()
-        self.host_inputs = {}
+        self.packed_host = {}
         for n, off in zip(names, offs):
             t = getattr(self, n)
             nb = t.numel() * t.element_size()
@@ -191,8 +192,26 @@ class DecodeBatchRunner:
             hv = host_arena[off:off + nb].view(t.dtype).view(t.shape)
             hv.copy_(t.cpu())
             setattr(self, n, dv)
-            self.host_inputs[n] = hv
+            self.packed_host[n] = hv
         self.input_arena, self.host_arena = dev_arena, host_arena
+
+    def host_inputs(self) -> int:
+        """Keep the step's inputs (q, the new K/V rows, slots, copy pairs,
+        tables, lengths, the shared prefix's block list; call after
+        plan_step) in pinned host memory, where the kernels read them
+        through its device mapping over the CPU-GPU link: a step then needs
+        no host-to-device copy call. Returns their bytes."""
+        names = ["q", "k_new", "v_new", "d_slots", "d_table", "d_lens"]
+        if self.d_pairs is not None:
+            names.append("d_pairs")
+        if getattr(self, "d_prefix", None) is not None:
+            names.append("d_prefix")
+        total = 0
+        for n in names:
+            h = getattr(self, n).cpu().pin_memory()
+            setattr(self, n, h)
+            total += h.numel() * h.element_size()
+        return total
 
     def upload_inputs(self, stream=None) -> int:
         """One host-to-device copy of the packed inputs; returns its bytes."""

@@ -146,3 +146,89 @@ def test_packed_inputs_step_matches_unpacked(pa):
         r2.run_step()
     torch.cuda.synchronize()
     assert torch.equal(r1.out, r2.out)
+    # then the same runner with its inputs moved to host memory (as the
+    # benchmark times both paths one after the other)
+    assert r2.host_inputs() == sum(t.numel() * t.element_size()
+                                   for t in r2.packed_host.values())
+    r2.run_step()
+    torch.cuda.synchronize()
+    assert torch.equal(r1.out, r2.out)
+
+
+def test_inputs_read_from_pinned_host_memory(pa):
+    """A step whose every input (q, new K/V rows, slots, copy pairs, tables,
+    lengths, the prefix block list) lives in pinned host memory gives the
+    same pools and output, bit for bit, as the step with device inputs."""
+    from paged_kv_cache_40_gb300.engine import DecodeBatchRunner, SharedPrefixRunner
+    g = synthetic.config2_gqa_batch(num_seqs=11, lo=1, hi=900)
+    a = DecodeBatchRunner(g)
+    a.plan_step()
+    a.run_step()
+    b = DecodeBatchRunner(g)
+    b.plan_step()
+    assert b.host_inputs() > 0 and not b.q.is_cuda and b.q.is_pinned()
+    b.out = torch.empty(b.out.shape, dtype=torch.float16).pin_memory()
+    b.run_step()
+    torch.cuda.synchronize()
+    assert torch.equal(a.k_pool, b.k_pool) and torch.equal(a.v_pool, b.v_pool)
+    assert torch.equal(a.out.cpu(), b.out)
+    # copy-on-write pairs and the shared prefix's block list from host memory
+    w = synthetic.config4_shared_prefix()
+    c = SharedPrefixRunner(w)
+    c.plan_step()
+    c.run_step()
+    e = SharedPrefixRunner(w)
+    e.plan_step()
+    e.host_inputs()
+    assert not e.d_pairs.is_cuda and not e.d_prefix.is_cuda
+    e.run_step()
+    torch.cuda.synchronize()
+    assert torch.equal(c.k_pool, e.k_pool) and torch.equal(c.out, e.out)
+    assert pa.pa_device_error() == 0
+
+
+def test_fp8_step_inputs_from_pinned_host_memory(pa):
+    from paged_kv_cache_40_gb300.engine import DecodeBatchRunner
+    g = synthetic.config2_gqa_batch(num_seqs=7, lo=1, hi=600)
+    c8 = synthetic.fp8_cache(g)
+    kw = dict(kv_dtype="fp8", k_pool=c8.k_pool, v_pool=c8.v_pool, k_scale=c8.k_scale,
+              v_scale=c8.v_scale)
+    a = DecodeBatchRunner(g, **kw)
+    a.plan_step()
+    a.run_step()
+    b = DecodeBatchRunner(g, **kw)
+    b.plan_step()
+    b.host_inputs()
+    b.k_scale = b.k_scale.cpu().pin_memory()
+    b.v_scale = b.v_scale.cpu().pin_memory()
+    b.run_step()
+    torch.cuda.synchronize()
+    assert torch.equal(a.k_pool, b.k_pool) and torch.equal(a.out, b.out)
+
+
+def test_pageable_inputs_and_host_pools_are_refused(pa):
+    q, kp, vp, table, lens = _case()
+    with pytest.raises(ValueError):
+        pa.pa_decode_attention(torch.from_numpy(q), d(kp), d(vp), d(table), d(lens), 0.1)
+    with pytest.raises(ValueError):
+        pa.pa_decode_attention(d(q), torch.from_numpy(kp).pin_memory(),
+                               torch.from_numpy(vp).pin_memory(), d(table), d(lens), 0.1)
+    # the library itself refuses a pageable table and a pinned host pool
+    lib = pa.lib()
+    S, Hq, D = q.shape
+    nb, BS, Hkv, _ = kp.shape
+    dq, dk, dv, dl = d(q), d(kp), d(vp), d(lens)
+    ws = pa.alloc_workspace(S, Hq, Hkv, D, BS, table.shape[1])
+    out = torch.empty(q.shape, dtype=torch.float16, device="cuda")
+    pageable_table = np.ascontiguousarray(table)
+    vp_ = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = lib.pa_decode_attention(vp_(dq), vp_(dk), vp_(dv),
+                                 ctypes.c_void_p(pageable_table.ctypes.data), vp_(dl), S, Hq, Hkv, D,
+                                 BS, table.shape[1], nb, 0, ctypes.c_float(0.1), vp_(out), vp_(ws),
+                                 ws.numel(), 0, None)
+    assert st == 1 and b"pinned" in lib.pa_last_error()
+    host_pool = torch.from_numpy(kp).pin_memory()
+    st = lib.pa_decode_attention(vp_(dq), vp_(host_pool), vp_(dv), vp_(d(table)), vp_(dl), S, Hq,
+                                 Hkv, D, BS, table.shape[1], nb, 0, ctypes.c_float(0.1), vp_(out),
+                                 vp_(ws), ws.numel(), 0, None)
+    assert st == 1 and b"device memory" in lib.pa_last_error()
