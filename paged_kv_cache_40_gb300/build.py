@@ -49,8 +49,20 @@ def _stamp() -> str:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link libpa.so; return its path."""
+    """Compile and link libpa.so; return its path. Processes that build at the
+    same time (one per rank) take turns on a lock file; those that come after
+    the first find the library current and return."""
+    import fcntl
     os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, "lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            return _build_locked(force, verbose)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(force: bool, verbose: bool) -> str:
     stamp_file = os.path.join(BUILD, "stamp")
     stamp = _stamp()
     if not force and os.path.exists(LIB) and os.path.exists(stamp_file):
