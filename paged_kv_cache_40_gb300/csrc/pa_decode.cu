@@ -241,10 +241,6 @@ struct Shape {
   static constexpr int ESZ = KV8 ? 1 : 2;            // bytes per cached value
   static constexpr int NHALF = D * ESZ / 128;        // 128-byte lines per row
   static constexpr int TS = BS < 16 ? BS : 16;       // tokens per stage
-  static constexpr int KSTEPS = D / 16;              // QK k-steps over head_dim
-  static constexpr int MT = D / 16;                  // PV m-tiles over head_dim
-  static constexpr int NT = TS / 8;                  // 8-token groups per stage
-  static constexpr int PK = (NT + 1) / 2;            // PV k-steps (16 tokens) per stage
   static constexpr int REC = rec_floats(G, D);
   // shared-memory layout: fixed part (bytes)
   static constexpr int OFF_FULL = 0;
@@ -1094,12 +1090,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         }
       }
     } else {
-      uint32_t qa[SH::KSTEPS][2];  // A fragments a0/a2 per k-step; rows (heads) >= G are zero
+      // fp16 consumer tiling
+      constexpr int KSTEPS = D / 16;  // QK k-steps over head_dim
+      constexpr int MT = D / 16;      // PV m-tiles over head_dim
+      constexpr int NT = TS / 8;      // 8-token groups per stage
+      constexpr int PK = (NT + 1) / 2;  // PV k-steps (16 tokens) per stage
+      uint32_t qa[KSTEPS][2];  // A fragments a0/a2 per k-step; rows (heads) >= G are zero
       {
         const uint32_t qrow = smem_addr(qslot + qs * QSLOT) +
                               (w * G + (ld_row < G ? ld_row : 0)) * (D * 2);
   #pragma unroll
-        for (int kk = 0; kk < SH::KSTEPS; kk += 2) {
+        for (int kk = 0; kk < KSTEPS; kk += 2) {
           uint32_t r0, r1, r2, r3;
           ldsm_x4(qrow + (2 * kk + ld_mat) * 16, r0, r1, r2, r3);
           qa[kk][0] = gid < G ? r0 : 0u;
@@ -1112,9 +1113,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       }
 
         float m_run = -INFINITY, l_run = 0.f;  // head gid: running max (log2 units), partial sum
-        float o[SH::MT][4];                     // O^T[d = mt*16 + gid (+8)][h = 2*tig (+1)]
+        float o[MT][4];                     // O^T[d = mt*16 + gid (+8)][h = 2*tig (+1)]
   #pragma unroll
-        for (int mt = 0; mt < SH::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
         for (int jj = 0; jj < n; ++jj) {
           const int blk = pj + jj;
@@ -1142,13 +1143,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
             // ---- S = Q K^T for each 8-token group ----
             // x4 of k-steps (kk, kk+1): matrix m covers dims (2*kk + m) * 8 .. +8
-            float s[SH::NT][4];
+            float s[NT][4];
   #pragma unroll
-            for (int nt = 0; nt < SH::NT; ++nt) {
+            for (int nt = 0; nt < NT; ++nt) {
               s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
               const uint32_t rowa = kaddr + (nt * 8 + ld_row) * 128;
   #pragma unroll
-              for (int kk = 0; kk < SH::KSTEPS; kk += 2) {
+              for (int kk = 0; kk < KSTEPS; kk += 2) {
                 const int gc = 2 * kk + ld_mat;  // 16-byte chunk of the row, 0 .. D/8-1
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(rowa + (gc >> 3) * HALF + (((gc & 7) ^ ld_row) << 4), b0, b1, b2, b3);
@@ -1159,7 +1160,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             // ---- online softmax over this stage's tokens (row gid = head) ----
             float mx = -INFINITY;
   #pragma unroll
-            for (int nt = 0; nt < SH::NT; ++nt) {
+            for (int nt = 0; nt < NT; ++nt) {
   #pragma unroll
               for (int e = 0; e < 2; ++e) {
                 const int t = nt * 8 + 2 * tig + e;
@@ -1175,9 +1176,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             const float alpha = fast_exp2(m_run - mu);
             m_run = m_new;
             float ps = 0.f;
-            uint32_t pb[SH::NT];  // P as fp16 pairs: B operand of the PV mma
+            uint32_t pb[NT];  // P as fp16 pairs: B operand of the PV mma
   #pragma unroll
-            for (int nt = 0; nt < SH::NT; ++nt) {
+            for (int nt = 0; nt < NT; ++nt) {
               const float p0 = fast_exp2(s[nt][0] - mu);
               const float p1 = fast_exp2(s[nt][1] - mu);
               ps += p0 + p1;
@@ -1188,7 +1189,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * tig);
             const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);
   #pragma unroll
-            for (int mt = 0; mt < SH::MT; ++mt) {
+            for (int mt = 0; mt < MT; ++mt) {
               o[mt][0] *= a_lo;
               o[mt][1] *= a_hi;
               o[mt][2] *= a_lo;
@@ -1197,16 +1198,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             // ---- O^T += V^T P^T over 16-token k-steps ----
             // x4.trans of m-tile mt: matrix m covers tokens +8*(m>>1), dims mt*16 + 8*(m&1)
   #pragma unroll
-            for (int pk = 0; pk < SH::PK; ++pk) {
+            for (int pk = 0; pk < PK; ++pk) {
               const uint32_t pb0 = pb[2 * pk];
-              const uint32_t pb1 = (2 * pk + 1 < SH::NT) ? pb[2 * pk + 1] : 0u;
+              const uint32_t pb1 = (2 * pk + 1 < NT) ? pb[2 * pk + 1] : 0u;
               const uint32_t rowa = vaddr + (pk * 16 + ld_row + (ld_mat >> 1) * 8) * 128;
   #pragma unroll
-              for (int mt = 0; mt < SH::MT; ++mt) {
+              for (int mt = 0; mt < MT; ++mt) {
                 const int gc = 2 * mt + (ld_mat & 1);
                 const uint32_t addr = rowa + (gc >> 3) * HALF + (((gc & 7) ^ ld_row) << 4);
                 uint32_t a0, a1, a2, a3;
-                if (2 * pk + 1 < SH::NT) {
+                if (2 * pk + 1 < NT) {
                   ldsm_x4_t(addr, a0, a1, a2, a3);
                 } else {
                   ldsm_x2_t(addr, a0, a1);
@@ -1230,7 +1231,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           const float l1 = __shfl_sync(0xffffffffu, l_run, 8 * tig + 4);
           const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
   #pragma unroll
-          for (int mt = 0; mt < SH::MT; ++mt) {
+          for (int mt = 0; mt < MT; ++mt) {
             const int d = mt * 16 + gid;
             if (h0 < G) {
               out_row[h0 * D + d] = __float2half_rn(o[mt][0] * i0);
@@ -1244,7 +1245,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         } else {
           // cut segment: this chunk's partial record
   #pragma unroll
-          for (int mt = 0; mt < SH::MT; ++mt) {
+          for (int mt = 0; mt < MT; ++mt) {
             const int d = mt * 16 + gid;
             if (h0 < G) {
               rec[h0 * D + d] = o[mt][0];
