@@ -372,12 +372,19 @@ struct Cursor {
   int seg_start;       // stream index of the segment's block 0
 };
 
+// Called by a whole warp (all 32 lanes, same x): the sequence is found by a
+// 32-way search, each lane probing one of 32 evenly spaced prefix entries,
+// so S sequences take ceil(log32 S) rounds of one shared-memory load each.
 __device__ __forceinline__ Cursor locate(int x, const int* pfx, int S, int nhg) {
-  int lo = 0, hi = S;  // largest i with pfx[i] * nhg <= x
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (pfx[mid] * nhg <= x) lo = mid;
-    else hi = mid;
+  const int lane = threadIdx.x & 31;
+  int lo = 0, n = S;  // the largest i with pfx[i] * nhg <= x lies in [lo, lo + n)
+  while (n > 1) {
+    const int step = (n + 31) >> 5;
+    const int idx = lo + lane * step;
+    const unsigned le = __ballot_sync(0xffffffffu, idx < lo + n && pfx[idx] * nhg <= x);
+    const int k = 31 - __clz(le);  // lane 0's probe is pfx[lo], always <= x
+    lo += k * step;
+    n = min(step, n - k * step);
   }
   Cursor c;
   c.seq = lo;
@@ -412,6 +419,7 @@ struct Walk {
   int xl;      // start of the trailing cut piece (xe if there is none)
   int xm;      // next uncut segment
   int phase;   // 0: first piece next, 1: trailing cut piece next, 2: middle
+  Cursor first, last;  // cursors at x0 and at xl
 };
 
 __device__ __forceinline__ void walk_begin(Walk& wk, int c, const Geometry& geo, const int* pfx,
@@ -421,12 +429,15 @@ __device__ __forceinline__ void walk_begin(Walk& wk, int c, const Geometry& geo,
   if (c >= geo.nchunks) return;
   wk.x0 = c * geo.chunk;
   wk.xe = min(geo.total, wk.x0 + geo.chunk);
-  const Cursor a = locate(wk.x0, pfx, S, nhg);
-  wk.x1 = min(a.seg_start + a.nb, wk.xe);
+  wk.first = locate(wk.x0, pfx, S, nhg);
+  wk.x1 = min(wk.first.seg_start + wk.first.nb, wk.xe);
   wk.xl = wk.xe;
   if (wk.x1 < wk.xe) {
-    const Cursor b = locate(wk.xe - 1, pfx, S, nhg);
-    if (b.seg_start + b.nb > wk.xe) wk.xl = b.seg_start;
+    wk.last = locate(wk.xe - 1, pfx, S, nhg);
+    if (wk.last.seg_start + wk.last.nb > wk.xe) {
+      wk.xl = wk.last.seg_start;
+      wk.last.j = 0;
+    }
   }
   wk.xm = wk.x1;
 }
@@ -445,14 +456,14 @@ __device__ __forceinline__ bool walk_next(Walk& wk, const Geometry& geo, int str
     pc.c = wk.c;
     if (wk.phase == 0) {
       wk.phase = 1;
-      pc.cur = locate(wk.x0, pfx, S, nhg);
+      pc.cur = wk.first;
       pc.n = wk.x1 - wk.x0;
       return true;
     }
     if (wk.phase == 1) {
       wk.phase = 2;
       if (wk.xl < wk.xe) {
-        pc.cur = locate(wk.xl, pfx, S, nhg);
+        pc.cur = wk.last;
         pc.n = wk.xe - wk.xl;
         return true;
       }
@@ -661,22 +672,27 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   const int chunk = geo.chunk;
   const bool has_work = static_cast<int>(blockIdx.x) < geo.nchunks;
 
-  // The producer's first piece, and an L2 prefetch of its table entries and
-  // q rows: a prefetch may run before the wait below, because L2 stays
-  // coherent with whatever the previous kernel writes.
+  // The producer's first two pieces, and an L2 prefetch of their table
+  // entries and q rows: a prefetch may run before the wait below, because L2
+  // stays coherent with whatever the previous kernel writes.
   Walk wk;
-  Piece P{};
-  bool have = false;
+  Piece P{}, PN{};
+  bool have = false, nhave = false;
+  int lraw_first = 0;  // the first piece's sequence length, as given
   if (warp == HG) {
     walk_begin(wk, blockIdx.x, geo, pfx, S, NHG);
     have = walk_next(wk, geo, gridDim.x, pfx, S, NHG, P);
-    if (have) {
+    if (have) lraw_first = __ldg(p.seq_lens + P.cur.seq);
+    nhave = have && walk_next(wk, geo, gridDim.x, pfx, S, NHG, PN);
+    for (int k = 0; k < 2; ++k) {
+      const Piece& X = k == 0 ? P : PN;
+      if (!(k == 0 ? have : nhave)) break;
       const int32_t* trow =
-          p.block_table + static_cast<long long>(P.cur.seq) * p.max_blocks + P.cur.j;
-      if (lane < min(32, P.n)) asm volatile("prefetch.global.L2 [%0];" ::"l"(trow + lane));
+          p.block_table + static_cast<long long>(X.cur.seq) * p.max_blocks + X.cur.j;
+      if (lane < min(32, X.n)) asm volatile("prefetch.global.L2 [%0];" ::"l"(trow + lane));
       const char* qrow = reinterpret_cast<const char*>(
-          p.q + (static_cast<long long>(P.cur.seq) * p.num_q_heads +
-                 static_cast<long long>(P.cur.hg) * HG * G) * D);
+          p.q + (static_cast<long long>(X.cur.seq) * p.num_q_heads +
+                 static_cast<long long>(X.cur.hg) * HG * G) * D);
       for (int off = lane * 128; off < QSLOT; off += 32 * 128)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow + off));
     }
@@ -697,17 +713,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     // =========================== producer warp ===========================
     // Streams the CTA's pieces, each in groups of up to 32 blocks. For each
     // piece it first publishes, in q slot (piece & 1), the piece's metadata
-    // and its HG*G q rows. The table entries of the next group (in this piece
-    // or the next) are loaded while the current group is issued, so no group
-    // or piece boundary waits on a global load.
+    // and its HG*G q rows. The table entries (and length) of the next group,
+    // in this piece or the next, are loaded while the current group is issued
+    // and used only once it is: no group or piece boundary waits on a global
+    // load, and no load holds up the current group's copies.
     uint32_t g = 0;   // ring sequence number (stages)
     uint32_t pc = 0;  // piece number
-    Piece PN{};
-    bool nhave = have && walk_next(wk, geo, gridDim.x, pfx, S, NHG, PN);
     int j0 = 0;
     int phys_cur = 0, len_cur = 0;
     if (have) {
-      len_cur = min(max(__ldg(p.seq_lens + P.cur.seq) - loff, 0), cap);
+      len_cur = min(max(lraw_first - loff, 0), cap);
       phys_cur = lane < min(32, P.n)
                      ? __ldg(p.block_table + static_cast<long long>(P.cur.seq) * p.max_blocks +
                              P.cur.j + lane)
@@ -743,20 +758,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         }
       }
       const int nn = min(32, P.n - j0);
-      // table entries (and length) of the next group
+      // table entries (and raw length) of the next group
       const bool next_in_piece = j0 + 32 < P.n;
-      int phys_nxt = 0, len_nxt = len_cur;
+      int phys_nxt = 0, lraw_nxt = 0;
       if (next_in_piece) {
-        phys_nxt = lane < min(32, P.n - j0 - 32)
-                       ? __ldg(p.block_table + static_cast<long long>(P.cur.seq) * p.max_blocks +
-                               P.cur.j + j0 + 32 + lane)
-                       : 0;
+        if (lane < min(32, P.n - j0 - 32))
+          phys_nxt = __ldg(p.block_table + static_cast<long long>(P.cur.seq) * p.max_blocks +
+                           P.cur.j + j0 + 32 + lane);
       } else if (nhave) {
-        len_nxt = min(max(__ldg(p.seq_lens + PN.cur.seq) - loff, 0), cap);
-        phys_nxt = lane < min(32, PN.n)
-                       ? __ldg(p.block_table + static_cast<long long>(PN.cur.seq) * p.max_blocks +
-                               PN.cur.j + lane)
-                       : 0;
+        lraw_nxt = __ldg(p.seq_lens + PN.cur.seq);
+        if (lane < min(32, PN.n))
+          phys_nxt = __ldg(p.block_table + static_cast<long long>(PN.cur.seq) * p.max_blocks +
+                           PN.cur.j + lane);
       }
       for (int jj = 0; jj < nn; ++jj) {
         const int phys = __shfl_sync(0xffffffffu, phys_cur, jj);
@@ -796,10 +809,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         P = PN;
         have = nhave;
         j0 = 0;
+        len_cur = min(max(lraw_nxt - loff, 0), cap);
         if (have) nhave = walk_next(wk, geo, gridDim.x, pfx, S, NHG, PN);
       }
       phys_cur = phys_nxt;
-      len_cur = len_nxt;
     }
     // After an abort, wait (bounded) for copies still landing in shared memory.
     if (*abort_flag) {
