@@ -93,11 +93,39 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def strip_c_comments(src: str) -> str:
+    """C/C++ source with its comments removed and each run of whitespace
+    collapsed to one space; string and character literals are kept whole."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+            out.append(" ")
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
+    """Identifies the attention kernel's code (comments and layout excluded),
+    so that recorded ncu traffic is used only for the code it was taken on."""
     h = hashlib.sha256()
     for name in ("pa_decode.cu",):
-        with open(os.path.join(ROOT, "paged_kv_cache_40_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "paged_kv_cache_40_gb300", "csrc", name)) as f:
+            h.update(strip_c_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -32,8 +32,10 @@
 //     each CTA streams them before the uncut segments in between, so most
 //     merges happen while the other CTAs are still streaming.
 //   * Warp specialisation. A producer warp is the only one that walks the
-//     CTA's chunk. It loads the block-table entries of the next 32 blocks
-//     while it issues the current ones, and moves K and V with TMA into a
+//     CTA's chunk, finding a stream position's segment with a warp-wide
+//     32-way search over the prefix sums. It loads the block-table entries of
+//     the next 32 blocks while it issues the current ones (and uses them only
+//     after), and moves K and V with TMA into a
 //     ring of shared-memory stages: a 4-D tensor map over the pool seen as
 //     (dim, token, KV head, block) — token stride larger than head stride —
 //     with box {64, tokens, HG, 1} and the 128-byte swizzle, so each head's
@@ -57,9 +59,10 @@
 //     score accumulators already hold (no transpose, no shared-memory trip).
 //     Rows past the sequence end are masked out of the softmax and zeroed in
 //     the V stage so they contribute exactly nothing.
-//   * Programmatic dependent launch: the prologue (prefix sum of lengths) can
-//     overlap the previous kernel on the stream; K/V, q and table reads wait
-//     for it with griddepcontrol.wait.
+//   * Programmatic dependent launch: the prologue (prefix sum of lengths, the
+//     producer's first two pieces, their L2 prefetches) can overlap the
+//     previous kernel on the stream; it reads only the lengths. K/V, q and
+//     table reads wait for that kernel with griddepcontrol.wait.
 //   * Every wait is bounded (about one second of %globaltimer); on expiry the
 //     kernel records PA_DEVERR_TIMEOUT, stops issuing copies, drains the copies
 //     already in flight (again bounded) and finishes without faulting.

@@ -95,3 +95,15 @@ def test_reference_arm_under_torchrun_two_ranks():
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_traffic_record_keys_on_code_not_comments():
+    """The recorded ncu traffic is tied to the attention kernel's code: a
+    comment or layout edit keeps the key, a code edit changes it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src = "int f(int a) {  // one\n  return a + 1; /* two */ }\nconst char* s = \"x // y\";\n"
+    assert bench.strip_c_comments(src) == bench.strip_c_comments(
+        "int f(int a) { /* other */\n\n return a + 1;   }\n// note\nconst char* s = \"x // y\";")
+    assert bench.strip_c_comments(src) != bench.strip_c_comments(src.replace("a + 1", "a + 2"))
+    assert "x // y" in bench.strip_c_comments(src)
