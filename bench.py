@@ -124,7 +124,8 @@ def kernel_source_hash() -> str:
     so that recorded ncu traffic is used only for the code it was taken on."""
     h = hashlib.sha256()
     for name in ("pa_decode.cu",):
-        with open(os.path.join(ROOT, "paged_kv_cache_40_gb300", "csrc", name)) as f:
+        with open(os.path.join(ROOT, "paged_kv_cache_40_gb300", "csrc", name),
+                  encoding="utf-8") as f:
             h.update(strip_c_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
