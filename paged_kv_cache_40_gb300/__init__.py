@@ -23,6 +23,8 @@ from __future__ import annotations
 import ctypes
 from typing import Iterable, Optional, Sequence, Tuple
 
+import numpy as np
+
 from ._lib import (  # noqa: F401
     AllocStats,
     OutOfBlocksError,
@@ -455,6 +457,13 @@ def _i32_array(values):
     return arr
 
 
+def _i64_ids(seqs) -> "np.ndarray":
+    """Sequence ids as a contiguous int64 buffer (at least one element, so
+    that its address is valid even for an empty batch)."""
+    ids = np.ascontiguousarray(seqs, dtype=np.int64).reshape(-1)
+    return ids if ids.size else np.zeros(1, np.int64)
+
+
 class BlockAllocator:
     """The host block manager of libpa (pa_alloc_*), one handle per pool."""
 
@@ -497,14 +506,15 @@ class BlockAllocator:
 
     def append_slots(self, seqs: Sequence[int]):
         """One decode step: (slots int32 list, cow pairs list of (src, dst))."""
+        ids = _i64_ids(seqs)
         n = len(seqs)
-        ids = (ctypes.c_int64 * max(n, 1))(*[int(x) for x in seqs])
-        slots = (ctypes.c_int32 * max(n, 1))()
-        pairs = (ctypes.c_int32 * max(2 * n, 2))()
+        slots = np.empty(max(n, 1), np.int32)
+        pairs = np.empty(max(2 * n, 2), np.int32)
         ncow, ndone = ctypes.c_int(), ctypes.c_int()
-        _check(_load().pa_alloc_append_slots(self._h, ids, n, slots, pairs, ctypes.byref(ncow),
+        _check(_load().pa_alloc_append_slots(self._h, ids.ctypes.data, n, slots.ctypes.data,
+                                             pairs.ctypes.data, ctypes.byref(ncow),
                                              ctypes.byref(ndone)))
-        return list(slots[:n]), [(pairs[2 * i], pairs[2 * i + 1]) for i in range(ncow.value)]
+        return slots[:n].tolist(), list(map(tuple, pairs[:2 * ncow.value].reshape(-1, 2).tolist()))
 
     def free_seq(self, seq: int) -> None:
         _check(_load().pa_alloc_free_seq(self._h, seq))
@@ -524,17 +534,14 @@ class BlockAllocator:
         return v.value
 
     def build_tables(self, seqs: Sequence[int], max_blocks: int, fill: int = -1):
-        """(table int32 [n][max_blocks] as a flat ctypes array, seq_lens [n])."""
-        import numpy as np
+        """(table int32 numpy [n][max_blocks], seq_lens int32 numpy [n])."""
+        ids = _i64_ids(seqs)
         n = len(seqs)
-        ids = (ctypes.c_int64 * max(n, 1))(*[int(x) for x in seqs])
-        table = np.empty((n, max_blocks), dtype=np.int32)
-        lens = np.empty((n,), dtype=np.int32)
-        _check(_load().pa_alloc_build_tables(
-            self._h, ids, n, max_blocks, fill,
-            table.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
-            lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))))
-        return table, lens
+        table = np.empty((max(n, 1), max_blocks), dtype=np.int32)
+        lens = np.empty((max(n, 1),), dtype=np.int32)
+        _check(_load().pa_alloc_build_tables(self._h, ids.ctypes.data, n, max_blocks, fill,
+                                             table.ctypes.data, lens.ctypes.data))
+        return table[:n], lens[:n]
 
     def stats(self) -> dict:
         st = AllocStats()

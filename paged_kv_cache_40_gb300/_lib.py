@@ -80,11 +80,12 @@ SIGNATURES = {
     "pa_alloc_add_seq": (_i32, [_vp, _i64, _i64]),
     "pa_alloc_fork": (_i32, [_vp, _i64, _i64]),
     "pa_alloc_append_slot": (_i32, [_vp, _i64, _pi32, _pi32, _pi32]),
-    "pa_alloc_append_slots": (_i32, [_vp, _pi64, _i32, _pi32, _pi32, _pint, _pint]),
+    # the per-step calls take their arrays as plain addresses (numpy buffers)
+    "pa_alloc_append_slots": (_i32, [_vp, _vp, _i32, _vp, _vp, _pint, _pint]),
     "pa_alloc_free_seq": (_i32, [_vp, _i64]),
     "pa_alloc_get_table": (_i32, [_vp, _i64, _pi32, _i32, _pint]),
     "pa_alloc_seq_len": (_i32, [_vp, _i64, _pi64]),
-    "pa_alloc_build_tables": (_i32, [_vp, _pi64, _i32, _i32, ctypes.c_int32, _pi32, _pi32]),
+    "pa_alloc_build_tables": (_i32, [_vp, _vp, _i32, _i32, ctypes.c_int32, _vp, _vp]),
     "pa_alloc_stats": (_i32, [_vp, ctypes.POINTER(AllocStats)]),
     "pa_alloc_export_state": (_i32, [_vp, _pi32, _pint, _pi32]),
     "pa_alloc_add_host_pool": (_i32, [_vp, _i32, _pi32]),
