@@ -123,6 +123,8 @@ def test_out_of_blocks_leaves_state(libpa):
         libpa.BlockAllocator(4, 4, [0, 1, 1, 2])
     slots, pairs = nat.append_slots([])
     assert slots == [] and pairs == []
+    table, lens = nat.build_tables([], 5)
+    assert table.shape == (0, 5) and lens.shape == (0,)
 
 
 def test_batched_append_stops_at_failure(libpa):
