@@ -57,7 +57,7 @@ from .interleaved import (  # noqa: F401
     decode_attention_interleaved,
     decode_attention_interleaved_fp8,
 )
-from .allocator import BlockAllocator, OutOfBlocks  # noqa: F401
+from .allocator import BlockAllocator, OutOfBlocks, shared_prefix_blocks  # noqa: F401
 from .accounting import (  # noqa: F401
     blocks_needed,
     paged_internal_waste,

@@ -231,6 +231,12 @@ class BlockAllocator:
         """(free list front to back, reference count per block)."""
         return list(self.free), list(self.ref)
 
+    def shared_prefix(self, seqs) -> List[int]:
+        """The whole blocks every sequence of `seqs` begins with; see
+        shared_prefix_blocks. Swapped-out or unknown sequences raise."""
+        return shared_prefix_blocks([self.tables[s] for s in seqs],
+                                    [self.lens[s] for s in seqs], self.block_size)
+
     def dense_table(self, seqs, max_blocks: int, fill: int = -1):
         """int32-style nested list [len(seqs)][max_blocks], padded with `fill`."""
         rows = []
@@ -240,3 +246,28 @@ class BlockAllocator:
                 raise ValueError("table longer than max_blocks")
             rows.append(t + [fill] * (max_blocks - len(t)))
         return rows
+
+
+def shared_prefix_blocks(tables, lens, block_size: int) -> List[int]:
+    """The physical blocks that every given sequence begins with, whole.
+
+    Sequences forked from one prompt point their tables at the same physical
+    blocks ("Phase 7 · Document 04 — PagedAttention", §2 block sharing and §3
+    Mental Model, where A -> [b3, b7, b1] and B -> [b3, b9] share b3; lux-666
+    notes "PagedAttention", prefix sharing). Reading: the shared prefix of a
+    batch is the longest run of leading table entries that is the same in
+    every table and whose blocks every sequence attends in full (k blocks
+    with k * block_size <= its length), so that each sequence's attention
+    splits into those k * block_size tokens and the rest of its own table.
+    An empty batch has none; a single sequence's whole blocks are its own.
+    """
+    if not tables:
+        return []
+    k = min(min(len(t), int(L) // block_size) for t, L in zip(tables, lens))
+    first = list(tables[0])
+    for t in tables[1:]:
+        j = 0
+        while j < k and t[j] == first[j]:
+            j += 1
+        k = j
+    return first[:k]

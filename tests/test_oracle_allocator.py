@@ -181,3 +181,68 @@ def test_bad_arguments():
         a.add_seq(0, 1)
     with pytest.raises(ValueError):
         a.fork(5, 6)
+
+
+def test_shared_prefix_of_the_sharing_picture():
+    """Document 04 §3: A -> [3,7,1] and B -> [3,9] share block 3; both attend
+    it whole, so the batch's shared prefix is [3]. A sequence that does not
+    fill block 3 yet shares no whole block."""
+    g = golden("sharing_picture.json")
+    order = [3, 7, 1, 9] + [b for b in range(10) if b not in (3, 7, 1, 9)]
+    a = BlockAllocator(10, 16, order)
+    a.add_seq(0, 16)
+    a.fork(0, 1)
+    for _ in range(32):
+        a.append_slot(0)
+    a.append_slot(1)
+    assert a.table(0) == g["seq_A"] and a.table(1) == g["seq_B"]
+    assert a.shared_prefix([0, 1]) == [g["shared_block"]]
+    assert a.shared_prefix([1, 0]) == [g["shared_block"]]
+    # a third sequence holding block 3 with only 10 of its 16 tokens
+    b = BlockAllocator(10, 16, order)
+    b.add_seq(0, 10)
+    b.fork(0, 1)
+    b.append_slot(0)                           # copy-on-write: seq 0 moves off block 3
+    assert b.table(1) == [3] and b.table(0) != [3]
+    assert b.shared_prefix([0, 1]) == []
+    assert oracle.shared_prefix_blocks([[3, 7, 1], [3, 9]], [40, 10], 16) == []
+
+
+def test_shared_prefix_special_cases():
+    assert oracle.shared_prefix_blocks([], [], 16) == []
+    # one sequence: its whole blocks (the worked mapping, 40 tokens = 2 whole)
+    assert oracle.shared_prefix_blocks([[7, 2, 9]], [40], 16) == [7, 2]
+    assert oracle.shared_prefix_blocks([[7, 2, 9]], [48], 16) == [7, 2, 9]
+    # no common first block
+    assert oracle.shared_prefix_blocks([[1, 2], [2, 1]], [32, 32], 16) == []
+
+
+def test_shared_prefix_invariants_under_random_forks():
+    """After random forks and appends: every returned block sits at the same
+    place in every table and is held by at least as many references as there
+    are sequences (reference counts are kept apart from the tables), every
+    sequence attends it whole, and no longer run has all three properties."""
+    rng = np.random.default_rng(12)
+    for trial in range(200):
+        bs = int(rng.choice([1, 2, 4, 16]))
+        a = BlockAllocator(600, bs)
+        a.add_seq(0, int(rng.integers(0, 6 * bs)))
+        live = [0]
+        for nid in range(1, int(rng.integers(2, 7))):
+            parent = int(rng.choice(live))
+            a.fork(parent, nid)
+            live.append(nid)
+            for s in live:
+                for _ in range(int(rng.integers(0, 2 * bs))):
+                    a.append_slot(s)
+        batch = [int(s) for s in rng.permutation(live)[:int(rng.integers(1, len(live) + 1))]]
+        pre = a.shared_prefix(batch)
+        k = len(pre)
+        _, ref = a.export_state()
+        for j, blk in enumerate(pre):
+            assert all(a.table(s)[j] == blk for s in batch)
+            assert ref[blk] >= len(batch)
+        assert all(a.seq_len(s) >= k * bs for s in batch)
+        longer = all(len(a.table(s)) > k and a.seq_len(s) >= (k + 1) * bs for s in batch) and \
+            len({a.table(s)[k] for s in batch}) == 1
+        assert not longer

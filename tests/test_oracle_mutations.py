@@ -111,3 +111,47 @@ def test_split_merge_mutant_caught():
 
     with pytest.raises(AssertionError):
         pins.check_split_merge(split_bad, oracle.decode_attention_one)
+
+
+def _prefix_ignoring_whole_blocks(tables, lens, bs):
+    k = min(len(t) for t in tables) if tables else 0
+    first = list(tables[0]) if tables else []
+    for t in tables[1:]:
+        j = 0
+        while j < k and t[j] == first[j]:
+            j += 1
+        k = j
+    return first[:k]
+
+
+def _prefix_ignoring_other_tables(tables, lens, bs):
+    if not tables:
+        return []
+    k = min(min(len(t), int(L) // bs) for t, L in zip(tables, lens))
+    return list(tables[0])[:k]
+
+
+_shared_prefix_blocks = oracle.shared_prefix_blocks
+
+
+def _prefix_one_block_short(tables, lens, bs):
+    return _shared_prefix_blocks(tables, lens, bs)[:-1]
+
+
+@pytest.mark.parametrize("mutant", [_prefix_ignoring_whole_blocks, _prefix_ignoring_other_tables,
+                                    _prefix_one_block_short])
+def test_shared_prefix_pins_catch_planted_mistakes(monkeypatch, mutant):
+    """Each planted mistake in the shared-prefix definition fails one of its
+    pins (the sharing picture, the special cases, the random-fork invariants)."""
+    from oracle import allocator as alloc
+    from tests import test_oracle_allocator as t
+    monkeypatch.setattr(alloc, "shared_prefix_blocks", mutant)
+    monkeypatch.setattr(oracle, "shared_prefix_blocks", mutant)
+    failed = 0
+    for check in (t.test_shared_prefix_of_the_sharing_picture, t.test_shared_prefix_special_cases,
+                  t.test_shared_prefix_invariants_under_random_forks):
+        try:
+            check()
+        except AssertionError:
+            failed += 1
+    assert failed > 0
