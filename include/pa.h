@@ -444,6 +444,21 @@ PA_API pa_status pa_alloc_build_tables(const pa_allocator* a, const int64_t* seq
                                 int n, int max_blocks, int32_t fill,
                                 int32_t* table, int32_t* seq_lens);
 
+/* The whole blocks that every sequence of a batch begins with ("Phase 7 ·
+ * Document 04 — PagedAttention", §2 block sharing and §3 Mental Model;
+ * lux-666 notes "PagedAttention", prefix sharing): the longest run of leading
+ * table entries that is the same in every table and whose blocks every
+ * sequence attends in full (run length k with k * block_size <= each length).
+ * This is the prefix pa_decode_attention_shared_prefix takes.
+ * seq_ids: host int64 [n]; blocks: host int32 [cap] receives the run's
+ * physical ids in logical order; *num_blocks = the run's length
+ * (PA_ERR_INVALID_ARG if cap < *num_blocks). An empty batch has none; one
+ * sequence's run is its whole blocks.
+ * Errors: PA_ERR_INVALID_ARG (bad arguments, a sequence unknown or swapped
+ *         out). Nothing is modified. */
+PA_API pa_status pa_alloc_shared_prefix(const pa_allocator* a, const int64_t* seq_ids,
+                                 int n, int32_t* blocks, int cap, int* num_blocks);
+
 PA_API pa_status pa_alloc_stats(const pa_allocator* a, pa_alloc_stats_t* out);
 
 /* free_order: host int32 [num_blocks], front to back, *num_free entries

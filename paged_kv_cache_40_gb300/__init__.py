@@ -543,6 +543,18 @@ class BlockAllocator:
                                              table.ctypes.data, lens.ctypes.data))
         return table[:n], lens[:n]
 
+    def shared_prefix(self, seqs: Sequence[int]):
+        """int32 numpy array of the whole blocks every sequence of `seqs`
+        begins with (pa_alloc_shared_prefix): the prefix that
+        pa_decode_attention_shared_prefix takes for this batch."""
+        ids = _i64_ids(seqs)
+        cap = max(self.num_blocks, 1)
+        out = np.empty(cap, np.int32)
+        k = ctypes.c_int()
+        _check(_load().pa_alloc_shared_prefix(self._h, ids.ctypes.data, len(seqs),
+                                              out.ctypes.data, cap, ctypes.byref(k)))
+        return out[:k.value].copy()
+
     def stats(self) -> dict:
         st = AllocStats()
         _check(_load().pa_alloc_stats(self._h, ctypes.byref(st)))

@@ -86,6 +86,7 @@ SIGNATURES = {
     "pa_alloc_get_table": (_i32, [_vp, _i64, _pi32, _i32, _pint]),
     "pa_alloc_seq_len": (_i32, [_vp, _i64, _pi64]),
     "pa_alloc_build_tables": (_i32, [_vp, _vp, _i32, _i32, ctypes.c_int32, _vp, _vp]),
+    "pa_alloc_shared_prefix": (_i32, [_vp, _vp, _i32, _vp, _i32, _pint]),
     "pa_alloc_stats": (_i32, [_vp, ctypes.POINTER(AllocStats)]),
     "pa_alloc_export_state": (_i32, [_vp, _pi32, _pint, _pi32]),
     "pa_alloc_add_host_pool": (_i32, [_vp, _i32, _pi32]),

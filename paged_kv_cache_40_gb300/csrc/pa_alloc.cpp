@@ -408,6 +408,40 @@ pa_status pa_alloc_build_tables(const pa_allocator* a, const int64_t* seq_ids, i
   return pa::ok();
 }
 
+pa_status pa_alloc_shared_prefix(const pa_allocator* a, const int64_t* seq_ids, int n,
+                                 int32_t* blocks, int cap, int* num_blocks) {
+  if (pa_status s = check_handle(a)) return s;
+  if (n < 0 || cap < 0 || !num_blocks || (n > 0 && !seq_ids))
+    return pa::fail(PA_ERR_INVALID_ARG, "shared_prefix: bad arguments");
+  *num_blocks = 0;
+  const std::vector<int32_t>* first = nullptr;
+  int64_t k = 0;  // length of the run common to the sequences seen so far
+  for (int i = 0; i < n; ++i) {
+    auto it = a->seqs.find(seq_ids[i]);
+    if (it == a->seqs.end() || it->second.swapped)
+      return pa::fail(PA_ERR_INVALID_ARG, "shared_prefix: sequence %lld unknown or swapped out",
+                      (long long)seq_ids[i]);
+    const auto& t = it->second.table;
+    // blocks this sequence attends in full
+    const int64_t whole = std::min<int64_t>(static_cast<int64_t>(t.size()),
+                                            it->second.len / a->block_size);
+    if (!first) {
+      first = &t;
+      k = whole;
+      continue;
+    }
+    int64_t j = 0;
+    const int64_t lim = std::min(k, whole);
+    while (j < lim && t[j] == (*first)[j]) ++j;
+    k = j;
+  }
+  *num_blocks = static_cast<int>(k);
+  if (cap < k || (k > 0 && !blocks))
+    return pa::fail(PA_ERR_INVALID_ARG, "shared_prefix: capacity %d < %lld", cap, (long long)k);
+  if (k > 0) std::copy(first->begin(), first->begin() + k, blocks);
+  return pa::ok();
+}
+
 pa_status pa_alloc_stats(const pa_allocator* a, pa_alloc_stats_t* out) {
   if (pa_status s = check_handle(a)) return s;
   if (!out) return pa::fail(PA_ERR_INVALID_ARG, "stats: out is NULL");

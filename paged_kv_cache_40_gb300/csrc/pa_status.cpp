@@ -90,6 +90,6 @@ const char* pa_status_string(pa_status s) {
   return "PA_ERR_UNKNOWN";
 }
 
-int pa_version(void) { return 200; }
+int pa_version(void) { return 300; }
 
 }  // extern "C"

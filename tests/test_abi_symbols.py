@@ -40,7 +40,7 @@ def test_only_the_api_is_exported(libpa):
 
 def test_version_and_status_strings(libpa):
     lib = libpa.lib()
-    assert lib.pa_version() == 200
+    assert lib.pa_version() == 300
     assert lib.pa_status_string(2) == b"PA_ERR_OUT_OF_BLOCKS"
     assert lib.pa_status_string(6) == b"PA_ERR_TIMEOUT"
 

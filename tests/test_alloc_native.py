@@ -216,3 +216,54 @@ def test_swapped_sequence_is_refused(libpa):
     assert a.seq_len(1) == 6
     a.swap_in(1)
     assert len(a.table(1)) == 2
+
+
+def test_shared_prefix_matches_oracle(libpa):
+    """pa_alloc_shared_prefix against the oracle's definition after random
+    forks and appends, for random batches (order and subset)."""
+    rng = np.random.default_rng(44)
+    for trial in range(150):
+        bs = int(rng.choice([1, 4, 16]))
+        nat, ref = libpa.BlockAllocator(800, bs), oracle.BlockAllocator(800, bs)
+        L0 = int(rng.integers(0, 8 * bs))
+        nat.add_seq(0, L0)
+        ref.add_seq(0, L0)
+        live = [0]
+        for nid in range(1, int(rng.integers(2, 8))):
+            parent = int(rng.choice(live))
+            nat.fork(parent, nid)
+            ref.fork(parent, nid)
+            live.append(nid)
+            for s in live:
+                for _ in range(int(rng.integers(0, 2 * bs))):
+                    assert nat.append_slot(s) == ref.append_slot(s)
+        batch = [int(s) for s in rng.permutation(live)[:int(rng.integers(0, len(live) + 1))]]
+        got = nat.shared_prefix(batch)
+        assert got.dtype == np.int32 and got.tolist() == ref.shared_prefix(batch)
+
+
+def test_shared_prefix_of_a_forked_prompt(libpa):
+    """128 sequences forked from a 2040-token prompt, after their first
+    append: the 127 whole prompt blocks are shared, the partial one was
+    copied on write."""
+    a = libpa.BlockAllocator(400, 16)
+    a.add_seq(0, 2040)
+    for c in range(1, 128):
+        a.fork(0, c)
+    a.append_slots(list(range(128)))
+    pre = a.shared_prefix(list(range(128)))
+    assert pre.tolist() == a.table(0)[:127]
+
+
+def test_shared_prefix_refusals(libpa):
+    a = libpa.BlockAllocator(8, 4)
+    a.add_seq(0, 8)
+    with pytest.raises(libpa.PaError):
+        a.shared_prefix([0, 5])                 # unknown sequence
+    a.add_host_pool(8)
+    a.fork(0, 1)
+    a.swap_out(1)
+    with pytest.raises(libpa.PaError):
+        a.shared_prefix([0, 1])                 # swapped out
+    assert a.shared_prefix([]).tolist() == []
+    assert a.shared_prefix([0]).tolist() == a.table(0)
