@@ -102,6 +102,22 @@ PA_API int pa_version(void);
 #define PA_DEVERR_TIMEOUT 8     /* a pipeline wait hit its time limit */
 PA_API pa_status pa_device_error(pa_stream_t stream, int32_t* flags);
 
+/* Time limit of the attention kernels' pipeline waits (the stage, q-slot and
+ * merge handoffs inside pa_decode_attention, pa_decode_attention_fp8,
+ * pa_decode_attention_fixed_scratch and the streaming pass of
+ * pa_decode_attention_shared_prefix), taken by every later call of those
+ * entry points from this process. The default, about one second, is far
+ * above any wait of a healthy launch. A wait that runs out records
+ * PA_DEVERR_TIMEOUT and the kernel stops streaming, lets the copies it
+ * already issued land (always on the one-second limit) and exits; its
+ * outputs are then undefined. A short limit makes that path run on demand,
+ * so that a test can check it without a fault or a hang; 0 restores the
+ * default. The pages have no counterpart: it belongs to the failure
+ * handling of the pages' explicit-failure rule ("Phase 7 · Document 04 —
+ * PagedAttention", §11: reject rather than thrash at the limit).
+ * Errors: none (PA_OK). */
+PA_API pa_status pa_set_wait_limit_ns(uint64_t limit_ns);
+
 /* ------------------------------------------------------------------------
  * pa_append_kv — write each sequence's new K/V token into its cache slot.
  *
@@ -195,9 +211,14 @@ PA_API pa_status pa_copy_blocks(pa_half* k_pool, pa_half* v_pool,
  *              otherwise a positive multiple of block_size capping the
  *              tokens of one chunk (more, shorter chunks: a CTA then streams
  *              several).
- * The call enqueues one kernel on `stream` (launched as a programmatic
- * dependent: its prologue, which reads only seq_lens, may overlap the end of
- * the previous kernel on the stream).
+ * The call enqueues one kernel on `stream`, launched as a programmatic
+ * dependent: its CTAs may start while the previous kernel on the stream is
+ * finishing, but they read no input (not even seq_lens) before that kernel
+ * has completed, so any input may be written by the kernel just before.
+ * After a PA_DEVERR_TIMEOUT report (pa_device_error), the counters of the
+ * workspace that call used may hold arrivals under its tag: clear them with
+ * pa_decode_workspace_init before a captured graph that uses the workspace
+ * is replayed (eager calls take a new tag and need nothing).
  * Supported shapes: head_dim in {64, 128}; block_size in {8, 16, 32};
  * num_q_heads / num_kv_heads in {1, 2, 4, 8}; num_seqs <= 16384.
  * Errors: PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED (shape outside the list, or
@@ -246,9 +267,11 @@ PA_API pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool,
  * - The first call on a device resolves the array's device address (once per
  *   device, with that device current); make that first call before any stream
  *   capture.
- * - Every call uses the same array (its counters need no clearing, as in
- *   pa_decode_attention); calls that overlap on the GPU (other streams,
- *   other host threads) race on it and must not be issued.
+ * - Every call uses the same array, which keeps what the last call left;
+ *   the call clears the array's arrival counters on `stream` before its
+ *   kernel (a memset, not an allocation), so a call cut short by a timeout
+ *   leaves nothing behind for the next. Calls that overlap on the GPU (other
+ *   streams, other host threads) race on the array and must not be issued.
  * - Shapes whose scratch would exceed 16 MiB (8 bytes per (sequence, KV
  *   head), plus two partial results of G x (head_dim + 2) floats per CTA of
  *   the grid and per KV head a CTA streams, up to 8) are refused with
@@ -438,6 +461,29 @@ PA_API pa_status pa_alloc_get_table(const pa_allocator* a, int64_t seq_id,
 PA_API pa_status pa_alloc_seq_len(const pa_allocator* a, int64_t seq_id,
                            int64_t* len);
 
+/* One decode step of a batch planned in a single call: the next slot of
+ * every sequence of seq_ids, in index order, exactly as
+ * pa_alloc_append_slots gives them (growth, copy-on-write pairs), then the
+ * batch's dense tables and lengths after those appends, exactly as
+ * pa_alloc_build_tables gives them ("Phase 7 · Document 04 —
+ * PagedAttention", §2 on-demand allocation and block sharing; lux-666 notes
+ * "PagedAttention", 最小模型: the table the kernel reads is the block
+ * manager's). Every output is written straight into the caller's buffers,
+ * which may be the pinned host memory the step's kernels read in place.
+ * seq_ids  host int64 [n], distinct
+ * slots    int32 [n]; cow_pairs int32 [n][2] (src, dst) with *num_cow rows
+ *          written; table int32 [n][max_blocks] (rows padded with fill);
+ *          seq_lens int32 [n] (lengths after the append)
+ * All or nothing: the whole batch is checked first (every sequence known,
+ * not swapped out, listed once, its table after the append within
+ * max_blocks) and the blocks its growth and copies take are counted against
+ * the free list; a refused call changes nothing but the failure counter.
+ * Errors: PA_ERR_INVALID_ARG, PA_ERR_OUT_OF_BLOCKS. */
+PA_API pa_status pa_alloc_plan_step(pa_allocator* a, const int64_t* seq_ids, int n,
+                             int max_blocks, int32_t fill, int32_t* slots,
+                             int32_t* cow_pairs, int* num_cow, int32_t* table,
+                             int32_t* seq_lens);
+
 /* Dense tables for a batch: table host int32 [n][max_blocks] (rows padded
  * with `fill`), seq_lens host int32 [n] = current lengths. */
 PA_API pa_status pa_alloc_build_tables(const pa_allocator* a, const int64_t* seq_ids,
@@ -451,11 +497,14 @@ PA_API pa_status pa_alloc_build_tables(const pa_allocator* a, const int64_t* seq
  * sequence attends in full (run length k with k * block_size <= each length).
  * This is the prefix pa_decode_attention_shared_prefix takes.
  * seq_ids: host int64 [n]; blocks: host int32 [cap] receives the run's
- * physical ids in logical order; *num_blocks = the run's length
- * (PA_ERR_INVALID_ARG if cap < *num_blocks). An empty batch has none; one
- * sequence's run is its whole blocks.
+ * physical ids in logical order; *num_blocks = the run's length. An empty
+ * batch has none; one sequence's run is its whole blocks.
+ * Sizing: when cap < the run's length (or blocks is NULL with a nonempty
+ * run) the call returns PA_ERR_INVALID_ARG with *num_blocks set to the
+ * length needed and `blocks` untouched, so a caller can ask with cap = 0.
  * Errors: PA_ERR_INVALID_ARG (bad arguments, a sequence unknown or swapped
- *         out). Nothing is modified. */
+ *         out; *num_blocks is then 0). The block manager's state is never
+ *         modified. */
 PA_API pa_status pa_alloc_shared_prefix(const pa_allocator* a, const int64_t* seq_ids,
                                  int n, int32_t* blocks, int cap, int* num_blocks);
 

@@ -451,6 +451,14 @@ def pa_device_error(stream=None) -> int:
     return int(flags.value)
 
 
+def pa_set_wait_limit_ns(limit_ns: int) -> None:
+    """Time limit of the attention kernels' pipeline waits for later calls
+    (0 restores the default of about one second). A wait that runs out sets
+    PA_DEVERR_TIMEOUT and the launch's outputs are undefined; tests use a
+    short limit to run that path."""
+    _check(_load().pa_set_wait_limit_ns(int(limit_ns)))
+
+
 # ------------------------------------------------------------ host allocator --
 def _i32_array(values):
     arr = (ctypes.c_int32 * len(values))(*[int(v) for v in values])
@@ -515,6 +523,34 @@ class BlockAllocator:
                                              pairs.ctypes.data, ctypes.byref(ncow),
                                              ctypes.byref(ndone)))
         return slots[:n].tolist(), list(map(tuple, pairs[:2 * ncow.value].reshape(-1, 2).tolist()))
+
+    def plan_step(self, seqs: Sequence[int], max_blocks: int, fill: int = -1, out=None):
+        """One decode step of the batch `seqs` in one library call
+        (pa_alloc_plan_step): (slots int32 [n], copy-on-write pairs int32
+        [ncow][2], table int32 [n][max_blocks], seq_lens int32 [n]) after the
+        appends. `out` = (slots, pairs, table, lens) preallocated contiguous
+        int32 numpy arrays of shapes [n], [n][2], [n][max_blocks], [n] (for
+        instance views of pinned host memory the kernels read) to be written
+        in place; the returned pairs are then a view of the first ncow rows."""
+        ids = _i64_ids(seqs)
+        n = len(seqs)
+        if out is None:
+            out = (np.empty(max(n, 1), np.int32), np.empty((max(n, 1), 2), np.int32),
+                   np.empty((max(n, 1), max_blocks), np.int32), np.empty(max(n, 1), np.int32))
+        slots, pairs, table, lens = out
+        for arr, shape in ((slots, (n,)), (pairs, (n, 2)), (table, (n, max_blocks)),
+                           (lens, (n,))):
+            if (arr.dtype != np.int32 or not arr.flags.c_contiguous
+                    or tuple(arr.shape[:len(shape)]) < shape or arr.size < int(np.prod(shape))):
+                raise ValueError("plan_step outputs must be contiguous int32 arrays of "
+                                 "[n], [n][2], [n][max_blocks], [n]")
+        ncow = ctypes.c_int()
+        _check(_load().pa_alloc_plan_step(self._h, ids.ctypes.data, n, max_blocks, fill,
+                                          slots.ctypes.data, pairs.ctypes.data,
+                                          ctypes.byref(ncow), table.ctypes.data,
+                                          lens.ctypes.data))
+        return (slots[:n], pairs.reshape(-1, 2)[:ncow.value],
+                table.reshape(-1, max_blocks)[:n], lens[:n])
 
     def free_seq(self, seq: int) -> None:
         _check(_load().pa_alloc_free_seq(self._h, seq))

@@ -58,6 +58,7 @@ SIGNATURES = {
     "pa_status_string": (ctypes.c_char_p, [_i32]),
     "pa_version": (_i32, []),
     "pa_device_error": (_i32, [_vp, _pi32]),
+    "pa_set_wait_limit_ns": (_i32, [ctypes.c_uint64]),
     "pa_append_kv": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _vp]),
     "pa_copy_blocks": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _vp]),
     "pa_decode_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32]),
@@ -86,6 +87,8 @@ SIGNATURES = {
     "pa_alloc_get_table": (_i32, [_vp, _i64, _pi32, _i32, _pint]),
     "pa_alloc_seq_len": (_i32, [_vp, _i64, _pi64]),
     "pa_alloc_build_tables": (_i32, [_vp, _vp, _i32, _i32, ctypes.c_int32, _vp, _vp]),
+    "pa_alloc_plan_step": (_i32, [_vp, _vp, _i32, _i32, ctypes.c_int32, _vp, _vp, _pint, _vp,
+                                  _vp]),
     "pa_alloc_shared_prefix": (_i32, [_vp, _vp, _i32, _vp, _i32, _pint]),
     "pa_alloc_stats": (_i32, [_vp, ctypes.POINTER(AllocStats)]),
     "pa_alloc_export_state": (_i32, [_vp, _pi32, _pint, _pi32]),

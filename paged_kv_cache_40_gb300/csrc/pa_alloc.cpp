@@ -41,7 +41,14 @@ struct pa_allocator {
     std::vector<int32_t> host;   // host blocks while swapped out
     int64_t len = 0;
     bool swapped = false;
+    uint64_t plan_mark = 0;      // last step plan that listed this sequence
   };
+  // step planning (pa_alloc_plan_step): the plans made so far, the batch's
+  // sequences, and per block the batch's writes into it (zero between calls)
+  uint64_t plans = 0;
+  std::vector<Seq*> plan_seqs;
+  std::vector<int32_t> plan_writes;
+  std::vector<int32_t> plan_blocks;
   // host pool: FIFO ring as above
   int num_host = 0;
   std::vector<int32_t> hring;
@@ -100,6 +107,9 @@ pa_status check_handle(const pa_allocator* a) {
   return PA_OK;
 }
 
+pa_status append_to(pa_allocator* a, pa_allocator::Seq& s, int64_t seq_id, int32_t* slot,
+                    int32_t* cs, int32_t* cd);
+
 pa_status append_one(pa_allocator* a, int64_t seq_id, int32_t* slot, int32_t* cs,
                      int32_t* cd) {
   auto it = a->seqs.find(seq_id);
@@ -110,6 +120,14 @@ pa_status append_one(pa_allocator* a, int64_t seq_id, int32_t* slot, int32_t* cs
   if (s.swapped)
     return pa::fail(PA_ERR_INVALID_ARG, "append_slot: sequence %lld is swapped out",
                     (long long)seq_id);
+  return append_to(a, s, seq_id, slot, cs, cd);
+}
+
+// The next token of sequence s (not swapped out): grow its table when its
+// length is a multiple of the block size, copy-on-write when the block it
+// writes is shared, then the slot of that token.
+pa_status append_to(pa_allocator* a, pa_allocator::Seq& s, int64_t seq_id, int32_t* slot,
+                    int32_t* cs, int32_t* cd) {
   const int64_t L = s.len;
   const int BS = a->block_size;
   int32_t src = -1, dst = -1;
@@ -238,6 +256,82 @@ pa_status pa_alloc_append_slots(pa_allocator* a, const int64_t* seq_ids, int n,
       ++*num_cow;
     }
     *num_done = i + 1;
+  }
+  return pa::ok();
+}
+
+pa_status pa_alloc_plan_step(pa_allocator* a, const int64_t* seq_ids, int n, int max_blocks,
+                             int32_t fill, int32_t* slots, int32_t* cow_pairs, int* num_cow,
+                             int32_t* table, int32_t* seq_lens) {
+  if (pa_status s = check_handle(a)) return s;
+  if (n < 0 || max_blocks <= 0 || !num_cow ||
+      (n > 0 && (!seq_ids || !slots || !cow_pairs || !table || !seq_lens)))
+    return pa::fail(PA_ERR_INVALID_ARG, "plan_step: bad arguments");
+  *num_cow = 0;
+  const int BS = a->block_size;
+  const uint64_t mark = ++a->plans;
+  a->plan_seqs.resize(static_cast<size_t>(n));
+  // 1. every sequence known, present once, tabled after its append within
+  //    max_blocks; the blocks the appends will take: one per sequence that
+  //    grows, plus the copies. A block with r holders written by k sequences
+  //    of the batch is copied min(k, r - 1) times: each writer copies while
+  //    another holder is left, and the last holder writes in place.
+  int64_t need = 0;
+  for (int i = 0; i < n; ++i) {
+    auto it = a->seqs.find(seq_ids[i]);
+    if (it == a->seqs.end() || it->second.swapped)
+      return pa::fail(PA_ERR_INVALID_ARG, "plan_step: sequence %lld unknown or swapped out",
+                      (long long)seq_ids[i]);
+    pa_allocator::Seq& sq = it->second;
+    if (sq.plan_mark == mark)
+      return pa::fail(PA_ERR_INVALID_ARG, "plan_step: sequence %lld listed twice",
+                      (long long)seq_ids[i]);
+    sq.plan_mark = mark;
+    const bool grows = sq.len % BS == 0;
+    if (static_cast<int64_t>(sq.table.size()) + (grows ? 1 : 0) > max_blocks)
+      return pa::fail(PA_ERR_INVALID_ARG, "plan_step: sequence %lld needs more than %d blocks",
+                      (long long)seq_ids[i], max_blocks);
+    if (sq.len + 1 > INT32_MAX)
+      return pa::fail(PA_ERR_INVALID_ARG, "plan_step: length exceeds int32");
+    a->plan_seqs[i] = &sq;
+  }
+  if (a->plan_writes.size() != static_cast<size_t>(a->num_blocks))
+    a->plan_writes.assign(static_cast<size_t>(a->num_blocks), 0);
+  a->plan_blocks.clear();
+  for (int i = 0; i < n; ++i) {
+    const pa_allocator::Seq& sq = *a->plan_seqs[i];
+    if (sq.len % BS == 0) {
+      ++need;
+    } else {
+      const int32_t b = sq.table[sq.len / BS];
+      if (a->ref[b] > 1 && a->plan_writes[b]++ == 0) a->plan_blocks.push_back(b);
+    }
+  }
+  for (int32_t b : a->plan_blocks) {
+    need += std::min<int64_t>(a->plan_writes[b], a->ref[b] - 1);
+    a->plan_writes[b] = 0;
+  }
+  if (need > a->count) {
+    ++a->alloc_failures;
+    return pa::fail(PA_ERR_OUT_OF_BLOCKS, "plan_step: %lld blocks needed, %lld free",
+                    (long long)need, (long long)a->count);
+  }
+  // 2. the appends (none can fail now), then the batch's tables and lengths
+  for (int i = 0; i < n; ++i) {
+    int32_t cs, cd;
+    append_to(a, *a->plan_seqs[i], seq_ids[i], &slots[i], &cs, &cd);
+    if (cs >= 0) {
+      cow_pairs[2 * *num_cow] = cs;
+      cow_pairs[2 * *num_cow + 1] = cd;
+      ++*num_cow;
+    }
+  }
+  for (int i = 0; i < n; ++i) {
+    const pa_allocator::Seq& sq = *a->plan_seqs[i];
+    int32_t* row = table + static_cast<size_t>(i) * max_blocks;
+    std::copy(sq.table.begin(), sq.table.end(), row);
+    std::fill(row + sq.table.size(), row + max_blocks, fill);
+    seq_lens[i] = static_cast<int32_t>(sq.len);
   }
   return pa::ok();
 }

@@ -222,9 +222,9 @@ pa_status check_pools_disjoint(const char* fn, const void* k, const void* v, int
 
 int32_t* device_error_word() {
   static std::mutex mu;
-  static int32_t* addr[64] = {};
+  static int32_t* addr[kMaxDevices] = {};
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+  if (cudaGetDevice(&dev) != cudaSuccess || !device_slot_ok(dev)) {
     fail(PA_ERR_CUDA, "device_error_word: no current device");
     return nullptr;
   }
@@ -296,7 +296,7 @@ pa_status pa_append_kv(const pa_half* k_new, const pa_half* v_new, pa_half* k_po
     // Same shared-memory carveout as the attention kernel that usually
     // follows, so its CTAs can start on SMs this kernel still occupies.
     static std::mutex mu;
-    static bool set[64] = {};
+    static bool set[pa::kMaxDevices] = {};
     std::lock_guard<std::mutex> lock(mu);
     if (!set[dev.device]) {
       cudaError_t e = cudaFuncSetAttribute(append_kv_kernel,
@@ -385,7 +385,7 @@ pa_status pa_append_kv_fp8(const pa_half* k_new, const pa_half* v_new, uint8_t* 
   if (!err) return PA_ERR_CUDA;
   {
     static std::mutex mu;
-    static bool set[64] = {};
+    static bool set[pa::kMaxDevices] = {};
     std::lock_guard<std::mutex> lock(mu);
     if (!set[dev.device]) {
       cudaError_t e = cudaFuncSetAttribute(append_kv_fp8_kernel,

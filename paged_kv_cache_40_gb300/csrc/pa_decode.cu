@@ -87,6 +87,7 @@ constexpr int kMaxStages = 16;
 constexpr int kRingBytesPerHead = 24 * 1024;       // ring size per KV head of the group
 constexpr int kArrivalBits = 20;                   // low bits of a counter word: arrivals
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+constexpr long long kPrefetchLines = 1ll << 17;     // 16 MB of table and q asked of L2 at most
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------------ PTX ---
@@ -201,9 +202,11 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 // flagged as aborted and PA_DEVERR_TIMEOUT recorded once) or if the CTA was
 // already aborted. A warp that is not latency critical passes kSleepNs > 0 to
 // sleep between polls and leave the issue slots to the warps that are.
+// `limit_ns` is the time limit (about a second unless a test shortens it).
 template <unsigned kSleepNs = 0>
 __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity,
-                                                volatile int* abort_flag, int32_t* err) {
+                                                volatile int* abort_flag, int32_t* err,
+                                                unsigned long long limit_ns = kWaitLimitNs) {
   const int lane = threadIdx.x & 31;
   unsigned long long t0 = 0;
   for (int iter = 0;; ++iter) {
@@ -216,7 +219,7 @@ __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity,
         t0 = global_ns();
       } else if (*abort_flag) {
         give_up = 1;
-      } else if (global_ns() - t0 > kWaitLimitNs) {
+      } else if (global_ns() - t0 > limit_ns) {
         if (atomicExch(const_cast<int*>(abort_flag), 1) == 0) atomicOr(err, PA_DEVERR_TIMEOUT);
         give_up = 1;
       }
@@ -299,6 +302,7 @@ struct DecodeParams {
   int hg;          // KV heads per group (consumer warps)
   int nst;         // ring stages
   float qscale;    // scale * log2(e)
+  unsigned long long wait_ns;    // time limit of the pipeline waits
   long long block_stride_bytes;  // host only: the pools' block stride, for their tensor maps
 };
 
@@ -669,6 +673,31 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
 
+  if constexpr (!PFX) {
+    // Every input may still be written by the kernel launched just before
+    // this one on the stream (programmatic dependent launch), so none is read
+    // before griddepcontrol.wait. The CTAs only ask L2 for the lengths, the
+    // block table and q meanwhile, spread over the grid (L2 stays coherent
+    // with whatever that kernel writes, so a prefetch is never stale).
+    const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+    const long long me = static_cast<long long>(blockIdx.x) * blockDim.x + tid;
+    const long long len_lines = (static_cast<long long>(S) * 4 + 127) / 128;
+    const long long tab_lines = (static_cast<long long>(S) * p.max_blocks * 4 + 127) / 128;
+    const long long q_lines = (static_cast<long long>(S) * p.num_q_heads * D * 2 + 127) / 128;
+    const long long n_lines = len_lines + min(tab_lines + q_lines, kPrefetchLines);
+    for (long long i = me; i < n_lines; i += nthreads) {
+      const char* a;
+      if (i < len_lines)
+        a = reinterpret_cast<const char*>(p.seq_lens) + i * 128;
+      else if (i < len_lines + tab_lines)
+        a = reinterpret_cast<const char*>(p.block_table) + (i - len_lines) * 128;
+      else
+        a = reinterpret_cast<const char*>(p.q) + (i - len_lines - tab_lines) * 128;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+  }
+
   // ---- blocks per sequence, exclusive prefix sum in shared memory ----
   block_prefix(pfx, flags + kFlagWsum, p.seq_lens, S, BS, cap, p.err, loff);
   const Geometry geo = chunk_geometry(pfx[S] * NHG, gridDim.x, p.cap_blocks);
@@ -676,8 +705,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   const bool has_work = static_cast<int>(blockIdx.x) < geo.nchunks;
 
   // The producer's first two pieces, and an L2 prefetch of their table
-  // entries and q rows: a prefetch may run before the wait below, because L2
-  // stays coherent with whatever the previous kernel writes.
+  // entries and q rows.
   Walk wk;
   Piece P{}, PN{};
   bool have = false, nhave = false;
@@ -701,15 +729,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     }
   }
 
-  // Everything above reads only seq_lens. The pool, q and the table may still
-  // be written by the kernel launched just before this one on the stream
-  // (programmatic dependent launch): wait for it before touching them. In
-  // shared-prefix mode that kernel is the prefix kernel, which writes only
-  // the prefix records and lets this kernel start once everything before it
-  // has completed; the wait then sits before the first read of a prefix
-  // record (pfx_wait), and the streaming overlaps the prefix kernel.
-  if constexpr (!PFX) asm volatile("griddepcontrol.wait;" ::: "memory");
-  // a dependent kernel launched after this one may start its own prologue
+  // In shared-prefix mode the kernel launched just before this one is the
+  // prefix kernel, which writes only the prefix records and lets this kernel
+  // start once everything launched before it has completed: the lengths,
+  // table, q and pools may be read at once, and the wait sits before the
+  // first read of a prefix record (pfx_wait), so the streaming overlaps the
+  // prefix kernel.
+  // A dependent kernel launched after this one may start its own prologue.
   asm volatile("griddepcontrol.launch_dependents;");
 
   if (warp == HG) {
@@ -722,6 +748,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     // load, and no load holds up the current group's copies.
     uint32_t g = 0;   // ring sequence number (stages)
     uint32_t pc = 0;  // piece number
+    // stages and q slots whose copies were issued (after an abort the walk
+    // goes on without issuing, so g and pc run ahead of these)
+    uint32_t g_iss = 0, pc_iss = 0;
     int j0 = 0;
     int phys_cur = 0, len_cur = 0;
     if (have) {
@@ -737,7 +766,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         const int qs = static_cast<int>(pc & 1);
         if (!__shfl_sync(0xffffffffu, *abort_flag, 0) &&
             (pc < 2 ||
-             warp_wait_phase(smem_addr(&qempty_bar[qs]), ((pc >> 1) - 1) & 1, abort_flag, p.err))) {
+             warp_wait_phase(smem_addr(&qempty_bar[qs]), ((pc >> 1) - 1) & 1, abort_flag, p.err, p.wait_ns))) {
           if (lane == 0) {
             PieceMeta* m = pmeta + qs;
             m->seq = P.cur.seq;
@@ -757,6 +786,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                                  static_cast<long long>(P.cur.hg) * HG * G) * D,
                           QSLOT, qb);
           }
+          pc_iss = pc + 1;
           __syncwarp();
         }
       }
@@ -785,7 +815,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           const uint32_t use = g / NST;
           if (__shfl_sync(0xffffffffu, *abort_flag, 0)) continue;
           if (use > 0 &&
-              !warp_wait_phase(smem_addr(&empty_bar[stage]), (use - 1) & 1, abort_flag, p.err))
+              !warp_wait_phase(smem_addr(&empty_bar[stage]), (use - 1) & 1, abort_flag, p.err, p.wait_ns))
             continue;
           if (lane == 0) {
             const uint32_t fb = smem_addr(&full_bar[stage]);
@@ -802,6 +832,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
               }
             }
           }
+          g_iss = g + 1;
           __syncwarp();
         }
       }
@@ -817,16 +848,20 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       }
       phys_cur = phys_nxt;
     }
-    // After an abort, wait (bounded) for copies still landing in shared memory.
+    // After an abort, wait (bounded, on the full limit whatever the pipeline
+    // waits used) for copies still landing in shared memory: the last NST
+    // stages and the last two q slots issued. Each of those barriers has one
+    // phase pending, the one waited for; every earlier phase of its slot
+    // completed before the slot was issued again.
     if (*abort_flag) {
-      const uint32_t first = g > static_cast<uint32_t>(NST) ? g - NST : 0;
-      for (uint32_t gi = first; gi < g; ++gi) {
+      const uint32_t first = g_iss > static_cast<uint32_t>(NST) ? g_iss - NST : 0;
+      for (uint32_t gi = first; gi < g_iss; ++gi) {
         const uint32_t bar = smem_addr(&full_bar[gi % NST]);
         const unsigned long long t0 = global_ns();
         while (!mbar_try_wait(bar, (gi / NST) & 1) && global_ns() - t0 < kWaitLimitNs) {
         }
       }
-      for (uint32_t pi = pc > 2 ? pc - 2 : 0; pi < pc; ++pi) {
+      for (uint32_t pi = pc_iss > 2 ? pc_iss - 2 : 0; pi < pc_iss; ++pi) {
         const unsigned long long t0 = global_ns();
         while (!mbar_try_wait(smem_addr(&qfull_bar[pi & 1]), (pi >> 1) & 1) &&
                global_ns() - t0 < kWaitLimitNs) {
@@ -847,7 +882,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     for (uint32_t mc = 0; has_work; ++mc) {
       const int ms = static_cast<int>(mc % kMsgSlots);
       if (!warp_wait_phase<256>(smem_addr(&mfull_bar[ms]), (mc / kMsgSlots) & 1, abort_flag,
-                                p.err))
+                                p.err, p.wait_ns))
         break;
       const MsgMeta msg = mmeta[ms];
       // the consumers' records (ordered before their arrivals on the barrier)
@@ -925,7 +960,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   for (uint32_t pc = 0;; ++pc) {
     // ---- the piece: metadata and q from q slot (pc & 1) ----
     const int qs = static_cast<int>(pc & 1);
-    const bool qok = warp_wait_phase(smem_addr(&qfull_bar[qs]), (pc >> 1) & 1, abort_flag, p.err);
+    const bool qok = warp_wait_phase(smem_addr(&qfull_bar[qs]), (pc >> 1) & 1, abort_flag, p.err, p.wait_ns);
     if (!qok) break;
     const PieceMeta pm = pmeta[qs];
     const int pj = pm.j, n = pm.n, L = pm.len;
@@ -981,7 +1016,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         const int nsb = (vb + TS - 1) / TS;
         for (int sb = 0; sb < nsb; ++sb, ++g) {
           const int stage = g % NST;
-          if (!warp_wait_phase(smem_addr(&full_bar[stage]), (g / NST) & 1, abort_flag, p.err))
+          if (!warp_wait_phase(smem_addr(&full_bar[stage]), (g / NST) & 1, abort_flag, p.err, p.wait_ns))
             continue;
           const int rows = min(TS, vb - sb * TS);
           unsigned char* kt = ring + static_cast<size_t>(stage) * STAGE;
@@ -1139,7 +1174,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           const int nsb = (vb + TS - 1) / TS;
           for (int sb = 0; sb < nsb; ++sb, ++g) {
             const int stage = g % NST;
-            if (!warp_wait_phase(smem_addr(&full_bar[stage]), (g / NST) & 1, abort_flag, p.err))
+            if (!warp_wait_phase(smem_addr(&full_bar[stage]), (g / NST) & 1, abort_flag, p.err, p.wait_ns))
               continue;
             const int rows = min(TS, vb - sb * TS);
             unsigned char* kt = ring + static_cast<size_t>(stage) * STAGE;
@@ -1294,7 +1329,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             // whose release makes them visible to the merge warps' acquire
             if (mc >= kMsgSlots)
               warp_wait_phase(smem_addr(&mempty_bar[mc % kMsgSlots]), ((mc / kMsgSlots) - 1) & 1,
-                              abort_flag, p.err);
+                              abort_flag, p.err, p.wait_ns);
             if (w == 0 && lane == 0) {
               MsgMeta* m = mmeta + mc % kMsgSlots;
               m->seq = pm.seq;
@@ -1347,7 +1382,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   if (!*abort_flag) {
     if (mc >= kMsgSlots)
       warp_wait_phase(smem_addr(&mempty_bar[mc % kMsgSlots]), ((mc / kMsgSlots) - 1) & 1,
-                      abort_flag, p.err);
+                      abort_flag, p.err, p.wait_ns);
     if (w == 0 && lane == 0) mmeta[mc % kMsgSlots].stop = 1;
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&mfull_bar[mc % kMsgSlots]));
@@ -1874,6 +1909,9 @@ Layout workspace_layout(int S, int Hq, int Hkv, int D, int MB, int cap_blocks) {
   return w;
 }
 
+// Time limit of the attention kernel's pipeline waits (pa_set_wait_limit_ns).
+std::atomic<unsigned long long> g_wait_limit_ns{kWaitLimitNs};
+
 // Tag of the next decode call: unique within the process (2^44 values), never
 // zero, so a zero counter word always reads as "no arrivals".
 unsigned long long next_call_tag() {
@@ -1982,7 +2020,7 @@ pa_status launch_config(const pa::DeviceInfo& dev, int S, int Hkv, LaunchCfg* cf
                     cfg->smem);
   cfg->threads = (cfg->hg + 1 + kMergeWarps) * 32;
   static std::mutex mu;
-  static bool attr_set[64] = {};
+  static bool attr_set[pa::kMaxDevices] = {};
   struct OccEntry {
     int device, threads;
     size_t smem;
@@ -2122,7 +2160,7 @@ pa_status launch_prefix(const PrefixParams& pp, const PfxGeom& geo, const void* 
   auto kernel = paged_prefix_kernel<BS, G>;
   {
     static std::mutex mu;
-    static bool set[64] = {};
+    static bool set[pa::kMaxDevices] = {};
     std::lock_guard<std::mutex> lock(mu);
     if (!set[dev.device]) {
       cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -2235,7 +2273,11 @@ static __device__ __align__(256) unsigned char g_pa_fixed_scratch[kFixedScratchB
 // address). Returns nullptr with a recorded message on failure.
 unsigned char* fixed_scratch_address(int device) {
   static std::mutex mu;
-  static unsigned char* addr[64] = {};
+  static unsigned char* addr[pa::kMaxDevices] = {};
+  if (!pa::device_slot_ok(device)) {
+    pa::fail(PA_ERR_UNSUPPORTED, "fixed decode scratch: device index %d", device);
+    return nullptr;
+  }
   std::lock_guard<std::mutex> lock(mu);
   if (!addr[device]) {
     void* ptr = nullptr;
@@ -2356,6 +2398,7 @@ static DecodeParams make_params(const pa_half* q, const pa_half* k_pool, const p
   prm.hg = 0;   // set by the launch
   prm.nst = 0;  // set by the launch
   prm.qscale = scale * kLog2e;
+  prm.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   prm.block_stride_bytes = stride_bytes;
   return prm;
 }
@@ -2611,8 +2654,15 @@ pa_status pa_decode_attention_fixed_scratch(const pa_half* q, const pa_half* k_p
                     "the fixed scratch holds %zu (use pa_decode_attention with a workspace)",
                     need, kFixedScratchBytes);
   unsigned char* ws = fixed_scratch_address(dev.device);
-  if (!ws) return PA_ERR_CUDA;
+  if (!ws) return pa::device_slot_ok(dev.device) ? PA_ERR_CUDA : PA_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The array keeps whatever the last call left. A call cut short by a
+  // timeout leaves arrival counts under its tag, and a replayed graph reuses
+  // its tag, so the counters are cleared here on every call (no caller can
+  // clear this array).
+  if (cudaError_t e = cudaMemsetAsync(ws + lay.counters, 0,
+                                      static_cast<size_t>(num_seqs) * num_kv_heads * 8, s))
+    return pa::cuda_fail(e, "pa_decode_attention_fixed_scratch: clearing the counters");
   DecodeParams prm = make_params(q, k_pool, v_pool, block_table, seq_lens, num_seqs, num_q_heads,
                                  num_kv_heads, max_blocks_per_seq, num_blocks, stride_bytes,
                                  scale, out, ws, lay, cap_blocks);
@@ -2621,6 +2671,11 @@ pa_status pa_decode_attention_fixed_scratch(const pa_half* q, const pa_half* k_p
   pa_status st = head_dim == 64 ? dispatch_bs<64>(block_size, G, prm, dev, s)
                                 : dispatch_bs<128>(block_size, G, prm, dev, s);
   return st == PA_OK ? pa::ok() : st;
+}
+
+pa_status pa_set_wait_limit_ns(uint64_t limit_ns) {
+  g_wait_limit_ns.store(limit_ns == 0 ? kWaitLimitNs : limit_ns, std::memory_order_relaxed);
+  return pa::ok();
 }
 
 }  // extern "C"

@@ -10,6 +10,13 @@
 
 namespace pa {
 
+// Devices libpa keeps per-device state for (tables indexed by the device
+// ordinal); current_device() refuses ordinals outside [0, kMaxDevices).
+constexpr int kMaxDevices = 64;
+
+// True for an ordinal the per-device tables can index.
+inline bool device_slot_ok(int device) { return device >= 0 && device < kMaxDevices; }
+
 // Record a message for pa_last_error() and return `s`.
 pa_status fail(pa_status s, const char* fmt, ...);
 // Clear the calling thread's message (successful call).

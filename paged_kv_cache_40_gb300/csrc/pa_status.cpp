@@ -10,8 +10,8 @@ thread_local std::string g_last_error;
 
 struct DevCache {
   std::mutex mu;
-  pa::DeviceInfo info[64];
-  bool valid[64] = {};
+  pa::DeviceInfo info[pa::kMaxDevices];
+  bool valid[pa::kMaxDevices] = {};
 };
 DevCache& dev_cache() {
   static DevCache c;
@@ -48,7 +48,9 @@ pa_status current_device(DeviceInfo* out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= 64) return fail(PA_ERR_UNSUPPORTED, "device index %d", dev);
+  if (!device_slot_ok(dev))
+    return fail(PA_ERR_UNSUPPORTED, "device index %d (libpa serves devices 0..%d)", dev,
+                kMaxDevices - 1);
   DevCache& c = dev_cache();
   std::lock_guard<std::mutex> lock(c.mu);
   if (!c.valid[dev]) {

@@ -34,5 +34,7 @@ from .configs import (  # noqa: F401
     CONFIG_NAMES,
     Fp8Cache,
     fp8_codes,
+    fp8_codes_every_finite,
+    fp8_finite_codes,
     fp8_cache,
 )

@@ -332,14 +332,40 @@ def fp8_codes(rng: np.random.Generator, shape) -> np.ndarray:
     return out.reshape(shape)
 
 
-def fp8_cache(batch: "DecodeBatch", seed: int = 100) -> Fp8Cache:
+def fp8_finite_codes() -> np.ndarray:
+    """The 254 finite E4M3 bytes: every byte but the two NaN codes 0x7F and
+    0xFF. They include both zeros, the subnormals (exponent field 0), every
+    normal exponent field and the largest magnitudes +-448 (0x7E, 0xFE)."""
+    b = np.arange(256, dtype=np.uint8)
+    return b[(b & 0x7F) != 0x7F]
+
+
+def fp8_codes_every_finite(rng: np.random.Generator, shape) -> np.ndarray:
+    """E4M3 bytes in which every finite code occurs equally often (the 254
+    codes tiled over the array, the last tile cut short) in a seeded random
+    order. An array of at least 254 elements holds each finite code at least
+    once."""
+    n = int(np.prod(shape))
+    codes = fp8_finite_codes()
+    out = np.resize(codes, n)
+    for lo in range(0, n, _CHUNK):
+        hi = min(n, lo + _CHUNK)
+        rng.shuffle(out[lo:hi])
+    return out.reshape(shape)
+
+
+def fp8_cache(batch: "DecodeBatch", seed: int = 100, every_code: bool = False) -> Fp8Cache:
     """An E4M3 cache with the shape of `batch`'s pools, from its own stream
-    (draw order: k_pool, v_pool, k_scale, v_scale); scales U[0.002, 0.02]."""
+    (draw order: k_pool, v_pool, k_scale, v_scale); scales U[0.002, 0.02].
+    Codes come from `fp8_codes` (the magnitudes a scaled N(0,1) tensor
+    mostly takes), or with `every_code` from `fp8_codes_every_finite` (each
+    finite code equally often)."""
     rng = np.random.default_rng(seed)
     shape = batch.k_pool.shape
     hkv = shape[2]
-    k = fp8_codes(rng, shape)
-    v = fp8_codes(rng, shape)
+    gen = fp8_codes_every_finite if every_code else fp8_codes
+    k = gen(rng, shape)
+    v = gen(rng, shape)
     ks = rng.uniform(0.002, 0.02, hkv).astype(np.float32)
     vs = rng.uniform(0.002, 0.02, hkv).astype(np.float32)
     return Fp8Cache(k, v, ks, vs)

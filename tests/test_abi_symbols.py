@@ -69,7 +69,9 @@ def _kind(c_type: str) -> str:
     if "*" in c_type:
         return "pointer"
     base = c_type.replace("const", "").strip()
-    return {"int": "int32", "int32_t": "int32", "int64_t": "int64", "size_t": "size",
+    # on LP64 ctypes has one type for size_t and uint64_t (c_ulong)
+    return {"int": "int32", "int32_t": "int32", "int64_t": "int64", "uint64_t": "size",
+            "size_t": "size",
             "float": "float", "pa_status": "int32", "pa_stream_t": "pointer",
             "pa_allocator": "pointer"}.get(base, "unknown:" + base)
 
@@ -78,7 +80,8 @@ def _ctypes_kind(t) -> str:
     if t in (ctypes.c_void_p, ctypes.c_char_p) or isinstance(t, type(ctypes.POINTER(ctypes.c_int))):
         return "pointer"
     return {ctypes.c_int: "int32", ctypes.c_int32: "int32", ctypes.c_int64: "int64",
-            ctypes.c_size_t: "size", ctypes.c_float: "float"}.get(t, "unknown")
+            ctypes.c_uint64: "size", ctypes.c_size_t: "size",
+            ctypes.c_float: "float"}.get(t, "unknown")
 
 
 def test_binding_signatures_match_the_header_argument_by_argument():

@@ -267,3 +267,120 @@ def test_shared_prefix_refusals(libpa):
         a.shared_prefix([0, 1])                 # swapped out
     assert a.shared_prefix([]).tolist() == []
     assert a.shared_prefix([0]).tolist() == a.table(0)
+
+
+def test_shared_prefix_capacity_reports_the_length_needed(libpa):
+    """A buffer too small for the run: PA_ERR_INVALID_ARG, the length needed
+    in *num_blocks, the caller's buffer untouched and the manager unchanged."""
+    import ctypes
+    from paged_kv_cache_40_gb300._lib import STATUS_NAMES
+    a = libpa.BlockAllocator(64, 4, list(range(63, -1, -1)))
+    a.add_seq(0, 22)                            # 5 whole blocks + 2 tokens
+    a.fork(0, 1)
+    before = a.export_state()
+    ids = np.array([0, 1], np.int64)
+    buf = np.full(8, -7, np.int32)
+    k = ctypes.c_int(-1)
+    L = libpa.lib()
+    st = L.pa_alloc_shared_prefix(a._h, ids.ctypes.data, 2, buf.ctypes.data, 3, ctypes.byref(k))
+    assert STATUS_NAMES[st] == "PA_ERR_INVALID_ARG"
+    assert k.value == 5
+    assert (buf == -7).all()
+    k.value = -1
+    st = L.pa_alloc_shared_prefix(a._h, ids.ctypes.data, 2, None, 0, ctypes.byref(k))
+    assert STATUS_NAMES[st] == "PA_ERR_INVALID_ARG" and k.value == 5
+    assert L.pa_alloc_shared_prefix(a._h, ids.ctypes.data, 2, buf.ctypes.data, 5,
+                                    ctypes.byref(k)) == 0
+    assert k.value == 5 and buf[:5].tolist() == a.table(0)[:5] and (buf[5:] == -7).all()
+    assert a.export_state() == before
+
+
+def _oracle_step(ref, ids, max_blocks, fill=-1):
+    slots, pairs = [], []
+    for s in ids:
+        sl, cs, cd = ref.append_slot(s)
+        slots.append(sl)
+        if cs >= 0:
+            pairs.append((cs, cd))
+    return slots, pairs, np.asarray(ref.dense_table(ids, max_blocks, fill), np.int32)
+
+
+def test_plan_step_matches_the_oracle_step_by_step(libpa):
+    """One call per step (slots, copy-on-write pairs, tables, lengths) equals
+    the oracle's block manager appending the batch in order and tabling it,
+    over steps of a forked batch (shared blocks, copies, in-place writes) and
+    random growth."""
+    rng = np.random.default_rng(44)
+    nb, bs = 400, 8
+    order = rng.permutation(nb).tolist()
+    nat = libpa.BlockAllocator(nb, bs, order)
+    ref = oracle.BlockAllocator(nb, bs, order)
+    for a in (nat, ref):
+        a.add_seq(0, 29)
+        a.add_seq(1, 16)
+        a.add_seq(2, 0)
+        a.fork(0, 3)
+        a.fork(0, 4)
+        a.fork(1, 5)
+    ids = [4, 0, 1, 2, 3, 5]
+    mb = 12
+    for step in range(40):
+        batch = [s for s in ids if rng.random() < 0.8]
+        slots, pairs, table, lens = nat.plan_step(batch, mb)
+        es, ep, et = _oracle_step(ref, batch, mb)
+        assert slots.tolist() == es, step
+        assert [tuple(p) for p in pairs.tolist()] == ep, step
+        assert table.tolist() == et.tolist(), step
+        assert lens.tolist() == [ref.seq_len(s) for s in batch], step
+        _same(nat, ref, ids)
+    assert nat.stats()["cow_copies"] > 0
+
+
+def test_plan_step_into_caller_buffers(libpa):
+    """Outputs land in preallocated arrays (as the pinned input buffers of a
+    step), pairs first rows only; the first step of 128 forks of a 2040-token
+    prompt makes 127 copies and one in-place write."""
+    a = libpa.BlockAllocator(400, 16)
+    a.add_seq(0, 2040)
+    for c in range(1, 128):
+        a.fork(0, c)
+    n, mb = 128, 130
+    bufs = (np.full(n, -9, np.int32), np.full((n, 2), -9, np.int32),
+            np.full((n, mb), -9, np.int32), np.full(n, -9, np.int32))
+    slots, pairs, table, lens = a.plan_step(list(range(n)), mb, fill=-1, out=bufs)
+    assert slots.base is bufs[0] or slots.ctypes.data == bufs[0].ctypes.data
+    assert len(pairs) == 127 and pairs.ctypes.data == bufs[1].ctypes.data
+    assert (bufs[1][127:] == -9).all()
+    assert (lens == 2041).all() and (bufs[3] == 2041).all()
+    assert (table[:, 128:] == -1).all()
+    prompt_last = a.table(127)[127]       # the last holder wrote in place
+    assert all(p[0] == prompt_last for p in pairs.tolist())
+
+
+def test_plan_step_refusals_change_nothing(libpa):
+    a = libpa.BlockAllocator(6, 4, list(range(6)))
+    a.add_seq(0, 8)      # 2 blocks, full: grows on append
+    a.add_seq(1, 6)      # 2 blocks
+    a.fork(1, 2)         # shares 1's blocks: the append of 1 or 2 copies
+    before, st = a.export_state(), a.stats()
+    with pytest.raises(libpa.PaError):
+        a.plan_step([0, 7], 4)              # unknown sequence
+    with pytest.raises(libpa.PaError):
+        a.plan_step([0, 1, 0], 4)           # listed twice
+    with pytest.raises(libpa.PaError):
+        a.plan_step([0], 2)                 # 3 blocks after the append
+    assert a.export_state() == before
+    a.add_seq(3, 4)      # takes the last two free blocks... one block
+    a.add_seq(4, 4)
+    before = a.export_state()
+    # 0 grows (1 block) and 1 copies (1 block): 2 needed, 0 free
+    with pytest.raises(libpa.OutOfBlocksError):
+        a.plan_step([0, 1, 2], 4)
+    assert a.export_state() == before
+    assert a.stats()["alloc_failures"] == st["alloc_failures"] + 1
+    # 2 then 1: 2 copies (refcount 2 -> 1), 1 writes in place: 1 block; still 0 free
+    with pytest.raises(libpa.OutOfBlocksError):
+        a.plan_step([2], 4)
+    a.free_seq(4)
+    slots, pairs, table, lens = a.plan_step([2, 1], 4)
+    assert len(pairs) == 1 and lens.tolist() == [7, 7]

@@ -86,7 +86,9 @@ def test_mha_lognormal_full_size_sampled(pa):
     rng = np.random.default_rng(0)
     seqs = sorted(rng.choice(b.num_seqs, 12, replace=False).tolist())
     seqs.append(int(np.argmax(b.prefill_lens)))          # the longest sequence too
-    run_and_compare(pa, b, seqs=sorted(set(seqs)), heads=[0, 7, 31])
+    # every head of the sampled sequences: KV heads 0-7, 8-15, 16-23 and 24-31
+    # are the kernel's four head groups, each chunked separately at this size
+    run_and_compare(pa, b, seqs=sorted(set(seqs)))
 
 
 @pytest.mark.parametrize("bs", [8, 16, 32])
@@ -97,8 +99,10 @@ def test_long_context_small(pa, bs):
 
 @pytest.mark.parametrize("bs", [8, 16, 32])
 def test_long_context_full_size_sampled(pa, bs):
+    """16 x 32768 tokens, 64 q / 8 KV heads: every head of three sequences,
+    with every pool row no sequence reads poisoned."""
     b = synthetic.config5_long_context(block_size=bs)
-    run_and_compare(pa, b, seqs=[0, 9, 15], heads=[0, 5, 63], poison=False)
+    run_and_compare(pa, b, seqs=[0, 9, 15])
 
 
 # ---------------------------------------------------------------- edge cases --
@@ -220,3 +224,26 @@ def test_length_beyond_table_is_reported(pa):
     with pytest.raises(pa.PaError) as e:
         pa.pa_device_error()
     assert e.value.flags & pa.PA_DEVERR_BAD_LEN
+
+
+def test_lengths_written_by_the_kernel_just_before(pa):
+    """A serving loop that bumps the lengths on the device right before the
+    attention call: the attention kernel (a programmatic dependent of that
+    kernel) must read the new lengths, never the old ones. Lengths cross
+    block boundaries, so a stale read would change the result."""
+    # from L - 4 to L: 29 -> 33, 60 -> 64, 13 -> 17, 2045 -> 2049 cross blocks
+    lens_end = [31, 33, 64, 1200, 2049, 17, 5, 500]
+    q, kp, vp, table = _random_case(23, len(lens_end), 32, 8, 128, 16, lens_end)
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    dq, dk, dv, dt = d(q), d(kp), d(vp), d(table)
+    steps = 4
+    lens_dev = d(np.asarray([L - steps for L in lens_end], np.int32))
+    for k in range(steps):
+        lens_dev.add_(1)                 # the kernel just before the attention call
+        out = pa.pa_decode_attention(dq, dk, dv, dt, lens_dev, np.float32(0.088))
+        lens_now = [L - steps + k + 1 for L in lens_end]
+        torch.cuda.synchronize()
+        assert lens_dev.cpu().tolist() == lens_now
+        exp = oracle.decode_attention(q, kp, vp, table, lens_now, np.float32(0.088))
+        assert_close_attention(out.cpu().numpy(), exp, f"lengths bumped, step {k}")
+    assert pa.pa_device_error() == 0

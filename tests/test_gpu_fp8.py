@@ -131,12 +131,15 @@ def test_fp8_zero_length(pa):
     assert_close_attention(got, exp, "fp8 zero length")
 
 
-def test_fp8_gqa_batch_full_size_sampled(pa):
+@pytest.mark.parametrize("every_code", [False, True])
+def test_fp8_gqa_batch_full_size_sampled(pa, every_code):
     """The 64-sequence GQA batch (lengths U[128, 2048], 32q/8kv, D=128,
     BS=16) over an E4M3 cache, in the launch configuration the benchmark
-    uses; sampled sequences checked against the oracle."""
+    uses; every head of sampled sequences checked against the oracle. The
+    cache's codes are those of a scaled N(0,1) tensor, or every finite code
+    equally often (zeros, subnormals, every exponent field, +-448)."""
     b = synthetic.config2_gqa_batch()
-    c = synthetic.fp8_cache(b)
+    c = synthetic.fp8_cache(b, every_code=every_code)
     ref = oracle.decode_step(b, compute_attention=False)
     keep = used_rows_mask(ref.block_table, ref.seq_lens, b.num_blocks, b.block_size)
     kp, vp = c.k_pool.copy(), c.v_pool.copy()
@@ -180,3 +183,62 @@ def test_fp8_unsupported_shapes_are_refused(pa, D, BS):
     q, kp, vp, ks, vs, table = _fp8_case(50, 1, 2, 2, D, BS, lens)
     with pytest.raises(PaError):
         _attend(pa, q, kp, vp, ks, vs, table, lens, np.float32(0.1))
+
+
+# ---------------------------------------------------- every finite E4M3 code --
+def _every_code_case(seed, lens, G, Hkv, BS):
+    """Pools whose attended rows hold every finite E4M3 code (each equally
+    often, seeded order) and whose other rows hold the NaN code."""
+    rng = np.random.default_rng(seed)
+    S, D = len(lens), 128
+    mb = max(1, max(-(-L // BS) for L in lens))
+    nb = sum(-(-L // BS) for L in lens) + 3
+    perm = rng.permutation(nb)
+    table = -np.ones((S, mb), np.int32)
+    pos = 0
+    for i, L in enumerate(lens):
+        n = -(-L // BS)
+        table[i, :n] = perm[pos:pos + n]
+        pos += n
+    keep = used_rows_mask(table, lens, nb, BS)
+    kp = np.full((nb, BS, Hkv, D), NAN8, np.uint8)
+    vp = np.full((nb, BS, Hkv, D), NAN8, np.uint8)
+    rows = int(keep.sum())
+    kp[keep] = synthetic.fp8_codes_every_finite(rng, (rows, Hkv, D))
+    vp[keep] = synthetic.fp8_codes_every_finite(rng, (rows, Hkv, D))
+    finite = set(synthetic.fp8_finite_codes().tolist())
+    assert set(np.unique(kp[keep]).tolist()) == finite
+    assert set(np.unique(vp[keep]).tolist()) == finite
+    q = rng.standard_normal((S, G * Hkv, D)).astype(np.float16)
+    ks, vs = _scales(rng, Hkv)
+    return q, kp, vp, ks, vs, table
+
+
+@pytest.mark.parametrize("layout", ["pools", "records"])
+@pytest.mark.parametrize("BS", [16, 32])
+@pytest.mark.parametrize("G", [1, 4, 8])
+def test_fp8_every_finite_code(pa, layout, BS, G):
+    """Attention over E4M3 pools holding every finite code (zero and -0,
+    +-subnormals, exponent fields 1..15, the saturation value +-448), in two
+    pools and in the one-pool record layout, against the oracle's attention
+    of the decoded values."""
+    lens = [1, BS - 1, BS, BS + 1, 300, 777]
+    Hkv = 2
+    q, kp, vp, ks, vs, table = _every_code_case(600 + 10 * BS + G, lens, G, Hkv, BS)
+    scale = np.float32(1 / math.sqrt(128))
+    if layout == "pools":
+        got = _attend(pa, q, kp, vp, ks, vs, table, lens, scale)
+        exp = oracle.decode_attention_fp8(q, kp, vp, ks, vs, table, lens, scale)
+    else:
+        recs = oracle.make_kv_pool(kp, vp)
+        raw = recs.view(np.uint8).reshape(len(recs), 2, BS, Hkv, 128)
+        kv = d(raw)
+        k, v = pa.kv_views(kv)
+        out = pa.pa_decode_attention_fp8(d(q), k, v, d(ks), d(vs), d(table),
+                                         d(np.asarray(lens, np.int32)), scale)
+        torch.cuda.synchronize()
+        got = out.cpu().numpy()
+        exp = oracle.decode_attention_interleaved_fp8(q, recs, ks, vs, table, lens, scale)
+    assert np.isfinite(got).all()
+    assert_close_attention(got, exp, f"fp8 every code {layout} BS{BS} G{G}")
+    assert pa.pa_device_error() == 0

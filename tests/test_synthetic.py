@@ -57,3 +57,21 @@ def test_fp8_cache_is_seeded_and_finite():
         e = (pool >> 3) & 0xF
         assert e.min() >= 8 and e.max() <= 14
     assert (a1.k_scale > 0).all() and (a1.v_scale > 0).all()
+
+
+def test_every_finite_code_generator():
+    codes = synthetic.fp8_finite_codes()
+    assert codes.size == 254 and codes.dtype == np.uint8
+    assert 0x7F not in codes and 0xFF not in codes
+    for c in (0x00, 0x80, 0x01, 0x07, 0x08, 0x7E, 0xFE, 0x3F):   # zeros, subnormals, 448
+        assert c in codes
+    rng = np.random.default_rng(3)
+    a = synthetic.fp8_codes_every_finite(rng, (5, 16, 2, 128))     # 20480 = 80 tiles + 160
+    counts = np.bincount(a.reshape(-1), minlength=256)
+    assert counts[0x7F] == 0 and counts[0xFF] == 0
+    fin = counts[codes]
+    assert fin.min() >= 80 and fin.max() <= 81 and fin.sum() == a.size
+    b = synthetic.fp8_codes_every_finite(np.random.default_rng(3), (5, 16, 2, 128))
+    assert (a == b).all()
+    c = synthetic.fp8_cache(synthetic.config1_tiny(), seed=5, every_code=True)
+    assert set(np.unique(c.k_pool).tolist()) == set(codes.tolist())
