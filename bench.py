@@ -408,6 +408,113 @@ def run_swap(args):
     }), flush=True)
 
 
+# ------------------------------------------------- end to end with planning --
+def time_planned(args, b, fp8, dev, stream, flush, world, steps):
+    """Decode steps whose timed region includes the host block manager.
+
+    serial: per step, with the stream idle, an event, then the step planned
+    (pa_alloc_plan_step into pinned host memory), its kernels launched and a
+    second event: planning, launch and the kernels, one after the other;
+    L2 flushed between steps outside the events.
+    overlap: steps back to back with no wait, step k+1 planned on the host
+    while the kernels of step k run (two rotating sets of plan buffers); one
+    event before the first step and one after the last. Inputs (the K/V the
+    steps read) are larger than L2, which is not flushed in this loop.
+    Both report KV GB/s over the bytes the steps actually attended (the
+    sequences grow by one token a step)."""
+    import torch
+    from paged_kv_cache_40_gb300.engine import DecodeBatchRunner
+    # the tokens every sequence may grow by in the batch's pool, and the
+    # steps of each loop that fit (both loops and their warm-up grow them)
+    bs = b.block_size
+    lens0 = [int(L) for L in b.prefill_lens]
+    free = int(b.num_blocks) - sum(-(-L // bs) for L in lens0)
+    grow = 0
+    while sum(-(-(L + grow + 1) // bs) - -(-L // bs) for L in lens0) <= free:
+        grow += 1
+    steps = min(steps, grow // 2 - args.warmup)
+    if steps < 10:
+        return {"skipped": f"the pool leaves room for {grow} more tokens per sequence"}
+    mb = int(max(-(-(L + grow) // bs) for L in lens0))
+    kw = dict(device=dev, partition_tokens=args.partition, layout=args.layout, max_blocks=mb)
+    if fp8 is not None:
+        kw.update(kv_dtype="fp8", k_pool=fp8.k_pool, v_pool=fp8.v_pool, k_scale=fp8.k_scale,
+                  v_scale=fp8.v_scale)
+    run = DecodeBatchRunner(b, **kw)
+    h2d = run.host_planned(sets=2)
+    out_h = torch.empty(run.out.shape, dtype=run.out.dtype).pin_memory()
+    run.out = out_h
+    esize = 1 if fp8 is not None else 2
+    per_tok = b.num_kv_heads * b.head_dim * esize * 2
+    native = fp8 is None
+    if native:
+        run.prepare_native_steps(stream)
+
+    def one():
+        if native:      # pa_decode_step: plan, copies, append, attention in one call
+            plan = run.run_native_step()
+        else:
+            plan = run.plan_step_host()
+            run.run_step()
+        return int(plan.seq_lens.astype(np.int64).sum())
+
+    for _ in range(args.warmup):
+        flush()
+        one()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    toks, host_s = 0, 0.0
+    for k in range(steps):
+        flush()
+        torch.cuda.synchronize(dev)
+        ev[k][0].record(stream)
+        t0 = time.perf_counter()
+        toks += one()
+        host_s += time.perf_counter() - t0
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    serial_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    serial_gbs, _, t_serial = aggregate(toks * per_tok, 0, 1, sum(serial_ms) / 1e3, world)
+    # overlapped: plan k+1 while step k runs; a set of plan buffers is reused
+    # only after the step that read it has completed
+    done = [torch.cuda.Event() for _ in range(steps)]
+    flush()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    toks_o = 0
+    e0.record(stream)
+    for k in range(steps):
+        if k >= 2:
+            done[k - 2].synchronize()
+        toks_o += one()
+        done[k].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    over_ms = e0.elapsed_time(e1)
+    over_gbs, _, t_over = aggregate(toks_o * per_tok, 0, 1, over_ms / 1e3, world)
+    import paged_kv_cache_40_gb300 as pa
+    assert pa.pa_device_error() == 0
+    d2h = out_h.numel() * out_h.element_size()
+    return {
+        "call": "pa_decode_step (one library call per step)" if native else
+                "pa_alloc_plan_step, then the kernel calls through the Python binding",
+        "value": round(serial_gbs, 2), "unit": "GB/s", "steps": steps,
+        "ms_per_step": round(1e3 * t_serial / steps, 5),
+        "host_plan_and_launch_us_per_step": round(1e6 * host_s / steps, 2),
+        "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+        "path": "per step with the stream idle: block-manager plan (one call) into pinned host "
+                "memory, then the step's kernels reading it in place; events around both; L2 "
+                "flushed between steps outside the events",
+        "overlap": {"value": round(over_gbs, 2), "unit": "GB/s",
+                    "ms_per_step": round(1e3 * t_over / steps, 5),
+                    "path": "steps back to back, step k+1 planned while step k runs (two sets "
+                            "of plan buffers); events around the whole loop; no L2 flush "
+                            "(the K/V read per step exceed L2)"},
+    }
+
+
 # ----------------------------------------------------------------- our arm --
 def run_ours(args, world, rank, local):
     import torch
@@ -458,15 +565,15 @@ def run_ours(args, world, rank, local):
             a.add_seq(i, int(b.prefill_lens[i]))
     # the binding's first-call costs (imports, ctypes set-up) are paid by calls
     # that change no state: an empty batch and a table build
-    ids = list(range(b.num_seqs))
-    a.append_slots([])
-    a.build_tables(ids, run.max_blocks)
-    host_us = []
+    ids = np.arange(b.num_seqs, dtype=np.int64)
     width = run.max_blocks + 2 + 11 // b.block_size  # room for eleven more tokens
+    bufs = (np.empty(b.num_seqs, np.int32), np.empty((b.num_seqs, 2), np.int32),
+            np.empty((b.num_seqs, width), np.int32), np.empty(b.num_seqs, np.int32))
+    a.plan_step(ids[:0], width, out=bufs)
+    host_us = []
     for _ in range(11):  # the step above, then ten more (the sequences grow)
         t_host0 = time.perf_counter()
-        a.append_slots(ids)
-        a.build_tables(ids, width)
+        a.plan_step(ids, width, out=bufs)       # one call: slots, copy pairs, tables, lengths
         host_us.append((time.perf_counter() - t_host0) * 1e6)
     t_host_first, t_host = host_us[0], statistics.median(host_us[1:])
     a.close()
@@ -567,6 +674,14 @@ def run_ours(args, world, rank, local):
     e2e_ms = time_e2e(run.run_step)
     run.out = dev_out
 
+    # end to end with the block manager inside the timed region: a decode
+    # loop on a second copy of the batch whose sequences grow by one token a
+    # step; each step is planned by one block-manager call straight into
+    # pinned host memory, which the kernels read in place
+    planned = None
+    if not shared:
+        planned = time_planned(args, b, fp8, dev, stream, flush, world, Ke)
+
     kvb = run.kv_bytes()
     tokens = int(plan.seq_lens.astype(np.int64).sum())
     value, tok_per_s, t_steps = aggregate(kvb, tokens, K, sum(step_ms) / 1e3, world)
@@ -618,6 +733,7 @@ def run_ours(args, world, rank, local):
                      "peak_source": peak_kind,
                      "kernel": "paged_decode_kernel",
                      "bytes_per_launch": run.io_bytes()},
+        "e2e_planned": planned,
         "e2e": {"value": round(value_e2e, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(1e3 * t_e2e / Ke, 5), "steps": Ke,

@@ -484,6 +484,32 @@ PA_API pa_status pa_alloc_plan_step(pa_allocator* a, const int64_t* seq_ids, int
                              int32_t* cow_pairs, int* num_cow, int32_t* table,
                              int32_t* seq_lens);
 
+/* One decode step in one call: pa_alloc_plan_step for the batch seq_ids
+ * (tables padded with -1), then, on `stream`, pa_copy_blocks of its
+ * copy-on-write pairs (if any), pa_append_kv of every sequence's new K/V row
+ * and pa_decode_attention over the tables and lengths just planned ("Phase 7
+ * · Document 04 — PagedAttention", §2 on-demand allocation and block
+ * sharing; lux-666 notes "PagedAttention", 最小模型). The plan is written
+ * into slot_mapping [n], cow_pairs [n][2] (*num_cow rows), block_table
+ * [n][max_blocks] and seq_lens [n]: pinned host memory, which the kernels
+ * read in place through its device mapping (the host writes them before the
+ * launches; they must not be rewritten until this step's kernels have
+ * completed). The block size is the block manager's; num_blocks must be its
+ * pool size. q, k_new, v_new, the pools, out and the workspace are as in the
+ * calls above (k_new/v_new row i and q row i belong to seq_ids[i]).
+ * Errors: those of the four calls. A refused plan launches nothing and
+ * changes nothing; an error after the plan leaves the block manager
+ * advanced by the step. */
+PA_API pa_status pa_decode_step(pa_allocator* a, const int64_t* seq_ids, int num_seqs,
+                         int max_blocks, int32_t* slot_mapping, int32_t* cow_pairs,
+                         int32_t* block_table, int32_t* seq_lens, int* num_cow,
+                         const pa_half* q, const pa_half* k_new, const pa_half* v_new,
+                         pa_half* k_pool, pa_half* v_pool, int num_q_heads,
+                         int num_kv_heads, int head_dim, int num_blocks,
+                         int64_t pool_block_stride, float scale, pa_half* out,
+                         void* workspace, size_t workspace_bytes, int partition_tokens,
+                         pa_stream_t stream);
+
 /* Dense tables for a batch: table host int32 [n][max_blocks] (rows padded
  * with `fill`), seq_lens host int32 [n] = current lengths. */
 PA_API pa_status pa_alloc_build_tables(const pa_allocator* a, const int64_t* seq_ids,

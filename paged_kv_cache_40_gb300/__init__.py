@@ -439,6 +439,53 @@ def pa_decode_attention_fixed_scratch(q, k_pool, v_pool, block_table, seq_lens, 
     return out
 
 
+class PreparedDecodeStep:
+    """pa_decode_step with its arguments marshalled once: the block manager
+    plans each call's step into `plan` (slots [n], copy-on-write pairs
+    [n][2], table [n][max_blocks], lengths [n]: pinned int32 host tensors
+    that the kernels read in place), then the copies, the append and the
+    attention are enqueued on `stream`, all in one library call. The
+    tensors are fixed for the object's life; each call returns the number of
+    copy-on-write pairs it planned."""
+
+    def __init__(self, alloc, seq_ids, max_blocks, plan, q, k_new, v_new, k_pool, v_pool, scale,
+                 out, workspace, partition_tokens: int = 0, stream=None):
+        torch = _torch()
+        nb, bs, hkv, d, stride = _pool_dims(k_pool, v_pool)
+        if bs != alloc.block_size or nb != alloc.num_blocks:
+            raise ValueError("the pools and the block manager differ in block size or blocks")
+        self.seq_ids = np.ascontiguousarray(seq_ids, dtype=np.int64).reshape(-1)
+        n = int(self.seq_ids.size)
+        slots, pairs, table, lens = plan
+        for t, shape, name in ((slots, (n,), "slots"), (pairs, (n, 2), "pairs"),
+                               (table, (n, max_blocks), "table"), (lens, (n,), "lens")):
+            if t.is_cuda or not t.is_pinned() or t.dtype != torch.int32 or \
+                    not t.is_contiguous() or tuple(t.shape) != shape:
+                raise ValueError(f"plan {name} must be a pinned int32 host tensor of shape {shape}")
+        if q.dim() != 3 or int(q.shape[0]) != n or int(q.shape[2]) != d:
+            raise ValueError("q must be [num_seqs][num_q_heads][head_dim]")
+        hq = int(q.shape[1])
+        self.plan = plan
+        self._keep = (alloc, q, k_new, v_new, k_pool, v_pool, out, workspace)
+        self._ncow = ctypes.c_int()
+        ids = self.seq_ids if n else np.zeros(1, np.int64)
+        self._ids = ids
+        self._fn = _load().pa_decode_step
+        self._args = (alloc._h, ids.ctypes.data, n, max_blocks,
+                      ctypes.c_void_p(slots.data_ptr()), ctypes.c_void_p(pairs.data_ptr()),
+                      ctypes.c_void_p(table.data_ptr()), ctypes.c_void_p(lens.data_ptr()),
+                      ctypes.byref(self._ncow), _in(q, "q", torch.float16),
+                      _in(k_new, "k_new", torch.float16), _in(v_new, "v_new", torch.float16),
+                      _pool(k_pool, "k_pool", torch.float16), _pool(v_pool, "v_pool", torch.float16),
+                      hq, hkv, d, nb, stride, ctypes.c_float(float(scale)), _out(out, q),
+                      _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+                      partition_tokens, _stream_ptr(stream))
+
+    def __call__(self) -> int:
+        _check(self._fn(*self._args))
+        return self._ncow.value
+
+
 def pa_device_error(stream=None) -> int:
     """Read and clear the device error word (synchronises the stream).
     Returns the PA_DEVERR_* bit set; raises PaError if any bit was set."""
@@ -538,10 +585,8 @@ class BlockAllocator:
             out = (np.empty(max(n, 1), np.int32), np.empty((max(n, 1), 2), np.int32),
                    np.empty((max(n, 1), max_blocks), np.int32), np.empty(max(n, 1), np.int32))
         slots, pairs, table, lens = out
-        for arr, shape in ((slots, (n,)), (pairs, (n, 2)), (table, (n, max_blocks)),
-                           (lens, (n,))):
-            if (arr.dtype != np.int32 or not arr.flags.c_contiguous
-                    or tuple(arr.shape[:len(shape)]) < shape or arr.size < int(np.prod(shape))):
+        for arr, need in ((slots, n), (pairs, 2 * n), (table, n * max_blocks), (lens, n)):
+            if arr.dtype != np.int32 or not arr.flags.c_contiguous or arr.size < need:
                 raise ValueError("plan_step outputs must be contiguous int32 arrays of "
                                  "[n], [n][2], [n][max_blocks], [n]")
         ncow = ctypes.c_int()

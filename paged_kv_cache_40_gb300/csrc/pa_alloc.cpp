@@ -163,6 +163,11 @@ pa_status append_to(pa_allocator* a, pa_allocator::Seq& s, int64_t seq_id, int32
 }
 }  // namespace
 
+namespace pa {
+int alloc_block_size(const pa_allocator* a) { return a->block_size; }
+int alloc_num_blocks(const pa_allocator* a) { return a->num_blocks; }
+}  // namespace pa
+
 extern "C" {
 
 pa_status pa_alloc_create(int num_blocks, int block_size, const int32_t* order,

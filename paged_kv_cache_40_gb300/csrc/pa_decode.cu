@@ -497,29 +497,38 @@ struct MsgMeta {
 };
 
 // Counts one arrival of a cut segment's head on its tagged counter word and
-// returns true for the arrival that completes the count (E arrivals), which
-// also puts the word back to zero so that a later call, even one with the
-// same tag (a replayed launch), starts from no arrivals. A word whose tag is
-// not this call's is stale and counts as zero. Each compare-and-swap starts
-// from a guess of the word: `guess_last` guesses that this is the last
-// arrival (E - 1 arrivals so far), otherwise that it is the first (a zero
-// word). A failed attempt returns the current word, and every failure means
-// another arrival succeeded, so at most E + 1 attempts are made (false, with
-// PA_DEVERR_TIMEOUT, if that were ever exceeded).
+// returns true for the arrival that completes the count (E >= 2 arrivals),
+// which also puts the word back to zero so that a later call, even one with
+// the same tag (a replayed launch), starts from no arrivals. A word whose tag
+// is not this call's (zero, or left by an earlier call) counts as none: the
+// first arrival installs the tag with a compare-and-swap from `seen`, the
+// caller's guess of the word (0 if it has none; retried from the value each
+// failure returns, until the tag is there). Every other arrival is one
+// atomic add, a single round trip to L2 whatever the others do.
 __device__ __forceinline__ bool arrive_last(unsigned long long* word, unsigned long long tag,
-                                            unsigned E, bool guess_last, int32_t* err) {
+                                            unsigned E, unsigned long long seen, int32_t* err) {
   constexpr unsigned long long kCountMask = (1ull << kArrivalBits) - 1;
-  unsigned long long cur = guess_last ? (tag << kArrivalBits) | (E - 1) : 0ull;
-  for (unsigned i = 0; i <= E + 1; ++i) {
-    const unsigned long long seen = (cur >> kArrivalBits) == tag ? (cur & kCountMask) : 0ull;
-    const bool last = seen + 1 == E;
-    const unsigned long long want = last ? 0ull : (tag << kArrivalBits) | (seen + 1);
-    const unsigned long long got = atomicCAS(word, cur, want);
-    if (got == cur) return last;
-    cur = got;
+  if ((seen >> kArrivalBits) != tag) {
+    for (int i = 0;; ++i) {
+      if (i == 4096) {
+        atomicOr(err, PA_DEVERR_TIMEOUT);
+        return false;
+      }
+      const unsigned long long got = atomicCAS(word, seen, (tag << kArrivalBits) | 1ull);
+      if (got == seen) return false;  // the first of E >= 2 arrivals
+      if ((got >> kArrivalBits) == tag) break;
+      seen = got;
+    }
   }
-  atomicOr(err, PA_DEVERR_TIMEOUT);
-  return false;
+  const unsigned long long old = atomicAdd(word, 1ull);
+  if ((old >> kArrivalBits) != tag || (old & kCountMask) + 1 > E) {
+    atomicOr(err, PA_DEVERR_TIMEOUT);  // cannot happen: the tag stays until the count is full
+    return false;
+  }
+  if ((old & kCountMask) + 1 < E) return false;
+  // the last arrival: no other arrival of this call is left to touch the word
+  *reinterpret_cast<volatile unsigned long long*>(word) = 0ull;
+  return true;
 }
 
 // Shared-prefix mode: wait for the prefix kernel (the grid launched just
@@ -898,7 +907,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           p.counters + static_cast<long long>(msg.seq) * Hkv + static_cast<long long>(msg.hg) * HG;
       const bool mine = lane < HG && lane % kMergeWarps == mw;
       const bool done =
-          mine && arrive_last(words + lane, p.tag, static_cast<unsigned>(E), false, p.err);
+          mine && arrive_last(words + lane, p.tag, static_cast<unsigned>(E), 0ull, p.err);
       unsigned last = __ballot_sync(0xffffffffu, done);
       if (last) fence_acq_rel_gpu();  // acquire: the other chunks' records are visible
       while (last) {
@@ -1354,12 +1363,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             unsigned long long* word = p.counters + static_cast<long long>(pm.seq) * Hkv + kvh;
             const unsigned long long claim = (p.tag << kArrivalBits) | static_cast<unsigned>(E - 1);
             int done = 0;
-            if (lane == 0) done = atomicCAS(word, claim, 0ull) == claim;
+            unsigned long long seen = 0;
+            if (lane == 0) {
+              seen = atomicCAS(word, claim, 0ull);
+              done = seen == claim;
+            }
             done = __shfl_sync(0xffffffffu, done, 0);
             if (!done) {
               fence_acq_rel_gpu();  // release: the record is visible before the arrival
               __syncwarp();
-              if (lane == 0) done = arrive_last(word, p.tag, static_cast<unsigned>(E), false, p.err);
+              // the failed claim returned the word: the arrival starts from it
+              if (lane == 0) done = arrive_last(word, p.tag, static_cast<unsigned>(E), seen, p.err);
               done = __shfl_sync(0xffffffffu, done, 0);
             }
             if (done) {
@@ -1425,6 +1439,8 @@ constexpr int kPfxTile = kPfxTok * 256;         // one operand tile: 128 rows x 
 // barriers, then the 1024-aligned tiles Q, K[stages], V[stages]
 constexpr int kPfxHead = 256;
 constexpr int kPfxSmem = 1024 + kPfxHead + (1 + kPfxKStages + kPfxVStages) * kPfxTile;
+constexpr int kFusedSuffixTokens = 32;          // fused mode: the longest suffix past the prefix
+constexpr int kMaxCluster = 8;                  // fused mode: prefix chunks (cluster size) at most
 
 struct PrefixParams {
   const __half* q;
@@ -1438,7 +1454,29 @@ struct PrefixParams {
   int prefix_blocks_n;
   int chunk_blocks;              // prefix blocks per chunk
   float qscale;                  // scale * log2(e)
+  // fused mode (every suffix at most kFusedSuffixTokens tokens): the chunks
+  // of one (row tile, KV head) form a cluster, merge their partials through
+  // distributed shared memory and attend each sequence's suffix themselves
+  const int32_t* block_table;    // [S][max_blocks]
+  const int32_t* seq_lens;       // [S]
+  const __half* k_pool;          // the pools, read row by row for the suffix
+  const __half* v_pool;
+  long long block_stride;        // values from one pool block to the next
+  __half* out;                   // [S][Hq][D]
+  int max_blocks;
 };
+
+// Shared-memory helpers of a thread-block cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+// The same shared-memory address in the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
 
 // ---- tcgen05 ----------------------------------------------------------------
 // Shared-memory operand descriptor: a tile of rows of 128 bytes with the
@@ -1533,7 +1571,262 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Fused mode: the rows one CTA of a cluster of C finishes, [c * 128 / C,
+// (c + 1) * 128 / C) of the row tile, and the sequences they belong to.
+// Their suffix rows (the tokens past the prefix, at most kFusedSuffixTokens
+// per sequence) are asked of L2 early, so the end of the kernel finds them
+// there; called by the four softmax warps while they wait for the first S.
 template <int BS, int G>
+__device__ __forceinline__ void prefetch_suffix_rows(const PrefixParams& p, int kvh, int c) {
+  constexpr int D = 128;
+  const int C = gridDim.z, rpc = kPfxRows / C;
+  const int r0 = blockIdx.x * kPfxRows + c * rpc;
+  const int s_lo = r0 / G, s_hi = min(p.num_seqs, (r0 + rpc + G - 1) / G);
+  const int P = p.prefix_blocks_n;
+  const int ntok = (p.max_blocks - P) * BS;
+  for (int i = threadIdx.x; i < (s_hi - s_lo) * ntok; i += kPfxSoftmaxWarps * 32) {
+    const int sq = s_lo + i / ntok, t = i % ntok;
+    const int L = min(p.seq_lens[sq], p.max_blocks * BS);
+    if (t >= L - P * BS) continue;
+    const int blk = p.block_table[static_cast<long long>(sq) * p.max_blocks + P + t / BS];
+    if (blk < 0 || blk >= p.num_blocks) continue;
+    const long long off = static_cast<long long>(blk) * p.block_stride +
+                          (static_cast<long long>(t % BS) * p.num_kv_heads + kvh) * D;
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.k_pool + off));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.k_pool + off + 64));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.v_pool + off));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.v_pool + off + 64));
+  }
+}
+
+// Bulk copy of `bytes` from this CTA's shared memory to shared memory of
+// another CTA of the cluster (`dst`, `bar`: shared::cluster addresses there),
+// counted on that CTA's barrier.
+__device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                    uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst),
+      "r"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Fused mode, after the cluster barrier: each CTA finishes rows [c * 128 / C,
+// (c + 1) * 128 / C) of the tile. Every chunk's CTA staged its rows'
+// partials (max and sum in log2 units, then the accumulator; rows of D + 4
+// floats) in its own shared memory at `stage`; each now sends the other
+// CTAs their rows with one bulk copy each into their `recv` area (slot =
+// sender's rank), counted on their `recv_bar`. A row's C partials are merged
+// with the log-sum-exp rule, then the row attends its sequence's suffix (the
+// tokens past the prefix, at most kFusedSuffixTokens) on CUDA cores,
+// continuing that running softmax eight tokens at a time, and the result is
+// written as fp16. Eight threads share a row, 16 dimensions each; a score is
+// their dot products summed by shuffles within the group.
+template <int BS, int G>
+__device__ __forceinline__ void fused_merge_and_suffix(const PrefixParams& p, const float* stage,
+                                                       float* recv, uint64_t* recv_bar, int kvh,
+                                                       int c) {
+  constexpr int D = 128, kPad = D + 4, TPR = 8, DPT = D / TPR, kGrp = 8;
+  const int C = gridDim.z, rpc = kPfxRows / C;
+  const int S = p.num_seqs, P = p.prefix_blocks_n, cap = p.max_blocks * BS;
+  const int part = threadIdx.x % TPR;
+  const uint32_t rows_bytes = static_cast<uint32_t>(rpc * kPad * 4);
+  // ---- exchange: my rows of every other chunk's partials arrive here ----
+  if (C > 1) {
+    if (threadIdx.x == 0) {
+      for (int k = 0; k < C; ++k) {
+        if (k == c) continue;
+        bulk_copy_s2cluster(cluster_map(smem_addr(recv) + c * rows_bytes, k),
+                            smem_addr(stage) + k * rows_bytes, rows_bytes,
+                            cluster_map(smem_addr(recv_bar), k));
+      }
+    }
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(smem_addr(recv_bar), 0) && global_ns() - t0 < kWaitLimitNs) {
+    }
+  }
+  // every lane of a warp runs the same rows loop (rpc is a multiple of 4)
+#pragma unroll 1
+  for (int lr = threadIdx.x / TPR; lr < rpc; lr += kPfxThreads / TPR) {
+    const int rt = c * rpc + lr;
+    const int row = blockIdx.x * kPfxRows + rt;
+    const int seq = row / G, gg = row % G;
+    const bool live = seq < S;
+    // this row's suffix length and, meanwhile, its q slice
+    int suf = 0;
+    uint4 qa = make_uint4(0, 0, 0, 0), qb = qa;
+    if (live) {
+      const __half* qrow =
+          p.q + (static_cast<long long>(seq) * p.num_q_heads + kvh * G + gg) * D + part * DPT;
+      qa = *reinterpret_cast<const uint4*>(qrow);
+      qb = *reinterpret_cast<const uint4*>(qrow + 8);
+      int Ls = p.seq_lens[seq];
+      if (Ls < P * BS || Ls > cap) {
+        if (part == 0 && gg == 0) atomicOr(p.err, PA_DEVERR_BAD_LEN);
+        Ls = Ls < 0 ? 0 : (Ls > cap ? cap : Ls);
+      }
+      suf = min(max(Ls - P * BS, 0), kFusedSuffixTokens);
+    }
+    // ---- merge the C chunk partials of the row (local shared memory) ----
+    auto src = [&](int k) -> const float* {
+      return k == c ? stage + rt * kPad : recv + k * rpc * kPad + lr * kPad;
+    };
+    float M = -INFINITY;
+#pragma unroll 1
+    for (int k = 0; k < C; ++k) M = fmaxf(M, src(k)[D]);
+    const float mu = M == -INFINITY ? 0.f : M;
+    float acc[DPT], L = 0.f;
+#pragma unroll
+    for (int i = 0; i < DPT; ++i) acc[i] = 0.f;
+#pragma unroll 1
+    for (int k = 0; k < C; ++k) {
+      const float* r = src(k);
+      const float mk = r[D];
+      if (mk != -INFINITY) {
+        const float w = fast_exp2(mk - mu);
+        L += w * r[D + 1];
+#pragma unroll
+        for (int i = 0; i < DPT; i += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(r + part * DPT + i);
+          acc[i] += w * v.x;
+          acc[i + 1] += w * v.y;
+          acc[i + 2] += w * v.z;
+          acc[i + 3] += w * v.w;
+        }
+      }
+    }
+    // ---- the suffix: tokens P * BS .. L - 1 of the sequence ----
+    float qv[DPT];
+    {
+      const __half2* h = reinterpret_cast<const __half2*>(&qa);
+      const __half2* h2 = reinterpret_cast<const __half2*>(&qb);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(h[i]), f2 = __half22float2(h2[i]);
+        qv[2 * i] = f.x;
+        qv[2 * i + 1] = f.y;
+        qv[8 + 2 * i] = f2.x;
+        qv[8 + 2 * i + 1] = f2.y;
+      }
+    }
+    // the suffix's block ids, loaded and checked once
+    constexpr int kSufBlocks = (kFusedSuffixTokens + BS - 1) / BS;
+    int blk[kSufBlocks];
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < kSufBlocks; ++j) {
+      blk[j] = -1;
+      if (j * BS < suf) {
+        blk[j] = p.block_table[static_cast<long long>(seq) * p.max_blocks + P + j];
+        if (blk[j] < 0 || blk[j] >= p.num_blocks) {
+          bad = true;
+          blk[j] = -1;
+        }
+      }
+    }
+    if (bad && part == 0) atomicOr(p.err, PA_DEVERR_BAD_BLOCK);
+    // pool offset of suffix token t of this row's KV head (-1: not read)
+    auto row_off = [&](int t) -> long long {
+      int b = blk[0];
+#pragma unroll
+      for (int j = 1; j < kSufBlocks; ++j)
+        if (t >= j * BS) b = blk[j];
+      if (t >= suf || b < 0) return -1;
+      return static_cast<long long>(b) * p.block_stride +
+             (static_cast<long long>(t % BS) * p.num_kv_heads + kvh) * D + part * DPT;
+    };
+    int suf_w = suf;  // the warp's longest suffix: every lane runs the shuffles
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) suf_w = max(suf_w, __shfl_xor_sync(0xffffffffu, suf_w, off));
+    // running softmax over the suffix from the merged prefix, eight tokens
+    // at a time: all their rows are loaded before any is used
+    float m_run = M;
+    const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll 1
+    for (int t0 = 0; t0 < suf_w; t0 += kGrp) {
+      uint4 kx[kGrp][2], vx[kGrp][2];
+      bool ok[kGrp];
+#pragma unroll
+      for (int u = 0; u < kGrp; ++u) {
+        const long long off = row_off(t0 + u);
+        ok[u] = off >= 0;
+        kx[u][0] = ok[u] ? *reinterpret_cast<const uint4*>(p.k_pool + off) : z;
+        kx[u][1] = ok[u] ? *reinterpret_cast<const uint4*>(p.k_pool + off + 8) : z;
+        vx[u][0] = ok[u] ? *reinterpret_cast<const uint4*>(p.v_pool + off) : z;
+        vx[u][1] = ok[u] ? *reinterpret_cast<const uint4*>(p.v_pool + off + 8) : z;
+      }
+      float sc[kGrp];
+#pragma unroll
+      for (int u = 0; u < kGrp; ++u) {
+        const __half2* h = reinterpret_cast<const __half2*>(&kx[u][0]);
+        const __half2* h2 = reinterpret_cast<const __half2*>(&kx[u][1]);
+        float d = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(h[i]), f2 = __half22float2(h2[i]);
+          d = fmaf(qv[2 * i], f.x, d);
+          d = fmaf(qv[2 * i + 1], f.y, d);
+          d = fmaf(qv[8 + 2 * i], f2.x, d);
+          d = fmaf(qv[8 + 2 * i + 1], f2.y, d);
+        }
+        sc[u] = d;
+      }
+      float gm = m_run;
+#pragma unroll
+      for (int u = 0; u < kGrp; ++u) {
+        float d = sc[u];
+        d += __shfl_xor_sync(0xffffffffu, d, 1);
+        d += __shfl_xor_sync(0xffffffffu, d, 2);
+        d += __shfl_xor_sync(0xffffffffu, d, 4);
+        sc[u] = ok[u] ? d * p.qscale : -INFINITY;
+        gm = fmaxf(gm, sc[u]);
+      }
+      if (gm != -INFINITY) {
+        const float cf = m_run == -INFINITY ? 0.f : fast_exp2(m_run - gm);
+        L *= cf;
+#pragma unroll
+        for (int i = 0; i < DPT; ++i) acc[i] *= cf;
+#pragma unroll
+        for (int u = 0; u < kGrp; ++u) {
+          if (ok[u]) {
+            const float w = fast_exp2(sc[u] - gm);
+            L += w;
+            const __half2* h = reinterpret_cast<const __half2*>(&vx[u][0]);
+            const __half2* h2 = reinterpret_cast<const __half2*>(&vx[u][1]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 f = __half22float2(h[i]), f2 = __half22float2(h2[i]);
+              acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
+              acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
+              acc[8 + 2 * i] = fmaf(w, f2.x, acc[8 + 2 * i]);
+              acc[8 + 2 * i + 1] = fmaf(w, f2.y, acc[8 + 2 * i + 1]);
+            }
+          }
+        }
+        m_run = gm;
+      }
+    }
+    if (live) {
+      // the merged prefix and the suffix are relative to m_run (or to the
+      // prefix's max when the suffix is empty): the sum L normalises both
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      uint4 o0, o1;
+      uint32_t* w0 = reinterpret_cast<uint32_t*>(&o0);
+      uint32_t* w1 = reinterpret_cast<uint32_t*>(&o1);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        w0[i] = pack_half2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+        w1[i] = pack_half2(acc[8 + 2 * i] * inv, acc[8 + 2 * i + 1] * inv);
+      }
+      __half* orow = p.out + (static_cast<long long>(seq) * p.num_q_heads + kvh * G + gg) * D +
+                     part * DPT;
+      *reinterpret_cast<uint4*>(orow) = o0;
+      *reinterpret_cast<uint4*>(orow + 8) = o1;
+    }
+  }
+}
+
+template <int BS, int G, bool FUSED>
 __global__ void __launch_bounds__(kPfxThreads, 1)
     paged_prefix_kernel(const PrefixParams p, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap) {
@@ -1558,7 +1851,8 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
   constexpr int kBars = 2 * NK + 2 * NV + 12;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  static_assert(kBars * 8 + 8 <= 256, "barriers fit below the tiles");
+  uint64_t* recv_bar = bars + kBars + 1;       // fused mode: the other chunks' partials arrived
+  static_assert(kBars * 8 + 16 <= 256, "barriers fit below the tiles");
   const uint32_t sbase = smem_addr(psm);
   unsigned char* tiles = psm + (((sbase + kPfxHead + 1023u) & ~1023u) - sbase);
   unsigned char* q_s = tiles;
@@ -1569,7 +1863,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
   const int kvh = blockIdx.y, c = blockIdx.z;
   const int S = p.num_seqs;
   const int tok_lo = c * p.chunk_blocks * BS;
-  const int tok_hi = min(p.prefix_blocks_n, (c + 1) * p.chunk_blocks) * BS;
+  const int tok_hi = max(tok_lo, min(p.prefix_blocks_n, (c + 1) * p.chunk_blocks) * BS);
   const int nsub = (tok_hi - tok_lo + kPfxTok - 1) / kPfxTok;
   auto sub_len = [&](int t) { return min(kPfxTok, tok_hi - (tok_lo + t * kPfxTok)); };
 
@@ -1582,6 +1876,14 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
       mbar_init(smem_addr(&bars[i]), softmax ? kPfxSoftmaxWarps : 1);
     }
     *abort_flag = 0;
+    if (FUSED) {
+      // the other C - 1 chunks of the cluster each send this CTA's rows of
+      // their partials (see the end of the kernel)
+      const uint32_t rb = smem_addr(recv_bar);
+      mbar_init(rb, 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      mbar_arrive_expect_tx(rb, (gridDim.z - 1) * (kPfxRows / gridDim.z) * (128 + 4) * 4);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -1746,6 +2048,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
     }
   } else {
     // ---- softmax warps: query row r = 32 * warp + lane (TMEM lane r) ----
+    if constexpr (FUSED) prefetch_suffix_rows<BS, G>(p, kvh, c);
     const int r = warp * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     float o[D];
@@ -1841,9 +2144,16 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
     for (int i = 0; i < D; i += 4)
       *reinterpret_cast<float4*>(stage + lane * kPad + i) =
           make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+    if constexpr (FUSED) {
+      // the cluster merges the rows from here (see the end of the kernel);
+      // bulk copies read them, so the writes are ordered for that proxy
+      stage[lane * kPad + D] = m;
+      stage[lane * kPad + D + 1] = l;
+      fence_proxy_async_smem();
+    }
     __syncwarp();
     const int row = blockIdx.x * kPfxRows + r, seq = row / G, gg = row % G;
-    const bool write = ok && !*abort_flag;
+    const bool write = !FUSED && ok && !*abort_flag;
     if (seq < S && write) {
       float* rec = p.records + ((static_cast<long long>(c) * S + seq) * p.num_kv_heads + kvh) * RS;
       rec[G * D + 2 * gg] = m;
@@ -1872,6 +2182,16 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "n"(kPfxTmemCols)
                  : "memory");
+  }
+  if constexpr (FUSED) {
+    // Every CTA of the cluster (the chunks of this row tile and KV head)
+    // reaches both barriers, whatever happened before: the first makes all
+    // staged partials visible, the second keeps each CTA's shared memory
+    // alive until the others have read it.
+    cluster_sync_all();
+    fused_merge_and_suffix<BS, G>(p, reinterpret_cast<const float*>(k_s),
+                                  reinterpret_cast<float*>(v_s), recv_bar, kvh, c);
+    cluster_sync_all();
   }
 }
 
@@ -2152,12 +2472,26 @@ PfxGeom prefix_geometry(int S, int G, int Hkv, int P, int sm_count) {
   return g;
 }
 
-template <int BS, int G>
+// Fused mode: the chunks of one (row tile, KV head) form a cluster, so their
+// count is the cluster size: the largest of 8, 4, 2 (at most one chunk per
+// prefix block) whose grid still fits one wave of one CTA per SM, else 1.
+PfxGeom fused_prefix_geometry(int S, int G, int Hkv, int P, int sm_count) {
+  PfxGeom g;
+  g.row_tiles = (S * G + kPfxRows - 1) / kPfxRows;
+  const long long base = static_cast<long long>(g.row_tiles) * Hkv;
+  int c = kMaxCluster;
+  while (c > 1 && (c > P || base * c > sm_count)) c /= 2;
+  g.chunks = c;
+  g.chunk_blocks = (P + c - 1) / c;
+  return g;
+}
+
+template <int BS, int G, bool FUSED>
 pa_status launch_prefix(const PrefixParams& pp, const PfxGeom& geo, const void* k_pool,
                         const void* v_pool, int Hkv, int NB, long long stride_bytes,
                         const pa::DeviceInfo& dev, cudaStream_t stream) {
   constexpr int D = 128;
-  auto kernel = paged_prefix_kernel<BS, G>;
+  auto kernel = paged_prefix_kernel<BS, G, FUSED>;
   {
     static std::mutex mu;
     static bool set[pa::kMaxDevices] = {};
@@ -2180,23 +2514,78 @@ pa_status launch_prefix(const PrefixParams& pp, const PfxGeom& geo, const void* 
   lc.blockDim = dim3(kPfxThreads);
   lc.dynamicSmemBytes = kPfxSmem;
   lc.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
+  if (FUSED && geo.chunks > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = static_cast<unsigned>(geo.chunks);
+    lc.numAttrs = 2;
+  }
   cudaError_t e = cudaLaunchKernelEx(&lc, kernel, pp, kmap, vmap);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "shared-prefix kernel launch");
   return PA_OK;
 }
 
+// Whether clusters of `chunks` prefix CTAs can be resident on this device
+// (checked once per device and cluster size).
 template <int BS, int G>
-pa_status shared_prefix_pass(const PrefixParams& pp, const PfxGeom& geo, DecodeParams prm,
-                             const void* k_pool, const void* v_pool, const pa::DeviceInfo& dev,
-                             cudaStream_t s) {
-  if (pa_status st = launch_prefix<BS, G>(pp, geo, k_pool, v_pool, prm.num_kv_heads,
-                                                prm.num_blocks, prm.block_stride_bytes, dev, s))
+bool fused_prefix_fits(const PfxGeom& geo, const pa::DeviceInfo& dev) {
+  if (geo.chunks <= 1) return true;
+  static std::mutex mu;
+  static signed char known[pa::kMaxDevices][kMaxCluster + 1] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  signed char& k = known[dev.device][geo.chunks];
+  if (k == 0) {
+    auto kernel = paged_prefix_kernel<BS, G, true>;
+    k = -1;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfxSmem) ==
+        cudaSuccess) {
+      cudaLaunchConfig_t lc = {};
+      lc.gridDim = dim3(static_cast<unsigned>(geo.row_tiles), 1, static_cast<unsigned>(geo.chunks));
+      lc.blockDim = dim3(kPfxThreads);
+      lc.dynamicSmemBytes = kPfxSmem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 1;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = static_cast<unsigned>(geo.chunks);
+      lc.attrs = attr;
+      lc.numAttrs = 1;
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &lc) == cudaSuccess && clusters > 0)
+        k = 1;
+    }
+    cudaGetLastError();  // a refused query is an answer, not an error of the call
+  }
+  return k > 0;
+}
+
+// The shared-prefix call: one fused launch when every suffix is short and
+// the clusters fit, else the prefix kernel then the attention kernel's
+// prefix mode.
+template <int BS, int G>
+pa_status shared_prefix_pass(PrefixParams pp, DecodeParams prm, const void* k_pool,
+                             const void* v_pool, const pa::DeviceInfo& dev, cudaStream_t s) {
+  const int S = prm.num_seqs, Hkv = prm.num_kv_heads, P = pp.prefix_blocks_n;
+  if ((prm.max_blocks - P) * BS <= kFusedSuffixTokens) {
+    const PfxGeom fg = fused_prefix_geometry(S, G, Hkv, P, dev.sm_count);
+    if (fused_prefix_fits<BS, G>(fg, dev)) {
+      pp.chunk_blocks = fg.chunk_blocks;
+      return launch_prefix<BS, G, true>(pp, fg, k_pool, v_pool, Hkv, prm.num_blocks,
+                                        prm.block_stride_bytes, dev, s);
+    }
+  }
+  const PfxGeom geo = prefix_geometry(S, G, Hkv, P, dev.sm_count);
+  pp.chunk_blocks = geo.chunk_blocks;
+  prm.pfx_chunks = geo.chunks;
+  if (pa_status st = launch_prefix<BS, G, false>(pp, geo, k_pool, v_pool, Hkv, prm.num_blocks,
+                                                 prm.block_stride_bytes, dev, s))
     return st;
   return launch_decode<128, BS, G, false, true>(prm, dev, s);
 }
@@ -2570,7 +2959,6 @@ pa_status pa_decode_attention_shared_prefix(
   if (pa_status s = pa::current_device(&dev)) return s;
   const int G = num_q_heads / num_kv_heads;
   const int P = num_prefix_blocks;
-  const PfxGeom geo = prefix_geometry(num_seqs, G, num_kv_heads, P, dev.sm_count);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   const size_t rec_bytes = static_cast<size_t>(rec_floats(G, head_dim)) * 4;
   // the suffix pass: the table past the prefix's columns, lengths past its tokens
@@ -2580,7 +2968,6 @@ pa_status pa_decode_attention_shared_prefix(
   prm.err = pa::device_error_word();
   if (!prm.err) return PA_ERR_CUDA;
   prm.pfx_blocks = P;
-  prm.pfx_chunks = geo.chunks;
   prm.pfx_own_base = lay.own_rec;
   prm.pfx_rec_base = lay.pfx_rec;
   PrefixParams pp;
@@ -2593,12 +2980,18 @@ pa_status pa_decode_attention_shared_prefix(
   pp.num_kv_heads = num_kv_heads;
   pp.num_blocks = num_blocks;
   pp.prefix_blocks_n = P;
-  pp.chunk_blocks = geo.chunk_blocks;
   pp.qscale = scale * kLog2e;
+  pp.block_table = prm.block_table - P;  // the whole table (prm's starts past the prefix)
+  pp.seq_lens = prm.seq_lens;
+  pp.k_pool = prm.k_pool;
+  pp.v_pool = prm.v_pool;
+  pp.block_stride = stride_bytes / 2;
+  pp.out = prm.out;
+  pp.max_blocks = max_blocks_per_seq;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   pa_status st;
 #define PA_PFX_CASE(bs, g) \
-  if (block_size == bs && G == g) st = shared_prefix_pass<bs, g>(pp, geo, prm, k_pool, v_pool, dev, s); else
+  if (block_size == bs && G == g) st = shared_prefix_pass<bs, g>(pp, prm, k_pool, v_pool, dev, s); else
   PA_PFX_CASE(16, 1) PA_PFX_CASE(16, 2) PA_PFX_CASE(16, 4) PA_PFX_CASE(16, 8)
   PA_PFX_CASE(32, 1) PA_PFX_CASE(32, 2) PA_PFX_CASE(32, 4) PA_PFX_CASE(32, 8)
   st = pa::fail(PA_ERR_UNSUPPORTED, "pa_decode_attention_shared_prefix: unsupported shape");

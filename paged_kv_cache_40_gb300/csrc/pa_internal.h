@@ -69,6 +69,10 @@ pa_status device_in(const char* fn, T*& p) {
 // workspaces) must be device memory: PA_ERR_INVALID_ARG otherwise.
 pa_status device_only(const char* fn, const void* p);
 
+// The block manager's block size and pool size (for the step driver).
+int alloc_block_size(const pa_allocator* a);
+int alloc_num_blocks(const pa_allocator* a);
+
 // Properties of the current device used for launch shaping.
 struct DeviceInfo {
   int device = -1;

@@ -120,11 +120,9 @@ class DecodeBatchRunner:
         """Reserve one slot per sequence (host block manager) and upload the
         slot mapping, copy-on-write pairs and block tables."""
         import torch
-        slots, pairs = self.alloc.append_slots(list(range(self.num_seqs)))
-        table, lens = self.alloc.build_tables(list(range(self.num_seqs)), self.max_blocks,
-                                              self.table_fill)
-        plan = StepPlan(np.asarray(slots, np.int32),
-                        np.asarray(pairs, np.int32).reshape(-1, 2), table, lens)
+        slots, pairs, table, lens = self.alloc.plan_step(np.arange(self.num_seqs, dtype=np.int64),
+                                                         self.max_blocks, self.table_fill)
+        plan = StepPlan(slots.copy(), pairs.copy(), table.copy(), lens.copy())
         self.plan = plan
         self.d_slots = _to_dev(plan.slots, self.device)
         self.d_pairs = _to_dev(plan.cow_pairs, self.device) if len(plan.cow_pairs) else None
@@ -212,6 +210,67 @@ class DecodeBatchRunner:
             setattr(self, n, h)
             total += h.numel() * h.element_size()
         return total
+
+    def host_planned(self, sets: int = 2) -> int:
+        """Plan every step straight into pinned host memory: `sets` rotating
+        sets of buffers for the slot mapping, copy pairs, tables and lengths,
+        which plan_step_host() fills with one block-manager call
+        (pa_alloc_plan_step) and the kernels read in place through their
+        device mapping; q and the new K/V rows stay in pinned host memory
+        too. With two sets, step k+1 can be planned while the kernels of step
+        k still read theirs. Returns the input bytes of one step."""
+        import torch
+        S, mb = self.num_seqs, self.max_blocks
+        pin = lambda shape: torch.empty(shape, dtype=torch.int32).pin_memory()
+        self._plan_sets = [(pin((S,)), pin((S, 2)), pin((S, mb)), pin((S,))) for _ in range(sets)]
+        self._plan_views = [tuple(t.numpy() for t in st) for st in self._plan_sets]
+        self._plan_ids = np.arange(S, dtype=np.int64)
+        self._plan_next = 0
+        total = 0
+        for n in ("q", "k_new", "v_new"):
+            h = getattr(self, n).cpu().pin_memory()
+            setattr(self, n, h)
+            total += h.numel() * h.element_size()
+        return total + S * 4 * (1 + 2 + mb + 1)
+
+    def prepare_native_steps(self, stream=None) -> None:
+        """After host_planned(): one PreparedDecodeStep per set of plan
+        buffers, so that run_native_step() plans and enqueues a whole step
+        (copies, append, attention) in one library call."""
+        from . import PreparedDecodeStep
+        if self.kv_dtype != "fp16":
+            raise ValueError("the one-call step serves fp16 caches")
+        self._native = [PreparedDecodeStep(self.alloc, self._plan_ids, self.max_blocks, st,
+                                           self.q, self.k_new, self.v_new, self.k_pool,
+                                           self.v_pool, float(self.batch.scale), self.out,
+                                           self.workspace, self.partition_tokens, stream)
+                        for st in self._plan_sets]
+
+    def run_native_step(self) -> StepPlan:
+        """One decode step through pa_decode_step (see prepare_native_steps);
+        returns the plan it wrote (views of that set's pinned buffers)."""
+        k = self._plan_next % len(self._native)
+        self._plan_next += 1
+        ncow = self._native[k]()
+        v = self._plan_views[k]
+        S = self.num_seqs
+        self.plan = StepPlan(v[0][:S], v[1][:ncow], v[2][:S], v[3][:S])
+        return self.plan
+
+    def plan_step_host(self) -> StepPlan:
+        """One decode step planned by the block manager in a single call into
+        the next set of pinned buffers (see host_planned); the step's kernels
+        then read that set."""
+        k = self._plan_next % len(self._plan_sets)
+        self._plan_next += 1
+        slots, pairs, table, lens = self.alloc.plan_step(self._plan_ids, self.max_blocks,
+                                                         self.table_fill, out=self._plan_views[k])
+        st = self._plan_sets[k]
+        self.d_slots, self.d_table, self.d_lens = st[0][:self.num_seqs], st[2][:self.num_seqs], \
+            st[3][:self.num_seqs]
+        self.d_pairs = st[1][:len(pairs)] if len(pairs) else None
+        self.plan = StepPlan(slots, pairs, table, lens)
+        return self.plan
 
     def upload_inputs(self, stream=None) -> int:
         """One host-to-device copy of the packed inputs; returns its bytes."""

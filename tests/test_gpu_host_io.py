@@ -232,3 +232,103 @@ def test_pageable_inputs_and_host_pools_are_refused(pa):
                                  Hkv, D, BS, table.shape[1], nb, 0, ctypes.c_float(0.1), vp_(out),
                                  vp_(ws), ws.numel(), 0, None)
     assert st == 1 and b"device memory" in lib.pa_last_error()
+
+
+def test_steps_planned_in_place_match_the_oracle(pa):
+    """A decode loop whose steps the block manager plans with one call each
+    straight into pinned host memory (two rotating buffer sets, the kernels
+    reading them in place), the sequences growing by a token a step: slots,
+    copy-on-write pairs, tables, lengths and the pools bit-exact with the
+    oracle's block manager and cache operations, attention within tolerance,
+    over steps that grow blocks."""
+    import dataclasses
+    from paged_kv_cache_40_gb300.engine import DecodeBatchRunner
+    rng = np.random.default_rng(12)
+    lens0 = rng.integers(14, 40, size=6, endpoint=True)
+    steps = 20
+    nb = sum(-(-(int(L) + steps + 1) // 16) for L in lens0) + 4   # room for the growth
+    b = synthetic.make_batch("planned", rng, lens0, 32, 8, 128, 16, nb, seed=12)
+    mb = max(-(-(int(L) + steps + 1) // b.block_size) for L in b.prefill_lens)
+    run = DecodeBatchRunner(b, max_blocks=mb)
+    run.host_planned(sets=2)
+    ref = oracle.BlockAllocator(b.num_blocks, b.block_size, b.free_order)
+    for i, L in enumerate(b.prefill_lens):
+        ref.add_seq(i, int(L))
+    kp, vp = b.k_pool.copy(), b.v_pool.copy()
+    ids = list(range(b.num_seqs))
+    for k in range(steps):
+        plan = run.plan_step_host()
+        slots, pairs = [], []
+        for s_ in ids:
+            sl, cs, cd = ref.append_slot(s_)
+            slots.append(sl)
+            if cs >= 0:
+                pairs.append((cs, cd))
+        table = np.asarray(ref.dense_table(ids, mb), np.int32)
+        lens = np.asarray([ref.seq_len(s_) for s_ in ids], np.int32)
+        assert plan.slots.tolist() == slots and plan.cow_pairs.tolist() == [list(p) for p in pairs]
+        assert plan.block_table.tolist() == table.tolist()
+        assert plan.seq_lens.tolist() == lens.tolist()
+        run.run_step()
+        torch.cuda.synchronize()
+        assert pa.pa_device_error() == 0
+        if pairs:
+            kp, vp = oracle.copy_blocks(kp, vp, np.asarray(pairs, np.int32))
+        kp, vp = oracle.append_kv(kp, vp, b.k_new, b.v_new, np.asarray(slots, np.int32))
+        assert np.array_equal(run.k_pool.cpu().numpy().view(np.uint16), kp.view(np.uint16))
+        assert np.array_equal(run.v_pool.cpu().numpy().view(np.uint16), vp.view(np.uint16))
+        exp = oracle.decode_attention(b.q, kp, vp, table, lens, b.scale)
+        assert_close_attention(run.out.cpu().numpy(), exp, f"planned step {k}")
+
+
+def test_one_call_steps_match_the_oracle(pa):
+    """pa_decode_step (plan, copy-on-write copies, append and attention in one
+    library call, the plan written into pinned host memory the kernels read in
+    place) over steps of a batch with forked sequences (shared blocks, so the
+    first steps copy): plans, pools and outputs against the oracle."""
+    from paged_kv_cache_40_gb300.engine import DecodeBatchRunner
+    rng = np.random.default_rng(21)
+    lens0 = rng.integers(14, 40, size=5, endpoint=True)
+    lens0[1] = 21                       # a partial last block: the fork's first append copies
+    steps = 12
+    nb = sum(-(-(int(L) + steps + 1) // 16) for L in lens0) * 2 + 8
+    b = synthetic.make_batch("one-call", rng, lens0, 16, 4, 128, 16, nb, seed=21)
+    mb = max(-(-(int(L) + steps + 1) // 16) for L in lens0) + 1
+    run = DecodeBatchRunner(b, max_blocks=mb)
+    ref = oracle.BlockAllocator(b.num_blocks, b.block_size, b.free_order)
+    for i, L in enumerate(b.prefill_lens):
+        ref.add_seq(i, int(L))
+    # sequence 4 becomes a fork of sequence 1: its blocks are shared
+    run.alloc.free_seq(4)
+    run.alloc.fork(1, 4)
+    ref.free_seq(4)
+    ref.fork(1, 4)
+    run.host_planned(sets=2)
+    run.prepare_native_steps()
+    kp, vp = b.k_pool.copy(), b.v_pool.copy()
+    ids = list(range(b.num_seqs))
+    copies = 0
+    for k in range(steps):
+        plan = run.run_native_step()
+        slots, pairs = [], []
+        for s_ in ids:
+            sl, cs, cd = ref.append_slot(s_)
+            slots.append(sl)
+            if cs >= 0:
+                pairs.append((cs, cd))
+        table = np.asarray(ref.dense_table(ids, mb), np.int32)
+        lens = np.asarray([ref.seq_len(s_) for s_ in ids], np.int32)
+        torch.cuda.synchronize()
+        assert pa.pa_device_error() == 0
+        assert plan.slots.tolist() == slots and plan.cow_pairs.tolist() == [list(p) for p in pairs]
+        assert plan.block_table.tolist() == table.tolist()
+        assert plan.seq_lens.tolist() == lens.tolist()
+        copies += len(pairs)
+        if pairs:
+            kp, vp = oracle.copy_blocks(kp, vp, np.asarray(pairs, np.int32))
+        kp, vp = oracle.append_kv(kp, vp, b.k_new, b.v_new, np.asarray(slots, np.int32))
+        assert np.array_equal(run.k_pool.cpu().numpy().view(np.uint16), kp.view(np.uint16))
+        assert np.array_equal(run.v_pool.cpu().numpy().view(np.uint16), vp.view(np.uint16))
+        exp = oracle.decode_attention(b.q, kp, vp, table, lens, b.scale)
+        assert_close_attention(run.out.cpu().numpy(), exp, f"one-call step {k}")
+    assert copies >= 1

@@ -27,15 +27,16 @@ def d(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-def _case(seed, S, Hq, Hkv, BS, P, suffix_lens, D=128, extra=4):
-    """P shared blocks, then per-sequence private blocks for its suffix."""
+def _case(seed, S, Hq, Hkv, BS, P, suffix_lens, D=128, extra=4, mb=None):
+    """P shared blocks, then per-sequence private blocks for its suffix; the
+    table is P + the longest suffix's blocks + 1 wide unless `mb` is given."""
     rng = np.random.default_rng(seed)
     lens = [P * BS + s for s in suffix_lens]
     priv = [-(-s // BS) for s in suffix_lens]
     nb = P + sum(priv) + extra
     perm = rng.permutation(nb).astype(np.int32)
     prefix = perm[:P]
-    mb = P + max(priv) + 1
+    mb = P + max(priv) + 1 if mb is None else mb
     table = -np.ones((S, mb), np.int32)
     pos = P
     for i in range(S):
@@ -121,3 +122,58 @@ def test_sequence_shorter_than_prefix_is_reported(pa):
     with pytest.raises(pa.PaError) as e:
         pa.pa_device_error()
     assert e.value.flags & pa.PA_DEVERR_BAD_LEN
+
+
+# ------------------------------------------------ short suffixes: one launch --
+# A table at most 32 tokens wider than the prefix means every suffix is that
+# short: the call then runs as one launch whose clusters (the prefix chunks of
+# a row tile and KV head) merge their partials on chip and attend the
+# suffixes themselves. Cluster sizes 8, 4, 2 and 1 come from the prefix
+# length and the grid; chunks past a short prefix are empty.
+@pytest.mark.parametrize("BS", [16, 32])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("P", [1, 2, 5, 9])
+def test_short_suffix_one_launch_matrix(pa, BS, G, P):
+    Hkv = 2
+    suffix = [0, 1, 7, BS - 1, BS, 32, 31, 2, 0, 17, 32]
+    q, kp, vp, prefix, table, lens = _case(1000 + 100 * P + BS + G, len(suffix), G * Hkv, Hkv,
+                                           BS, P, suffix, mb=P + 32 // BS)
+    scale = np.float32(1 / math.sqrt(128))
+    got = _run(pa, q, kp, vp, prefix, table, lens, scale)
+    exp = oracle.decode_attention(q, kp, vp, table, lens, scale)
+    assert_close_attention(got, exp, f"short suffix BS{BS} G{G} P{P}")
+    assert pa.pa_device_error() == 0
+
+
+@pytest.mark.parametrize("S,G,Hkv", [(128, 4, 8), (300, 4, 8), (40, 8, 8), (3, 1, 1)])
+def test_short_suffix_one_launch_grids(pa, S, G, Hkv):
+    """Row tiles x KV heads x cluster sizes across the grid's range: the
+    prefix workload's shape (4 row tiles, clusters of 4), 10 row tiles (no
+    cluster), one row tile of 8 heads, a single row."""
+    rng = np.random.default_rng(S)
+    suffix = rng.integers(0, 17, S).tolist()
+    P = 40
+    q, kp, vp, prefix, table, lens = _case(7 + S, S, G * Hkv, Hkv, 16, P, suffix, mb=P + 1)
+    got = _run(pa, q, kp, vp, prefix, table, lens, np.float32(0.088))
+    seqs = sorted({0, 1, S // 2, S - 1})
+    exp = oracle.decode_attention(q, kp, vp, table, lens, np.float32(0.088), seqs=seqs)
+    assert_close_attention(got[seqs], exp[seqs], f"short suffix S{S} G{G} Hkv{Hkv}")
+    assert np.isfinite(got).all()
+    assert pa.pa_device_error() == 0
+
+
+def test_short_suffix_bad_length_and_block_are_reported(pa):
+    q, kp, vp, prefix, table, lens = _case(11, 4, 8, 2, 16, 6, [3, 9, 16, 0], mb=8)
+    lens = lens.copy()
+    lens[3] = 6 * 16 - 5                           # shorter than the prefix
+    _run(pa, q, kp, vp, prefix, table, lens, np.float32(0.1))
+    with pytest.raises(pa.PaError) as e:
+        pa.pa_device_error()
+    assert e.value.flags & pa.PA_DEVERR_BAD_LEN
+    table = table.copy()
+    table[1, 6] = 10_000_000                       # a suffix block outside the pool
+    lens[3] = 6 * 16
+    _run(pa, q, kp, vp, prefix, table, lens, np.float32(0.1))
+    with pytest.raises(pa.PaError) as e:
+        pa.pa_device_error()
+    assert e.value.flags & pa.PA_DEVERR_BAD_BLOCK
