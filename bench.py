@@ -123,7 +123,7 @@ def kernel_source_hash() -> str:
     """Identifies the attention kernel's code (comments and layout excluded),
     so that recorded ncu traffic is used only for the code it was taken on."""
     h = hashlib.sha256()
-    for name in ("pa_decode.cu",):
+    for name in ("pa_decode.cu", "pa_device.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_40_gb300", "csrc", name),
                   encoding="utf-8") as f:
             h.update(strip_c_comments(f.read()).encode())

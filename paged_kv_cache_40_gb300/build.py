@@ -25,7 +25,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CUFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                   "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr",
                   f"-I{INCLUDE}", f"-I{CSRC}"]
-SOURCES = ["pa_status.cpp", "pa_alloc.cpp", "pa_step.cpp", "pa_cache.cu", "pa_decode.cu"]
+SOURCES = ["pa_status.cpp", "pa_alloc.cpp", "pa_step.cpp", "pa_cache.cu", "pa_decode.cu",
+           "pa_prefix.cu"]
 
 
 def _nvcc() -> str:
