@@ -46,6 +46,7 @@ import numpy as np  # noqa: E402
 
 METRIC = "paged decode attention: KV GB/s (fraction of GB300 HBM peak) and tokens attended/s"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 512 << 20
 
 
@@ -93,6 +94,17 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def tensor_peak():
+    """Dense bf16 tensor rate, burst (a kernel timed alone); fp16 has the same
+    nominal rate on this GPU."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
 def strip_c_comments(src: str) -> str:
     """C/C++ source with its comments removed and each run of whitespace
     collapsed to one space; string and character literals are kept whole."""
@@ -119,18 +131,22 @@ def strip_c_comments(src: str) -> str:
     return " ".join("".join(out).split())
 
 
-def kernel_source_hash() -> str:
-    """Identifies the attention kernel's code (comments and layout excluded),
-    so that recorded ncu traffic is used only for the code it was taken on."""
+DECODE_SOURCES = ("pa_decode.cu", "pa_device.cuh")
+PREFIX_SOURCES = ("pa_prefix.cu", "pa_device.cuh")
+
+
+def kernel_source_hash(names=DECODE_SOURCES) -> str:
+    """Identifies a kernel's code (comments and layout excluded), so that
+    recorded ncu traffic is used only for the code it was taken on."""
     h = hashlib.sha256()
-    for name in ("pa_decode.cu", "pa_device.cuh"):
+    for name in names:
         with open(os.path.join(ROOT, "paged_kv_cache_40_gb300", "csrc", name),
                   encoding="utf-8") as f:
             h.update(strip_c_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_name: str):
+def recorded_traffic(workload_name: str, sources=DECODE_SOURCES):
     """DRAM bytes per attention launch from a committed ncu summary, if it was
     taken on the current kernel source; else None."""
     path = os.path.join(ROOT, "profiles", "decode_traffic.json")
@@ -140,7 +156,7 @@ def recorded_traffic(workload_name: str):
     except (OSError, ValueError):
         return None
     ent = rec.get(workload_name)
-    if not ent or ent.get("kernel_source_sha256_16") != kernel_source_hash():
+    if not ent or ent.get("kernel_source_sha256_16") != kernel_source_hash(sources):
         return None
     return int(ent["dram_bytes_per_launch"])
 
@@ -586,8 +602,6 @@ def run_ours(args, world, rank, local):
     # convert the whole buffer to int64)
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_sink = torch.empty((), dtype=torch.float32, device=dev)
-    launches_per_step = ((1 if len(plan.cow_pairs) else 0) + 1 +
-                         getattr(run, "attend_launches", DecodeBatchRunner.ATTEND_LAUNCHES))
 
     def flush():
         flush_w.fill_(1)
@@ -607,6 +621,7 @@ def run_ours(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize(dev)
     w0 = time.perf_counter()
+    launches0 = pa.pa_kernel_launches()
     # the step as a caller issues it: nothing between the append and the
     # attention kernel, which is launched as a programmatic dependent and so
     # may start its prologue while the append runs
@@ -616,6 +631,7 @@ def run_ours(args, world, rank, local):
         run.copy_and_append()
         run.attend()
         ev[k][1].record(stream)
+    launches = pa.pa_kernel_launches() - launches0
     torch.cuda.synchronize(dev)
     barrier(world)
     wall = time.perf_counter() - w0
@@ -715,6 +731,31 @@ def run_ours(args, world, rank, local):
             "note": "every sequence attends the same 2040-token prefix; bytes are logical "
                     "(per sequence), the prefix's blocks are served from L2 after the first read",
         })
+    if shared and run.prefix_aware:
+        # one launch of the prefix kernel (every suffix is short): its
+        # contraction runs on the tensor cores and it reads the prefix once,
+        # so the tensor roof bounds it, not HBM
+        flops = run.prefix_flops()
+        tpeak, tpeak_kind = tensor_peak()
+        tf = flops / attn_mean_s / 1e12
+        roofline = {"bound": "tensor", "achieved": round(tf, 2), "peak": tpeak,
+                    "unit": "TFLOP/s", "frac": round(tf / tpeak, 4),
+                    "traffic": recorded_traffic(b.name, PREFIX_SOURCES),
+                    "peak_source": tpeak_kind + " (dense bf16 burst; fp16 has the same rate)",
+                    "kernel": "paged_prefix_kernel", "flops_per_launch": flops,
+                    "hbm_logical": {"achieved": round(achieved, 1), "peak": peak,
+                                    "unit": "GB/s", "bytes_per_launch": run.io_bytes(),
+                                    "note": "logical per-sequence bytes; the prefix is read "
+                                            "once, so this is not a DRAM rate"}}
+    else:
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                    "unit": "GB/s", "frac": round(achieved / peak, 4),
+                    "traffic": recorded_traffic(b.name + ("_fp8" if fp8 is not None else "")
+                                                + ("_records" if args.layout == "records"
+                                                   else "")),
+                    "peak_source": peak_kind,
+                    "kernel": "paged_decode_kernel",
+                    "bytes_per_launch": run.io_bytes()}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(1e3 * t_steps / K, 5),
@@ -726,13 +767,7 @@ def run_ours(args, world, rank, local):
         "attention_us": {"mean": round(1e6 * attn_mean_s, 3),
                          "median": round(1e3 * statistics.median(attn_ms), 3),
                          "min": round(1e3 * min(attn_ms), 3)},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(b.name + ("_fp8" if fp8 is not None else "")
-                                                + ("_records" if args.layout == "records" else "")),
-                     "peak_source": peak_kind,
-                     "kernel": "paged_decode_kernel",
-                     "bytes_per_launch": run.io_bytes()},
+        "roofline": roofline,
         "e2e_planned": planned,
         "e2e": {"value": round(value_e2e, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -745,7 +780,7 @@ def run_ours(args, world, rank, local):
                                 "path": "inputs packed in one pinned buffer, one host-to-device "
                                         "copy per step; output as above"}},
         "cpu_baseline": cpu,
-        "gpu_launches": launches_per_step * K,
+        "gpu_launches": launches,
         "clocks": clocks,
         "host_slot_assign_us": round(t_host, 1) if t_host is not None else None,
         "host_slot_assign_first_us": (round(t_host_first, 1) if t_host_first is not None

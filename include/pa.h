@@ -118,6 +118,15 @@ PA_API pa_status pa_device_error(pa_stream_t stream, int32_t* flags);
  * Errors: none (PA_OK). */
 PA_API pa_status pa_set_wait_limit_ns(uint64_t limit_ns);
 
+/* Number of kernels this library has enqueued in this process, on any
+ * device or stream (every call counts the launches it made; a call that
+ * launches nothing, such as pa_copy_blocks with no pairs, counts none).
+ * Read it before and after a region of calls to know how many of the
+ * library's kernels that region ran: pa_decode_attention_shared_prefix, for
+ * one, launches one kernel or two depending on the suffix lengths. A
+ * monotonic counter: no reset, no error. */
+PA_API uint64_t pa_kernel_launches(void);
+
 /* ------------------------------------------------------------------------
  * pa_append_kv — write each sequence's new K/V token into its cache slot.
  *

@@ -45,7 +45,7 @@ __all__ = [
     "pa_decode_attention_shared_prefix", "pa_decode_shared_prefix_workspace_bytes",
     "pa_swap_blocks",
     "pa_decode_attention_fixed_scratch", "kv_block_pool", "kv_views",
-    "pa_version", "BlockAllocator", "PaError", "OutOfBlocksError", "lib",
+    "pa_version", "pa_kernel_launches", "pa_set_wait_limit_ns", "BlockAllocator", "PaError", "OutOfBlocksError", "lib",
 ]
 
 
@@ -55,6 +55,12 @@ def lib() -> ctypes.CDLL:
 
 def pa_version() -> int:
     return int(_load().pa_version())
+
+
+def pa_kernel_launches() -> int:
+    """Kernels the library has enqueued in this process so far (a monotonic
+    count; read it before and after a region of calls)."""
+    return int(_load().pa_kernel_launches())
 
 
 # ----------------------------------------------------------------- helpers --

@@ -59,6 +59,7 @@ SIGNATURES = {
     "pa_version": (_i32, []),
     "pa_device_error": (_i32, [_vp, _pi32]),
     "pa_set_wait_limit_ns": (_i32, [ctypes.c_uint64]),
+    "pa_kernel_launches": (ctypes.c_uint64, []),
     "pa_append_kv": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _vp]),
     "pa_copy_blocks": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _vp]),
     "pa_decode_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32]),

@@ -313,6 +313,7 @@ pa_status pa_append_kv(const pa_half* k_new, const pa_half* v_new, pa_half* k_po
       row_vecs, block_size, stride / 8, static_cast<int64_t>(num_blocks) * block_size, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_append_kv launch");
+  pa::count_launch();
   return pa::ok();
 }
 
@@ -350,6 +351,7 @@ pa_status pa_copy_blocks(pa_half* k_pool, pa_half* v_pool, const int32_t* pairs,
       stride / 8, stride / 8, num_blocks, num_blocks, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_copy_blocks launch");
+  pa::count_launch();
   return pa::ok();
 }
 
@@ -403,6 +405,7 @@ pa_status pa_append_kv_fp8(const pa_half* k_new, const pa_half* v_new, uint8_t* 
       static_cast<int64_t>(num_blocks) * block_size, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_append_kv_fp8 launch");
+  pa::count_launch();
   return pa::ok();
 }
 
@@ -443,6 +446,7 @@ pa_status pa_copy_blocks_fp8(uint8_t* k_pool, uint8_t* v_pool, const int32_t* pa
       stride / 16, stride / 16, num_blocks, num_blocks, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_copy_blocks_fp8 launch");
+  pa::count_launch();
   return pa::ok();
 }
 
@@ -532,6 +536,7 @@ pa_status pa_swap_blocks(const void* src_k, const void* src_v, int src_blocks,
       dst_stride / 16, src_blocks, dst_blocks, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_swap_blocks launch");
+  pa::count_launch();
   return pa::ok();
 }
 

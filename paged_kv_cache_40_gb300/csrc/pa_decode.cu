@@ -1392,6 +1392,7 @@ pa_status launch_decode(DecodeParams prm, const pa::DeviceInfo& dev, cudaStream_
   cudaError_t e = cudaLaunchKernelEx(&lc, paged_decode_kernel<D, BS, G, KV8, PFX>, prm, kmap, vmap);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_decode_attention launch");
+  pa::count_launch();
 
   return PA_OK;
 }

@@ -27,6 +27,9 @@ pa_status ok();
 // message on failure.
 int32_t* device_error_word();
 
+// Count one kernel launch the library enqueued (pa_kernel_launches).
+void count_launch();
+
 // Map a CUDA runtime error to a status with a message naming `what`.
 pa_status cuda_fail(int cuda_err, const char* what);
 

@@ -880,6 +880,7 @@ pa_status launch_prefix(const PrefixParams& pp, const PfxGeom& geo, const void* 
   cudaError_t e = cudaLaunchKernelEx(&lc, kernel, pp, kmap, vmap);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "shared-prefix kernel launch");
+  pa::count_launch();
   return PA_OK;
 }
 

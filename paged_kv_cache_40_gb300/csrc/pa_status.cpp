@@ -1,6 +1,7 @@
 // Status codes, per-thread error messages and device queries for libpa.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "pa_internal.h"
@@ -73,9 +74,17 @@ pa_status current_device(DeviceInfo* out) {
   return PA_OK;
 }
 
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}  // namespace
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 }  // namespace pa
 
 extern "C" {
+
+uint64_t pa_kernel_launches(void) { return pa::g_launches.load(std::memory_order_relaxed); }
 
 const char* pa_last_error(void) { return g_last_error.c_str(); }
 

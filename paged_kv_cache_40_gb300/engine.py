@@ -31,7 +31,7 @@ import numpy as np
 from . import (BlockAllocator, alloc_workspace, kv_block_pool, kv_views, pa_append_kv,
                pa_append_kv_fp8, pa_copy_blocks, pa_copy_blocks_fp8, pa_decode_attention,
                pa_decode_attention_fp8, pa_decode_attention_shared_prefix,
-               pa_decode_shared_prefix_workspace_bytes)
+               pa_decode_shared_prefix_workspace_bytes, pa_kernel_launches)
 
 
 def _to_dev(arr, device, dtype=None):
@@ -131,20 +131,17 @@ class DecodeBatchRunner:
         return plan
 
     # -- device: the hot path ----------------------------------------------
-    def copy_and_append(self, stream=None) -> int:
-        launches = 0
+    def copy_and_append(self, stream=None) -> None:
         fp8 = self.kv_dtype == "fp8"
         if self.d_pairs is not None:
             (pa_copy_blocks_fp8 if fp8 else pa_copy_blocks)(self.k_pool, self.v_pool, self.d_pairs,
                                                             stream=stream)
-            launches += 1
         if fp8:
             pa_append_kv_fp8(self.k_new, self.v_new, self.k_pool, self.v_pool, self.d_slots,
                              self.k_scale, self.v_scale, stream=stream)
         else:
             pa_append_kv(self.k_new, self.v_new, self.k_pool, self.v_pool, self.d_slots,
                          stream=stream)
-        return launches + 1
 
     def attend(self, stream=None):
         if self.kv_dtype == "fp8":
@@ -157,10 +154,6 @@ class DecodeBatchRunner:
                                 float(self.batch.scale), out=self.out, workspace=self.workspace,
                                 partition_tokens=self.partition_tokens, stream=stream)
         return self.out
-
-    # kernels one attend() enqueues (the attention kernel merges split
-    # sequences itself)
-    ATTEND_LAUNCHES = 1
 
     # -- host <-> device: one copy of the step's inputs ----------------------
     def pack_inputs(self) -> None:
@@ -283,11 +276,12 @@ class DecodeBatchRunner:
         return int(self.host_arena.numel())
 
     def run_step(self, stream=None):
-        """copy-on-write copies (if any), append, attend. Returns the kernel
-        launch count."""
-        n = self.copy_and_append(stream)
+        """copy-on-write copies (if any), append, attend. Returns how many
+        kernels the library launched for it."""
+        n0 = pa_kernel_launches()
+        self.copy_and_append(stream)
         self.attend(stream)
-        return n + self.ATTEND_LAUNCHES
+        return pa_kernel_launches() - n0
 
     def kv_bytes(self) -> int:
         """Algorithmic K+V bytes one attention launch reads."""
@@ -372,10 +366,13 @@ class SharedPrefixRunner(DecodeBatchRunner):
                                           out=self.out, workspace=self.workspace, stream=stream)
         return self.out
 
-    # kernels one attend() enqueues with the prefix-aware call
-    @property
-    def attend_launches(self) -> int:
-        return 2 if self.prefix_aware else 1
+    def prefix_flops(self) -> int:
+        """Tensor-core flops of the shared prefix's contraction in one call:
+        S = Q K^T and O = P V over every (sequence, query head) row and
+        every prefix token, 2 flops per multiply-add."""
+        w = self.batch
+        tokens = self.num_prefix_blocks * w.block_size
+        return 2 * 2 * self.num_seqs * w.num_q_heads * tokens * w.head_dim
 
     def unique_kv_bytes(self) -> int:
         """K+V bytes of the distinct rows the step attends (the shared prefix
