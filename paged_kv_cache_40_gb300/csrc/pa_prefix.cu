@@ -25,10 +25,15 @@ namespace {
 // TMEM lane quarter each, one query row per thread) run the softmax. The
 // prefix's tokens are split into chunks across CTAs and each chunk into
 // sub-chunks of up to 128 tokens; a row's online softmax runs over its
-// chunk's sub-chunks, and each (chunk, sequence, KV head) leaves one partial
-// record (the layout the merges use). The attention kernel then streams each
-// sequence's remaining blocks and merges the prefix chunks' records into that
-// sequence's result.
+// chunk's sub-chunks. O accumulates in TMEM over the whole chunk: the
+// softmax takes P against a reference max that moves only when a
+// sub-chunk's max exceeds it by more than 2^8, and only then rescales O in
+// TMEM (the "online softmax" of the pages with a lazy rescale: the result is
+// the same ratio, every exponent stays at most 2^8). Each (chunk, sequence,
+// KV head) leaves one partial record (the layout the merges use). The
+// attention kernel then streams each sequence's remaining blocks and merges
+// the prefix chunks' records into that sequence's result; in the fused mode
+// the chunks of a cluster merge their partials themselves.
 constexpr int kPfxRows = 128;                   // query rows per CTA = TMEM lanes
 constexpr int kPfxTok = 128;                    // tokens per sub-chunk (MMA N of S)
 constexpr int kPfxSoftmaxWarps = 4;             // warps 0-3: one TMEM lane quarter each
@@ -40,12 +45,15 @@ constexpr int kPfxThreads = 8 * 32;
 constexpr int kPfxKStages = 3;                  // K tiles in flight (S runs ahead)
 constexpr int kPfxVStages = 3;                  // V tiles in flight
 constexpr int kMaxPfxChunks = 32;
-constexpr int kPfxTmemCols = 512;               // S[2] (P over S) and O[2], 128 columns each
+constexpr int kPfxTmemCols = 512;               // S[2] (P over S) at 0 and 128, O at 256
+constexpr int kPfxOCol = 256;                   // O accumulates here over every sub-chunk
+constexpr float kRescaleLog2 = 8.f;             // the running max moves by more than this only
 constexpr int kPfxTile = kPfxTok * 256;         // one operand tile: 128 rows x 128 fp16
 // barriers, then the 1024-aligned tiles Q, K[stages], V[stages]
 constexpr int kPfxHead = 256;
 constexpr int kPfxSmem = 1024 + kPfxHead + (1 + kPfxKStages + kPfxVStages) * kPfxTile;
 constexpr int kFusedSuffixTokens = 32;          // fused mode: the longest suffix past the prefix
+constexpr int kMaxSuffixSub = 2;                // fused mode: suffix sub-chunks per CTA at most
 constexpr int kMaxCluster = 8;                  // fused mode: prefix chunks (cluster size) at most
 
 struct PrefixParams {
@@ -61,21 +69,22 @@ struct PrefixParams {
   int chunk_blocks;              // prefix blocks per chunk
   float qscale;                  // scale * log2(e)
   // fused mode (every suffix at most kFusedSuffixTokens tokens): the chunks
-  // of one (row tile, KV head) form a cluster, merge their partials through
-  // distributed shared memory and attend each sequence's suffix themselves
+  // of one (row tile, KV head) form a cluster; each attends the suffixes of
+  // the rows it finishes as extra sub-chunks, and the cluster merges the
+  // partials through distributed shared memory
   const int32_t* block_table;    // [S][max_blocks]
   const int32_t* seq_lens;       // [S]
-  const __half* k_pool;          // the pools, read row by row for the suffix
-  const __half* v_pool;
-  long long block_stride;        // values from one pool block to the next
   __half* out;                   // [S][Hq][D]
   int max_blocks;
 };
 
-// Shared-memory helpers of a thread-block cluster.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
-                   "memory");
+// Shared-memory helpers of a thread-block cluster. The cluster barrier is
+// split: every thread of every CTA arrives, and a wait returns once all have.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 // The same shared-memory address in the CTA of cluster rank `rank`.
 __device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
@@ -128,38 +137,8 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// 16 / 32 consecutive fp32 columns of this thread's TMEM lane; returns after
-// the load has completed.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15}, [%16];\n\ttcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-// 16 / 8 consecutive 32-bit columns of this thread's TMEM lane; returns after
-// the store has completed.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16};\n\ttcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n\t"
-      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-      : "memory");
-}
+// 32 consecutive fp32 columns of this thread's TMEM lane; returns after the
+// load has completed.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   asm volatile(
@@ -177,32 +156,67 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Fused mode: the rows one CTA of a cluster of C finishes, [c * 128 / C,
-// (c + 1) * 128 / C) of the row tile, and the sequences they belong to.
-// Their suffix rows (the tokens past the prefix, at most kFusedSuffixTokens
-// per sequence) are asked of L2 early, so the end of the kernel finds them
-// there; called by the four softmax warps while they wait for the first S.
-template <int BS, int G>
-__device__ __forceinline__ void prefetch_suffix_rows(const PrefixParams& p, int kvh, int c) {
-  constexpr int D = 128;
-  const int C = gridDim.z, rpc = kPfxRows / C;
-  const int r0 = blockIdx.x * kPfxRows + c * rpc;
-  const int s_lo = r0 / G, s_hi = min(p.num_seqs, (r0 + rpc + G - 1) / G);
-  const int P = p.prefix_blocks_n;
-  const int ntok = (p.max_blocks - P) * BS;
-  for (int i = threadIdx.x; i < (s_hi - s_lo) * ntok; i += kPfxSoftmaxWarps * 32) {
-    const int sq = s_lo + i / ntok, t = i % ntok;
-    const int L = min(p.seq_lens[sq], p.max_blocks * BS);
-    if (t >= L - P * BS) continue;
-    const int blk = p.block_table[static_cast<long long>(sq) * p.max_blocks + P + t / BS];
-    if (blk < 0 || blk >= p.num_blocks) continue;
-    const long long off = static_cast<long long>(blk) * p.block_stride +
-                          (static_cast<long long>(t % BS) * p.num_kv_heads + kvh) * D;
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.k_pool + off));
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.k_pool + off + 64));
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.v_pool + off));
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.v_pool + off + 64));
-  }
+// The 128 fp32 columns of this thread's TMEM lane from `taddr` (an S row)
+// in one load; returns after it has completed.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,"
+      "%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+      "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,"
+      "%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+      "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]),
+        "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]),
+        "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]),
+        "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]),
+        "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]),
+        "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]),
+        "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]),
+        "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]),
+        "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+      : "r"(taddr)
+      : "memory");
+}
+// 64 / 32 consecutive 32-bit columns of this thread's lane; returns after the
+// store has completed.
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&h)[64]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,"
+      "%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,"
+      "%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]), "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7]),
+        "r"(h[8]), "r"(h[9]), "r"(h[10]), "r"(h[11]), "r"(h[12]), "r"(h[13]), "r"(h[14]), "r"(h[15]),
+        "r"(h[16]), "r"(h[17]), "r"(h[18]), "r"(h[19]), "r"(h[20]), "r"(h[21]), "r"(h[22]), "r"(h[23]),
+        "r"(h[24]), "r"(h[25]), "r"(h[26]), "r"(h[27]), "r"(h[28]), "r"(h[29]), "r"(h[30]), "r"(h[31]),
+        "r"(h[32]), "r"(h[33]), "r"(h[34]), "r"(h[35]), "r"(h[36]), "r"(h[37]), "r"(h[38]), "r"(h[39]),
+        "r"(h[40]), "r"(h[41]), "r"(h[42]), "r"(h[43]), "r"(h[44]), "r"(h[45]), "r"(h[46]), "r"(h[47]),
+        "r"(h[48]), "r"(h[49]), "r"(h[50]), "r"(h[51]), "r"(h[52]), "r"(h[53]), "r"(h[54]), "r"(h[55]),
+        "r"(h[56]), "r"(h[57]), "r"(h[58]), "r"(h[59]), "r"(h[60]), "r"(h[61]), "r"(h[62]), "r"(h[63])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+        "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+        "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
 }
 
 // Bulk copy of `bytes` from this CTA's shared memory to shared memory of
@@ -217,27 +231,26 @@ __device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst, uint32_t src, 
       : "memory");
 }
 
-// Fused mode, after the cluster barrier: each CTA finishes rows [c * 128 / C,
-// (c + 1) * 128 / C) of the tile. Every chunk's CTA staged its rows'
-// partials (max and sum in log2 units, then the accumulator; rows of D + 4
-// floats) in its own shared memory at `stage`; each now sends the other
-// CTAs their rows with one bulk copy each into their `recv` area (slot =
-// sender's rank), counted on their `recv_bar`. A row's C partials are merged
-// with the log-sum-exp rule, then the row attends its sequence's suffix (the
-// tokens past the prefix, at most kFusedSuffixTokens) on CUDA cores,
-// continuing that running softmax eight tokens at a time, and the result is
-// written as fp16. Eight threads share a row, 16 dimensions each; a score is
-// their dot products summed by shuffles within the group.
-template <int BS, int G>
-__device__ __forceinline__ void fused_merge_and_suffix(const PrefixParams& p, const float* stage,
-                                                       float* recv, uint64_t* recv_bar, int kvh,
-                                                       int c) {
-  constexpr int D = 128, kPad = D + 4, TPR = 8, DPT = D / TPR, kGrp = 8;
+// Fused mode, once every CTA of the cluster has staged its partials: each CTA
+// finishes rows [c * 128 / C, (c + 1) * 128 / C) of the tile, whose suffix
+// tokens its own last sub-chunks attended. Every chunk's CTA staged its rows'
+// partials (the accumulator, then max and sum in log2 units; rows of D + 4
+// floats) in its own shared memory at `stage`; thread 0 sends each other CTA
+// its rows with one bulk copy into that CTA's `recv` area (slot = sender's
+// rank), counted on the receiver's `recv_bar`; once they have landed this
+// CTA arrives on the cluster barrier that the end of the kernel waits for
+// (so no CTA leaves while its partials are still being copied out). A row's
+// C partials are then merged with the log-sum-exp rule and the result is
+// written as fp16, eight threads per row; thread `part` of a row takes the
+// dimensions 4 * part + 32 * k .. + 3 (k < 4), so that the row's eight
+// threads read 128 contiguous bytes of a partial at a time.
+template <int G>
+__device__ __forceinline__ void fused_merge(const PrefixParams& p, const float* stage, float* recv,
+                                            uint64_t* recv_bar, int kvh, int c) {
+  constexpr int D = 128, kPad = D + 4, TPR = 8, DPT = D / TPR;
   const int C = gridDim.z, rpc = kPfxRows / C;
-  const int S = p.num_seqs, P = p.prefix_blocks_n, cap = p.max_blocks * BS;
   const int part = threadIdx.x % TPR;
   const uint32_t rows_bytes = static_cast<uint32_t>(rpc * kPad * 4);
-  // ---- exchange: my rows of every other chunk's partials arrive here ----
   if (C > 1) {
     if (threadIdx.x == 0) {
       for (int k = 0; k < C; ++k) {
@@ -248,32 +261,20 @@ __device__ __forceinline__ void fused_merge_and_suffix(const PrefixParams& p, co
       }
     }
     const unsigned long long t0 = global_ns();
-    while (!mbar_try_wait(smem_addr(recv_bar), 0) && global_ns() - t0 < kWaitLimitNs) {
+    while (!mbar_try_wait(smem_addr(recv_bar), 0)) {
+      if (global_ns() - t0 > kWaitLimitNs) {
+        atomicOr(p.err, PA_DEVERR_TIMEOUT);
+        break;
+      }
     }
   }
-  // every lane of a warp runs the same rows loop (rpc is a multiple of 4)
+  cluster_arrive();
 #pragma unroll 1
   for (int lr = threadIdx.x / TPR; lr < rpc; lr += kPfxThreads / TPR) {
     const int rt = c * rpc + lr;
     const int row = blockIdx.x * kPfxRows + rt;
     const int seq = row / G, gg = row % G;
-    const bool live = seq < S;
-    // this row's suffix length and, meanwhile, its q slice
-    int suf = 0;
-    uint4 qa = make_uint4(0, 0, 0, 0), qb = qa;
-    if (live) {
-      const __half* qrow =
-          p.q + (static_cast<long long>(seq) * p.num_q_heads + kvh * G + gg) * D + part * DPT;
-      qa = *reinterpret_cast<const uint4*>(qrow);
-      qb = *reinterpret_cast<const uint4*>(qrow + 8);
-      int Ls = p.seq_lens[seq];
-      if (Ls < P * BS || Ls > cap) {
-        if (part == 0 && gg == 0) atomicOr(p.err, PA_DEVERR_BAD_LEN);
-        Ls = Ls < 0 ? 0 : (Ls > cap ? cap : Ls);
-      }
-      suf = min(max(Ls - P * BS, 0), kFusedSuffixTokens);
-    }
-    // ---- merge the C chunk partials of the row (local shared memory) ----
+    if (seq >= p.num_seqs) continue;
     auto src = [&](int k) -> const float* {
       return k == c ? stage + rt * kPad : recv + k * rpc * kPad + lr * kPad;
     };
@@ -292,143 +293,22 @@ __device__ __forceinline__ void fused_merge_and_suffix(const PrefixParams& p, co
         const float w = fast_exp2(mk - mu);
         L += w * r[D + 1];
 #pragma unroll
-        for (int i = 0; i < DPT; i += 4) {
-          const float4 v = *reinterpret_cast<const float4*>(r + part * DPT + i);
-          acc[i] += w * v.x;
-          acc[i + 1] += w * v.y;
-          acc[i + 2] += w * v.z;
-          acc[i + 3] += w * v.w;
+        for (int k4 = 0; k4 < DPT / 4; ++k4) {
+          const float4 v = *reinterpret_cast<const float4*>(r + 4 * part + 32 * k4);
+          acc[4 * k4] = fmaf(w, v.x, acc[4 * k4]);
+          acc[4 * k4 + 1] = fmaf(w, v.y, acc[4 * k4 + 1]);
+          acc[4 * k4 + 2] = fmaf(w, v.z, acc[4 * k4 + 2]);
+          acc[4 * k4 + 3] = fmaf(w, v.w, acc[4 * k4 + 3]);
         }
       }
     }
-    // ---- the suffix: tokens P * BS .. L - 1 of the sequence ----
-    float qv[DPT];
-    {
-      const __half2* h = reinterpret_cast<const __half2*>(&qa);
-      const __half2* h2 = reinterpret_cast<const __half2*>(&qb);
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    __half* orow = p.out + (static_cast<long long>(seq) * p.num_q_heads + kvh * G + gg) * D;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __half22float2(h[i]), f2 = __half22float2(h2[i]);
-        qv[2 * i] = f.x;
-        qv[2 * i + 1] = f.y;
-        qv[8 + 2 * i] = f2.x;
-        qv[8 + 2 * i + 1] = f2.y;
-      }
-    }
-    // the suffix's block ids, loaded and checked once
-    constexpr int kSufBlocks = (kFusedSuffixTokens + BS - 1) / BS;
-    int blk[kSufBlocks];
-    bool bad = false;
-#pragma unroll
-    for (int j = 0; j < kSufBlocks; ++j) {
-      blk[j] = -1;
-      if (j * BS < suf) {
-        blk[j] = p.block_table[static_cast<long long>(seq) * p.max_blocks + P + j];
-        if (blk[j] < 0 || blk[j] >= p.num_blocks) {
-          bad = true;
-          blk[j] = -1;
-        }
-      }
-    }
-    if (bad && part == 0) atomicOr(p.err, PA_DEVERR_BAD_BLOCK);
-    // pool offset of suffix token t of this row's KV head (-1: not read)
-    auto row_off = [&](int t) -> long long {
-      int b = blk[0];
-#pragma unroll
-      for (int j = 1; j < kSufBlocks; ++j)
-        if (t >= j * BS) b = blk[j];
-      if (t >= suf || b < 0) return -1;
-      return static_cast<long long>(b) * p.block_stride +
-             (static_cast<long long>(t % BS) * p.num_kv_heads + kvh) * D + part * DPT;
-    };
-    int suf_w = suf;  // the warp's longest suffix: every lane runs the shuffles
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) suf_w = max(suf_w, __shfl_xor_sync(0xffffffffu, suf_w, off));
-    // running softmax over the suffix from the merged prefix, eight tokens
-    // at a time: all their rows are loaded before any is used
-    float m_run = M;
-    const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll 1
-    for (int t0 = 0; t0 < suf_w; t0 += kGrp) {
-      uint4 kx[kGrp][2], vx[kGrp][2];
-      bool ok[kGrp];
-#pragma unroll
-      for (int u = 0; u < kGrp; ++u) {
-        const long long off = row_off(t0 + u);
-        ok[u] = off >= 0;
-        kx[u][0] = ok[u] ? *reinterpret_cast<const uint4*>(p.k_pool + off) : z;
-        kx[u][1] = ok[u] ? *reinterpret_cast<const uint4*>(p.k_pool + off + 8) : z;
-        vx[u][0] = ok[u] ? *reinterpret_cast<const uint4*>(p.v_pool + off) : z;
-        vx[u][1] = ok[u] ? *reinterpret_cast<const uint4*>(p.v_pool + off + 8) : z;
-      }
-      float sc[kGrp];
-#pragma unroll
-      for (int u = 0; u < kGrp; ++u) {
-        const __half2* h = reinterpret_cast<const __half2*>(&kx[u][0]);
-        const __half2* h2 = reinterpret_cast<const __half2*>(&kx[u][1]);
-        float d = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __half22float2(h[i]), f2 = __half22float2(h2[i]);
-          d = fmaf(qv[2 * i], f.x, d);
-          d = fmaf(qv[2 * i + 1], f.y, d);
-          d = fmaf(qv[8 + 2 * i], f2.x, d);
-          d = fmaf(qv[8 + 2 * i + 1], f2.y, d);
-        }
-        sc[u] = d;
-      }
-      float gm = m_run;
-#pragma unroll
-      for (int u = 0; u < kGrp; ++u) {
-        float d = sc[u];
-        d += __shfl_xor_sync(0xffffffffu, d, 1);
-        d += __shfl_xor_sync(0xffffffffu, d, 2);
-        d += __shfl_xor_sync(0xffffffffu, d, 4);
-        sc[u] = ok[u] ? d * p.qscale : -INFINITY;
-        gm = fmaxf(gm, sc[u]);
-      }
-      if (gm != -INFINITY) {
-        const float cf = m_run == -INFINITY ? 0.f : fast_exp2(m_run - gm);
-        L *= cf;
-#pragma unroll
-        for (int i = 0; i < DPT; ++i) acc[i] *= cf;
-#pragma unroll
-        for (int u = 0; u < kGrp; ++u) {
-          if (ok[u]) {
-            const float w = fast_exp2(sc[u] - gm);
-            L += w;
-            const __half2* h = reinterpret_cast<const __half2*>(&vx[u][0]);
-            const __half2* h2 = reinterpret_cast<const __half2*>(&vx[u][1]);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 f = __half22float2(h[i]), f2 = __half22float2(h2[i]);
-              acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
-              acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
-              acc[8 + 2 * i] = fmaf(w, f2.x, acc[8 + 2 * i]);
-              acc[8 + 2 * i + 1] = fmaf(w, f2.y, acc[8 + 2 * i + 1]);
-            }
-          }
-        }
-        m_run = gm;
-      }
-    }
-    if (live) {
-      // the merged prefix and the suffix are relative to m_run (or to the
-      // prefix's max when the suffix is empty): the sum L normalises both
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      uint4 o0, o1;
-      uint32_t* w0 = reinterpret_cast<uint32_t*>(&o0);
-      uint32_t* w1 = reinterpret_cast<uint32_t*>(&o1);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        w0[i] = pack_half2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-        w1[i] = pack_half2(acc[8 + 2 * i] * inv, acc[8 + 2 * i + 1] * inv);
-      }
-      __half* orow = p.out + (static_cast<long long>(seq) * p.num_q_heads + kvh * G + gg) * D +
-                     part * DPT;
-      *reinterpret_cast<uint4*>(orow) = o0;
-      *reinterpret_cast<uint4*>(orow + 8) = o1;
-    }
+    for (int k4 = 0; k4 < DPT / 4; ++k4)
+      *reinterpret_cast<uint2*>(orow + 4 * part + 32 * k4) =
+          make_uint2(pack_half2(acc[4 * k4] * inv, acc[4 * k4 + 1] * inv),
+                     pack_half2(acc[4 * k4 + 2] * inv, acc[4 * k4 + 3] * inv));
   }
 }
 
@@ -451,10 +331,9 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
   uint64_t* s_full = bars + 2 * NK + 2 * NV;   // [2] S buffer written
   uint64_t* s_free = s_full + 2;               // [2] PV MMAs done with the P written over S
   uint64_t* p_full = s_full + 4;               // [2] P written (4 softmax warps)
-  uint64_t* o_full = s_full + 6;               // [2] O buffer written
-  uint64_t* o_free = s_full + 8;               // [2] O buffer read (4 softmax warps)
-  uint64_t* mma_done = s_full + 10;            // [2] every MMA of an issuer completed
-  constexpr int kBars = 2 * NK + 2 * NV + 12;
+  uint64_t* o_done = s_full + 6;               // one phase per sub-chunk's P V MMAs completed
+  uint64_t* mma_done = s_full + 7;             // [2] every MMA of an issuer (S, PV) completed
+  constexpr int kBars = 2 * NK + 2 * NV + 9;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint64_t* recv_bar = bars + kBars + 1;       // fused mode: the other chunks' partials arrived
@@ -471,14 +350,40 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
   const int tok_lo = c * p.chunk_blocks * BS;
   const int tok_hi = max(tok_lo, min(p.prefix_blocks_n, (c + 1) * p.chunk_blocks) * BS);
   const int nsub = (tok_hi - tok_lo + kPfxTok - 1) / kPfxTok;
-  auto sub_len = [&](int t) { return min(kPfxTok, tok_hi - (tok_lo + t * kPfxTok)); };
+  // Fused mode: after its nsub prefix sub-chunks the CTA attends the suffixes
+  // (the table's columns past the prefix, W tokens per sequence) of the
+  // sequences whose rows it finishes, [c * 128 / C, (c + 1) * 128 / C) of the
+  // tile, as nsfx more sub-chunks: sub-chunk j holds the W suffix tokens of
+  // each of the slice's sequences j * QPS .. j * QPS + QPS - 1 (QPS = 128 /
+  // W), and each row takes only its own sequence's tokens, up to its length.
+  const int P = p.prefix_blocks_n;
+  const int W = FUSED ? (p.max_blocks - P) * BS : 0;  // 0, 16 or 32
+  const int Wd = W > 0 ? W : kPfxTok;  // W as a divisor (only used when W > 0)
+  const int QPS = kPfxTok / Wd;
+  const int rpc = kPfxRows / static_cast<int>(gridDim.z);
+  const int slice_s0 = (blockIdx.x * kPfxRows + c * rpc) / G;
+  const int slice_n = W > 0 ? max(0, min(S, slice_s0 + rpc / G) - slice_s0) : 0;
+  const int nsfx = (slice_n + QPS - 1) / QPS;
+  const int ntot = nsub + nsfx;
+  auto sub_len = [&](int t) {
+    return t < nsub ? min(kPfxTok, tok_hi - (tok_lo + t * kPfxTok)) : kPfxTok;
+  };
+  // suffix tokens of a sequence of length L (checked against the prefix and
+  // the table, a bad one reported when `report`)
+  auto suffix_of = [&](int L, bool report) {
+    const int cap = p.max_blocks * BS;
+    if (L < P * BS || L > cap) {
+      if (report) atomicOr(p.err, PA_DEVERR_BAD_LEN);
+      L = L < 0 ? 0 : (L > cap ? cap : L);
+    }
+    return min(max(L - P * BS, 0), W);
+  };
 
   if (threadIdx.x == 0) {
-    // p_full and o_free count the four softmax warps; the others one arrival
-    // (a TMA transaction count or an MMA commit)
+    // p_full counts the four softmax warps; the others one arrival (a TMA
+    // transaction count or an MMA commit)
     for (int i = 0; i < kBars; ++i) {
-      const uint64_t* b = &bars[i];
-      const bool softmax = (b >= p_full && b < p_full + 2) || (b >= o_free && b < o_free + 2);
+      const bool softmax = &bars[i] >= p_full && &bars[i] < p_full + 2;
       mbar_init(smem_addr(&bars[i]), softmax ? kPfxSoftmaxWarps : 1);
     }
     *abort_flag = 0;
@@ -556,16 +461,33 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
       const int nb = sub_len(t) / BS;
       int id = 0;
       if (lane < nb) {
-        id = __ldg(p.prefix_blocks + (tok_lo + t * kPfxTok) / BS + lane);
-        if (id < 0 || id >= p.num_blocks) {
-          if (is_k) atomicOr(p.err, PA_DEVERR_BAD_BLOCK);
-          id = 0;  // an in-range block keeps the byte count; the result is flagged
+        if (t < nsub) {
+          id = __ldg(p.prefix_blocks + (tok_lo + t * kPfxTok) / BS + lane);
+          if (id < 0 || id >= p.num_blocks) {
+            if (is_k) atomicOr(p.err, PA_DEVERR_BAD_BLOCK);
+            id = 0;  // an in-range block keeps the byte count; the result is flagged
+          }
+        } else {
+          // suffix sub-chunk: slot `lane` is block jb of the slice's sequence q
+          const int bpq = Wd / BS, q = (t - nsub) * QPS + lane / bpq, jb = lane % bpq;
+          if (q < slice_n) {
+            const int seq = slice_s0 + q;
+            if (jb * BS < suffix_of(p.seq_lens[seq], false)) {
+              id = p.block_table[static_cast<long long>(seq) * p.max_blocks + P + jb];
+              if (id < 0 || id >= p.num_blocks) {
+                if (is_k) atomicOr(p.err, PA_DEVERR_BAD_BLOCK);
+                id = 0;
+              }
+            }
+          }
+          // a slot no row reads loads block 0: its scores are masked and its
+          // V rows cleared before the P V MMAs
         }
       }
       return id;
     };
-    int next_ids = nsub > 0 ? load_ids(0) : 0;
-    for (int t = 0; t < nsub; ++t, ++issued) {
+    int next_ids = ntot > 0 ? load_ids(0) : 0;
+    for (int t = 0; t < ntot; ++t, ++issued) {
       const int st = t % nst, n = sub_len(t);
       const int ids = next_ids;
       if (t >= nst &&
@@ -584,7 +506,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
           }
         }
       }
-      if (t + 1 < nsub) next_ids = load_ids(t + 1);
+      if (t + 1 < ntot) next_ids = load_ids(t + 1);
       __syncwarp();
     }
     if (*abort_flag) {
@@ -599,7 +521,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
   } else if (warp == kPfxWarpS) {
     // ---- S issuer: S_t = Q K_t^T into TMEM buffer t % 2 ----
     const uint32_t qa = smem_addr(q_s);
-    for (int t = 0; t < nsub; ++t) {
+    for (int t = 0; t < ntot; ++t) {
       const int st = t % NK, b = t & 1;
       if (!warp_wait_phase(smem_addr(&k_full[st]), (t / NK) & 1, abort_flag, p.err)) break;
       if (t >= 2 && !warp_wait_phase(smem_addr(&s_free[b]), ((t - 2) >> 1) & 1, abort_flag, p.err))
@@ -625,13 +547,36 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
     while (!mbar_try_wait(smem_addr(&mma_done[0]), 0) && global_ns() - w0 < kWaitLimitNs) {
     }
   } else if (warp == kPfxWarpPV) {
-    // ---- PV issuer: O_t = P_t V_t into TMEM buffer 2 + t % 2 ----
-    for (int t = 0; t < nsub; ++t) {
+    // ---- PV issuer: O += P_t V_t, O in TMEM for the whole chunk ----
+    // suffix lengths of the slice's sequences, lane q for sequence q (a slice
+    // has at most 16), for the suffix sub-chunks' V rows
+    int my_suf = 0;
+    if (FUSED && lane < slice_n) my_suf = suffix_of(p.seq_lens[slice_s0 + lane], false);
+    for (int t = 0; t < ntot; ++t) {
       const int st = t % NV, b = t & 1;
       if (!warp_wait_phase(smem_addr(&p_full[b]), (t >> 1) & 1, abort_flag, p.err)) break;
       if (!warp_wait_phase(smem_addr(&v_full[st]), (t / NV) & 1, abort_flag, p.err)) break;
-      if (t >= 2 && !warp_wait_phase(smem_addr(&o_free[b]), ((t - 2) >> 1) & 1, abort_flag, p.err))
-        break;
+      if (FUSED && t >= nsub) {
+        // V rows of a suffix sub-chunk that no row attends (past a sequence's
+        // length, or past the slice) may hold anything, NaN included, and
+        // 0 * NaN would reach O: clear them
+        unsigned char* vt = v_s + st * kPfxTile;
+#pragma unroll 1
+        for (int rho = lane; rho < kPfxTok; rho += 32) {
+          const int q = (t - nsub) * QPS + rho / Wd;
+          const int sq = __shfl_sync(0xffffffffu, my_suf, q & 31);
+          if (q >= slice_n || rho % Wd >= sq) {
+            const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              *reinterpret_cast<uint4*>(vt + rho * 128 + i * 16) = z;
+              *reinterpret_cast<uint4*>(vt + HALF + rho * 128 + i * 16) = z;
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
       tc_fence_after();
       if (lane == 0) {
         const uint32_t vb = smem_addr(v_s + st * kPfxTile);
@@ -639,9 +584,9 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
         const int n = sub_len(t);
         // A = P over S buffer b: 16 tokens per MMA, 8 TMEM columns
         for (int k = 0; k < n / 16; ++k)
-          tc_mma_ts(tmem + (2 + b) * kPfxTok, tmem + b * kPfxTok + 8 * k,
-                    sw128_desc(vb + k * 2048, HALF, 1024), id, k > 0);
-        tc_commit(smem_addr(&o_full[b]));
+          tc_mma_ts(tmem + kPfxOCol, tmem + b * kPfxTok + 8 * k,
+                    sw128_desc(vb + k * 2048, HALF, 1024), id, (t > 0 || k > 0) ? 1u : 0u);
+        tc_commit(smem_addr(o_done));
         tc_commit(smem_addr(&v_empty[st]));
         tc_commit(smem_addr(&s_free[b]));
       }
@@ -654,102 +599,149 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
     }
   } else {
     // ---- softmax warps: query row r = 32 * warp + lane (TMEM lane r) ----
-    if constexpr (FUSED) prefetch_suffix_rows<BS, G>(p, kvh, c);
     const int r = warp * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    float o[D];
-#pragma unroll
-    for (int i = 0; i < D; ++i) o[i] = 0.f;
-    float m = -INFINITY, l = 0.f, alpha_prev = 0.f;
-    bool ok = true;
-    // fold O_t (relative to the max after sub-chunk t) into o
-    auto fold = [&](int t, float alpha) -> bool {
-      const int b = t & 1;
-      if (!warp_wait_phase(smem_addr(&o_full[b]), (t >> 1) & 1, abort_flag, p.err)) return false;
-      tc_fence_after();
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        float v[32];
-        tmem_ld32(lane_base + (2 + b) * kPfxTok + c0, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[c0 + i] = fmaf(o[c0 + i], alpha, v[i]);
+    const uint32_t o_tm = lane_base + kPfxOCol;
+    // scores are scaled by qscale (any sign); the row max of the scaled
+    // scores is the max of the raw ones times qscale, or the min if qscale < 0
+    const bool qpos = p.qscale >= 0.f;
+    // fused mode: this row's place among the slice's sequences (-1: not in
+    // the slice) and its sequence's length, read now and checked when the
+    // suffix sub-chunks come
+    int sfx_q = -1, sfx_len = 0;
+    if (FUSED && r >= c * rpc && r < (c + 1) * rpc) {
+      const int seq = (blockIdx.x * kPfxRows + r) / G;
+      if (seq < S) {
+        sfx_q = seq - slice_s0;
+        sfx_len = p.seq_lens[seq];
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&o_free[b]));
-      return true;
-    };
-    for (int t = 0; t < nsub && ok; ++t) {
+    }
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int t = 0; t < ntot; ++t) {
       const int n = sub_len(t), b = t & 1;
-      if (!warp_wait_phase(smem_addr(&s_full[b]), (t >> 1) & 1, abort_flag, p.err)) break;
+      if (!warp_wait_phase(smem_addr(&s_full[b]), (t >> 1) & 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       const uint32_t sa = lane_base + b * kPfxTok;
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      int c0 = 0;
-      for (; c0 + 32 <= n; c0 += 32) {
-        float v[32];
-        tmem_ld32(sa + c0, v);
+      uint32_t sv[kPfxTok];
+      tmem_ld128(sa, sv);
+      const uint32_t neutral = qpos ? 0xff800000u : 0x7f800000u;  // -inf / +inf
+      if (n < kPfxTok) {
+        // a short last sub-chunk: the columns past it hold no scores; they
+        // take no part in the max, their P is never read (the P V MMAs stop
+        // at n) and their sum is left out below
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], v[i] * p.qscale);
+        for (int i = 0; i < kPfxTok; ++i)
+          if (i >= n) sv[i] = neutral;
       }
-      if (c0 < n) {
-        float v[16];
-        tmem_ld16(sa + c0, v);
+      if (FUSED && t >= nsub) {
+        // a suffix sub-chunk: this row's columns are its own sequence's
+        // suffix tokens [lo, lo + sfx_n); every other score becomes the
+        // neutral value, whose P is exactly 0 (qscale is not 0 here)
+        const int j = t - nsub;
+        const bool mine = sfx_q >= j * QPS && sfx_q < (j + 1) * QPS;
+        const int lo = mine ? (sfx_q - j * QPS) * W : 0;
+        const int hi = mine ? lo + suffix_of(sfx_len, (blockIdx.x * kPfxRows + r) % G == 0) : 0;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], v[i] * p.qscale);
+        for (int i = 0; i < kPfxTok; ++i)
+          if (i < lo || i >= hi) sv[i] = neutral;
       }
-      const float mn = fmaxf(m, fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])));
-      const float alpha = fast_exp2(m - mn);
-      m = mn;
-      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-      // P = exp2(S * qscale - m) as fp16 pairs, written over the S columns
-      // already read: tokens c0 .. c0+2k-1 go to columns c0/2 .. c0/2+k-1
-      auto emit = [&](const float* v, uint32_t* h, int cnt) {
+      float e4[4];
+      if (qpos) {
+        e4[0] = e4[1] = e4[2] = e4[3] = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          if (i < cnt) {
-            const float e0 = fast_exp2(fmaf(v[2 * i], p.qscale, -mn));
-            const float e1 = fast_exp2(fmaf(v[2 * i + 1], p.qscale, -mn));
-            sum4[(2 * i) & 3] += e0;
-            sum4[(2 * i + 1) & 3] += e1;
-            h[i] = pack_half2(e0, e1);
-          }
+        for (int i = 0; i < kPfxTok; ++i) e4[i & 3] = fmaxf(e4[i & 3], __uint_as_float(sv[i]));
+      } else {
+        e4[0] = e4[1] = e4[2] = e4[3] = INFINITY;
+#pragma unroll
+        for (int i = 0; i < kPfxTok; ++i) e4[i & 3] = fminf(e4[i & 3], __uint_as_float(sv[i]));
+      }
+      const float ext = qpos ? fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]))
+                             : fminf(fminf(e4[0], e4[1]), fminf(e4[2], e4[3]));
+      const float mx = ext * p.qscale;
+      // The reference max m moves only when this sub-chunk's max exceeds it
+      // by more than kRescaleLog2; otherwise P is taken against m (each
+      // value at most 2^kRescaleLog2) and O in TMEM is left as it is.
+      const bool grow = mx > m + kRescaleLog2;
+      if (t > 0 && __any_sync(0xffffffffu, grow)) {
+        // O holds P V up to the previous sub-chunk once those MMAs complete
+        // (S_t was issued after P V of sub-chunk t - 2 had completed, so
+        // o_done is at most one phase short of the one waited for)
+        if (!warp_wait_phase(smem_addr(o_done), (t - 1) & 1, abort_flag, p.err)) {
+          ok = false;
+          break;
         }
-      };
-      for (c0 = 0; c0 + 32 <= n; c0 += 32) {
-        float v[32];
-        tmem_ld32(sa + c0, v);
-        uint32_t h[16];
-        emit(v, h, 16);
-        tmem_st16(sa + c0 / 2, h);
+        tc_fence_after();
+        const float f = grow ? fast_exp2(m - mx) : 1.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float v[32];
+          tmem_ld32(o_tm + c0, v);
+          uint32_t w[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i] * f);
+          tmem_st32(o_tm + c0, w);
+        }
       }
-      if (c0 < n) {
-        float v[16];
-        tmem_ld16(sa + c0, v);
-        uint32_t h[16];
-        emit(v, h, 8);
-        tmem_st8(sa + c0 / 2, h);
+      if (grow) {
+        l *= fast_exp2(m - mx);  // 0 while m is -inf
+        m = mx;
       }
-      l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+      // P = exp2(S * qscale - m) as fp16 pairs, written over the S columns:
+      // tokens 2i, 2i+1 go to column i; sums per 16 tokens. While m is still
+      // -inf every score so far was masked: take 0, so that masked scores
+      // give exactly 0 (not NaN)
+      const float mz = m == -INFINITY ? 0.f : m;
+      uint32_t h[kPfxTok / 2];
+      float sum16[kPfxTok / 16];
+#pragma unroll
+      for (int g = 0; g < kPfxTok / 16; ++g) sum16[g] = 0.f;
+#pragma unroll
+      for (int i = 0; i < kPfxTok / 2; ++i) {
+        const float e0 = fast_exp2(fmaf(__uint_as_float(sv[2 * i]), p.qscale, -mz));
+        const float e1 = fast_exp2(fmaf(__uint_as_float(sv[2 * i + 1]), p.qscale, -mz));
+        sum16[i / 8] += e0 + e1;
+        h[i] = pack_half2(e0, e1);
+      }
+      tmem_st64(sa, h);
+      float sum = 0.f;
+#pragma unroll
+      for (int g = 0; g < kPfxTok / 16; ++g) sum += g * 16 < n ? sum16[g] : 0.f;
+      l += sum;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&p_full[b]));
-      // O of the previous sub-chunk, folded while the tensor cores run this one's
-      if (t > 0) ok = fold(t - 1, alpha_prev);
-      alpha_prev = alpha;
     }
-    if (ok && nsub > 0) ok = fold(nsub - 1, alpha_prev);
-    // ---- the chunk's partial records of this warp's 32 rows ----
-    // Every MMA has completed (the last O was folded), so the K tiles are
-    // free: each warp stages its rows there (16.5 KB, rows padded to 132
-    // floats against bank conflicts) and writes each sequence's G rows as one
-    // contiguous run, 512 bytes per store instruction.
+    // a table with no columns past the prefix: each length must be the prefix's
+    if (FUSED && W == 0 && sfx_q >= 0) suffix_of(sfx_len, (blockIdx.x * kPfxRows + r) % G == 0);
+    // O (relative to m) once every P V MMA has completed: the PV issuer's
+    // final commit (o_done cannot tell: up to two of its phases may still be
+    // open here). Every MMA has then completed, so the K tiles are free: each
+    // warp stages its rows there (16.5 KB, rows padded to 132 floats against
+    // bank conflicts)
+    if (ok && ntot > 0) {
+      ok = warp_wait_phase(smem_addr(&mma_done[1]), 0, abort_flag, p.err);
+      if (ok) tc_fence_after();
+    }
     constexpr int kPad = D + 4;
     float* stage = reinterpret_cast<float*>(k_s) + warp * 32 * kPad;
+#pragma unroll 1
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      float v[32];
+      if (ok && ntot > 0) {
+        tmem_ld32(o_tm + c0, v);
+      } else {
 #pragma unroll
-    for (int i = 0; i < D; i += 4)
-      *reinterpret_cast<float4*>(stage + lane * kPad + i) =
-          make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 32; i += 4)
+        *reinterpret_cast<float4*>(stage + lane * kPad + c0 + i) =
+            make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    }
     if constexpr (FUSED) {
       // the cluster merges the rows from here (see the end of the kernel);
       // bulk copies read them, so the writes are ordered for that proxy
@@ -781,6 +773,12 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
       }
     }
   }
+  // Fused mode: every thread of every CTA of the cluster (the chunks of this
+  // row tile and KV head) arrives here, whatever happened before, once its
+  // part is done: the softmax warps after staging their rows, when this
+  // CTA's P V MMAs have completed and its V tiles (where the other CTAs'
+  // partials will land) are free; the other warps after their loops.
+  if constexpr (FUSED) cluster_arrive();
   tc_fence_before();
   __syncthreads();
   if (warp == kPfxWarpS) {
@@ -790,14 +788,13 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
                  : "memory");
   }
   if constexpr (FUSED) {
-    // Every CTA of the cluster (the chunks of this row tile and KV head)
-    // reaches both barriers, whatever happened before: the first makes all
-    // staged partials visible, the second keeps each CTA's shared memory
-    // alive until the others have read it.
-    cluster_sync_all();
-    fused_merge_and_suffix<BS, G>(p, reinterpret_cast<const float*>(k_s),
-                                  reinterpret_cast<float*>(v_s), recv_bar, kvh, c);
-    cluster_sync_all();
+    cluster_wait();
+    fused_merge<G>(p, reinterpret_cast<const float*>(k_s), reinterpret_cast<float*>(v_s),
+                   recv_bar, kvh, c);
+    // the barrier fused_merge arrived on: every CTA's partials have landed
+    // where they were sent, so no copy out of this CTA's shared memory is
+    // still running when it leaves
+    cluster_wait();
   }
 }
 
@@ -934,16 +931,19 @@ pa_status prefix_pass(const pa::SharedPrefixCall& call, const pa::DeviceInfo& de
   pp.qscale = call.qscale;
   pp.block_table = call.block_table;
   pp.seq_lens = call.seq_lens;
-  pp.k_pool = static_cast<const __half*>(call.k_pool);
-  pp.v_pool = static_cast<const __half*>(call.v_pool);
-  pp.block_stride = call.block_stride_bytes / 2;
   pp.out = static_cast<__half*>(call.out);
   pp.max_blocks = call.max_blocks;
   const int S = call.num_seqs, Hkv = call.num_kv_heads, P = call.prefix_blocks_n;
-  // one launch when every suffix is short and the clusters fit
-  if ((call.max_blocks - P) * BS <= kFusedSuffixTokens) {
+  // One launch when every suffix is short, the clusters fit and each CTA's
+  // suffixes fill at most kMaxSuffixSub sub-chunks. The suffix masks need
+  // qscale != 0 (a zero scale makes every weight equal: the unfused path
+  // handles it).
+  const int W = (call.max_blocks - P) * BS;
+  if (W <= kFusedSuffixTokens && call.qscale != 0.f) {
     const PfxGeom fg = fused_prefix_geometry(S, G, Hkv, P, dev.sm_count);
-    if (fused_prefix_fits<BS, G>(fg, dev)) {
+    const int per_slice = kPfxRows / fg.chunks / G;  // sequences whose rows one CTA finishes
+    const int nsfx = (per_slice * W + kPfxTok - 1) / kPfxTok;
+    if (nsfx <= kMaxSuffixSub && fused_prefix_fits<BS, G>(fg, dev)) {
       pp.chunk_blocks = fg.chunk_blocks;
       *suffix_pass = false;
       *chunks = fg.chunks;

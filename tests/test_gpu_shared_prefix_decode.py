@@ -177,3 +177,54 @@ def test_short_suffix_bad_length_and_block_are_reported(pa):
     with pytest.raises(pa.PaError) as e:
         pa.pa_device_error()
     assert e.value.flags & pa.PA_DEVERR_BAD_BLOCK
+
+
+# ---------------------------------- short suffixes on the tensor cores --
+# In the one-launch mode the CTA that finishes a slice of a tile's rows also
+# attends the suffixes of that slice's sequences, as extra 128-token
+# sub-chunks: W = (table width - P) * BS tokens per sequence, 128 / W
+# sequences per sub-chunk, each row masked to its own sequence's tokens; V
+# rows past a length are cleared before the P V MMAs (the poisoned rows here
+# would otherwise reach the output as 0 * NaN).
+@pytest.mark.parametrize("scale", [0.088, -0.07, 0.6])
+def test_two_suffix_subchunks_and_an_empty_chunk(pa, scale):
+    """64 sequences, G = 2: one row tile in clusters of 4 chunks over a
+    5-block prefix (the last chunk holds no prefix block), 16 sequences per
+    slice with 16 suffix tokens each = two suffix sub-chunks per CTA; the
+    last CTA's rows have only suffix sub-chunks. At scale 0.6 the running
+    max often moves by more than 2^8, so O is rescaled in tensor memory."""
+    rng = np.random.default_rng(21)
+    suffix = rng.integers(0, 17, 64).tolist()
+    suffix[:4] = [0, 16, 1, 15]
+    suffix[-3:] = [0, 16, 3]
+    q, kp, vp, prefix, table, lens = _case(31, 64, 4, 2, 16, 5, suffix, mb=6)
+    got = _run(pa, q, kp, vp, prefix, table, lens, np.float32(scale))
+    exp = oracle.decode_attention(q, kp, vp, table, lens, np.float32(scale))
+    assert_close_attention(got, exp, f"two suffix sub-chunks, scale {scale}")
+    assert pa.pa_device_error() == 0
+
+
+def test_suffix_width_32_in_two_subchunks(pa):
+    """128 sequences, 32 q / 8 kv heads, a 40-block prefix and a table two
+    blocks wider: 8 sequences per slice x 32 suffix tokens = two sub-chunks."""
+    rng = np.random.default_rng(22)
+    suffix = rng.integers(0, 33, 128).tolist()
+    suffix[:5] = [0, 32, 16, 17, 31]
+    q, kp, vp, prefix, table, lens = _case(32, 128, 32, 8, 16, 40, suffix, mb=42)
+    got = _run(pa, q, kp, vp, prefix, table, lens, np.float32(0.088))
+    seqs = [0, 1, 2, 3, 4, 63, 64, 127]
+    exp = oracle.decode_attention(q, kp, vp, table, lens, np.float32(0.088), seqs=seqs)
+    assert_close_attention(got[seqs], exp[seqs], "suffix width 32")
+    assert np.isfinite(got).all()
+    assert pa.pa_device_error() == 0
+
+
+def test_zero_scale_gives_uniform_weights(pa):
+    """scale 0: every token of a sequence weighs the same (the call takes the
+    two-kernel path for it)."""
+    suffix = [0, 1, 9, 16, 5]
+    q, kp, vp, prefix, table, lens = _case(33, 5, 8, 2, 16, 6, suffix, mb=7)
+    got = _run(pa, q, kp, vp, prefix, table, lens, np.float32(0.0))
+    exp = oracle.decode_attention(q, kp, vp, table, lens, np.float32(0.0))
+    assert_close_attention(got, exp, "scale 0")
+    assert pa.pa_device_error() == 0
