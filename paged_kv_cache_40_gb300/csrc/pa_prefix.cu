@@ -54,6 +54,9 @@ constexpr int kPfxHead = 256;
 constexpr int kPfxSmem = 1024 + kPfxHead + (1 + kPfxKStages + kPfxVStages) * kPfxTile;
 constexpr int kFusedSuffixTokens = 32;          // fused mode: the longest suffix past the prefix
 constexpr int kMaxSuffixSub = 2;                // fused mode: suffix sub-chunks per CTA at most
+// fused mode: a row's partial as it crosses the cluster: the accumulator
+// divided by its sum as 128 fp16, then max and sum (fp32), padded to 16 bytes
+constexpr int kXRow = 128 * 2 + 16;
 constexpr int kMaxCluster = 8;                  // fused mode: prefix chunks (cluster size) at most
 
 struct PrefixParams {
@@ -231,35 +234,27 @@ __device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst, uint32_t src, 
       : "memory");
 }
 
-// Fused mode, once every CTA of the cluster has staged its partials: each CTA
-// finishes rows [c * 128 / C, (c + 1) * 128 / C) of the tile, whose suffix
-// tokens its own last sub-chunks attended. Every chunk's CTA staged its rows'
-// partials (the accumulator, then max and sum in log2 units; rows of D + 4
-// floats) in its own shared memory at `stage`; thread 0 sends each other CTA
-// its rows with one bulk copy into that CTA's `recv` area (slot = sender's
-// rank), counted on the receiver's `recv_bar`; once they have landed this
-// CTA arrives on the cluster barrier that the end of the kernel waits for
-// (so no CTA leaves while its partials are still being copied out). A row's
-// C partials are then merged with the log-sum-exp rule and the result is
+// Fused mode: each CTA finishes rows [c * 128 / C, (c + 1) * 128 / C) of the
+// tile, whose suffix tokens its own last sub-chunks attended. Every chunk's
+// CTA staged each row's partial in its own shared memory (`stage`, rows of
+// kXRow bytes: the accumulator divided by the sum as fp16, then max and sum
+// in log2 units as fp32) and sent the rows of this CTA's slice with bulk
+// copies into `recv` at [sender's rank][row in the slice], counted on
+// `recv_bar`. Once the C - 1 other chunks' rows have landed this CTA arrives
+// on the cluster barrier that the end of the kernel waits for (so no CTA
+// leaves while its staged rows are still being copied out). A row's C
+// partials are then merged with the log-sum-exp rule and the result is
 // written as fp16, eight threads per row; thread `part` of a row takes the
-// dimensions 4 * part + 32 * k .. + 3 (k < 4), so that the row's eight
-// threads read 128 contiguous bytes of a partial at a time.
+// dimensions 4 * part + 32 * k .. + 3 (k < 4), so that the row's eight threads
+// read 64 contiguous bytes of a partial at a time.
 template <int G>
-__device__ __forceinline__ void fused_merge(const PrefixParams& p, const float* stage, float* recv,
-                                            uint64_t* recv_bar, int kvh, int c) {
-  constexpr int D = 128, kPad = D + 4, TPR = 8, DPT = D / TPR;
+__device__ __forceinline__ void fused_merge(const PrefixParams& p, const unsigned char* stage,
+                                            const unsigned char* recv, uint64_t* recv_bar,
+                                            int kvh, int c) {
+  constexpr int D = 128, TPR = 8;
   const int C = gridDim.z, rpc = kPfxRows / C;
   const int part = threadIdx.x % TPR;
-  const uint32_t rows_bytes = static_cast<uint32_t>(rpc * kPad * 4);
   if (C > 1) {
-    if (threadIdx.x == 0) {
-      for (int k = 0; k < C; ++k) {
-        if (k == c) continue;
-        bulk_copy_s2cluster(cluster_map(smem_addr(recv) + c * rows_bytes, k),
-                            smem_addr(stage) + k * rows_bytes, rows_bytes,
-                            cluster_map(smem_addr(recv_bar), k));
-      }
-    }
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(smem_addr(recv_bar), 0)) {
       if (global_ns() - t0 > kWaitLimitNs) {
@@ -275,37 +270,40 @@ __device__ __forceinline__ void fused_merge(const PrefixParams& p, const float* 
     const int row = blockIdx.x * kPfxRows + rt;
     const int seq = row / G, gg = row % G;
     if (seq >= p.num_seqs) continue;
-    auto src = [&](int k) -> const float* {
-      return k == c ? stage + rt * kPad : recv + k * rpc * kPad + lr * kPad;
+    auto src = [&](int k) -> const unsigned char* {
+      return k == c ? stage + rt * kXRow : recv + (k * rpc + lr) * kXRow;
     };
     float M = -INFINITY;
 #pragma unroll 1
-    for (int k = 0; k < C; ++k) M = fmaxf(M, src(k)[D]);
+    for (int k = 0; k < C; ++k) M = fmaxf(M, reinterpret_cast<const float*>(src(k) + 2 * D)[0]);
     const float mu = M == -INFINITY ? 0.f : M;
-    float acc[DPT], L = 0.f;
+    float acc[16], L = 0.f;
 #pragma unroll
-    for (int i = 0; i < DPT; ++i) acc[i] = 0.f;
+    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
 #pragma unroll 1
     for (int k = 0; k < C; ++k) {
-      const float* r = src(k);
-      const float mk = r[D];
+      const unsigned char* r = src(k);
+      const float mk = reinterpret_cast<const float*>(r + 2 * D)[0];
       if (mk != -INFINITY) {
-        const float w = fast_exp2(mk - mu);
-        L += w * r[D + 1];
+        // w * l_k: the weight of the partial's normalised accumulator
+        const float wl = fast_exp2(mk - mu) * reinterpret_cast<const float*>(r + 2 * D)[1];
+        L += wl;
 #pragma unroll
-        for (int k4 = 0; k4 < DPT / 4; ++k4) {
-          const float4 v = *reinterpret_cast<const float4*>(r + 4 * part + 32 * k4);
-          acc[4 * k4] = fmaf(w, v.x, acc[4 * k4]);
-          acc[4 * k4 + 1] = fmaf(w, v.y, acc[4 * k4 + 1]);
-          acc[4 * k4 + 2] = fmaf(w, v.z, acc[4 * k4 + 2]);
-          acc[4 * k4 + 3] = fmaf(w, v.w, acc[4 * k4 + 3]);
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const uint2 h = *reinterpret_cast<const uint2*>(r + 2 * (4 * part + 32 * k4));
+          const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
+          const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
+          acc[4 * k4] = fmaf(wl, a.x, acc[4 * k4]);
+          acc[4 * k4 + 1] = fmaf(wl, a.y, acc[4 * k4 + 1]);
+          acc[4 * k4 + 2] = fmaf(wl, b.x, acc[4 * k4 + 2]);
+          acc[4 * k4 + 3] = fmaf(wl, b.y, acc[4 * k4 + 3]);
         }
       }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     __half* orow = p.out + (static_cast<long long>(seq) * p.num_q_heads + kvh * G + gg) * D;
 #pragma unroll
-    for (int k4 = 0; k4 < DPT / 4; ++k4)
+    for (int k4 = 0; k4 < 4; ++k4)
       *reinterpret_cast<uint2*>(orow + 4 * part + 32 * k4) =
           make_uint2(pack_half2(acc[4 * k4] * inv, acc[4 * k4 + 1] * inv),
                      pack_half2(acc[4 * k4 + 2] * inv, acc[4 * k4 + 3] * inv));
@@ -353,9 +351,13 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
   // Fused mode: after its nsub prefix sub-chunks the CTA attends the suffixes
   // (the table's columns past the prefix, W tokens per sequence) of the
   // sequences whose rows it finishes, [c * 128 / C, (c + 1) * 128 / C) of the
-  // tile, as nsfx more sub-chunks: sub-chunk j holds the W suffix tokens of
-  // each of the slice's sequences j * QPS .. j * QPS + QPS - 1 (QPS = 128 /
-  // W), and each row takes only its own sequence's tokens, up to its length.
+  // tile, as nsfx more sub-chunks: sub-chunk j holds a W-row segment for each
+  // of the slice's sequences j * QPS .. j * QPS + QPS - 1 (QPS = 128 / W).
+  // A sequence with s suffix tokens has them in the last s rows of its
+  // segment (its blocks in reverse order, each copied from a token
+  // coordinate shifted down so that the rows past its length fall before
+  // the block and are filled with zeros by the copy), and each row takes only
+  // its own segment's last s columns.
   const int P = p.prefix_blocks_n;
   const int W = FUSED ? (p.max_blocks - P) * BS : 0;  // 0, 16 or 32
   const int Wd = W > 0 ? W : kPfxTok;  // W as a divisor (only used when W > 0)
@@ -388,12 +390,12 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
     }
     *abort_flag = 0;
     if (FUSED) {
-      // the other C - 1 chunks of the cluster each send this CTA's rows of
-      // their partials (see the end of the kernel)
+      // the other C - 1 chunks of the cluster each send this CTA the
+      // partials of its rows (see the end of the kernel)
       const uint32_t rb = smem_addr(recv_bar);
       mbar_init(rb, 1);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-      mbar_arrive_expect_tx(rb, (gridDim.z - 1) * (kPfxRows / gridDim.z) * (128 + 4) * 4);
+      mbar_arrive_expect_tx(rb, (gridDim.z - 1) * (kPfxRows / gridDim.z) * kXRow);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -457,9 +459,13 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
     unsigned char* ring = is_k ? k_s : v_s;
     // block ids of a sub-chunk: one per lane, all loaded at once; the next
     // sub-chunk's are in flight while this one's copies are issued
-    auto load_ids = [&](int t) {
+    // block id of slot `lane` of sub-chunk t, and (suffix sub-chunks) how
+    // many of its rows are read: the copy's token coordinate is shifted down
+    // by the rest, which the copy fills with zeros
+    auto load_ids = [&](int t, int& valid) {
       const int nb = sub_len(t) / BS;
       int id = 0;
+      valid = BS;
       if (lane < nb) {
         if (t < nsub) {
           id = __ldg(p.prefix_blocks + (tok_lo + t * kPfxTok) / BS + lane);
@@ -468,28 +474,34 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
             id = 0;  // an in-range block keeps the byte count; the result is flagged
           }
         } else {
-          // suffix sub-chunk: slot `lane` is block jb of the slice's sequence q
-          const int bpq = Wd / BS, q = (t - nsub) * QPS + lane / bpq, jb = lane % bpq;
+          // suffix sub-chunk: slot `lane` holds block jb of the slice's
+          // sequence q, the segment's blocks in reverse order
+          const int bpq = Wd / BS, q = (t - nsub) * QPS + lane / bpq;
+          const int jb = bpq - 1 - lane % bpq;
+          valid = 0;
           if (q < slice_n) {
             const int seq = slice_s0 + q;
-            if (jb * BS < suffix_of(p.seq_lens[seq], false)) {
+            const int v = min(max(suffix_of(p.seq_lens[seq], false) - jb * BS, 0), BS);
+            if (v > 0) {
               id = p.block_table[static_cast<long long>(seq) * p.max_blocks + P + jb];
               if (id < 0 || id >= p.num_blocks) {
                 if (is_k) atomicOr(p.err, PA_DEVERR_BAD_BLOCK);
                 id = 0;
+              } else {
+                valid = v;
               }
             }
           }
-          // a slot no row reads loads block 0: its scores are masked and its
-          // V rows cleared before the P V MMAs
+          // a slot with no rows read copies only fill (zeros)
         }
       }
       return id;
     };
-    int next_ids = ntot > 0 ? load_ids(0) : 0;
+    int next_valid = BS;
+    int next_ids = ntot > 0 ? load_ids(0, next_valid) : 0;
     for (int t = 0; t < ntot; ++t, ++issued) {
       const int st = t % nst, n = sub_len(t);
-      const int ids = next_ids;
+      const int ids = next_ids, valids = next_valid;
       if (t >= nst &&
           !warp_wait_phase(smem_addr(&empty[st]), ((t / nst) - 1) & 1, abort_flag, p.err))
         break;
@@ -497,16 +509,17 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
       if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n) * 256u);
       for (int j = 0; j < n / BS; ++j) {
         const int phys = __shfl_sync(0xffffffffu, ids, j);
+        const int y0 = __shfl_sync(0xffffffffu, valids, j) - BS;  // 0 but in suffix slots
         if (lane == 0) {
 #pragma unroll
           for (int sb = 0; sb < BS / 16; ++sb) {
             const uint32_t off = static_cast<uint32_t>(j * BS + sb * 16) * 128u;
-            tma_load_4d(dst + off, map, 0, sb * 16, kvh, phys, bar);
-            tma_load_4d(dst + HALF + off, map, 64, sb * 16, kvh, phys, bar);
+            tma_load_4d(dst + off, map, 0, y0 + sb * 16, kvh, phys, bar);
+            tma_load_4d(dst + HALF + off, map, 64, y0 + sb * 16, kvh, phys, bar);
           }
         }
       }
-      if (t + 1 < ntot) next_ids = load_ids(t + 1);
+      if (t + 1 < ntot) next_ids = load_ids(t + 1, next_valid);
       __syncwarp();
     }
     if (*abort_flag) {
@@ -548,35 +561,10 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
     }
   } else if (warp == kPfxWarpPV) {
     // ---- PV issuer: O += P_t V_t, O in TMEM for the whole chunk ----
-    // suffix lengths of the slice's sequences, lane q for sequence q (a slice
-    // has at most 16), for the suffix sub-chunks' V rows
-    int my_suf = 0;
-    if (FUSED && lane < slice_n) my_suf = suffix_of(p.seq_lens[slice_s0 + lane], false);
     for (int t = 0; t < ntot; ++t) {
       const int st = t % NV, b = t & 1;
       if (!warp_wait_phase(smem_addr(&p_full[b]), (t >> 1) & 1, abort_flag, p.err)) break;
       if (!warp_wait_phase(smem_addr(&v_full[st]), (t / NV) & 1, abort_flag, p.err)) break;
-      if (FUSED && t >= nsub) {
-        // V rows of a suffix sub-chunk that no row attends (past a sequence's
-        // length, or past the slice) may hold anything, NaN included, and
-        // 0 * NaN would reach O: clear them
-        unsigned char* vt = v_s + st * kPfxTile;
-#pragma unroll 1
-        for (int rho = lane; rho < kPfxTok; rho += 32) {
-          const int q = (t - nsub) * QPS + rho / Wd;
-          const int sq = __shfl_sync(0xffffffffu, my_suf, q & 31);
-          if (q >= slice_n || rho % Wd >= sq) {
-            const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              *reinterpret_cast<uint4*>(vt + rho * 128 + i * 16) = z;
-              *reinterpret_cast<uint4*>(vt + HALF + rho * 128 + i * 16) = z;
-            }
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
       tc_fence_after();
       if (lane == 0) {
         const uint32_t vb = smem_addr(v_s + st * kPfxTile);
@@ -617,12 +605,18 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
       }
     }
     float m = -INFINITY, l = 0.f;
-    bool ok = true;
+    bool ok = true, arrived = false;
     for (int t = 0; t < ntot; ++t) {
       const int n = sub_len(t), b = t & 1;
       if (!warp_wait_phase(smem_addr(&s_full[b]), (t >> 1) & 1, abort_flag, p.err)) {
         ok = false;
         break;
+      }
+      if (FUSED && t == ntot - 1) {
+        // this CTA's last S MMAs have completed: its Q and K tiles are free
+        // for the rows the cluster sends it (see below)
+        cluster_arrive();
+        arrived = true;
       }
       tc_fence_after();
       const uint32_t sa = lane_base + b * kPfxTok;
@@ -638,13 +632,13 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
           if (i >= n) sv[i] = neutral;
       }
       if (FUSED && t >= nsub) {
-        // a suffix sub-chunk: this row's columns are its own sequence's
-        // suffix tokens [lo, lo + sfx_n); every other score becomes the
-        // neutral value, whose P is exactly 0 (qscale is not 0 here)
+        // a suffix sub-chunk: this row's columns are the last s of its own
+        // sequence's segment; every other score becomes the neutral value,
+        // whose P is exactly 0 (qscale is not 0 here)
         const int j = t - nsub;
         const bool mine = sfx_q >= j * QPS && sfx_q < (j + 1) * QPS;
-        const int lo = mine ? (sfx_q - j * QPS) * W : 0;
-        const int hi = mine ? lo + suffix_of(sfx_len, (blockIdx.x * kPfxRows + r) % G == 0) : 0;
+        const int hi = mine ? (sfx_q - j * QPS + 1) * W : 0;
+        const int lo = mine ? hi - suffix_of(sfx_len, (blockIdx.x * kPfxRows + r) % G == 0) : 0;
 #pragma unroll
         for (int i = 0; i < kPfxTok; ++i)
           if (i < lo || i >= hi) sv[i] = neutral;
@@ -717,68 +711,109 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
     }
     // a table with no columns past the prefix: each length must be the prefix's
     if (FUSED && W == 0 && sfx_q >= 0) suffix_of(sfx_len, (blockIdx.x * kPfxRows + r) % G == 0);
+    if (FUSED && !arrived) cluster_arrive();
     // O (relative to m) once every P V MMA has completed: the PV issuer's
     // final commit (o_done cannot tell: up to two of its phases may still be
-    // open here). Every MMA has then completed, so the K tiles are free: each
-    // warp stages its rows there (16.5 KB, rows padded to 132 floats against
-    // bank conflicts)
+    // open here)
     if (ok && ntot > 0) {
       ok = warp_wait_phase(smem_addr(&mma_done[1]), 0, abort_flag, p.err);
       if (ok) tc_fence_after();
     }
     constexpr int kPad = D + 4;
-    float* stage = reinterpret_cast<float*>(k_s) + warp * 32 * kPad;
-#pragma unroll 1
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      float v[32];
-      if (ok && ntot > 0) {
-        tmem_ld32(o_tm + c0, v);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < 32; i += 4)
-        *reinterpret_cast<float4*>(stage + lane * kPad + c0 + i) =
-            make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-    }
     if constexpr (FUSED) {
-      // the cluster merges the rows from here (see the end of the kernel);
-      // bulk copies read them, so the writes are ordered for that proxy
-      stage[lane * kPad + D] = m;
-      stage[lane * kPad + D + 1] = l;
+      // The row's partial, staged in this CTA's V tiles (free: every P V MMA
+      // has completed) as kXRow bytes: the accumulator divided by the sum as
+      // fp16 (within the range of the V values it averages), then max and
+      // sum; the warp then copies its rows of each other CTA's slice into
+      // that CTA's Q and K tiles, free once every CTA has arrived above.
+      unsigned char* srow = v_s + r * kXRow;
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float v[32];
+        if (ok && ntot > 0) {
+          tmem_ld32(o_tm + c0, v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; i += 8)
+          *reinterpret_cast<uint4*>(srow + 2 * (c0 + i)) =
+              make_uint4(pack_half2(v[i] * inv_l, v[i + 1] * inv_l),
+                         pack_half2(v[i + 2] * inv_l, v[i + 3] * inv_l),
+                         pack_half2(v[i + 4] * inv_l, v[i + 5] * inv_l),
+                         pack_half2(v[i + 6] * inv_l, v[i + 7] * inv_l));
+      }
+      *reinterpret_cast<float2*>(srow + 2 * D) = make_float2(m, l);
       fence_proxy_async_smem();
-    }
-    __syncwarp();
-    const int row = blockIdx.x * kPfxRows + r, seq = row / G, gg = row % G;
-    const bool write = !FUSED && ok && !*abort_flag;
-    if (seq < S && write) {
-      float* rec = p.records + ((static_cast<long long>(c) * S + seq) * p.num_kv_heads + kvh) * RS;
-      rec[G * D + 2 * gg] = m;
-      rec[G * D + 2 * gg + 1] = l;
-    }
-    if (write) {
-      // the warp's rows 32w .. 32w+31 belong to sequences row / G; a record's
-      // G rows are contiguous ([G][D] floats)
-      const int row0 = blockIdx.x * kPfxRows + warp * 32;
-      for (int e = lane; e < 32 * (D / 4); e += 32) {
-        const int rr = e / (D / 4), i4 = e % (D / 4);
-        const int rw = row0 + rr, sq = rw / G, g2 = rw % G;
-        if (sq < S) {
-          float* rec =
-              p.records + ((static_cast<long long>(c) * S + sq) * p.num_kv_heads + kvh) * RS;
-          *reinterpret_cast<float4*>(rec + g2 * D + 4 * i4) =
-              *reinterpret_cast<const float4*>(stage + rr * kPad + 4 * i4);
+      __syncwarp();
+      cluster_wait();
+      if (lane == 0) {
+        // rows 32 * warp .. + 31 split by the slice they belong to
+        const int C = static_cast<int>(gridDim.z);
+        for (int k = (warp * 32) / rpc; k <= (warp * 32 + 31) / rpc && k < C; ++k) {
+          if (k == c) continue;
+          const int r0 = max(warp * 32, k * rpc), r1 = min(warp * 32 + 32, (k + 1) * rpc);
+          bulk_copy_s2cluster(
+              cluster_map(smem_addr(q_s) + static_cast<uint32_t>((c * rpc + r0 - k * rpc) * kXRow),
+                          k),
+              smem_addr(v_s) + static_cast<uint32_t>(r0 * kXRow),
+              static_cast<uint32_t>((r1 - r0) * kXRow), cluster_map(smem_addr(recv_bar), k));
+        }
+      }
+    } else {
+      // Every MMA has completed, so the K tiles are free: each warp stages its
+      // rows there (16.5 KB, rows padded to 132 floats against bank
+      // conflicts) and writes each sequence's G rows as one contiguous run
+      float* stage = reinterpret_cast<float*>(k_s) + warp * 32 * kPad;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float v[32];
+        if (ok && ntot > 0) {
+          tmem_ld32(o_tm + c0, v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<float4*>(stage + lane * kPad + c0 + i) =
+              make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+      }
+      __syncwarp();
+      const int row = blockIdx.x * kPfxRows + r, seq = row / G, gg = row % G;
+      const bool write = ok && !*abort_flag;
+      if (seq < S && write) {
+        float* rec =
+            p.records + ((static_cast<long long>(c) * S + seq) * p.num_kv_heads + kvh) * RS;
+        rec[G * D + 2 * gg] = m;
+        rec[G * D + 2 * gg + 1] = l;
+      }
+      if (write) {
+        // the warp's rows 32w .. 32w+31 belong to sequences row / G; a
+        // record's G rows are contiguous ([G][D] floats)
+        const int row0 = blockIdx.x * kPfxRows + warp * 32;
+        for (int e = lane; e < 32 * (D / 4); e += 32) {
+          const int rr = e / (D / 4), i4 = e % (D / 4);
+          const int rw = row0 + rr, sq = rw / G, g2 = rw % G;
+          if (sq < S) {
+            float* rec =
+                p.records + ((static_cast<long long>(c) * S + sq) * p.num_kv_heads + kvh) * RS;
+            *reinterpret_cast<float4*>(rec + g2 * D + 4 * i4) =
+                *reinterpret_cast<const float4*>(stage + rr * kPad + 4 * i4);
+          }
         }
       }
     }
   }
   // Fused mode: every thread of every CTA of the cluster (the chunks of this
-  // row tile and KV head) arrives here, whatever happened before, once its
-  // part is done: the softmax warps after staging their rows, when this
-  // CTA's P V MMAs have completed and its V tiles (where the other CTAs'
-  // partials will land) are free; the other warps after their loops.
-  if constexpr (FUSED) cluster_arrive();
+  // row tile and KV head) arrives once on the barrier the softmax warps wait
+  // for before sending rows, whatever happened before: the softmax warps
+  // when their last S has been read, the other warps after their loops.
+  if constexpr (FUSED) {
+    if (warp >= kPfxSoftmaxWarps) cluster_arrive();
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == kPfxWarpS) {
@@ -788,12 +823,11 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
                  : "memory");
   }
   if constexpr (FUSED) {
-    cluster_wait();
-    fused_merge<G>(p, reinterpret_cast<const float*>(k_s), reinterpret_cast<float*>(v_s),
-                   recv_bar, kvh, c);
-    // the barrier fused_merge arrived on: every CTA's partials have landed
-    // where they were sent, so no copy out of this CTA's shared memory is
-    // still running when it leaves
+    if (warp >= kPfxSoftmaxWarps) cluster_wait();
+    fused_merge<G>(p, v_s, q_s, recv_bar, kvh, c);
+    // the barrier fused_merge arrived on: every CTA's rows have landed where
+    // they were sent, so no copy out of a CTA's shared memory is still
+    // running when it leaves
     cluster_wait();
   }
 }
