@@ -462,16 +462,12 @@ def time_planned(args, b, fp8, dev, stream, flush, world, steps):
     run.out = out_h
     esize = 1 if fp8 is not None else 2
     per_tok = b.num_kv_heads * b.head_dim * esize * 2
-    native = fp8 is None
-    if native:
-        run.prepare_native_steps(stream)
+    # pa_decode_step / pa_decode_step_fp8: plan, copies, append, attention in
+    # one library call per step
+    run.prepare_native_steps(stream)
 
     def one():
-        if native:      # pa_decode_step: plan, copies, append, attention in one call
-            plan = run.run_native_step()
-        else:
-            plan = run.plan_step_host()
-            run.run_step()
+        plan = run.run_native_step()
         return int(plan.seq_lens.astype(np.int64).sum())
 
     for _ in range(args.warmup):
@@ -514,8 +510,8 @@ def time_planned(args, b, fp8, dev, stream, flush, world, steps):
     assert pa.pa_device_error() == 0
     d2h = out_h.numel() * out_h.element_size()
     return {
-        "call": "pa_decode_step (one library call per step)" if native else
-                "pa_alloc_plan_step, then the kernel calls through the Python binding",
+        "call": ("pa_decode_step_fp8" if fp8 is not None else "pa_decode_step")
+                + " (one library call per step)",
         "value": round(serial_gbs, 2), "unit": "GB/s", "steps": steps,
         "ms_per_step": round(1e3 * t_serial / steps, 5),
         "host_plan_and_launch_us_per_step": round(1e6 * host_s / steps, 2),

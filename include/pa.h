@@ -519,6 +519,22 @@ PA_API pa_status pa_decode_step(pa_allocator* a, const int64_t* seq_ids, int num
                          void* workspace, size_t workspace_bytes, int partition_tokens,
                          pa_stream_t stream);
 
+/* pa_decode_step over an E4M3 cache: the same plan, then pa_copy_blocks_fp8,
+ * pa_append_kv_fp8 (each new row quantized with the KV head's k_scale /
+ * v_scale, device fp32 [num_kv_heads]) and pa_decode_attention_fp8 on
+ * `stream`; arguments and plan buffers as for pa_decode_step, pools of
+ * one-byte codes ("Phase 7 · Document 04 — PagedAttention", §11: the fp8
+ * KV cache). Errors: those of the four calls, as for pa_decode_step. */
+PA_API pa_status pa_decode_step_fp8(pa_allocator* a, const int64_t* seq_ids, int num_seqs,
+                             int max_blocks, int32_t* slot_mapping, int32_t* cow_pairs,
+                             int32_t* block_table, int32_t* seq_lens, int* num_cow,
+                             const pa_half* q, const pa_half* k_new, const pa_half* v_new,
+                             uint8_t* k_pool, uint8_t* v_pool, const float* k_scale,
+                             const float* v_scale, int num_q_heads, int num_kv_heads,
+                             int head_dim, int num_blocks, int64_t pool_block_stride,
+                             float scale, pa_half* out, void* workspace,
+                             size_t workspace_bytes, int partition_tokens, pa_stream_t stream);
+
 /* Dense tables for a batch: table host int32 [n][max_blocks] (rows padded
  * with `fill`), seq_lens host int32 [n] = current lengths. */
 PA_API pa_status pa_alloc_build_tables(const pa_allocator* a, const int64_t* seq_ids,

@@ -455,8 +455,14 @@ class PreparedDecodeStep:
     copy-on-write pairs it planned."""
 
     def __init__(self, alloc, seq_ids, max_blocks, plan, q, k_new, v_new, k_pool, v_pool, scale,
-                 out, workspace, partition_tokens: int = 0, stream=None):
+                 out, workspace, partition_tokens: int = 0, stream=None, k_scale=None,
+                 v_scale=None):
+        """With uint8 pools (E4M3 codes) and device fp32 k_scale / v_scale
+        [num_kv_heads] the step is pa_decode_step_fp8."""
         torch = _torch()
+        fp8 = k_pool.dtype == torch.uint8
+        if fp8 and (k_scale is None or v_scale is None):
+            raise ValueError("an E4M3 cache needs k_scale and v_scale")
         nb, bs, hkv, d, stride = _pool_dims(k_pool, v_pool)
         if bs != alloc.block_size or nb != alloc.num_blocks:
             raise ValueError("the pools and the block manager differ in block size or blocks")
@@ -472,20 +478,28 @@ class PreparedDecodeStep:
             raise ValueError("q must be [num_seqs][num_q_heads][head_dim]")
         hq = int(q.shape[1])
         self.plan = plan
-        self._keep = (alloc, q, k_new, v_new, k_pool, v_pool, out, workspace)
+        self._keep = (alloc, q, k_new, v_new, k_pool, v_pool, out, workspace, k_scale, v_scale)
         self._ncow = ctypes.c_int()
         ids = self.seq_ids if n else np.zeros(1, np.int64)
         self._ids = ids
-        self._fn = _load().pa_decode_step
-        self._args = (alloc._h, ids.ctypes.data, n, max_blocks,
-                      ctypes.c_void_p(slots.data_ptr()), ctypes.c_void_p(pairs.data_ptr()),
-                      ctypes.c_void_p(table.data_ptr()), ctypes.c_void_p(lens.data_ptr()),
-                      ctypes.byref(self._ncow), _in(q, "q", torch.float16),
-                      _in(k_new, "k_new", torch.float16), _in(v_new, "v_new", torch.float16),
-                      _pool(k_pool, "k_pool", torch.float16), _pool(v_pool, "v_pool", torch.float16),
-                      hq, hkv, d, nb, stride, ctypes.c_float(float(scale)), _out(out, q),
-                      _dev(workspace, "workspace", torch.uint8), workspace.numel(),
-                      partition_tokens, _stream_ptr(stream))
+        head = (alloc._h, ids.ctypes.data, n, max_blocks,
+                ctypes.c_void_p(slots.data_ptr()), ctypes.c_void_p(pairs.data_ptr()),
+                ctypes.c_void_p(table.data_ptr()), ctypes.c_void_p(lens.data_ptr()),
+                ctypes.byref(self._ncow), _in(q, "q", torch.float16),
+                _in(k_new, "k_new", torch.float16), _in(v_new, "v_new", torch.float16))
+        tail = (hq, hkv, d, nb, stride, ctypes.c_float(float(scale)), _out(out, q),
+                _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+                partition_tokens, _stream_ptr(stream))
+        if fp8:
+            self._fn = _load().pa_decode_step_fp8
+            self._args = head + (_pool(k_pool, "k_pool", torch.uint8),
+                                 _pool(v_pool, "v_pool", torch.uint8),
+                                 _dev(k_scale, "k_scale", torch.float32),
+                                 _dev(v_scale, "v_scale", torch.float32)) + tail
+        else:
+            self._fn = _load().pa_decode_step
+            self._args = head + (_pool(k_pool, "k_pool", torch.float16),
+                                 _pool(v_pool, "v_pool", torch.float16)) + tail
 
     def __call__(self) -> int:
         _check(self._fn(*self._args))

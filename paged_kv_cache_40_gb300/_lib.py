@@ -93,6 +93,9 @@ SIGNATURES = {
     "pa_decode_step": (_i32, [_vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _pint, _vp, _vp, _vp,
                               _vp, _vp, _i32, _i32, _i32, _i32, _i64, ctypes.c_float, _vp, _vp,
                               _sz, _i32, _vp]),
+    "pa_decode_step_fp8": (_i32, [_vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _pint, _vp, _vp,
+                                  _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64,
+                                  ctypes.c_float, _vp, _vp, _sz, _i32, _vp]),
     "pa_alloc_shared_prefix": (_i32, [_vp, _vp, _i32, _vp, _i32, _pint]),
     "pa_alloc_stats": (_i32, [_vp, ctypes.POINTER(AllocStats)]),
     "pa_alloc_export_state": (_i32, [_vp, _pi32, _pint, _pi32]),

@@ -231,12 +231,13 @@ class DecodeBatchRunner:
         buffers, so that run_native_step() plans and enqueues a whole step
         (copies, append, attention) in one library call."""
         from . import PreparedDecodeStep
-        if self.kv_dtype != "fp16":
-            raise ValueError("the one-call step serves fp16 caches")
+        fp8 = self.kv_dtype == "fp8"
         self._native = [PreparedDecodeStep(self.alloc, self._plan_ids, self.max_blocks, st,
                                            self.q, self.k_new, self.v_new, self.k_pool,
                                            self.v_pool, float(self.batch.scale), self.out,
-                                           self.workspace, self.partition_tokens, stream)
+                                           self.workspace, self.partition_tokens, stream,
+                                           k_scale=self.k_scale if fp8 else None,
+                                           v_scale=self.v_scale if fp8 else None)
                         for st in self._plan_sets]
 
     def run_native_step(self) -> StepPlan:

@@ -332,3 +332,57 @@ def test_one_call_steps_match_the_oracle(pa):
         exp = oracle.decode_attention(b.q, kp, vp, table, lens, b.scale)
         assert_close_attention(run.out.cpu().numpy(), exp, f"one-call step {k}")
     assert copies >= 1
+
+
+def test_one_call_fp8_steps_match_the_oracle(pa):
+    """pa_decode_step_fp8 over steps of a batch with a forked sequence: the
+    plans, the E4M3 pools (bit-exact: copies, then each new row quantized with
+    its KV head's scale) and the outputs against the oracle."""
+    from paged_kv_cache_40_gb300.engine import DecodeBatchRunner
+    rng = np.random.default_rng(23)
+    lens0 = rng.integers(14, 40, size=5, endpoint=True)
+    lens0[2] = 37                       # a partial last block: the fork's first append copies
+    steps = 10
+    nb = sum(-(-(int(L) + steps + 1) // 16) for L in lens0) * 2 + 8
+    b = synthetic.make_batch("one-call-fp8", rng, lens0, 16, 4, 128, 16, nb, seed=23)
+    c = synthetic.fp8_cache(b, seed=24)
+    mb = max(-(-(int(L) + steps + 1) // 16) for L in lens0) + 1
+    run = DecodeBatchRunner(b, max_blocks=mb, kv_dtype="fp8", k_pool=c.k_pool, v_pool=c.v_pool,
+                            k_scale=c.k_scale, v_scale=c.v_scale)
+    ref = oracle.BlockAllocator(b.num_blocks, b.block_size, b.free_order)
+    for i, L in enumerate(b.prefill_lens):
+        ref.add_seq(i, int(L))
+    run.alloc.free_seq(4)
+    run.alloc.fork(2, 4)
+    ref.free_seq(4)
+    ref.fork(2, 4)
+    run.host_planned(sets=2)
+    run.prepare_native_steps()
+    kp, vp = c.k_pool.copy(), c.v_pool.copy()
+    ids = list(range(b.num_seqs))
+    copies = 0
+    for k in range(steps):
+        plan = run.run_native_step()
+        slots, pairs = [], []
+        for s_ in ids:
+            sl, cs, cd = ref.append_slot(s_)
+            slots.append(sl)
+            if cs >= 0:
+                pairs.append((cs, cd))
+        table = np.asarray(ref.dense_table(ids, mb), np.int32)
+        lens = np.asarray([ref.seq_len(s_) for s_ in ids], np.int32)
+        torch.cuda.synchronize()
+        assert pa.pa_device_error() == 0
+        assert plan.slots.tolist() == slots and plan.cow_pairs.tolist() == [list(p) for p in pairs]
+        assert plan.block_table.tolist() == table.tolist()
+        assert plan.seq_lens.tolist() == lens.tolist()
+        copies += len(pairs)
+        if pairs:
+            kp, vp = oracle.copy_blocks(kp, vp, np.asarray(pairs, np.int32))
+        kp, vp = oracle.append_kv_fp8(kp, vp, b.k_new, b.v_new, np.asarray(slots, np.int32),
+                                      c.k_scale, c.v_scale)
+        assert np.array_equal(run.k_pool.cpu().numpy(), kp)
+        assert np.array_equal(run.v_pool.cpu().numpy(), vp)
+        exp = oracle.decode_attention_fp8(b.q, kp, vp, c.k_scale, c.v_scale, table, lens, b.scale)
+        assert_close_attention(run.out.cpu().numpy(), exp, f"one-call fp8 step {k}")
+    assert copies >= 1
