@@ -21,6 +21,7 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <utility>
 
 #include "pa_internal.h"
 
@@ -29,6 +30,25 @@
 __device__ int32_t g_pa_device_error = 0;
 
 namespace {
+
+// Launch `kernel` on `stream` as a programmatic dependent of the kernel
+// ahead of it: its CTAs may be scheduled while that one finishes, and wait
+// (griddepcontrol.wait) before touching memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, int threads, cudaStream_t stream,
+                             Args&&... args) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = dim3(threads);
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&lc, kernel, std::forward<Args>(args)...);
+  return e == cudaSuccess ? cudaGetLastError() : e;
+}
 
 constexpr int kAppendThreads = 128;
 constexpr int kCopyThreads = 256;
@@ -42,8 +62,11 @@ append_kv_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_ne
                  const int32_t* __restrict__ slots, int row_vecs, int block_size,
                  int64_t block_vecs, int64_t num_slots, int32_t* __restrict__ err) {
   // A decode launched right after this kernel may start its prologue now; it
-  // waits for this grid to finish before it reads the pool.
+  // waits for this grid to finish before it reads the pool. This kernel is
+  // itself launched as a programmatic dependent (of the copy-on-write copies,
+  // say): it reads nothing before the kernel ahead of it has completed.
   asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = blockIdx.x;
   const int32_t slot = __ldg(slots + t);
   if (slot < 0) return;
@@ -84,6 +107,7 @@ append_kv_fp8_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ 
                      int block_size, int64_t block_vecs, int64_t num_slots,
                      int32_t* __restrict__ err) {
   asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = blockIdx.x;
   const int32_t slot = __ldg(slots + t);
   if (slot < 0) return;
@@ -130,6 +154,11 @@ copy_blocks_kernel(const uint4* __restrict__ src_k, const uint4* __restrict__ sr
                    const int32_t* __restrict__ pairs, int64_t block_vecs, int64_t src_stride,
                    int64_t dst_stride, int src_blocks, int dst_blocks,
                    int32_t* __restrict__ err) {
+  // the append that follows may launch now; it waits for this grid before it
+  // writes. Launched as a programmatic dependent itself, this kernel touches
+  // nothing before the kernel ahead of it has completed.
+  asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int p = blockIdx.x;
   const int32_t src = __ldg(pairs + 2 * p);
   const int32_t dst = __ldg(pairs + 2 * p + 1);
@@ -307,11 +336,11 @@ pa_status pa_append_kv(const pa_half* k_new, const pa_half* v_new, pa_half* k_po
     }
   }
   const int row_vecs = num_kv_heads * head_dim / 8;
-  append_kv_kernel<<<num_tokens, kAppendThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+  cudaError_t e = launch_dependent(
+      append_kv_kernel, dim3(num_tokens), kAppendThreads, static_cast<cudaStream_t>(stream),
       reinterpret_cast<const uint4*>(k_new), reinterpret_cast<const uint4*>(v_new),
       reinterpret_cast<uint4*>(k_pool), reinterpret_cast<uint4*>(v_pool), slot_mapping,
       row_vecs, block_size, stride / 8, static_cast<int64_t>(num_blocks) * block_size, err);
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_append_kv launch");
   pa::count_launch();
   return pa::ok();
@@ -345,11 +374,11 @@ pa_status pa_copy_blocks(pa_half* k_pool, pa_half* v_pool, const int32_t* pairs,
   const int64_t slices = (block_vecs + slice - 1) / slice;
   if (slices > 65535) return pa::fail(PA_ERR_UNSUPPORTED, "pa_copy_blocks: block too large");
   dim3 grid(num_pairs, static_cast<unsigned>(slices));
-  copy_blocks_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+  cudaError_t e = launch_dependent(
+      copy_blocks_kernel, grid, kCopyThreads, static_cast<cudaStream_t>(stream),
       reinterpret_cast<const uint4*>(k_pool), reinterpret_cast<const uint4*>(v_pool),
       reinterpret_cast<uint4*>(k_pool), reinterpret_cast<uint4*>(v_pool), pairs, block_vecs,
       stride / 8, stride / 8, num_blocks, num_blocks, err);
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_copy_blocks launch");
   pa::count_launch();
   return pa::ok();
@@ -398,12 +427,12 @@ pa_status pa_append_kv_fp8(const pa_half* k_new, const pa_half* v_new, uint8_t* 
     }
   }
   const int row_vecs = num_kv_heads * head_dim / 8;
-  append_kv_fp8_kernel<<<num_tokens, kAppendThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+  cudaError_t e = launch_dependent(
+      append_kv_fp8_kernel, dim3(num_tokens), kAppendThreads, static_cast<cudaStream_t>(stream),
       reinterpret_cast<const uint4*>(k_new), reinterpret_cast<const uint4*>(v_new),
       reinterpret_cast<uint2*>(k_pool), reinterpret_cast<uint2*>(v_pool), slot_mapping, k_scale,
       v_scale, row_vecs, head_dim / 8, block_size, stride / 8,
       static_cast<int64_t>(num_blocks) * block_size, err);
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_append_kv_fp8 launch");
   pa::count_launch();
   return pa::ok();
@@ -440,11 +469,11 @@ pa_status pa_copy_blocks_fp8(uint8_t* k_pool, uint8_t* v_pool, const int32_t* pa
   const int64_t slices = (block_vecs + slice - 1) / slice;
   if (slices > 65535) return pa::fail(PA_ERR_UNSUPPORTED, "pa_copy_blocks_fp8: block too large");
   dim3 grid(num_pairs, static_cast<unsigned>(slices));
-  copy_blocks_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+  cudaError_t e = launch_dependent(
+      copy_blocks_kernel, grid, kCopyThreads, static_cast<cudaStream_t>(stream),
       reinterpret_cast<const uint4*>(k_pool), reinterpret_cast<const uint4*>(v_pool),
       reinterpret_cast<uint4*>(k_pool), reinterpret_cast<uint4*>(v_pool), pairs, block_vecs,
       stride / 16, stride / 16, num_blocks, num_blocks, err);
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "pa_copy_blocks_fp8 launch");
   pa::count_launch();
   return pa::ok();
