@@ -618,14 +618,15 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     w0 = time.perf_counter()
     launches0 = pa.pa_kernel_launches()
-    # the step as a caller issues it: nothing between the append and the
-    # attention kernel, which is launched as a programmatic dependent and so
-    # may start its prologue while the append runs
+    # the step as a caller issues it (DecodeBatchRunner.step): the copies if
+    # any, then for an fp16 cache one kernel that appends the new rows and
+    # attends (pa_decode_append_attention); for an E4M3 cache the append,
+    # then the attention kernel as a programmatic dependent of it; for the
+    # shared-prefix workload the copies, the append and the prefix-aware call
     for k in range(K):
         flush()
         ev[k][0].record(stream)
-        run.copy_and_append()
-        run.attend()
+        run.step()
         ev[k][1].record(stream)
     launches = pa.pa_kernel_launches() - launches0
     torch.cuda.synchronize(dev)

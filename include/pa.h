@@ -376,6 +376,29 @@ PA_API pa_status pa_copy_blocks_fp8(uint8_t* k_pool, uint8_t* v_pool,
                                     int num_blocks, int64_t pool_block_stride,
                                     pa_stream_t stream);
 
+/* pa_append_kv then pa_decode_attention in one kernel, for one new token per
+ * sequence (k_new/v_new row i belongs to sequence i): the step the pages'
+ * decode loop takes ("Phase 7 · Document 04 — PagedAttention", §2: the
+ * cache grows one token per step, then attention reads it through the
+ * table). slot_mapping[i] must be the row of sequence i's last token
+ * (position seq_lens[i] - 1 of its table), as the block manager assigns it;
+ * the kernel writes the new K/V row there just before it copies that block,
+ * so the attention includes it. A negative slot writes nothing (the row
+ * already in the pool is attended); any other slot that is not that row is
+ * not written and sets PA_DEVERR_BAD_SLOT. seq_lens count the new token.
+ * Other arguments, layouts, the workspace and the errors are those of
+ * pa_append_kv and pa_decode_attention (fp16 pools, K and V pools
+ * disjoint). */
+PA_API pa_status pa_decode_append_attention(const pa_half* q, const pa_half* k_new,
+                                     const pa_half* v_new, const int32_t* slot_mapping,
+                                     pa_half* k_pool, pa_half* v_pool,
+                                     const int32_t* block_table, const int32_t* seq_lens,
+                                     int num_seqs, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int block_size, int max_blocks_per_seq,
+                                     int num_blocks, int64_t pool_block_stride, float scale,
+                                     pa_half* out, void* workspace, size_t workspace_bytes,
+                                     int partition_tokens, pa_stream_t stream);
+
 /* pa_decode_attention over E4M3 pools: out[i][h] = sum_t softmax_t(scale *
  * q[i][h] . Kd[t]) Vd[t] with Kd, Vd the dequantized rows (code value times
  * the KV head's scale), computed in fp32 and rounded once to fp16. q, out,
@@ -495,8 +518,9 @@ PA_API pa_status pa_alloc_plan_step(pa_allocator* a, const int64_t* seq_ids, int
 
 /* One decode step in one call: pa_alloc_plan_step for the batch seq_ids
  * (tables padded with -1), then, on `stream`, pa_copy_blocks of its
- * copy-on-write pairs (if any), pa_append_kv of every sequence's new K/V row
- * and pa_decode_attention over the tables and lengths just planned ("Phase 7
+ * copy-on-write pairs (if any) and pa_decode_append_attention (every
+ * sequence's new K/V row, then attention over the tables and lengths just
+ * planned, in one kernel) ("Phase 7
  * · Document 04 — PagedAttention", §2 on-demand allocation and block
  * sharing; lux-666 notes "PagedAttention", 最小模型). The plan is written
  * into slot_mapping [n], cow_pairs [n][2] (*num_cow rows), block_table

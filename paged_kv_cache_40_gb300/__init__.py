@@ -39,7 +39,7 @@ from ._lib import (  # noqa: F401
 )
 
 __all__ = [
-    "pa_append_kv", "pa_copy_blocks", "pa_decode_attention",
+    "pa_append_kv", "pa_copy_blocks", "pa_decode_attention", "pa_decode_append_attention",
     "pa_decode_workspace_bytes", "pa_decode_workspace_init", "pa_device_error",
     "pa_append_kv_fp8", "pa_copy_blocks_fp8", "pa_decode_attention_fp8",
     "pa_decode_attention_shared_prefix", "pa_decode_shared_prefix_workspace_bytes",
@@ -246,6 +246,43 @@ def pa_decode_attention(q, k_pool, v_pool, block_table, seq_lens, scale, out=Non
         *args, S, hq, hkv, d, bs, mb, nb, stride, ctypes.c_float(float(scale)),
         _out(out, q), _dev(workspace, "workspace", torch.uint8),
         workspace.numel(), partition_tokens, _stream_ptr(stream)))
+    return out
+
+
+def pa_decode_append_attention(q, k_new, v_new, slot_mapping, k_pool, v_pool, block_table,
+                               seq_lens, scale, out=None, workspace=None,
+                               partition_tokens: int = 0, stream=None):
+    """pa_append_kv then pa_decode_attention in one kernel, one new token per
+    sequence (k_new/v_new [S][Hkv][D] fp16, row i for sequence i;
+    slot_mapping int32 [S], the row of each sequence's last token). The
+    other arguments are pa_decode_attention's. Returns out."""
+    torch = _torch()
+    nb, bs, hkv, d, stride = _pool_dims(k_pool, v_pool)
+    if q.dim() != 3 or int(q.shape[2]) != d:
+        raise ValueError("q must be [num_seqs][num_q_heads][head_dim]")
+    S, hq = int(q.shape[0]), int(q.shape[1])
+    for t, name in ((k_new, "k_new"), (v_new, "v_new")):
+        if tuple(t.shape) != (S, hkv, d):
+            raise ValueError(f"{name} must be [num_seqs][num_kv_heads][head_dim]")
+    if tuple(slot_mapping.shape) != (S,):
+        raise ValueError("slot_mapping must be [num_seqs]")
+    if block_table.dim() != 2 or int(block_table.shape[0]) != S:
+        raise ValueError("block_table must be [num_seqs][max_blocks_per_seq]")
+    mb = int(block_table.shape[1])
+    if tuple(seq_lens.shape) != (S,):
+        raise ValueError("seq_lens must be [num_seqs]")
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float16, device=k_pool.device)
+    if workspace is None:
+        workspace = alloc_workspace(S, hq, hkv, d, bs, mb, partition_tokens, k_pool.device)
+    _check(_load().pa_decode_append_attention(
+        _in(q, "q", torch.float16), _in(k_new, "k_new", torch.float16),
+        _in(v_new, "v_new", torch.float16), _in(slot_mapping, "slot_mapping", torch.int32),
+        _pool(k_pool, "k_pool", torch.float16), _pool(v_pool, "v_pool", torch.float16),
+        _in(block_table, "block_table", torch.int32), _in(seq_lens, "seq_lens", torch.int32),
+        S, hq, hkv, d, bs, mb, nb, stride, ctypes.c_float(float(scale)), _out(out, q),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), partition_tokens,
+        _stream_ptr(stream)))
     return out
 
 

@@ -66,6 +66,9 @@ SIGNATURES = {
     "pa_decode_workspace_init": (_i32, [_vp, _sz, _i32, _i32, _vp]),
     "pa_decode_attention": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                    _i32, _i32, _i64, _f32, _vp, _vp, _sz, _i32, _vp]),
+    "pa_decode_append_attention": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32,
+                                          _i32, _i32, _i32, _i32, _i32, _i64, _f32, _vp, _vp,
+                                          _sz, _i32, _vp]),
     "pa_decode_attention_fixed_scratch": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                                  _i32, _i32, _i32, _i64, _f32, _vp, _i32, _vp]),
     "pa_append_kv_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,

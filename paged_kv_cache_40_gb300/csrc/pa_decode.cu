@@ -162,6 +162,14 @@ struct DecodeParams {
   float qscale;    // scale * log2(e)
   unsigned long long wait_ns;    // time limit of the pipeline waits
   long long block_stride_bytes;  // host only: the pools' block stride, for their tensor maps
+  // append mode (fp16 pools, not shared-prefix mode): each sequence's new K/V
+  // row (k_new/v_new [num_seqs][num_kv_heads][D]) goes to slot_mapping[seq],
+  // which must be the row of its last token; the producer writes it just
+  // before it copies that block, so the attention sees it
+  const __half* k_new;
+  const __half* v_new;
+  const int32_t* slot_mapping;
+  long long block_stride;        // values from one pool block to the next
 };
 
 __device__ __forceinline__ int clamp_len(int L, int cap, int32_t* err) {
@@ -610,6 +618,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     uint32_t g_iss = 0, pc_iss = 0;
     int j0 = 0;
     int phys_cur = 0, len_cur = 0;
+    // append mode: the current piece's appended row (its head group's part)
+    // when the piece holds its segment's last block a_blk
+    constexpr int kAV = (kMaxHG * D / 8 + 31) / 32;  // 16-byte vectors per lane
+    uint4 ak[kAV], av[kAV];
+    int a_blk = -1, a_slot = -1;
     if (have) {
       len_cur = min(max(lraw_first - loff, 0), cap);
       phys_cur = lane < min(32, P.n)
@@ -646,6 +659,30 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           pc_iss = pc + 1;
           __syncwarp();
         }
+        if constexpr (!KV8 && !PFX) {
+          // append mode: the new row of the piece's sequence is loaded now,
+          // used when its block's copy is issued
+          a_blk = -1;
+          if (p.k_new != nullptr && len_cur > 0) {
+            const int lb = (len_cur - 1) / BS;
+            if (lb >= P.cur.j && lb < P.cur.j + P.n) {
+              a_blk = lb;
+              a_slot = __ldg(p.slot_mapping + P.cur.seq);
+              const long long src =
+                  (static_cast<long long>(P.cur.seq) * p.num_kv_heads + P.cur.hg * HG) * (D / 8);
+              const uint4* kn = reinterpret_cast<const uint4*>(p.k_new) + src;
+              const uint4* vn = reinterpret_cast<const uint4*>(p.v_new) + src;
+#pragma unroll
+              for (int i = 0; i < kAV; ++i) {
+                const int idx = lane + 32 * i;
+                if (idx < HG * D / 8) {
+                  ak[i] = __ldg(kn + idx);
+                  av[i] = __ldg(vn + idx);
+                }
+              }
+            }
+          }
+        }
       }
       const int nn = min(32, P.n - j0);
       // table entries (and raw length) of the next group
@@ -667,6 +704,34 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         const int vb = min(BS, len_cur - blk * BS);  // valid rows of the block (>= 1)
         const int nsb = (vb + TS - 1) / TS;           // stages that hold valid rows
         const bool bad = phys < 0 || phys >= p.num_blocks;
+        if constexpr (!KV8 && !PFX) {
+          if (blk == a_blk) {
+            // append mode: the sequence's new row (its last token) is written
+            // into this block before any of its copies is issued; a slot
+            // that is not that row is refused
+            const int row = (len_cur - 1) % BS;
+            const bool ok_slot = !bad && a_slot == phys * BS + row;
+            if (a_slot >= 0 && !ok_slot && lane == 0) atomicOr(p.err, PA_DEVERR_BAD_SLOT);
+            if (ok_slot) {
+              const long long off =
+                  static_cast<long long>(phys) * p.block_stride +
+                  (static_cast<long long>(row) * p.num_kv_heads + P.cur.hg * HG) * D;
+              uint4* kd = reinterpret_cast<uint4*>(const_cast<__half*>(p.k_pool) + off);
+              uint4* vd = reinterpret_cast<uint4*>(const_cast<__half*>(p.v_pool) + off);
+#pragma unroll
+              for (int i = 0; i < kAV; ++i) {
+                const int idx = lane + 32 * i;
+                if (idx < HG * D / 8) {
+                  kd[idx] = ak[i];
+                  vd[idx] = av[i];
+                }
+              }
+              // the block's copies (async proxy) read what was just written
+              asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
+            __syncwarp();
+          }
+        }
         for (int sb = 0; sb < nsb; ++sb, ++g) {
           const int stage = g % NST;
           const uint32_t use = g / NST;
@@ -1702,6 +1767,10 @@ static DecodeParams make_params(const pa_half* q, const pa_half* k_pool, const p
   prm.qscale = scale * kLog2e;
   prm.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   prm.block_stride_bytes = stride_bytes;
+  prm.k_new = nullptr;
+  prm.v_new = nullptr;
+  prm.slot_mapping = nullptr;
+  prm.block_stride = stride_bytes / 2;
   return prm;
 }
 
@@ -1742,6 +1811,68 @@ pa_status pa_decode_attention(const pa_half* q, const pa_half* k_pool, const pa_
                                  cap_blocks);
   prm.err = pa::device_error_word();
   if (!prm.err) return PA_ERR_CUDA;
+  const int G = num_q_heads / num_kv_heads;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  pa_status st = head_dim == 64 ? dispatch_bs<64>(block_size, G, prm, dev, s)
+                                : dispatch_bs<128>(block_size, G, prm, dev, s);
+  return st == PA_OK ? pa::ok() : st;
+}
+
+pa_status pa_decode_append_attention(const pa_half* q, const pa_half* k_new,
+                                     const pa_half* v_new, const int32_t* slot_mapping,
+                                     pa_half* k_pool, pa_half* v_pool,
+                                     const int32_t* block_table, const int32_t* seq_lens,
+                                     int num_seqs, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int block_size, int max_blocks_per_seq,
+                                     int num_blocks, int64_t pool_block_stride, float scale,
+                                     pa_half* out, void* workspace, size_t workspace_bytes,
+                                     int partition_tokens, pa_stream_t stream) {
+  const char* fn = "pa_decode_append_attention";
+  long long stride_bytes = 0;
+  if (pa_status s = check_decode_call(fn, q, k_pool, v_pool, block_table, seq_lens, num_seqs,
+                                      num_q_heads, num_kv_heads, head_dim, block_size,
+                                      max_blocks_per_seq, num_blocks, pool_block_stride, 2, scale,
+                                      out, partition_tokens, &stride_bytes))
+    return s;
+  if (num_seqs == 0) return pa::ok();
+  if (!k_new || !v_new || !slot_mapping)
+    return pa::fail(PA_ERR_INVALID_ARG, "%s: NULL k_new, v_new or slot_mapping", fn);
+  if (!pa::aligned16(k_new) || !pa::aligned16(v_new) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 3))
+    return pa::fail(PA_ERR_INVALID_ARG, "%s: misaligned k_new, v_new or slot_mapping", fn);
+  if (pa_status s = pa::check_pools_disjoint(
+          fn, k_pool, v_pool, num_blocks, stride_bytes,
+          static_cast<int64_t>(block_size) * num_kv_heads * head_dim * 2))
+    return s;
+  const pa_half* qd = q;
+  const int32_t* table = block_table;
+  const int32_t* lens = seq_lens;
+  pa_half* outd = out;
+  if (pa_status s = resolve_io(fn, qd, k_pool, v_pool, table, lens, outd)) return s;
+  if (pa_status s = pa::device_in("pa_decode_append_attention(k_new)", k_new)) return s;
+  if (pa_status s = pa::device_in("pa_decode_append_attention(v_new)", v_new)) return s;
+  if (pa_status s = pa::device_in("pa_decode_append_attention(slot_mapping)", slot_mapping))
+    return s;
+  if (!workspace) return pa::fail(PA_ERR_INVALID_ARG, "%s: NULL workspace", fn);
+  if (pa_status s = pa::device_only("pa_decode_append_attention(workspace)", workspace)) return s;
+  if (!pa::aligned16(workspace)) return pa::fail(PA_ERR_INVALID_ARG, "%s: misaligned workspace", fn);
+  const int cap_blocks = partition_tokens / block_size;
+  const Layout lay = workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                      max_blocks_per_seq, cap_blocks);
+  if (workspace_bytes < lay.total)
+    return pa::fail(PA_ERR_INVALID_ARG, "%s: workspace %zu < %zu bytes", fn, workspace_bytes,
+                    lay.total);
+  pa::DeviceInfo dev;
+  if (pa_status s = pa::current_device(&dev)) return s;
+  DecodeParams prm = make_params(qd, k_pool, v_pool, table, lens, num_seqs, num_q_heads,
+                                 num_kv_heads, max_blocks_per_seq, num_blocks, stride_bytes,
+                                 scale, outd, static_cast<unsigned char*>(workspace), lay,
+                                 cap_blocks);
+  prm.err = pa::device_error_word();
+  if (!prm.err) return PA_ERR_CUDA;
+  prm.k_new = reinterpret_cast<const __half*>(k_new);
+  prm.v_new = reinterpret_cast<const __half*>(v_new);
+  prm.slot_mapping = slot_mapping;
   const int G = num_q_heads / num_kv_heads;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   pa_status st = head_dim == 64 ? dispatch_bs<64>(block_size, G, prm, dev, s)

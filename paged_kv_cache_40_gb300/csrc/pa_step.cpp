@@ -32,13 +32,10 @@ pa_status pa_decode_step(pa_allocator* a, const int64_t* seq_ids, int num_seqs, 
                                      BS, num_blocks, pool_block_stride, stream))
       return s;
   }
-  if (pa_status s = pa_append_kv(k_new, v_new, k_pool, v_pool, slot_mapping, num_seqs,
-                                 num_kv_heads, head_dim, BS, num_blocks, pool_block_stride, stream))
-    return s;
-  return pa_decode_attention(q, k_pool, v_pool, block_table, seq_lens, num_seqs, num_q_heads,
-                             num_kv_heads, head_dim, BS, max_blocks, num_blocks,
-                             pool_block_stride, scale, out, workspace, workspace_bytes,
-                             partition_tokens, stream);
+  return pa_decode_append_attention(q, k_new, v_new, slot_mapping, k_pool, v_pool, block_table,
+                                    seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, BS,
+                                    max_blocks, num_blocks, pool_block_stride, scale, out,
+                                    workspace, workspace_bytes, partition_tokens, stream);
 }
 
 pa_status pa_decode_step_fp8(pa_allocator* a, const int64_t* seq_ids, int num_seqs,

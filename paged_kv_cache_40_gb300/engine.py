@@ -29,6 +29,7 @@ from typing import List, Optional, Tuple
 import numpy as np
 
 from . import (BlockAllocator, alloc_workspace, kv_block_pool, kv_views, pa_append_kv,
+               pa_decode_append_attention,
                pa_append_kv_fp8, pa_copy_blocks, pa_copy_blocks_fp8, pa_decode_attention,
                pa_decode_attention_fp8, pa_decode_attention_shared_prefix,
                pa_decode_shared_prefix_workspace_bytes, pa_kernel_launches)
@@ -142,6 +143,22 @@ class DecodeBatchRunner:
         else:
             pa_append_kv(self.k_new, self.v_new, self.k_pool, self.v_pool, self.d_slots,
                          stream=stream)
+
+    def step(self, stream=None):
+        """The step's copy-on-write copies (if any), then the append and the
+        attention: one pa_decode_append_attention kernel for an fp16 cache,
+        pa_append_kv_fp8 and pa_decode_attention_fp8 for an E4M3 one."""
+        if self.kv_dtype == "fp8":
+            self.copy_and_append(stream)
+            return self.attend(stream)
+        if self.d_pairs is not None:
+            pa_copy_blocks(self.k_pool, self.v_pool, self.d_pairs, stream=stream)
+        pa_decode_append_attention(self.q, self.k_new, self.v_new, self.d_slots, self.k_pool,
+                                   self.v_pool, self.d_table, self.d_lens,
+                                   float(self.batch.scale), out=self.out,
+                                   workspace=self.workspace,
+                                   partition_tokens=self.partition_tokens, stream=stream)
+        return self.out
 
     def attend(self, stream=None):
         if self.kv_dtype == "fp8":
@@ -277,11 +294,10 @@ class DecodeBatchRunner:
         return int(self.host_arena.numel())
 
     def run_step(self, stream=None):
-        """copy-on-write copies (if any), append, attend. Returns how many
-        kernels the library launched for it."""
+        """copy-on-write copies (if any), append, attend (see step()).
+        Returns how many kernels the library launched for it."""
         n0 = pa_kernel_launches()
-        self.copy_and_append(stream)
-        self.attend(stream)
+        self.step(stream)
         return pa_kernel_launches() - n0
 
     def kv_bytes(self) -> int:
@@ -358,6 +374,12 @@ class SharedPrefixRunner(DecodeBatchRunner):
         self.d_prefix = _to_dev(plan.block_table[0, :self.num_prefix_blocks].astype(np.int32),
                                 self.device)
         return plan
+
+    def step(self, stream=None):
+        """The copies, the append, then the prefix-aware attention (or the
+        generic one)."""
+        self.copy_and_append(stream)
+        return self.attend(stream)
 
     def attend(self, stream=None):
         if not self.prefix_aware:

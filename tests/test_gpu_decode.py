@@ -247,3 +247,89 @@ def test_lengths_written_by_the_kernel_just_before(pa):
         exp = oracle.decode_attention(q, kp, vp, table, lens_now, np.float32(0.088))
         assert_close_attention(out.cpu().numpy(), exp, f"lengths bumped, step {k}")
     assert pa.pa_device_error() == 0
+
+
+# ------------------------------------------- append + attention, one kernel --
+def _append_case(seed, D=128, BS=16, G=4, hkv=2, S=9):
+    rng = np.random.default_rng(seed)
+    lens0 = rng.integers(1, 90, size=S, endpoint=True)
+    nb = sum(-(-(int(L) + 1) // BS) for L in lens0) + 12
+    b = synthetic.make_batch(f"append-attend-{seed}", rng, lens0, G * hkv, hkv, D, BS, nb,
+                             seed=seed)
+    ref = oracle.decode_step(b, compute_attention=False)
+    return b, ref
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+@pytest.mark.parametrize("D,BS,G,hkv", [(128, 16, 4, 2), (64, 8, 1, 3), (128, 32, 8, 1),
+                                        (128, 16, 2, 16)])
+def test_append_attention_equals_append_then_attention(pa, D, BS, G, hkv):
+    """pa_decode_append_attention gives the pools pa_append_kv gives
+    (bit-exact) and the output of pa_decode_attention after it (bit-equal:
+    the same kernel reads the same rows), with every row past a length
+    poisoned; 16 KV heads make two head groups, each writing its part."""
+    b, ref = _append_case(40 + D + BS + G + hkv, D, BS, G, hkv)
+    kp, vp = poison_unread_rows(b.k_pool, b.v_pool, ref.block_table, ref.seq_lens, BS)
+    # the rows the append writes are poisoned too: only the append fills them
+    for s, slot in enumerate(ref.slot_mapping.tolist()):
+        kp[slot // BS, slot % BS] = np.float16(np.nan)
+        vp[slot // BS, slot % BS] = np.float16(np.nan)
+    args = (_dev(b.q), _dev(b.k_new), _dev(b.v_new), _dev(ref.slot_mapping))
+    tab, lens = _dev(ref.block_table), _dev(ref.seq_lens)
+    k1, v1 = _dev(kp), _dev(vp)
+    out1 = pa.pa_decode_append_attention(*args, k1, v1, tab, lens, float(b.scale))
+    k2, v2 = _dev(kp), _dev(vp)
+    pa.pa_append_kv(args[1], args[2], k2, v2, args[3])
+    out2 = pa.pa_decode_attention(args[0], k2, v2, tab, lens, float(b.scale))
+    torch.cuda.synchronize()
+    assert pa.pa_device_error() == 0
+    assert torch.equal(k1.view(torch.int16), k2.view(torch.int16))
+    assert torch.equal(v1.view(torch.int16), v2.view(torch.int16))
+    ek, ev = oracle.append_kv(kp, vp, b.k_new, b.v_new, ref.slot_mapping)
+    assert np.array_equal(k1.cpu().numpy().view(np.uint16), ek.view(np.uint16))
+    assert np.array_equal(v1.cpu().numpy().view(np.uint16), ev.view(np.uint16))
+    assert torch.equal(out1, out2)
+    exp = oracle.decode_attention(b.q, ek, ev, ref.block_table, ref.seq_lens, b.scale)
+    assert_close_attention(out1.cpu().numpy(), exp, f"append+attention D{D} BS{BS} G{G}")
+
+
+def test_append_attention_slot_checks(pa):
+    """A negative slot writes nothing (the pool's row is attended); a slot
+    that is not the row of the sequence's last token (another row, or past
+    the pool) is not written and sets PA_DEVERR_BAD_SLOT."""
+    b, ref = _append_case(77)
+    BS = b.block_size
+    slots = ref.slot_mapping.copy()
+    kp, vp = b.k_pool.copy(), b.v_pool.copy()
+    base_k, base_v = _dev(kp), _dev(vp)
+    # sequence 0: negative slot; its last row keeps the pool's value
+    slots[0] = -1
+    tab, lens = _dev(ref.block_table), _dev(ref.seq_lens)
+    out = pa.pa_decode_append_attention(_dev(b.q), _dev(b.k_new), _dev(b.v_new), _dev(slots),
+                                        base_k, base_v, tab, lens, float(b.scale))
+    torch.cuda.synchronize()
+    assert pa.pa_device_error() == 0
+    ek, ev = oracle.append_kv(kp, vp, b.k_new, b.v_new, slots)
+    assert np.array_equal(base_k.cpu().numpy().view(np.uint16), ek.view(np.uint16))
+    exp = oracle.decode_attention(b.q, ek, ev, ref.block_table, ref.seq_lens, b.scale)
+    assert_close_attention(out.cpu().numpy(), exp, "negative slot")
+    # sequence 1: the slot of another row of its last block; sequence 2: past the pool
+    for bad in (ref.slot_mapping[1] ^ 1 if BS > 1 else ref.slot_mapping[1] + BS,
+                b.num_blocks * BS + 3):
+        slots2 = ref.slot_mapping.copy()
+        who = 1 if bad < b.num_blocks * BS else 2
+        slots2[who] = bad
+        k3, v3 = _dev(kp), _dev(vp)
+        pa.pa_decode_append_attention(_dev(b.q), _dev(b.k_new), _dev(b.v_new), _dev(slots2),
+                                      k3, v3, tab, lens, float(b.scale))
+        with pytest.raises(pa.PaError) as e:
+            pa.pa_device_error()
+        assert e.value.flags & pa.PA_DEVERR_BAD_SLOT
+        # that sequence's row was not written anywhere; the others were
+        good = ref.slot_mapping.copy()
+        good[who] = -1
+        ek3, _ = oracle.append_kv(kp, vp, b.k_new, b.v_new, good)
+        assert np.array_equal(k3.cpu().numpy().view(np.uint16), ek3.view(np.uint16))
