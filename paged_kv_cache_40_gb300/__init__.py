@@ -10,6 +10,7 @@ Device calls                            Host block manager
   pa_copy_blocks, pa_copy_blocks_fp8      a host pool for swapping
   pa_swap_blocks
   pa_decode_attention (+ _fp8, _shared_prefix, _fixed_scratch)
+  pa_decode_append_attention: the append and the attention in one kernel
   pa_decode_workspace_bytes / _init
   pa_device_error
 
@@ -45,7 +46,8 @@ __all__ = [
     "pa_decode_attention_shared_prefix", "pa_decode_shared_prefix_workspace_bytes",
     "pa_swap_blocks",
     "pa_decode_attention_fixed_scratch", "kv_block_pool", "kv_views",
-    "pa_version", "pa_kernel_launches", "pa_set_wait_limit_ns", "BlockAllocator", "PaError", "OutOfBlocksError", "lib",
+    "pa_version", "pa_kernel_launches", "pa_set_wait_limit_ns", "BlockAllocator", "PaError",
+    "OutOfBlocksError", "lib",
 ]
 
 
