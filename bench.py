@@ -470,8 +470,12 @@ def time_planned(args, b, fp8, dev, stream, flush, world, steps):
         plan = run.run_native_step()
         return int(plan.seq_lens.astype(np.int64).sum())
 
+    # a set of plan buffers is rewritten two steps after the step that read
+    # it: that step must have completed (the flush makes the device the slow
+    # side, so without the wait the host would plan over a set still queued)
     for _ in range(args.warmup):
         flush()
+        torch.cuda.synchronize(dev)
         one()
     torch.cuda.synchronize(dev)
     barrier(world)
