@@ -228,7 +228,9 @@ class DecodeBatchRunner:
         (pa_alloc_plan_step) and the kernels read in place through their
         device mapping; q and the new K/V rows stay in pinned host memory
         too. With two sets, step k+1 can be planned while the kernels of step
-        k still read theirs. Returns the input bytes of one step."""
+        k still read theirs; a set is written again only once the kernels that
+        read it last have completed (see _take_plan_set). Returns the input
+        bytes of one step."""
         import torch
         S, mb = self.num_seqs, self.max_blocks
         pin = lambda shape: torch.empty(shape, dtype=torch.int32).pin_memory()
@@ -236,6 +238,9 @@ class DecodeBatchRunner:
         self._plan_views = [tuple(t.numpy() for t in st) for st in self._plan_sets]
         self._plan_ids = np.arange(S, dtype=np.int64)
         self._plan_next = 0
+        self._plan_marks = [torch.cuda.Event() for _ in range(sets)]
+        self._plan_marked = [False] * sets
+        self._plan_stream = None
         total = 0
         for n in ("q", "k_new", "v_new"):
             h = getattr(self, n).cpu().pin_memory()
@@ -256,12 +261,34 @@ class DecodeBatchRunner:
                                            k_scale=self.k_scale if fp8 else None,
                                            v_scale=self.v_scale if fp8 else None)
                         for st in self._plan_sets]
+        import torch
+        # the stream the prepared steps launch on (resolved as they resolved it)
+        self._plan_stream = stream if stream is not None else torch.cuda.current_stream()
+
+    def _take_plan_set(self) -> int:
+        """Index of the next set of plan buffers, once the kernels that read it
+        last have completed: each call first marks, with an event on the
+        stream, the work enqueued so far (which includes the kernels that read
+        the set planned last), then waits for the mark left on the set it is
+        about to write. Host memory the kernels read in place is never
+        rewritten under them, however far the host runs ahead."""
+        import torch
+        n = len(self._plan_sets)
+        k = self._plan_next % n
+        stream = self._plan_stream or torch.cuda.current_stream()
+        if self._plan_next > 0:
+            prev = (self._plan_next - 1) % n
+            self._plan_marks[prev].record(stream)
+            self._plan_marked[prev] = True
+        if self._plan_marked[k]:
+            self._plan_marks[k].synchronize()
+        self._plan_next += 1
+        return k
 
     def run_native_step(self) -> StepPlan:
         """One decode step through pa_decode_step (see prepare_native_steps);
         returns the plan it wrote (views of that set's pinned buffers)."""
-        k = self._plan_next % len(self._native)
-        self._plan_next += 1
+        k = self._take_plan_set()
         ncow = self._native[k]()
         v = self._plan_views[k]
         S = self.num_seqs
@@ -272,8 +299,7 @@ class DecodeBatchRunner:
         """One decode step planned by the block manager in a single call into
         the next set of pinned buffers (see host_planned); the step's kernels
         then read that set."""
-        k = self._plan_next % len(self._plan_sets)
-        self._plan_next += 1
+        k = self._take_plan_set()
         slots, pairs, table, lens = self.alloc.plan_step(self._plan_ids, self.max_blocks,
                                                          self.table_fill, out=self._plan_views[k])
         st = self._plan_sets[k]

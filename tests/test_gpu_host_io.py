@@ -386,3 +386,51 @@ def test_one_call_fp8_steps_match_the_oracle(pa):
         exp = oracle.decode_attention_fp8(b.q, kp, vp, c.k_scale, c.v_scale, table, lens, b.scale)
         assert_close_attention(run.out.cpu().numpy(), exp, f"one-call fp8 step {k}")
     assert copies >= 1
+
+
+def test_one_call_steps_queued_behind_slow_work(pa):
+    """Steps enqueued back to back with no wait, each behind slow device work,
+    so the host plans far ahead of the device over two rotating sets of plan
+    buffers that the kernels read in place: no set may be rewritten before the
+    kernels that read it have run (the runner waits for them), so every step
+    appends its own row. The pools after all steps are bit-exact with the
+    oracle's block manager replayed over the same steps, and the last output
+    matches the oracle's attention."""
+    from paged_kv_cache_40_gb300.engine import DecodeBatchRunner
+    rng = np.random.default_rng(25)
+    lens0 = rng.integers(14, 40, size=6, endpoint=True)
+    steps = 16
+    nb = sum(-(-(int(L) + steps + 1) // 16) for L in lens0) + 8
+    b = synthetic.make_batch("queued", rng, lens0, 16, 4, 128, 16, nb, seed=25)
+    mb = max(-(-(int(L) + steps + 1) // 16) for L in lens0) + 1
+    run = DecodeBatchRunner(b, max_blocks=mb)
+    ref = oracle.BlockAllocator(b.num_blocks, b.block_size, b.free_order)
+    for i, L in enumerate(b.prefill_lens):
+        ref.add_seq(i, int(L))
+    run.host_planned(sets=2)
+    run.prepare_native_steps()
+    slow = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    for k in range(steps):
+        slow.fill_(k & 0xFF)            # about 0.1 ms of device work ahead of each step
+        run.run_native_step()
+    torch.cuda.synchronize()
+    assert pa.pa_device_error() == 0
+    kp, vp = b.k_pool.copy(), b.v_pool.copy()
+    ids = list(range(b.num_seqs))
+    for k in range(steps):
+        slots, pairs = [], []
+        for s_ in ids:
+            sl, cs, cd = ref.append_slot(s_)
+            slots.append(sl)
+            if cs >= 0:
+                pairs.append((cs, cd))
+        if pairs:
+            kp, vp = oracle.copy_blocks(kp, vp, np.asarray(pairs, np.int32))
+        kp, vp = oracle.append_kv(kp, vp, b.k_new, b.v_new, np.asarray(slots, np.int32))
+    assert np.array_equal(run.k_pool.cpu().numpy().view(np.uint16), kp.view(np.uint16))
+    assert np.array_equal(run.v_pool.cpu().numpy().view(np.uint16), vp.view(np.uint16))
+    table = np.asarray(ref.dense_table(ids, mb), np.int32)
+    lens = np.asarray([ref.seq_len(s_) for s_ in ids], np.int32)
+    exp = oracle.decode_attention(b.q, kp, vp, table, lens, b.scale)
+    assert_close_attention(run.out.cpu().numpy(), exp, "queued one-call steps")
