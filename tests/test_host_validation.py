@@ -162,3 +162,86 @@ def test_cache_ops_fp8_reject(libpa):
     assert lib.pa_copy_blocks_fp8(NULL, NULL, NULL, 0, 8, 128, 16, 64, 0, NULL) == 0
     assert lib.pa_copy_blocks_fp8(NULL, NULL, NULL, 2, 8, 120, 16, 64, 0, NULL) == 4  # 120 % 16
     assert lib.pa_copy_blocks_fp8(NULL, NULL, NULL, 2, 8, 128, 16, 64, 0, NULL) == 1
+
+
+# pa_decode_append_attention: the attention call's checks, then its own
+# arguments (the new rows and their slots) and the pools' disjointness, all
+# before any device query. Fake aligned addresses stand for the arrays.
+_FAKE = dict(q=0x10000, k=0x20000000, v=0x40000000, table=0x60000, lens=0x70000, out=0x80000)
+
+
+def _append_attn(lib, **kw):
+    a = dict(q=NULL, kn=NULL, vn=NULL, slots=NULL, k=NULL, v=NULL, table=NULL, lens=NULL, S=4,
+             Hq=32, Hkv=8, D=128, BS=16, MB=8, NB=64, stride=0, scale=0.1, out=NULL, ws=NULL,
+             wsb=0, pt=0, stream=NULL)
+    a.update(kw)
+    return lib.pa_decode_append_attention(
+        a["q"], a["kn"], a["vn"], a["slots"], a["k"], a["v"], a["table"], a["lens"], a["S"],
+        a["Hq"], a["Hkv"], a["D"], a["BS"], a["MB"], a["NB"], a["stride"],
+        ctypes.c_float(a["scale"]), a["out"], a["ws"], a["wsb"], a["pt"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status,msg", [
+    (dict(), 1, b"NULL pointer"),                                   # the attention's arrays
+    (dict(_FAKE, D=96), 4, b""),                                    # an unsupported shape
+    (dict(_FAKE, scale=float("nan")), 1, b"scale"),
+    (dict(_FAKE), 1, b"NULL k_new"),                                # the new rows and slots
+    (dict(_FAKE, kn=0x90000, vn=0xA0000), 1, b"NULL k_new"),
+    (dict(_FAKE, kn=0x90008, vn=0xA0000, slots=0xB0000), 1, b"misaligned k_new"),
+    (dict(_FAKE, kn=0x90000, vn=0xA0000, slots=0xB0002), 1, b"misaligned k_new"),
+    # V one block past K: every block of the two pools overlaps the other's
+    (dict(_FAKE, v=0x20000000 + 32 * 1024, kn=0x90000, vn=0xA0000, slots=0xB0000), 1,
+     b"overlap"),
+])
+def test_append_attention_rejects(libpa, kw, status, msg):
+    lib = libpa.lib()
+    assert _append_attn(lib, **kw) == status
+    assert msg in lib.pa_last_error()
+
+
+def test_append_attention_zero_sequences_is_a_no_op(libpa):
+    assert _append_attn(libpa.lib(), S=0) == 0
+
+
+def _step(lib, handle, ids, mb, nb, ncow, **kw):
+    a = dict(slots=NULL, pairs=NULL, table=NULL, lens=NULL, q=NULL, kn=NULL, vn=NULL, k=NULL,
+             v=NULL, Hq=32, Hkv=8, D=128, stride=0, scale=0.1, out=NULL, ws=NULL, wsb=0, pt=0,
+             stream=NULL)
+    a.update(kw)
+    return lib.pa_decode_step(handle, ids.ctypes.data if ids is not None else NULL,
+                              0 if ids is None else len(ids), mb, a["slots"], a["pairs"],
+                              a["table"], a["lens"], ctypes.byref(ncow), a["q"], a["kn"], a["vn"],
+                              a["k"], a["v"], a["Hq"], a["Hkv"], a["D"], nb, a["stride"],
+                              ctypes.c_float(a["scale"]), a["out"], a["ws"], a["wsb"], a["pt"],
+                              a["stream"])
+
+
+def test_decode_step_refuses_before_planning(libpa):
+    """pa_decode_step checks its handle and that the pool is the block
+    manager's before it plans anything, and a plan that cannot be made
+    (a table narrower than a sequence's blocks) changes nothing."""
+    import numpy as np
+    lib = libpa.lib()
+    ncow = ctypes.c_int(7)
+    assert _step(lib, NULL, None, 4, 64, ncow) == 1
+    a = libpa.BlockAllocator(64, 16)
+    a.add_seq(0, 40)                   # three blocks of 16 tokens
+    a.add_seq(1, 16)                   # a full block: the next token opens a second
+    ids = np.array([0, 1], np.int64)
+    before = a.export_state()
+    slots = np.zeros(2, np.int32)
+    pairs = np.zeros((2, 2), np.int32)
+    lens = np.zeros(2, np.int32)
+    table = np.zeros((2, 4), np.int32)
+    bufs = dict(slots=slots.ctypes.data, pairs=pairs.ctypes.data, table=table.ctypes.data,
+                lens=lens.ctypes.data)
+    # the pool is not the block manager's
+    assert _step(lib, a._h, ids, 4, 32, ncow, **bufs) == 1
+    assert b"block manager" in lib.pa_last_error()
+    assert ncow.value == 0
+    # sequence 0 needs three table columns: two are refused, all or nothing
+    narrow = np.zeros((2, 2), np.int32)
+    bufs_n = dict(bufs, table=narrow.ctypes.data)
+    assert _step(lib, a._h, ids, 2, 64, ncow, **bufs_n) == 1
+    assert b"needs more than 2 blocks" in lib.pa_last_error()
+    assert a.export_state() == before
