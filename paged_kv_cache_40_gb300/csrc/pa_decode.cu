@@ -44,7 +44,10 @@
 //     own head), so a stage is released after HG arrivals. For each piece the
 //     producer also publishes, in one of two q slots, the piece's metadata
 //     and its q rows, so the next piece's q is in flight while the current
-//     one streams and the consumers never search the block stream.
+//     one streams and the consumers never search the block stream. For fp16
+//     pools the copies carry an L2 evict-first policy: the stream is read once,
+//     and what is read again (partial records, counters, table, q, the code)
+//     stays in L2 while it passes.
 //     Merge warps take the cut pieces off the consumers' critical path: the
 //     consumer warps write their partial records, send a message (segment and
 //     place) through a small shared-memory ring and go on streaming; the
